@@ -1,0 +1,333 @@
+"""Pins of the CPU oracle against what the tutorial pages and the mathematics fix.
+
+Each test is chosen so that a plausible slip in the oracle (a dropped term, a
+wrong sign or index, a transposed operand, the other RoPE pairing, the other
+SwiGLU branch) fails it.  Values come from tests/golden/page_examples.json
+(cited there) or from closed forms computed here by hand.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_examples.json")))
+
+
+# ---------------------------------------------------------------- Linear / Embedding
+def test_linear_page_example_first_row():
+    g = GOLD["linear_first_row"]
+    W = np.zeros((3, 4))
+    W[0] = g["w_row0"]
+    y = oracle.linear(np.array(g["x"], float), W)
+    assert y[0] == g["y0"] == g["y_printed"][0]
+
+
+def test_linear_orientation_and_brute_force():
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((2, 3, 5))
+    W = rng.standard_normal((7, 5))          # (out, in)
+    y = oracle.linear(x, W)
+    assert y.shape == (2, 3, 7)
+    for b in range(2):
+        for s in range(3):
+            for o in range(7):
+                ref = sum(x[b, s, i] * W[o, i] for i in range(5))
+                assert abs(y[b, s, o] - ref) < 1e-12
+
+
+def test_embedding_lookup_and_range():
+    E = np.arange(12, dtype=float).reshape(4, 3)
+    h = oracle.embedding(E, np.array([[3, 0], [1, 1]]))
+    assert h.shape == (2, 2, 3)
+    assert np.array_equal(h[0, 0], [9, 10, 11]) and np.array_equal(h[1, 1], [3, 4, 5])
+    with pytest.raises(ValueError):
+        oracle.embedding(E, np.array([[4]]))
+    with pytest.raises(ValueError):
+        oracle.embedding(E, np.array([[-1]]))
+
+
+# ---------------------------------------------------------------- RMSNorm / LayerNorm
+def test_rmsnorm_hand_vector_and_scale_invariance():
+    g = GOLD["rmsnorm_scale"]
+    y = oracle.rmsnorm(np.array(g["x"], float), np.ones(2), eps=0.0)
+    assert np.allclose(y, np.array(g["x"]) / g["rms"], atol=1e-15)
+    assert np.allclose(y, [0.6324555320336759, 1.2649110640673518])
+    y10 = oracle.rmsnorm(np.array(g["x_scaled"], float), np.ones(2), eps=0.0)
+    assert np.allclose(y, y10, atol=1e-15)
+    # with eps = 1e-5 the two differ only by the eps term
+    ye = oracle.rmsnorm(np.array(g["x"], float), np.ones(2), eps=1e-5)
+    assert np.allclose(ye, np.array(g["x"]) / math.sqrt(10 + 1e-5))
+
+
+def test_rmsnorm_gain_and_constant_vector():
+    c = -3.0
+    gain = np.array([0.5, 1.0, 2.0, 4.0])
+    y = oracle.rmsnorm(np.full(4, c), gain, eps=1e-5)
+    assert np.allclose(y, math.copysign(1, c) * gain * abs(c) / math.sqrt(c * c + 1e-5))
+    # zero row: eps keeps it finite
+    assert np.all(oracle.rmsnorm(np.zeros(4), gain) == 0)
+
+
+def test_rmsnorm_equals_layernorm_on_zero_mean():
+    x = np.array([1.0, -2.0, 3.0, -2.0])            # mean 0
+    g = np.array([1.0, 2.0, 0.5, 1.5])
+    assert np.allclose(oracle.rmsnorm(x, g, 1e-5), oracle.layernorm(x, g, np.zeros(4), 1e-5))
+    # LayerNorm hand vector: [1,2,3] -> mean 2, var 2/3 -> [-sqrt(1.5), 0, sqrt(1.5)]
+    ln = oracle.layernorm(np.array([1.0, 2.0, 3.0]), np.ones(3), np.zeros(3), 0.0)
+    assert np.allclose(ln, [-math.sqrt(1.5), 0.0, math.sqrt(1.5)])
+    # and RMSNorm of the same non-zero-mean vector differs (no mean subtraction)
+    assert not np.allclose(oracle.rmsnorm(np.array([1.0, 2.0, 3.0]), np.ones(3), 0.0), ln)
+
+
+# ---------------------------------------------------------------- RoPE
+def test_rope_frequency_table_page_example():
+    g = GOLD["rope_frequencies"]
+    assert np.allclose(oracle.rope_frequencies(g["d_head"], g["theta"]), g["omega"])
+    # CS336 form 1/theta^((2k-2)/d), k = 1..d/2
+    d, th = 16, 10000.0
+    k = np.arange(1, d // 2 + 1)
+    assert np.allclose(oracle.rope_frequencies(d, th), 1.0 / th ** ((2 * k - 2) / d))
+
+
+def test_rope_hand_values_pairing_and_direction():
+    # x = e0, d = 4, theta = 100, position 1: the pair (x0, x1) turns by 1 rad
+    # counter-clockwise; (x2, x3) stays zero.  The half-split pairing would move
+    # the value into x2 instead, and a clockwise turn would flip the sign of x1.
+    x = np.array([[1.0, 0.0, 0.0, 0.0]])
+    y = oracle.rope(x, np.array([1.0]), 100.0)
+    assert np.allclose(y, [[math.cos(1), math.sin(1), 0, 0]])
+    x = np.array([[0.0, 0.0, 0.0, 1.0]])
+    y = oracle.rope(x, np.array([3.0]), 100.0)       # second pair, 0.1 rad/pos
+    assert np.allclose(y, [[0, 0, -math.sin(0.3), math.cos(0.3)]])
+
+
+def test_rope_identity_at_zero_and_norm_preserved():
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((3, 7, 32))
+    pos = np.arange(7, dtype=float)
+    y = oracle.rope(x, pos, 10000.0)
+    assert np.allclose(y[:, 0], x[:, 0])
+    assert np.allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1))
+    # every pair keeps its own length
+    assert np.allclose(np.hypot(y[..., 0::2], y[..., 1::2]), np.hypot(x[..., 0::2], x[..., 1::2]))
+
+
+def test_rope_relative_position_page_example_and_all_offsets():
+    g = GOLD["rope_relative"]
+    rng = np.random.default_rng(2)
+    d, th = g["d_head"], g["theta"]
+    q0, k0 = rng.standard_normal(d), rng.standard_normal(d)
+    S = 64
+    pos = np.arange(S, dtype=float)
+    qr = oracle.rope(np.tile(q0, (S, 1)), pos, th)
+    kr = oracle.rope(np.tile(k0, (S, 1)), pos, th)
+    (a, b), (c, e) = g["pairs"]
+    assert abs(qr[a] @ kr[b] - qr[c] @ kr[e]) < 1e-12
+    dots = qr @ kr.T                                 # [m, n]
+    for delta in range(-S + 1, S):
+        diag = np.diagonal(dots, offset=delta)
+        assert np.ptp(diag) < 1e-10
+
+
+def test_rope_two_dim_closed_form():
+    # (R(m) q)^T (R(n) k) = (ac + bd) cos D + (bc - ad) sin D, D = (n - m) omega
+    a, b, c, d = 0.3, -1.2, 0.7, 2.1
+    theta, m, n = 10000.0, 3.0, 11.0
+    qm = oracle.rope(np.array([[a, b]]), np.array([m]), theta)[0]
+    kn = oracle.rope(np.array([[c, d]]), np.array([n]), theta)[0]
+    D = (n - m) * 1.0                                # omega_0 = 1 for d = 2
+    assert abs(qm @ kn - ((a * c + b * d) * math.cos(D) + (b * c - a * d) * math.sin(D))) < 1e-12
+
+
+# ---------------------------------------------------------------- softmax / attention
+def test_softmax_rows_sum_and_shift_invariance():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((5, 9)) * 30
+    p = oracle.softmax(x)
+    assert np.allclose(p.sum(-1), 1.0)
+    assert np.allclose(oracle.softmax(x + 123.0), p)
+    assert np.all(np.isfinite(oracle.softmax(np.array([1000.0, 0.0]))))
+
+
+def test_masked_scores_page_example():
+    rows = GOLD["masked_scores"]["scores"]
+    S = np.array([[(-np.inf if v is None else v) for v in r] for r in rows], float)
+    P = oracle.softmax(S)
+    e5 = math.exp(-5)
+    z3 = math.exp(-8) + math.exp(-2) + 1.0
+    want = [[1, 0, 0],
+            [e5 / (1 + e5), 1 / (1 + e5), 0],
+            [math.exp(-8) / z3, math.exp(-2) / z3, 1 / z3]]
+    assert np.allclose(P, want, atol=1e-15)
+    assert abs(P[1, 0] - 0.0066928509242848554) < 1e-15
+
+
+def test_attention_uniform_scores_give_prefix_mean():
+    rng = np.random.default_rng(4)
+    B, H, S, dh = 2, 3, 9, 8
+    q = np.zeros((B, H, S, dh))
+    k = rng.standard_normal((B, H, S, dh))
+    v = rng.standard_normal((B, H, S, dh))
+    o = oracle.causal_attention(q, k, v)
+    prefix_mean = np.cumsum(v, axis=2) / np.arange(1, S + 1)[None, None, :, None]
+    assert np.allclose(o, prefix_mean)
+
+
+def test_attention_matches_brute_force_loops_with_gqa():
+    rng = np.random.default_rng(5)
+    B, H, Hkv, S, dh = 2, 4, 2, 6, 4
+    q = rng.standard_normal((B, H, S, dh))
+    k = rng.standard_normal((B, Hkv, S, dh))
+    v = rng.standard_normal((B, Hkv, S, dh))
+    assert np.allclose(oracle.causal_attention(q, k, v), oracle.naive_causal_attention(q, k, v))
+    # first query sees only key 0: its output is v[0] of its kv head
+    o = oracle.causal_attention(q, k, v)
+    assert np.allclose(o[:, 0, 0], v[:, 0, 0]) and np.allclose(o[:, 3, 0], v[:, 1, 0])
+
+
+def test_gqa_equals_mha_with_replicated_kv():
+    rng = np.random.default_rng(6)
+    B, H, Hkv, S, dh = 1, 6, 2, 7, 4
+    q = rng.standard_normal((B, H, S, dh))
+    k = rng.standard_normal((B, Hkv, S, dh))
+    v = rng.standard_normal((B, Hkv, S, dh))
+    rep = H // Hkv
+    k_full = np.repeat(k, rep, axis=1)               # contiguous groups: head h -> h // rep
+    v_full = np.repeat(v, rep, axis=1)
+    assert np.allclose(oracle.causal_attention(q, k, v), oracle.causal_attention(q, k_full, v_full))
+
+
+def test_attention_is_causal():
+    rng = np.random.default_rng(7)
+    B, H, S, dh, t = 1, 2, 10, 4, 5
+    q, k, v = (rng.standard_normal((B, H, S, dh)) for _ in range(3))
+    o = oracle.causal_attention(q, k, v)
+    k2, v2 = k.copy(), v.copy()
+    k2[:, :, t + 1:] += 5.0
+    v2[:, :, t + 1:] -= 3.0
+    o2 = oracle.causal_attention(q, k2, v2)
+    assert np.array_equal(o[:, :, : t + 1], o2[:, :, : t + 1])
+    assert not np.allclose(o[:, :, t + 1:], o2[:, :, t + 1:])
+
+
+def test_attention_scale_is_inverse_sqrt_dhead():
+    # two keys, query aligned with key 1: weight ratio exp((q.k1 - q.k0)/sqrt(dh))
+    dh = 16
+    q = np.zeros((1, 1, 2, dh)); q[0, 0, 1, 0] = 2.0
+    k = np.zeros((1, 1, 2, dh)); k[0, 0, 1, 0] = 1.0
+    v = np.zeros((1, 1, 2, dh)); v[0, 0, 1, 1] = 1.0
+    o = oracle.causal_attention(q, k, v)
+    w1 = 1.0 / (1.0 + math.exp(-2.0 / math.sqrt(dh)))
+    assert abs(o[0, 0, 1, 1] - w1) < 1e-15
+
+
+# ---------------------------------------------------------------- SwiGLU
+def test_silu_values():
+    assert oracle.silu(0.0) == 0.0
+    assert abs(oracle.silu(1.0) - 1.0 / (1.0 + math.exp(-1.0))) < 1e-15
+    assert abs(oracle.silu(2.0) - 1.7615941559557650) < 1e-15
+    assert abs(oracle.silu(40.0) - 40.0) < 1e-12 and abs(oracle.silu(-40.0)) < 1e-15
+
+
+def test_swiglu_gating_page_example():
+    g = GOLD["swiglu_gating"]
+    # pick W1 so that silu(W1 x) equals the page's gate, W3 x its value branch, W2 = I
+    gate = np.array(g["gate"], float)
+    val = np.array(g["value"], float)
+    # invert silu numerically for the gate values (silu is monotone for z > -1.2785)
+    def silu_inv(y):
+        lo, hi = -1.27846454, 50.0
+        for _ in range(200):
+            mid = 0.5 * (lo + hi)
+            lo, hi = (mid, hi) if oracle.silu(mid) < y else (lo, mid)
+        return 0.5 * (lo + hi)
+    z = np.array([silu_inv(y) for y in gate])
+    x = np.ones(1)
+    y = oracle.swiglu(x, z[:, None], val[:, None], np.eye(4))
+    assert np.allclose(y, g["product"], atol=1e-12)
+
+
+def test_swiglu_branch_order():
+    # x = [1], W1 = [[2]], W3 = [[-3]], W2 = [[1]]: silu(2) * (-3); swapping the
+    # branches would give silu(-3) * 2 instead.
+    y = oracle.swiglu(np.ones(1), np.array([[2.0]]), np.array([[-3.0]]), np.array([[1.0]]))
+    assert abs(y[0] - (-3.0 * 1.7615941559557650)) < 1e-12
+
+
+# ---------------------------------------------------------------- whole model
+def _tiny(n_layer=2, **kw):
+    cfg = workloads.get_config("tiny").replace(n_layer=n_layer, **kw)
+    return cfg, workloads.make_weights(cfg), workloads.make_tokens(cfg, batch=2, seq=12)
+
+
+def test_zero_layers_is_lmhead_of_normed_embedding():
+    cfg, w, tok = _tiny(n_layer=0)
+    logits = oracle.forward(tok, w, cfg)
+    x = w["embed"].astype(float)[tok]
+    ms = (x ** 2).sum(-1, keepdims=True) / cfg.d_model
+    want = np.einsum("bsd,vd->bsv", x / np.sqrt(ms + cfg.norm_eps) * w["final_norm"], w["lm_head"].astype(float))
+    assert logits.shape == (2, 12, cfg.vocab)
+    assert np.allclose(logits, want, atol=1e-13)
+
+
+def test_block_is_identity_when_writers_are_zero():
+    cfg, w, tok = _tiny(n_layer=1)
+    for key in ("wo", "w2"):
+        w["layers"][0][key] = np.zeros_like(w["layers"][0][key])
+    w0 = {**w, "layers": []}
+    assert np.allclose(oracle.forward(tok, w, cfg), oracle.forward(tok, w0, cfg.replace(n_layer=0)), atol=1e-13)
+
+
+def test_model_is_causal_end_to_end():
+    cfg, w, tok = _tiny()
+    t = 6
+    tok2 = tok.copy()
+    tok2[:, t + 1:] = (tok2[:, t + 1:] + 5) % cfg.vocab
+    a, b = oracle.forward(tok, w, cfg), oracle.forward(tok2, w, cfg)
+    assert np.abs(a[:, : t + 1] - b[:, : t + 1]).max() < 1e-12
+    assert np.abs(a[:, t + 1:] - b[:, t + 1:]).max() > 1e-6
+
+
+def test_sequences_are_independent():
+    cfg, w, tok = _tiny()
+    full = oracle.forward(tok, w, cfg)
+    alone = oracle.forward(tok[1:2], w, cfg)
+    assert np.array_equal(full[1], alone[0])
+    assert np.array_equal(oracle.forward(tok, w, cfg, rows=[1])[0], full[1])
+
+
+def test_gqa_model_equals_mha_model_with_replicated_kv_weights():
+    cfg = workloads.get_config("tiny").replace(n_head=4, n_kv_head=2, n_layer=1)
+    w = workloads.make_weights(cfg)
+    tok = workloads.make_tokens(cfg, batch=1, seq=9)
+    mha_cfg = cfg.replace(n_kv_head=4)
+    w_mha = {**w, "layers": [dict(w["layers"][0])]}
+    dh = cfg.d_head
+    for key in ("wk", "wv"):
+        heads = w["layers"][0][key].reshape(2, dh, cfg.d_model)
+        w_mha["layers"][0][key] = np.repeat(heads, 2, axis=0).reshape(4 * dh, cfg.d_model)
+    assert np.allclose(oracle.forward(tok, w, cfg), oracle.forward(tok, w_mha, mha_cfg), atol=1e-13)
+
+
+def test_param_count_formula():
+    g = GOLD["param_counts"]
+    c = g["cs336b"]
+    assert oracle.param_count(c["vocab"], c["d_model"], c["n_layer"], c["d_ff"]) == c["count"]
+    x = g["gpt2xl"]
+    n = oracle.param_count(x["vocab"], x["d_model"], x["n_layer"], 4288, x["n_head"], x["n_head"])
+    assert abs(n - x["approx_count"]) / x["approx_count"] < 0.005
+    assert abs(n * 4 / 1e9 - x["approx_fp32_gb"]) < 0.01
+    # and it counts exactly the generated weight arrays, GQA included
+    for name in ("tiny",):
+        cfg = workloads.get_config(name)
+        for kv in (cfg.n_head, cfg.n_head // 2):
+            c2 = cfg.replace(n_kv_head=kv)
+            w = workloads.make_weights(c2)
+            total = w["embed"].size + w["final_norm"].size + w["lm_head"].size
+            total += sum(a.size for layer in w["layers"] for a in layer.values())
+            assert total == oracle.param_count(c2.vocab, c2.d_model, c2.n_layer, c2.d_ff, c2.n_head, kv)
