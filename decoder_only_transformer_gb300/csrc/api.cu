@@ -1,0 +1,673 @@
+// api.cu - host side of the libtfm C ABI (include/tfm.h): argument checks,
+// the model handle (workspace, packed weights, RoPE table), the forward
+// launch sequence and the single-operation entry points.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+// Sticky device error word (one per device; see tfm_device_status).
+__device__ int g_tfm_err_word;
+
+namespace tfm {
+
+namespace {
+
+thread_local std::string t_last_error;
+
+tfm_status fail(tfm_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return s;
+}
+
+tfm_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(TFM_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+int* g_err_addr[kMaxDevices];
+int g_sms[kMaxDevices];
+
+int current_device() {
+    int d = 0;
+    cudaGetDevice(&d);
+    return (d >= 0 && d < kMaxDevices) ? d : 0;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+int* device_error_word() {
+    const int d = current_device();
+    std::lock_guard<std::mutex> lk(g_dev_mutex);
+    if (!g_err_addr[d]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_tfm_err_word) != cudaSuccess) return nullptr;
+        g_err_addr[d] = static_cast<int*>(p);
+    }
+    return g_err_addr[d];
+}
+
+int sm_count() {
+    const int d = current_device();
+    std::lock_guard<std::mutex> lk(g_dev_mutex);
+    if (!g_sms[d]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || n <= 0)
+            n = 148;
+        g_sms[d] = n;
+    }
+    return g_sms[d];
+}
+
+const char* cuda_error_text(cudaError_t e) { return cudaGetErrorString(e); }
+
+// ------------------------------------------------------------------ config
+namespace {
+
+tfm_status check_config(const tfm_config* c) {
+    if (!c) return fail(TFM_EINVAL, "config is NULL");
+    if (c->vocab < 1 || c->d_model < 1 || c->n_head < 1 || c->n_kv_head < 1 || c->n_layer < 0 ||
+        c->d_ff < 1 || c->max_seq < 1 || c->max_batch < 1)
+        return fail(TFM_EINVAL, "sizes must be positive (n_layer >= 0)");
+    if (c->mode != TFM_FP32 && c->mode != TFM_BF16) return fail(TFM_EINVAL, "unknown mode %d", c->mode);
+    if (c->d_model % c->n_head) return fail(TFM_EINVAL, "d_model %% n_head != 0");
+    if (c->n_head % c->n_kv_head) return fail(TFM_EINVAL, "n_head %% n_kv_head != 0");
+    const int dh = c->d_model / c->n_head;
+    if (dh % 2) return fail(TFM_EINVAL, "d_head must be even for RoPE");
+    if (!(c->norm_eps > 0.f) || !std::isfinite(c->norm_eps)) return fail(TFM_EINVAL, "norm_eps must be > 0");
+    if (!(c->rope_theta > 1.f) || !std::isfinite(c->rope_theta)) return fail(TFM_EINVAL, "rope_theta must be > 1");
+    if ((int64_t)c->max_seq * c->max_batch > (int64_t)1 << 30) return fail(TFM_EINVAL, "max_batch*max_seq too large");
+    if (c->mode == TFM_BF16) {
+        if (dh != 32 && dh != 64 && dh != 128)
+            return fail(TFM_EUNSUPPORTED, "bf16 mode supports d_head 32, 64, 128 (got %d)", dh);
+        if (c->d_model % 64) return fail(TFM_EUNSUPPORTED, "bf16 mode needs d_model %% 64 == 0");
+        if (c->d_ff % 8) return fail(TFM_EUNSUPPORTED, "bf16 mode needs d_ff %% 8 == 0");
+    } else {
+        if (dh % 8 || dh > 128) return fail(TFM_EUNSUPPORTED, "fp32 mode needs d_head %% 8 == 0, <= 128");
+        if (c->d_model % 8) return fail(TFM_EUNSUPPORTED, "fp32 mode needs d_model %% 8 == 0");
+        if (c->d_ff % 4) return fail(TFM_EUNSUPPORTED, "fp32 mode needs d_ff %% 4 == 0");
+    }
+    return TFM_OK;
+}
+
+inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+struct Sizes {
+    int64_t M, D, Dq, Dkv, Nqkv, F, V, ldV, es;   // es = element size of matrices/activations
+};
+
+Sizes sizes_of(const tfm_config* c) {
+    Sizes s;
+    s.M = (int64_t)c->max_batch * c->max_seq;
+    s.D = c->d_model;
+    const int64_t dh = c->d_model / c->n_head;
+    s.Dq = c->n_head * dh;
+    s.Dkv = c->n_kv_head * dh;
+    s.Nqkv = s.Dq + 2 * s.Dkv;
+    s.F = c->d_ff;
+    s.V = c->vocab;
+    s.ldV = round_up(s.V, 4);
+    s.es = c->mode == TFM_BF16 ? 2 : 4;
+    return s;
+}
+
+// Workspace carve-up, every piece 256-byte aligned.
+struct Layout {
+    size_t h, xn, q, k, v, o, a, rcos, rsin, tok, logits, total;
+};
+
+Layout layout_of(const tfm_config* c) {
+    const Sizes s = sizes_of(c);
+    Layout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += (bytes + 255) / 256 * 256;
+        return at;
+    };
+    const int64_t dh = c->d_model / c->n_head;
+    L.h = take(s.M * s.D * 4);
+    L.xn = take(s.M * s.D * s.es);
+    L.q = take(s.M * s.Dq * s.es);
+    L.k = take(s.M * s.Dkv * s.es);
+    L.v = take(s.M * s.Dkv * s.es);
+    L.o = take(s.M * s.Dq * s.es);
+    L.a = take(s.M * s.F * s.es);
+    L.rcos = take((size_t)c->max_seq * (dh / 2) * 4);
+    L.rsin = take((size_t)c->max_seq * (dh / 2) * 4);
+    L.tok = take(s.M * 4);
+    L.logits = take(s.M * s.ldV * 4);
+    L.total = off;
+    return L;
+}
+
+size_t weight_bytes_of(const tfm_config* c) {
+    const Sizes s = sizes_of(c);
+    // matrices and gains of one layer (9 pieces), plus embed, final_norm and
+    // lm_head; each piece is rounded up to 256 bytes by the loader.
+    const size_t per_layer =
+        (size_t)(s.Nqkv * s.D + s.D * s.Dq + 2 * s.F * s.D + s.D * s.F) * s.es + 2 * s.D * 4;
+    return (size_t)c->n_layer * (per_layer + 9 * 256) + 2 * (size_t)s.V * s.D * s.es + s.D * 4 +
+           3 * 256;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ handle
+struct Model {
+    tfm_config cfg;
+    Sizes sz;
+    Layout lay;
+    int device = 0;
+    uint8_t* ws = nullptr;         // workspace
+    uint8_t* wmem = nullptr;       // packed weights
+    size_t wbytes = 0;
+    bool loaded = false;
+    // packed weights (device pointers into wmem)
+    void* embed = nullptr;
+    void* lm_head = nullptr;
+    float* final_norm = nullptr;
+    std::vector<float*> attn_norm, ffn_norm;
+    std::vector<void*> wqkv, wo, w1, w3, w2;
+    // cached tensor-core plans for the current token count
+    int64_t plan_m = -1;
+    std::vector<GemmPlan> p_qkv, p_o, p_gu, p_down;
+    GemmPlan p_lm;
+    const float* plan_logits = nullptr;
+    int64_t plan_ld = -1;
+    int plan_S = -1;
+
+    float* h() { return reinterpret_cast<float*>(ws + lay.h); }
+    void* xn() { return ws + lay.xn; }
+    void* q() { return ws + lay.q; }
+    void* k() { return ws + lay.k; }
+    void* v() { return ws + lay.v; }
+    void* o() { return ws + lay.o; }
+    void* a() { return ws + lay.a; }
+    float* rcos() { return reinterpret_cast<float*>(ws + lay.rcos); }
+    float* rsin() { return reinterpret_cast<float*>(ws + lay.rsin); }
+    int32_t* tok() { return reinterpret_cast<int32_t*>(ws + lay.tok); }
+    float* logits() { return reinterpret_cast<float*>(ws + lay.logits); }
+};
+
+}  // namespace tfm
+
+using tfm::Model;
+using tfm::fail;
+
+extern "C" {
+
+int32_t tfm_abi_version(void) { return 1; }
+
+const char* tfm_last_error(void) { return tfm::t_last_error.c_str(); }
+
+tfm_status tfm_validate_config(const tfm_config* cfg) { return tfm::check_config(cfg); }
+
+size_t tfm_workspace_bytes(const tfm_config* cfg) {
+    if (tfm::check_config(cfg) != TFM_OK) return 0;
+    return tfm::layout_of(cfg).total;
+}
+
+size_t tfm_weight_bytes(const tfm_config* cfg) {
+    if (tfm::check_config(cfg) != TFM_OK) return 0;
+    return tfm::weight_bytes_of(cfg);
+}
+
+tfm_status tfm_create(const tfm_config* cfg, void** handle) {
+    if (!handle) return fail(TFM_EINVAL, "handle pointer is NULL");
+    tfm_status st = tfm::check_config(cfg);
+    if (st != TFM_OK) return st;
+    Model* m = new Model();
+    m->cfg = *cfg;
+    m->sz = tfm::sizes_of(cfg);
+    m->lay = tfm::layout_of(cfg);
+    cudaGetDevice(&m->device);
+    cudaError_t e = cudaMalloc(&m->ws, m->lay.total);
+    if (e != cudaSuccess) {
+        const size_t bytes = m->lay.total;
+        delete m;
+        cudaGetLastError();
+        return fail(TFM_ENOMEM, "workspace of %zu bytes: %s", bytes, cudaGetErrorString(e));
+    }
+    m->wbytes = tfm::weight_bytes_of(cfg);
+    e = cudaMalloc(&m->wmem, m->wbytes);
+    if (e != cudaSuccess) {
+        cudaFree(m->ws);
+        delete m;
+        cudaGetLastError();
+        return fail(TFM_ENOMEM, "weights: %s", cudaGetErrorString(e));
+    }
+    // RoPE table: angle = s * theta^(-2i/dh) in float64, stored as fp32 cos/sin.
+    const int dh = cfg->d_model / cfg->n_head, half = dh / 2;
+    std::vector<float> hc((size_t)cfg->max_seq * half), hs(hc.size());
+    for (int s = 0; s < cfg->max_seq; ++s)
+        for (int i = 0; i < half; ++i) {
+            const double ang = (double)s * std::pow((double)cfg->rope_theta, -2.0 * i / dh);
+            hc[(size_t)s * half + i] = (float)std::cos(ang);
+            hs[(size_t)s * half + i] = (float)std::sin(ang);
+        }
+    e = cudaMemcpy(m->rcos(), hc.data(), hc.size() * 4, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(m->rsin(), hs.data(), hs.size() * 4, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !tfm::device_error_word()) e = cudaErrorSymbolNotFound;
+    if (e != cudaSuccess) {
+        cudaFree(m->ws);
+        cudaFree(m->wmem);
+        delete m;
+        return tfm::cuda_fail(e, "tfm_create");
+    }
+    *handle = m;
+    return TFM_OK;
+}
+
+void tfm_destroy(void* handle) {
+    Model* m = static_cast<Model*>(handle);
+    if (!m) return;
+    cudaFree(m->ws);
+    cudaFree(m->wmem);
+    delete m;
+}
+
+tfm_status tfm_load_weights(void* handle, const tfm_weights* w, int32_t weights_on_host) {
+    Model* m = static_cast<Model*>(handle);
+    if (!m || !w) return fail(TFM_EINVAL, "NULL handle or weights");
+    const tfm_config& c = m->cfg;
+    const auto& s = m->sz;
+    if (!w->embed || !w->final_norm || !w->lm_head) return fail(TFM_EINVAL, "NULL embed/final_norm/lm_head");
+    if (c.n_layer > 0 && (!w->attn_norm || !w->wq || !w->wk || !w->wv || !w->wo || !w->ffn_norm ||
+                          !w->w1 || !w->w3 || !w->w2))
+        return fail(TFM_EINVAL, "NULL per-layer weight array");
+    for (int l = 0; l < c.n_layer; ++l)
+        if (!w->attn_norm[l] || !w->wq[l] || !w->wk[l] || !w->wv[l] || !w->wo[l] ||
+            !w->ffn_norm[l] || !w->w1[l] || !w->w3[l] || !w->w2[l])
+            return fail(TFM_EINVAL, "NULL weight pointer in layer %d", l);
+    const cudaMemcpyKind kind = weights_on_host ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t* p = m->wmem + off;
+        off += (bytes + 255) / 256 * 256;
+        return p;
+    };
+    cudaError_t e = cudaSuccess;
+    auto copy = [&](void* dst, const void* src, size_t bytes) {
+        if (e == cudaSuccess) e = cudaMemcpy(dst, src, bytes, kind);
+    };
+    const size_t es = s.es;
+    m->embed = take(s.V * s.D * es);
+    copy(m->embed, w->embed, s.V * s.D * es);
+    m->attn_norm.assign(c.n_layer, nullptr);
+    m->ffn_norm.assign(c.n_layer, nullptr);
+    m->wqkv.assign(c.n_layer, nullptr);
+    m->wo.assign(c.n_layer, nullptr);
+    m->w1.assign(c.n_layer, nullptr);
+    m->w3.assign(c.n_layer, nullptr);
+    m->w2.assign(c.n_layer, nullptr);
+    for (int l = 0; l < c.n_layer; ++l) {
+        m->attn_norm[l] = reinterpret_cast<float*>(take(s.D * 4));
+        copy(m->attn_norm[l], w->attn_norm[l], s.D * 4);
+        uint8_t* qkv = take(s.Nqkv * s.D * es);
+        m->wqkv[l] = qkv;
+        copy(qkv, w->wq[l], s.Dq * s.D * es);
+        copy(qkv + s.Dq * s.D * es, w->wk[l], s.Dkv * s.D * es);
+        copy(qkv + (s.Dq + s.Dkv) * s.D * es, w->wv[l], s.Dkv * s.D * es);
+        m->wo[l] = take(s.D * s.Dq * es);
+        copy(m->wo[l], w->wo[l], s.D * s.Dq * es);
+        m->ffn_norm[l] = reinterpret_cast<float*>(take(s.D * 4));
+        copy(m->ffn_norm[l], w->ffn_norm[l], s.D * 4);
+        m->w1[l] = take(s.F * s.D * es);
+        copy(m->w1[l], w->w1[l], s.F * s.D * es);
+        m->w3[l] = take(s.F * s.D * es);
+        copy(m->w3[l], w->w3[l], s.F * s.D * es);
+        m->w2[l] = take(s.D * s.F * es);
+        copy(m->w2[l], w->w2[l], s.D * s.F * es);
+    }
+    m->final_norm = reinterpret_cast<float*>(take(s.D * 4));
+    copy(m->final_norm, w->final_norm, s.D * 4);
+    if (w->lm_head == w->embed) {
+        m->lm_head = m->embed;
+    } else {
+        m->lm_head = take(s.V * s.D * es);
+        copy(m->lm_head, w->lm_head, s.V * s.D * es);
+    }
+    if (off > m->wbytes) return fail(TFM_EINVAL, "internal: weight storage overflow");
+    if (e != cudaSuccess) return tfm::cuda_fail(e, "tfm_load_weights");
+    m->loaded = true;
+    m->plan_m = -1;
+    return TFM_OK;
+}
+
+}  // extern "C"
+
+namespace tfm {
+namespace {
+
+EpiParams epi_basic(int kind, int M, int N, void* out, int64_t ldo) {
+    EpiParams p{};
+    p.kind = kind;
+    p.M = M;
+    p.N = N;
+    p.out = out;
+    p.ldo = ldo;
+    return p;
+}
+
+EpiParams epi_qkv(Model* m, int M, int S) {
+    const tfm_config& c = m->cfg;
+    EpiParams p{};
+    p.kind = EPI_QKV_ROPE;
+    p.M = M;
+    p.N = (int)m->sz.Nqkv;
+    p.out_bf16 = c.mode == TFM_BF16;
+    p.S = S;
+    p.n_head = c.n_head;
+    p.n_kv_head = c.n_kv_head;
+    p.dh = c.d_model / c.n_head;
+    p.rope_cos = m->rcos();
+    p.rope_sin = m->rsin();
+    p.q = m->q();
+    p.k = m->k();
+    p.v = m->v();
+    return p;
+}
+
+// (Re)builds the tensor maps of every tensor-core GEMM of the forward for M
+// tokens of sequences of length S writing logits at (logits, ld).
+tfm_status build_plans(Model* m, int M, int S, float* logits, int64_t ld) {
+    if (m->plan_m == M && m->plan_S == S && m->plan_logits == logits && m->plan_ld == ld)
+        return TFM_OK;
+    const tfm_config& c = m->cfg;
+    const auto& s = m->sz;
+    m->p_qkv.resize(c.n_layer);
+    m->p_o.resize(c.n_layer);
+    m->p_gu.resize(c.n_layer);
+    m->p_down.resize(c.n_layer);
+    m->plan_m = -1;
+    tfm_status st = TFM_OK;
+    for (int l = 0; l < c.n_layer && st == TFM_OK; ++l) {
+        st = plan_gemm_tc(&m->p_qkv[l], m->xn(), s.D, m->wqkv[l], nullptr, s.D, M, (int)s.Nqkv,
+                          (int)s.D, epi_qkv(m, M, S));
+        if (st == TFM_OK)
+            st = plan_gemm_tc(&m->p_o[l], m->o(), s.Dq, m->wo[l], nullptr, s.Dq, M, (int)s.D,
+                              (int)s.Dq, epi_basic(EPI_ACCUM_F32, M, (int)s.D, m->h(), s.D));
+        if (st == TFM_OK) {
+            EpiParams e = epi_basic(EPI_SWIGLU, M, (int)s.F, m->a(), s.F);
+            e.out_bf16 = 1;
+            st = plan_gemm_tc(&m->p_gu[l], m->xn(), s.D, m->w1[l], m->w3[l], s.D, M, (int)s.F,
+                              (int)s.D, e);
+        }
+        if (st == TFM_OK)
+            st = plan_gemm_tc(&m->p_down[l], m->a(), s.F, m->w2[l], nullptr, s.F, M, (int)s.D,
+                              (int)s.F, epi_basic(EPI_ACCUM_F32, M, (int)s.D, m->h(), s.D));
+    }
+    if (st == TFM_OK)
+        st = plan_gemm_tc(&m->p_lm, m->xn(), s.D, m->lm_head, nullptr, s.D, M, (int)s.V, (int)s.D,
+                          epi_basic(EPI_STORE_F32, M, (int)s.V, logits, ld));
+    if (st != TFM_OK) return fail(st, "could not encode TMA tensor maps (driver entry point missing?)");
+    m->plan_m = M;
+    m->plan_S = S;
+    m->plan_logits = logits;
+    m->plan_ld = ld;
+    return TFM_OK;
+}
+
+#define TFM_LAUNCH(expr)                                            \
+    do {                                                            \
+        cudaError_t _e = (expr);                                    \
+        if (_e != cudaSuccess) return cuda_fail(_e, #expr);         \
+    } while (0)
+
+tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* logits, int64_t ld,
+                        cudaStream_t st) {
+    const tfm_config& c = m->cfg;
+    const auto& s = m->sz;
+    const int M = B * S;
+    const int dh = c.d_model / c.n_head;
+    const float scale = 1.0f / std::sqrt((float)dh);
+    const bool bf = c.mode == TFM_BF16;
+    if (!device_error_word()) return fail(TFM_ECUDA, "device error word unavailable");
+    TFM_LAUNCH(launch_embedding(tokens, m->embed, m->h(), M, c.vocab, c.d_model, bf, st));
+    if (bf) {
+        tfm_status ps = build_plans(m, M, S, logits, ld);
+        if (ps != TFM_OK) return ps;
+        for (int l = 0; l < c.n_layer; ++l) {
+            TFM_LAUNCH(launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 1, st));
+            TFM_LAUNCH(launch_gemm_tc(m->p_qkv[l], st));
+            TFM_LAUNCH(launch_attention_bf16(m->q(), m->k(), m->v(), m->o(), B, c.n_head,
+                                             c.n_kv_head, S, dh, scale, st));
+            TFM_LAUNCH(launch_gemm_tc(m->p_o[l], st));
+            TFM_LAUNCH(launch_rmsnorm(m->h(), m->ffn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 1, st));
+            TFM_LAUNCH(launch_gemm_tc(m->p_gu[l], st));
+            TFM_LAUNCH(launch_gemm_tc(m->p_down[l], st));
+        }
+        TFM_LAUNCH(launch_rmsnorm(m->h(), m->final_norm, m->xn(), M, c.d_model, c.norm_eps, 1, st));
+        TFM_LAUNCH(launch_gemm_tc(m->p_lm, st));
+    } else {
+        const float* xn = static_cast<const float*>(m->xn());
+        for (int l = 0; l < c.n_layer; ++l) {
+            TFM_LAUNCH(launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 0, st));
+            TFM_LAUNCH(launch_gemm_simt(xn, static_cast<const float*>(m->wqkv[l]), nullptr, M,
+                                        (int)s.Nqkv, c.d_model, epi_qkv(m, M, S), st));
+            TFM_LAUNCH(launch_attention_simt(static_cast<const float*>(m->q()),
+                                             static_cast<const float*>(m->k()),
+                                             static_cast<const float*>(m->v()),
+                                             static_cast<float*>(m->o()), B, c.n_head, c.n_kv_head,
+                                             S, dh, scale, st));
+            TFM_LAUNCH(launch_gemm_simt(static_cast<const float*>(m->o()),
+                                        static_cast<const float*>(m->wo[l]), nullptr, M, c.d_model,
+                                        (int)s.Dq, epi_basic(EPI_ACCUM_F32, M, c.d_model, m->h(), s.D),
+                                        st));
+            TFM_LAUNCH(launch_rmsnorm(m->h(), m->ffn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 0, st));
+            EpiParams e = epi_basic(EPI_SWIGLU, M, c.d_ff, m->a(), s.F);
+            e.out_bf16 = 0;
+            TFM_LAUNCH(launch_gemm_simt(xn, static_cast<const float*>(m->w1[l]),
+                                        static_cast<const float*>(m->w3[l]), M, c.d_ff, c.d_model, e, st));
+            TFM_LAUNCH(launch_gemm_simt(static_cast<const float*>(m->a()),
+                                        static_cast<const float*>(m->w2[l]), nullptr, M, c.d_model,
+                                        c.d_ff, epi_basic(EPI_ACCUM_F32, M, c.d_model, m->h(), s.D), st));
+        }
+        TFM_LAUNCH(launch_rmsnorm(m->h(), m->final_norm, m->xn(), M, c.d_model, c.norm_eps, 0, st));
+        TFM_LAUNCH(launch_gemm_simt(xn, static_cast<const float*>(m->lm_head), nullptr, M, c.vocab,
+                                    c.d_model, epi_basic(EPI_STORE_F32, M, c.vocab, logits, ld), st));
+    }
+    return TFM_OK;
+}
+
+tfm_status check_forward_args(Model* m, const void* tokens, int B, int S, const float* logits,
+                              int64_t ld) {
+    if (!m) return fail(TFM_EINVAL, "NULL handle");
+    if (!m->loaded) return fail(TFM_EINVAL, "weights not loaded");
+    if (!tokens || !logits) return fail(TFM_EINVAL, "NULL tokens or logits");
+    if (B < 1 || B > m->cfg.max_batch) return fail(TFM_EINVAL, "B=%d outside [1, max_batch=%d]", B, m->cfg.max_batch);
+    if (S < 1 || S > m->cfg.max_seq) return fail(TFM_EINVAL, "S=%d outside [1, max_seq=%d]", S, m->cfg.max_seq);
+    if (ld < m->cfg.vocab || ld % 4) return fail(TFM_EINVAL, "ld_logits=%lld must be >= vocab and a multiple of 4", (long long)ld);
+    return TFM_OK;
+}
+
+}  // namespace
+}  // namespace tfm
+
+extern "C" {
+
+tfm_status tfm_forward(void* handle, const int32_t* tokens, int32_t B, int32_t S, float* logits,
+                       int64_t ld_logits, void* stream) {
+    Model* m = static_cast<Model*>(handle);
+    tfm_status st = tfm::check_forward_args(m, tokens, B, S, logits, ld_logits);
+    if (st != TFM_OK) return st;
+    if (!tfm::aligned16(logits)) return fail(TFM_EINVAL, "logits must be 16-byte aligned");
+    return tfm::forward_impl(m, tokens, B, S, logits, ld_logits, static_cast<cudaStream_t>(stream));
+}
+
+tfm_status tfm_forward_host(void* handle, const int32_t* tokens_host, int32_t B, int32_t S,
+                            float* logits_host, int64_t ld_logits, void* stream) {
+    Model* m = static_cast<Model*>(handle);
+    tfm_status st = tfm::check_forward_args(m, tokens_host, B, S, logits_host, ld_logits);
+    if (st != TFM_OK) return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const int64_t M = (int64_t)B * S;
+    cudaError_t e = cudaMemcpyAsync(m->tok(), tokens_host, M * 4, cudaMemcpyHostToDevice, cs);
+    if (e != cudaSuccess) return tfm::cuda_fail(e, "tokens host->device");
+    st = tfm::forward_impl(m, m->tok(), B, S, m->logits(), m->sz.ldV, cs);
+    if (st != TFM_OK) return st;
+    e = cudaMemcpy2DAsync(logits_host, ld_logits * 4, m->logits(), m->sz.ldV * 4,
+                          (size_t)m->cfg.vocab * 4, M, cudaMemcpyDeviceToHost, cs);
+    if (e != cudaSuccess) return tfm::cuda_fail(e, "logits device->host");
+    return TFM_OK;
+}
+
+tfm_status tfm_device_status(void* handle) {
+    (void)handle;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return tfm::cuda_fail(e, "device synchronize");
+    int* w = tfm::device_error_word();
+    if (!w) return fail(TFM_ECUDA, "device error word unavailable");
+    int v = 0, zero = 0;
+    e = cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && v != 0) e = cudaMemcpy(w, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return tfm::cuda_fail(e, "read device error word");
+    if (v == TFM_EBADTOKEN) return fail(TFM_EBADTOKEN, "a token id was outside [0, vocab)");
+    if (v == TFM_ETIMEOUT) return fail(TFM_ETIMEOUT, "a pipeline wait timed out on the device");
+    if (v != 0) return fail((tfm_status)v, "device error %d", v);
+    return TFM_OK;
+}
+
+// ------------------------------------------------------------------ components
+
+tfm_status tfm_embedding(const int32_t* tokens, const void* E, float* h, int64_t M, int32_t V,
+                         int32_t D, int32_t mode, void* stream) {
+    if (!tokens || !E || !h) return fail(TFM_EINVAL, "NULL pointer");
+    if (M < 0 || V < 1 || D < 1) return fail(TFM_EINVAL, "bad sizes");
+    if (mode != TFM_FP32 && mode != TFM_BF16) return fail(TFM_EINVAL, "bad mode");
+    if (D % (mode == TFM_BF16 ? 8 : 4)) return fail(TFM_EINVAL, "D must be a multiple of %d", mode == TFM_BF16 ? 8 : 4);
+    if (!tfm::aligned16(E) || !tfm::aligned16(h)) return fail(TFM_EINVAL, "E and h must be 16-byte aligned");
+    if (!tfm::device_error_word()) return fail(TFM_ECUDA, "device error word unavailable");
+    cudaError_t e = tfm::launch_embedding(tokens, E, h, M, V, D, mode == TFM_BF16,
+                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TFM_OK : tfm::cuda_fail(e, "embedding launch");
+}
+
+tfm_status tfm_rmsnorm(const float* x, const float* g, void* y, int64_t M, int32_t D, float eps,
+                       int32_t out_mode, void* stream) {
+    if (!x || !g || !y) return fail(TFM_EINVAL, "NULL pointer");
+    if (M < 0 || D < 8 || D % 8) return fail(TFM_EINVAL, "D must be a positive multiple of 8");
+    if (!(eps > 0.f)) return fail(TFM_EINVAL, "eps must be > 0");
+    if (out_mode != TFM_FP32 && out_mode != TFM_BF16) return fail(TFM_EINVAL, "bad out_mode");
+    if (!tfm::aligned16(x) || !tfm::aligned16(g) || !tfm::aligned16(y))
+        return fail(TFM_EINVAL, "x, g, y must be 16-byte aligned");
+    cudaError_t e = tfm::launch_rmsnorm(x, g, y, M, D, eps, out_mode == TFM_BF16,
+                                        static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TFM_OK : tfm::cuda_fail(e, "rmsnorm launch");
+}
+
+tfm_status tfm_rope(void* x, const int32_t* positions, int32_t B, int32_t H, int32_t S, int32_t dh,
+                    float theta, int32_t mode, void* stream) {
+    if (!x) return fail(TFM_EINVAL, "NULL x");
+    if (B < 0 || H < 0 || S < 0 || dh < 2 || dh % 2 || dh > 256) return fail(TFM_EINVAL, "bad sizes");
+    if (!(theta > 1.f)) return fail(TFM_EINVAL, "theta must be > 1");
+    if (mode != TFM_FP32 && mode != TFM_BF16) return fail(TFM_EINVAL, "bad mode");
+    cudaError_t e = tfm::launch_rope(x, positions, B, H, S, dh, theta, mode == TFM_BF16,
+                                     static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TFM_OK : tfm::cuda_fail(e, "rope launch");
+}
+
+tfm_status tfm_causal_attention(const void* q, const void* k, const void* v, void* o, int32_t B,
+                                int32_t H, int32_t Hkv, int32_t S, int32_t dh, float scale,
+                                int32_t mode, void* stream) {
+    if (!q || !k || !v || !o) return fail(TFM_EINVAL, "NULL pointer");
+    if (B < 0 || S < 0 || H < 1 || Hkv < 1 || H % Hkv) return fail(TFM_EINVAL, "bad head counts");
+    if (!tfm::aligned16(q) || !tfm::aligned16(k) || !tfm::aligned16(v) || !tfm::aligned16(o))
+        return fail(TFM_EINVAL, "q, k, v, o must be 16-byte aligned");
+    if (scale <= 0.f) scale = 1.0f / std::sqrt((float)dh);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (mode == TFM_BF16) {
+        if (dh != 32 && dh != 64 && dh != 128) return fail(TFM_EUNSUPPORTED, "bf16 attention: dh in {32,64,128}");
+        e = tfm::launch_attention_bf16(q, k, v, o, B, H, Hkv, S, dh, scale, cs);
+    } else if (mode == TFM_FP32) {
+        if (dh < 1 || dh > 128) return fail(TFM_EUNSUPPORTED, "fp32 attention: dh <= 128");
+        e = tfm::launch_attention_simt(static_cast<const float*>(q), static_cast<const float*>(k),
+                                       static_cast<const float*>(v), static_cast<float*>(o), B, H,
+                                       Hkv, S, dh, scale, cs);
+    } else {
+        return fail(TFM_EINVAL, "bad mode");
+    }
+    return e == cudaSuccess ? TFM_OK : tfm::cuda_fail(e, "attention launch");
+}
+
+tfm_status tfm_linear(const void* x, const void* W, void* y, int64_t M, int32_t N, int32_t K,
+                      int64_t ldy, int32_t out_fp32, int32_t accumulate, int32_t mode, void* stream) {
+    if (!x || !W || !y) return fail(TFM_EINVAL, "NULL pointer");
+    if (M < 0 || M > INT32_MAX || N < 1 || K < 1 || ldy < N || ldy % 8) return fail(TFM_EINVAL, "bad sizes");
+    if (!tfm::aligned16(x) || !tfm::aligned16(W) || !tfm::aligned16(y)) return fail(TFM_EINVAL, "pointers must be 16-byte aligned");
+    if (!out_fp32 && (accumulate || mode != TFM_BF16)) return fail(TFM_EINVAL, "bf16 output: bf16 mode, no accumulate");
+    const int kind = out_fp32 ? (accumulate ? tfm::EPI_ACCUM_F32 : tfm::EPI_STORE_F32) : tfm::EPI_STORE_BF16;
+    tfm::EpiParams epi = tfm::epi_basic(kind, (int)M, N, y, ldy);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (mode == TFM_BF16) {
+        if (K % 8) return fail(TFM_EINVAL, "bf16 mode: K %% 8 == 0");
+        tfm::GemmPlan plan;
+        tfm_status st = tfm::plan_gemm_tc(&plan, x, K, W, nullptr, K, (int)M, N, K, epi);
+        if (st != TFM_OK) return fail(st, "tensor map encoding failed");
+        e = tfm::launch_gemm_tc(plan, cs);
+    } else if (mode == TFM_FP32) {
+        e = tfm::launch_gemm_simt(static_cast<const float*>(x), static_cast<const float*>(W), nullptr,
+                                  (int)M, N, K, epi, cs);
+    } else {
+        return fail(TFM_EINVAL, "bad mode");
+    }
+    return e == cudaSuccess ? TFM_OK : tfm::cuda_fail(e, "linear launch");
+}
+
+size_t tfm_swiglu_workspace_bytes(int64_t M, int32_t F, int32_t mode) {
+    if (M < 0 || F < 1) return 0;
+    return (size_t)M * F * (mode == TFM_BF16 ? 2 : 4);
+}
+
+tfm_status tfm_swiglu(const void* x, const void* w1, const void* w3, const void* w2, float* y,
+                      int64_t M, int32_t D, int32_t F, int32_t accumulate, void* workspace,
+                      size_t workspace_bytes, int32_t mode, void* stream) {
+    if (!x || !w1 || !w3 || !w2 || !y || !workspace) return fail(TFM_EINVAL, "NULL pointer");
+    if (M < 0 || M > INT32_MAX || D < 1 || F < 1) return fail(TFM_EINVAL, "bad sizes");
+    if (mode != TFM_FP32 && mode != TFM_BF16) return fail(TFM_EINVAL, "bad mode");
+    if (workspace_bytes < tfm_swiglu_workspace_bytes(M, F, mode)) return fail(TFM_EINVAL, "workspace too small");
+    if (!tfm::aligned16(x) || !tfm::aligned16(w1) || !tfm::aligned16(w3) || !tfm::aligned16(w2) ||
+        !tfm::aligned16(y) || !tfm::aligned16(workspace))
+        return fail(TFM_EINVAL, "pointers must be 16-byte aligned");
+    if (D % 8 || F % 8) return fail(TFM_EINVAL, "D and F must be multiples of 8");
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    tfm::EpiParams eg = tfm::epi_basic(tfm::EPI_SWIGLU, (int)M, F, workspace, F);
+    tfm::EpiParams ed = tfm::epi_basic(accumulate ? tfm::EPI_ACCUM_F32 : tfm::EPI_STORE_F32, (int)M,
+                                       D, y, D);
+    cudaError_t e;
+    if (mode == TFM_BF16) {
+        eg.out_bf16 = 1;
+        tfm::GemmPlan pg, pd;
+        tfm_status st = tfm::plan_gemm_tc(&pg, x, D, w1, w3, D, (int)M, F, D, eg);
+        if (st == TFM_OK) st = tfm::plan_gemm_tc(&pd, workspace, F, w2, nullptr, F, (int)M, D, F, ed);
+        if (st != TFM_OK) return fail(st, "tensor map encoding failed");
+        e = tfm::launch_gemm_tc(pg, cs);
+        if (e == cudaSuccess) e = tfm::launch_gemm_tc(pd, cs);
+    } else {
+        eg.out_bf16 = 0;
+        e = tfm::launch_gemm_simt(static_cast<const float*>(x), static_cast<const float*>(w1),
+                                  static_cast<const float*>(w3), (int)M, F, D, eg, cs);
+        if (e == cudaSuccess)
+            e = tfm::launch_gemm_simt(static_cast<const float*>(workspace),
+                                      static_cast<const float*>(w2), nullptr, (int)M, D, F, ed, cs);
+    }
+    return e == cudaSuccess ? TFM_OK : tfm::cuda_fail(e, "swiglu launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,184 @@
+// epilogue.cuh - what a GEMM does with a chunk of W consecutive accumulator
+// columns of one output row.  Shared by the tensor-core GEMM (W = 32, one
+// TMEM load per chunk) and the CUDA-core GEMM of fp32 mode (W = 4).
+//
+// The fusions are the ones the pre-norm block allows without changing what is
+// computed:
+//  - residual add after the output and down projections (CS336 walkthrough,
+//    section 5.7: x = x + attention(norm1(x)); x = x + ffn(norm2(x)));
+//  - silu(gate) * up after the W1/W3 projections (section 5.3 SwiGLU);
+//  - RoPE on the q and k columns and the head split (B,S,H*dh) -> (B,H,S,dh)
+//    after the QKV projection (sections 5.4 多头注意力 and 5.5 RoPE: rotate
+//    adjacent pairs of each head by position * theta^(-2i/dh); v is not rotated).
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace tfm {
+
+template <int N>
+__device__ __forceinline__ void load_vec(const float* p, float (&v)[N]) {
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < N; i += 4) {
+            float4 t = *reinterpret_cast<const float4*>(p + i);
+            v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
+        }
+    } else if constexpr (N % 2 == 0) {
+#pragma unroll
+        for (int i = 0; i < N; i += 2) {
+            float2 t = *reinterpret_cast<const float2*>(p + i);
+            v[i] = t.x; v[i + 1] = t.y;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) v[i] = p[i];
+    }
+}
+
+// Store W values starting at element `col0` of a row (`n_valid` of them are in
+// range).  Full chunks use 16-byte (or 8-byte) vector stores.
+template <int W>
+__device__ __forceinline__ void store_row_f32(float* dst, const float (&v)[W], int n_valid) {
+    if (n_valid >= W) {
+        if constexpr (W % 4 == 0) {
+#pragma unroll
+            for (int i = 0; i < W; i += 4)
+                *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < W; ++i) dst[i] = v[i];
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < W; ++i)
+            if (i < n_valid) dst[i] = v[i];
+    }
+}
+
+template <int W>
+__device__ __forceinline__ void accum_row_f32(float* dst, const float (&v)[W], int n_valid) {
+    if (n_valid >= W) {
+        if constexpr (W % 4 == 0) {
+#pragma unroll
+            for (int i = 0; i < W; i += 4) {
+                float4 t = *reinterpret_cast<float4*>(dst + i);
+                t.x += v[i]; t.y += v[i + 1]; t.z += v[i + 2]; t.w += v[i + 3];
+                *reinterpret_cast<float4*>(dst + i) = t;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < W; ++i) dst[i] += v[i];
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < W; ++i)
+            if (i < n_valid) dst[i] += v[i];
+    }
+}
+
+template <int W>
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float (&v)[W], int n_valid) {
+    if (n_valid >= W) {
+        if constexpr (W % 8 == 0) {
+#pragma unroll
+            for (int i = 0; i < W; i += 8) {
+                uint4 t;
+                t.x = pack_bf16x2(v[i], v[i + 1]);
+                t.y = pack_bf16x2(v[i + 2], v[i + 3]);
+                t.z = pack_bf16x2(v[i + 4], v[i + 5]);
+                t.w = pack_bf16x2(v[i + 6], v[i + 7]);
+                *reinterpret_cast<uint4*>(dst + i) = t;
+            }
+        } else if constexpr (W % 4 == 0) {
+#pragma unroll
+            for (int i = 0; i < W; i += 4) {
+                uint2 t;
+                t.x = pack_bf16x2(v[i], v[i + 1]);
+                t.y = pack_bf16x2(v[i + 2], v[i + 3]);
+                *reinterpret_cast<uint2*>(dst + i) = t;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < W; ++i) dst[i] = __float2bfloat16_rn(v[i]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < W; ++i)
+            if (i < n_valid) dst[i] = __float2bfloat16_rn(v[i]);
+    }
+}
+
+// a: accumulator columns [col0, col0+W) of output row `row`; u: the matching
+// "up" columns for EPI_SWIGLU (ignored otherwise).  For EPI_QKV_ROPE the chunk
+// lies inside one head (W divides dh) and col0 is a multiple of W.
+template <int W>
+__device__ __forceinline__ void apply_epilogue(const EpiParams& p, int row, int col0,
+                                               const float (&a)[W], const float (&u)[W]) {
+    if (row >= p.M || col0 >= p.N) return;
+    const int n_valid = p.N - col0;
+    switch (p.kind) {
+        case EPI_STORE_F32:
+            store_row_f32<W>(static_cast<float*>(p.out) + (int64_t)row * p.ldo + col0, a, n_valid);
+            break;
+        case EPI_ACCUM_F32:
+            accum_row_f32<W>(static_cast<float*>(p.out) + (int64_t)row * p.ldo + col0, a, n_valid);
+            break;
+        case EPI_STORE_BF16:
+            store_row_bf16<W>(static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * p.ldo + col0, a,
+                              n_valid);
+            break;
+        case EPI_SWIGLU: {
+            float h[W];
+#pragma unroll
+            for (int i = 0; i < W; ++i) h[i] = silu(a[i]) * u[i];
+            if (p.out_bf16)
+                store_row_bf16<W>(static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * p.ldo + col0,
+                                  h, n_valid);
+            else
+                store_row_f32<W>(static_cast<float*>(p.out) + (int64_t)row * p.ldo + col0, h,
+                                 n_valid);
+            break;
+        }
+        case EPI_QKV_ROPE: {
+            const int dh = p.dh, Dq = p.n_head * dh, Dkv = p.n_kv_head * dh;
+            int c = col0, heads = p.n_head;
+            void* base = p.q;
+            bool rotate = true;
+            if (c >= Dq + Dkv) {
+                c -= Dq + Dkv; base = p.v; heads = p.n_kv_head; rotate = false;
+            } else if (c >= Dq) {
+                c -= Dq; base = p.k; heads = p.n_kv_head;
+            }
+            const int hd = c / dh, d0 = c - hd * dh;
+            const int b = row / p.S, s = row - b * p.S;
+            const int64_t off = (((int64_t)b * heads + hd) * p.S + s) * dh + d0;
+            float o[W];
+            if (rotate) {
+                float cs[W / 2], sn[W / 2];
+                const int64_t t = (int64_t)s * (dh / 2) + d0 / 2;
+                load_vec<W / 2>(p.rope_cos + t, cs);
+                load_vec<W / 2>(p.rope_sin + t, sn);
+#pragma unroll
+                for (int j = 0; j < W / 2; ++j) {
+                    const float x0 = a[2 * j], x1 = a[2 * j + 1];
+                    o[2 * j] = x0 * cs[j] - x1 * sn[j];
+                    o[2 * j + 1] = x0 * sn[j] + x1 * cs[j];
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < W; ++j) o[j] = a[j];
+            }
+            if (p.out_bf16)
+                store_row_bf16<W>(static_cast<__nv_bfloat16*>(base) + off, o, W);
+            else
+                store_row_f32<W>(static_cast<float*>(base) + off, o, W);
+            break;
+        }
+        default:
+            break;
+    }
+}
+
+}  // namespace tfm

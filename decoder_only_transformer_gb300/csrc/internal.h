@@ -1,0 +1,77 @@
+// internal.h - declarations shared by libtfm's translation units (host side).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tfm.h"
+
+namespace tfm {
+
+// Epilogues a GEMM applies to its fp32 accumulator tile.
+enum EpiKind {
+    EPI_STORE_F32 = 0,   // out[m, n] = acc                      (fp32, e.g. logits)
+    EPI_ACCUM_F32 = 1,   // out[m, n] += acc                     (fp32 residual stream)
+    EPI_STORE_BF16 = 2,  // out[m, n] = bf16(acc)
+    EPI_SWIGLU = 3,      // out[m, f] = silu(gate) * up          (bf16 or fp32 hidden activation)
+    EPI_QKV_ROPE = 4,    // RoPE on q/k columns, scatter to head-major q, k, v
+};
+
+struct EpiParams {
+    int kind;
+    int M, N;             // output rows; output columns (F for EPI_SWIGLU, Dq+2Dkv for QKV)
+    void* out;            // STORE/ACCUM/SWIGLU destination
+    int64_t ldo;          // its row stride in elements
+    int out_bf16;         // SWIGLU/QKV: 1 = bf16 outputs, 0 = fp32
+    // EPI_QKV_ROPE: row m = b*S + s; columns [0,Dq) -> q[b,h,s,:], then k, then v
+    int S, n_head, n_kv_head, dh;
+    const float* rope_cos;   // [>= S, dh/2], cos(s * theta^(-2i/dh))
+    const float* rope_sin;
+    void* q;
+    void* k;
+    void* v;
+};
+
+// Library-global device error word of the current device (see raise_error).
+int* device_error_word();
+int sm_count();
+const char* cuda_error_text(cudaError_t e);
+
+// ---- elementwise kernels (k_rows.cu)
+cudaError_t launch_embedding(const int32_t* tok, const void* E, float* h, int64_t M, int V,
+                             int D, int e_bf16, cudaStream_t st);
+cudaError_t launch_rmsnorm(const float* x, const float* g, void* y, int64_t M, int D, float eps,
+                           int out_bf16, cudaStream_t st);
+cudaError_t launch_rope(void* x, const int32_t* pos, int B, int H, int S, int dh, float theta,
+                        int is_bf16, cudaStream_t st);
+
+// ---- CUDA-core kernels (k_simt.cu), fp32 mode
+// C = A[M,K] . B[N,K]^T (and A . B2^T for EPI_SWIGLU), then the epilogue.
+cudaError_t launch_gemm_simt(const float* A, const float* B, const float* B2, int M, int N,
+                             int K, const EpiParams& epi, cudaStream_t st);
+cudaError_t launch_attention_simt(const float* q, const float* k, const float* v, float* o,
+                                  int B, int H, int Hkv, int S, int dh, float scale,
+                                  cudaStream_t st);
+
+// ---- tensor-core GEMM (k_gemm_tc.cu), bf16 mode
+// Tensor maps for one GEMM: A [M,K] and B [N,K] bf16 row-major (B2 for SwiGLU).
+struct GemmPlan {
+    CUtensorMap map_a;
+    CUtensorMap map_b;
+    CUtensorMap map_b2;
+    int M, N, K;          // N = GEMM columns covered by tiles (F for SwiGLU)
+    int block_n;          // tile width (128 or 256); SwiGLU: gate+up halves of block_n/2
+    int dual;             // SwiGLU: B tile = [W1 rows; W3 rows]
+    EpiParams epi;
+};
+// Builds the tensor maps; returns TFM_OK or an error status with a message.
+tfm_status plan_gemm_tc(GemmPlan* plan, const void* A, int64_t lda, const void* B,
+                        const void* B2, int64_t ldb, int M, int N, int K, const EpiParams& epi);
+cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t st);
+
+// ---- bf16 flash attention (k_attention.cu)
+cudaError_t launch_attention_bf16(const void* q, const void* k, const void* v, void* o, int B,
+                                  int H, int Hkv, int S, int dh, float scale, cudaStream_t st);
+
+}  // namespace tfm

@@ -1,0 +1,315 @@
+// k_gemm_tc.cu - bf16 GEMM on the sm_103a tensor cores with fused epilogues.
+//
+// C[M, N] = A[M, K] . B[N, K]^T with both operands K-major (row-major, K
+// contiguous): the bias-free Linear of the CS336 walkthrough (section 5.3,
+// y = x W^T with W stored (out_features, in_features)).  fp32 accumulation in
+// tensor memory; the epilogue (epilogue.cuh) applies the fused residual add,
+// silu*mul, or RoPE + head split.
+//
+// Structure (one CTA per SM, persistent over 128 x BN output tiles):
+//   warp 0      TMA producer: A box 128x64 and B box BNx64 (bf16, 128-byte
+//               swizzle) into a STAGES-deep shared-memory ring (full/empty mbarriers)
+//   warp 1      allocates 2*BN TMEM columns; one thread issues
+//               tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16) into one of two
+//               TMEM accumulators, tcgen05.commit frees ring slots and hands the
+//               finished accumulator to the epilogue
+//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time (warp w reads TMEM lanes
+//               32*(w%4)..), apply the epilogue, release the accumulator
+// Double-buffered accumulators let the epilogue of tile i overlap the MMAs of
+// tile i+1.  For SwiGLU (kDual) a B tile is [W1 rows n..n+BN/2; W3 rows
+// n..n+BN/2] so matching gate and up columns land in the same tile without
+// repacking the weights.  Every mbarrier wait is bounded (common.cuh).
+#include "epilogue.cuh"
+
+#include <mutex>
+
+namespace tfm {
+
+constexpr int kBM = 128;                 // tile rows = UMMA M
+constexpr int kBK = 64;                  // one 128-byte swizzle row of bf16
+constexpr int kUmmaK = 16;               // K per tcgen05.mma kind::f16
+constexpr int kTileABytes = kBM * kBK * 2;
+constexpr int kThreads = 192;
+
+template <int BN, int STAGES>
+struct TcSmem {
+    static constexpr int kTileBBytes = BN * kBK * 2;
+    static constexpr int kStageBytes = kTileABytes + kTileBBytes;
+    static constexpr int kBarOffset = STAGES * kStageBytes;
+    // full[S], empty[S], tfull[2], tempty[2], done
+    static constexpr int kNumBars = 2 * STAGES + 5;
+    static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
+    static constexpr int kBytes = kMiscOffset + 16 + 1024;   // + alignment slack
+};
+
+template <int BN, int STAGES, bool kDual>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+              const __grid_constant__ CUtensorMap map_b2, int M, int N, int K, EpiParams epi,
+              int* err) {
+    using L = TcSmem<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+
+    const uint32_t sA0 = base;
+    const uint32_t sB0 = base + STAGES * kTileABytes;
+    const uint32_t bars = base + L::kBarOffset;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int a) { return bars + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bars + 8u * (2 * STAGES + 2 + a); };
+    const uint32_t done_bar = bars + 8u * (2 * STAGES + 4);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + L::kMiscOffset);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMiscOffset + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_per_tile = kDual ? BN / 2 : BN;
+    const int num_m = (M + kBM - 1) / kBM;
+    const int num_n = (N + n_per_tile - 1) / n_per_tile;
+    const int num_tiles = num_m * num_n;
+    const int num_kb = (K + kBK - 1) / kBK;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 4);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&map_a);
+        tma_prefetch_desc(&map_b);
+        if (kDual) tma_prefetch_desc(&map_b2);
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_holder), 2 * BN);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const int m0 = (t % num_m) * kBM;
+                const int n0 = (t / num_m) * n_per_tile;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, err, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(full_bar(stage), L::kStageBytes);
+                    const uint32_t sa = sA0 + stage * kTileABytes;
+                    const uint32_t sb = sB0 + stage * L::kTileBBytes;
+                    tma_load_2d(sa, &map_a, kb * kBK, m0, full_bar(stage));
+                    if (kDual) {
+                        tma_load_2d(sb, &map_b, kb * kBK, n0, full_bar(stage));
+                        tma_load_2d(sb + (BN / 2) * kBK * 2, &map_b2, kb * kBK, n0, full_bar(stage));
+                    } else {
+                        tma_load_2d(sb, &map_b, kb * kBK, n0, full_bar(stage));
+                    }
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // Drain: every armed stage's last phase must have landed before exit.
+            for (int s = 0; s < STAGES && issued > 0; ++s) {
+                if (s >= issued) break;
+                const int64_t last = issued - 1 - ((issued - 1 - s) % STAGES);
+                mbar_wait(full_bar(s), (uint32_t)((last / STAGES) & 1), err, abort_flag);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = umma_idesc_bf16(kBM, BN);
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, err, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase, err, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = sA0 + stage * kTileABytes;
+                    const uint32_t sb = sB0 + stage * L::kTileBBytes;
+#pragma unroll
+                    for (int k = 0; k < kBK / kUmmaK; ++k) {
+                        const uint64_t ad = umma_desc_sw128(sa + k * kUmmaK * 2);
+                        const uint64_t bd = umma_desc_sw128(sb + k * kUmmaK * 2);
+                        umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    umma_commit(empty_bar(stage));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit(tfull_bar(acc));
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+            // All MMAs this thread issued must be complete before TMEM is freed.
+            umma_commit(done_bar);
+            mbar_wait(done_bar, 0, err, abort_flag);
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;                       // TMEM lane quarter of this warp
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+            const int m0 = (t % num_m) * kBM;
+            const int n0 = (t / num_m) * n_per_tile;
+            // Lane 0 waits (bounded); the outcome is broadcast so the warp stays
+            // converged for the .sync.aligned TMEM loads even on a timeout.
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(tfull_bar(acc), acc_phase, err, abort_flag) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            (void)mbar_try_wait(tfull_bar(acc), acc_phase);   // acquire in every lane
+            tc_fence_after();
+            const int row = m0 + q * 32 + lane;
+            const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            if (kDual) {
+#pragma unroll 1
+                for (int c = 0; c < BN / 2; c += 32) {
+                    float g[32], u[32];
+                    __syncwarp();
+                    tmem_ld32(trow + c, g);
+                    tmem_ld32(trow + BN / 2 + c, u);
+                    apply_epilogue<32>(epi, row, n0 + c, g, u);
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    float v[32];
+                    __syncwarp();
+                    tmem_ld32(trow + c, v);
+                    apply_epilogue<32>(epi, row, n0 + c, v, v);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, 2 * BN);
+}
+
+// ------------------------------------------------------------------ host side
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix with row stride ld
+// (elements), box = box_rows x 64 columns, 128-byte swizzle, zero fill out of range.
+bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
+              int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tile width minimising (waves x tile width), the per-SM critical path when
+// every tile costs time proportional to its width; ties go to the wider tile.
+int choose_block_n(int M, int N, bool dual) {
+    const int sms = sm_count();
+    const int num_m = (M + kBM - 1) / kBM;
+    int best = 256;
+    int64_t best_cost = -1;
+    for (int bn : {256, 128}) {
+        const int per = dual ? bn / 2 : bn;
+        const int64_t tiles = (int64_t)num_m * ((N + per - 1) / per);
+        const int64_t cost = ((tiles + sms - 1) / sms) * bn;
+        if (best_cost < 0 || cost < best_cost) { best = bn; best_cost = cost; }
+    }
+    return best;
+}
+
+template <int BN, int STAGES, bool kDual>
+cudaError_t launch_inst(const GemmPlan& p, cudaStream_t st) {
+    using L = TcSmem<BN, STAGES>;
+    static bool attr_set = false;   // per instantiation; set once per process
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, STAGES, kDual>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int per = kDual ? BN / 2 : BN;
+    const int64_t tiles = (int64_t)((p.M + kBM - 1) / kBM) * ((p.N + per - 1) / per);
+    const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
+    k_gemm_tc<BN, STAGES, kDual><<<grid, kThreads, L::kBytes, st>>>(
+        p.map_a, p.map_b, p.map_b2, p.M, p.N, p.K, p.epi, device_error_word());
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+tfm_status plan_gemm_tc(GemmPlan* plan, const void* A, int64_t lda, const void* B, const void* B2,
+                        int64_t ldb, int M, int N, int K, const EpiParams& epi) {
+    const bool dual = B2 != nullptr;
+    plan->M = M;
+    plan->N = N;
+    plan->K = K;
+    plan->dual = dual ? 1 : 0;
+    plan->block_n = choose_block_n(M, N, dual);
+    plan->epi = epi;
+    const int box_b = dual ? plan->block_n / 2 : plan->block_n;
+    if (!make_map(&plan->map_a, A, M, K, lda, kBM)) return TFM_ECUDA;
+    if (!make_map(&plan->map_b, B, N, K, ldb, box_b)) return TFM_ECUDA;
+    if (dual) {
+        if (!make_map(&plan->map_b2, B2, N, K, ldb, box_b)) return TFM_ECUDA;
+    } else {
+        plan->map_b2 = plan->map_b;
+    }
+    return TFM_OK;
+}
+
+cudaError_t launch_gemm_tc(const GemmPlan& p, cudaStream_t st) {
+    if (p.M <= 0 || p.N <= 0) return cudaSuccess;
+    if (p.dual) {
+        if (p.block_n == 256) return launch_inst<256, 4, true>(p, st);
+        return launch_inst<128, 6, true>(p, st);
+    }
+    if (p.block_n == 256) return launch_inst<256, 4, false>(p, st);
+    return launch_inst<128, 6, false>(p, st);
+}
+
+}  // namespace tfm

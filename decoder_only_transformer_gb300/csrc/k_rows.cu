@@ -1,0 +1,215 @@
+// k_rows.cu - HBM-bound row kernels: embedding gather, RMSNorm (fp32 in,
+// bf16/fp32 out) and the standalone RoPE used by the component entry point.
+//
+// All three move each byte once: 16-byte vector loads and stores, one warp per
+// row, the row held in registers between the reduction and the write.
+#include "common.cuh"
+#include "internal.h"
+
+namespace tfm {
+
+// ------------------------------------------------------------------ embedding
+// h[m, :] = E[tok[m], :] (CS336 walkthrough, section 5.2: the Embedding layer
+// looks each token id up in a [vocab, d_model] table).  One warp per row; an
+// id outside [0, V) writes zeros and raises TFM_EBADTOKEN.
+template <bool kBf16>
+__global__ void __launch_bounds__(256) k_embedding(const int32_t* __restrict__ tok,
+                                                   const void* __restrict__ E,
+                                                   float* __restrict__ h, int64_t M, int V, int D,
+                                                   int* err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t m = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); m < M;
+         m += warps) {
+        const int t = __ldg(tok + m);
+        float* dst = h + m * D;
+        const bool ok = (t >= 0 && t < V);
+        if (!ok && lane == 0) raise_error(err, TFM_EBADTOKEN);
+        if (kBf16) {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                static_cast<const __nv_bfloat16*>(E) + (int64_t)(ok ? t : 0) * D);
+            for (int c = lane; c < D / 8; c += 32) {
+                uint4 w = ok ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                float4 lo = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+                float4 hi = make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+                reinterpret_cast<float4*>(dst)[2 * c] = lo;
+                reinterpret_cast<float4*>(dst)[2 * c + 1] = hi;
+            }
+        } else {
+            const float4* src = reinterpret_cast<const float4*>(
+                static_cast<const float*>(E) + (int64_t)(ok ? t : 0) * D);
+            for (int c = lane; c < D / 4; c += 32)
+                reinterpret_cast<float4*>(dst)[c] = ok ? __ldg(src + c) : make_float4(0, 0, 0, 0);
+        }
+    }
+}
+
+cudaError_t launch_embedding(const int32_t* tok, const void* E, float* h, int64_t M, int V, int D,
+                             int e_bf16, cudaStream_t st) {
+    if (M <= 0) return cudaSuccess;
+    int64_t blocks = (M + 7) / 8;
+    const int cap = sm_count() * 16;
+    if (blocks > cap) blocks = cap;
+    if (e_bf16)
+        k_embedding<true><<<(int)blocks, 256, 0, st>>>(tok, E, h, M, V, D, device_error_word());
+    else
+        k_embedding<false><<<(int)blocks, 256, 0, st>>>(tok, E, h, M, V, D, device_error_word());
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ RMSNorm
+// y = x / sqrt(mean(x^2) + eps) * g, in fp32, rounded once to the output type
+// (CS336 walkthrough, section 5.6: fp32 through the gain multiply, then cast).
+// One warp per row; lane l owns the float4 groups l, l+32, ...; kV groups per
+// lane are held in registers (rows up to 128*kV floats).
+template <int kV, bool kBf16>
+__global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ x,
+                                                 const float* __restrict__ g,
+                                                 void* __restrict__ y, int64_t M, int D,
+                                                 float eps) {
+    const int lane = threadIdx.x & 31;
+    const int64_t m = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (m >= M) return;
+    const int n4 = D >> 2;
+    const float4* xr = reinterpret_cast<const float4*>(x + m * D);
+    float4 v[kV];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < kV; ++i) {
+        const int c = lane + 32 * i;
+        v[i] = (c < n4) ? xr[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+        ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float r = 1.0f / sqrtf(ss / (float)D + eps);
+    const float4* g4 = reinterpret_cast<const float4*>(g);
+#pragma unroll
+    for (int i = 0; i < kV; ++i) {
+        const int c = lane + 32 * i;
+        if (c >= n4) break;
+        const float4 w = __ldg(g4 + c);
+        const float a0 = v[i].x * r * w.x, a1 = v[i].y * r * w.y;
+        const float a2 = v[i].z * r * w.z, a3 = v[i].w * r * w.w;
+        if (kBf16) {
+            uint2 o;
+            o.x = pack_bf16x2(a0, a1);
+            o.y = pack_bf16x2(a2, a3);
+            reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(y) + m * D)[c] = o;
+        } else {
+            reinterpret_cast<float4*>(static_cast<float*>(y) + m * D)[c] = make_float4(a0, a1, a2, a3);
+        }
+    }
+}
+
+// Rows longer than 128*32 floats: two passes over the row.
+template <bool kBf16>
+__global__ void __launch_bounds__(256) k_rmsnorm_long(const float* __restrict__ x,
+                                                      const float* __restrict__ g,
+                                                      void* __restrict__ y, int64_t M, int D,
+                                                      float eps) {
+    const int lane = threadIdx.x & 31;
+    const int64_t m = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (m >= M) return;
+    const float4* xr = reinterpret_cast<const float4*>(x + m * D);
+    float ss = 0.f;
+    for (int c = lane; c < D / 4; c += 32) {
+        const float4 t = xr[c];
+        ss += t.x * t.x + t.y * t.y + t.z * t.z + t.w * t.w;
+    }
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float r = 1.0f / sqrtf(ss / (float)D + eps);
+    for (int c = lane; c < D / 4; c += 32) {
+        const float4 t = xr[c], w = reinterpret_cast<const float4*>(g)[c];
+        const float a0 = t.x * r * w.x, a1 = t.y * r * w.y, a2 = t.z * r * w.z, a3 = t.w * r * w.w;
+        if (kBf16) {
+            uint2 o;
+            o.x = pack_bf16x2(a0, a1);
+            o.y = pack_bf16x2(a2, a3);
+            reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(y) + m * D)[c] = o;
+        } else {
+            reinterpret_cast<float4*>(static_cast<float*>(y) + m * D)[c] = make_float4(a0, a1, a2, a3);
+        }
+    }
+}
+
+template <int kV>
+static void rms_launch(const float* x, const float* g, void* y, int64_t M, int D, float eps,
+                       int out_bf16, cudaStream_t st) {
+    const unsigned blocks = (unsigned)((M + 7) / 8);
+    if (out_bf16)
+        k_rmsnorm<kV, true><<<blocks, 256, 0, st>>>(x, g, y, M, D, eps);
+    else
+        k_rmsnorm<kV, false><<<blocks, 256, 0, st>>>(x, g, y, M, D, eps);
+}
+
+cudaError_t launch_rmsnorm(const float* x, const float* g, void* y, int64_t M, int D, float eps,
+                           int out_bf16, cudaStream_t st) {
+    if (M <= 0) return cudaSuccess;
+    const int groups = (D / 4 + 31) / 32;   // float4 groups per lane
+    if (groups <= 1) rms_launch<1>(x, g, y, M, D, eps, out_bf16, st);
+    else if (groups <= 2) rms_launch<2>(x, g, y, M, D, eps, out_bf16, st);
+    else if (groups <= 4) rms_launch<4>(x, g, y, M, D, eps, out_bf16, st);
+    else if (groups <= 6) rms_launch<6>(x, g, y, M, D, eps, out_bf16, st);
+    else if (groups <= 8) rms_launch<8>(x, g, y, M, D, eps, out_bf16, st);
+    else if (groups <= 16) rms_launch<16>(x, g, y, M, D, eps, out_bf16, st);
+    else if (groups <= 32) rms_launch<32>(x, g, y, M, D, eps, out_bf16, st);
+    else {
+        const unsigned blocks = (unsigned)((M + 7) / 8);
+        if (out_bf16) k_rmsnorm_long<true><<<blocks, 256, 0, st>>>(x, g, y, M, D, eps);
+        else k_rmsnorm_long<false><<<blocks, 256, 0, st>>>(x, g, y, M, D, eps);
+    }
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ RoPE
+// In place on x [B, H, S, dh]: the pair (x[2i], x[2i+1]) of token s is turned
+// counter-clockwise by pos * theta^(-2i/dh) ("LLM 2", section RoPE: R_i(m)).
+// The angle and its sine/cosine are formed in double precision so the result
+// does not depend on fp32 angle rounding at large positions.  One thread per pair.
+template <typename T>
+__global__ void k_rope(T* __restrict__ x, const int32_t* __restrict__ pos, int B, int H, int S,
+                       int dh, double log_theta) {
+    const int half = dh >> 1;
+    const int64_t total = (int64_t)B * H * S * half;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int i = (int)(idx % half);
+        const int64_t row = idx / half;                  // (b*H + h)*S + s
+        const int s = (int)(row % S);
+        const int b = (int)(row / ((int64_t)S * H));
+        const double p = pos ? (double)pos[(int64_t)b * S + s] : (double)s;
+        const double ang = p * exp(-2.0 * (double)i / (double)dh * log_theta);
+        double sd, cd;
+        sincos(ang, &sd, &cd);
+        const float c = (float)cd, sn = (float)sd;
+        T* e = x + row * dh + 2 * i;
+        const float x0 = (float)e[0], x1 = (float)e[1];
+        const float y0 = x0 * c - x1 * sn, y1 = x0 * sn + x1 * c;
+        if constexpr (sizeof(T) == 2) {
+            e[0] = __float2bfloat16_rn(y0);
+            e[1] = __float2bfloat16_rn(y1);
+        } else {
+            e[0] = y0;
+            e[1] = y1;
+        }
+    }
+}
+
+cudaError_t launch_rope(void* x, const int32_t* pos, int B, int H, int S, int dh, float theta,
+                        int is_bf16, cudaStream_t st) {
+    const int64_t total = (int64_t)B * H * S * (dh / 2);
+    if (total <= 0) return cudaSuccess;
+    int64_t blocks = (total + 255) / 256;
+    const int64_t cap = (int64_t)sm_count() * 32;
+    if (blocks > cap) blocks = cap;
+    const double lt = log((double)theta);
+    if (is_bf16)
+        k_rope<__nv_bfloat16><<<(int)blocks, 256, 0, st>>>(static_cast<__nv_bfloat16*>(x), pos, B,
+                                                            H, S, dh, lt);
+    else
+        k_rope<float><<<(int)blocks, 256, 0, st>>>(static_cast<float*>(x), pos, B, H, S, dh, lt);
+    return cudaGetLastError();
+}
+
+}  // namespace tfm

@@ -1,0 +1,249 @@
+"""Thin ctypes binding of libtfm (include/tfm.h).
+
+Argument marshalling only: every step of the forward pass runs in the CUDA
+kernels of libtfm.so.  Tensors are torch tensors used as plain device (or host)
+buffers; the current torch CUDA stream is passed as the launch stream.  There is
+no fallback: if the library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+from . import _build
+
+TFM_OK, TFM_EINVAL, TFM_ENOMEM, TFM_ECUDA, TFM_EBADTOKEN, TFM_ETIMEOUT, TFM_EUNSUPPORTED = range(7)
+TFM_FP32, TFM_BF16 = 0, 1
+STATUS_NAMES = {0: "TFM_OK", 1: "TFM_EINVAL", 2: "TFM_ENOMEM", 3: "TFM_ECUDA",
+                4: "TFM_EBADTOKEN", 5: "TFM_ETIMEOUT", 6: "TFM_EUNSUPPORTED"}
+HEADER = os.path.join(_build.ROOT, "include", "tfm.h")
+
+
+class TfmError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("vocab", ctypes.c_int32), ("d_model", ctypes.c_int32),
+                ("n_head", ctypes.c_int32), ("n_kv_head", ctypes.c_int32),
+                ("n_layer", ctypes.c_int32), ("d_ff", ctypes.c_int32),
+                ("max_seq", ctypes.c_int32), ("max_batch", ctypes.c_int32),
+                ("rope_theta", ctypes.c_float), ("norm_eps", ctypes.c_float),
+                ("mode", ctypes.c_int32)]
+
+
+_PP = ctypes.POINTER(ctypes.c_void_p)
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("embed", ctypes.c_void_p), ("attn_norm", _PP), ("wq", _PP), ("wk", _PP),
+                ("wv", _PP), ("wo", _PP), ("ffn_norm", _PP), ("w1", _PP), ("w3", _PP),
+                ("w2", _PP), ("final_norm", ctypes.c_void_p), ("lm_head", ctypes.c_void_p)]
+
+
+_lib = None
+
+_V, _I32, _I64, _F, _SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                           ctypes.c_size_t)
+_SIGS = {
+    "tfm_abi_version": ([], _I32),
+    "tfm_validate_config": ([ctypes.POINTER(Config)], _I32),
+    "tfm_workspace_bytes": ([ctypes.POINTER(Config)], _SZ),
+    "tfm_weight_bytes": ([ctypes.POINTER(Config)], _SZ),
+    "tfm_create": ([ctypes.POINTER(Config), ctypes.POINTER(_V)], _I32),
+    "tfm_load_weights": ([_V, ctypes.POINTER(Weights), _I32], _I32),
+    "tfm_forward": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
+    "tfm_forward_host": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
+    "tfm_device_status": ([_V], _I32),
+    "tfm_last_error": ([], ctypes.c_char_p),
+    "tfm_destroy": ([_V], None),
+    "tfm_embedding": ([_V, _V, _V, _I64, _I32, _I32, _I32, _V], _I32),
+    "tfm_rmsnorm": ([_V, _V, _V, _I64, _I32, _F, _I32, _V], _I32),
+    "tfm_rope": ([_V, _V, _I32, _I32, _I32, _I32, _F, _I32, _V], _I32),
+    "tfm_causal_attention": ([_V, _V, _V, _V, _I32, _I32, _I32, _I32, _I32, _F, _I32, _V], _I32),
+    "tfm_linear": ([_V, _V, _V, _I64, _I32, _I32, _I64, _I32, _I32, _I32, _V], _I32),
+    "tfm_swiglu": ([_V, _V, _V, _V, _V, _I64, _I32, _I32, _I32, _V, _SZ, _I32, _V], _I32),
+    "tfm_swiglu_workspace_bytes": ([_I64, _I32, _I32], _SZ),
+}
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/tfm.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tfm_[a-z0-9_]+)\s*\(", text)))
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libtfm.so (building it first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_missing and _build.is_stale():
+        _build.build()
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError(f"libtfm.so not found at {_build.LIB}; run the package build first")
+    lib = ctypes.CDLL(_build.LIB)
+    for name, (args, res) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != TFM_OK:
+        raise TfmError(status, load().tfm_last_error().decode(errors="replace"))
+
+
+def _stream(stream=None):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _mode_of(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return TFM_BF16
+    if t.dtype == torch.float32:
+        return TFM_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def make_config(cfg, max_batch=None, max_seq=None) -> Config:
+    """Config from a workloads.ModelConfig-like object."""
+    return Config(cfg.vocab, cfg.d_model, cfg.n_head, cfg.n_kv_head, cfg.n_layer, cfg.d_ff,
+                  max_seq or cfg.seq, max_batch or cfg.batch, cfg.rope_theta, cfg.norm_eps,
+                  TFM_BF16 if cfg.mode == "bf16" else TFM_FP32)
+
+
+def validate_config(c: Config) -> int:
+    return load().tfm_validate_config(ctypes.byref(c))
+
+
+def workspace_bytes(c: Config) -> int:
+    return load().tfm_workspace_bytes(ctypes.byref(c))
+
+
+def weight_bytes(c: Config) -> int:
+    return load().tfm_weight_bytes(ctypes.byref(c))
+
+
+def device_status():
+    _check(load().tfm_device_status(None))
+
+
+class Model:
+    """A libtfm model handle.  ``weights`` is the dict layout of
+    ``workloads.make_weights`` with torch tensors (device or pinned host)."""
+
+    def __init__(self, cfg, max_batch=None, max_seq=None):
+        self.lib = load()
+        self.cfg = cfg
+        self.c = make_config(cfg, max_batch, max_seq)
+        h = ctypes.c_void_p()
+        _check(self.lib.tfm_create(ctypes.byref(self.c), ctypes.byref(h)))
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None):
+            self.lib.tfm_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def load_weights(self, w: dict):
+        L = self.cfg.n_layer
+
+        def arr(key):
+            a = (ctypes.c_void_p * max(L, 1))()
+            for i in range(L):
+                a[i] = w["layers"][i][key].data_ptr()
+            return ctypes.cast(a, _PP), a
+
+        keep = {}
+        fields = {}
+        for key in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w1", "w3", "w2"):
+            fields[key], keep[key] = arr(key)
+        ws = Weights(w["embed"].data_ptr(), fields["attn_norm"], fields["wq"], fields["wk"],
+                     fields["wv"], fields["wo"], fields["ffn_norm"], fields["w1"], fields["w3"],
+                     fields["w2"], w["final_norm"].data_ptr(), w["lm_head"].data_ptr())
+        on_host = 0 if w["embed"].is_cuda else 1
+        _check(self.lib.tfm_load_weights(self.handle, ctypes.byref(ws), on_host))
+
+    def forward(self, tokens, logits, stream=None):
+        """tokens: int32 [B, S] (device); logits: fp32 [B*S, ld] (device)."""
+        B, S = tokens.shape
+        _check(self.lib.tfm_forward(self.handle, _ptr(tokens), B, S, _ptr(logits),
+                                    logits.stride(0), _stream(stream)))
+
+    def forward_host(self, tokens, logits, stream=None):
+        """tokens: int32 [B, S] (host, pinned); logits: fp32 [B*S, ld] (host, pinned)."""
+        B, S = tokens.shape
+        _check(self.lib.tfm_forward_host(self.handle, _ptr(tokens), B, S, _ptr(logits),
+                                         logits.stride(0), _stream(stream)))
+
+
+# ---------------------------------------------------------------- components
+def embedding(tokens, E, h, stream=None):
+    M = tokens.numel()
+    _check(load().tfm_embedding(_ptr(tokens), _ptr(E), _ptr(h), M, E.shape[0], E.shape[1],
+                                _mode_of(E), _stream(stream)))
+
+
+def rmsnorm(x, g, y, eps=1e-5, stream=None):
+    M, D = x.shape
+    _check(load().tfm_rmsnorm(_ptr(x), _ptr(g), _ptr(y), M, D, eps, _mode_of(y), _stream(stream)))
+
+
+def rope(x, theta, positions=None, stream=None):
+    B, H, S, dh = x.shape
+    _check(load().tfm_rope(_ptr(x), _ptr(positions), B, H, S, dh, theta, _mode_of(x),
+                           _stream(stream)))
+
+
+def causal_attention(q, k, v, o, scale=0.0, stream=None):
+    B, H, S, dh = q.shape
+    Hkv = k.shape[1]
+    _check(load().tfm_causal_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Hkv, S, dh,
+                                       scale, _mode_of(q), _stream(stream)))
+
+
+def linear(x, W, y, accumulate=False, stream=None):
+    M, K = x.shape
+    N = W.shape[0]
+    import torch
+    out_fp32 = 1 if y.dtype == torch.float32 else 0
+    _check(load().tfm_linear(_ptr(x), _ptr(W), _ptr(y), M, N, K, y.stride(0), out_fp32,
+                             1 if accumulate else 0, _mode_of(x), _stream(stream)))
+
+
+def swiglu_workspace_bytes(M, F, mode):
+    return load().tfm_swiglu_workspace_bytes(M, F, mode)
+
+
+def swiglu(x, w1, w3, w2, y, workspace, accumulate=False, stream=None):
+    M, D = x.shape
+    F = w1.shape[0]
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().tfm_swiglu(_ptr(x), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(y), M, D, F,
+                             1 if accumulate else 0, _ptr(workspace), nbytes, _mode_of(x),
+                             _stream(stream)))

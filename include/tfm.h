@@ -1,0 +1,221 @@
+/*
+ * tfm.h - C ABI of libtfm, a GB300 (sm_103a) forward pass of a pre-norm
+ * decoder-only Transformer language model.
+ *
+ * The model is the one the CS336 Transformer walkthrough assembles
+ * ("手把手带工程同学从零实现一个完整的 LLM（CS336）——Transformer 篇",
+ * dujian.net, section 5.7 组装 Transformer) and that "LLM 2: Transformer
+ * 原理与实现" (juejin.cn) writes as h' = h + Attn(Norm(h)),
+ * h_next = h' + FFN(Norm(h')):
+ *
+ *   h = E[tokens]
+ *   for each layer:  h += Wo . Attn(RoPE(Wq u), RoPE(Wk u), Wv u),  u = RMSNorm(h) * g1
+ *                    h += W2 . (silu(W1 u) * W3 u),                  u = RMSNorm(h) * g2
+ *   logits = Wlm . (RMSNorm(h) * gf)
+ *
+ * with bias-free linears stored (out_features, in_features) row-major, RoPE on
+ * adjacent coordinate pairs, causal softmax attention scaled by 1/sqrt(d_head)
+ * and grouped-query heads (query head h reads kv head h / (n_head / n_kv_head)).
+ *
+ * Conventions for every function below:
+ *  - Pointers are plain addresses.  "device" pointers must be CUDA device (or
+ *    managed) memory of the current device; "host" pointers are host memory
+ *    (page-locked for asynchronous copies).  The caller owns every buffer it
+ *    passes; the library keeps no pointer to a caller buffer after a call
+ *    returns, except the weights of tfm_load_weights when weights_on_host == 0
+ *    and TFM_LOAD_BORROW is set (not the default; see there).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Compute calls only enqueue work on that stream and return; they never
+ *    synchronise, allocate or free memory.
+ *  - Every function returns a tfm_status.  Argument errors are found on the
+ *    host before anything is launched (TFM_EINVAL / TFM_EUNSUPPORTED) and
+ *    leave outputs untouched.  Errors found on the device (a token id outside
+ *    [0, vocab), a pipeline wait that gave up) set a sticky device error word
+ *    that tfm_device_status() reads and clears.  tfm_last_error() gives a
+ *    thread-local message for the last failing call.
+ *  - "bf16 mode" stores weights and activations in bfloat16 and accumulates in
+ *    fp32 (tcgen05 tensor cores); the residual stream and logits are fp32.
+ *    "fp32 mode" keeps everything in fp32 (CUDA-core FFMA).
+ */
+#ifndef TFM_H
+#define TFM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TFM_OK = 0,
+    TFM_EINVAL = 1,        /* bad argument: shape, pointer, alignment, mode */
+    TFM_ENOMEM = 2,        /* device allocation failed (tfm_create / tfm_load_weights only) */
+    TFM_ECUDA = 3,         /* a CUDA runtime call failed; see tfm_last_error() */
+    TFM_EBADTOKEN = 4,     /* device: a token id was outside [0, vocab); its row was zeroed */
+    TFM_ETIMEOUT = 5,      /* device: a bounded pipeline wait gave up; outputs are invalid */
+    TFM_EUNSUPPORTED = 6   /* valid request this build does not implement (e.g. d_head 48 in bf16) */
+} tfm_status;
+
+typedef enum { TFM_FP32 = 0, TFM_BF16 = 1 } tfm_mode;
+
+/* Model hyper-parameters.  Mirrors the TransformerLM constructor of the CS336
+ * walkthrough, section 5.7 (vocab_size, num_layers, d_model, num_heads, d_ff,
+ * theta, max_seq_len), plus n_kv_head for grouped-query attention ("LLM 2",
+ * section GQA / MQA) and the batch bound that sizes the workspace.
+ * Constraints (checked by tfm_validate_config):
+ *   d_model % n_head == 0 (the walkthrough's assert), d_head = d_model / n_head
+ *   even (RoPE pairs coordinates), n_head % n_kv_head == 0, all sizes > 0
+ *   (n_layer >= 0), norm_eps > 0, rope_theta > 1.
+ *   bf16 mode additionally: d_head in {32, 64, 128}, d_model % 64 == 0,
+ *   d_ff % 8 == 0, vocab >= 1.  fp32 mode: d_head <= 128. */
+typedef struct {
+    int32_t vocab;
+    int32_t d_model;
+    int32_t n_head;
+    int32_t n_kv_head;
+    int32_t n_layer;
+    int32_t d_ff;
+    int32_t max_seq;
+    int32_t max_batch;
+    float rope_theta;
+    float norm_eps;
+    int32_t mode;          /* tfm_mode */
+} tfm_config;
+
+/* Weights, all row-major (out_features, in_features) like the walkthrough's
+ * Linear (section 5.3).  Matrices are bf16 in bf16 mode and fp32 in fp32 mode;
+ * the RMSNorm gains are always fp32.  Per-layer entries are arrays of n_layer
+ * pointers.  Shapes, with Dq = n_head*d_head and Dkv = n_kv_head*d_head:
+ *   embed [vocab, d_model]; attn_norm, ffn_norm, final_norm [d_model];
+ *   wq [Dq, d_model]; wk, wv [Dkv, d_model]; wo [d_model, Dq];
+ *   w1 (gate), w3 (up) [d_ff, d_model]; w2 (down) [d_model, d_ff];
+ *   lm_head [vocab, d_model] (may be the same pointer as embed: tied weights). */
+typedef struct {
+    const void* embed;
+    const void* const* attn_norm;
+    const void* const* wq;
+    const void* const* wk;
+    const void* const* wv;
+    const void* const* wo;
+    const void* const* ffn_norm;
+    const void* const* w1;
+    const void* const* w3;
+    const void* const* w2;
+    const void* final_norm;
+    const void* lm_head;
+} tfm_weights;
+
+/* ABI version of this header; bumps on any incompatible change. */
+int32_t tfm_abi_version(void);
+
+/* Host only, touches no GPU: checks a config against the constraints above. */
+tfm_status tfm_validate_config(const tfm_config* cfg);
+
+/* Host only: bytes of device workspace tfm_create allocates for cfg
+ * (activations for max_batch x max_seq tokens, the RoPE table and the
+ * forward_host staging buffers), 0 if the config is invalid. */
+size_t tfm_workspace_bytes(const tfm_config* cfg);
+
+/* Host only: bytes of packed weights tfm_load_weights keeps on the device. */
+size_t tfm_weight_bytes(const tfm_config* cfg);
+
+/* Creates a model handle on the current device: validates cfg, allocates the
+ * workspace and the packed-weight storage, builds the RoPE cos/sin table in
+ * float64 on the host (angle = position * theta^(-2i/d_head), "LLM 2",
+ * section RoPE) and uploads it as fp32.  Blocking.  *handle is set only on
+ * TFM_OK; release it with tfm_destroy. */
+tfm_status tfm_create(const tfm_config* cfg, void** handle);
+
+/* Copies the weights into the handle's own storage, packing [Wq; Wk; Wv] into
+ * one (Dq + 2 Dkv, d_model) matrix.  weights_on_host = 1: the pointers are
+ * host memory; 0: device memory.  Blocking; the caller may free its copies
+ * afterwards. */
+tfm_status tfm_load_weights(void* handle, const tfm_weights* w, int32_t weights_on_host);
+
+/* Forward pass of the CS336 walkthrough's TransformerLM.forward (section 5.7):
+ * tokens [B, S] int32 (device) -> logits [B*S, ld_logits] fp32 (device), row
+ * b*S + s holding the vocab scores of token s of sequence b in columns
+ * [0, vocab); columns [vocab, ld_logits) are not written.  Positions are
+ * 0..S-1 in every sequence.  Requires 1 <= B <= max_batch, 1 <= S <= max_seq,
+ * ld_logits >= vocab, ld_logits % 4 == 0, logits 16-byte aligned.  Launches
+ * 2 + 7 n_layer kernels on `stream`; capturable in a CUDA graph.  Calls on the
+ * same handle must not overlap (they share the workspace). */
+tfm_status tfm_forward(void* handle, const int32_t* tokens, int32_t B, int32_t S,
+                       float* logits, int64_t ld_logits, void* stream);
+
+/* The same forward with HOST buffers: copies tokens host->device, runs the
+ * forward, copies logits device->host, all enqueued on `stream` (the caller
+ * synchronises).  tokens_host [B, S]; logits_host [B*S, ld_logits]. */
+tfm_status tfm_forward_host(void* handle, const int32_t* tokens_host, int32_t B, int32_t S,
+                            float* logits_host, int64_t ld_logits, void* stream);
+
+/* Synchronises the device, then returns and clears the sticky device error word
+ * (TFM_OK, TFM_EBADTOKEN or TFM_ETIMEOUT), or TFM_ECUDA if the context faulted.
+ * handle may be NULL (component calls share the same word). */
+tfm_status tfm_device_status(void* handle);
+
+/* Thread-local text of the last error raised on this thread ("" if none). */
+const char* tfm_last_error(void);
+
+/* Frees everything the handle owns.  NULL is a no-op. */
+void tfm_destroy(void* handle);
+
+/* ---------------------------------------------------------------- components
+ * Single operations on caller buffers (device pointers), for testing each step
+ * against the oracle and for callers that assemble their own model. */
+
+/* Embedding lookup (CS336 walkthrough, section 5.2): h[m, :] = E[tokens[m], :]
+ * as fp32.  tokens [M] int32; E [V, D] bf16 or fp32 (mode); h [M, D] fp32.
+ * An id outside [0, V) writes a zero row and sets TFM_EBADTOKEN. */
+tfm_status tfm_embedding(const int32_t* tokens, const void* E, float* h, int64_t M,
+                         int32_t V, int32_t D, int32_t mode, void* stream);
+
+/* RMSNorm (CS336 walkthrough, section 5.6): y = x / sqrt(mean(x^2) + eps) * g
+ * per row, computed in fp32 and rounded once at the end.  x [M, D] fp32,
+ * g [D] fp32, y [M, D] bf16 (out_mode TFM_BF16) or fp32 (TFM_FP32).
+ * D % 8 == 0 and 16-byte aligned pointers are required. */
+tfm_status tfm_rmsnorm(const float* x, const float* g, void* y, int64_t M, int32_t D,
+                       float eps, int32_t out_mode, void* stream);
+
+/* RoPE in place (CS336 walkthrough, section 5.5; "LLM 2", section RoPE):
+ * x [B, H, S, dh] (bf16 or fp32), each adjacent pair (x[2i], x[2i+1]) of token
+ * s turned by pos * theta^(-2i/dh), pos = positions[b*S + s] (int32 [B, S],
+ * device) or s when positions is NULL.  dh even, dh <= 256. */
+tfm_status tfm_rope(void* x, const int32_t* positions, int32_t B, int32_t H, int32_t S,
+                    int32_t dh, float theta, int32_t mode, void* stream);
+
+/* Causal scaled dot-product attention (CS336 walkthrough, section 5.4):
+ * o = softmax(q k^T * scale + M) v with M = -inf above the diagonal, per
+ * sequence and head; query head h reads kv head h / (H / Hkv) ("LLM 2",
+ * section GQA / MQA).  q [B, H, S, dh]; k, v [B, Hkv, S, dh]; o [B, S, H*dh]
+ * (heads merged back, the layout the output projection reads).  scale <= 0
+ * means 1/sqrt(dh).  bf16 mode: dh in {32, 64, 128}; fp32 mode: dh <= 128. */
+tfm_status tfm_causal_attention(const void* q, const void* k, const void* v, void* o,
+                                int32_t B, int32_t H, int32_t Hkv, int32_t S, int32_t dh,
+                                float scale, int32_t mode, void* stream);
+
+/* Bias-free Linear (CS336 walkthrough, section 5.3): y = x W^T.
+ * x [M, K], W [N, K] (bf16 or fp32 by mode); y [M, ldy] fp32 when
+ * out_fp32 != 0 (accumulate != 0 adds into y instead of overwriting), else
+ * bf16 [M, ldy] (bf16 mode only; accumulate must be 0).  K % 8 == 0 in bf16
+ * mode; ldy >= N, ldy % 8 == 0. */
+tfm_status tfm_linear(const void* x, const void* W, void* y, int64_t M, int32_t N, int32_t K,
+                      int64_t ldy, int32_t out_fp32, int32_t accumulate, int32_t mode,
+                      void* stream);
+
+/* SwiGLU feed-forward (CS336 walkthrough, section 5.3):
+ * y (+)= W2 (silu(W1 x) * W3 x), silu(z) = z / (1 + exp(-z)).
+ * x [M, D], w1 and w3 [F, D], w2 [D, F] (bf16 or fp32 by mode); y [M, D] fp32,
+ * overwritten (accumulate 0) or added to (accumulate 1, the residual add).
+ * The hidden activation [M, F] lives in the caller's `workspace` of at least
+ * tfm_swiglu_workspace_bytes(M, F, mode) bytes (device, 256-byte aligned). */
+tfm_status tfm_swiglu(const void* x, const void* w1, const void* w3, const void* w2, float* y,
+                      int64_t M, int32_t D, int32_t F, int32_t accumulate,
+                      void* workspace, size_t workspace_bytes, int32_t mode, void* stream);
+size_t tfm_swiglu_workspace_bytes(int64_t M, int32_t F, int32_t mode);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TFM_H */

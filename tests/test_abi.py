@@ -1,0 +1,84 @@
+"""CPU checks of the C ABI: the library builds, loads without a GPU, exports
+every function include/tfm.h declares, and validates configs on the host."""
+import ctypes
+
+import pytest
+
+import workloads
+from decoder_only_transformer_gb300 import tfm
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return tfm.load()
+
+
+def test_exports_every_declared_function(lib):
+    names = tfm.header_functions()
+    assert len(names) >= 17
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    # the binding covers exactly the declared functions
+    assert sorted(tfm._SIGS) == names
+
+
+def test_abi_version(lib):
+    assert lib.tfm_abi_version() == 1
+
+
+@pytest.mark.parametrize("name", list(workloads.CONFIGS))
+def test_benchmark_configs_are_valid(lib, name):
+    cfg = workloads.get_config(name)
+    c = tfm.make_config(cfg)
+    assert tfm.validate_config(c) == tfm.TFM_OK, lib.tfm_last_error()
+    assert tfm.workspace_bytes(c) > cfg.tokens * cfg.d_model * 4
+    assert tfm.weight_bytes(c) >= 2 * cfg.vocab * cfg.d_model * (2 if cfg.mode == "bf16" else 4)
+
+
+def _cfg(**kw):
+    base = dict(vocab=100, d_model=256, n_head=4, n_kv_head=4, n_layer=2, d_ff=512,
+                max_seq=128, max_batch=2, rope_theta=10000.0, norm_eps=1e-5, mode=tfm.TFM_BF16)
+    base.update(kw)
+    return tfm.Config(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(), tfm.TFM_OK),
+    (dict(d_model=250), tfm.TFM_EINVAL),             # d_model % n_head
+    (dict(n_kv_head=3), tfm.TFM_EINVAL),             # n_head % n_kv_head
+    (dict(n_head=8, d_model=8 * 6, mode=tfm.TFM_FP32), tfm.TFM_EUNSUPPORTED),  # dh 6
+    (dict(d_model=4 * 48), tfm.TFM_EUNSUPPORTED),    # bf16 dh 48
+    (dict(norm_eps=0.0), tfm.TFM_EINVAL),
+    (dict(rope_theta=1.0), tfm.TFM_EINVAL),
+    (dict(vocab=0), tfm.TFM_EINVAL),
+    (dict(max_seq=0), tfm.TFM_EINVAL),
+    (dict(mode=7), tfm.TFM_EINVAL),
+    (dict(n_layer=0), tfm.TFM_OK),
+    (dict(d_ff=500), tfm.TFM_EUNSUPPORTED),          # bf16 d_ff % 8
+    (dict(n_head=8, n_kv_head=2), tfm.TFM_OK),       # GQA, dh 32
+])
+def test_config_validation(lib, kw, status):
+    c = _cfg(**kw)
+    assert tfm.validate_config(c) == status, lib.tfm_last_error()
+    if status != tfm.TFM_OK:
+        assert lib.tfm_last_error()
+        assert tfm.workspace_bytes(c) == 0
+
+
+def test_null_arguments_are_rejected_on_the_host(lib):
+    assert lib.tfm_validate_config(None) == tfm.TFM_EINVAL
+    assert lib.tfm_create(None, None) == tfm.TFM_EINVAL
+    assert lib.tfm_forward(None, None, 1, 1, None, 8, None) == tfm.TFM_EINVAL
+    assert lib.tfm_rmsnorm(None, None, None, 4, 64, 1e-5, 1, None) == tfm.TFM_EINVAL
+    assert lib.tfm_linear(None, None, None, 4, 4, 4, 8, 1, 0, 1, None) == tfm.TFM_EINVAL
+    x = ctypes.c_void_p(256)
+    assert lib.tfm_rmsnorm(x, x, x, 4, 60, 1e-5, 1, None) == tfm.TFM_EINVAL      # D % 8
+    assert lib.tfm_rmsnorm(ctypes.c_void_p(260), x, x, 4, 64, 1e-5, 1, None) == tfm.TFM_EINVAL  # align
+    assert lib.tfm_swiglu_workspace_bytes(10, 16, tfm.TFM_BF16) == 320
+    lib.tfm_destroy(None)
+
+
+def test_workspace_grows_with_batch(lib):
+    a = tfm.workspace_bytes(_cfg(max_batch=1))
+    b = tfm.workspace_bytes(_cfg(max_batch=4))
+    assert b > a > 0
