@@ -1,0 +1,396 @@
+"""Forward-pass throughput of the decoder-only Transformer LM on GB300.
+
+One step = one tfm_forward over the whole batch of the chosen workload (every
+kernel of the path: embedding, 2L+1 RMSNorms, L x [QKV+RoPE GEMM, causal
+attention, output projection + residual, gate/up + SwiGLU, down + residual],
+LM head).  Prints one JSON line.
+
+  python bench.py [--config small] [--steps K] [--warmup W] [--gpus N] [--impl ours|reference]
+
+Inputs are seeded synthetic weights and tokens of the workload's shapes,
+resident in HBM before timing.  Each timed step is bracketed by CUDA events on
+the launch stream; L2 is flushed (a 512 MiB write) between timed steps.
+"""
+from __future__ import annotations
+
+import os
+
+_THREADS = str(os.cpu_count() or 1)
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, _THREADS)
+
+import argparse
+import json
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+from decoder_only_transformer_gb300 import accounting  # noqa: E402
+
+METRIC = "forward tokens/sec on 1 GB300; attention & GEMM % of bf16 tensor peak"
+UNIT = "tokens/s"
+WORKLOAD_TEXT = {
+    "tiny": "tiny: vocab 23, d_model 64, 4 heads (d_head 16), 2 layers, d_ff 176, batch 4 x seq 64, fp32",
+    "small": "small: vocab 10000, d_model 512, 16 heads (d_head 32), 4 layers, d_ff 1344, batch 32 x seq 256, bf16",
+    "gpt2s": "GPT-2-small shape: vocab 50257, d_model 768, 12 heads (d_head 64), 12 layers, d_ff 2048, batch 8 x seq 1024, bf16, Zipf(1.1) tokens",
+    "long": "long-context: vocab 32000, d_model 1024, 16 heads (d_head 64), 4 layers, d_ff 2752, batch 1 x seq 8192, bf16",
+    "gqa": "GQA: vocab 32000, d_model 2048, 16 query / 4 KV heads (d_head 128), 8 layers, d_ff 5632, batch 4 x seq 2048, bf16",
+}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ---------------------------------------------------------------- per-kernel work
+def kernel_work(cfg, B, S):
+    """Algorithmic work of ONE launch of each kernel kind: ("tensor", flops) or
+    ("hbm", bytes)."""
+    M = B * S
+    D, F, V = cfg.d_model, cfg.d_ff, cfg.vocab
+    dh = cfg.d_head
+    Dq, Dkv = cfg.n_head * dh, cfg.n_kv_head * dh
+    es = 2 if cfg.mode == "bf16" else 4
+    return {
+        "embedding": ("hbm", M * 4 + M * D * es + M * D * 4),
+        "rmsnorm": ("hbm", accounting.rmsnorm_bytes(M, D, out_bytes=es)),
+        "qkv_rope_gemm": ("tensor", accounting.gemm_flops(M, Dq + 2 * Dkv, D)),
+        "attention": ("tensor", accounting.attention_flops(B, cfg.n_head, S, dh)),
+        "oproj_residual_gemm": ("tensor", accounting.gemm_flops(M, D, Dq)),
+        "gateup_swiglu_gemm": ("tensor", accounting.gemm_flops(M, 2 * F, D)),
+        "down_residual_gemm": ("tensor", accounting.gemm_flops(M, D, F)),
+        "lmhead_gemm": ("tensor", accounting.gemm_flops(M, V, D)),
+    }
+
+
+def kernel_table(cfg, B, S, prof, peaks):
+    work = kernel_work(cfg, B, S)
+    total_ms = sum(ms for ms, _ in prof.values()) or 1.0
+    out = {}
+    for name, (ms, n) in prof.items():
+        if n == 0:
+            continue
+        bound, units = work[name]
+        avg_s = ms / n / 1e3
+        if bound == "tensor":
+            ach = units / avg_s / 1e12
+            peak = peaks["bf16_tflops"]
+            unit = "TFLOP/s"
+        else:
+            ach = units / avg_s / 1e9
+            peak = peaks["hbm_gbs"]
+            unit = "GB/s"
+        out[name] = {"bound": bound, "launches": n, "avg_us": round(avg_s * 1e6, 2),
+                     "share": round(ms / total_ms, 4), "achieved": round(ach, 1), "unit": unit,
+                     "frac": round(ach / peak, 4)}
+    return out
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+        rows = []
+        try:
+            for line in open(self.file.name):
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9 and p[1].isdigit():
+                    rows.append(p)
+        finally:
+            os.unlink(self.file.name)
+        return rows
+
+    @staticmethod
+    def summary(rows):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [int(r[1]) for r in rows]
+        mx = int(rows[0][2])
+
+        def idle(r):
+            try:
+                return int(r[4], 16) & 0x1
+            except ValueError:
+                return 0
+        loaded = [r for r in rows if not idle(r)]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        under = [int(r[1]) for r in loaded]
+        return {"sm_mhz": statistics.median(under or sm), "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_rate(cfg, w, tokens, budget_s=12.0, max_tokens=None):
+    """Oracle tokens/s on a bounded sample: whole sequences (or, for one long
+    sequence, a prefix: causal logits of a prefix do not depend on later tokens)
+    until ~budget_s of CPU work."""
+    import oracle
+    B, S = tokens.shape
+    # size the sample from one small probe
+    probe = min(S, 64)
+    t0 = time.perf_counter()
+    oracle.forward(tokens[:1, :probe], w, cfg)
+    dt = time.perf_counter() - t0
+    est_seq = dt * (S / probe) ** 1.3
+    if est_seq > budget_s:
+        seq = max(probe, int(S * (budget_s / est_seq) ** (1 / 1.3)) // 64 * 64)
+        seq = min(seq, S)
+    else:
+        seq = S
+    done, t_total, rows = 0, 0.0, 0
+    for b in range(B):
+        t0 = time.perf_counter()
+        oracle.forward(tokens[b:b + 1, :seq], w, cfg)
+        t_total += time.perf_counter() - t0
+        done += seq
+        rows += 1
+        if t_total >= budget_s or (max_tokens and done >= max_tokens):
+            break
+    sample = f"{rows} sequence(s) x {seq} tokens of the full model (fp64 NumPy oracle)"
+    return done / t_total, sample, t_total
+
+
+# ---------------------------------------------------------------- main
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="small", choices=list(workloads.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    cfg = workloads.get_config(args.config)
+    w = workloads.make_weights(cfg)
+    tok = workloads.make_tokens(cfg)
+    # each step is one bounded sample of the workload
+    budget = max(1.0, 120.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_rate(cfg, w, tok, budget_s=budget, max_tokens=1)
+    rates, samples, secs = [], None, 0.0
+    for _ in range(args.steps):
+        r, samples, t = oracle_rate(cfg, w, tok, budget_s=budget, max_tokens=1)
+        rates.append(r)
+        secs += t
+    value = statistics.mean(rates)
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", _THREADS))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[cfg.name], "global_batch": cfg.batch,
+                       "seq_len": cfg.seq, "parallelism": "none (CPU)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": samples},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    from decoder_only_transformer_gb300 import tfm
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    cfg = workloads.get_config(args.config)
+    B, S = cfg.batch, cfg.seq
+    M = B * S
+    w = workloads.make_weights(cfg)
+    tok_np = workloads.make_tokens(cfg, seed=cfg.token_seed + rank)
+    bf = cfg.mode == "bf16"
+    mat = torch.bfloat16 if bf else torch.float32
+
+    def conv(key, a):
+        return torch.from_numpy(a).to(torch.float32 if key.endswith("norm") else mat).cuda()
+
+    tw = {k: conv(k, w[k]) for k in ("embed", "final_norm", "lm_head")}
+    tw["layers"] = [{k: conv(k, v) for k, v in layer.items()} for layer in w["layers"]]
+    model = tfm.Model(cfg)
+    model.load_weights(tw)
+    del tw
+    ld = (cfg.vocab + 3) // 4 * 4
+    tokens = torch.from_numpy(tok_np).cuda()
+    logits = torch.empty(M, ld, device="cuda")
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    sampler = ClockSampler(int(vis.split(",")[local]) if vis and vis.split(",")[local].isdigit()
+                           else local)
+    sampler.start()
+    for _ in range(max(args.warmup, 3)):
+        model.forward(tokens, logits)
+        flush.zero_()
+    torch.cuda.synchronize()
+    tfm.device_status()
+
+    # ---- timed region: exactly K steps, device time of each forward
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    model.profile(True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        model.forward(tokens, logits)
+        ends[i].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t_wall1 = time.time()
+    model.profile(False)
+    prof = model.profile_read()
+    tfm.device_status()
+    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * M * args.steps / (total_ms / 1e3)
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_tok = torch.from_numpy(tok_np).pin_memory()
+        h_logits = torch.empty(M, ld, dtype=torch.float32).pin_memory()
+        for _ in range(2):
+            model.forward_host(h_tok, h_logits)
+        torch.cuda.synchronize()
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+        if dist:
+            dist.barrier()
+        for i in range(args.steps):
+            es[2 * i].record(stream)
+            model.forward_host(h_tok, h_logits)
+            es[2 * i + 1].record(stream)
+            flush.zero_()
+        torch.cuda.synchronize()
+        tfm.device_status()
+        e2e_ms = sum(es[2 * i].elapsed_time(es[2 * i + 1]) for i in range(args.steps))
+        if dist:
+            t = torch.tensor([e2e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * M * args.steps / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": M * 4, "d2h_bytes_per_step": M * cfg.vocab * 4}
+    rows = sampler.stop()
+    clocks = ClockSampler.summary(rows)
+    clocks["window_s"] = round(t_wall1 - t_wall0, 3)
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    peaks = load_peaks()
+    kernels = kernel_table(cfg, B, S, prof, peaks)
+    dom_name = max(kernels, key=lambda k: kernels[k]["share"])
+    dom = kernels[dom_name]
+    roofline = {"kernel": dom_name, "bound": dom["bound"], "achieved": dom["achieved"],
+                "peak": peaks["bf16_tflops"] if dom["bound"] == "tensor" else peaks["hbm_gbs"],
+                "unit": dom["unit"], "frac": dom["frac"], "traffic": None,
+                "peak_source": f"{peaks['source']} ({'bf16 burst' if dom['bound'] == 'tensor' else 'HBM copy'})"}
+    gemm_attn = {k: v for k, v in kernels.items() if v["bound"] == "tensor"}
+    ms_t = sum(prof[k][0] for k in gemm_attn)
+    fl_t = sum(kernel_work(cfg, B, S)[k][1] * prof[k][1] for k in gemm_attn)
+    total_flops = accounting.forward_flops(cfg.vocab, cfg.d_model, cfg.n_layer, cfg.n_head,
+                                           cfg.d_ff, S, B, cfg.n_kv_head, causal=True)["total"]
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rate, sample, secs = oracle_rate(cfg, w, tok_np, budget_s=12.0)
+        cpu = {"value": rate, "unit": UNIT, "cores": int(os.environ["OPENBLAS_NUM_THREADS"]),
+               "kind": "oracle", "sample": sample + f", {secs:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf else "f32",
+        "data": "synthetic (seeded N(0,0.02) weights, token ids of the workload's distribution)",
+        "config": {"workload": WORKLOAD_TEXT[cfg.name], "global_batch": B * world, "seq_len": S,
+                   "parallelism": f"replicas x{world} (independent batches, no collective)",
+                   "l2": "flushed between timed steps (512 MiB write)"},
+        "roofline": roofline,
+        "tensor_path": {"achieved_tflops": round(fl_t / (ms_t / 1e3) / 1e12, 1) if ms_t else None,
+                        "frac": round(fl_t / (ms_t / 1e3) / 1e12 / peaks["bf16_tflops"], 4) if ms_t else None,
+                        "whole_forward_tflops": round(total_flops / (ms_per_step / 1e3) / 1e12, 1)},
+        "kernels": kernels,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": (3 + 7 * cfg.n_layer) * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -189,6 +189,24 @@ struct Model {
     const float* plan_logits = nullptr;
     int64_t plan_ld = -1;
     int plan_S = -1;
+    // per-kernel event timing (tfm_profile_*)
+    bool prof = false;
+    struct ProfRun {
+        size_t ev0;
+        std::vector<int> kinds;
+    };
+    std::vector<cudaEvent_t> ev_pool;
+    size_t ev_used = 0;
+    std::vector<ProfRun> runs;
+
+    cudaEvent_t next_event() {
+        if (ev_used == ev_pool.size()) {
+            cudaEvent_t e = nullptr;
+            if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+            ev_pool.push_back(e);
+        }
+        return ev_pool[ev_used++];
+    }
 
     float* h() { return reinterpret_cast<float*>(ws + lay.h); }
     void* xn() { return ws + lay.xn; }
@@ -275,6 +293,7 @@ tfm_status tfm_create(const tfm_config* cfg, void** handle) {
 void tfm_destroy(void* handle) {
     Model* m = static_cast<Model*>(handle);
     if (!m) return;
+    for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
     cudaFree(m->ws);
     cudaFree(m->wmem);
     delete m;
@@ -422,10 +441,19 @@ tfm_status build_plans(Model* m, int M, int S, float* logits, int64_t ld) {
     return TFM_OK;
 }
 
-#define TFM_LAUNCH(expr)                                            \
-    do {                                                            \
-        cudaError_t _e = (expr);                                    \
-        if (_e != cudaSuccess) return cuda_fail(_e, #expr);         \
+enum Kind { K_EMBED = 0, K_NORM, K_QKV, K_ATTN, K_OPROJ, K_GATEUP, K_DOWN, K_LMHEAD };
+
+// Launch `expr`; when profiling, record an event after it and remember its kind.
+#define TFM_LAUNCH(kind, expr)                                                  \
+    do {                                                                        \
+        cudaError_t _e = (expr);                                                \
+        if (_e != cudaSuccess) return cuda_fail(_e, #expr);                     \
+        if (run) {                                                              \
+            cudaEvent_t _ev = m->next_event();                                  \
+            if (!_ev) return fail(TFM_ECUDA, "cudaEventCreate failed");         \
+            cudaEventRecord(_ev, st);                                           \
+            run->kinds.push_back(kind);                                         \
+        }                                                                       \
     } while (0)
 
 tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* logits, int64_t ld,
@@ -437,49 +465,62 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
     const float scale = 1.0f / std::sqrt((float)dh);
     const bool bf = c.mode == TFM_BF16;
     if (!device_error_word()) return fail(TFM_ECUDA, "device error word unavailable");
-    TFM_LAUNCH(launch_embedding(tokens, m->embed, m->h(), M, c.vocab, c.d_model, bf, st));
     if (bf) {
         tfm_status ps = build_plans(m, M, S, logits, ld);
         if (ps != TFM_OK) return ps;
+    }
+    Model::ProfRun* run = nullptr;
+    if (m->prof) {
+        m->runs.push_back(Model::ProfRun{m->ev_used, {}});
+        run = &m->runs.back();
+        cudaEvent_t ev = m->next_event();
+        if (!ev) return fail(TFM_ECUDA, "cudaEventCreate failed");
+        cudaEventRecord(ev, st);
+    }
+    TFM_LAUNCH(K_EMBED, launch_embedding(tokens, m->embed, m->h(), M, c.vocab, c.d_model, bf, st));
+    if (bf) {
         for (int l = 0; l < c.n_layer; ++l) {
-            TFM_LAUNCH(launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 1, st));
-            TFM_LAUNCH(launch_gemm_tc(m->p_qkv[l], st));
-            TFM_LAUNCH(launch_attention_bf16(m->q(), m->k(), m->v(), m->o(), B, c.n_head,
-                                             c.n_kv_head, S, dh, scale, st));
-            TFM_LAUNCH(launch_gemm_tc(m->p_o[l], st));
-            TFM_LAUNCH(launch_rmsnorm(m->h(), m->ffn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 1, st));
-            TFM_LAUNCH(launch_gemm_tc(m->p_gu[l], st));
-            TFM_LAUNCH(launch_gemm_tc(m->p_down[l], st));
+            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 1, st));
+            TFM_LAUNCH(K_QKV, launch_gemm_tc(m->p_qkv[l], st));
+            TFM_LAUNCH(K_ATTN, launch_attention_bf16(m->q(), m->k(), m->v(), m->o(), B, c.n_head,
+                                                     c.n_kv_head, S, dh, scale, st));
+            TFM_LAUNCH(K_OPROJ, launch_gemm_tc(m->p_o[l], st));
+            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->ffn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 1, st));
+            TFM_LAUNCH(K_GATEUP, launch_gemm_tc(m->p_gu[l], st));
+            TFM_LAUNCH(K_DOWN, launch_gemm_tc(m->p_down[l], st));
         }
-        TFM_LAUNCH(launch_rmsnorm(m->h(), m->final_norm, m->xn(), M, c.d_model, c.norm_eps, 1, st));
-        TFM_LAUNCH(launch_gemm_tc(m->p_lm, st));
+        TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->final_norm, m->xn(), M, c.d_model, c.norm_eps, 1, st));
+        TFM_LAUNCH(K_LMHEAD, launch_gemm_tc(m->p_lm, st));
     } else {
         const float* xn = static_cast<const float*>(m->xn());
         for (int l = 0; l < c.n_layer; ++l) {
-            TFM_LAUNCH(launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 0, st));
-            TFM_LAUNCH(launch_gemm_simt(xn, static_cast<const float*>(m->wqkv[l]), nullptr, M,
-                                        (int)s.Nqkv, c.d_model, epi_qkv(m, M, S), st));
-            TFM_LAUNCH(launch_attention_simt(static_cast<const float*>(m->q()),
-                                             static_cast<const float*>(m->k()),
-                                             static_cast<const float*>(m->v()),
-                                             static_cast<float*>(m->o()), B, c.n_head, c.n_kv_head,
-                                             S, dh, scale, st));
-            TFM_LAUNCH(launch_gemm_simt(static_cast<const float*>(m->o()),
-                                        static_cast<const float*>(m->wo[l]), nullptr, M, c.d_model,
-                                        (int)s.Dq, epi_basic(EPI_ACCUM_F32, M, c.d_model, m->h(), s.D),
-                                        st));
-            TFM_LAUNCH(launch_rmsnorm(m->h(), m->ffn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 0, st));
+            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 0, st));
+            TFM_LAUNCH(K_QKV, launch_gemm_simt(xn, static_cast<const float*>(m->wqkv[l]), nullptr, M,
+                                               (int)s.Nqkv, c.d_model, epi_qkv(m, M, S), st));
+            TFM_LAUNCH(K_ATTN, launch_attention_simt(static_cast<const float*>(m->q()),
+                                                     static_cast<const float*>(m->k()),
+                                                     static_cast<const float*>(m->v()),
+                                                     static_cast<float*>(m->o()), B, c.n_head,
+                                                     c.n_kv_head, S, dh, scale, st));
+            TFM_LAUNCH(K_OPROJ, launch_gemm_simt(static_cast<const float*>(m->o()),
+                                                 static_cast<const float*>(m->wo[l]), nullptr, M,
+                                                 c.d_model, (int)s.Dq,
+                                                 epi_basic(EPI_ACCUM_F32, M, c.d_model, m->h(), s.D), st));
+            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->ffn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 0, st));
             EpiParams e = epi_basic(EPI_SWIGLU, M, c.d_ff, m->a(), s.F);
             e.out_bf16 = 0;
-            TFM_LAUNCH(launch_gemm_simt(xn, static_cast<const float*>(m->w1[l]),
-                                        static_cast<const float*>(m->w3[l]), M, c.d_ff, c.d_model, e, st));
-            TFM_LAUNCH(launch_gemm_simt(static_cast<const float*>(m->a()),
-                                        static_cast<const float*>(m->w2[l]), nullptr, M, c.d_model,
-                                        c.d_ff, epi_basic(EPI_ACCUM_F32, M, c.d_model, m->h(), s.D), st));
+            TFM_LAUNCH(K_GATEUP, launch_gemm_simt(xn, static_cast<const float*>(m->w1[l]),
+                                                  static_cast<const float*>(m->w3[l]), M, c.d_ff,
+                                                  c.d_model, e, st));
+            TFM_LAUNCH(K_DOWN, launch_gemm_simt(static_cast<const float*>(m->a()),
+                                                static_cast<const float*>(m->w2[l]), nullptr, M,
+                                                c.d_model, c.d_ff,
+                                                epi_basic(EPI_ACCUM_F32, M, c.d_model, m->h(), s.D), st));
         }
-        TFM_LAUNCH(launch_rmsnorm(m->h(), m->final_norm, m->xn(), M, c.d_model, c.norm_eps, 0, st));
-        TFM_LAUNCH(launch_gemm_simt(xn, static_cast<const float*>(m->lm_head), nullptr, M, c.vocab,
-                                    c.d_model, epi_basic(EPI_STORE_F32, M, c.vocab, logits, ld), st));
+        TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->final_norm, m->xn(), M, c.d_model, c.norm_eps, 0, st));
+        TFM_LAUNCH(K_LMHEAD, launch_gemm_simt(xn, static_cast<const float*>(m->lm_head), nullptr, M,
+                                              c.vocab, c.d_model,
+                                              epi_basic(EPI_STORE_F32, M, c.vocab, logits, ld), st));
     }
     return TFM_OK;
 }
@@ -524,6 +565,41 @@ tfm_status tfm_forward_host(void* handle, const int32_t* tokens_host, int32_t B,
                           (size_t)m->cfg.vocab * 4, M, cudaMemcpyDeviceToHost, cs);
     if (e != cudaSuccess) return tfm::cuda_fail(e, "logits device->host");
     return TFM_OK;
+}
+
+tfm_status tfm_profile_enable(void* handle, int32_t enable) {
+    Model* m = static_cast<Model*>(handle);
+    if (!m) return fail(TFM_EINVAL, "NULL handle");
+    m->prof = enable != 0;
+    return TFM_OK;
+}
+
+tfm_status tfm_profile_read(void* handle, double* ms, int64_t* launches) {
+    Model* m = static_cast<Model*>(handle);
+    if (!m || !ms || !launches) return fail(TFM_EINVAL, "NULL argument");
+    for (const auto& r : m->runs) {
+        const size_t n = r.kinds.size();
+        cudaError_t e = cudaEventSynchronize(m->ev_pool[r.ev0 + n]);
+        if (e != cudaSuccess) return tfm::cuda_fail(e, "profile event");
+        for (size_t i = 0; i < n; ++i) {
+            float t = 0.f;
+            e = cudaEventElapsedTime(&t, m->ev_pool[r.ev0 + i], m->ev_pool[r.ev0 + i + 1]);
+            if (e != cudaSuccess) return tfm::cuda_fail(e, "profile elapsed time");
+            ms[r.kinds[i]] += t;
+            launches[r.kinds[i]] += 1;
+        }
+    }
+    m->runs.clear();
+    m->ev_used = 0;
+    return TFM_OK;
+}
+
+const char* tfm_profile_kind_name(int32_t kind) {
+    static const char* names[TFM_PROFILE_KINDS] = {"embedding", "rmsnorm", "qkv_rope_gemm",
+                                                   "attention", "oproj_residual_gemm",
+                                                   "gateup_swiglu_gemm", "down_residual_gemm",
+                                                   "lmhead_gemm"};
+    return (kind >= 0 && kind < TFM_PROFILE_KINDS) ? names[kind] : "";
 }
 
 tfm_status tfm_device_status(void* handle) {

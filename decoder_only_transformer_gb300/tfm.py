@@ -67,7 +67,11 @@ _SIGS = {
     "tfm_linear": ([_V, _V, _V, _I64, _I32, _I32, _I64, _I32, _I32, _I32, _V], _I32),
     "tfm_swiglu": ([_V, _V, _V, _V, _V, _I64, _I32, _I32, _I32, _V, _SZ, _I32, _V], _I32),
     "tfm_swiglu_workspace_bytes": ([_I64, _I32, _I32], _SZ),
+    "tfm_profile_enable": ([_V, _I32], _I32),
+    "tfm_profile_read": ([_V, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)], _I32),
+    "tfm_profile_kind_name": ([_I32], ctypes.c_char_p),
 }
+PROFILE_KINDS = 8
 
 
 def header_functions() -> list[str]:
@@ -200,6 +204,17 @@ class Model:
         B, S = tokens.shape
         _check(self.lib.tfm_forward_host(self.handle, _ptr(tokens), B, S, _ptr(logits),
                                          logits.stride(0), _stream(stream)))
+
+    def profile(self, enable: bool = True):
+        _check(self.lib.tfm_profile_enable(self.handle, 1 if enable else 0))
+
+    def profile_read(self) -> dict:
+        """{kind name: (total ms, launches)} of the profiled forwards since the last read."""
+        ms = (ctypes.c_double * PROFILE_KINDS)()
+        n = (ctypes.c_int64 * PROFILE_KINDS)()
+        _check(self.lib.tfm_profile_read(self.handle, ms, n))
+        return {self.lib.tfm_profile_kind_name(i).decode(): (ms[i], n[i])
+                for i in range(PROFILE_KINDS)}
 
 
 # ---------------------------------------------------------------- components
