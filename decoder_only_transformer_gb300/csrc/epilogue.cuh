@@ -110,66 +110,92 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float (
     }
 }
 
-// a: accumulator columns [col0, col0+W) of output row `row`; u: the matching
-// "up" columns for EPI_SWIGLU (ignored otherwise).  For EPI_QKV_ROPE the chunk
-// lies inside one head (W divides dh) and col0 is a multiple of W.
+// Where a QKV column chunk goes: region 0/1/2 = q/k/v, head index, offset in
+// the head, and whether it is rotated (q and k are, v is not).
+struct QkvSlot {
+    int region, head, d0, heads;
+};
+__device__ __forceinline__ QkvSlot qkv_slot(const EpiParams& p, int col0) {
+    const int dh = p.dh, Dq = p.n_head * dh, Dkv = p.n_kv_head * dh;
+    QkvSlot r;
+    int c = col0;
+    if (c >= Dq + Dkv) {
+        r.region = 2; c -= Dq + Dkv; r.heads = p.n_kv_head;
+    } else if (c >= Dq) {
+        r.region = 1; c -= Dq; r.heads = p.n_kv_head;
+    } else {
+        r.region = 0; r.heads = p.n_head;
+    }
+    r.head = c / dh;
+    r.d0 = c - r.head * dh;
+    return r;
+}
+
+// Output values of one chunk: a = accumulator columns [col0, col0+W) of output
+// row `row`; u = the matching "up" columns for EPI_SWIGLU (ignored otherwise).
+// For EPI_QKV_ROPE the chunk lies inside one head (W divides dh), col0 % W == 0.
 template <int W>
-__device__ __forceinline__ void apply_epilogue(const EpiParams& p, int row, int col0,
-                                               const float (&a)[W], const float (&u)[W]) {
+__device__ __forceinline__ void epi_compute(const EpiParams& p, int row, int col0,
+                                            const float (&a)[W], const float (&u)[W],
+                                            float (&o)[W]) {
+    if (p.kind == EPI_SWIGLU) {
+#pragma unroll
+        for (int i = 0; i < W; ++i) o[i] = silu(a[i]) * u[i];
+    } else if (p.kind == EPI_QKV_ROPE) {
+        const QkvSlot q = qkv_slot(p, col0);
+        if (q.region < 2 && row < p.M) {
+            const int dh = p.dh;
+            const int s = row % p.S;
+            float cs[W / 2], sn[W / 2];
+            const int64_t t = (int64_t)s * (dh / 2) + q.d0 / 2;
+            load_vec<W / 2>(p.rope_cos + t, cs);
+            load_vec<W / 2>(p.rope_sin + t, sn);
+#pragma unroll
+            for (int j = 0; j < W / 2; ++j) {
+                const float x0 = a[2 * j], x1 = a[2 * j + 1];
+                o[2 * j] = x0 * cs[j] - x1 * sn[j];
+                o[2 * j + 1] = x0 * sn[j] + x1 * cs[j];
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < W; ++j) o[j] = a[j];
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < W; ++i) o[i] = a[i];
+    }
+}
+
+// Per-thread global stores of one computed chunk.
+template <int W>
+__device__ __forceinline__ void epi_store_direct(const EpiParams& p, int row, int col0,
+                                                 const float (&o)[W]) {
     if (row >= p.M || col0 >= p.N) return;
     const int n_valid = p.N - col0;
     switch (p.kind) {
         case EPI_STORE_F32:
-            store_row_f32<W>(static_cast<float*>(p.out) + (int64_t)row * p.ldo + col0, a, n_valid);
+            store_row_f32<W>(static_cast<float*>(p.out) + (int64_t)row * p.ldo + col0, o, n_valid);
             break;
         case EPI_ACCUM_F32:
-            accum_row_f32<W>(static_cast<float*>(p.out) + (int64_t)row * p.ldo + col0, a, n_valid);
+            accum_row_f32<W>(static_cast<float*>(p.out) + (int64_t)row * p.ldo + col0, o, n_valid);
             break;
         case EPI_STORE_BF16:
-            store_row_bf16<W>(static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * p.ldo + col0, a,
+            store_row_bf16<W>(static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * p.ldo + col0, o,
                               n_valid);
             break;
-        case EPI_SWIGLU: {
-            float h[W];
-#pragma unroll
-            for (int i = 0; i < W; ++i) h[i] = silu(a[i]) * u[i];
+        case EPI_SWIGLU:
             if (p.out_bf16)
                 store_row_bf16<W>(static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * p.ldo + col0,
-                                  h, n_valid);
+                                  o, n_valid);
             else
-                store_row_f32<W>(static_cast<float*>(p.out) + (int64_t)row * p.ldo + col0, h,
+                store_row_f32<W>(static_cast<float*>(p.out) + (int64_t)row * p.ldo + col0, o,
                                  n_valid);
             break;
-        }
         case EPI_QKV_ROPE: {
-            const int dh = p.dh, Dq = p.n_head * dh, Dkv = p.n_kv_head * dh;
-            int c = col0, heads = p.n_head;
-            void* base = p.q;
-            bool rotate = true;
-            if (c >= Dq + Dkv) {
-                c -= Dq + Dkv; base = p.v; heads = p.n_kv_head; rotate = false;
-            } else if (c >= Dq) {
-                c -= Dq; base = p.k; heads = p.n_kv_head;
-            }
-            const int hd = c / dh, d0 = c - hd * dh;
+            const QkvSlot q = qkv_slot(p, col0);
+            void* base = q.region == 0 ? p.q : (q.region == 1 ? p.k : p.v);
             const int b = row / p.S, s = row - b * p.S;
-            const int64_t off = (((int64_t)b * heads + hd) * p.S + s) * dh + d0;
-            float o[W];
-            if (rotate) {
-                float cs[W / 2], sn[W / 2];
-                const int64_t t = (int64_t)s * (dh / 2) + d0 / 2;
-                load_vec<W / 2>(p.rope_cos + t, cs);
-                load_vec<W / 2>(p.rope_sin + t, sn);
-#pragma unroll
-                for (int j = 0; j < W / 2; ++j) {
-                    const float x0 = a[2 * j], x1 = a[2 * j + 1];
-                    o[2 * j] = x0 * cs[j] - x1 * sn[j];
-                    o[2 * j + 1] = x0 * sn[j] + x1 * cs[j];
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < W; ++j) o[j] = a[j];
-            }
+            const int64_t off = (((int64_t)b * q.heads + q.head) * p.S + s) * p.dh + q.d0;
             if (p.out_bf16)
                 store_row_bf16<W>(static_cast<__nv_bfloat16*>(base) + off, o, W);
             else
@@ -179,6 +205,15 @@ __device__ __forceinline__ void apply_epilogue(const EpiParams& p, int row, int 
         default:
             break;
     }
+}
+
+template <int W>
+__device__ __forceinline__ void apply_epilogue(const EpiParams& p, int row, int col0,
+                                               const float (&a)[W], const float (&u)[W]) {
+    if (row >= p.M || col0 >= p.N) return;
+    float o[W];
+    epi_compute<W>(p, row, col0, a, u, o);
+    epi_store_direct<W>(p, row, col0, o);
 }
 
 }  // namespace tfm

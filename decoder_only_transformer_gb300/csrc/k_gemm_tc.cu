@@ -14,7 +14,9 @@
 //               TMEM accumulators, tcgen05.commit frees ring slots and hands the
 //               finished accumulator to the epilogue
 //   warps 2..5  epilogue: tcgen05.ld 32 columns at a time (warp w reads TMEM lanes
-//               32*(w%4)..), apply the epilogue, release the accumulator
+//               32*(w%4)..), compute the fused output, stage the 32x32 block in
+//               swizzled shared memory (double-buffered per warp) and write it with
+//               a TMA tile store (or a TMA reduce-add into the fp32 residual stream)
 // Double-buffered accumulators let the epilogue of tile i overlap the MMAs of
 // tile i+1.  For SwiGLU (kDual) a B tile is [W1 rows n..n+BN/2; W3 rows
 // n..n+BN/2] so matching gate and up columns land in the same tile without
@@ -30,23 +32,56 @@ constexpr int kBK = 64;                  // one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;               // K per tcgen05.mma kind::f16
 constexpr int kTileABytes = kBM * kBK * 2;
 constexpr int kThreads = 192;
+constexpr int kStageOutBytes = 32 * 128; // one 32 x 32 output block (fp32 rows of 128 B)
 
 template <int BN, int STAGES>
 struct TcSmem {
     static constexpr int kTileBBytes = BN * kBK * 2;
     static constexpr int kStageBytes = kTileABytes + kTileBBytes;
-    static constexpr int kBarOffset = STAGES * kStageBytes;
+    static constexpr int kOutOffset = STAGES * kStageBytes;              // 4 warps x 2 buffers
+    static constexpr int kBarOffset = kOutOffset + 8 * kStageOutBytes;
     // full[S], empty[S], tfull[2], tempty[2], done
     static constexpr int kNumBars = 2 * STAGES + 5;
     static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
     static constexpr int kBytes = kMiscOffset + 16 + 1024;   // + alignment slack
 };
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// Thread `lane` writes row `lane` of a 32 x 32 block into the staging buffer in
+// the layout the output tensor map's swizzle expects: fp32 rows of 128 bytes
+// with the 128-byte swizzle (16-byte chunk j of row r at j ^ (r % 8)), or bf16
+// rows of 64 bytes with the 64-byte swizzle (chunk j at j ^ ((r / 2) % 4)).
+__device__ __forceinline__ void stage_row(uint32_t buf, int lane, const float (&o)[32], bool bf16) {
+    if (bf16) {
+        const uint32_t row = buf + lane * 64;
+        const int x = (lane >> 1) & 3;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            st_shared_v4(row + ((j ^ x) << 4), pack_bf16x2(o[8 * j], o[8 * j + 1]),
+                         pack_bf16x2(o[8 * j + 2], o[8 * j + 3]),
+                         pack_bf16x2(o[8 * j + 4], o[8 * j + 5]),
+                         pack_bf16x2(o[8 * j + 6], o[8 * j + 7]));
+    } else {
+        const uint32_t row = buf + lane * 128;
+        const int x = lane & 7;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            st_shared_v4(row + ((j ^ x) << 4), __float_as_uint(o[4 * j]),
+                         __float_as_uint(o[4 * j + 1]), __float_as_uint(o[4 * j + 2]),
+                         __float_as_uint(o[4 * j + 3]));
+    }
+}
+
 template <int BN, int STAGES, bool kDual>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-              const __grid_constant__ CUtensorMap map_b2, int M, int N, int K, EpiParams epi,
-              int* err) {
+    k_gemm_tc(const __grid_constant__ TcMaps maps, int M, int N, int K, int out_mode,
+              int out_bf16, EpiParams epi, int* err) {
     using L = TcSmem<BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -55,6 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const uint32_t sA0 = base;
     const uint32_t sB0 = base + STAGES * kTileABytes;
+    const uint32_t sOut = base + L::kOutOffset;
     const uint32_t bars = base + L::kBarOffset;
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
@@ -83,9 +119,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(done_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&map_a);
-        tma_prefetch_desc(&map_b);
-        if (kDual) tma_prefetch_desc(&map_b2);
+        tma_prefetch_desc(&maps.a);
+        tma_prefetch_desc(&maps.b);
+        if (kDual) tma_prefetch_desc(&maps.b2);
     }
     if (warp == 1) tmem_alloc(smem_u32(tmem_holder), 2 * BN);
     tc_fence_before();
@@ -108,12 +144,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(full_bar(stage), L::kStageBytes);
                     const uint32_t sa = sA0 + stage * kTileABytes;
                     const uint32_t sb = sB0 + stage * L::kTileBBytes;
-                    tma_load_2d(sa, &map_a, kb * kBK, m0, full_bar(stage));
+                    tma_load_2d(sa, &maps.a, kb * kBK, m0, full_bar(stage));
                     if (kDual) {
-                        tma_load_2d(sb, &map_b, kb * kBK, n0, full_bar(stage));
-                        tma_load_2d(sb + (BN / 2) * kBK * 2, &map_b2, kb * kBK, n0, full_bar(stage));
+                        tma_load_2d(sb, &maps.b, kb * kBK, n0, full_bar(stage));
+                        tma_load_2d(sb + (BN / 2) * kBK * 2, &maps.b2, kb * kBK, n0, full_bar(stage));
                     } else {
-                        tma_load_2d(sb, &map_b, kb * kBK, n0, full_bar(stage));
+                        tma_load_2d(sb, &maps.b, kb * kBK, n0, full_bar(stage));
                     }
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -162,7 +198,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;                       // TMEM lane quarter of this warp
-        int acc = 0;
+        const uint32_t stg = sOut + (uint32_t)((warp - 2) * 2 * kStageOutBytes);
+        const bool tma = out_mode != OUT_DIRECT;
+        const bool obf = out_bf16 != 0;
+        const bool ragged_n = ((int64_t)N * (obf ? 2 : 4)) % 16 != 0;
+        int acc = 0, nst = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
             const int m0 = (t % num_m) * kBM;
@@ -175,31 +215,55 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             (void)mbar_try_wait(tfull_bar(acc), acc_phase);   // acquire in every lane
             tc_fence_after();
-            const int row = m0 + q * 32 + lane;
+            const int row0 = m0 + q * 32;
+            const int row = row0 + lane;
             const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            if (kDual) {
 #pragma unroll 1
-                for (int c = 0; c < BN / 2; c += 32) {
-                    float g[32], u[32];
-                    __syncwarp();
-                    tmem_ld32(trow + c, g);
-                    tmem_ld32(trow + BN / 2 + c, u);
-                    apply_epilogue<32>(epi, row, n0 + c, g, u);
+            for (int c = 0; c < n_per_tile; c += 32) {
+                const int col = n0 + c;
+                if (col >= N) break;                  // uniform across the warp
+                float a[32], u[32], o[32];
+                __syncwarp();
+                tmem_ld32(trow + c, a);
+                if (kDual) tmem_ld32(trow + BN / 2 + c, u);
+                epi_compute<32>(epi, row, col, a, kDual ? u : a, o);
+                // The tensor unit bounds the innermost dimension in 16-byte units: a
+                // last chunk whose row end is not 16-byte aligned is stored directly
+                // so nothing past column N is written.
+                if (!tma || (col + 32 > N && ragged_n)) {
+                    epi_store_direct<32>(epi, row, col, o);
+                    continue;
                 }
-            } else {
-#pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
-                    float v[32];
+                const uint32_t buf = stg + (uint32_t)((nst & 1) * kStageOutBytes);
+                if (nst >= 2) {
+                    if (lane == 0) bulk_wait_read<1>();   // this buffer's previous store has read it
                     __syncwarp();
-                    tmem_ld32(trow + c, v);
-                    apply_epilogue<32>(epi, row, n0 + c, v, v);
                 }
+                stage_row(buf, lane, o, obf);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && row0 < M) {
+                    if (out_mode == OUT_STORE) {
+                        tma_store_2d(&maps.out[0], buf, col, row0);
+                    } else if (out_mode == OUT_REDUCE_ADD) {
+                        tma_reduce_add_2d(&maps.out[0], buf, col, row0);
+                    } else {                          // OUT_QKV_3D: 32 rows inside one sequence
+                        const QkvSlot s = qkv_slot(epi, col);
+                        const int b = row0 / epi.S;
+                        tma_store_3d(&maps.out[s.region], buf, s.d0, row0 - b * epi.S,
+                                     b * s.heads + s.head);
+                    }
+                }
+                if (lane == 0) bulk_commit();
+                ++nst;
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
+        if (lane == 0) bulk_wait<0>();                // stores done before the CTA exits
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -230,33 +294,63 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [rows, cols] matrix with row stride ld
-// (elements), box = box_rows x 64 columns, 128-byte swizzle, zero fill out of range.
-bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
-              int box_rows) {
+// Tensor map over a row-major matrix (or a stack of them): dims innermost
+// first, byte strides of dims 1.., a box, a swizzle.  Zero fill out of range.
+bool encode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* ptr,
+            const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+            CUtensorMapSwizzle swz) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, dt, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 operand [rows, cols] (row stride ld), box box_rows x 64, 128-byte swizzle.
+bool make_operand_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
+                      int box_rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Output [rows, cols] with row stride ld, 32 x 32 boxes (fp32: 128-byte rows,
+// 128-byte swizzle; bf16: 64-byte rows, 64-byte swizzle).
+bool make_out_map(CUtensorMap* map, void* ptr, int64_t rows, int64_t cols, int64_t ld, bool bf16) {
+    const int es = bf16 ? 2 : 4;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * es)};
+    cuuint32_t box[2] = {32, 32};
+    return encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                  ptr, dims, strides, box,
+                  bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Head-major bf16 q/k/v [n_seq_heads, S, dh] as a 3-D map with 32 x 32 x 1 boxes.
+bool make_heads_map(CUtensorMap* map, void* ptr, int64_t n_seq_heads, int64_t S, int64_t dh) {
+    cuuint64_t dims[3] = {(cuuint64_t)dh, (cuuint64_t)S, (cuuint64_t)n_seq_heads};
+    cuuint64_t strides[2] = {(cuuint64_t)(dh * 2), (cuuint64_t)(S * dh * 2)};
+    cuuint32_t box[3] = {32, 32, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 // Tile width minimising (waves x tile width), the per-SM critical path when
-// every tile costs time proportional to its width; ties go to the wider tile.
+// every tile costs time proportional to its width.  A 128-wide tile moves 25%
+// more operand bytes from L2 per flop than a 256-wide one (85 vs 64 flop per
+// byte), so its cost carries a 1.25 factor; ties go to the wider tile.
 int choose_block_n(int M, int N, bool dual) {
     const int sms = sm_count();
     const int num_m = (M + kBM - 1) / kBM;
     int best = 256;
-    int64_t best_cost = -1;
+    double best_cost = -1.0;
     for (int bn : {256, 128}) {
         const int per = dual ? bn / 2 : bn;
         const int64_t tiles = (int64_t)num_m * ((N + per - 1) / per);
-        const int64_t cost = ((tiles + sms - 1) / sms) * bn;
+        const double cost = (double)((tiles + sms - 1) / sms) * bn * (bn == 128 ? 1.25 : 1.0);
         if (best_cost < 0 || cost < best_cost) { best = bn; best_cost = cost; }
     }
     return best;
@@ -265,6 +359,7 @@ int choose_block_n(int M, int N, bool dual) {
 template <int BN, int STAGES, bool kDual>
 cudaError_t launch_inst(const GemmPlan& p, cudaStream_t st) {
     using L = TcSmem<BN, STAGES>;
+    static_assert(L::kBytes <= 232448, "shared memory budget");
     static bool attr_set = false;   // per instantiation; set once per process
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, STAGES, kDual>,
@@ -276,7 +371,7 @@ cudaError_t launch_inst(const GemmPlan& p, cudaStream_t st) {
     const int64_t tiles = (int64_t)((p.M + kBM - 1) / kBM) * ((p.N + per - 1) / per);
     const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
     k_gemm_tc<BN, STAGES, kDual><<<grid, kThreads, L::kBytes, st>>>(
-        p.map_a, p.map_b, p.map_b2, p.M, p.N, p.K, p.epi, device_error_word());
+        p.maps, p.M, p.N, p.K, p.out_mode, p.out_bf16, p.epi, device_error_word());
     return cudaGetLastError();
 }
 
@@ -292,14 +387,43 @@ tfm_status plan_gemm_tc(GemmPlan* plan, const void* A, int64_t lda, const void* 
     plan->block_n = choose_block_n(M, N, dual);
     plan->epi = epi;
     const int box_b = dual ? plan->block_n / 2 : plan->block_n;
-    if (!make_map(&plan->map_a, A, M, K, lda, kBM)) return TFM_ECUDA;
-    if (!make_map(&plan->map_b, B, N, K, ldb, box_b)) return TFM_ECUDA;
+    if (!make_operand_map(&plan->maps.a, A, M, K, lda, kBM)) return TFM_ECUDA;
+    if (!make_operand_map(&plan->maps.b, B, N, K, ldb, box_b)) return TFM_ECUDA;
     if (dual) {
-        if (!make_map(&plan->map_b2, B2, N, K, ldb, box_b)) return TFM_ECUDA;
+        if (!make_operand_map(&plan->maps.b2, B2, N, K, ldb, box_b)) return TFM_ECUDA;
     } else {
-        plan->map_b2 = plan->map_b;
+        plan->maps.b2 = plan->maps.b;
     }
-    return TFM_OK;
+    // Output path: TMA tile stores wherever the destination allows it.
+    plan->out_mode = OUT_DIRECT;
+    plan->out_bf16 = 0;
+    bool ok = true;
+    switch (epi.kind) {
+        case EPI_STORE_F32:
+        case EPI_ACCUM_F32:
+            plan->out_mode = epi.kind == EPI_STORE_F32 ? OUT_STORE : OUT_REDUCE_ADD;
+            ok = make_out_map(&plan->maps.out[0], epi.out, M, epi.N, epi.ldo, false);
+            break;
+        case EPI_STORE_BF16:
+        case EPI_SWIGLU:
+            plan->out_mode = OUT_STORE;
+            plan->out_bf16 = epi.kind == EPI_STORE_BF16 ? 1 : epi.out_bf16;
+            ok = make_out_map(&plan->maps.out[0], epi.out, M, epi.N, epi.ldo, plan->out_bf16 != 0);
+            break;
+        case EPI_QKV_ROPE:
+            if (epi.out_bf16 && epi.S % 32 == 0 && epi.dh % 32 == 0) {
+                const int64_t B = M / epi.S;
+                plan->out_mode = OUT_QKV_3D;
+                plan->out_bf16 = 1;
+                ok = make_heads_map(&plan->maps.out[0], epi.q, B * epi.n_head, epi.S, epi.dh) &&
+                     make_heads_map(&plan->maps.out[1], epi.k, B * epi.n_kv_head, epi.S, epi.dh) &&
+                     make_heads_map(&plan->maps.out[2], epi.v, B * epi.n_kv_head, epi.S, epi.dh);
+            }
+            break;
+        default:
+            break;
+    }
+    return ok ? TFM_OK : TFM_ECUDA;
 }
 
 cudaError_t launch_gemm_tc(const GemmPlan& p, cudaStream_t st) {
