@@ -186,6 +186,8 @@ struct Model {
     int64_t plan_m = -1;
     std::vector<GemmPlan> p_qkv, p_o, p_gu, p_down;
     GemmPlan p_lm;
+    AttnPlan p_attn;               // tcgen05 attention (d_head 64 / 128)
+    bool attn_tc = false;
     const float* plan_logits = nullptr;
     int64_t plan_ld = -1;
     int plan_S = -1;
@@ -436,6 +438,14 @@ tfm_status build_plans(Model* m, int M, int S, float* logits, int64_t ld) {
     if (st != TFM_OK) return fail(st, "could not encode TMA tensor maps (driver entry point missing?)");
     m->plan_m = M;
     m->plan_S = S;
+    const int dh = c.d_model / c.n_head;
+    m->attn_tc = attention_tc_supported(dh);
+    if (m->attn_tc &&
+        plan_attention_tc(&m->p_attn, m->q(), m->k(), m->v(), m->o(), M / S, c.n_head,
+                          c.n_kv_head, S, dh, 1.0f / std::sqrt((float)dh)) != TFM_OK) {
+        m->plan_m = -1;
+        return fail(TFM_ECUDA, "could not encode attention tensor maps");
+    }
     m->plan_logits = logits;
     m->plan_ld = ld;
     return TFM_OK;
@@ -482,8 +492,11 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
         for (int l = 0; l < c.n_layer; ++l) {
             TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 1, st));
             TFM_LAUNCH(K_QKV, launch_gemm_tc(m->p_qkv[l], st));
-            TFM_LAUNCH(K_ATTN, launch_attention_bf16(m->q(), m->k(), m->v(), m->o(), B, c.n_head,
-                                                     c.n_kv_head, S, dh, scale, st));
+            if (m->attn_tc)
+                TFM_LAUNCH(K_ATTN, launch_attention_tc(m->p_attn, st));
+            else
+                TFM_LAUNCH(K_ATTN, launch_attention_bf16(m->q(), m->k(), m->v(), m->o(), B,
+                                                         c.n_head, c.n_kv_head, S, dh, scale, st));
             TFM_LAUNCH(K_OPROJ, launch_gemm_tc(m->p_o[l], st));
             TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->ffn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 1, st));
             TFM_LAUNCH(K_GATEUP, launch_gemm_tc(m->p_gu[l], st));
@@ -669,7 +682,14 @@ tfm_status tfm_causal_attention(const void* q, const void* k, const void* v, voi
     cudaError_t e;
     if (mode == TFM_BF16) {
         if (dh != 32 && dh != 64 && dh != 128) return fail(TFM_EUNSUPPORTED, "bf16 attention: dh in {32,64,128}");
-        e = tfm::launch_attention_bf16(q, k, v, o, B, H, Hkv, S, dh, scale, cs);
+        if (tfm::attention_tc_supported(dh)) {
+            tfm::AttnPlan plan;
+            tfm_status ps = tfm::plan_attention_tc(&plan, q, k, v, o, B, H, Hkv, S, dh, scale);
+            if (ps != TFM_OK) return fail(ps, "could not encode attention tensor maps");
+            e = tfm::launch_attention_tc(plan, cs);
+        } else {
+            e = tfm::launch_attention_bf16(q, k, v, o, B, H, Hkv, S, dh, scale, cs);
+        }
     } else if (mode == TFM_FP32) {
         if (dh < 1 || dh > 128) return fail(TFM_EUNSUPPORTED, "fp32 attention: dh <= 128");
         e = tfm::launch_attention_simt(static_cast<const float*>(q), static_cast<const float*>(k),

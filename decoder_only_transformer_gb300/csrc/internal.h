@@ -84,8 +84,20 @@ tfm_status plan_gemm_tc(GemmPlan* plan, const void* A, int64_t lda, const void* 
                         const void* B2, int64_t ldb, int M, int N, int K, const EpiParams& epi);
 cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t st);
 
-// ---- bf16 flash attention (k_attention.cu)
+// ---- bf16 flash attention on mma.sync (k_attention.cu), any dh in {32, 64, 128}
 cudaError_t launch_attention_bf16(const void* q, const void* k, const void* v, void* o, int B,
                                   int H, int Hkv, int S, int dh, float scale, cudaStream_t st);
+
+// ---- bf16 flash attention on tcgen05 (k_attention_tc.cu), dh in {64, 128}
+struct AttnPlan {
+    CUtensorMap qmap, kmap, vmap;   // [B*heads, S, dh] views of q, k, v
+    int B, H, Hkv, S, dh;
+    float scale;
+    void* o;                        // [B, S, H*dh] bf16
+};
+bool attention_tc_supported(int dh);
+tfm_status plan_attention_tc(AttnPlan* p, const void* q, const void* k, const void* v, void* o,
+                             int B, int H, int Hkv, int S, int dh, float scale);
+cudaError_t launch_attention_tc(const AttnPlan& p, cudaStream_t st);
 
 }  // namespace tfm

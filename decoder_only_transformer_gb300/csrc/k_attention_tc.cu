@@ -1,0 +1,417 @@
+// k_attention_tc.cu - causal softmax attention on the sm_103a tensor cores
+// (tcgen05 + tensor memory), d_head 64 or 128.
+//
+// o = softmax(q k^T * scale + M) v per (sequence, head), M = -inf above the
+// diagonal (CS336 walkthrough, section 5.4), query head h reading kv head
+// h / (H / Hkv) ("LLM 2", section GQA / MQA).  The softmax is evaluated online
+// over key tiles: a running row max and row sum, the partial output rescaled
+// when the max grows (stable softmax: subtracting any common constant leaves
+// the result unchanged, so the rescale is exact up to rounding).
+//
+// One CTA = 128 query rows of one (sequence, head), keys in tiles of 128:
+//   warp 0      TMA: the Q tile once, then K and V tiles (3-D maps [seq*heads,
+//               S, dh], 128-byte swizzle, zero fill past S) into separate K and V
+//               rings, in the order the MMA thread consumes them
+//   warp 1      TMEM (512 columns: S double buffer 2 x 128, O dh) and one MMA
+//               thread: S_j = Q K_j^T (M=128, N=128, K=dh), then O += P_{j-1} V_{j-1}
+//               (M=128, N=dh, K=128; V read MN-major straight from its [key, dh]
+//               tile, so it is never transposed)
+//   warps 2..5  softmax, one thread per query row: S row from TMEM, causal /
+//               length mask, row max, p = 2^(s*scale*log2e - m) written as bf16
+//               into a swizzled P tile (the A operand of P.V), row sum; the partial
+//               O in TMEM is rescaled only when the row max grows by more than
+//               2^8, so P entries stay below 256 and most tiles skip the rescale
+// S_{j+1} runs on the tensor cores while the softmax warps work on S_j.
+// Tiles entirely above the diagonal are never loaded.  All waits are bounded.
+#include "common.cuh"
+#include "internal.h"
+
+namespace tfm {
+
+namespace {
+
+constexpr int kQ = 128;
+constexpr int kKV = 128;
+constexpr int kThreadsAtt = 192;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+template <int DH>
+struct AttTc {
+    static constexpr int kStages = DH == 64 ? 3 : 2;
+    static constexpr int kSub = DH / 64;              // 64-column (128-byte) sub-tiles
+    static constexpr int kQBytes = kQ * DH * 2;
+    static constexpr int kKBytes = kKV * DH * 2;
+    static constexpr int kVBytes = kKV * DH * 2;
+    static constexpr int kPBytes = kQ * kKV * 2;
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = kQOff + kQBytes;
+    static constexpr int kVOff = kKOff + kStages * kKBytes;
+    static constexpr int kPOff = kVOff + kStages * kVBytes;
+    static constexpr int kBarOff = kPOff + 2 * kPBytes;
+    // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2],
+    // o_done[2], done
+    static constexpr int kNumBars = 1 + 4 * kStages + 7;
+    static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+    static constexpr int kBytes = kMiscOff + 16 + 1024;
+};
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// Bounded wait by lane 0, result broadcast, acquire in every lane.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int lane, int* err,
+                                          volatile int* abort) {
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(bar, parity, err, abort) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) (void)mbar_try_wait(bar, parity);
+    return ok != 0;
+}
+
+template <int DH>
+__global__ void __launch_bounds__(kThreadsAtt, 1)
+    k_attention_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap, __nv_bfloat16* __restrict__ o, int H,
+                   int Hkv, int S, float scale_log2, int* err) {
+    using L = AttTc<DH>;
+    constexpr int ST = L::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t sQ = base + L::kQOff, sK = base + L::kKOff, sV = base + L::kVOff,
+                   sP = base + L::kPOff;
+    const uint32_t bars = base + L::kBarOff;
+    const uint32_t q_full = bars;
+    auto k_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto k_empty = [&](int s) { return bars + 8u * (1 + ST + s); };
+    auto v_full = [&](int s) { return bars + 8u * (1 + 2 * ST + s); };
+    auto v_empty = [&](int s) { return bars + 8u * (1 + 3 * ST + s); };
+    auto s_full = [&](int i) { return bars + 8u * (1 + 4 * ST + i); };
+    auto p_full = [&](int i) { return bars + 8u * (3 + 4 * ST + i); };
+    auto o_done = [&](int i) { return bars + 8u * (5 + 4 * ST + i); };
+    const uint32_t done_bar = bars + 8u * (7 + 4 * ST);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + L::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMiscOff + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int num_qt = (S + kQ - 1) / kQ;
+    const int qt = num_qt - 1 - (int)blockIdx.x;      // heavy (late) tiles first
+    const int bh = blockIdx.y, b = bh / H, h = bh - b * H;
+    const int g = h / (H / Hkv);
+    const int n = qt + 1;                              // key tiles 0..qt
+
+    if (warp == 0 && lane == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < ST; ++s) {
+            mbar_init(k_full(s), 1);
+            mbar_init(k_empty(s), 1);
+            mbar_init(v_full(s), 1);
+            mbar_init(v_empty(s), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(s_full(i), 1);
+            mbar_init(p_full(i), 4);
+            mbar_init(o_done(i), 1);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&qmap);
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_holder), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    const uint32_t t_o = tmem_base + 256;             // O: columns [256, 256 + DH)
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(q_full, L::kQBytes);
+#pragma unroll
+            for (int sub = 0; sub < L::kSub; ++sub)
+                tma_load_3d(sQ + sub * 16384, &qmap, 64 * sub, qt * kQ, b * H + h, q_full);
+            // Loads follow the order the MMA thread consumes them: K_0, then
+            // K_j, V_{j-1} for j >= 1, then V_{n-1}.
+            int k_issued = 0, v_issued = 0;
+            auto load_k = [&](int j) -> bool {
+                const int st = j % ST;
+                if (!mbar_wait(k_empty(st), ((uint32_t)(j / ST) & 1u) ^ 1u, err, abort_flag)) return false;
+                mbar_arrive_expect_tx(k_full(st), L::kKBytes);
+#pragma unroll
+                for (int sub = 0; sub < L::kSub; ++sub)
+                    tma_load_3d(sK + st * L::kKBytes + sub * 16384, &kmap, 64 * sub, j * kKV,
+                                b * Hkv + g, k_full(st));
+                ++k_issued;
+                return true;
+            };
+            auto load_v = [&](int j) -> bool {
+                const int st = j % ST;
+                if (!mbar_wait(v_empty(st), ((uint32_t)(j / ST) & 1u) ^ 1u, err, abort_flag)) return false;
+                mbar_arrive_expect_tx(v_full(st), L::kVBytes);
+#pragma unroll
+                for (int sub = 0; sub < L::kSub; ++sub)
+                    tma_load_3d(sV + st * L::kVBytes + sub * 16384, &vmap, 64 * sub, j * kKV,
+                                b * Hkv + g, v_full(st));
+                ++v_issued;
+                return true;
+            };
+            bool ok = load_k(0);
+            for (int j = 1; j < n && ok; ++j) ok = load_k(j) && load_v(j - 1);
+            if (ok) load_v(n - 1);
+            // Drain: the copies of every armed slot (and Q) must land before exit.
+            mbar_wait(q_full, 0, err, abort_flag);
+            for (int s = 0; s < ST && s < k_issued; ++s) {
+                const int last = k_issued - 1 - ((k_issued - 1 - s) % ST);
+                mbar_wait(k_full(s), (uint32_t)((last / ST) & 1), err, abort_flag);
+            }
+            for (int s = 0; s < ST && s < v_issued; ++s) {
+                const int last = v_issued - 1 - ((v_issued - 1 - s) % ST);
+                mbar_wait(v_full(s), (uint32_t)((last / ST) & 1), err, abort_flag);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = umma_idesc_bf16(kQ, kKV);
+            constexpr uint32_t idesc_o = umma_idesc_bf16(kQ, DH, true);
+            bool ok = mbar_wait(q_full, 0, err, abort_flag);
+            auto issue_pv = [&](int i) -> bool {
+                const int sbp = i & 1, stp = i % ST;
+                if (!mbar_wait(p_full(sbp), (uint32_t)(i >> 1) & 1u, err, abort_flag)) return false;
+                if (!mbar_wait(v_full(stp), (uint32_t)(i / ST) & 1u, err, abort_flag)) return false;
+                tc_fence_after();
+                const uint32_t pa = sP + sbp * L::kPBytes;
+                const uint32_t vb = sV + stp * L::kVBytes;
+#pragma unroll
+                for (int kk = 0; kk < kKV / 16; ++kk) {
+                    const uint64_t ad = umma_desc_sw128(pa + (kk >> 2) * 16384 + (kk & 3) * 32);
+                    const uint64_t bd = umma_desc_sw128_mn(vb + kk * 2048, 16384, 1024);
+                    umma_bf16(t_o, ad, bd, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(v_empty(stp));
+                umma_commit(o_done(sbp));
+                return true;
+            };
+            for (int j = 0; j < n && ok; ++j) {
+                const int sb = j & 1, st = j % ST;
+                if (j >= 2 && !mbar_wait(p_full(sb), (uint32_t)((j - 2) >> 1) & 1u, err, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (!mbar_wait(k_full(st), (uint32_t)(j / ST) & 1u, err, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(sb * kKV);
+                const uint32_t kb = sK + st * L::kKBytes;
+#pragma unroll
+                for (int kk = 0; kk < DH / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    umma_bf16(d, umma_desc_sw128(sQ + off), umma_desc_sw128(kb + off), idesc_s,
+                              kk > 0 ? 1u : 0u);
+                }
+                umma_commit(k_empty(st));
+                umma_commit(s_full(sb));
+                if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+            }
+            if (ok) issue_pv(n - 1);
+            umma_commit(done_bar);
+            mbar_wait(done_bar, 0, err, abort_flag);
+        }
+    } else {
+        // ---------------------------------------------------------- softmax
+        const int q4 = warp & 3;
+        const int r = q4 * 32 + lane;                 // query row in the tile
+        const int qi = qt * kQ + r;                   // query position
+        const uint32_t trow = tmem_base + ((uint32_t)(q4 * 32) << 16);
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n; ++j) {
+            const int sb = j & 1;
+            if (!warp_wait(s_full(sb), (uint32_t)(j >> 1) & 1u, lane, err, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            // All four 32-column loads in flight before the single wait.
+            uint32_t sr[kKV / 32][32];
+#pragma unroll
+            for (int c = 0; c < kKV / 32; ++c) tmem_ld32_issue(trow + sb * kKV + c * 32, sr[c]);
+            tmem_ld_wait();
+            float s[kKV];
+#pragma unroll
+            for (int c = 0; c < kKV / 32; ++c) {
+                reg_fence32(sr[c]);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[c][e]);
+            }
+            const int k0 = j * kKV;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kKV; ++c) {
+                float t = s[c] * scale_log2;
+                if (k0 + c > qi || k0 + c >= S) t = -INFINITY;
+                s[c] = t;
+                mx = fmaxf(mx, t);
+            }
+            float corr = 1.f;
+            if (mx > m + kRescaleThreshold) {         // also true on the first tile (m = -inf)
+                corr = fast_exp2(m - mx);
+                m = mx;
+            }
+            const bool need_rescale = __any_sync(0xffffffffu, corr != 1.f && j > 0);
+            // P[sb] is free once P_{j-2} V_{j-2} has completed.
+            if (j >= 2 && !warp_wait(o_done(sb), (uint32_t)((j - 2) >> 1) & 1u, lane, err, abort_flag)) {
+                ok = false;
+                break;
+            }
+            float sum = 0.f;
+            const uint32_t prow = sP + sb * L::kPBytes + r * 128;
+#pragma unroll
+            for (int c8 = 0; c8 < kKV / 8; ++c8) {
+                float p[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    p[e] = fast_exp2(s[c8 * 8 + e] - m);
+                    sum += p[e];
+                }
+                const uint32_t addr = prow + (c8 >> 3) * 16384 + (((c8 & 7) ^ (r & 7)) << 4);
+                st_shared_v4(addr, pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
+                             pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
+            }
+            fence_proxy_async_smem();
+            l = l * corr + sum;
+            if (need_rescale) {
+                // O must hold P_{j-1} V_{j-1} before it is rescaled.
+                if (!warp_wait(o_done((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, lane, err,
+                               abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < DH / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(t_o + ((uint32_t)(q4 * 32) << 16) + c * 32, v);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] *= corr;
+                    tmem_st32(t_o + ((uint32_t)(q4 * 32) << 16) + c * 32, v);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full(sb));
+        }
+        // Final: O / l, written with heads merged, o[b, s, h*DH + d].
+        if (ok && warp_wait(o_done((n - 1) & 1), (uint32_t)((n - 1) >> 1) & 1u, lane, err, abort_flag)) {
+            tc_fence_after();
+            const float inv = 1.0f / l;
+            __nv_bfloat16* orow = o + ((int64_t)b * S + qi) * ((int64_t)H * DH) + (int64_t)h * DH;
+#pragma unroll 1
+            for (int c = 0; c < DH / 32; ++c) {
+                float v[32];
+                tmem_ld32(t_o + ((uint32_t)(q4 * 32) << 16) + c * 32, v);
+                if (qi < S) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 w;
+                        w.x = pack_bf16x2(v[e] * inv, v[e + 1] * inv);
+                        w.y = pack_bf16x2(v[e + 2] * inv, v[e + 3] * inv);
+                        w.z = pack_bf16x2(v[e + 4] * inv, v[e + 5] * inv);
+                        w.w = pack_bf16x2(v[e + 6] * inv, v[e + 7] * inv);
+                        *reinterpret_cast<uint4*>(orow + c * 32 + e) = w;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, 512);
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn att_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        tried = true;
+    }
+    return fn;
+}
+
+// [n_seq_heads, S, dh] bf16, box 64 x 128 x 1, 128-byte swizzle, zero fill.
+bool heads_map(CUtensorMap* map, const void* ptr, int64_t n_seq_heads, int64_t S, int64_t dh) {
+    EncodeTiledFn fn = att_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)dh, (cuuint64_t)S, (cuuint64_t)n_seq_heads};
+    cuuint64_t strides[2] = {(cuuint64_t)(dh * 2), (cuuint64_t)(S * dh * 2)};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int DH>
+cudaError_t launch_tc(const AttnPlan& p, cudaStream_t st) {
+    using L = AttTc<DH>;
+    static_assert(L::kBytes <= 232448, "shared memory budget");
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_attention_tc<DH>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    dim3 grid((p.S + kQ - 1) / kQ, p.B * p.H);
+    k_attention_tc<DH><<<grid, kThreadsAtt, L::kBytes, st>>>(
+        p.qmap, p.kmap, p.vmap, static_cast<__nv_bfloat16*>(p.o), p.H, p.Hkv, p.S,
+        p.scale * 1.4426950408889634f, device_error_word());
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attention_tc_supported(int dh) { return dh == 64 || dh == 128; }
+
+tfm_status plan_attention_tc(AttnPlan* p, const void* q, const void* k, const void* v, void* o,
+                             int B, int H, int Hkv, int S, int dh, float scale) {
+    p->B = B;
+    p->H = H;
+    p->Hkv = Hkv;
+    p->S = S;
+    p->dh = dh;
+    p->scale = scale;
+    p->o = o;
+    if (!heads_map(&p->qmap, q, (int64_t)B * H, S, dh) ||
+        !heads_map(&p->kmap, k, (int64_t)B * Hkv, S, dh) ||
+        !heads_map(&p->vmap, v, (int64_t)B * Hkv, S, dh))
+        return TFM_ECUDA;
+    return TFM_OK;
+}
+
+cudaError_t launch_attention_tc(const AttnPlan& p, cudaStream_t st) {
+    if (p.B <= 0 || p.S <= 0) return cudaSuccess;
+    if (p.dh == 64) return launch_tc<64>(p, st);
+    if (p.dh == 128) return launch_tc<128>(p, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace tfm

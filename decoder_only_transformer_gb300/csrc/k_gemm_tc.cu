@@ -218,21 +218,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row0 = m0 + q * 32;
             const int row = row0 + lane;
             const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-#pragma unroll 1
-            for (int c = 0; c < n_per_tile; c += 32) {
-                const int col = n0 + c;
-                if (col >= N) break;                  // uniform across the warp
+            // Chunks of 32 columns in range; the warp-uniform count keeps every
+            // .sync.aligned TMEM load converged.
+            const int left = N - n0;
+            const int nck = (left >= n_per_tile ? n_per_tile : left + 31) / 32;
+
+            auto process = [&](const uint32_t (&ra)[32], const uint32_t (&ru)[32], int c) {
+                const int col = n0 + c * 32;
                 float a[32], u[32], o[32];
-                __syncwarp();
-                tmem_ld32(trow + c, a);
-                if (kDual) tmem_ld32(trow + BN / 2 + c, u);
-                epi_compute<32>(epi, row, col, a, kDual ? u : a, o);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    a[e] = __uint_as_float(ra[e]);
+                    u[e] = __uint_as_float(ru[e]);
+                }
+                epi_compute<32>(epi, row, col, a, u, o);
                 // The tensor unit bounds the innermost dimension in 16-byte units: a
                 // last chunk whose row end is not 16-byte aligned is stored directly
                 // so nothing past column N is written.
                 if (!tma || (col + 32 > N && ragged_n)) {
                     epi_store_direct<32>(epi, row, col, o);
-                    continue;
+                    return;
                 }
                 const uint32_t buf = stg + (uint32_t)((nst & 1) * kStageOutBytes);
                 if (nst >= 2) {
@@ -256,6 +261,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (lane == 0) bulk_commit();
                 ++nst;
+            };
+            // Two register buffers: the TMEM load of chunk c+1 is in flight while
+            // chunk c is processed.
+            uint32_t ra0[32], ru0[32], ra1[32], ru1[32];
+            auto issue = [&](uint32_t (&ra)[32], uint32_t (&ru)[32], int c) {
+                __syncwarp();
+                tmem_ld32_issue(trow + c * 32, ra);
+                if (kDual) tmem_ld32_issue(trow + BN / 2 + c * 32, ru);
+            };
+            auto land = [&](uint32_t (&ra)[32], uint32_t (&ru)[32]) {
+                tmem_ld_wait();
+                reg_fence32(ra);
+                if (kDual) reg_fence32(ru);
+            };
+            if (nck > 0) issue(ra0, ru0, 0);
+#pragma unroll 1
+            for (int c = 0; c < nck; c += 2) {
+                land(ra0, ru0);
+                if (c + 1 < nck) issue(ra1, ru1, c + 1);
+                process(ra0, kDual ? ru0 : ra0, c);
+                if (c + 1 >= nck) break;
+                land(ra1, ru1);
+                if (c + 2 < nck) issue(ra0, ru0, c + 2);
+                process(ra1, kDual ? ru1 : ra1, c + 1);
             }
             tc_fence_before();
             __syncwarp();
