@@ -250,14 +250,25 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
                 for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[c][e]);
             }
             const int k0 = j * kKV;
-            float mx = -INFINITY;
+            // Only the diagonal tile and a tile reaching past S need the mask
+            // (warp-uniform test).
+            if (j == qt || k0 + kKV > S) {
 #pragma unroll
-            for (int c = 0; c < kKV; ++c) {
-                float t = s[c] * scale_log2;
-                if (k0 + c > qi || k0 + c >= S) t = -INFINITY;
-                s[c] = t;
-                mx = fmaxf(mx, t);
+                for (int c = 0; c < kKV; ++c)
+                    if (k0 + c > qi || k0 + c >= S) s[c] = -INFINITY;
             }
+            // Row max over raw scores with 8 independent chains (the scale is
+            // positive, so it commutes with the max).
+            float mx8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx8[e] = s[e];
+#pragma unroll
+            for (int c = 8; c < kKV; c += 8)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], s[c + e]);
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+                             scale_log2;
             float corr = 1.f;
             if (mx > m + kRescaleThreshold) {         // also true on the first tile (m = -inf)
                 corr = fast_exp2(m - mx);
@@ -269,21 +280,24 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
                 ok = false;
                 break;
             }
-            float sum = 0.f;
+            float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            const float neg_m = -m;
             const uint32_t prow = sP + sb * L::kPBytes + r * 128;
 #pragma unroll
             for (int c8 = 0; c8 < kKV / 8; ++c8) {
                 float p[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    p[e] = fast_exp2(s[c8 * 8 + e] - m);
-                    sum += p[e];
+                    p[e] = fast_exp2(fmaf(s[c8 * 8 + e], scale_log2, neg_m));
+                    sum8[e] += p[e];
                 }
                 const uint32_t addr = prow + (c8 >> 3) * 16384 + (((c8 & 7) ^ (r & 7)) << 4);
                 st_shared_v4(addr, pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
                              pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
             }
             fence_proxy_async_smem();
+            const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                              ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
             l = l * corr + sum;
             if (need_rescale) {
                 // O must hold P_{j-1} V_{j-1} before it is rescaled.
