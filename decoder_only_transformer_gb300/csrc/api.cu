@@ -74,6 +74,8 @@ int sm_count() {
 
 const char* cuda_error_text(cudaError_t e) { return cudaGetErrorString(e); }
 
+void set_last_error(const char* msg) { t_last_error = msg ? msg : ""; }
+
 // ------------------------------------------------------------------ config
 namespace {
 

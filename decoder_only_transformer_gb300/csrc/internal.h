@@ -35,6 +35,8 @@ struct EpiParams {
 
 // Library-global device error word of the current device (see raise_error).
 int* device_error_word();
+// Sets the thread-local text tfm_last_error() returns.
+void set_last_error(const char* msg);
 int sm_count();
 const char* cuda_error_text(cudaError_t e);
 

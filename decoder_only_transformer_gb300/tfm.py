@@ -67,6 +67,8 @@ _SIGS = {
     "tfm_linear": ([_V, _V, _V, _I64, _I32, _I32, _I64, _I32, _I32, _I32, _V], _I32),
     "tfm_swiglu": ([_V, _V, _V, _V, _V, _I64, _I32, _I32, _I32, _V, _SZ, _I32, _V], _I32),
     "tfm_swiglu_workspace_bytes": ([_I64, _I32, _I32], _SZ),
+    "tfm_swiglu_noalloc": ([_V, _V, _V, _V, _V, _I64, _I32, _I32, _I32, _I32, _V], _I32),
+    "tfm_swiglu_noalloc_max_bytes": ([], _SZ),
     "tfm_profile_enable": ([_V, _I32], _I32),
     "tfm_profile_read": ([_V, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)], _I32),
     "tfm_profile_kind_name": ([_I32], ctypes.c_char_p),
@@ -253,6 +255,20 @@ def linear(x, W, y, accumulate=False, stream=None):
 
 def swiglu_workspace_bytes(M, F, mode):
     return load().tfm_swiglu_workspace_bytes(M, F, mode)
+
+
+def swiglu_noalloc(x, w1, w3, w2, y, accumulate=False, stream=None):
+    """tfm_swiglu without a workspace argument, for callers that cannot
+    allocate device memory: the hidden activation goes to a fixed device array
+    of swiglu_noalloc_max_bytes() bytes owned by the library."""
+    M, D = x.shape
+    F = w1.shape[0]
+    _check(load().tfm_swiglu_noalloc(_ptr(x), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(y), M, D, F,
+                                     1 if accumulate else 0, _mode_of(x), _stream(stream)))
+
+
+def swiglu_noalloc_max_bytes() -> int:
+    return load().tfm_swiglu_noalloc_max_bytes()
 
 
 def swiglu(x, w1, w3, w2, y, workspace, accumulate=False, stream=None):
