@@ -57,28 +57,17 @@ cudaError_t launch_attention_simt(const float* q, const float* k, const float* v
                                   cudaStream_t st);
 
 // ---- tensor-core GEMM (k_gemm_tc.cu), bf16 mode
-// How the tensor-core epilogue writes its tile.
-enum TmaOut {
-    OUT_DIRECT = 0,      // per-thread global stores (apply_epilogue)
-    OUT_STORE = 1,       // TMA tile store through shared memory (out[0])
-    OUT_REDUCE_ADD = 2,  // TMA tile reduce-add (fp32 residual, out[0])
-    OUT_QKV_3D = 3,      // TMA 3-D stores into q/k/v [B*heads, S, dh] (out[0..2])
-};
-// Tensor maps of one GEMM: A [M,K] and B [N,K] bf16 row-major (B2 = W3 for
-// SwiGLU), and up to three output maps.
+// Tensor maps of one GEMM: A [M,K] and B [N,K] bf16 row-major (B2 = W3 for SwiGLU).
 struct TcMaps {
     CUtensorMap a;
     CUtensorMap b;
     CUtensorMap b2;
-    CUtensorMap out[3];
 };
 struct GemmPlan {
     TcMaps maps;
     int M, N, K;          // N = GEMM columns covered by tiles (F for SwiGLU)
     int block_n;          // tile width (128 or 256); SwiGLU: gate+up halves of block_n/2
     int dual;             // SwiGLU: B tile = [W1 rows; W3 rows]
-    int out_mode;         // TmaOut
-    int out_bf16;         // element type written by the TMA path
     EpiParams epi;
 };
 // Builds the tensor maps; returns TFM_OK or an error status with a message.

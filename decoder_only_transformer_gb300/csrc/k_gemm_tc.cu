@@ -13,10 +13,14 @@
 //               tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16) into one of two
 //               TMEM accumulators, tcgen05.commit frees ring slots and hands the
 //               finished accumulator to the epilogue
-//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time (warp w reads TMEM lanes
-//               32*(w%4)..), compute the fused output, stage the 32x32 block in
-//               swizzled shared memory (double-buffered per warp) and write it with
-//               a TMA tile store (or a TMA reduce-add into the fp32 residual stream)
+//   warps 2..9  epilogue, two warps per TMEM lane quarter (warp w reads lanes
+//               32*(w%4).., the pair takes alternate 32-column chunks): tcgen05.ld,
+//               compute the fused output (one row per thread), transpose the 32x32
+//               block through swizzled shared memory and write it with coalesced
+//               16-byte stores (row segments of whole sectors), or with 16-byte fp32
+//               reductions at L2 for the residual add.  A warp can keep only a few
+//               stores in flight, so the store rate scales with the number of
+//               storing warps; measured, a 32x32 chunk costs ~700-1000 cycles per warp.
 // Double-buffered accumulators let the epilogue of tile i overlap the MMAs of
 // tile i+1.  For SwiGLU (kDual) a B tile is [W1 rows n..n+BN/2; W3 rows
 // n..n+BN/2] so matching gate and up columns land in the same tile without
@@ -31,15 +35,16 @@ constexpr int kBM = 128;                 // tile rows = UMMA M
 constexpr int kBK = 64;                  // one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;               // K per tcgen05.mma kind::f16
 constexpr int kTileABytes = kBM * kBK * 2;
-constexpr int kThreads = 192;
-constexpr int kStageOutBytes = 32 * 128; // one 32 x 32 output block (fp32 rows of 128 B)
+constexpr int kEpiWarps = 8;             // two per TMEM lane quarter
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kStageOutBytes = 32 * 128; // one 32 x 32 block (fp32 rows of 128 B) per warp
 
 template <int BN, int STAGES>
 struct TcSmem {
     static constexpr int kTileBBytes = BN * kBK * 2;
     static constexpr int kStageBytes = kTileABytes + kTileBBytes;
-    static constexpr int kOutOffset = STAGES * kStageBytes;              // 4 warps x 2 buffers
-    static constexpr int kBarOffset = kOutOffset + 8 * kStageOutBytes;
+    static constexpr int kOutOffset = STAGES * kStageBytes;              // epilogue staging
+    static constexpr int kBarOffset = kOutOffset + kEpiWarps * kStageOutBytes;
     // full[S], empty[S], tfull[2], tempty[2], done
     static constexpr int kNumBars = 2 * STAGES + 5;
     static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
@@ -53,10 +58,10 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
-// Thread `lane` writes row `lane` of a 32 x 32 block into the staging buffer in
-// the layout the output tensor map's swizzle expects: fp32 rows of 128 bytes
-// with the 128-byte swizzle (16-byte chunk j of row r at j ^ (r % 8)), or bf16
-// rows of 64 bytes with the 64-byte swizzle (chunk j at j ^ ((r / 2) % 4)).
+// Thread `lane` writes row `lane` of a 32 x 32 block into the staging buffer:
+// fp32 rows of 128 bytes (16-byte chunk j of row r at position j ^ (r % 8)) or
+// bf16 rows of 64 bytes (chunk j at j ^ ((r / 2) % 4)).  The XOR keeps both
+// this row-wise write and the segment-wise read below free of bank conflicts.
 __device__ __forceinline__ void stage_row(uint32_t buf, int lane, const float (&o)[32], bool bf16) {
     if (bf16) {
         const uint32_t row = buf + lane * 64;
@@ -78,10 +83,77 @@ __device__ __forceinline__ void stage_row(uint32_t buf, int lane, const float (&
     }
 }
 
+// Writes the staged 32 x 32 block (rows row0.., columns col..) to its
+// destination with each lane moving one 16-byte row segment per step, so a warp
+// store covers whole 32-byte sectors.  Rows >= M and columns >= N are skipped
+// exactly (element-wise at a ragged right edge).
+__device__ __forceinline__ void flush_block(const EpiParams& p, uint32_t buf, int lane, int row0,
+                                            int col) {
+    if (p.kind == EPI_STORE_F32 || p.kind == EPI_ACCUM_F32) {
+        const int seg = lane & 7;
+        const int ncol = col + seg * 4;
+#pragma unroll
+        for (int step = 0; step < 8; ++step) {
+            const int r = step * 4 + (lane >> 3);
+            const uint4 v = ld_shared_v4(buf + r * 128 + ((seg ^ (r & 7)) << 4));
+            const int row = row0 + r;
+            if (row >= p.M || ncol >= p.N) continue;
+            float* d = static_cast<float*>(p.out) + (int64_t)row * p.ldo + ncol;
+            if (ncol + 4 <= p.N) {
+                if (p.kind == EPI_STORE_F32)
+                    *reinterpret_cast<uint4*>(d) = v;
+                else
+                    red_add_v4_f32(d, v);
+            } else {
+                const float f[4] = {__uint_as_float(v.x), __uint_as_float(v.y),
+                                    __uint_as_float(v.z), __uint_as_float(v.w)};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (ncol + e < p.N) {
+                        if (p.kind == EPI_STORE_F32) d[e] = f[e];
+                        else atomicAdd(d + e, f[e]);
+                    }
+            }
+        }
+        return;
+    }
+    // bf16 destinations: 4 lanes per 64-byte row, 8 rows per step.
+    const int seg = lane & 3;
+    QkvSlot qs{};
+    __nv_bfloat16* qbase = nullptr;
+    if (p.kind == EPI_QKV_ROPE) {
+        qs = qkv_slot(p, col);
+        qbase = static_cast<__nv_bfloat16*>(qs.region == 0 ? p.q : (qs.region == 1 ? p.k : p.v));
+    }
+    const int ncol = col + seg * 8;
+#pragma unroll
+    for (int step = 0; step < 4; ++step) {
+        const int r = step * 8 + (lane >> 2);
+        const uint4 v = ld_shared_v4(buf + r * 64 + ((seg ^ ((r >> 1) & 3)) << 4));
+        const int row = row0 + r;
+        if (row >= p.M || ncol >= p.N) continue;
+        __nv_bfloat16* d;
+        if (p.kind == EPI_QKV_ROPE) {
+            const int b = row / p.S, s = row - b * p.S;
+            d = qbase + (((int64_t)b * qs.heads + qs.head) * p.S + s) * p.dh + qs.d0 + seg * 8;
+        } else {
+            d = static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * p.ldo + ncol;
+        }
+        if (ncol + 8 <= p.N) {
+            *reinterpret_cast<uint4*>(d) = v;
+        } else {
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (ncol + e < p.N)
+                    d[e] = __ushort_as_bfloat16((unsigned short)((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu));
+        }
+    }
+}
+
 template <int BN, int STAGES, bool kDual>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemm_tc(const __grid_constant__ TcMaps maps, int M, int N, int K, int out_mode,
-              int out_bf16, EpiParams epi, int* err) {
+    k_gemm_tc(const __grid_constant__ TcMaps maps, int M, int N, int K, EpiParams epi, int* err) {
     using L = TcSmem<BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -114,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 4);
+            mbar_init(tempty_bar(a), kEpiWarps);
         }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
@@ -198,11 +270,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;                       // TMEM lane quarter of this warp
-        const uint32_t stg = sOut + (uint32_t)((warp - 2) * 2 * kStageOutBytes);
-        const bool tma = out_mode != OUT_DIRECT;
-        const bool obf = out_bf16 != 0;
-        const bool ragged_n = ((int64_t)N * (obf ? 2 : 4)) % 16 != 0;
-        int acc = 0, nst = 0;
+        const int half = (warp - 2) >> 2;             // the two warps of a quarter split the chunks
+        const uint32_t stg = sOut + (uint32_t)((warp - 2) * kStageOutBytes);
+        const bool obf = !(epi.kind == EPI_STORE_F32 || epi.kind == EPI_ACCUM_F32);
+        int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
             const int m0 = (t % num_m) * kBM;
@@ -232,67 +303,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     u[e] = __uint_as_float(ru[e]);
                 }
                 epi_compute<32>(epi, row, col, a, u, o);
-                // The tensor unit bounds the innermost dimension in 16-byte units: a
-                // last chunk whose row end is not 16-byte aligned is stored directly
-                // so nothing past column N is written.
-                if (!tma || (col + 32 > N && ragged_n)) {
-                    epi_store_direct<32>(epi, row, col, o);
-                    return;
-                }
-                const uint32_t buf = stg + (uint32_t)((nst & 1) * kStageOutBytes);
-                if (nst >= 2) {
-                    if (lane == 0) bulk_wait_read<1>();   // this buffer's previous store has read it
-                    __syncwarp();
-                }
-                stage_row(buf, lane, o, obf);
-                fence_proxy_async_smem();
+                stage_row(stg, lane, o, obf);
                 __syncwarp();
-                if (lane == 0 && row0 < M) {
-                    if (out_mode == OUT_STORE) {
-                        tma_store_2d(&maps.out[0], buf, col, row0);
-                    } else if (out_mode == OUT_REDUCE_ADD) {
-                        tma_reduce_add_2d(&maps.out[0], buf, col, row0);
-                    } else {                          // OUT_QKV_3D: 32 rows inside one sequence
-                        const QkvSlot s = qkv_slot(epi, col);
-                        const int b = row0 / epi.S;
-                        tma_store_3d(&maps.out[s.region], buf, s.d0, row0 - b * epi.S,
-                                     b * s.heads + s.head);
-                    }
-                }
-                if (lane == 0) bulk_commit();
-                ++nst;
+                flush_block(epi, stg, lane, row0, col);
+                __syncwarp();                         // the buffer is reused by the next chunk
             };
-            // Two register buffers: the TMEM load of chunk c+1 is in flight while
-            // chunk c is processed.
-            uint32_t ra0[32], ru0[32], ra1[32], ru1[32];
-            auto issue = [&](uint32_t (&ra)[32], uint32_t (&ru)[32], int c) {
+            // This warp takes every other chunk; a TMEM load costs only a few tens
+            // of cycles, the global stores dominate, so more storing warps (not
+            // deeper load pipelining) is what raises the epilogue's throughput.
+#pragma unroll 1
+            for (int c = half; c < nck; c += 2) {
+                uint32_t ra[32], ru[32];
                 __syncwarp();
                 tmem_ld32_issue(trow + c * 32, ra);
                 if (kDual) tmem_ld32_issue(trow + BN / 2 + c * 32, ru);
-            };
-            auto land = [&](uint32_t (&ra)[32], uint32_t (&ru)[32]) {
                 tmem_ld_wait();
                 reg_fence32(ra);
                 if (kDual) reg_fence32(ru);
-            };
-            if (nck > 0) issue(ra0, ru0, 0);
-#pragma unroll 1
-            for (int c = 0; c < nck; c += 2) {
-                land(ra0, ru0);
-                if (c + 1 < nck) issue(ra1, ru1, c + 1);
-                process(ra0, kDual ? ru0 : ra0, c);
-                if (c + 1 >= nck) break;
-                land(ra1, ru1);
-                if (c + 2 < nck) issue(ra0, ru0, c + 2);
-                process(ra1, kDual ? ru1 : ra1, c + 1);
+                process(ra, kDual ? ru : ra, c);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
-        if (lane == 0) bulk_wait<0>();                // stores done before the CTA exits
-        __syncwarp();
     }
 
     tc_fence_before();
@@ -323,48 +357,19 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Tensor map over a row-major matrix (or a stack of them): dims innermost
-// first, byte strides of dims 1.., a box, a swizzle.  Zero fill out of range.
-bool encode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* ptr,
-            const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
-            CUtensorMapSwizzle swz) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, dt, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// bf16 operand [rows, cols] (row stride ld), box box_rows x 64, 128-byte swizzle.
+// bf16 operand [rows, cols] (row stride ld), box box_rows x 64, 128-byte swizzle,
+// zero fill out of range.
 bool make_operand_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
                       int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
     cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
-    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box,
-                  CU_TENSOR_MAP_SWIZZLE_128B);
-}
-
-// Output [rows, cols] with row stride ld, 32 x 32 boxes (fp32: 128-byte rows,
-// 128-byte swizzle; bf16: 64-byte rows, 64-byte swizzle).
-bool make_out_map(CUtensorMap* map, void* ptr, int64_t rows, int64_t cols, int64_t ld, bool bf16) {
-    const int es = bf16 ? 2 : 4;
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)(ld * es)};
-    cuuint32_t box[2] = {32, 32};
-    return encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-                  ptr, dims, strides, box,
-                  bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
-}
-
-// Head-major bf16 q/k/v [n_seq_heads, S, dh] as a 3-D map with 32 x 32 x 1 boxes.
-bool make_heads_map(CUtensorMap* map, void* ptr, int64_t n_seq_heads, int64_t S, int64_t dh) {
-    cuuint64_t dims[3] = {(cuuint64_t)dh, (cuuint64_t)S, (cuuint64_t)n_seq_heads};
-    cuuint64_t strides[2] = {(cuuint64_t)(dh * 2), (cuuint64_t)(S * dh * 2)};
-    cuuint32_t box[3] = {32, 32, 1};
-    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box,
-                  CU_TENSOR_MAP_SWIZZLE_64B);
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Tile width minimising (waves x tile width), the per-SM critical path when
@@ -399,8 +404,8 @@ cudaError_t launch_inst(const GemmPlan& p, cudaStream_t st) {
     const int per = kDual ? BN / 2 : BN;
     const int64_t tiles = (int64_t)((p.M + kBM - 1) / kBM) * ((p.N + per - 1) / per);
     const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
-    k_gemm_tc<BN, STAGES, kDual><<<grid, kThreads, L::kBytes, st>>>(
-        p.maps, p.M, p.N, p.K, p.out_mode, p.out_bf16, p.epi, device_error_word());
+    k_gemm_tc<BN, STAGES, kDual><<<grid, kThreads, L::kBytes, st>>>(p.maps, p.M, p.N, p.K, p.epi,
+                                                                    device_error_word());
     return cudaGetLastError();
 }
 
@@ -423,36 +428,7 @@ tfm_status plan_gemm_tc(GemmPlan* plan, const void* A, int64_t lda, const void* 
     } else {
         plan->maps.b2 = plan->maps.b;
     }
-    // Output path: TMA tile stores wherever the destination allows it.
-    plan->out_mode = OUT_DIRECT;
-    plan->out_bf16 = 0;
-    bool ok = true;
-    switch (epi.kind) {
-        case EPI_STORE_F32:
-        case EPI_ACCUM_F32:
-            plan->out_mode = epi.kind == EPI_STORE_F32 ? OUT_STORE : OUT_REDUCE_ADD;
-            ok = make_out_map(&plan->maps.out[0], epi.out, M, epi.N, epi.ldo, false);
-            break;
-        case EPI_STORE_BF16:
-        case EPI_SWIGLU:
-            plan->out_mode = OUT_STORE;
-            plan->out_bf16 = epi.kind == EPI_STORE_BF16 ? 1 : epi.out_bf16;
-            ok = make_out_map(&plan->maps.out[0], epi.out, M, epi.N, epi.ldo, plan->out_bf16 != 0);
-            break;
-        case EPI_QKV_ROPE:
-            if (epi.out_bf16 && epi.S % 32 == 0 && epi.dh % 32 == 0) {
-                const int64_t B = M / epi.S;
-                plan->out_mode = OUT_QKV_3D;
-                plan->out_bf16 = 1;
-                ok = make_heads_map(&plan->maps.out[0], epi.q, B * epi.n_head, epi.S, epi.dh) &&
-                     make_heads_map(&plan->maps.out[1], epi.k, B * epi.n_kv_head, epi.S, epi.dh) &&
-                     make_heads_map(&plan->maps.out[2], epi.v, B * epi.n_kv_head, epi.S, epi.dh);
-            }
-            break;
-        default:
-            break;
-    }
-    return ok ? TFM_OK : TFM_ECUDA;
+    return TFM_OK;
 }
 
 cudaError_t launch_gemm_tc(const GemmPlan& p, cudaStream_t st) {
