@@ -193,6 +193,13 @@ struct Model {
     const float* plan_logits = nullptr;
     int64_t plan_ld = -1;
     int plan_S = -1;
+    // recorded forward (tfm_forward_graph) and the arguments it was recorded for
+    cudaGraphExec_t gexec = nullptr;
+    const void* g_tokens = nullptr;
+    const float* g_logits = nullptr;
+    int g_B = 0, g_S = 0;
+    int64_t g_ld = 0;
+    void* g_stream = nullptr;
     // per-kernel event timing (tfm_profile_*)
     bool prof = false;
     struct ProfRun {
@@ -297,6 +304,7 @@ tfm_status tfm_create(const tfm_config* cfg, void** handle) {
 void tfm_destroy(void* handle) {
     Model* m = static_cast<Model*>(handle);
     if (!m) return;
+    if (m->gexec) cudaGraphExecDestroy(m->gexec);
     for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
     cudaFree(m->ws);
     cudaFree(m->wmem);
@@ -563,6 +571,53 @@ tfm_status tfm_forward(void* handle, const int32_t* tokens, int32_t B, int32_t S
     if (st != TFM_OK) return st;
     if (!tfm::aligned16(logits)) return fail(TFM_EINVAL, "logits must be 16-byte aligned");
     return tfm::forward_impl(m, tokens, B, S, logits, ld_logits, static_cast<cudaStream_t>(stream));
+}
+
+tfm_status tfm_forward_graph(void* handle, const int32_t* tokens, int32_t B, int32_t S,
+                             float* logits, int64_t ld_logits, void* stream) {
+    Model* m = static_cast<Model*>(handle);
+    tfm_status st = tfm::check_forward_args(m, tokens, B, S, logits, ld_logits);
+    if (st != TFM_OK) return st;
+    if (!tfm::aligned16(logits)) return fail(TFM_EINVAL, "logits must be 16-byte aligned");
+    if (!stream) return fail(TFM_EINVAL, "tfm_forward_graph needs a non-default stream");
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const bool same = m->gexec && m->g_tokens == tokens && m->g_B == B && m->g_S == S &&
+                      m->g_logits == logits && m->g_ld == ld_logits && m->g_stream == stream;
+    if (!same) {
+        if (m->gexec) {
+            cudaGraphExecDestroy(m->gexec);
+            m->gexec = nullptr;
+        }
+        const bool prof = m->prof;
+        m->prof = false;
+        cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+        if (e != cudaSuccess) {
+            m->prof = prof;
+            return tfm::cuda_fail(e, "begin capture");
+        }
+        st = tfm::forward_impl(m, tokens, B, S, logits, ld_logits, cs);
+        cudaGraph_t graph = nullptr;
+        e = cudaStreamEndCapture(cs, &graph);
+        m->prof = prof;
+        if (st != TFM_OK || e != cudaSuccess) {
+            if (graph) cudaGraphDestroy(graph);
+            return st != TFM_OK ? st : tfm::cuda_fail(e, "end capture");
+        }
+        e = cudaGraphInstantiate(&m->gexec, graph, 0);
+        cudaGraphDestroy(graph);
+        if (e != cudaSuccess) {
+            m->gexec = nullptr;
+            return tfm::cuda_fail(e, "graph instantiate");
+        }
+        m->g_tokens = tokens;
+        m->g_B = B;
+        m->g_S = S;
+        m->g_logits = logits;
+        m->g_ld = ld_logits;
+        m->g_stream = stream;
+    }
+    const cudaError_t e = cudaGraphLaunch(m->gexec, cs);
+    return e == cudaSuccess ? TFM_OK : tfm::cuda_fail(e, "graph launch");
 }
 
 tfm_status tfm_forward_host(void* handle, const int32_t* tokens_host, int32_t B, int32_t S,

@@ -18,6 +18,17 @@ __device__ __forceinline__ void raise_error(int* err, int code) {
     if (err) atomicCAS(err, 0, code);
 }
 
+// ------------------------------------------------------------------ PDL
+// Programmatic dependent launch: a kernel launched with launch_pdl() may start
+// while its predecessor on the stream is still running.  It must execute
+// pdl_wait() (which returns once the predecessor grid has completed and its
+// memory is visible) before touching global memory; pdl_trigger() lets the
+// next kernel begin launching once every CTA of this grid has issued it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ bf16
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);   // round to nearest even

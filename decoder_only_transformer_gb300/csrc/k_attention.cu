@@ -76,6 +76,8 @@ __global__ void __launch_bounds__(128) k_attention_mma(const __nv_bfloat16* __re
     __nv_bfloat16* Vs = Ks + 2 * L::kTile;                  // [2][BN][LD]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_wait();
+    pdl_trigger();
     const int num_qt = (S + kAttBM - 1) / kAttBM;
     const int qt = num_qt - 1 - (int)blockIdx.x;            // heavy tiles first
     const int bh = blockIdx.y, b = bh / H, h = bh - b * H;
@@ -243,11 +245,10 @@ cudaError_t launch_dh(const void* q, const void* k, const void* v, void* o, int 
         attr_set = true;
     }
     dim3 grid((S + kAttBM - 1) / kAttBM, B * H);
-    k_attention_mma<DH><<<grid, 128, L::kBytes, st>>>(
-        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-        static_cast<const __nv_bfloat16*>(v), static_cast<__nv_bfloat16*>(o), H, Hkv, S,
-        scale * 1.4426950408889634f);
-    return cudaGetLastError();
+    return launch_pdl(k_attention_mma<DH>, grid, dim3(128), L::kBytes, st,
+                      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+                      static_cast<const __nv_bfloat16*>(v), static_cast<__nv_bfloat16*>(o), H, Hkv,
+                      S, scale * 1.4426950408889634f);
 }
 
 }  // namespace

@@ -130,6 +130,9 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // Everything above overlaps the previous kernel's tail; global memory only after.
+    pdl_wait();
+    pdl_trigger();
     const uint32_t t_o = tmem_base + 256;             // O: columns [256, 256 + DH)
 
     if (warp == 0) {
@@ -395,10 +398,9 @@ cudaError_t launch_tc(const AttnPlan& p, cudaStream_t st) {
         attr_set = true;
     }
     dim3 grid((p.S + kQ - 1) / kQ, p.B * p.H);
-    k_attention_tc<DH><<<grid, kThreadsAtt, L::kBytes, st>>>(
-        p.qmap, p.kmap, p.vmap, static_cast<__nv_bfloat16*>(p.o), p.H, p.Hkv, p.S,
-        p.scale * 1.4426950408889634f, device_error_word());
-    return cudaGetLastError();
+    return launch_pdl(k_attention_tc<DH>, grid, dim3(kThreadsAtt), L::kBytes, st, p.qmap, p.kmap,
+                      p.vmap, static_cast<__nv_bfloat16*>(p.o), p.H, p.Hkv, p.S,
+                      p.scale * 1.4426950408889634f, device_error_word());
 }
 
 }  // namespace

@@ -200,6 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // Everything above overlaps the previous kernel's tail; global memory only after.
+    pdl_wait();
+    pdl_trigger();
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
@@ -404,9 +407,8 @@ cudaError_t launch_inst(const GemmPlan& p, cudaStream_t st) {
     const int per = kDual ? BN / 2 : BN;
     const int64_t tiles = (int64_t)((p.M + kBM - 1) / kBM) * ((p.N + per - 1) / per);
     const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
-    k_gemm_tc<BN, STAGES, kDual><<<grid, kThreads, L::kBytes, st>>>(p.maps, p.M, p.N, p.K, p.epi,
-                                                                    device_error_word());
-    return cudaGetLastError();
+    return launch_pdl(k_gemm_tc<BN, STAGES, kDual>, dim3(grid), dim3(kThreads), L::kBytes, st,
+                      p.maps, p.M, p.N, p.K, p.epi, device_error_word());
 }
 
 }  // namespace

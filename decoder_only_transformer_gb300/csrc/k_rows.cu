@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(256) k_embedding(const int32_t* __restrict__ t
                                                    float* __restrict__ h, int64_t M, int V, int D,
                                                    int* err) {
     const int lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     for (int64_t m = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); m < M;
          m += warps) {
@@ -51,10 +53,10 @@ cudaError_t launch_embedding(const int32_t* tok, const void* E, float* h, int64_
     const int cap = sm_count() * 16;
     if (blocks > cap) blocks = cap;
     if (e_bf16)
-        k_embedding<true><<<(int)blocks, 256, 0, st>>>(tok, E, h, M, V, D, device_error_word());
-    else
-        k_embedding<false><<<(int)blocks, 256, 0, st>>>(tok, E, h, M, V, D, device_error_word());
-    return cudaGetLastError();
+        return launch_pdl(k_embedding<true>, dim3((unsigned)blocks), dim3(256), 0, st, tok, E, h, M,
+                          V, D, device_error_word());
+    return launch_pdl(k_embedding<false>, dim3((unsigned)blocks), dim3(256), 0, st, tok, E, h, M, V,
+                      D, device_error_word());
 }
 
 // ------------------------------------------------------------------ RMSNorm
@@ -68,6 +70,8 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ x,
                                                  void* __restrict__ y, int64_t M, int D,
                                                  float eps) {
     const int lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
     const int64_t m = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (m >= M) return;
     const int n4 = D >> 2;
@@ -109,6 +113,8 @@ __global__ void __launch_bounds__(256) k_rmsnorm_long(const float* __restrict__ 
                                                       void* __restrict__ y, int64_t M, int D,
                                                       float eps) {
     const int lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
     const int64_t m = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (m >= M) return;
     const float4* xr = reinterpret_cast<const float4*>(x + m * D);
@@ -134,32 +140,27 @@ __global__ void __launch_bounds__(256) k_rmsnorm_long(const float* __restrict__ 
 }
 
 template <int kV>
-static void rms_launch(const float* x, const float* g, void* y, int64_t M, int D, float eps,
-                       int out_bf16, cudaStream_t st) {
-    const unsigned blocks = (unsigned)((M + 7) / 8);
-    if (out_bf16)
-        k_rmsnorm<kV, true><<<blocks, 256, 0, st>>>(x, g, y, M, D, eps);
-    else
-        k_rmsnorm<kV, false><<<blocks, 256, 0, st>>>(x, g, y, M, D, eps);
+static cudaError_t rms_launch(const float* x, const float* g, void* y, int64_t M, int D, float eps,
+                              int out_bf16, cudaStream_t st) {
+    const dim3 blocks((unsigned)((M + 7) / 8));
+    if (out_bf16) return launch_pdl(k_rmsnorm<kV, true>, blocks, dim3(256), 0, st, x, g, y, M, D, eps);
+    return launch_pdl(k_rmsnorm<kV, false>, blocks, dim3(256), 0, st, x, g, y, M, D, eps);
 }
 
 cudaError_t launch_rmsnorm(const float* x, const float* g, void* y, int64_t M, int D, float eps,
                            int out_bf16, cudaStream_t st) {
     if (M <= 0) return cudaSuccess;
     const int groups = (D / 4 + 31) / 32;   // float4 groups per lane
-    if (groups <= 1) rms_launch<1>(x, g, y, M, D, eps, out_bf16, st);
-    else if (groups <= 2) rms_launch<2>(x, g, y, M, D, eps, out_bf16, st);
-    else if (groups <= 4) rms_launch<4>(x, g, y, M, D, eps, out_bf16, st);
-    else if (groups <= 6) rms_launch<6>(x, g, y, M, D, eps, out_bf16, st);
-    else if (groups <= 8) rms_launch<8>(x, g, y, M, D, eps, out_bf16, st);
-    else if (groups <= 16) rms_launch<16>(x, g, y, M, D, eps, out_bf16, st);
-    else if (groups <= 32) rms_launch<32>(x, g, y, M, D, eps, out_bf16, st);
-    else {
-        const unsigned blocks = (unsigned)((M + 7) / 8);
-        if (out_bf16) k_rmsnorm_long<true><<<blocks, 256, 0, st>>>(x, g, y, M, D, eps);
-        else k_rmsnorm_long<false><<<blocks, 256, 0, st>>>(x, g, y, M, D, eps);
-    }
-    return cudaGetLastError();
+    if (groups <= 1) return rms_launch<1>(x, g, y, M, D, eps, out_bf16, st);
+    if (groups <= 2) return rms_launch<2>(x, g, y, M, D, eps, out_bf16, st);
+    if (groups <= 4) return rms_launch<4>(x, g, y, M, D, eps, out_bf16, st);
+    if (groups <= 6) return rms_launch<6>(x, g, y, M, D, eps, out_bf16, st);
+    if (groups <= 8) return rms_launch<8>(x, g, y, M, D, eps, out_bf16, st);
+    if (groups <= 16) return rms_launch<16>(x, g, y, M, D, eps, out_bf16, st);
+    if (groups <= 32) return rms_launch<32>(x, g, y, M, D, eps, out_bf16, st);
+    const dim3 blocks((unsigned)((M + 7) / 8));
+    if (out_bf16) return launch_pdl(k_rmsnorm_long<true>, blocks, dim3(256), 0, st, x, g, y, M, D, eps);
+    return launch_pdl(k_rmsnorm_long<false>, blocks, dim3(256), 0, st, x, g, y, M, D, eps);
 }
 
 // ------------------------------------------------------------------ RoPE

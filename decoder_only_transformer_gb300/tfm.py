@@ -57,6 +57,7 @@ _SIGS = {
     "tfm_load_weights": ([_V, ctypes.POINTER(Weights), _I32], _I32),
     "tfm_forward": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
     "tfm_forward_host": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
+    "tfm_forward_graph": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
     "tfm_device_status": ([_V], _I32),
     "tfm_last_error": ([], ctypes.c_char_p),
     "tfm_destroy": ([_V], None),
@@ -200,6 +201,13 @@ class Model:
         B, S = tokens.shape
         _check(self.lib.tfm_forward(self.handle, _ptr(tokens), B, S, _ptr(logits),
                                     logits.stride(0), _stream(stream)))
+
+    def forward_graph(self, tokens, logits, stream=None):
+        """forward() replayed from a CUDA graph recorded on first use; the
+        current torch stream must not be the legacy default stream."""
+        B, S = tokens.shape
+        _check(self.lib.tfm_forward_graph(self.handle, _ptr(tokens), B, S, _ptr(logits),
+                                          logits.stride(0), _stream(stream)))
 
     def forward_host(self, tokens, logits, stream=None):
         """tokens: int32 [B, S] (host, pinned); logits: fp32 [B*S, ld] (host, pinned)."""

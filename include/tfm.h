@@ -144,6 +144,16 @@ tfm_status tfm_load_weights(void* handle, const tfm_weights* w, int32_t weights_
 tfm_status tfm_forward(void* handle, const int32_t* tokens, int32_t B, int32_t S,
                        float* logits, int64_t ld_logits, void* stream);
 
+/* tfm_forward replayed from a CUDA graph.  The first call for a given
+ * (tokens, B, S, logits, ld_logits, stream) records the launch sequence into a
+ * graph (nothing executes while recording), instantiates it and launches it;
+ * later calls with the same arguments only launch the graph, which removes the
+ * per-kernel host launch cost.  Other arguments re-record.  Same results and
+ * requirements as tfm_forward; `stream` must not be the legacy default stream
+ * (NULL); per-kernel profiling does not apply to graph launches. */
+tfm_status tfm_forward_graph(void* handle, const int32_t* tokens, int32_t B, int32_t S,
+                             float* logits, int64_t ld_logits, void* stream);
+
 /* The same forward with HOST buffers: copies tokens host->device, runs the
  * forward, copies logits device->host, all enqueued on `stream` (the caller
  * synchronises).  tokens_host [B, S]; logits_host [B*S, ld_logits]. */

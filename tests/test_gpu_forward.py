@@ -124,6 +124,29 @@ def test_forward_host_matches_device_forward():
     model.close()
 
 
+def test_forward_graph_matches_direct_forward_and_rerecords():
+    cfg = workloads.get_config("small").replace(n_layer=2)
+    w = workloads.make_weights(cfg, gains="random")
+    model = tfm.Model(cfg, max_batch=4, max_seq=256)
+    model.load_weights(to_torch_weights(w, bf16=True))
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for seed, (B, S) in ((1, (2, 200)), (2, (2, 200)), (3, (4, 128))):
+            tok = torch.from_numpy(workloads.make_tokens(cfg, batch=B, seq=S, seed=seed)).cuda()
+            ref = torch.empty(B * S, cfg.vocab, device="cuda")
+            got = torch.full((B * S, cfg.vocab), float("nan"), device="cuda")
+            model.forward(tok, ref)
+            # the same buffers twice: the second call replays the recorded graph
+            model.forward_graph(tok, got)
+            model.forward_graph(tok, got)
+            stream.synchronize()
+            assert torch.equal(got, ref)
+    tfm.device_status()
+    with pytest.raises(tfm.TfmError):          # the legacy default stream cannot be recorded
+        model.forward_graph(tok, got, stream=torch.cuda.default_stream())
+    model.close()
+
+
 def test_bad_token_is_reported():
     cfg = workloads.get_config("tiny")
     w = workloads.make_weights(cfg)
