@@ -108,5 +108,7 @@ bool attention_tc_supported(int dh);
 tfm_status plan_attention_tc(AttnPlan* p, const void* q, const void* k, const void* v, void* o,
                              int B, int H, int Hkv, int S, int dh, float scale);
 cudaError_t launch_attention_tc(const AttnPlan& p, cudaStream_t st);
+// two query tiles per CTA, dh in {32, 64} (k_attention_pp.cu)
+cudaError_t launch_attention_pp(const AttnPlan& p, cudaStream_t st);
 
 }  // namespace tfm

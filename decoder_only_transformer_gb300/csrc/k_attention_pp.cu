@@ -1,0 +1,406 @@
+// k_attention_pp.cu - causal softmax attention on tcgen05, two query tiles per
+// CTA whose softmax phases alternate ("ping-pong"), for d_head 32 and 64 (the
+// library uses it for 64).
+//
+// Same mathematics as k_attention_tc.cu (CS336 walkthrough, section 5.4;
+// "LLM 2", section GQA / MQA): o = softmax(q k^T / sqrt(dh) + M) v, online over
+// key tiles of 128 with a lazily rescaled running max.  What differs is the
+// schedule.  A CTA owns query tiles A = 2p and B = 2p + 1 of one (sequence,
+// head) and every key/value tile is loaded once for both:
+//   warp 0      TMA: Q_A and Q_B, then K_0, V_0, K_1, V_1, ... (two rings)
+//   warp 1      TMEM (S_A, S_B: 128 columns each; O_A, O_B: dh each) and the MMA
+//               thread: S_x = Q_x K_j^T and O_x += P_x V_j for x = A, B
+//   warps 2..5  softmax of tile A, warps 6..9 softmax of tile B (one thread per
+//               query row), so while one group runs its exponentials the other's
+//               scores are being computed and the two groups share the issue slots
+//               and the special-function unit of each scheduler.
+// The softmax works on packed fp32 pairs (f32x2 FMA/ADD) and three-input
+// maxima, about 3 instructions per score; the special-function unit's
+// exponentials (8 cycles per warp instruction) then bound it.  (Evaluating part
+// of the exponentials with a polynomial on the FMA pipe was measured slower
+// here: it costs more issue slots than it frees.)  The MMA thread issues, per
+// key tile, S_A(j+1) and S_B(j+1) as soon as each softmax group has read its
+// current scores, then P_A.V_j and P_B.V_j as the groups finish.  All waits are
+// bounded; tiles above the diagonal are never loaded.
+#include "common.cuh"
+#include "internal.h"
+
+namespace tfm {
+
+namespace {
+
+constexpr int kQ = 128;
+constexpr int kKV = 128;
+constexpr int kThreadsPP = 320;
+constexpr float kRescaleThresholdPP = 8.0f;   // log2 units: P entries stay below 2^8
+
+template <int DH>
+struct AttPP {
+    static constexpr int kRowBytes = DH * 2;                 // 64 (dh 32) or 128 (dh 64)
+    static constexpr int kStages = DH == 32 ? 4 : 3;
+    static constexpr int kQBytes = kQ * DH * 2;
+    static constexpr int kKBytes = kKV * DH * 2;
+    static constexpr int kVBytes = kKV * DH * 2;
+    static constexpr int kPBytes = kQ * kKV * 2;
+    static constexpr int kQOff = 0;                          // Q_A, Q_B
+    static constexpr int kKOff = kQOff + 2 * kQBytes;
+    static constexpr int kVOff = kKOff + kStages * kKBytes;
+    static constexpr int kPOff = kVOff + kStages * kVBytes;  // P_A, P_B
+    static constexpr int kBarOff = kPOff + 2 * kPBytes;
+    // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], o_done[2],
+    // done, s_free[2]
+    static constexpr int kNumBars = 1 + 4 * kStages + 9;
+    static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+    static constexpr int kBytes = kMiscOff + 16 + 1024;
+    // Shared-memory descriptor swizzle of the Q/K/V tiles: 128-byte rows use the
+    // 128-byte swizzle (code 2), 64-byte rows the 64-byte swizzle (code 4).
+    static constexpr uint32_t kSwz = DH == 32 ? 4u : 2u;
+    static constexpr uint32_t kGroup = 8 * kRowBytes;        // 8-row swizzle atom
+};
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor with a given swizzle code, leading and stride
+// byte offsets (tcgen05 descriptor version 1).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t swz, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)swz << 61;
+    return d;
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int lane, int* err,
+                                          volatile int* abort) {
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(bar, parity, err, abort) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) (void)mbar_try_wait(bar, parity);
+    return ok != 0;
+}
+
+template <int DH>
+__global__ void __launch_bounds__(kThreadsPP, 1)
+    k_attention_pp(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap, __nv_bfloat16* __restrict__ o, int H,
+                   int Hkv, int S, float scale_log2, int* err) {
+    using L = AttPP<DH>;
+    constexpr int ST = L::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t sQ = base + L::kQOff, sK = base + L::kKOff, sV = base + L::kVOff,
+                   sP = base + L::kPOff;
+    const uint32_t bars = base + L::kBarOff;
+    const uint32_t q_full = bars;
+    auto k_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto k_empty = [&](int s) { return bars + 8u * (1 + ST + s); };
+    auto v_full = [&](int s) { return bars + 8u * (1 + 2 * ST + s); };
+    auto v_empty = [&](int s) { return bars + 8u * (1 + 3 * ST + s); };
+    auto s_full = [&](int x) { return bars + 8u * (1 + 4 * ST + x); };
+    auto p_full = [&](int x) { return bars + 8u * (3 + 4 * ST + x); };
+    auto o_done = [&](int x) { return bars + 8u * (5 + 4 * ST + x); };
+    const uint32_t done_bar = bars + 8u * (7 + 4 * ST);
+    auto s_free = [&](int x) { return bars + 8u * (8 + 4 * ST + x); };
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + L::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMiscOff + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int num_qt = (S + kQ - 1) / kQ;
+    const int num_pairs = (num_qt + 1) / 2;
+    const int pair = num_pairs - 1 - (int)blockIdx.x;          // heavy pairs first
+    const int qA = 2 * pair, qB = 2 * pair + 1;
+    const int nA = qA + 1;                                      // key tiles of tile A
+    const int nB = qB < num_qt ? qB + 1 : 0;                    // 0: tile B does not exist
+    const int nmax = nB > nA ? nB : nA;
+    const int bh = blockIdx.y, b = bh / H, h = bh - b * H;
+    const int g = h / (H / Hkv);
+
+    if (warp == 0 && lane == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < ST; ++s) {
+            mbar_init(k_full(s), 1);
+            mbar_init(k_empty(s), 1);
+            mbar_init(v_full(s), 1);
+            mbar_init(v_empty(s), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(s_full(x), 1);
+            mbar_init(p_full(x), 4);
+            mbar_init(o_done(x), 1);
+            mbar_init(s_free(x), 4);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&qmap);
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_holder), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    pdl_wait();
+    pdl_trigger();
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(q_full, 2 * L::kQBytes);
+            tma_load_3d(sQ, &qmap, 0, qA * kQ, b * H + h, q_full);
+            tma_load_3d(sQ + L::kQBytes, &qmap, 0, qB * kQ, b * H + h, q_full);
+            int k_issued = 0, v_issued = 0;
+            bool ok = true;
+            for (int j = 0; j < nmax && ok; ++j) {
+                const int st = j % ST;
+                const uint32_t ph = ((uint32_t)(j / ST) & 1u) ^ 1u;
+                if (!mbar_wait(k_empty(st), ph, err, abort_flag)) { ok = false; break; }
+                mbar_arrive_expect_tx(k_full(st), L::kKBytes);
+                tma_load_3d(sK + st * L::kKBytes, &kmap, 0, j * kKV, b * Hkv + g, k_full(st));
+                ++k_issued;
+                if (!mbar_wait(v_empty(st), ph, err, abort_flag)) { ok = false; break; }
+                mbar_arrive_expect_tx(v_full(st), L::kVBytes);
+                tma_load_3d(sV + st * L::kVBytes, &vmap, 0, j * kKV, b * Hkv + g, v_full(st));
+                ++v_issued;
+            }
+            mbar_wait(q_full, 0, err, abort_flag);
+            for (int s = 0; s < ST && s < k_issued; ++s) {
+                const int last = k_issued - 1 - ((k_issued - 1 - s) % ST);
+                mbar_wait(k_full(s), (uint32_t)((last / ST) & 1), err, abort_flag);
+            }
+            for (int s = 0; s < ST && s < v_issued; ++s) {
+                const int last = v_issued - 1 - ((v_issued - 1 - s) % ST);
+                mbar_wait(v_full(s), (uint32_t)((last / ST) & 1), err, abort_flag);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        {
+            constexpr uint32_t idesc_s = umma_idesc_bf16(kQ, kKV);
+            constexpr uint32_t idesc_o = umma_idesc_bf16(kQ, DH, true);
+            const int n_of[2] = {nA, nB};
+            auto issue_s = [&](int x, int j) {             // S_x = Q_x K_j^T
+                const uint32_t qa = sQ + x * L::kQBytes, kb = sK + (j % ST) * L::kKBytes;
+#pragma unroll
+                for (int kk = 0; kk < DH / 16; ++kk)
+                    umma_bf16(tmem_base + x * kKV, sdesc(qa + kk * 32, L::kSwz, 16, L::kGroup),
+                              sdesc(kb + kk * 32, L::kSwz, 16, L::kGroup), idesc_s, kk > 0 ? 1u : 0u);
+                umma_commit(s_full(x));
+            };
+            auto issue_pv = [&](int x, int j) {            // O_x += P_x V_j
+                const uint32_t pa = sP + x * L::kPBytes, vb = sV + (j % ST) * L::kVBytes;
+                const uint32_t t_o = tmem_base + 256 + x * DH;
+#pragma unroll
+                for (int kk = 0; kk < kKV / 16; ++kk)
+                    umma_bf16(t_o, sdesc(pa + (kk >> 2) * 16384 + (kk & 3) * 32, 2, 16, 1024),
+                              sdesc(vb + kk * 16 * L::kRowBytes, L::kSwz, 0, L::kGroup), idesc_o,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(o_done(x));
+            };
+            // Fixed order that matches when the inputs become ready: the next S of
+            // each tile as soon as its softmax has read the current S (s_free),
+            // then the P.V products as the softmax groups finish.
+            if (lane == 0) {
+                bool ok = mbar_wait(q_full, 0, err, abort_flag) &&
+                          mbar_wait(k_full(0), 0, err, abort_flag);
+                if (ok) {
+                    tc_fence_after();
+                    for (int x = 0; x < 2; ++x)
+                        if (n_of[x] > 0) issue_s(x, 0);
+                    umma_commit(k_empty(0));
+                }
+                for (int j = 0; j < nmax && ok; ++j) {
+                    const int jn = j + 1;
+                    if (jn < nmax) {
+                        ok = mbar_wait(k_full(jn % ST), (uint32_t)(jn / ST) & 1u, err, abort_flag);
+                        for (int x = 0; x < 2 && ok; ++x) {
+                            if (jn >= n_of[x]) continue;
+                            ok = mbar_wait(s_free(x), (uint32_t)j & 1u, err, abort_flag);
+                            if (ok) {
+                                tc_fence_after();
+                                issue_s(x, jn);
+                            }
+                        }
+                        if (!ok) break;
+                        umma_commit(k_empty(jn % ST));
+                    }
+                    ok = mbar_wait(v_full(j % ST), (uint32_t)(j / ST) & 1u, err, abort_flag);
+                    for (int x = 0; x < 2 && ok; ++x) {
+                        if (j >= n_of[x]) continue;
+                        ok = mbar_wait(p_full(x), (uint32_t)j & 1u, err, abort_flag);
+                        if (ok) {
+                            tc_fence_after();
+                            issue_pv(x, j);
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit(v_empty(j % ST));
+                }
+                umma_commit(done_bar);
+                mbar_wait(done_bar, 0, err, abort_flag);
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- softmax
+        const int x = (warp - 2) >> 2;                 // 0: tile A, 1: tile B
+        const int q4 = warp & 3;
+        const int r = q4 * 32 + lane;
+        const int qt = x == 0 ? qA : qB;
+        const int n = x == 0 ? nA : nB;
+        const int qi = qt * kQ + r;
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        const uint32_t t_s = tmem_base + x * kKV + lane_off;
+        const uint32_t t_o = tmem_base + 256 + x * DH + lane_off;
+        const uint32_t prow = sP + x * L::kPBytes + r * 128;
+        float m = -INFINITY, l = 0.f;
+        bool ok = n > 0;
+        for (int j = 0; j < n && ok; ++j) {
+            if (!warp_wait(s_full(x), (uint32_t)j & 1u, lane, err, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t sr[kKV / 32][32];
+#pragma unroll
+            for (int c = 0; c < kKV / 32; ++c) tmem_ld32_issue(t_s + c * 32, sr[c]);
+            tmem_ld_wait();
+            // S_x is in registers: the tensor cores may overwrite it with the next tile.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free(x));
+            float s[kKV];
+#pragma unroll
+            for (int c = 0; c < kKV / 32; ++c) {
+                reg_fence32(sr[c]);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[c][e]);
+            }
+            const int k0 = j * kKV;
+            if (j == qt || k0 + kKV > S) {
+#pragma unroll
+                for (int c = 0; c < kKV; ++c)
+                    if (k0 + c > qi || k0 + c >= S) s[c] = -INFINITY;
+            }
+            // Row max: four independent chains of three-input maxima.
+            float mx4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+            for (int c = 4; c < kKV; c += 8)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) mx4[e] = fmax3(mx4[e], s[c + 2 * e], s[c + 2 * e + 1]);
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
+            float corr = 1.f;
+            if (mx > m + kRescaleThresholdPP) {
+                corr = fast_exp2(m - mx);
+                m = mx;
+            }
+            const bool need_rescale = __any_sync(0xffffffffu, corr != 1.f && j > 0);
+            // P_x and O_x are free once O_x += P_x V_{j-1} has completed.
+            if (j >= 1 && !warp_wait(o_done(x), (uint32_t)(j - 1) & 1u, lane, err, abort_flag)) {
+                ok = false;
+                break;
+            }
+            // p = 2^(s*scale - m): scale and offset as packed pairs, one exponential
+            // per element, row sum in four packed accumulators.
+            const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
+            const uint64_t negm2 = f2_pack(-m, -m);
+            uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+            for (int c8 = 0; c8 < kKV / 8; ++c8) {
+                float p[8];
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    float t0, t1;
+                    f2_unpack(f2_fma(f2_pack(s[c8 * 8 + e], s[c8 * 8 + e + 1]), scale2, negm2), t0, t1);
+                    p[e] = fast_exp2(t0);
+                    p[e + 1] = fast_exp2(t1);
+                    sum2[e >> 1] = f2_add(sum2[e >> 1], f2_pack(p[e], p[e + 1]));
+                }
+                const uint32_t addr = prow + (c8 >> 3) * 16384 + (((c8 & 7) ^ (r & 7)) << 4);
+                st_shared_v4(addr, pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
+                             pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
+            }
+            fence_proxy_async_smem();
+            float sa[4], sb[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f2_unpack(sum2[e], sa[e], sb[e]);
+            const float sum = ((sa[0] + sb[0]) + (sa[1] + sb[1])) + ((sa[2] + sb[2]) + (sa[3] + sb[3]));
+            l = l * corr + sum;
+            if (need_rescale) {
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < DH / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(t_o + c * 32, v);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] *= corr;
+                    tmem_st32(t_o + c * 32, v);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full(x));
+        }
+        if (ok && warp_wait(o_done(x), (uint32_t)(n - 1) & 1u, lane, err, abort_flag)) {
+            tc_fence_after();
+            const float inv = 1.0f / l;
+            __nv_bfloat16* orow = o + ((int64_t)b * S + qi) * ((int64_t)H * DH) + (int64_t)h * DH;
+#pragma unroll
+            for (int c = 0; c < DH / 32; ++c) {
+                float v[32];
+                tmem_ld32(t_o + c * 32, v);
+                if (qi < S) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 w;
+                        w.x = pack_bf16x2(v[e] * inv, v[e + 1] * inv);
+                        w.y = pack_bf16x2(v[e + 2] * inv, v[e + 3] * inv);
+                        w.z = pack_bf16x2(v[e + 4] * inv, v[e + 5] * inv);
+                        w.w = pack_bf16x2(v[e + 6] * inv, v[e + 7] * inv);
+                        *reinterpret_cast<uint4*>(orow + c * 32 + e) = w;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, 512);
+}
+
+template <int DH>
+cudaError_t launch_pp(const AttnPlan& p, cudaStream_t st) {
+    using L = AttPP<DH>;
+    static_assert(L::kBytes <= 232448, "shared memory budget");
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_attention_pp<DH>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int num_qt = (p.S + kQ - 1) / kQ;
+    dim3 grid((num_qt + 1) / 2, p.B * p.H);
+    return launch_pdl(k_attention_pp<DH>, grid, dim3(kThreadsPP), L::kBytes, st, p.qmap, p.kmap,
+                      p.vmap, static_cast<__nv_bfloat16*>(p.o), p.H, p.Hkv, p.S,
+                      p.scale * 1.4426950408889634f, device_error_word());
+}
+
+}  // namespace
+
+cudaError_t launch_attention_pp(const AttnPlan& p, cudaStream_t st) {
+    if (p.B <= 0 || p.S <= 0) return cudaSuccess;
+    if (p.dh == 32) return launch_pp<32>(p, st);
+    if (p.dh == 64) return launch_pp<64>(p, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace tfm

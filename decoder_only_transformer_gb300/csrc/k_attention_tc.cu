@@ -260,18 +260,14 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
                 for (int c = 0; c < kKV; ++c)
                     if (k0 + c > qi || k0 + c >= S) s[c] = -INFINITY;
             }
-            // Row max over raw scores with 8 independent chains (the scale is
-            // positive, so it commutes with the max).
-            float mx8[8];
+            // Row max over raw scores: four independent chains of three-input
+            // maxima (the scale is positive, so it commutes with the max).
+            float mx4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) mx8[e] = s[e];
+            for (int c = 4; c < kKV; c += 8)
 #pragma unroll
-            for (int c = 8; c < kKV; c += 8)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], s[c + e]);
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
-                             scale_log2;
+                for (int e = 0; e < 4; ++e) mx4[e] = fmax3(mx4[e], s[c + 2 * e], s[c + 2 * e + 1]);
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
             float corr = 1.f;
             if (mx > m + kRescaleThreshold) {         // also true on the first tile (m = -inf)
                 corr = fast_exp2(m - mx);
@@ -283,24 +279,32 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
                 ok = false;
                 break;
             }
-            float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            const float neg_m = -m;
+            // p = 2^(s*scale - m): scale and offset as packed pairs, one exponential
+            // per element, row sum in four packed accumulators.
+            const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
+            const uint64_t negm2 = f2_pack(-m, -m);
+            uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
             const uint32_t prow = sP + sb * L::kPBytes + r * 128;
 #pragma unroll
             for (int c8 = 0; c8 < kKV / 8; ++c8) {
                 float p[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    p[e] = fast_exp2(fmaf(s[c8 * 8 + e], scale_log2, neg_m));
-                    sum8[e] += p[e];
+                for (int e = 0; e < 8; e += 2) {
+                    float t0, t1;
+                    f2_unpack(f2_fma(f2_pack(s[c8 * 8 + e], s[c8 * 8 + e + 1]), scale2, negm2), t0, t1);
+                    p[e] = fast_exp2(t0);
+                    p[e + 1] = fast_exp2(t1);
+                    sum2[e >> 1] = f2_add(sum2[e >> 1], f2_pack(p[e], p[e + 1]));
                 }
                 const uint32_t addr = prow + (c8 >> 3) * 16384 + (((c8 & 7) ^ (r & 7)) << 4);
                 st_shared_v4(addr, pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
                              pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
             }
             fence_proxy_async_smem();
-            const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                              ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+            float sa[4], sb2[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f2_unpack(sum2[e], sa[e], sb2[e]);
+            const float sum = ((sa[0] + sb2[0]) + (sa[1] + sb2[1])) + ((sa[2] + sb2[2]) + (sa[3] + sb2[3]));
             l = l * corr + sum;
             if (need_rescale) {
                 // O must hold P_{j-1} V_{j-1} before it is rescaled.
@@ -373,16 +377,20 @@ EncodeTiledFn att_encode_fn() {
     return fn;
 }
 
-// [n_seq_heads, S, dh] bf16, box 64 x 128 x 1, 128-byte swizzle, zero fill.
+// [n_seq_heads, S, dh] bf16, box min(dh, 64) x 128 x 1 with the swizzle that
+// matches the box row (128 bytes: 128-byte swizzle; 64 bytes: 64-byte swizzle),
+// zero fill past S.
 bool heads_map(CUtensorMap* map, const void* ptr, int64_t n_seq_heads, int64_t S, int64_t dh) {
     EncodeTiledFn fn = att_encode_fn();
     if (!fn) return false;
+    const cuuint32_t inner = dh >= 64 ? 64 : (cuuint32_t)dh;
     cuuint64_t dims[3] = {(cuuint64_t)dh, (cuuint64_t)S, (cuuint64_t)n_seq_heads};
     cuuint64_t strides[2] = {(cuuint64_t)(dh * 2), (cuuint64_t)(S * dh * 2)};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {inner, 128, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              inner * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -405,6 +413,8 @@ cudaError_t launch_tc(const AttnPlan& p, cudaStream_t st) {
 
 }  // namespace
 
+// d_head 32 stays on the mma.sync kernel (k_attention.cu): measured faster at the
+// short sequences it is used with.
 bool attention_tc_supported(int dh) { return dh == 64 || dh == 128; }
 
 tfm_status plan_attention_tc(AttnPlan* p, const void* q, const void* k, const void* v, void* o,
@@ -425,7 +435,9 @@ tfm_status plan_attention_tc(AttnPlan* p, const void* q, const void* k, const vo
 
 cudaError_t launch_attention_tc(const AttnPlan& p, cudaStream_t st) {
     if (p.B <= 0 || p.S <= 0) return cudaSuccess;
-    if (p.dh == 64) return launch_tc<64>(p, st);
+    // d_head 64: two query tiles per CTA (k_attention_pp.cu); d_head 128: one tile
+    // per CTA (two Q tiles, two P tiles and a K/V ring exceed shared memory).
+    if (p.dh == 64) return launch_attention_pp(p, st);
     if (p.dh == 128) return launch_tc<128>(p, st);
     return cudaErrorInvalidValue;
 }
