@@ -100,6 +100,32 @@ def kernel_table(cfg, B, S, prof, peaks):
     return out
 
 
+def rmsnorm_hbm(tfm, torch, stream, peaks, rows=131072, d=2048, launches=20):
+    """RMSNorm alone on a working set far above L2 (fp32 in 1 GiB, bf16 out),
+    so that its bytes come from HBM: the bandwidth figure the in-forward
+    launches (a few MB, L2-resident) cannot give."""
+    x = torch.randn(rows, d, device="cuda", generator=torch.Generator("cuda").manual_seed(5))
+    g = torch.ones(d, device="cuda")
+    y = torch.empty(rows, d, dtype=torch.bfloat16, device="cuda")
+    for _ in range(3):
+        tfm.rmsnorm(x, g, y, stream=stream)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for _ in range(launches):
+        tfm.rmsnorm(x, g, y, stream=stream)
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    avg_s = ev[0].elapsed_time(ev[1]) / launches / 1e3
+    nbytes = accounting.rmsnorm_bytes(rows, d, out_bytes=2)
+    ach = nbytes / avg_s / 1e9
+    del x, y
+    return {"rows": rows, "d_model": d, "bytes_per_launch": nbytes, "avg_us": round(avg_s * 1e6, 2),
+            "achieved": round(ach, 1), "unit": "GB/s", "peak": peaks["hbm_gbs"],
+            "frac": round(ach / peaks["hbm_gbs"], 4),
+            "note": "fp32 in, bf16 out, back-to-back launches on a 1.5 GiB working set"}
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -212,6 +238,26 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(x, dist, device):
+    """Largest x over all ranks of the process group (x itself without one)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, tokens_per_rank_step, steps, slowest_ms):
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank_step * steps / (slowest_ms / 1e3)
+
+
+def rank_tokens(cfg, rank):
+    """Each replica forwards its own independent batch (seed offset by rank)."""
+    return workloads.make_tokens(cfg, seed=cfg.token_seed + rank)
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
@@ -261,7 +307,7 @@ def main():
     B, S = cfg.batch, cfg.seq
     M = B * S
     w = workloads.make_weights(cfg)
-    tok_np = workloads.make_tokens(cfg, seed=cfg.token_seed + rank)
+    tok_np = rank_tokens(cfg, rank)
     bf = cfg.mode == "bf16"
     mat = torch.bfloat16 if bf else torch.float32
 
@@ -322,12 +368,9 @@ def main():
     model.profile(False)
     prof = model.profile_read()
     tfm.device_status()
-    if dist:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, "cuda")
     ms_per_step = total_ms / args.steps
-    value = world * M * args.steps / (total_ms / 1e3)
+    value = job_rate(world, M, args.steps, total_ms)
 
     # ---- end to end through the C ABI with host buffers
     e2e = None
@@ -348,12 +391,10 @@ def main():
         torch.cuda.synchronize()
         tfm.device_status()
         e2e_ms = sum(es[2 * i].elapsed_time(es[2 * i + 1]) for i in range(args.steps))
-        if dist:
-            t = torch.tensor([e2e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * M * args.steps / (e2e_ms / 1e3), "unit": UNIT,
+        e2e_ms = max_over_ranks(e2e_ms, dist, "cuda")
+        e2e = {"value": job_rate(world, M, args.steps, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": M * 4, "d2h_bytes_per_step": M * cfg.vocab * 4}
+    rms = rmsnorm_hbm(tfm, torch, stream, load_peaks()) if rank == 0 else None
     rows = sampler.stop()
     clocks = ClockSampler.summary(rows)
     clocks["window_s"] = round(t_wall1 - t_wall0, 3)
@@ -400,6 +441,7 @@ def main():
                         "frac": round(fl_t / (ms_t / 1e3) / 1e12 / peaks["bf16_tflops"], 4) if ms_t else None,
                         "whole_forward_tflops": round(total_flops / (ms_per_step / 1e3) / 1e12, 1)},
         "kernels": kernels,
+        "rmsnorm_hbm": rms,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": (3 + 7 * cfg.n_layer) * args.steps,

@@ -128,7 +128,7 @@ Sizes sizes_of(const tfm_config* c) {
 
 // Workspace carve-up, every piece 256-byte aligned.
 struct Layout {
-    size_t h, xn, q, k, v, o, a, rcos, rsin, tok, logits, total;
+    size_t h, xn, q, k, v, o, a, rope, tok, logits, total;
 };
 
 Layout layout_of(const tfm_config* c) {
@@ -148,8 +148,7 @@ Layout layout_of(const tfm_config* c) {
     L.v = take(s.M * s.Dkv * s.es);
     L.o = take(s.M * s.Dq * s.es);
     L.a = take(s.M * s.F * s.es);
-    L.rcos = take((size_t)c->max_seq * (dh / 2) * 4);
-    L.rsin = take((size_t)c->max_seq * (dh / 2) * 4);
+    L.rope = take((size_t)c->max_seq * (dh / 2) * 8);
     L.tok = take(s.M * 4);
     L.logits = take(s.M * s.ldV * 4);
     L.total = off;
@@ -226,8 +225,7 @@ struct Model {
     void* v() { return ws + lay.v; }
     void* o() { return ws + lay.o; }
     void* a() { return ws + lay.a; }
-    float* rcos() { return reinterpret_cast<float*>(ws + lay.rcos); }
-    float* rsin() { return reinterpret_cast<float*>(ws + lay.rsin); }
+    float* rope() { return reinterpret_cast<float*>(ws + lay.rope); }
     int32_t* tok() { return reinterpret_cast<int32_t*>(ws + lay.tok); }
     float* logits() { return reinterpret_cast<float*>(ws + lay.logits); }
 };
@@ -279,17 +277,17 @@ tfm_status tfm_create(const tfm_config* cfg, void** handle) {
         cudaGetLastError();
         return fail(TFM_ENOMEM, "weights: %s", cudaGetErrorString(e));
     }
-    // RoPE table: angle = s * theta^(-2i/dh) in float64, stored as fp32 cos/sin.
+    // RoPE table: angle = s * theta^(-2i/dh) in float64, stored as fp32
+    // (cos, sin) pairs, [max_seq][dh/2][2].
     const int dh = cfg->d_model / cfg->n_head, half = dh / 2;
-    std::vector<float> hc((size_t)cfg->max_seq * half), hs(hc.size());
+    std::vector<float> hcs((size_t)cfg->max_seq * half * 2);
     for (int s = 0; s < cfg->max_seq; ++s)
         for (int i = 0; i < half; ++i) {
             const double ang = (double)s * std::pow((double)cfg->rope_theta, -2.0 * i / dh);
-            hc[(size_t)s * half + i] = (float)std::cos(ang);
-            hs[(size_t)s * half + i] = (float)std::sin(ang);
+            hcs[((size_t)s * half + i) * 2] = (float)std::cos(ang);
+            hcs[((size_t)s * half + i) * 2 + 1] = (float)std::sin(ang);
         }
-    e = cudaMemcpy(m->rcos(), hc.data(), hc.size() * 4, cudaMemcpyHostToDevice);
-    if (e == cudaSuccess) e = cudaMemcpy(m->rsin(), hs.data(), hs.size() * 4, cudaMemcpyHostToDevice);
+    e = cudaMemcpy(m->rope(), hcs.data(), hcs.size() * 4, cudaMemcpyHostToDevice);
     if (e == cudaSuccess && !tfm::device_error_word()) e = cudaErrorSymbolNotFound;
     if (e != cudaSuccess) {
         cudaFree(m->ws);
@@ -405,8 +403,7 @@ EpiParams epi_qkv(Model* m, int M, int S) {
     p.n_head = c.n_head;
     p.n_kv_head = c.n_kv_head;
     p.dh = c.d_model / c.n_head;
-    p.rope_cos = m->rcos();
-    p.rope_sin = m->rsin();
+    p.rope_cs = m->rope();
     p.q = m->q();
     p.k = m->k();
     p.v = m->v();
@@ -635,6 +632,14 @@ tfm_status tfm_forward_host(void* handle, const int32_t* tokens_host, int32_t B,
                           (size_t)m->cfg.vocab * 4, M, cudaMemcpyDeviceToHost, cs);
     if (e != cudaSuccess) return tfm::cuda_fail(e, "logits device->host");
     return TFM_OK;
+}
+
+tfm_status tfm_selftest_wait_timeout(int32_t limit_ms, void* stream) {
+    if (limit_ms < 1 || limit_ms > 2000) return fail(TFM_EINVAL, "limit_ms must be in [1, 2000]");
+    if (!tfm::device_error_word()) return fail(TFM_ECUDA, "device error word unavailable");
+    const cudaError_t e = tfm::launch_selftest_wait((uint64_t)limit_ms * 1000000ull,
+                                                    static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TFM_OK : tfm::cuda_fail(e, "self-test launch");
 }
 
 tfm_status tfm_profile_enable(void* handle, int32_t enable) {

@@ -146,15 +146,13 @@ __device__ __forceinline__ void epi_compute(const EpiParams& p, int row, int col
         if (q.region < 2 && row < p.M) {
             const int dh = p.dh;
             const int s = row % p.S;
-            float cs[W / 2], sn[W / 2];
-            const int64_t t = (int64_t)s * (dh / 2) + q.d0 / 2;
-            load_vec<W / 2>(p.rope_cos + t, cs);
-            load_vec<W / 2>(p.rope_sin + t, sn);
+            float cs[W];                       // (cos, sin) of the W/2 pairs
+            load_vec<W>(p.rope_cs + ((int64_t)s * (dh / 2) + q.d0 / 2) * 2, cs);
 #pragma unroll
             for (int j = 0; j < W / 2; ++j) {
                 const float x0 = a[2 * j], x1 = a[2 * j + 1];
-                o[2 * j] = x0 * cs[j] - x1 * sn[j];
-                o[2 * j + 1] = x0 * sn[j] + x1 * cs[j];
+                o[2 * j] = x0 * cs[2 * j] - x1 * cs[2 * j + 1];
+                o[2 * j + 1] = x0 * cs[2 * j + 1] + x1 * cs[2 * j];
             }
         } else {
 #pragma unroll

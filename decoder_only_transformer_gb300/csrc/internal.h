@@ -26,8 +26,7 @@ struct EpiParams {
     int out_bf16;         // SWIGLU/QKV: 1 = bf16 outputs, 0 = fp32
     // EPI_QKV_ROPE: row m = b*S + s; columns [0,Dq) -> q[b,h,s,:], then k, then v
     int S, n_head, n_kv_head, dh;
-    const float* rope_cos;   // [>= S, dh/2], cos(s * theta^(-2i/dh))
-    const float* rope_sin;
+    const float* rope_cs;    // [>= S, dh/2, 2]: cos, sin of s * theta^(-2i/dh)
     void* q;
     void* k;
     void* v;
@@ -65,6 +64,7 @@ cudaError_t launch_rmsnorm(const float* x, const float* g, void* y, int64_t M, i
                            int out_bf16, cudaStream_t st);
 cudaError_t launch_rope(void* x, const int32_t* pos, int B, int H, int S, int dh, float theta,
                         int is_bf16, cudaStream_t st);
+cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t st);
 
 // ---- CUDA-core kernels (k_simt.cu), fp32 mode
 // C = A[M,K] . B[N,K]^T (and A . B2^T for EPI_SWIGLU), then the epilogue.

@@ -7,20 +7,24 @@
 // key tiles of 128 with a lazily rescaled running max.  What differs is the
 // schedule.  A CTA owns query tiles A = 2p and B = 2p + 1 of one (sequence,
 // head) and every key/value tile is loaded once for both:
-//   warp 0      TMA: Q_A and Q_B, then K_0, V_0, K_1, V_1, ... (two rings)
-//   warp 1      TMEM (S_A, S_B: 128 columns each; O_A, O_B: dh each) and the MMA
-//               thread: S_x = Q_x K_j^T and O_x += P_x V_j for x = A, B
+//   warp 0      TMA: Q_A and Q_B, then K_j and V_j into two rings
+//   warp 1      TMEM (S_A, S_B: 128 columns each; O_A, O_B: dh each; P_A, P_B:
+//               64 each) and the S MMAs: S_x = Q_x K_j^T for x = A, B
+//   warp 10     the P.V MMAs: O_x += P_x V_j, P_x read from tensor memory
 //   warps 2..5  softmax of tile A, warps 6..9 softmax of tile B (one thread per
 //               query row), so while one group runs its exponentials the other's
 //               scores are being computed and the two groups share the issue slots
 //               and the special-function unit of each scheduler.
 // The softmax works on packed fp32 pairs (f32x2 FMA/ADD) and three-input
-// maxima, about 3 instructions per score; the special-function unit's
-// exponentials (8 cycles per warp instruction) then bound it.  (Evaluating part
-// of the exponentials with a polynomial on the FMA pipe was measured slower
-// here: it costs more issue slots than it frees.)  The MMA thread issues, per
-// key tile, S_A(j+1) and S_B(j+1) as soon as each softmax group has read its
-// current scores, then P_A.V_j and P_B.V_j as the groups finish.  All waits are
+// maxima, about 3 instructions per score besides the exponential (the
+// special-function unit takes 4 cycles per warp ex2 on each scheduler; the
+// bf16 packing and the FMAs overlap with it).  (Evaluating part of the
+// exponentials with a polynomial on the FMA pipe was measured slower here: it
+// costs more issue slots than it frees.)  S_x(j+1) is issued as soon as the
+// softmax of tile x has read S_x(j) into registers, P_x.V_j as soon as it has
+// written P_x(j).  An MMA warp shares its scheduler with two softmax warps,
+// which leaves it few issue slots; one thread issuing all ~24 MMAs of a key tile
+// was measured to be the bound, hence two issuing threads.  All waits are
 // bounded; tiles above the diagonal are never loaded.
 #include "common.cuh"
 #include "internal.h"
@@ -31,22 +35,24 @@ namespace {
 
 constexpr int kQ = 128;
 constexpr int kKV = 128;
-constexpr int kThreadsPP = 320;
+constexpr int kThreadsPP = 352;
 constexpr float kRescaleThresholdPP = 8.0f;   // log2 units: P entries stay below 2^8
 
 template <int DH>
 struct AttPP {
     static constexpr int kRowBytes = DH * 2;                 // 64 (dh 32) or 128 (dh 64)
-    static constexpr int kStages = DH == 32 ? 4 : 3;
+    static constexpr int kStages = 6;
     static constexpr int kQBytes = kQ * DH * 2;
     static constexpr int kKBytes = kKV * DH * 2;
     static constexpr int kVBytes = kKV * DH * 2;
-    static constexpr int kPBytes = kQ * kKV * 2;
     static constexpr int kQOff = 0;                          // Q_A, Q_B
     static constexpr int kKOff = kQOff + 2 * kQBytes;
     static constexpr int kVOff = kKOff + kStages * kKBytes;
-    static constexpr int kPOff = kVOff + kStages * kVBytes;  // P_A, P_B
-    static constexpr int kBarOff = kPOff + 2 * kPBytes;
+    static constexpr int kBarOff = kVOff + kStages * kVBytes;
+    // Tensor-memory columns: S_A, S_B (128 each), O_A, O_B (DH each), then P_A,
+    // P_B (64 each: 128 bf16 per row, two per 32-bit column).
+    static constexpr int kOCol = 2 * kKV;
+    static constexpr int kPCol = kOCol + 2 * DH;
     // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], o_done[2],
     // done, s_free[2]
     static constexpr int kNumBars = 1 + 4 * kStages + 9;
@@ -57,13 +63,6 @@ struct AttPP {
     static constexpr uint32_t kSwz = DH == 32 ? 4u : 2u;
     static constexpr uint32_t kGroup = 8 * kRowBytes;        // 8-row swizzle atom
 };
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
-}
 
 // Shared-memory matrix descriptor with a given swizzle code, leading and stride
 // byte offsets (tcgen05 descriptor version 1).
@@ -97,8 +96,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t sQ = base + L::kQOff, sK = base + L::kKOff, sV = base + L::kVOff,
-                   sP = base + L::kPOff;
+    const uint32_t sQ = base + L::kQOff, sK = base + L::kKOff, sV = base + L::kVOff;
     const uint32_t bars = base + L::kBarOff;
     const uint32_t q_full = bars;
     auto k_full = [&](int s) { return bars + 8u * (1 + s); };
@@ -138,7 +136,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
             mbar_init(o_done(x), 1);
             mbar_init(s_free(x), 4);
         }
-        mbar_init(done_bar, 1);
+        mbar_init(done_bar, 2);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&qmap);
@@ -153,105 +151,112 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
     pdl_wait();
     pdl_trigger();
 
+    constexpr uint32_t idesc_s = umma_idesc_bf16(kQ, kKV);
+    constexpr uint32_t idesc_o = umma_idesc_bf16(kQ, DH, true);
+    const int n_of[2] = {nA, nB};
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
+        // Q_A, Q_B, then K_j and V_j into their rings.  Before exiting it waits for
+        // its last load into every slot, so no copy is in flight when the CTA ends.
         if (lane == 0) {
             mbar_arrive_expect_tx(q_full, 2 * L::kQBytes);
             tma_load_3d(sQ, &qmap, 0, qA * kQ, b * H + h, q_full);
             tma_load_3d(sQ + L::kQBytes, &qmap, 0, qB * kQ, b * H + h, q_full);
-            int k_issued = 0, v_issued = 0;
-            bool ok = true;
-            for (int j = 0; j < nmax && ok; ++j) {
+            int issued = 0;
+            for (int j = 0; j < nmax; ++j) {
                 const int st = j % ST;
                 const uint32_t ph = ((uint32_t)(j / ST) & 1u) ^ 1u;
-                if (!mbar_wait(k_empty(st), ph, err, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(k_empty(st), ph, err, abort_flag)) break;
                 mbar_arrive_expect_tx(k_full(st), L::kKBytes);
                 tma_load_3d(sK + st * L::kKBytes, &kmap, 0, j * kKV, b * Hkv + g, k_full(st));
-                ++k_issued;
-                if (!mbar_wait(v_empty(st), ph, err, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(v_empty(st), ph, err, abort_flag)) {
+                    mbar_wait(k_full(st), (uint32_t)((j / ST) & 1), err, abort_flag);
+                    break;
+                }
                 mbar_arrive_expect_tx(v_full(st), L::kVBytes);
                 tma_load_3d(sV + st * L::kVBytes, &vmap, 0, j * kKV, b * Hkv + g, v_full(st));
-                ++v_issued;
+                ++issued;
             }
             mbar_wait(q_full, 0, err, abort_flag);
-            for (int s = 0; s < ST && s < k_issued; ++s) {
-                const int last = k_issued - 1 - ((k_issued - 1 - s) % ST);
+            for (int s = 0; s < ST && s < issued; ++s) {
+                const int last = issued - 1 - ((issued - 1 - s) % ST);
                 mbar_wait(k_full(s), (uint32_t)((last / ST) & 1), err, abort_flag);
-            }
-            for (int s = 0; s < ST && s < v_issued; ++s) {
-                const int last = v_issued - 1 - ((v_issued - 1 - s) % ST);
                 mbar_wait(v_full(s), (uint32_t)((last / ST) & 1), err, abort_flag);
             }
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
-        {
-            constexpr uint32_t idesc_s = umma_idesc_bf16(kQ, kKV);
-            constexpr uint32_t idesc_o = umma_idesc_bf16(kQ, DH, true);
-            const int n_of[2] = {nA, nB};
-            auto issue_s = [&](int x, int j) {             // S_x = Q_x K_j^T
-                const uint32_t qa = sQ + x * L::kQBytes, kb = sK + (j % ST) * L::kKBytes;
+    } else if (warp == 1 || warp == 10) {
+        // ---------------------------------------------------------- MMA issuers
+        // Two threads on different schedulers: warp 1 issues S_x = Q_x K_j^T (into
+        // the S columns), warp 10 issues O_x += P_x V_j (P from its TMEM columns).
+        // The two streams touch disjoint tensor memory and are ordered only through
+        // the softmax barriers; each commit covers its own thread's MMAs.  Both
+        // share the scheduler with two busy softmax warps, so the per-MMA work is
+        // kept small: descriptors are built once and advanced by adding
+        // (byte offset >> 4) to their start-address field (shared addresses stay
+        // below 256 KB, so the 14-bit field never carries).
+        if (lane == 0) {
+            bool ok = true;
+            if (warp == 1) {
+                const uint64_t dq = sdesc(sQ, L::kSwz, 16, L::kGroup);
+                const uint64_t dk = sdesc(sK, L::kSwz, 16, L::kGroup);
+                auto issue_s = [&](int x, int st) {
+                    const uint64_t a0 = dq + (uint64_t)(x * (L::kQBytes >> 4));
+                    const uint64_t b0 = dk + (uint64_t)(st * (L::kKBytes >> 4));
+                    const uint32_t t_s = tmem_base + x * kKV;
 #pragma unroll
-                for (int kk = 0; kk < DH / 16; ++kk)
-                    umma_bf16(tmem_base + x * kKV, sdesc(qa + kk * 32, L::kSwz, 16, L::kGroup),
-                              sdesc(kb + kk * 32, L::kSwz, 16, L::kGroup), idesc_s, kk > 0 ? 1u : 0u);
-                umma_commit(s_full(x));
-            };
-            auto issue_pv = [&](int x, int j) {            // O_x += P_x V_j
-                const uint32_t pa = sP + x * L::kPBytes, vb = sV + (j % ST) * L::kVBytes;
-                const uint32_t t_o = tmem_base + 256 + x * DH;
-#pragma unroll
-                for (int kk = 0; kk < kKV / 16; ++kk)
-                    umma_bf16(t_o, sdesc(pa + (kk >> 2) * 16384 + (kk & 3) * 32, 2, 16, 1024),
-                              sdesc(vb + kk * 16 * L::kRowBytes, L::kSwz, 0, L::kGroup), idesc_o,
-                              (j > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(o_done(x));
-            };
-            // Fixed order that matches when the inputs become ready: the next S of
-            // each tile as soon as its softmax has read the current S (s_free),
-            // then the P.V products as the softmax groups finish.
-            if (lane == 0) {
-                bool ok = mbar_wait(q_full, 0, err, abort_flag) &&
-                          mbar_wait(k_full(0), 0, err, abort_flag);
-                if (ok) {
-                    tc_fence_after();
-                    for (int x = 0; x < 2; ++x)
-                        if (n_of[x] > 0) issue_s(x, 0);
-                    umma_commit(k_empty(0));
-                }
+                    for (int kk = 0; kk < DH / 16; ++kk)
+                        umma_bf16(t_s, a0 + 2 * kk, b0 + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
+                    umma_commit(s_full(x));
+                };
+                ok = mbar_wait(q_full, 0, err, abort_flag);
                 for (int j = 0; j < nmax && ok; ++j) {
-                    const int jn = j + 1;
-                    if (jn < nmax) {
-                        ok = mbar_wait(k_full(jn % ST), (uint32_t)(jn / ST) & 1u, err, abort_flag);
-                        for (int x = 0; x < 2 && ok; ++x) {
-                            if (jn >= n_of[x]) continue;
-                            ok = mbar_wait(s_free(x), (uint32_t)j & 1u, err, abort_flag);
-                            if (ok) {
-                                tc_fence_after();
-                                issue_s(x, jn);
-                            }
+                    const int st = j % ST;
+                    ok = mbar_wait(k_full(st), (uint32_t)(j / ST) & 1u, err, abort_flag);
+                    for (int x = 0; x < 2 && ok; ++x) {
+                        if (j >= n_of[x]) continue;
+                        // S_x is free once the softmax has read the previous tile's
+                        // scores into registers.
+                        if (j > 0) ok = mbar_wait(s_free(x), (uint32_t)(j - 1) & 1u, err, abort_flag);
+                        if (ok) {
+                            tc_fence_after();
+                            issue_s(x, st);
                         }
-                        if (!ok) break;
-                        umma_commit(k_empty(jn % ST));
                     }
-                    ok = mbar_wait(v_full(j % ST), (uint32_t)(j / ST) & 1u, err, abort_flag);
+                    if (ok) umma_commit(k_empty(st));
+                }
+            } else {
+                const uint64_t dv = sdesc(sV, L::kSwz, 0, L::kGroup);
+                auto issue_pv = [&](int x, int st, bool first) {
+                    const uint64_t b0 = dv + (uint64_t)(st * (L::kVBytes >> 4));
+                    const uint32_t t_o = tmem_base + L::kOCol + x * DH;
+                    const uint32_t t_p = tmem_base + L::kPCol + x * (kKV / 2);
+#pragma unroll
+                    for (int kk = 0; kk < kKV / 16; ++kk)
+                        umma_bf16_ts(t_o, t_p + kk * 8, b0 + kk * ((16 * L::kRowBytes) >> 4),
+                                     idesc_o, (!first || kk > 0) ? 1u : 0u);
+                    umma_commit(o_done(x));
+                };
+                for (int j = 0; j < nmax && ok; ++j) {
+                    const int st = j % ST;
+                    ok = mbar_wait(v_full(st), (uint32_t)(j / ST) & 1u, err, abort_flag);
                     for (int x = 0; x < 2 && ok; ++x) {
                         if (j >= n_of[x]) continue;
                         ok = mbar_wait(p_full(x), (uint32_t)j & 1u, err, abort_flag);
                         if (ok) {
                             tc_fence_after();
-                            issue_pv(x, j);
+                            issue_pv(x, st, j == 0);
                         }
                     }
-                    if (!ok) break;
-                    umma_commit(v_empty(j % ST));
+                    if (ok) umma_commit(v_empty(st));
                 }
-                umma_commit(done_bar);
-                mbar_wait(done_bar, 0, err, abort_flag);
             }
+            // Every MMA this thread issued must be complete before TMEM is freed
+            // (done_bar counts one commit from each issuer).
+            umma_commit(done_bar);
+            mbar_wait(done_bar, 0, err, abort_flag);
         }
     } else {
-        // ---------------------------------------------------------- softmax
+        // ---------------------------------------------------------- softmax (warps 2..9)
         const int x = (warp - 2) >> 2;                 // 0: tile A, 1: tile B
         const int q4 = warp & 3;
         const int r = q4 * 32 + lane;
@@ -260,8 +265,8 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
         const int qi = qt * kQ + r;
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const uint32_t t_s = tmem_base + x * kKV + lane_off;
-        const uint32_t t_o = tmem_base + 256 + x * DH + lane_off;
-        const uint32_t prow = sP + x * L::kPBytes + r * 128;
+        const uint32_t t_o = tmem_base + L::kOCol + x * DH + lane_off;
+        const uint32_t t_p = tmem_base + L::kPCol + x * (kKV / 2) + lane_off;
         float m = -INFINITY, l = 0.f;
         bool ok = n > 0;
         for (int j = 0; j < n && ok; ++j) {
@@ -307,26 +312,26 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                 break;
             }
             // p = 2^(s*scale - m): scale and offset as packed pairs, one exponential
-            // per element, row sum in four packed accumulators.
+            // per element, row sum in four packed accumulators; P goes to tensor
+            // memory as bf16 pairs, 64 keys (32 columns) per store.
             const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
             const uint64_t negm2 = f2_pack(-m, -m);
             uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-            for (int c8 = 0; c8 < kKV / 8; ++c8) {
-                float p[8];
+            for (int h64 = 0; h64 < kKV / 64; ++h64) {
+                uint32_t pw[32];
 #pragma unroll
-                for (int e = 0; e < 8; e += 2) {
+                for (int e = 0; e < 64; e += 2) {
                     float t0, t1;
-                    f2_unpack(f2_fma(f2_pack(s[c8 * 8 + e], s[c8 * 8 + e + 1]), scale2, negm2), t0, t1);
-                    p[e] = fast_exp2(t0);
-                    p[e + 1] = fast_exp2(t1);
-                    sum2[e >> 1] = f2_add(sum2[e >> 1], f2_pack(p[e], p[e + 1]));
+                    const int c = h64 * 64 + e;
+                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), scale2, negm2), t0, t1);
+                    const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+                    sum2[(e >> 1) & 3] = f2_add(sum2[(e >> 1) & 3], f2_pack(p0, p1));
+                    pw[e >> 1] = pack_bf16x2(p0, p1);
                 }
-                const uint32_t addr = prow + (c8 >> 3) * 16384 + (((c8 & 7) ^ (r & 7)) << 4);
-                st_shared_v4(addr, pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
-                             pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
+                tmem_st32_async(t_p + h64 * 32, pw);
             }
-            fence_proxy_async_smem();
+            tmem_st_wait();
             float sa[4], sb[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) f2_unpack(sum2[e], sa[e], sb[e]);

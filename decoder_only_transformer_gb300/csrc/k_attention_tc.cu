@@ -12,13 +12,16 @@
 //   warp 0      TMA: the Q tile once, then K and V tiles (3-D maps [seq*heads,
 //               S, dh], 128-byte swizzle, zero fill past S) into separate K and V
 //               rings, in the order the MMA thread consumes them
-//   warp 1      TMEM (512 columns: S double buffer 2 x 128, O dh) and one MMA
-//               thread: S_j = Q K_j^T (M=128, N=128, K=dh), then O += P_{j-1} V_{j-1}
-//               (M=128, N=dh, K=128; V read MN-major straight from its [key, dh]
-//               tile, so it is never transposed)
+//   warp 1      TMEM (512 columns: S double buffer 2 x 128, O dh, P double buffer
+//               2 x 64) and the S MMAs: S_j = Q K_j^T (M=128, N=128, K=dh)
+//   warp 6      the P.V MMAs: O += P_j V_j (M=128, N=dh, K=128; P read from tensor
+//               memory, V read MN-major straight from its [key, dh] tile, so it is
+//               never transposed).  Issuing from two threads keeps the per-thread
+//               instruction stream short: an MMA warp shares its scheduler with a
+//               softmax warp and gets few issue slots.
 //   warps 2..5  softmax, one thread per query row: S row from TMEM, causal /
-//               length mask, row max, p = 2^(s*scale*log2e - m) written as bf16
-//               into a swizzled P tile (the A operand of P.V), row sum; the partial
+//               length mask, row max, p = 2^(s*scale*log2e - m) stored as bf16
+//               pairs into the P columns of tensor memory, row sum; the partial
 //               O in TMEM is rescaled only when the row max grows by more than
 //               2^8, so P entries stay below 256 and most tiles skip the rescale
 // S_{j+1} runs on the tensor cores while the softmax warps work on S_j.
@@ -32,35 +35,28 @@ namespace {
 
 constexpr int kQ = 128;
 constexpr int kKV = 128;
-constexpr int kThreadsAtt = 192;
+constexpr int kThreadsAtt = 224;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 template <int DH>
 struct AttTc {
-    static constexpr int kStages = DH == 64 ? 3 : 2;
+    static constexpr int kStages = DH == 64 ? 4 : 3;
     static constexpr int kSub = DH / 64;              // 64-column (128-byte) sub-tiles
     static constexpr int kQBytes = kQ * DH * 2;
     static constexpr int kKBytes = kKV * DH * 2;
     static constexpr int kVBytes = kKV * DH * 2;
-    static constexpr int kPBytes = kQ * kKV * 2;
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kQOff + kQBytes;
     static constexpr int kVOff = kKOff + kStages * kKBytes;
-    static constexpr int kPOff = kVOff + kStages * kVBytes;
-    static constexpr int kBarOff = kPOff + 2 * kPBytes;
+    static constexpr int kBarOff = kVOff + kStages * kVBytes;
+    static constexpr int kOCol = 2 * kKV;             // TMEM columns: S[2], O, P[2]
+    static constexpr int kPCol = kOCol + DH;
     // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2],
     // o_done[2], done
     static constexpr int kNumBars = 1 + 4 * kStages + 7;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kBytes = kMiscOff + 16 + 1024;
 };
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
-}
 
 // Bounded wait by lane 0, result broadcast, acquire in every lane.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int lane, int* err,
@@ -83,8 +79,7 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t sQ = base + L::kQOff, sK = base + L::kKOff, sV = base + L::kVOff,
-                   sP = base + L::kPOff;
+    const uint32_t sQ = base + L::kQOff, sK = base + L::kKOff, sV = base + L::kVOff;
     const uint32_t bars = base + L::kBarOff;
     const uint32_t q_full = bars;
     auto k_full = [&](int s) { return bars + 8u * (1 + s); };
@@ -118,7 +113,7 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
             mbar_init(p_full(i), 4);
             mbar_init(o_done(i), 1);
         }
-        mbar_init(done_bar, 1);
+        mbar_init(done_bar, 2);              // one commit from each MMA thread
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&qmap);
@@ -133,7 +128,7 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
     // Everything above overlaps the previous kernel's tail; global memory only after.
     pdl_wait();
     pdl_trigger();
-    const uint32_t t_o = tmem_base + 256;             // O: columns [256, 256 + DH)
+    const uint32_t t_o = tmem_base + L::kOCol;
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
@@ -181,50 +176,55 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
                 mbar_wait(v_full(s), (uint32_t)((last / ST) & 1), err, abort_flag);
             }
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
+    } else if (warp == 1 || warp == 6) {
+        // ---------------------------------------------------------- MMA issuers
+        // Descriptors are built once and advanced by adding (byte offset >> 4) to
+        // their start-address field (shared addresses stay below 256 KB, so the
+        // 14-bit field never carries).
         if (lane == 0) {
             constexpr uint32_t idesc_s = umma_idesc_bf16(kQ, kKV);
             constexpr uint32_t idesc_o = umma_idesc_bf16(kQ, DH, true);
-            bool ok = mbar_wait(q_full, 0, err, abort_flag);
-            auto issue_pv = [&](int i) -> bool {
-                const int sbp = i & 1, stp = i % ST;
-                if (!mbar_wait(p_full(sbp), (uint32_t)(i >> 1) & 1u, err, abort_flag)) return false;
-                if (!mbar_wait(v_full(stp), (uint32_t)(i / ST) & 1u, err, abort_flag)) return false;
-                tc_fence_after();
-                const uint32_t pa = sP + sbp * L::kPBytes;
-                const uint32_t vb = sV + stp * L::kVBytes;
+            bool ok = true;
+            if (warp == 1) {
+                // S_j into S[j % 2] once the softmax of tile j-2 is done with it.
+                const uint64_t dq = umma_desc_sw128(sQ), dk = umma_desc_sw128(sK);
+                ok = mbar_wait(q_full, 0, err, abort_flag);
+                for (int j = 0; j < n && ok; ++j) {
+                    const int sb = j & 1, st = j % ST;
+                    if (j >= 2 && !mbar_wait(p_full(sb), (uint32_t)((j - 2) >> 1) & 1u, err, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!mbar_wait(k_full(st), (uint32_t)(j / ST) & 1u, err, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + (uint32_t)(sb * kKV);
+                    const uint64_t kb = dk + (uint64_t)((st * L::kKBytes) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < kKV / 16; ++kk) {
-                    const uint64_t ad = umma_desc_sw128(pa + (kk >> 2) * 16384 + (kk & 3) * 32);
-                    const uint64_t bd = umma_desc_sw128_mn(vb + kk * 2048, 16384, 1024);
-                    umma_bf16(t_o, ad, bd, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < DH / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                        umma_bf16(d, dq + off, kb + off, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(k_empty(st));
+                    umma_commit(s_full(sb));
                 }
-                umma_commit(v_empty(stp));
-                umma_commit(o_done(sbp));
-                return true;
-            };
-            for (int j = 0; j < n && ok; ++j) {
-                const int sb = j & 1, st = j % ST;
-                if (j >= 2 && !mbar_wait(p_full(sb), (uint32_t)((j - 2) >> 1) & 1u, err, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                if (!mbar_wait(k_full(st), (uint32_t)(j / ST) & 1u, err, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t d = tmem_base + (uint32_t)(sb * kKV);
-                const uint32_t kb = sK + st * L::kKBytes;
+            } else {
+                // O += P_i V_i once the softmax has written P_i.
+                const uint64_t dv = umma_desc_sw128_mn(sV, 16384, 1024);
+                for (int i = 0; i < n && ok; ++i) {
+                    const int sbp = i & 1, stp = i % ST;
+                    if (!mbar_wait(p_full(sbp), (uint32_t)(i >> 1) & 1u, err, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(v_full(stp), (uint32_t)(i / ST) & 1u, err, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t t_p = tmem_base + L::kPCol + sbp * (kKV / 2);
+                    const uint64_t vb = dv + (uint64_t)((stp * L::kVBytes) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < DH / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    umma_bf16(d, umma_desc_sw128(sQ + off), umma_desc_sw128(kb + off), idesc_s,
-                              kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < kKV / 16; ++kk)
+                        umma_bf16_ts(t_o, t_p + kk * 8, vb + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                                     (i > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(v_empty(stp));
+                    umma_commit(o_done(sbp));
                 }
-                umma_commit(k_empty(st));
-                umma_commit(s_full(sb));
-                if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
             }
-            if (ok) issue_pv(n - 1);
             umma_commit(done_bar);
             mbar_wait(done_bar, 0, err, abort_flag);
         }
@@ -280,27 +280,27 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
                 break;
             }
             // p = 2^(s*scale - m): scale and offset as packed pairs, one exponential
-            // per element, row sum in four packed accumulators.
+            // per element, row sum in four packed accumulators; P goes to tensor
+            // memory as bf16 pairs, 64 keys (32 columns) per store.
             const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
             const uint64_t negm2 = f2_pack(-m, -m);
             uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
-            const uint32_t prow = sP + sb * L::kPBytes + r * 128;
+            const uint32_t t_p = trow + L::kPCol + sb * (kKV / 2);
 #pragma unroll
-            for (int c8 = 0; c8 < kKV / 8; ++c8) {
-                float p[8];
+            for (int h64 = 0; h64 < kKV / 64; ++h64) {
+                uint32_t pw[32];
 #pragma unroll
-                for (int e = 0; e < 8; e += 2) {
+                for (int e = 0; e < 64; e += 2) {
                     float t0, t1;
-                    f2_unpack(f2_fma(f2_pack(s[c8 * 8 + e], s[c8 * 8 + e + 1]), scale2, negm2), t0, t1);
-                    p[e] = fast_exp2(t0);
-                    p[e + 1] = fast_exp2(t1);
-                    sum2[e >> 1] = f2_add(sum2[e >> 1], f2_pack(p[e], p[e + 1]));
+                    const int c = h64 * 64 + e;
+                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), scale2, negm2), t0, t1);
+                    const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+                    sum2[(e >> 1) & 3] = f2_add(sum2[(e >> 1) & 3], f2_pack(p0, p1));
+                    pw[e >> 1] = pack_bf16x2(p0, p1);
                 }
-                const uint32_t addr = prow + (c8 >> 3) * 16384 + (((c8 & 7) ^ (r & 7)) << 4);
-                st_shared_v4(addr, pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
-                             pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
+                tmem_st32_async(t_p + h64 * 32, pw);
             }
-            fence_proxy_async_smem();
+            tmem_st_wait();
             float sa[4], sb2[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) f2_unpack(sum2[e], sa[e], sb2[e]);

@@ -86,16 +86,24 @@ __device__ __forceinline__ void stage_row(uint32_t buf, int lane, const float (&
 // Writes the staged 32 x 32 block (rows row0.., columns col..) to its
 // destination with each lane moving one 16-byte row segment per step, so a warp
 // store covers whole 32-byte sectors.  Rows >= M and columns >= N are skipped
-// exactly (element-wise at a ragged right edge).
+// exactly (element-wise at a ragged right edge).  All shared-memory reads of
+// the block are issued before the first global store: the reads are ordered
+// against memory operations, so interleaving them would serialise the steps.
 __device__ __forceinline__ void flush_block(const EpiParams& p, uint32_t buf, int lane, int row0,
                                             int col) {
     if (p.kind == EPI_STORE_F32 || p.kind == EPI_ACCUM_F32) {
         const int seg = lane & 7;
         const int ncol = col + seg * 4;
+        uint4 vs[8];
 #pragma unroll
         for (int step = 0; step < 8; ++step) {
             const int r = step * 4 + (lane >> 3);
-            const uint4 v = ld_shared_v4(buf + r * 128 + ((seg ^ (r & 7)) << 4));
+            vs[step] = ld_shared_v4(buf + r * 128 + ((seg ^ (r & 7)) << 4));
+        }
+#pragma unroll
+        for (int step = 0; step < 8; ++step) {
+            const int r = step * 4 + (lane >> 3);
+            const uint4 v = vs[step];
             const int row = row0 + r;
             if (row >= p.M || ncol >= p.N) continue;
             float* d = static_cast<float*>(p.out) + (int64_t)row * p.ldo + ncol;
@@ -126,16 +134,33 @@ __device__ __forceinline__ void flush_block(const EpiParams& p, uint32_t buf, in
         qbase = static_cast<__nv_bfloat16*>(qs.region == 0 ? p.q : (qs.region == 1 ? p.k : p.v));
     }
     const int ncol = col + seg * 8;
+    uint4 vs[4];
 #pragma unroll
     for (int step = 0; step < 4; ++step) {
         const int r = step * 8 + (lane >> 2);
-        const uint4 v = ld_shared_v4(buf + r * 64 + ((seg ^ ((r >> 1) & 3)) << 4));
+        vs[step] = ld_shared_v4(buf + r * 64 + ((seg ^ ((r >> 1) & 3)) << 4));
+    }
+    // QKV: (batch, position) of this lane's first row, advanced by 8 rows a step
+    int qb = 0, qpos = 0;
+    if (p.kind == EPI_QKV_ROPE) {
+        const int row = row0 + (lane >> 2);
+        qb = row / p.S;
+        qpos = row - qb * p.S;
+    }
+#pragma unroll
+    for (int step = 0; step < 4; ++step) {
+        const int r = step * 8 + (lane >> 2);
+        const uint4 v = vs[step];
         const int row = row0 + r;
+        const int b = qb, pos = qpos;
+        if (p.kind == EPI_QKV_ROPE) {
+            qpos += 8;
+            while (qpos >= p.S) { qpos -= p.S; ++qb; }
+        }
         if (row >= p.M || ncol >= p.N) continue;
         __nv_bfloat16* d;
         if (p.kind == EPI_QKV_ROPE) {
-            const int b = row / p.S, s = row - b * p.S;
-            d = qbase + (((int64_t)b * qs.heads + qs.head) * p.S + s) * p.dh + qs.d0 + seg * 8;
+            d = qbase + (((int64_t)b * qs.heads + qs.head) * p.S + pos) * p.dh + qs.d0 + seg * 8;
         } else {
             d = static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * p.ldo + ncol;
         }
@@ -276,11 +301,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = (warp - 2) >> 2;             // the two warps of a quarter split the chunks
         const uint32_t stg = sOut + (uint32_t)((warp - 2) * kStageOutBytes);
         const bool obf = !(epi.kind == EPI_STORE_F32 || epi.kind == EPI_ACCUM_F32);
+        // QKV with d_head <= 64: every chunk this warp takes starts at the same
+        // offset inside its head (chunks step by 64 columns), so the thread's
+        // (cos, sin) pairs are the same for all of them.  They are loaded once per
+        // tile, before the accumulator wait, instead of once per chunk.
+        const bool rope_pre = epi.kind == EPI_QKV_ROPE && epi.dh <= 64;
+        const int rope_d0 = (half * 32) % epi.dh;
+        const int rot_cols = (epi.n_head + epi.n_kv_head) * epi.dh;   // q and k columns
+        float rcs[32];
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
             const int m0 = (t % num_m) * kBM;
             const int n0 = (t / num_m) * n_per_tile;
+            if (rope_pre) {
+                const int r = m0 + q * 32 + lane;
+                const int pos = (r < M ? r : 0) % epi.S;
+                load_vec<32>(epi.rope_cs + ((int64_t)pos * (epi.dh / 2) + rope_d0 / 2) * 2, rcs);
+            }
             // Lane 0 waits (bounded); the outcome is broadcast so the warp stays
             // converged for the .sync.aligned TMEM loads even on a timeout.
             int ok = 1;
@@ -305,7 +343,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     a[e] = __uint_as_float(ra[e]);
                     u[e] = __uint_as_float(ru[e]);
                 }
-                epi_compute<32>(epi, row, col, a, u, o);
+                if (rope_pre) {
+                    if (col < rot_cols) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float x0 = a[2 * j], x1 = a[2 * j + 1];
+                            o[2 * j] = x0 * rcs[2 * j] - x1 * rcs[2 * j + 1];
+                            o[2 * j + 1] = x0 * rcs[2 * j + 1] + x1 * rcs[2 * j];
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] = a[j];
+                    }
+                } else {
+                    epi_compute<32>(epi, row, col, a, u, o);
+                }
                 stage_row(stg, lane, o, obf);
                 __syncwarp();
                 flush_block(epi, stg, lane, row0, col);

@@ -213,4 +213,26 @@ cudaError_t launch_rope(void* x, const int32_t* pos, int B, int H, int S, int dh
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ self-test
+// One warp waits on an mbarrier that expects one arrival nobody makes; the
+// bounded wait gives up after limit_ns and latches TFM_ETIMEOUT.
+__global__ void k_selftest_wait(uint64_t limit_ns, int* err) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0) (void)mbar_wait(b, 0, err, &abort_flag, limit_ns);
+    __syncwarp();
+}
+
+cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t st) {
+    k_selftest_wait<<<1, 32, 0, st>>>(limit_ns, device_error_word());
+    return cudaGetLastError();
+}
+
 }  // namespace tfm

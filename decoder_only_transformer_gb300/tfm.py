@@ -59,6 +59,7 @@ _SIGS = {
     "tfm_forward_host": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
     "tfm_forward_graph": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
     "tfm_device_status": ([_V], _I32),
+    "tfm_selftest_wait_timeout": ([_I32, _V], _I32),
     "tfm_last_error": ([], ctypes.c_char_p),
     "tfm_destroy": ([_V], None),
     "tfm_embedding": ([_V, _V, _V, _I64, _I32, _I32, _I32, _V], _I32),
@@ -152,6 +153,11 @@ def weight_bytes(c: Config) -> int:
 
 def device_status():
     _check(load().tfm_device_status(None))
+
+
+def selftest_wait_timeout(limit_ms: int = 50, stream=None):
+    """Launch the failure-detection self-test (a wait that must time out)."""
+    _check(load().tfm_selftest_wait_timeout(limit_ms, _stream(stream)))
 
 
 class Model:

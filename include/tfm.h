@@ -165,6 +165,14 @@ tfm_status tfm_forward_host(void* handle, const int32_t* tokens_host, int32_t B,
  * handle may be NULL (component calls share the same word). */
 tfm_status tfm_device_status(void* handle);
 
+/* Self-test of the failure-detection path: launches one small kernel that waits
+ * on an mbarrier nothing will ever complete, with the same bounded-wait code as
+ * the pipelines but a limit of `limit_ms` milliseconds (1..2000).  The wait gives
+ * up, the kernel latches TFM_ETIMEOUT in the device error word and returns, so
+ * a following tfm_device_status() returns TFM_ETIMEOUT and the context stays
+ * usable.  No fault, trap or hang is involved. */
+tfm_status tfm_selftest_wait_timeout(int32_t limit_ms, void* stream);
+
 /* Thread-local text of the last error raised on this thread ("" if none). */
 const char* tfm_last_error(void);
 

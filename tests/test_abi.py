@@ -75,6 +75,8 @@ def test_null_arguments_are_rejected_on_the_host(lib):
     assert lib.tfm_rmsnorm(x, x, x, 4, 60, 1e-5, 1, None) == tfm.TFM_EINVAL      # D % 8
     assert lib.tfm_rmsnorm(ctypes.c_void_p(260), x, x, 4, 64, 1e-5, 1, None) == tfm.TFM_EINVAL  # align
     assert lib.tfm_swiglu_workspace_bytes(10, 16, tfm.TFM_BF16) == 320
+    assert lib.tfm_selftest_wait_timeout(0, None) == tfm.TFM_EINVAL
+    assert lib.tfm_selftest_wait_timeout(2001, None) == tfm.TFM_EINVAL
     lib.tfm_destroy(None)
 
 

@@ -74,6 +74,9 @@ def test_tiny_gqa_ragged_fp32():
 
 @pytest.mark.parametrize("name,B,S", [
     ("small", 2, 256), ("small", 1, 100), ("gpt2s", 1, 300), ("gqa", 1, 260), ("long", 1, 513),
+    # 32-row output blocks that span several sequences (the head-major scatter
+    # and RoPE positions wrap inside a block)
+    ("small", 9, 3), ("small", 5, 7), ("gpt2s", 3, 45), ("gqa", 2, 33),
 ])
 def test_bf16_reduced_shapes(name, B, S):
     cfg = workloads.get_config(name).replace(n_layer=2)
@@ -175,3 +178,21 @@ def test_forward_rejects_bad_arguments():
     with pytest.raises(tfm.TfmError):          # ld not a multiple of 4
         model.forward(tok, torch.empty(32, 23, device="cuda"))
     model.close()
+
+
+def test_bounded_wait_times_out_without_faulting():
+    """A wait nothing satisfies gives up, latches TFM_ETIMEOUT and the context survives."""
+    tfm.device_status()                        # nothing latched before
+    tfm.selftest_wait_timeout(50)
+    torch.cuda.synchronize()
+    with pytest.raises(tfm.TfmError) as ei:
+        tfm.device_status()
+    assert ei.value.status == tfm.TFM_ETIMEOUT
+    tfm.device_status()                        # reading the status clears it
+    # the context still runs work: a tiny forward matches the oracle afterwards
+    cfg = workloads.get_config("tiny")
+    w = workloads.make_weights(cfg)
+    tok = workloads.make_tokens(cfg, batch=1, seq=16)
+    got = run_model(cfg, w, tok)
+    ref = oracle.forward(tok, w, cfg)
+    assert rel_err(got, ref) < TOL["fp32"]
