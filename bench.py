@@ -56,6 +56,17 @@ def load_peaks():
             "source": "fallback"}
 
 
+# DRAM bytes (read + written) of one launch, from one ncu --set full capture of
+# the layer-0 launches (cold caches) of the kernels as they are now; an op
+# without an entry reports traffic null.
+DRAM_TRAFFIC = {
+    ("small", "qkv_rope_gemm"): 10.04e6, ("small", "attention"): 25.18e6,
+    ("small", "oproj_residual_gemm"): 25.73e6, ("small", "gateup_swiglu_gemm"): 11.19e6,
+    ("gqa", "qkv_rope_gemm"): 67.31e6, ("gqa", "attention"): 51.94e6,
+    ("gqa", "oproj_residual_gemm"): 126.73e6, ("gqa", "gateup_swiglu_gemm"): 148.57e6,
+}
+
+
 # ---------------------------------------------------------------- per-kernel work
 def kernel_work(cfg, B, S):
     """Algorithmic work of ONE launch of each kernel kind: ("tensor", flops) or
@@ -410,7 +421,9 @@ def main():
     dom = kernels[dom_name]
     roofline = {"kernel": dom_name, "bound": dom["bound"], "achieved": dom["achieved"],
                 "peak": peaks["bf16_tflops"] if dom["bound"] == "tensor" else peaks["hbm_gbs"],
-                "unit": dom["unit"], "frac": dom["frac"], "traffic": None,
+                "unit": dom["unit"], "frac": dom["frac"],
+                "traffic": DRAM_TRAFFIC.get((cfg.name, dom_name)),
+                "traffic_source": "ncu --set full of the layer-0 launch, cold caches, bytes per launch",
                 "peak_source": f"{peaks['source']} ({'bf16 burst' if dom['bound'] == 'tensor' else 'HBM copy'})",
                 "timing": "average launch duration from CUDA events recorded on the launch stream "
                           "after every kernel, over K directly launched steps run after the value region"}
