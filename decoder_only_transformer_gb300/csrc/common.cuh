@@ -113,6 +113,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* er
     }
 }
 
+// Every lane of a warp waits (bounded) on the barrier itself; the vote keeps the
+// warp converged for the .sync.aligned tensor-memory operations that follow and
+// turns a timeout in any lane into a timeout of the warp.  (Waiting in one lane,
+// broadcasting the outcome and then acquiring in every lane was measured to cost
+// ~80 cycles more per wait in the attention softmax loop.)
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* err,
+                                          volatile int* abort) {
+    const bool ok = mbar_wait(bar, parity, err, abort);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x,
                                             int32_t y, uint32_t bar) {

@@ -76,15 +76,6 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t swz, uint32_t
     return d;
 }
 
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int lane, int* err,
-                                          volatile int* abort) {
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait(bar, parity, err, abort) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) (void)mbar_try_wait(bar, parity);
-    return ok != 0;
-}
-
 template <int DH>
 __global__ void __launch_bounds__(kThreadsPP, 1)
     k_attention_pp(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -270,7 +261,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
         float m = -INFINITY, l = 0.f;
         bool ok = n > 0;
         for (int j = 0; j < n && ok; ++j) {
-            if (!warp_wait(s_full(x), (uint32_t)j & 1u, lane, err, abort_flag)) { ok = false; break; }
+            if (!warp_wait(s_full(x), (uint32_t)j & 1u, err, abort_flag)) { ok = false; break; }
             tc_fence_after();
             uint32_t sr[kKV / 32][32];
 #pragma unroll
@@ -307,7 +298,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
             }
             const bool need_rescale = __any_sync(0xffffffffu, corr != 1.f && j > 0);
             // P_x and O_x are free once O_x += P_x V_{j-1} has completed.
-            if (j >= 1 && !warp_wait(o_done(x), (uint32_t)(j - 1) & 1u, lane, err, abort_flag)) {
+            if (j >= 1 && !warp_wait(o_done(x), (uint32_t)(j - 1) & 1u, err, abort_flag)) {
                 ok = false;
                 break;
             }
@@ -352,7 +343,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full(x));
         }
-        if (ok && warp_wait(o_done(x), (uint32_t)(n - 1) & 1u, lane, err, abort_flag)) {
+        if (ok && warp_wait(o_done(x), (uint32_t)(n - 1) & 1u, err, abort_flag)) {
             tc_fence_after();
             const float inv = 1.0f / l;
             __nv_bfloat16* orow = o + ((int64_t)b * S + qi) * ((int64_t)H * DH) + (int64_t)h * DH;

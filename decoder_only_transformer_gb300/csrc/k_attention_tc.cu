@@ -58,16 +58,6 @@ struct AttTc {
     static constexpr int kBytes = kMiscOff + 16 + 1024;
 };
 
-// Bounded wait by lane 0, result broadcast, acquire in every lane.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int lane, int* err,
-                                          volatile int* abort) {
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait(bar, parity, err, abort) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) (void)mbar_try_wait(bar, parity);
-    return ok != 0;
-}
-
 template <int DH>
 __global__ void __launch_bounds__(kThreadsAtt, 1)
     k_attention_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -238,7 +228,7 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
         bool ok = true;
         for (int j = 0; j < n; ++j) {
             const int sb = j & 1;
-            if (!warp_wait(s_full(sb), (uint32_t)(j >> 1) & 1u, lane, err, abort_flag)) { ok = false; break; }
+            if (!warp_wait(s_full(sb), (uint32_t)(j >> 1) & 1u, err, abort_flag)) { ok = false; break; }
             tc_fence_after();
             // All four 32-column loads in flight before the single wait.
             uint32_t sr[kKV / 32][32];
@@ -275,7 +265,7 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
             }
             const bool need_rescale = __any_sync(0xffffffffu, corr != 1.f && j > 0);
             // P[sb] is free once P_{j-2} V_{j-2} has completed.
-            if (j >= 2 && !warp_wait(o_done(sb), (uint32_t)((j - 2) >> 1) & 1u, lane, err, abort_flag)) {
+            if (j >= 2 && !warp_wait(o_done(sb), (uint32_t)((j - 2) >> 1) & 1u, err, abort_flag)) {
                 ok = false;
                 break;
             }
@@ -308,7 +298,7 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
             l = l * corr + sum;
             if (need_rescale) {
                 // O must hold P_{j-1} V_{j-1} before it is rescaled.
-                if (!warp_wait(o_done((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, lane, err,
+                if (!warp_wait(o_done((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, err,
                                abort_flag)) {
                     ok = false;
                     break;
@@ -328,7 +318,7 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
             if (lane == 0) mbar_arrive(p_full(sb));
         }
         // Final: O / l, written with heads merged, o[b, s, h*DH + d].
-        if (ok && warp_wait(o_done((n - 1) & 1), (uint32_t)((n - 1) >> 1) & 1u, lane, err, abort_flag)) {
+        if (ok && warp_wait(o_done((n - 1) & 1), (uint32_t)((n - 1) >> 1) & 1u, err, abort_flag)) {
             tc_fence_after();
             const float inv = 1.0f / l;
             __nv_bfloat16* orow = o + ((int64_t)b * S + qi) * ((int64_t)H * DH) + (int64_t)h * DH;

@@ -319,13 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int pos = (r < M ? r : 0) % epi.S;
                 load_vec<32>(epi.rope_cs + ((int64_t)pos * (epi.dh / 2) + rope_d0 / 2) * 2, rcs);
             }
-            // Lane 0 waits (bounded); the outcome is broadcast so the warp stays
-            // converged for the .sync.aligned TMEM loads even on a timeout.
-            int ok = 1;
-            if (lane == 0) ok = mbar_wait(tfull_bar(acc), acc_phase, err, abort_flag) ? 1 : 0;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            (void)mbar_try_wait(tfull_bar(acc), acc_phase);   // acquire in every lane
+            if (!warp_wait(tfull_bar(acc), acc_phase, err, abort_flag)) break;
             tc_fence_after();
             const int row0 = m0 + q * 32;
             const int row = row0 + lane;
@@ -439,7 +433,9 @@ int choose_block_n(int M, int N, bool dual) {
     for (int bn : {256, 128}) {
         const int per = dual ? bn / 2 : bn;
         const int64_t tiles = (int64_t)num_m * ((N + per - 1) / per);
-        const double cost = (double)((tiles + sms - 1) / sms) * bn * (bn == 128 ? 1.25 : 1.0);
+        // A 128-wide tile was measured to take ~0.8 of a 256-wide one (the same
+        // A tile, fill and MMA issue per tile), so it wins only by saving a wave.
+        const double cost = (double)((tiles + sms - 1) / sms) * bn * (bn == 128 ? 1.6 : 1.0);
         if (best_cost < 0 || cost < best_cost) { best = bn; best_cost = cost; }
     }
     return best;
