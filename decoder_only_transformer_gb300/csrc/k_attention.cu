@@ -149,30 +149,36 @@ __global__ void __launch_bounds__(128) k_attention_mma(const __nv_bfloat16* __re
             }
         }
 
-        // Scale into the log2 domain; mask keys above the diagonal and past S.
-        const int key0 = j * kAttBN + 2 * (lane & 3);
-        float mx_lo = m_lo, mx_hi = m_hi;
+        // Mask keys above the diagonal and past S: only the diagonal tile and a
+        // tile reaching past S need it (warp-uniform test).
+        if (j == qt || (j + 1) * kAttBN > S) {
+            const int key0 = j * kAttBN + 2 * (lane & 3);
 #pragma unroll
-        for (int nb = 0; nb < 8; ++nb) {
+            for (int nb = 0; nb < 8; ++nb)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int key = key0 + nb * 8 + e;
-                float a = s[nb][e] * scale_log2, c = s[nb][2 + e] * scale_log2;
-                if (key > row_lo || key >= S) a = -INFINITY;
-                if (key > row_hi || key >= S) c = -INFINITY;
-                s[nb][e] = a;
-                s[nb][2 + e] = c;
-                mx_lo = fmaxf(mx_lo, a);
-                mx_hi = fmaxf(mx_hi, c);
-            }
+                for (int e = 0; e < 2; ++e) {
+                    const int key = key0 + nb * 8 + e;
+                    if (key > row_lo || key >= S) s[nb][e] = -INFINITY;
+                    if (key > row_hi || key >= S) s[nb][2 + e] = -INFINITY;
+                }
+        }
+        // Row max of the raw scores (the scale is positive, so it commutes with
+        // the max), three-input maxima, then across the four lanes of a row.
+        float mx_lo = fmaxf(s[0][0], s[0][1]), mx_hi = fmaxf(s[0][2], s[0][3]);
+#pragma unroll
+        for (int nb = 1; nb < 8; ++nb) {
+            mx_lo = fmax3(mx_lo, s[nb][0], s[nb][1]);
+            mx_hi = fmax3(mx_hi, s[nb][2], s[nb][3]);
         }
         mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
         mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
         mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
         mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+        mx_lo = fmaxf(m_lo, mx_lo * scale_log2);
+        mx_hi = fmaxf(m_hi, mx_hi * scale_log2);
         const float base_lo = (mx_lo == -INFINITY) ? 0.f : mx_lo;
         const float base_hi = (mx_hi == -INFINITY) ? 0.f : mx_hi;
-        const float corr_lo = exp2f(m_lo - base_lo), corr_hi = exp2f(m_hi - base_hi);
+        const float corr_lo = fast_exp2(m_lo - base_lo), corr_hi = fast_exp2(m_hi - base_hi);
         m_lo = mx_lo;
         m_hi = mx_hi;
         l_lo *= corr_lo;
@@ -182,12 +188,13 @@ __global__ void __launch_bounds__(128) k_attention_mma(const __nv_bfloat16* __re
             oacc[i][0] *= corr_lo; oacc[i][1] *= corr_lo;
             oacc[i][2] *= corr_hi; oacc[i][3] *= corr_hi;
         }
+        // p = 2^(s*scale - base): one FMA and one exponential per score.
 #pragma unroll
         for (int nb = 0; nb < 8; ++nb) {
-            s[nb][0] = exp2f(s[nb][0] - base_lo);
-            s[nb][1] = exp2f(s[nb][1] - base_lo);
-            s[nb][2] = exp2f(s[nb][2] - base_hi);
-            s[nb][3] = exp2f(s[nb][3] - base_hi);
+            s[nb][0] = fast_exp2(fmaf(s[nb][0], scale_log2, -base_lo));
+            s[nb][1] = fast_exp2(fmaf(s[nb][1], scale_log2, -base_lo));
+            s[nb][2] = fast_exp2(fmaf(s[nb][2], scale_log2, -base_hi));
+            s[nb][3] = fast_exp2(fmaf(s[nb][3], scale_log2, -base_hi));
             l_lo += s[nb][0] + s[nb][1];
             l_hi += s[nb][2] + s[nb][3];
         }
