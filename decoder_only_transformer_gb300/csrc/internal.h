@@ -50,6 +50,27 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// The same with a cluster of two CTAs along x (CTA pairs for cta_group::2).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl_pair(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                   cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Library-global device error word of the current device (see raise_error).
 int* device_error_word();
 // Sets the thread-local text tfm_last_error() returns.
@@ -86,6 +107,7 @@ struct GemmPlan {
     int M, N, K;          // N = GEMM columns covered by tiles (F for SwiGLU)
     int block_n;          // tile width (128 or 256); SwiGLU: gate+up halves of block_n/2
     int dual;             // SwiGLU: B tile = [W1 rows; W3 rows]
+    int pair;             // 1: CTA pairs (cta_group::2) on 256-row tiles
     EpiParams epi;
 };
 // Builds the tensor maps; returns TFM_OK or an error status with a message.

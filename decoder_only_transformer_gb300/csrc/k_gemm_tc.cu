@@ -39,9 +39,11 @@ constexpr int kEpiWarps = 8;             // two per TMEM lane quarter
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kStageOutBytes = 32 * 128; // one 32 x 32 block (fp32 rows of 128 B) per warp
 
-template <int BN, int STAGES>
+// kPair: a CTA pair shares one 256 x BN tile; each CTA holds 128 rows of A and
+// BN/2 rows of B per stage.
+template <int BN, int STAGES, bool kPair = false>
 struct TcSmem {
-    static constexpr int kTileBBytes = BN * kBK * 2;
+    static constexpr int kTileBBytes = (kPair ? BN / 2 : BN) * kBK * 2;
     static constexpr int kStageBytes = kTileABytes + kTileBBytes;
     static constexpr int kOutOffset = STAGES * kStageBytes;              // epilogue staging
     static constexpr int kBarOffset = kOutOffset + kEpiWarps * kStageOutBytes;
@@ -176,10 +178,10 @@ __device__ __forceinline__ void flush_block(const EpiParams& p, uint32_t buf, in
     }
 }
 
-template <int BN, int STAGES, bool kDual>
+template <int BN, int STAGES, bool kDual, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ TcMaps maps, int M, int N, int K, EpiParams epi, int* err) {
-    using L = TcSmem<BN, STAGES>;
+    using L = TcSmem<BN, STAGES, kPair>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -199,10 +201,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_per_tile = kDual ? BN / 2 : BN;
-    const int num_m = (M + kBM - 1) / kBM;
+    // A pair's tile has 256 rows: rank 0 holds rows [0, 128), rank 1 [128, 256).
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+    const int tile_rows = kPair ? 2 * kBM : kBM;
+    const int num_m = (M + tile_rows - 1) / tile_rows;
     const int num_n = (N + n_per_tile - 1) / n_per_tile;
     const int num_tiles = num_m * num_n;
     const int num_kb = (K + kBK - 1) / kBK;
+    const int unit = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;   // tile scheduler slot
+    const int units = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    const bool leader = rank == 0;
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -211,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), kEpiWarps);
+            mbar_init(tempty_bar(a), kPair ? 2 * kEpiWarps : kEpiWarps);   // both CTAs' epilogues
         }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
@@ -220,9 +228,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&maps.b);
         if (kDual) tma_prefetch_desc(&maps.b2);
     }
-    if (warp == 1) tmem_alloc(smem_u32(tmem_holder), 2 * BN);
+    if (warp == 1) {
+        if (kPair) tmem_alloc_pair(smem_u32(tmem_holder), 2 * BN);
+        else tmem_alloc(smem_u32(tmem_holder), 2 * BN);
+    }
     tc_fence_before();
-    __syncthreads();
+    // The pair's barriers must be initialised before either CTA signals the other's.
+    if (kPair) cluster_sync();
+    else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     // Everything above overlaps the previous kernel's tail; global memory only after.
@@ -236,27 +249,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const int m0 = (t % num_m) * kBM;
+            for (int t = unit; t < num_tiles && ok; t += units) {
+                const int m0 = (t % num_m) * tile_rows + (int)rank * kBM;
                 const int n0 = (t / num_m) * n_per_tile;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, err, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(full_bar(stage), L::kStageBytes);
                     const uint32_t sa = sA0 + stage * kTileABytes;
                     const uint32_t sb = sB0 + stage * L::kTileBBytes;
-                    tma_load_2d(sa, &maps.a, kb * kBK, m0, full_bar(stage));
-                    if (kDual) {
-                        tma_load_2d(sb, &maps.b, kb * kBK, n0, full_bar(stage));
-                        tma_load_2d(sb + (BN / 2) * kBK * 2, &maps.b2, kb * kBK, n0, full_bar(stage));
+                    if (kPair) {
+                        // Both CTAs' copies complete on the leader's full barrier; the
+                        // leader announces the bytes of both.
+                        const uint32_t fb = mapa_shared(full_bar(stage), 0);
+                        if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * L::kStageBytes);
+                        tma_load_2d_pair(sa, &maps.a, kb * kBK, m0, fb);
+                        if (kDual)   // rank 0: W1 rows, rank 1: W3 rows of the same columns
+                            tma_load_2d_pair(sb, leader ? &maps.b : &maps.b2, kb * kBK, n0, fb);
+                        else
+                            tma_load_2d_pair(sb, &maps.b, kb * kBK, n0 + (int)rank * (BN / 2), fb);
                     } else {
-                        tma_load_2d(sb, &maps.b, kb * kBK, n0, full_bar(stage));
+                        mbar_arrive_expect_tx(full_bar(stage), L::kStageBytes);
+                        tma_load_2d(sa, &maps.a, kb * kBK, m0, full_bar(stage));
+                        if (kDual) {
+                            tma_load_2d(sb, &maps.b, kb * kBK, n0, full_bar(stage));
+                            tma_load_2d(sb + (BN / 2) * kBK * 2, &maps.b2, kb * kBK, n0, full_bar(stage));
+                        } else {
+                            tma_load_2d(sb, &maps.b, kb * kBK, n0, full_bar(stage));
+                        }
                     }
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
-            // Drain: every armed stage's last phase must have landed before exit.
-            for (int s = 0; s < STAGES && issued > 0; ++s) {
+            // Drain: every armed stage's last phase must have landed before exit.  In
+            // a pair only the leader's full barriers exist; they count the peer's
+            // copies too, and the closing cluster barrier holds the peer until then.
+            for (int s = 0; s < STAGES && issued > 0 && leader; ++s) {
                 if (s >= issued) break;
                 const int64_t last = issued - 1 - ((issued - 1 - s) % STAGES);
                 mbar_wait(full_bar(s), (uint32_t)((last / STAGES) & 1), err, abort_flag);
@@ -264,12 +291,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = umma_idesc_bf16(kBM, BN);
+        // In a pair only the leader issues: M = 256 over both CTAs' operands;
+        // the commits arrive on the barriers of both CTAs.
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = umma_idesc_bf16(kPair ? 2 * kBM : kBM, BN);
+            constexpr uint16_t kBoth = 3;
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            for (int t = unit; t < num_tiles && ok; t += units) {
                 if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, err, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -282,17 +312,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 0; k < kBK / kUmmaK; ++k) {
                         const uint64_t ad = umma_desc_sw128(sa + k * kUmmaK * 2);
                         const uint64_t bd = umma_desc_sw128(sb + k * kUmmaK * 2);
-                        umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                        if (kPair) umma_bf16_pair(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                        else umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
                     }
-                    umma_commit(empty_bar(stage));
+                    if (kPair) umma_commit_pair(empty_bar(stage), kBoth);
+                    else umma_commit(empty_bar(stage));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                umma_commit(tfull_bar(acc));
+                if (kPair) umma_commit_pair(tfull_bar(acc), kBoth);
+                else umma_commit(tfull_bar(acc));
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
             // All MMAs this thread issued must be complete before TMEM is freed.
-            umma_commit(done_bar);
+            if (kPair) umma_commit_pair(done_bar, 1);
+            else umma_commit(done_bar);
             mbar_wait(done_bar, 0, err, abort_flag);
         }
     } else {
@@ -311,8 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         float rcs[32];
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-            const int m0 = (t % num_m) * kBM;
+        // Rank 1 releases the accumulator on the leader's barrier.
+        const uint32_t tempty0 = kPair ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
+        for (int t = unit; t < num_tiles; t += units) {
+            const int m0 = (t % num_m) * tile_rows + (int)rank * kBM;
             const int n0 = (t / num_m) * n_per_tile;
             if (rope_pre) {
                 const int r = m0 + q * 32 + lane;
@@ -373,15 +409,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (lane == 0) {
+                if (kPair) mbar_arrive_cluster(tempty0 + 8u * acc);
+                else mbar_arrive(tempty_bar(acc));
+            }
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
     }
 
     tc_fence_before();
-    __syncthreads();
+    // A pair frees its tensor memory together and neither CTA leaves while the
+    // other may still read its shared memory.
+    if (kPair) cluster_sync();
+    else __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, 2 * BN);
+    if (warp == 1) {
+        if (kPair) tmem_dealloc_pair(tmem_base, 2 * BN);
+        else tmem_dealloc(tmem_base, 2 * BN);
+    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -441,22 +486,27 @@ int choose_block_n(int M, int N, bool dual) {
     return best;
 }
 
-template <int BN, int STAGES, bool kDual>
+template <int BN, int STAGES, bool kDual, bool kPair = false>
 cudaError_t launch_inst(const GemmPlan& p, cudaStream_t st) {
-    using L = TcSmem<BN, STAGES>;
+    using L = TcSmem<BN, STAGES, kPair>;
     static_assert(L::kBytes <= 232448, "shared memory budget");
     static bool attr_set = false;   // per instantiation; set once per process
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, STAGES, kDual>,
+        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, STAGES, kDual, kPair>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     const int per = kDual ? BN / 2 : BN;
-    const int64_t tiles = (int64_t)((p.M + kBM - 1) / kBM) * ((p.N + per - 1) / per);
-    const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
-    return launch_pdl(k_gemm_tc<BN, STAGES, kDual>, dim3(grid), dim3(kThreads), L::kBytes, st,
-                      p.maps, p.M, p.N, p.K, p.epi, device_error_word());
+    const int rows = kPair ? 2 * kBM : kBM;
+    const int64_t tiles = (int64_t)((p.M + rows - 1) / rows) * ((p.N + per - 1) / per);
+    const int slots = kPair ? sm_count() / 2 : sm_count();
+    const int units = (int)(tiles < slots ? tiles : slots);
+    if (kPair)
+        return launch_pdl_pair(k_gemm_tc<BN, STAGES, kDual, kPair>, dim3(2 * units), dim3(kThreads),
+                               L::kBytes, st, p.maps, p.M, p.N, p.K, p.epi, device_error_word());
+    return launch_pdl(k_gemm_tc<BN, STAGES, kDual, kPair>, dim3(units), dim3(kThreads), L::kBytes,
+                      st, p.maps, p.M, p.N, p.K, p.epi, device_error_word());
 }
 
 }  // namespace
@@ -468,9 +518,21 @@ tfm_status plan_gemm_tc(GemmPlan* plan, const void* A, int64_t lda, const void* 
     plan->N = N;
     plan->K = K;
     plan->dual = dual ? 1 : 0;
-    plan->block_n = choose_block_n(M, N, dual);
+    // CTA pairs (256 x 256 tiles, half of B per SM): per k-block each SM holds
+    // 32 KB instead of 48 KB, so six stages are in flight and a long main loop
+    // keeps up with the tensor cores.  With a short K the tile time is set by the
+    // epilogue's stores, and the pair (whose accumulator is released only when
+    // both CTAs' epilogues are done) was measured slower; so pairs are used for
+    // K >= 2048, or K >= 1024 with many waves of tiles.
+    {
+        const int64_t pair_tiles = (int64_t)((M + 2 * kBM - 1) / (2 * kBM)) *
+                                   ((N + (dual ? 127 : 255)) / (dual ? 128 : 256));
+        const bool long_k = K >= 2048 || (K >= 1024 && pair_tiles >= 8LL * (sm_count() / 2));
+        plan->pair = (M > kBM && long_k) ? 1 : 0;
+    }
+    plan->block_n = plan->pair ? 256 : choose_block_n(M, N, dual);
     plan->epi = epi;
-    const int box_b = dual ? plan->block_n / 2 : plan->block_n;
+    const int box_b = (dual || plan->pair) ? plan->block_n / 2 : plan->block_n;
     if (!make_operand_map(&plan->maps.a, A, M, K, lda, kBM)) return TFM_ECUDA;
     if (!make_operand_map(&plan->maps.b, B, N, K, ldb, box_b)) return TFM_ECUDA;
     if (dual) {
@@ -483,6 +545,10 @@ tfm_status plan_gemm_tc(GemmPlan* plan, const void* A, int64_t lda, const void* 
 
 cudaError_t launch_gemm_tc(const GemmPlan& p, cudaStream_t st) {
     if (p.M <= 0 || p.N <= 0) return cudaSuccess;
+    if (p.pair) {
+        if (p.dual) return launch_inst<256, 6, true, true>(p, st);
+        return launch_inst<256, 6, false, true>(p, st);
+    }
     if (p.dual) {
         if (p.block_n == 256) return launch_inst<256, 4, true>(p, st);
         return launch_inst<128, 6, true>(p, st);
