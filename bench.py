@@ -61,9 +61,9 @@ def load_peaks():
 # without an entry reports traffic null.
 DRAM_TRAFFIC = {
     ("small", "qkv_rope_gemm"): 10.04e6, ("small", "attention"): 25.18e6,
-    ("small", "oproj_residual_gemm"): 25.73e6, ("small", "gateup_swiglu_gemm"): 11.19e6,
-    ("gqa", "qkv_rope_gemm"): 67.31e6, ("gqa", "attention"): 51.94e6,
-    ("gqa", "oproj_residual_gemm"): 126.73e6, ("gqa", "gateup_swiglu_gemm"): 148.57e6,
+    ("small", "oproj_residual_gemm"): 25.74e6, ("small", "gateup_swiglu_gemm"): 11.19e6,
+    ("gqa", "qkv_rope_gemm"): 68.94e6, ("gqa", "attention"): 52.12e6,
+    ("gqa", "oproj_residual_gemm"): 129.26e6, ("gqa", "gateup_swiglu_gemm"): 150.65e6,
 }
 
 

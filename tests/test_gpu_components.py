@@ -164,6 +164,8 @@ def test_attention_bf16_uniform_scores_prefix_mean():
 @pytest.mark.parametrize("M,N,K", [
     (128, 256, 64), (1, 64, 64), (100, 200, 72), (300, 1000, 512), (257, 384, 136),
     (1024, 2304, 768), (8192, 512, 512),
+    # long K: CTA-pair kernel (256-row tiles over two SMs); ragged M, N and K
+    (300, 1000, 2048), (257, 384, 2112), (2048, 768, 4096), (129, 256, 2048),
 ])
 def test_linear_bf16_fp32_out(M, N, K):
     r = rng(M + N + K)
@@ -205,7 +207,8 @@ def test_linear_fp32():
 
 # ---------------------------------------------------------------- SwiGLU
 @pytest.mark.parametrize("bf16", [False, True])
-@pytest.mark.parametrize("M,D,F", [(200, 64, 176), (1000, 512, 1344), (256, 768, 2048)])
+@pytest.mark.parametrize("M,D,F", [(200, 64, 176), (1000, 512, 1344), (256, 768, 2048),
+                                   (600, 2048, 1000)])   # gate/up with K = 2048: CTA pairs
 def test_swiglu(bf16, M, D, F):
     r = rng(M + F)
     cast = bf16_exact if bf16 else (lambda a: a)
