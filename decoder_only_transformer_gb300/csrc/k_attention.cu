@@ -11,8 +11,8 @@
 // value tiles of 64 rows are double-buffered in shared memory with cp.async
 // (zero-filled past the sequence end).  Both products run on the tensor cores
 // with mma.sync m16n8k16 (bf16 in, fp32 accumulate); the score fragments are
-// reused in registers as the A operand of P.V.  Heavy (late) query tiles are
-// scheduled first.
+// reused in registers as the A operand of P.V.  Heavy (late) query tiles of
+// every head are scheduled before any light one.
 #include "common.cuh"
 #include "internal.h"
 
@@ -79,8 +79,10 @@ __global__ void __launch_bounds__(128) k_attention_mma(const __nv_bfloat16* __re
     pdl_wait();
     pdl_trigger();
     const int num_qt = (S + kAttBM - 1) / kAttBM;
-    const int qt = num_qt - 1 - (int)blockIdx.x;            // heavy tiles first
-    const int bh = blockIdx.y, b = bh / H, h = bh - b * H;
+    // 1-D grid ordered heaviest first across all (sequence, head) (longest first).
+    const int BH = (int)gridDim.x / num_qt;
+    const int qt = num_qt - 1 - (int)blockIdx.x / BH;
+    const int bh = (int)blockIdx.x % BH, b = bh / H, h = bh - b * H;
     const int g = h / (H / Hkv);
     const __nv_bfloat16* qg = q + ((int64_t)(b * H + h) * S) * DH;
     const __nv_bfloat16* kg = k + ((int64_t)(b * Hkv + g) * S) * DH;
@@ -251,7 +253,7 @@ cudaError_t launch_dh(const void* q, const void* k, const void* v, void* o, int 
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    dim3 grid((S + kAttBM - 1) / kAttBM, B * H);
+    dim3 grid(((S + kAttBM - 1) / kAttBM) * B * H);
     return launch_pdl(k_attention_mma<DH>, grid, dim3(128), L::kBytes, st,
                       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
                       static_cast<const __nv_bfloat16*>(v), static_cast<__nv_bfloat16*>(o), H, Hkv,

@@ -105,12 +105,16 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_qt = (S + kQ - 1) / kQ;
     const int num_pairs = (num_qt + 1) / 2;
-    const int pair = num_pairs - 1 - (int)blockIdx.x;          // heavy pairs first
+    // 1-D grid ordered heaviest first across all (sequence, head): CTA i takes
+    // pair (num_pairs - 1 - i / BH) of head i % BH, so every head's late (long)
+    // pairs are dispatched before any short one (longest-first across the GPU).
+    const int BH = (int)gridDim.x / num_pairs;
+    const int pair = num_pairs - 1 - (int)blockIdx.x / BH;
     const int qA = 2 * pair, qB = 2 * pair + 1;
     const int nA = qA + 1;                                      // key tiles of tile A
     const int nB = qB < num_qt ? qB + 1 : 0;                    // 0: tile B does not exist
     const int nmax = nB > nA ? nB : nA;
-    const int bh = blockIdx.y, b = bh / H, h = bh - b * H;
+    const int bh = (int)blockIdx.x % BH, b = bh / H, h = bh - b * H;
     const int g = h / (H / Hkv);
 
     if (warp == 0 && lane == 0) {
@@ -384,7 +388,7 @@ cudaError_t launch_pp(const AttnPlan& p, cudaStream_t st) {
         attr_set = true;
     }
     const int num_qt = (p.S + kQ - 1) / kQ;
-    dim3 grid((num_qt + 1) / 2, p.B * p.H);
+    dim3 grid(((num_qt + 1) / 2) * p.B * p.H);
     return launch_pdl(k_attention_pp<DH>, grid, dim3(kThreadsPP), L::kBytes, st, p.qmap, p.kmap,
                       p.vmap, static_cast<__nv_bfloat16*>(p.o), p.H, p.Hkv, p.S,
                       p.scale * 1.4426950408889634f, device_error_word());

@@ -85,8 +85,11 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_qt = (S + kQ - 1) / kQ;
-    const int qt = num_qt - 1 - (int)blockIdx.x;      // heavy (late) tiles first
-    const int bh = blockIdx.y, b = bh / H, h = bh - b * H;
+    // 1-D grid ordered heaviest first across all (sequence, head): CTA i takes
+    // query tile (num_qt - 1 - i / BH) of head i % BH (longest first).
+    const int BH = (int)gridDim.x / num_qt;
+    const int qt = num_qt - 1 - (int)blockIdx.x / BH;
+    const int bh = (int)blockIdx.x % BH, b = bh / H, h = bh - b * H;
     const int g = h / (H / Hkv);
     const int n = qt + 1;                              // key tiles 0..qt
 
@@ -395,7 +398,7 @@ cudaError_t launch_tc(const AttnPlan& p, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    dim3 grid((p.S + kQ - 1) / kQ, p.B * p.H);
+    dim3 grid(((p.S + kQ - 1) / kQ) * p.B * p.H);
     return launch_pdl(k_attention_tc<DH>, grid, dim3(kThreadsAtt), L::kBytes, st, p.qmap, p.kmap,
                       p.vmap, static_cast<__nv_bfloat16*>(p.o), p.H, p.Hkv, p.S,
                       p.scale * 1.4426950408889634f, device_error_word());
