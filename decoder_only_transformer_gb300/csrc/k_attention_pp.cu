@@ -5,9 +5,12 @@
 // Same mathematics as k_attention_tc.cu (CS336 walkthrough, section 5.4;
 // "LLM 2", section GQA / MQA): o = softmax(q k^T / sqrt(dh) + M) v, online over
 // key tiles of 128 with a lazily rescaled running max.  What differs is the
-// schedule.  A CTA owns query tiles A = 2p and B = 2p + 1 of one (sequence,
-// head) and every key/value tile is loaded once for both:
-//   warp 0      TMA: Q_A and Q_B, then K_j and V_j into two rings
+// schedule.  A work item is the pair of query tiles A = 2p and B = 2p + 1 of one
+// (sequence, head), and every key/value tile is loaded once for both.  The
+// kernel is persistent: one CTA per SM walks a list of items (longest first
+// across all heads, dealt in snake order), with Q double-buffered so the next
+// item's loads overlap the current one's tail:
+//   warp 0      TMA: Q_A and Q_B of each item, then K_j and V_j into two rings
 //   warp 1      TMEM (S_A, S_B: 128 columns each; O_A, O_B: dh each; P_A, P_B:
 //               64 each) and the S MMAs: S_x = Q_x K_j^T for x = A, B
 //   warp 10     the P.V MMAs: O_x += P_x V_j, P_x read from tensor memory
@@ -41,21 +44,21 @@ constexpr float kRescaleThresholdPP = 8.0f;   // log2 units: P entries stay belo
 template <int DH>
 struct AttPP {
     static constexpr int kRowBytes = DH * 2;                 // 64 (dh 32) or 128 (dh 64)
-    static constexpr int kStages = 6;
+    static constexpr int kStages = DH == 64 ? 5 : 6;
     static constexpr int kQBytes = kQ * DH * 2;
     static constexpr int kKBytes = kKV * DH * 2;
     static constexpr int kVBytes = kKV * DH * 2;
-    static constexpr int kQOff = 0;                          // Q_A, Q_B
-    static constexpr int kKOff = kQOff + 2 * kQBytes;
+    static constexpr int kQOff = 0;                          // two buffers of Q_A, Q_B
+    static constexpr int kKOff = kQOff + 4 * kQBytes;
     static constexpr int kVOff = kKOff + kStages * kKBytes;
     static constexpr int kBarOff = kVOff + kStages * kVBytes;
     // Tensor-memory columns: S_A, S_B (128 each), O_A, O_B (DH each), then P_A,
     // P_B (64 each: 128 bf16 per row, two per 32-bit column).
     static constexpr int kOCol = 2 * kKV;
     static constexpr int kPCol = kOCol + 2 * DH;
-    // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], o_done[2],
-    // done, s_free[2]
-    static constexpr int kNumBars = 1 + 4 * kStages + 9;
+    // q_full[0], k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2],
+    // o_done[2], done, s_free[2], q_empty[2], q_full[1]
+    static constexpr int kNumBars = 1 + 4 * kStages + 12;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kBytes = kMiscOff + 16 + 1024;
     // Shared-memory descriptor swizzle of the Q/K/V tiles: 128-byte rows use the
@@ -79,8 +82,8 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t swz, uint32_t
 template <int DH>
 __global__ void __launch_bounds__(kThreadsPP, 1)
     k_attention_pp(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                   const __grid_constant__ CUtensorMap vmap, __nv_bfloat16* __restrict__ o, int H,
-                   int Hkv, int S, float scale_log2, int* err) {
+                   const __grid_constant__ CUtensorMap vmap, __nv_bfloat16* __restrict__ o, int BH,
+                   int H, int Hkv, int S, float scale_log2, int* err) {
     using L = AttPP<DH>;
     constexpr int ST = L::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -89,7 +92,9 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
     uint8_t* gbase = smem_raw + (base - raw);
     const uint32_t sQ = base + L::kQOff, sK = base + L::kKOff, sV = base + L::kVOff;
     const uint32_t bars = base + L::kBarOff;
-    const uint32_t q_full = bars;
+    // Q is double-buffered: item k uses buffer k % 2.
+    auto q_full = [&](int qb) { return qb == 0 ? bars : bars + 8u * (12 + 4 * ST); };
+    auto q_empty = [&](int qb) { return bars + 8u * (10 + 4 * ST + qb); };
     auto k_full = [&](int s) { return bars + 8u * (1 + s); };
     auto k_empty = [&](int s) { return bars + 8u * (1 + ST + s); };
     auto v_full = [&](int s) { return bars + 8u * (1 + 2 * ST + s); };
@@ -105,20 +110,38 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_qt = (S + kQ - 1) / kQ;
     const int num_pairs = (num_qt + 1) / 2;
-    // 1-D grid ordered heaviest first across all (sequence, head): CTA i takes
-    // pair (num_pairs - 1 - i / BH) of head i % BH, so every head's late (long)
-    // pairs are dispatched before any short one (longest-first across the GPU).
-    const int BH = (int)gridDim.x / num_pairs;
-    const int pair = num_pairs - 1 - (int)blockIdx.x / BH;
-    const int qA = 2 * pair, qB = 2 * pair + 1;
-    const int nA = qA + 1;                                      // key tiles of tile A
-    const int nB = qB < num_qt ? qB + 1 : 0;                    // 0: tile B does not exist
-    const int nmax = nB > nA ? nB : nA;
-    const int bh = (int)blockIdx.x % BH, b = bh / H, h = bh - b * H;
-    const int g = h / (H / Hkv);
+    const int total = num_pairs * BH;
+    // Persistent: work items (pair p of (sequence, head) bh) are numbered longest
+    // first across all heads, item i = (pair num_pairs-1 - i/BH, head i%BH), and
+    // dealt to the CTAs round by round in snake order (even rounds c, odd rounds
+    // G-1-c), which keeps the sum of item lengths per CTA even.  Every role walks
+    // the same sequence; barrier phases follow running counters across items.
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    struct Item {
+        int qA, qB, n[2], nmax, b, h, g;
+    };
+    auto item_of = [&](int rnd, Item& it) -> bool {
+        const int idx = rnd * G + ((rnd & 1) ? G - 1 - c : c);
+        if (idx >= total) return false;
+        const int pair = num_pairs - 1 - idx / BH;
+        const int bh = idx % BH;
+        it.b = bh / H;
+        it.h = bh - it.b * H;
+        it.g = it.h / (H / Hkv);
+        it.qA = 2 * pair;
+        it.qB = 2 * pair + 1;
+        it.n[0] = it.qA + 1;                                     // key tiles of tile A
+        it.n[1] = it.qB < num_qt ? it.qB + 1 : 0;                // 0: tile B does not exist
+        it.nmax = it.n[1] > it.n[0] ? it.n[1] : it.n[0];
+        return true;
+    };
+    const int rounds = (total + G - 1) / G;
 
     if (warp == 0 && lane == 0) {
-        mbar_init(q_full, 1);
+        for (int qb = 0; qb < 2; ++qb) {
+            mbar_init(q_full(qb), 1);
+            mbar_init(q_empty(qb), 1);
+        }
         for (int s = 0; s < ST; ++s) {
             mbar_init(k_full(s), 1);
             mbar_init(k_empty(s), 1);
@@ -148,33 +171,48 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
 
     constexpr uint32_t idesc_s = umma_idesc_bf16(kQ, kKV);
     constexpr uint32_t idesc_o = umma_idesc_bf16(kQ, DH, true);
-    const int n_of[2] = {nA, nB};
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
-        // Q_A, Q_B, then K_j and V_j into their rings.  Before exiting it waits for
-        // its last load into every slot, so no copy is in flight when the CTA ends.
+        // Per item k: Q_A and Q_B into Q buffer k % 2 (once item k-2's S MMAs are
+        // done with it), then K_j and V_j into the two rings, which run on across
+        // items, so the next item's loads overlap this item's tail.  Before exiting
+        // it waits for its last load into every slot, so no copy is in flight when
+        // the CTA ends.
         if (lane == 0) {
-            mbar_arrive_expect_tx(q_full, 2 * L::kQBytes);
-            tma_load_3d(sQ, &qmap, 0, qA * kQ, b * H + h, q_full);
-            tma_load_3d(sQ + L::kQBytes, &qmap, 0, qB * kQ, b * H + h, q_full);
-            int issued = 0;
-            for (int j = 0; j < nmax; ++j) {
-                const int st = j % ST;
-                const uint32_t ph = ((uint32_t)(j / ST) & 1u) ^ 1u;
-                if (!mbar_wait(k_empty(st), ph, err, abort_flag)) break;
-                mbar_arrive_expect_tx(k_full(st), L::kKBytes);
-                tma_load_3d(sK + st * L::kKBytes, &kmap, 0, j * kKV, b * Hkv + g, k_full(st));
-                if (!mbar_wait(v_empty(st), ph, err, abort_flag)) {
-                    mbar_wait(k_full(st), (uint32_t)((j / ST) & 1), err, abort_flag);
+            int kv = 0, items = 0;
+            bool ok = true;
+            Item it;
+            for (int rnd = 0; rnd < rounds && ok; ++rnd) {
+                if (!item_of(rnd, it)) continue;
+                const int qb = items & 1;
+                if (items >= 2 &&
+                    !mbar_wait(q_empty(qb), (uint32_t)((items >> 1) - 1) & 1u, err, abort_flag))
                     break;
+                const uint32_t sq = sQ + qb * 2 * L::kQBytes;
+                mbar_arrive_expect_tx(q_full(qb), 2 * L::kQBytes);
+                tma_load_3d(sq, &qmap, 0, it.qA * kQ, it.b * H + it.h, q_full(qb));
+                tma_load_3d(sq + L::kQBytes, &qmap, 0, it.qB * kQ, it.b * H + it.h, q_full(qb));
+                ++items;
+                for (int j = 0; j < it.nmax; ++j) {
+                    const int st = kv % ST;
+                    const uint32_t ph = ((uint32_t)(kv / ST) & 1u) ^ 1u;
+                    if (!mbar_wait(k_empty(st), ph, err, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(k_full(st), L::kKBytes);
+                    tma_load_3d(sK + st * L::kKBytes, &kmap, 0, j * kKV, it.b * Hkv + it.g, k_full(st));
+                    if (!mbar_wait(v_empty(st), ph, err, abort_flag)) {
+                        mbar_wait(k_full(st), (uint32_t)((kv / ST) & 1), err, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(v_full(st), L::kVBytes);
+                    tma_load_3d(sV + st * L::kVBytes, &vmap, 0, j * kKV, it.b * Hkv + it.g, v_full(st));
+                    ++kv;
                 }
-                mbar_arrive_expect_tx(v_full(st), L::kVBytes);
-                tma_load_3d(sV + st * L::kVBytes, &vmap, 0, j * kKV, b * Hkv + g, v_full(st));
-                ++issued;
             }
-            mbar_wait(q_full, 0, err, abort_flag);
-            for (int s = 0; s < ST && s < issued; ++s) {
-                const int last = issued - 1 - ((issued - 1 - s) % ST);
+            for (int k = items - 2 < 0 ? 0 : items - 2; k < items; ++k)
+                mbar_wait(q_full(k & 1), (uint32_t)(k >> 1) & 1u, err, abort_flag);
+            for (int s = 0; s < ST && s < kv; ++s) {
+                const int last = kv - 1 - ((kv - 1 - s) % ST);
                 mbar_wait(k_full(s), (uint32_t)((last / ST) & 1), err, abort_flag);
                 mbar_wait(v_full(s), (uint32_t)((last / ST) & 1), err, abort_flag);
             }
@@ -191,11 +229,13 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
         // below 256 KB, so the 14-bit field never carries).
         if (lane == 0) {
             bool ok = true;
+            int kv = 0, items = 0, cnt[2] = {0, 0};   // K/V tiles, items, MMAs per tile x
+            Item it;
             if (warp == 1) {
                 const uint64_t dq = sdesc(sQ, L::kSwz, 16, L::kGroup);
                 const uint64_t dk = sdesc(sK, L::kSwz, 16, L::kGroup);
-                auto issue_s = [&](int x, int st) {
-                    const uint64_t a0 = dq + (uint64_t)(x * (L::kQBytes >> 4));
+                auto issue_s = [&](int qb, int x, int st) {
+                    const uint64_t a0 = dq + (uint64_t)((qb * 2 + x) * (L::kQBytes >> 4));
                     const uint64_t b0 = dk + (uint64_t)(st * (L::kKBytes >> 4));
                     const uint32_t t_s = tmem_base + x * kKV;
 #pragma unroll
@@ -203,21 +243,31 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                         umma_bf16(t_s, a0 + 2 * kk, b0 + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
                     umma_commit(s_full(x));
                 };
-                ok = mbar_wait(q_full, 0, err, abort_flag);
-                for (int j = 0; j < nmax && ok; ++j) {
-                    const int st = j % ST;
-                    ok = mbar_wait(k_full(st), (uint32_t)(j / ST) & 1u, err, abort_flag);
-                    for (int x = 0; x < 2 && ok; ++x) {
-                        if (j >= n_of[x]) continue;
-                        // S_x is free once the softmax has read the previous tile's
-                        // scores into registers.
-                        if (j > 0) ok = mbar_wait(s_free(x), (uint32_t)(j - 1) & 1u, err, abort_flag);
-                        if (ok) {
-                            tc_fence_after();
-                            issue_s(x, st);
+                for (int rnd = 0; rnd < rounds && ok; ++rnd) {
+                    if (!item_of(rnd, it)) continue;
+                    const int qb = items & 1;
+                    ok = mbar_wait(q_full(qb), (uint32_t)(items >> 1) & 1u, err, abort_flag);
+                    for (int j = 0; j < it.nmax && ok; ++j) {
+                        const int st = kv % ST;
+                        ok = mbar_wait(k_full(st), (uint32_t)(kv / ST) & 1u, err, abort_flag);
+                        for (int x = 0; x < 2 && ok; ++x) {
+                            if (j >= it.n[x]) continue;
+                            // S_x is free once the softmax has read the previous
+                            // scores into registers (possibly of the previous item).
+                            if (cnt[x] > 0)
+                                ok = mbar_wait(s_free(x), (uint32_t)(cnt[x] - 1) & 1u, err, abort_flag);
+                            if (ok) {
+                                tc_fence_after();
+                                issue_s(qb, x, st);
+                                ++cnt[x];
+                            }
                         }
+                        if (ok) umma_commit(k_empty(st));
+                        ++kv;
                     }
-                    if (ok) umma_commit(k_empty(st));
+                    // Q buffer qb may be refilled once this item's S MMAs are complete.
+                    if (ok) umma_commit(q_empty(qb));
+                    ++items;
                 }
             } else {
                 const uint64_t dv = sdesc(sV, L::kSwz, 0, L::kGroup);
@@ -231,18 +281,26 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                                      idesc_o, (!first || kk > 0) ? 1u : 0u);
                     umma_commit(o_done(x));
                 };
-                for (int j = 0; j < nmax && ok; ++j) {
-                    const int st = j % ST;
-                    ok = mbar_wait(v_full(st), (uint32_t)(j / ST) & 1u, err, abort_flag);
-                    for (int x = 0; x < 2 && ok; ++x) {
-                        if (j >= n_of[x]) continue;
-                        ok = mbar_wait(p_full(x), (uint32_t)j & 1u, err, abort_flag);
-                        if (ok) {
-                            tc_fence_after();
-                            issue_pv(x, st, j == 0);
+                for (int rnd = 0; rnd < rounds && ok; ++rnd) {
+                    if (!item_of(rnd, it)) continue;
+                    for (int j = 0; j < it.nmax && ok; ++j) {
+                        const int st = kv % ST;
+                        ok = mbar_wait(v_full(st), (uint32_t)(kv / ST) & 1u, err, abort_flag);
+                        for (int x = 0; x < 2 && ok; ++x) {
+                            if (j >= it.n[x]) continue;
+                            // The first P of an item is written only after the
+                            // softmax has read the previous item's O_x, so the
+                            // overwrite (first = true) cannot race that read.
+                            ok = mbar_wait(p_full(x), (uint32_t)cnt[x] & 1u, err, abort_flag);
+                            if (ok) {
+                                tc_fence_after();
+                                issue_pv(x, st, j == 0);
+                                ++cnt[x];
+                            }
                         }
+                        if (ok) umma_commit(v_empty(st));
+                        ++kv;
                     }
-                    if (ok) umma_commit(v_empty(st));
                 }
             }
             // Every MMA this thread issued must be complete before TMEM is freed
@@ -255,117 +313,129 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
         const int x = (warp - 2) >> 2;                 // 0: tile A, 1: tile B
         const int q4 = warp & 3;
         const int r = q4 * 32 + lane;
-        const int qt = x == 0 ? qA : qB;
-        const int n = x == 0 ? nA : nB;
-        const int qi = qt * kQ + r;
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const uint32_t t_s = tmem_base + x * kKV + lane_off;
         const uint32_t t_o = tmem_base + L::kOCol + x * DH + lane_off;
         const uint32_t t_p = tmem_base + L::kPCol + x * (kKV / 2) + lane_off;
-        float m = -INFINITY, l = 0.f;
-        bool ok = n > 0;
-        for (int j = 0; j < n && ok; ++j) {
-            if (!warp_wait(s_full(x), (uint32_t)j & 1u, err, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            uint32_t sr[kKV / 32][32];
-#pragma unroll
-            for (int c = 0; c < kKV / 32; ++c) tmem_ld32_issue(t_s + c * 32, sr[c]);
-            tmem_ld_wait();
-            // S_x is in registers: the tensor cores may overwrite it with the next tile.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free(x));
-            float s[kKV];
-#pragma unroll
-            for (int c = 0; c < kKV / 32; ++c) {
-                reg_fence32(sr[c]);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[c][e]);
-            }
-            const int k0 = j * kKV;
-            if (j == qt || k0 + kKV > S) {
-#pragma unroll
-                for (int c = 0; c < kKV; ++c)
-                    if (k0 + c > qi || k0 + c >= S) s[c] = -INFINITY;
-            }
-            // Row max: four independent chains of three-input maxima.
-            float mx4[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-            for (int c = 4; c < kKV; c += 8)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) mx4[e] = fmax3(mx4[e], s[c + 2 * e], s[c + 2 * e + 1]);
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
-            float corr = 1.f;
-            if (mx > m + kRescaleThresholdPP) {
-                corr = fast_exp2(m - mx);
-                m = mx;
-            }
-            const bool need_rescale = __any_sync(0xffffffffu, corr != 1.f && j > 0);
-            // P_x and O_x are free once O_x += P_x V_{j-1} has completed.
-            if (j >= 1 && !warp_wait(o_done(x), (uint32_t)(j - 1) & 1u, err, abort_flag)) {
-                ok = false;
-                break;
-            }
-            // p = 2^(s*scale - m): scale and offset as packed pairs, one exponential
-            // per element, row sum in four packed accumulators; P goes to tensor
-            // memory as bf16 pairs, 64 keys (32 columns) per store.
-            const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
-            const uint64_t negm2 = f2_pack(-m, -m);
-            uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-            for (int h64 = 0; h64 < kKV / 64; ++h64) {
-                uint32_t pw[32];
-#pragma unroll
-                for (int e = 0; e < 64; e += 2) {
-                    float t0, t1;
-                    const int c = h64 * 64 + e;
-                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), scale2, negm2), t0, t1);
-                    const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
-                    sum2[(e >> 1) & 3] = f2_add(sum2[(e >> 1) & 3], f2_pack(p0, p1));
-                    pw[e >> 1] = pack_bf16x2(p0, p1);
-                }
-                tmem_st32_async(t_p + h64 * 32, pw);
-            }
-            tmem_st_wait();
-            float sa[4], sb[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) f2_unpack(sum2[e], sa[e], sb[e]);
-            const float sum = ((sa[0] + sb[0]) + (sa[1] + sb[1])) + ((sa[2] + sb[2]) + (sa[3] + sb[3]));
-            l = l * corr + sum;
-            if (need_rescale) {
+        int cnt = 0;                                   // tiles of this x processed so far
+        bool ok = true;
+        Item it;
+        for (int rnd = 0; rnd < rounds && ok; ++rnd) {
+            if (!item_of(rnd, it)) continue;
+            const int n = it.n[x];
+            if (n == 0) continue;
+            const int qt = x == 0 ? it.qA : it.qB;
+            const int qi = qt * kQ + r;
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < n && ok; ++j, ++cnt) {
+                if (!warp_wait(s_full(x), (uint32_t)cnt & 1u, err, abort_flag)) { ok = false; break; }
                 tc_fence_after();
+                uint32_t sr[kKV / 32][32];
 #pragma unroll
-                for (int c = 0; c < DH / 32; ++c) {
-                    float v[32];
-                    tmem_ld32(t_o + c * 32, v);
+                for (int cc = 0; cc < kKV / 32; ++cc) tmem_ld32_issue(t_s + cc * 32, sr[cc]);
+                tmem_ld_wait();
+                // S_x is in registers: the tensor cores may overwrite it with the next tile.
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_free(x));
+                float s[kKV];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] *= corr;
-                    tmem_st32(t_o + c * 32, v);
+                for (int cc = 0; cc < kKV / 32; ++cc) {
+                    reg_fence32(sr[cc]);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) s[cc * 32 + e] = __uint_as_float(sr[cc][e]);
                 }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_full(x));
-        }
-        if (ok && warp_wait(o_done(x), (uint32_t)(n - 1) & 1u, err, abort_flag)) {
-            tc_fence_after();
-            const float inv = 1.0f / l;
-            __nv_bfloat16* orow = o + ((int64_t)b * S + qi) * ((int64_t)H * DH) + (int64_t)h * DH;
+                const int k0 = j * kKV;
+                if (j == qt || k0 + kKV > S) {
 #pragma unroll
-            for (int c = 0; c < DH / 32; ++c) {
-                float v[32];
-                tmem_ld32(t_o + c * 32, v);
-                if (qi < S) {
+                    for (int cc = 0; cc < kKV; ++cc)
+                        if (k0 + cc > qi || k0 + cc >= S) s[cc] = -INFINITY;
+                }
+                // Row max: four independent chains of three-input maxima.
+                float mx4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 w;
-                        w.x = pack_bf16x2(v[e] * inv, v[e + 1] * inv);
-                        w.y = pack_bf16x2(v[e + 2] * inv, v[e + 3] * inv);
-                        w.z = pack_bf16x2(v[e + 4] * inv, v[e + 5] * inv);
-                        w.w = pack_bf16x2(v[e + 6] * inv, v[e + 7] * inv);
-                        *reinterpret_cast<uint4*>(orow + c * 32 + e) = w;
+                for (int cc = 4; cc < kKV; cc += 8)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) mx4[e] = fmax3(mx4[e], s[cc + 2 * e], s[cc + 2 * e + 1]);
+                const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
+                float corr = 1.f;
+                if (mx > m + kRescaleThresholdPP) {
+                    corr = fast_exp2(m - mx);
+                    m = mx;
+                }
+                const bool need_rescale = __any_sync(0xffffffffu, corr != 1.f && j > 0);
+                // P_x and O_x are free once the previous O_x += P_x V (possibly of the
+                // previous item) has completed.
+                if (cnt > 0 && !warp_wait(o_done(x), (uint32_t)(cnt - 1) & 1u, err, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                // p = 2^(s*scale - m): scale and offset as packed pairs, one exponential
+                // per element, row sum in four packed accumulators; P goes to tensor
+                // memory as bf16 pairs, 64 keys (32 columns) per store.
+                const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
+                const uint64_t negm2 = f2_pack(-m, -m);
+                uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+                for (int h64 = 0; h64 < kKV / 64; ++h64) {
+                    uint32_t pw[32];
+#pragma unroll
+                    for (int e = 0; e < 64; e += 2) {
+                        float t0, t1;
+                        const int cc = h64 * 64 + e;
+                        f2_unpack(f2_fma(f2_pack(s[cc], s[cc + 1]), scale2, negm2), t0, t1);
+                        const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+                        sum2[(e >> 1) & 3] = f2_add(sum2[(e >> 1) & 3], f2_pack(p0, p1));
+                        pw[e >> 1] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32_async(t_p + h64 * 32, pw);
+                }
+                tmem_st_wait();
+                float sa[4], sb[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) f2_unpack(sum2[e], sa[e], sb[e]);
+                const float sum = ((sa[0] + sb[0]) + (sa[1] + sb[1])) + ((sa[2] + sb[2]) + (sa[3] + sb[3]));
+                l = l * corr + sum;
+                if (need_rescale) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int cc = 0; cc < DH / 32; ++cc) {
+                        float v[32];
+                        tmem_ld32(t_o + cc * 32, v);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] *= corr;
+                        tmem_st32(t_o + cc * 32, v);
                     }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full(x));
+            }
+            // O_x of this item is complete after its last P.V; read it out before
+            // the next item's first P is published (its P.V overwrites O_x).
+            if (ok && warp_wait(o_done(x), (uint32_t)(cnt - 1) & 1u, err, abort_flag)) {
+                tc_fence_after();
+                const float inv = 1.0f / l;
+                __nv_bfloat16* orow =
+                    o + ((int64_t)it.b * S + qi) * ((int64_t)H * DH) + (int64_t)it.h * DH;
+#pragma unroll
+                for (int cc = 0; cc < DH / 32; ++cc) {
+                    float v[32];
+                    tmem_ld32(t_o + cc * 32, v);
+                    if (qi < S) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 8) {
+                            uint4 w;
+                            w.x = pack_bf16x2(v[e] * inv, v[e + 1] * inv);
+                            w.y = pack_bf16x2(v[e + 2] * inv, v[e + 3] * inv);
+                            w.z = pack_bf16x2(v[e + 4] * inv, v[e + 5] * inv);
+                            w.w = pack_bf16x2(v[e + 6] * inv, v[e + 7] * inv);
+                            *reinterpret_cast<uint4*>(orow + cc * 32 + e) = w;
+                        }
+                    }
+                }
+            } else {
+                ok = false;
             }
         }
     }
@@ -387,11 +457,13 @@ cudaError_t launch_pp(const AttnPlan& p, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
+    // One CTA per SM (shared memory allows no more), each looping over items.
     const int num_qt = (p.S + kQ - 1) / kQ;
-    dim3 grid(((num_qt + 1) / 2) * p.B * p.H);
-    return launch_pdl(k_attention_pp<DH>, grid, dim3(kThreadsPP), L::kBytes, st, p.qmap, p.kmap,
-                      p.vmap, static_cast<__nv_bfloat16*>(p.o), p.H, p.Hkv, p.S,
-                      p.scale * 1.4426950408889634f, device_error_word());
+    const int items = ((num_qt + 1) / 2) * p.B * p.H;
+    const int grid = items < sm_count() ? items : sm_count();
+    return launch_pdl(k_attention_pp<DH>, dim3(grid), dim3(kThreadsPP), L::kBytes, st, p.qmap,
+                      p.kmap, p.vmap, static_cast<__nv_bfloat16*>(p.o), p.B * p.H, p.H, p.Hkv,
+                      p.S, p.scale * 1.4426950408889634f, device_error_word());
 }
 
 }  // namespace
