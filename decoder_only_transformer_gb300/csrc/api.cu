@@ -494,10 +494,16 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
         if (!ev) return fail(TFM_ECUDA, "cudaEventCreate failed");
         cudaEventRecord(ev, st);
     }
-    TFM_LAUNCH(K_EMBED, launch_embedding(tokens, m->embed, m->h(), M, c.vocab, c.d_model, bf, st));
+    // Embedding and the first norm (layer 0's input norm, or the final norm of a
+    // model without layers) in one pass.
+    TFM_LAUNCH(K_EMBED, launch_embed_rmsnorm(tokens, m->embed,
+                                             c.n_layer > 0 ? m->attn_norm[0] : m->final_norm,
+                                             m->h(), m->xn(), M, c.vocab, c.d_model, c.norm_eps,
+                                             bf, st));
     if (bf) {
         for (int l = 0; l < c.n_layer; ++l) {
-            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 1, st));
+            if (l > 0)
+                TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 1, st));
             TFM_LAUNCH(K_QKV, launch_gemm_tc(m->p_qkv[l], st));
             if (m->attn_tc)
                 TFM_LAUNCH(K_ATTN, launch_attention_tc(m->p_attn, st));
@@ -509,12 +515,14 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
             TFM_LAUNCH(K_GATEUP, launch_gemm_tc(m->p_gu[l], st));
             TFM_LAUNCH(K_DOWN, launch_gemm_tc(m->p_down[l], st));
         }
-        TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->final_norm, m->xn(), M, c.d_model, c.norm_eps, 1, st));
+        if (c.n_layer > 0)
+            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->final_norm, m->xn(), M, c.d_model, c.norm_eps, 1, st));
         TFM_LAUNCH(K_LMHEAD, launch_gemm_tc(m->p_lm, st));
     } else {
         const float* xn = static_cast<const float*>(m->xn());
         for (int l = 0; l < c.n_layer; ++l) {
-            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 0, st));
+            if (l > 0)
+                TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 0, st));
             TFM_LAUNCH(K_QKV, launch_gemm_simt(xn, static_cast<const float*>(m->wqkv[l]), nullptr, M,
                                                (int)s.Nqkv, c.d_model, epi_qkv(m, M, S), st));
             TFM_LAUNCH(K_ATTN, launch_attention_simt(static_cast<const float*>(m->q()),
@@ -537,7 +545,8 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
                                                 c.d_model, c.d_ff,
                                                 epi_basic(EPI_ACCUM_F32, M, c.d_model, m->h(), s.D), st));
         }
-        TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->final_norm, m->xn(), M, c.d_model, c.norm_eps, 0, st));
+        if (c.n_layer > 0)
+            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->final_norm, m->xn(), M, c.d_model, c.norm_eps, 0, st));
         TFM_LAUNCH(K_LMHEAD, launch_gemm_simt(xn, static_cast<const float*>(m->lm_head), nullptr, M,
                                               c.vocab, c.d_model,
                                               epi_basic(EPI_STORE_F32, M, c.vocab, logits, ld), st));
@@ -670,7 +679,7 @@ tfm_status tfm_profile_read(void* handle, double* ms, int64_t* launches) {
 }
 
 const char* tfm_profile_kind_name(int32_t kind) {
-    static const char* names[TFM_PROFILE_KINDS] = {"embedding", "rmsnorm", "qkv_rope_gemm",
+    static const char* names[TFM_PROFILE_KINDS] = {"embedding_rmsnorm", "rmsnorm", "qkv_rope_gemm",
                                                    "attention", "oproj_residual_gemm",
                                                    "gateup_swiglu_gemm", "down_residual_gemm",
                                                    "lmhead_gemm"};

@@ -86,6 +86,10 @@ cudaError_t launch_rmsnorm(const float* x, const float* g, void* y, int64_t M, i
 cudaError_t launch_rope(void* x, const int32_t* pos, int B, int H, int S, int dh, float theta,
                         int is_bf16, cudaStream_t st);
 cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t st);
+// h = E[tok] and y = RMSNorm(h) * g in one pass (bf16: E and y bf16; else fp32).
+cudaError_t launch_embed_rmsnorm(const int32_t* tok, const void* E, const float* g, float* h,
+                                 void* y, int64_t M, int V, int D, float eps, int bf16,
+                                 cudaStream_t st);
 
 // ---- CUDA-core kernels (k_simt.cu), fp32 mode
 // C = A[M,K] . B[N,K]^T (and A . B2^T for EPI_SWIGLU), then the epilogue.

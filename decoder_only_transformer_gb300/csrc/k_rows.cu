@@ -59,6 +59,97 @@ cudaError_t launch_embedding(const int32_t* tok, const void* E, float* h, int64_
                       D, device_error_word());
 }
 
+// ------------------------------------------------------------------ embedding + RMSNorm
+// The forward's first two steps in one pass: h[m] = E[tok[m]] (fp32 residual
+// stream) and y[m] = h[m] / sqrt(mean(h[m]^2) + eps) * g (the first block's
+// input norm), the row held in registers in between.  One warp per row; lane l
+// owns the 4-float groups l, l+32, ...; an id outside [0, V) writes zeros and
+// raises TFM_EBADTOKEN.
+template <int kV, bool kBf16E, bool kBf16Y>
+__global__ void __launch_bounds__(256) k_embed_rmsnorm(const int32_t* __restrict__ tok,
+                                                       const void* __restrict__ E,
+                                                       const float* __restrict__ g,
+                                                       float* __restrict__ h, void* __restrict__ y,
+                                                       int64_t M, int V, int D, float eps,
+                                                       int* err) {
+    const int lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
+    const int64_t m = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (m >= M) return;
+    const int n4 = D >> 2;
+    const int t = __ldg(tok + m);
+    const bool ok = (t >= 0 && t < V);
+    if (!ok && lane == 0) raise_error(err, TFM_EBADTOKEN);
+    const int64_t row = ok ? t : 0;
+    float4 v[kV];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < kV; ++i) {
+        const int c = lane + 32 * i;
+        v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < n4 && ok) {
+            if (kBf16E) {
+                const uint2 w = __ldg(reinterpret_cast<const uint2*>(
+                                          static_cast<const __nv_bfloat16*>(E) + row * D) + c);
+                v[i] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+            } else {
+                v[i] = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(E) + row * D) + c);
+            }
+        }
+        if (c < n4) reinterpret_cast<float4*>(h + m * D)[c] = v[i];
+        ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float r = 1.0f / sqrtf(ss / (float)D + eps);
+    const float4* g4 = reinterpret_cast<const float4*>(g);
+#pragma unroll
+    for (int i = 0; i < kV; ++i) {
+        const int c = lane + 32 * i;
+        if (c >= n4) break;
+        const float4 w = __ldg(g4 + c);
+        const float a0 = v[i].x * r * w.x, a1 = v[i].y * r * w.y;
+        const float a2 = v[i].z * r * w.z, a3 = v[i].w * r * w.w;
+        if (kBf16Y) {
+            uint2 o;
+            o.x = pack_bf16x2(a0, a1);
+            o.y = pack_bf16x2(a2, a3);
+            reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(y) + m * D)[c] = o;
+        } else {
+            reinterpret_cast<float4*>(static_cast<float*>(y) + m * D)[c] = make_float4(a0, a1, a2, a3);
+        }
+    }
+}
+
+template <int kV>
+cudaError_t embed_norm_launch(const int32_t* tok, const void* E, const float* g, float* h, void* y,
+                              int64_t M, int V, int D, float eps, int bf16, cudaStream_t st) {
+    const dim3 blocks((unsigned)((M + 7) / 8));
+    if (bf16)
+        return launch_pdl(k_embed_rmsnorm<kV, true, true>, blocks, dim3(256), 0, st, tok, E, g, h,
+                          y, M, V, D, eps, device_error_word());
+    return launch_pdl(k_embed_rmsnorm<kV, false, false>, blocks, dim3(256), 0, st, tok, E, g, h, y,
+                      M, V, D, eps, device_error_word());
+}
+
+cudaError_t launch_embed_rmsnorm(const int32_t* tok, const void* E, const float* g, float* h,
+                                 void* y, int64_t M, int V, int D, float eps, int bf16,
+                                 cudaStream_t st) {
+    if (M <= 0) return cudaSuccess;
+    const int groups = (D / 4 + 31) / 32;   // 4-float groups per lane
+    if (groups <= 1) return embed_norm_launch<1>(tok, E, g, h, y, M, V, D, eps, bf16, st);
+    if (groups <= 2) return embed_norm_launch<2>(tok, E, g, h, y, M, V, D, eps, bf16, st);
+    if (groups <= 4) return embed_norm_launch<4>(tok, E, g, h, y, M, V, D, eps, bf16, st);
+    if (groups <= 8) return embed_norm_launch<8>(tok, E, g, h, y, M, V, D, eps, bf16, st);
+    if (groups <= 16) return embed_norm_launch<16>(tok, E, g, h, y, M, V, D, eps, bf16, st);
+    if (groups <= 32) return embed_norm_launch<32>(tok, E, g, h, y, M, V, D, eps, bf16, st);
+    // Rows beyond 4096: the gather and the norm as two launches.
+    cudaError_t e = launch_embedding(tok, E, h, M, V, D, bf16, st);
+    if (e != cudaSuccess) return e;
+    return launch_rmsnorm(h, g, y, M, D, eps, bf16, st);
+}
+
 // ------------------------------------------------------------------ RMSNorm
 // y = x / sqrt(mean(x^2) + eps) * g, in fp32, rounded once to the output type
 // (CS336 walkthrough, section 5.6: fp32 through the gain multiply, then cast).

@@ -139,7 +139,7 @@ tfm_status tfm_load_weights(void* handle, const tfm_weights* w, int32_t weights_
  * [0, vocab); columns [vocab, ld_logits) are not written.  Positions are
  * 0..S-1 in every sequence.  Requires 1 <= B <= max_batch, 1 <= S <= max_seq,
  * ld_logits >= vocab, ld_logits % 4 == 0, logits 16-byte aligned.  Launches
- * 3 + 7 n_layer kernels on `stream`; capturable in a CUDA graph.  Calls on the
+ * 2 + 7 n_layer kernels on `stream`; capturable in a CUDA graph.  Calls on the
  * same handle must not overlap (they share the workspace). */
 tfm_status tfm_forward(void* handle, const int32_t* tokens, int32_t B, int32_t S,
                        float* logits, int64_t ld_logits, void* stream);
@@ -186,7 +186,8 @@ void tfm_destroy(void* handle);
  * tfm_profile_read() synchronises those events and adds, per kernel kind, the
  * elapsed milliseconds and launch counts of every forward since the last read
  * into ms[kind] and launches[kind] (arrays of TFM_PROFILE_KINDS entries, which
- * the caller zeroes), then forgets them.  Kinds: 0 embedding, 1 RMSNorm,
+ * the caller zeroes), then forgets them.  Kinds: 0 embedding fused with the
+ * first RMSNorm, 1 RMSNorm,
  * 2 QKV projection + RoPE, 3 attention, 4 output projection + residual,
  * 5 gate/up projection + SwiGLU, 6 down projection + residual, 7 LM head. */
 #define TFM_PROFILE_KINDS 8
