@@ -25,10 +25,15 @@
 // exponentials with a polynomial on the FMA pipe was measured slower here: it
 // costs more issue slots than it frees.)  S_x(j+1) is issued as soon as the
 // softmax of tile x has read S_x(j) into registers, P_x.V_j as soon as it has
-// written P_x(j).  An MMA warp shares its scheduler with two softmax warps,
-// which leaves it few issue slots; one thread issuing all ~24 MMAs of a key tile
-// was measured to be the bound, hence two issuing threads.  All waits are
-// bounded; tiles above the diagonal are never loaded.
+// written P_x(j); the exponentials of tile j+1 run before the wait for P_x.V_j
+// (which frees the P_x columns), so that wait overlaps them.  (Two threads per
+// row, 16 softmax warps exchanging partial row maxima through shared memory,
+// was measured slower: the bounded barrier round trip of the exchange costs
+// ~600 cycles per tile and the two tiles fall into lockstep.)  An MMA warp
+// shares its scheduler with two softmax warps, which leaves it few issue slots;
+// one thread issuing all ~24 MMAs of a key tile was measured to be the bound,
+// hence two issuing threads.  All waits are bounded; tiles above the diagonal
+// are never loaded.
 #include "common.cuh"
 #include "internal.h"
 
@@ -364,21 +369,16 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                     m = mx;
                 }
                 const bool need_rescale = __any_sync(0xffffffffu, corr != 1.f && j > 0);
-                // P_x and O_x are free once the previous O_x += P_x V (possibly of the
-                // previous item) has completed.
-                if (cnt > 0 && !warp_wait(o_done(x), (uint32_t)(cnt - 1) & 1u, err, abort_flag)) {
-                    ok = false;
-                    break;
-                }
                 // p = 2^(s*scale - m): scale and offset as packed pairs, one exponential
-                // per element, row sum in four packed accumulators; P goes to tensor
-                // memory as bf16 pairs, 64 keys (32 columns) per store.
+                // per element, row sum in four packed accumulators, P kept in registers
+                // as bf16 pairs.  The exponentials do not depend on the previous P.V,
+                // so they run before the wait for it.
                 const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
                 const uint64_t negm2 = f2_pack(-m, -m);
                 uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
+                uint32_t pw[kKV / 64][32];
 #pragma unroll
                 for (int h64 = 0; h64 < kKV / 64; ++h64) {
-                    uint32_t pw[32];
 #pragma unroll
                     for (int e = 0; e < 64; e += 2) {
                         float t0, t1;
@@ -386,10 +386,19 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                         f2_unpack(f2_fma(f2_pack(s[cc], s[cc + 1]), scale2, negm2), t0, t1);
                         const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
                         sum2[(e >> 1) & 3] = f2_add(sum2[(e >> 1) & 3], f2_pack(p0, p1));
-                        pw[e >> 1] = pack_bf16x2(p0, p1);
+                        pw[h64][e >> 1] = pack_bf16x2(p0, p1);
                     }
-                    tmem_st32_async(t_p + h64 * 32, pw);
                 }
+                // P_x and O_x are free once the previous O_x += P_x V (possibly of the
+                // previous item) has completed; then P goes to tensor memory, 64 keys
+                // (32 columns) per store.
+                if (cnt > 0 && !warp_wait(o_done(x), (uint32_t)(cnt - 1) & 1u, err, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int h64 = 0; h64 < kKV / 64; ++h64) tmem_st32_async(t_p + h64 * 32, pw[h64]);
                 tmem_st_wait();
                 float sa[4], sb[4];
 #pragma unroll
