@@ -8,10 +8,17 @@
 // when the max grows (stable softmax: subtracting any common constant leaves
 // the result unchanged, so the rescale is exact up to rounding).
 //
-// One CTA = 128 query rows of one (sequence, head), keys in tiles of 128:
-//   warp 0      TMA: the Q tile once, then K and V tiles (3-D maps [seq*heads,
-//               S, dh], 128-byte swizzle, zero fill past S) into separate K and V
-//               rings, in the order the MMA thread consumes them
+// A work item is 128 query rows of one (sequence, head), keys in tiles of 128.
+// The kernel is persistent: one CTA per SM walks a list of items (longest first
+// across all heads, dealt in snake order), so one item's tail (its last
+// softmax tiles, the final P.V, the O write-out) overlaps the next item's Q
+// load and first S MMA instead of a CTA exit and launch (measured per-CTA
+// timelines of the one-item-per-CTA grid showed the SMs idle ~30 % of the
+// kernel between CTAs):
+//   warp 0      TMA: each item's Q tile (once the previous item's S MMAs are done
+//               with the buffer), then K and V tiles (3-D maps [seq*heads, S,
+//               dh], 128-byte swizzle, zero fill past S) into separate K and V
+//               rings, in the order the MMA threads consume them
 //   warp 1      TMEM (512 columns: S double buffer 2 x 128, O dh, P double buffer
 //               2 x 64) and the S MMAs: S_j = Q K_j^T (M=128, N=128, K=dh)
 //   warp 6      the P.V MMAs: O += P_j V_j (M=128, N=dh, K=128; P read from tensor
@@ -52,8 +59,8 @@ struct AttTc {
     static constexpr int kOCol = 2 * kKV;             // TMEM columns: S[2], O, P[2]
     static constexpr int kPCol = kOCol + DH;
     // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2],
-    // o_done[2], done
-    static constexpr int kNumBars = 1 + 4 * kStages + 7;
+    // o_done[2], done, q_empty
+    static constexpr int kNumBars = 1 + 4 * kStages + 8;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kBytes = kMiscOff + 16 + 1024;
 };
@@ -61,8 +68,8 @@ struct AttTc {
 template <int DH>
 __global__ void __launch_bounds__(kThreadsAtt, 1)
     k_attention_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                   const __grid_constant__ CUtensorMap vmap, __nv_bfloat16* __restrict__ o, int H,
-                   int Hkv, int S, float scale_log2, int* err) {
+                   const __grid_constant__ CUtensorMap vmap, __nv_bfloat16* __restrict__ o, int BH,
+                   int H, int Hkv, int S, float scale_log2, int* err) {
     using L = AttTc<DH>;
     constexpr int ST = L::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -80,21 +87,39 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
     auto p_full = [&](int i) { return bars + 8u * (3 + 4 * ST + i); };
     auto o_done = [&](int i) { return bars + 8u * (5 + 4 * ST + i); };
     const uint32_t done_bar = bars + 8u * (7 + 4 * ST);
+    const uint32_t q_empty = bars + 8u * (8 + 4 * ST);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + L::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMiscOff + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_qt = (S + kQ - 1) / kQ;
-    // 1-D grid ordered heaviest first across all (sequence, head): CTA i takes
-    // query tile (num_qt - 1 - i / BH) of head i % BH (longest first).
-    const int BH = (int)gridDim.x / num_qt;
-    const int qt = num_qt - 1 - (int)blockIdx.x / BH;
-    const int bh = (int)blockIdx.x % BH, b = bh / H, h = bh - b * H;
-    const int g = h / (H / Hkv);
-    const int n = qt + 1;                              // key tiles 0..qt
+    const int total = num_qt * BH;
+    // Persistent: work items (query tile, (sequence, head)) are numbered longest
+    // first across all heads, item i = (tile num_qt-1 - i/BH, head i%BH), and
+    // dealt to the CTAs round by round in snake order (even rounds c, odd rounds
+    // G-1-c), which keeps the sum of item lengths per CTA even.  Every role walks
+    // the same sequence; ring slots and barrier phases follow a running key-tile
+    // counter g across items.
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    struct Item {
+        int qt, n, b, h, g;
+    };
+    auto item_of = [&](int rnd, Item& it) -> bool {
+        const int idx = rnd * G + ((rnd & 1) ? G - 1 - c : c);
+        if (idx >= total) return false;
+        it.qt = num_qt - 1 - idx / BH;
+        it.n = it.qt + 1;                              // key tiles 0..qt
+        const int bh = idx % BH;
+        it.b = bh / H;
+        it.h = bh - it.b * H;
+        it.g = it.h / (H / Hkv);
+        return true;
+    };
+    const int rounds = (total + G - 1) / G;
 
     if (warp == 0 && lane == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
         for (int s = 0; s < ST; ++s) {
             mbar_init(k_full(s), 1);
             mbar_init(k_empty(s), 1);
@@ -125,47 +150,57 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
+        // Per item: its Q tile once the previous item's S MMAs are done with the
+        // Q buffer, then the K and V tiles in the order the MMA threads consume
+        // them (K_0, then K_j, V_{j-1} for j >= 1, then V_{n-1}).  The rings run
+        // on across items.  Before exiting it waits for its last load into every
+        // slot, so no copy is in flight when the CTA ends.
         if (lane == 0) {
-            mbar_arrive_expect_tx(q_full, L::kQBytes);
-#pragma unroll
-            for (int sub = 0; sub < L::kSub; ++sub)
-                tma_load_3d(sQ + sub * 16384, &qmap, 64 * sub, qt * kQ, b * H + h, q_full);
-            // Loads follow the order the MMA thread consumes them: K_0, then
-            // K_j, V_{j-1} for j >= 1, then V_{n-1}.
-            int k_issued = 0, v_issued = 0;
+            int kn = 0, vn = 0, items = 0;           // K, V tiles and items loaded
+            bool ok = true;
+            Item it;
             auto load_k = [&](int j) -> bool {
-                const int st = j % ST;
-                if (!mbar_wait(k_empty(st), ((uint32_t)(j / ST) & 1u) ^ 1u, err, abort_flag)) return false;
+                const int st = kn % ST;
+                if (!mbar_wait(k_empty(st), ((uint32_t)(kn / ST) & 1u) ^ 1u, err, abort_flag)) return false;
                 mbar_arrive_expect_tx(k_full(st), L::kKBytes);
 #pragma unroll
                 for (int sub = 0; sub < L::kSub; ++sub)
                     tma_load_3d(sK + st * L::kKBytes + sub * 16384, &kmap, 64 * sub, j * kKV,
-                                b * Hkv + g, k_full(st));
-                ++k_issued;
+                                it.b * Hkv + it.g, k_full(st));
+                ++kn;
                 return true;
             };
             auto load_v = [&](int j) -> bool {
-                const int st = j % ST;
-                if (!mbar_wait(v_empty(st), ((uint32_t)(j / ST) & 1u) ^ 1u, err, abort_flag)) return false;
+                const int st = vn % ST;
+                if (!mbar_wait(v_empty(st), ((uint32_t)(vn / ST) & 1u) ^ 1u, err, abort_flag)) return false;
                 mbar_arrive_expect_tx(v_full(st), L::kVBytes);
 #pragma unroll
                 for (int sub = 0; sub < L::kSub; ++sub)
                     tma_load_3d(sV + st * L::kVBytes + sub * 16384, &vmap, 64 * sub, j * kKV,
-                                b * Hkv + g, v_full(st));
-                ++v_issued;
+                                it.b * Hkv + it.g, v_full(st));
+                ++vn;
                 return true;
             };
-            bool ok = load_k(0);
-            for (int j = 1; j < n && ok; ++j) ok = load_k(j) && load_v(j - 1);
-            if (ok) load_v(n - 1);
-            // Drain: the copies of every armed slot (and Q) must land before exit.
-            mbar_wait(q_full, 0, err, abort_flag);
-            for (int s = 0; s < ST && s < k_issued; ++s) {
-                const int last = k_issued - 1 - ((k_issued - 1 - s) % ST);
+            for (int rnd = 0; rnd < rounds && ok; ++rnd) {
+                if (!item_of(rnd, it)) continue;
+                if (items > 0 && !mbar_wait(q_empty, (uint32_t)(items - 1) & 1u, err, abort_flag)) break;
+                mbar_arrive_expect_tx(q_full, L::kQBytes);
+#pragma unroll
+                for (int sub = 0; sub < L::kSub; ++sub)
+                    tma_load_3d(sQ + sub * 16384, &qmap, 64 * sub, it.qt * kQ, it.b * H + it.h, q_full);
+                ++items;
+                ok = load_k(0);
+                for (int j = 1; j < it.n && ok; ++j) ok = load_k(j) && load_v(j - 1);
+                if (ok) ok = load_v(it.n - 1);
+            }
+            // Drain: the copies of every armed slot (and the last Q) must land.
+            if (items > 0) mbar_wait(q_full, (uint32_t)(items - 1) & 1u, err, abort_flag);
+            for (int s = 0; s < ST && s < kn; ++s) {
+                const int last = kn - 1 - ((kn - 1 - s) % ST);
                 mbar_wait(k_full(s), (uint32_t)((last / ST) & 1), err, abort_flag);
             }
-            for (int s = 0; s < ST && s < v_issued; ++s) {
-                const int last = v_issued - 1 - ((v_issued - 1 - s) % ST);
+            for (int s = 0; s < ST && s < vn; ++s) {
+                const int last = vn - 1 - ((vn - 1 - s) % ST);
                 mbar_wait(v_full(s), (uint32_t)((last / ST) & 1), err, abort_flag);
             }
         }
@@ -178,46 +213,60 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
             constexpr uint32_t idesc_s = umma_idesc_bf16(kQ, kKV);
             constexpr uint32_t idesc_o = umma_idesc_bf16(kQ, DH, true);
             bool ok = true;
+            int g = 0, items = 0;                    // key tiles, items so far
+            Item it;
             if (warp == 1) {
-                // S_j into S[j % 2] once the softmax of tile j-2 is done with it.
+                // S_g into S[g % 2] once the softmax of tile g-2 is done with it.
                 const uint64_t dq = umma_desc_sw128(sQ), dk = umma_desc_sw128(sK);
-                ok = mbar_wait(q_full, 0, err, abort_flag);
-                for (int j = 0; j < n && ok; ++j) {
-                    const int sb = j & 1, st = j % ST;
-                    if (j >= 2 && !mbar_wait(p_full(sb), (uint32_t)((j - 2) >> 1) & 1u, err, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    if (!mbar_wait(k_full(st), (uint32_t)(j / ST) & 1u, err, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t d = tmem_base + (uint32_t)(sb * kKV);
-                    const uint64_t kb = dk + (uint64_t)((st * L::kKBytes) >> 4);
+                for (int rnd = 0; rnd < rounds && ok; ++rnd) {
+                    if (!item_of(rnd, it)) continue;
+                    ok = mbar_wait(q_full, (uint32_t)items & 1u, err, abort_flag);
+                    for (int j = 0; j < it.n && ok; ++j, ++g) {
+                        const int sb = g & 1, st = g % ST;
+                        if (g >= 2 && !mbar_wait(p_full(sb), (uint32_t)((g - 2) >> 1) & 1u, err, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        if (!mbar_wait(k_full(st), (uint32_t)(g / ST) & 1u, err, abort_flag)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t d = tmem_base + (uint32_t)(sb * kKV);
+                        const uint64_t kb = dk + (uint64_t)((st * L::kKBytes) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < DH / 16; ++kk) {
-                        const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                        umma_bf16(d, dq + off, kb + off, idesc_s, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < DH / 16; ++kk) {
+                            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                            umma_bf16(d, dq + off, kb + off, idesc_s, kk > 0 ? 1u : 0u);
+                        }
+                        umma_commit(k_empty(st));
+                        umma_commit(s_full(sb));
                     }
-                    umma_commit(k_empty(st));
-                    umma_commit(s_full(sb));
+                    // The Q buffer may be refilled once this item's S MMAs are complete.
+                    if (ok) umma_commit(q_empty);
+                    ++items;
                 }
             } else {
-                // O += P_i V_i once the softmax has written P_i.
+                // O += P_g V_g once the softmax has written P_g; the first tile of
+                // an item overwrites O (its softmax read the previous item's O
+                // before publishing that P).
                 const uint64_t dv = umma_desc_sw128_mn(sV, 16384, 1024);
-                for (int i = 0; i < n && ok; ++i) {
-                    const int sbp = i & 1, stp = i % ST;
-                    if (!mbar_wait(p_full(sbp), (uint32_t)(i >> 1) & 1u, err, abort_flag)) { ok = false; break; }
-                    if (!mbar_wait(v_full(stp), (uint32_t)(i / ST) & 1u, err, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t t_p = tmem_base + L::kPCol + sbp * (kKV / 2);
-                    const uint64_t vb = dv + (uint64_t)((stp * L::kVBytes) >> 4);
+                for (int rnd = 0; rnd < rounds && ok; ++rnd) {
+                    if (!item_of(rnd, it)) continue;
+                    for (int j = 0; j < it.n && ok; ++j, ++g) {
+                        const int sbp = g & 1, stp = g % ST;
+                        if (!mbar_wait(p_full(sbp), (uint32_t)(g >> 1) & 1u, err, abort_flag)) { ok = false; break; }
+                        if (!mbar_wait(v_full(stp), (uint32_t)(g / ST) & 1u, err, abort_flag)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t t_p = tmem_base + L::kPCol + sbp * (kKV / 2);
+                        const uint64_t vb = dv + (uint64_t)((stp * L::kVBytes) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kKV / 16; ++kk)
-                        umma_bf16_ts(t_o, t_p + kk * 8, vb + (uint64_t)((kk * 2048) >> 4), idesc_o,
-                                     (i > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(v_empty(stp));
-                    umma_commit(o_done(sbp));
+                        for (int kk = 0; kk < kKV / 16; ++kk)
+                            umma_bf16_ts(t_o, t_p + kk * 8, vb + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                                         (j > 0 || kk > 0) ? 1u : 0u);
+                        umma_commit(v_empty(stp));
+                        umma_commit(o_done(sbp));
+                    }
                 }
             }
+            // Every MMA this thread issued must be complete before TMEM is freed.
             umma_commit(done_bar);
             mbar_wait(done_bar, 0, err, abort_flag);
         }
@@ -225,110 +274,125 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
         // ---------------------------------------------------------- softmax
         const int q4 = warp & 3;
         const int r = q4 * 32 + lane;                 // query row in the tile
-        const int qi = qt * kQ + r;                   // query position
         const uint32_t trow = tmem_base + ((uint32_t)(q4 * 32) << 16);
-        float m = -INFINITY, l = 0.f;
+        const uint32_t t_orow = t_o + ((uint32_t)(q4 * 32) << 16);
         bool ok = true;
-        for (int j = 0; j < n; ++j) {
-            const int sb = j & 1;
-            if (!warp_wait(s_full(sb), (uint32_t)(j >> 1) & 1u, err, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            // All four 32-column loads in flight before the single wait.
-            uint32_t sr[kKV / 32][32];
+        int g = 0;                                    // key tiles so far
+        Item it;
+        for (int rnd = 0; rnd < rounds && ok; ++rnd) {
+            if (!item_of(rnd, it)) continue;
+            const int qt = it.qt;
+            const int qi = qt * kQ + r;               // query position
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < it.n; ++j, ++g) {
+                const int sb = g & 1;
+                if (!warp_wait(s_full(sb), (uint32_t)(g >> 1) & 1u, err, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                // All four 32-column loads in flight before the single wait.
+                uint32_t sr[kKV / 32][32];
 #pragma unroll
-            for (int c = 0; c < kKV / 32; ++c) tmem_ld32_issue(trow + sb * kKV + c * 32, sr[c]);
-            tmem_ld_wait();
-            float s[kKV];
+                for (int cc = 0; cc < kKV / 32; ++cc) tmem_ld32_issue(trow + sb * kKV + cc * 32, sr[cc]);
+                tmem_ld_wait();
+                float s[kKV];
 #pragma unroll
-            for (int c = 0; c < kKV / 32; ++c) {
-                reg_fence32(sr[c]);
+                for (int cc = 0; cc < kKV / 32; ++cc) {
+                    reg_fence32(sr[cc]);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[c][e]);
-            }
-            const int k0 = j * kKV;
-            // Only the diagonal tile and a tile reaching past S need the mask
-            // (warp-uniform test).
-            if (j == qt || k0 + kKV > S) {
-#pragma unroll
-                for (int c = 0; c < kKV; ++c)
-                    if (k0 + c > qi || k0 + c >= S) s[c] = -INFINITY;
-            }
-            // Row max over raw scores: four independent chains of three-input
-            // maxima (the scale is positive, so it commutes with the max).
-            float mx4[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-            for (int c = 4; c < kKV; c += 8)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) mx4[e] = fmax3(mx4[e], s[c + 2 * e], s[c + 2 * e + 1]);
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
-            float corr = 1.f;
-            if (mx > m + kRescaleThreshold) {         // also true on the first tile (m = -inf)
-                corr = fast_exp2(m - mx);
-                m = mx;
-            }
-            const bool need_rescale = __any_sync(0xffffffffu, corr != 1.f && j > 0);
-            // P[sb] is free once P_{j-2} V_{j-2} has completed.
-            if (j >= 2 && !warp_wait(o_done(sb), (uint32_t)((j - 2) >> 1) & 1u, err, abort_flag)) {
-                ok = false;
-                break;
-            }
-            // p = 2^(s*scale - m): scale and offset as packed pairs, one exponential
-            // per element, row sum in four packed accumulators; P goes to tensor
-            // memory as bf16 pairs, 64 keys (32 columns) per store.
-            const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
-            const uint64_t negm2 = f2_pack(-m, -m);
-            uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
-            const uint32_t t_p = trow + L::kPCol + sb * (kKV / 2);
-#pragma unroll
-            for (int h64 = 0; h64 < kKV / 64; ++h64) {
-                uint32_t pw[32];
-#pragma unroll
-                for (int e = 0; e < 64; e += 2) {
-                    float t0, t1;
-                    const int c = h64 * 64 + e;
-                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), scale2, negm2), t0, t1);
-                    const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
-                    sum2[(e >> 1) & 3] = f2_add(sum2[(e >> 1) & 3], f2_pack(p0, p1));
-                    pw[e >> 1] = pack_bf16x2(p0, p1);
+                    for (int e = 0; e < 32; ++e) s[cc * 32 + e] = __uint_as_float(sr[cc][e]);
                 }
-                tmem_st32_async(t_p + h64 * 32, pw);
-            }
-            tmem_st_wait();
-            float sa[4], sb2[4];
+                const int k0 = j * kKV;
+                // Only the diagonal tile and a tile reaching past S need the mask
+                // (warp-uniform test).
+                if (j == qt || k0 + kKV > S) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) f2_unpack(sum2[e], sa[e], sb2[e]);
-            const float sum = ((sa[0] + sb2[0]) + (sa[1] + sb2[1])) + ((sa[2] + sb2[2]) + (sa[3] + sb2[3]));
-            l = l * corr + sum;
-            if (need_rescale) {
-                // O must hold P_{j-1} V_{j-1} before it is rescaled.
-                if (!warp_wait(o_done((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, err,
-                               abort_flag)) {
+                    for (int cc = 0; cc < kKV; ++cc)
+                        if (k0 + cc > qi || k0 + cc >= S) s[cc] = -INFINITY;
+                }
+                // Row max over raw scores: four independent chains of three-input
+                // maxima (the scale is positive, so it commutes with the max).
+                float mx4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+                for (int cc = 4; cc < kKV; cc += 8)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) mx4[e] = fmax3(mx4[e], s[cc + 2 * e], s[cc + 2 * e + 1]);
+                const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
+                float corr = 1.f;
+                if (mx > m + kRescaleThreshold) {     // also true on the first tile (m = -inf)
+                    corr = fast_exp2(m - mx);
+                    m = mx;
+                }
+                const bool need_rescale = __any_sync(0xffffffffu, corr != 1.f && j > 0);
+                // p = 2^(s*scale - m): scale and offset as packed pairs, one
+                // exponential per element, row sum in four packed accumulators, P
+                // kept in registers as bf16 pairs until its buffer is free.
+                const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
+                const uint64_t negm2 = f2_pack(-m, -m);
+                uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
+                uint32_t pw[kKV / 64][32];
+#pragma unroll
+                for (int h64 = 0; h64 < kKV / 64; ++h64) {
+#pragma unroll
+                    for (int e = 0; e < 64; e += 2) {
+                        float t0, t1;
+                        const int cc = h64 * 64 + e;
+                        f2_unpack(f2_fma(f2_pack(s[cc], s[cc + 1]), scale2, negm2), t0, t1);
+                        const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+                        sum2[(e >> 1) & 3] = f2_add(sum2[(e >> 1) & 3], f2_pack(p0, p1));
+                        pw[h64][e >> 1] = pack_bf16x2(p0, p1);
+                    }
+                }
+                // P[sb] is free once P_{g-2} V_{g-2} has completed; then P goes to
+                // tensor memory, 64 keys (32 columns) per store.
+                if (g >= 2 && !warp_wait(o_done(sb), (uint32_t)((g - 2) >> 1) & 1u, err, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-#pragma unroll 1
-                for (int c = 0; c < DH / 32; ++c) {
-                    float v[32];
-                    tmem_ld32(t_o + ((uint32_t)(q4 * 32) << 16) + c * 32, v);
+                const uint32_t t_p = trow + L::kPCol + sb * (kKV / 2);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] *= corr;
-                    tmem_st32(t_o + ((uint32_t)(q4 * 32) << 16) + c * 32, v);
+                for (int h64 = 0; h64 < kKV / 64; ++h64) tmem_st32_async(t_p + h64 * 32, pw[h64]);
+                tmem_st_wait();
+                float sa[4], sb2[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) f2_unpack(sum2[e], sa[e], sb2[e]);
+                const float sum = ((sa[0] + sb2[0]) + (sa[1] + sb2[1])) + ((sa[2] + sb2[2]) + (sa[3] + sb2[3]));
+                l = l * corr + sum;
+                if (need_rescale) {
+                    // O must hold P_{g-1} V_{g-1} before it is rescaled.
+                    if (!warp_wait(o_done((g - 1) & 1), (uint32_t)((g - 1) >> 1) & 1u, err,
+                                   abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int cc = 0; cc < DH / 32; ++cc) {
+                        float v[32];
+                        tmem_ld32(t_orow + cc * 32, v);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] *= corr;
+                        tmem_st32(t_orow + cc * 32, v);
+                    }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full(sb));
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_full(sb));
-        }
-        // Final: O / l, written with heads merged, o[b, s, h*DH + d].
-        if (ok && warp_wait(o_done((n - 1) & 1), (uint32_t)((n - 1) >> 1) & 1u, err, abort_flag)) {
+            if (!ok) break;
+            // Final: O / l, written with heads merged, o[b, s, h*DH + d].  O is read
+            // out before the next item's first P is published (its P.V overwrites O).
+            if (!warp_wait(o_done((g - 1) & 1), (uint32_t)((g - 1) >> 1) & 1u, err, abort_flag)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
             const float inv = 1.0f / l;
-            __nv_bfloat16* orow = o + ((int64_t)b * S + qi) * ((int64_t)H * DH) + (int64_t)h * DH;
+            __nv_bfloat16* orow =
+                o + ((int64_t)it.b * S + qi) * ((int64_t)H * DH) + (int64_t)it.h * DH;
 #pragma unroll 1
-            for (int c = 0; c < DH / 32; ++c) {
+            for (int cc = 0; cc < DH / 32; ++cc) {
                 float v[32];
-                tmem_ld32(t_o + ((uint32_t)(q4 * 32) << 16) + c * 32, v);
+                tmem_ld32(t_orow + cc * 32, v);
                 if (qi < S) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {
@@ -337,7 +401,7 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
                         w.y = pack_bf16x2(v[e + 2] * inv, v[e + 3] * inv);
                         w.z = pack_bf16x2(v[e + 4] * inv, v[e + 5] * inv);
                         w.w = pack_bf16x2(v[e + 6] * inv, v[e + 7] * inv);
-                        *reinterpret_cast<uint4*>(orow + c * 32 + e) = w;
+                        *reinterpret_cast<uint4*>(orow + cc * 32 + e) = w;
                     }
                 }
             }
@@ -398,10 +462,12 @@ cudaError_t launch_tc(const AttnPlan& p, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    dim3 grid(((p.S + kQ - 1) / kQ) * p.B * p.H);
-    return launch_pdl(k_attention_tc<DH>, grid, dim3(kThreadsAtt), L::kBytes, st, p.qmap, p.kmap,
-                      p.vmap, static_cast<__nv_bfloat16*>(p.o), p.H, p.Hkv, p.S,
-                      p.scale * 1.4426950408889634f, device_error_word());
+    // One CTA per SM (shared memory allows no more), each looping over items.
+    const int items = ((p.S + kQ - 1) / kQ) * p.B * p.H;
+    const int grid = items < sm_count() ? items : sm_count();
+    return launch_pdl(k_attention_tc<DH>, dim3(grid), dim3(kThreadsAtt), L::kBytes, st, p.qmap,
+                      p.kmap, p.vmap, static_cast<__nv_bfloat16*>(p.o), p.B * p.H, p.H, p.Hkv,
+                      p.S, p.scale * 1.4426950408889634f, device_error_word());
 }
 
 }  // namespace
