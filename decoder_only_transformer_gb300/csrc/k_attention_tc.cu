@@ -1,5 +1,5 @@
 // k_attention_tc.cu - causal softmax attention on the sm_103a tensor cores
-// (tcgen05 + tensor memory), d_head 64 or 128.
+// (tcgen05 + tensor memory), d_head 128.
 //
 // o = softmax(q k^T * scale + M) v per (sequence, head), M = -inf above the
 // diagonal (CS336 walkthrough, section 5.4), query head h reading kv head
@@ -10,27 +10,33 @@
 //
 // A work item is 128 query rows of one (sequence, head), keys in tiles of 128.
 // The kernel is persistent: one CTA per SM walks a list of items (longest first
-// across all heads, dealt in snake order), so one item's tail (its last
-// softmax tiles, the final P.V, the O write-out) overlaps the next item's Q
-// load and first S MMA instead of a CTA exit and launch (measured per-CTA
-// timelines of the one-item-per-CTA grid showed the SMs idle ~30 % of the
-// kernel between CTAs):
+// across all heads, dealt in snake order), and an item's tail overlaps the next
+// item's start.  Measured per-item timelines showed why both matter: a CTA per
+// item left the SMs idle ~30 % of the kernel between CTAs, and writing O out
+// from the softmax warps stalled them ~4000 cycles per item (wait for the last
+// P.V, read O, normalise, store 32 KB) against ~1400 cycles per key tile.
 //   warp 0      TMA: each item's Q tile (once the previous item's S MMAs are done
 //               with the buffer), then K and V tiles (3-D maps [seq*heads, S,
 //               dh], 128-byte swizzle, zero fill past S) into separate K and V
 //               rings, in the order the MMA threads consume them
 //   warp 1      TMEM (512 columns: S double buffer 2 x 128, O dh, P double buffer
 //               2 x 64) and the S MMAs: S_j = Q K_j^T (M=128, N=128, K=dh)
-//   warp 6      the P.V MMAs: O += P_j V_j (M=128, N=dh, K=128; P read from tensor
+//   warp 2      the P.V MMAs: O += P_j V_j (M=128, N=dh, K=128; P read from tensor
 //               memory, V read MN-major straight from its [key, dh] tile, so it is
-//               never transposed).  Issuing from two threads keeps the per-thread
-//               instruction stream short: an MMA warp shares its scheduler with a
-//               softmax warp and gets few issue slots.
-//   warps 2..5  softmax, one thread per query row: S row from TMEM, causal /
+//               never transposed); an item's first P.V (which overwrites O) waits
+//               until the epilogue warps have read the previous item's O.
+//               Issuing from two threads keeps the per-thread instruction stream
+//               short: an MMA warp shares its scheduler with busy warps.
+//   warp 3      idle (the control warps form one warpgroup)
+//   warps 4..7  softmax, one thread per query row: S row from TMEM, causal /
 //               length mask, row max, p = 2^(s*scale*log2e - m) stored as bf16
 //               pairs into the P columns of tensor memory, row sum; the partial
 //               O in TMEM is rescaled only when the row max grows by more than
-//               2^8, so P entries stay below 256 and most tiles skip the rescale
+//               2^8, so P entries stay below 256 and most tiles skip the rescale.
+//               At the end of an item they hand the row sums to the epilogue
+//               through shared memory and go on to the next item.
+//   warps 8..11 epilogue: per item, after its last P.V, O out of tensor memory,
+//               O / l as bf16 to global memory (heads merged).
 // S_{j+1} runs on the tensor cores while the softmax warps work on S_j.
 // Tiles entirely above the diagonal are never loaded.  All waits are bounded.
 #include "common.cuh"
@@ -42,7 +48,7 @@ namespace {
 
 constexpr int kQ = 128;
 constexpr int kKV = 128;
-constexpr int kThreadsAtt = 224;
+constexpr int kThreadsAtt = 384;   // 4 control warps, 4 softmax warps, 4 epilogue warps
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 template <int DH>
@@ -59,9 +65,11 @@ struct AttTc {
     static constexpr int kOCol = 2 * kKV;             // TMEM columns: S[2], O, P[2]
     static constexpr int kPCol = kOCol + DH;
     // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2],
-    // o_done[2], done, q_empty
-    static constexpr int kNumBars = 1 + 4 * kStages + 8;
-    static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+    // o_done[2], done, q_empty, l_ready, o_free
+    static constexpr int kNumBars = 1 + 4 * kStages + 10;
+    // Row sums handed from the softmax to the epilogue warps, [item parity][row].
+    static constexpr int kRedOff = kBarOff + 8 * kNumBars;
+    static constexpr int kMiscOff = kRedOff + 2 * kQ * 4;
     static constexpr int kBytes = kMiscOff + 16 + 1024;
 };
 
@@ -88,6 +96,9 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
     auto o_done = [&](int i) { return bars + 8u * (5 + 4 * ST + i); };
     const uint32_t done_bar = bars + 8u * (7 + 4 * ST);
     const uint32_t q_empty = bars + 8u * (8 + 4 * ST);
+    const uint32_t l_ready = bars + 8u * (9 + 4 * ST);
+    const uint32_t o_free = bars + 8u * (10 + 4 * ST);
+    float* red_l = reinterpret_cast<float*>(gbase + L::kRedOff);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + L::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMiscOff + 4);
 
@@ -132,6 +143,8 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
             mbar_init(o_done(i), 1);
         }
         mbar_init(done_bar, 2);              // one commit from each MMA thread
+        mbar_init(l_ready, 4);               // one arrival per softmax warp
+        mbar_init(o_free, 4);                // one arrival per epilogue warp
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&qmap);
@@ -147,7 +160,12 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
     pdl_wait();
     pdl_trigger();
     const uint32_t t_o = tmem_base + L::kOCol;
-
+    // Register split per warpgroup (launched with 168 per thread, 64512 in all):
+    // the control warps give theirs up to the softmax, the epilogue keeps 168:
+    // 128 * (80 + 232 + 168) = 61440 <= 64512.  Each warpgroup executes one
+    // setmaxnreg at the top of its own branch.
+    if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
         // Per item: its Q tile once the previous item's S MMAs are done with the
@@ -204,7 +222,7 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
                 mbar_wait(v_full(s), (uint32_t)((last / ST) & 1), err, abort_flag);
             }
         }
-    } else if (warp == 1 || warp == 6) {
+    } else if (warp == 1 || warp == 2) {
         // ---------------------------------------------------------- MMA issuers
         // Descriptors are built once and advanced by adding (byte offset >> 4) to
         // their start-address field (shared addresses stay below 256 KB, so the
@@ -245,11 +263,17 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
                 }
             } else {
                 // O += P_g V_g once the softmax has written P_g; the first tile of
-                // an item overwrites O (its softmax read the previous item's O
-                // before publishing that P).
+                // an item overwrites O.
                 const uint64_t dv = umma_desc_sw128_mn(sV, 16384, 1024);
                 for (int rnd = 0; rnd < rounds && ok; ++rnd) {
                     if (!item_of(rnd, it)) continue;
+                    // O is overwritten by this item's first P.V once the epilogue
+                    // warps have read the previous item's O out of tensor memory.
+                    if (items > 0 && !mbar_wait(o_free, (uint32_t)(items - 1) & 1u, err, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    ++items;
                     for (int j = 0; j < it.n && ok; ++j, ++g) {
                         const int sbp = g & 1, stp = g % ST;
                         if (!mbar_wait(p_full(sbp), (uint32_t)(g >> 1) & 1u, err, abort_flag)) { ok = false; break; }
@@ -270,19 +294,23 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
             umma_commit(done_bar);
             mbar_wait(done_bar, 0, err, abort_flag);
         }
-    } else {
+    }
+    } else if (warp < 8) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
         // ---------------------------------------------------------- softmax
         const int q4 = warp & 3;
         const int r = q4 * 32 + lane;                 // query row in the tile
         const uint32_t trow = tmem_base + ((uint32_t)(q4 * 32) << 16);
         const uint32_t t_orow = t_o + ((uint32_t)(q4 * 32) << 16);
         bool ok = true;
-        int g = 0;                                    // key tiles so far
+        int g = 0, items = 0;                         // key tiles, items so far
         Item it;
         for (int rnd = 0; rnd < rounds && ok; ++rnd) {
             if (!item_of(rnd, it)) continue;
             const int qt = it.qt;
             const int qi = qt * kQ + r;               // query position
+            // Last visible key of this row: the diagonal, or S - 1 past the end.
+            const int kmax = qi < S ? qi : S - 1;
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < it.n; ++j, ++g) {
                 const int sb = g & 1;
@@ -304,9 +332,9 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
                 // Only the diagonal tile and a tile reaching past S need the mask
                 // (warp-uniform test).
                 if (j == qt || k0 + kKV > S) {
+                    const int lim = kmax - k0;         // keys cc > lim are masked
 #pragma unroll
-                    for (int cc = 0; cc < kKV; ++cc)
-                        if (k0 + cc > qi || k0 + cc >= S) s[cc] = -INFINITY;
+                    for (int cc = 0; cc < kKV; ++cc) s[cc] = cc > lim ? -INFINITY : s[cc];
                 }
                 // Row max over raw scores: four independent chains of three-input
                 // maxima (the scale is positive, so it commutes with the max).
@@ -374,35 +402,69 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
                         tmem_st32(t_orow + cc * 32, v);
                     }
                 }
+                // Before the last P of item k is published, the epilogue must have
+                // taken item k-1 (its O read out, so its row-sum slot is free):
+                // the softmax runs at most one item ahead of the epilogue, and
+                // the wait cannot alias, since item k's O is not final before
+                // this P exists.
+                if (j == it.n - 1 && items > 0 &&
+                    !warp_wait(o_free, (uint32_t)(items - 1) & 1u, err, abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_full(sb));
             }
             if (!ok) break;
-            // Final: O / l, written with heads merged, o[b, s, h*DH + d].  O is read
-            // out before the next item's first P is published (its P.V overwrites O).
-            if (!warp_wait(o_done((g - 1) & 1), (uint32_t)((g - 1) >> 1) & 1u, err, abort_flag)) {
-                ok = false;
-                break;
-            }
+            // The row sum goes to the epilogue warps, which write O / l once the
+            // last P.V is done; this warp moves on to the next item.
+            red_l[(items & 1) * kQ + r] = l;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(l_ready);
+            ++items;
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        // Per item: wait for its row sums and its last P.V, read O out of tensor
+        // memory (all DH columns into registers), release O for the next item's
+        // first P.V, then write O / l with heads merged, o[b, s, h*DH + d].
+        const int q4 = warp & 3;
+        const int r = q4 * 32 + lane;
+        const uint32_t t_orow = t_o + ((uint32_t)(q4 * 32) << 16);
+        int g = 0, items = 0;
+        Item it;
+        for (int rnd = 0; rnd < rounds; ++rnd) {
+            if (!item_of(rnd, it)) continue;
+            g += it.n;                                 // g - 1: this item's last key tile
+            if (!warp_wait(l_ready, (uint32_t)items & 1u, err, abort_flag)) break;
+            const float l = red_l[(items & 1) * kQ + r];
+            if (!warp_wait(o_done((g - 1) & 1), (uint32_t)((g - 1) >> 1) & 1u, err, abort_flag)) break;
             tc_fence_after();
+            uint32_t ov[DH / 32][32];
+#pragma unroll
+            for (int cc = 0; cc < DH / 32; ++cc) tmem_ld32_issue(t_orow + cc * 32, ov[cc]);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_free);
+            ++items;
+            const int qi = it.qt * kQ + r;
+            if (qi >= S) continue;
             const float inv = 1.0f / l;
             __nv_bfloat16* orow =
                 o + ((int64_t)it.b * S + qi) * ((int64_t)H * DH) + (int64_t)it.h * DH;
-#pragma unroll 1
-            for (int cc = 0; cc < DH / 32; ++cc) {
-                float v[32];
-                tmem_ld32(t_orow + cc * 32, v);
-                if (qi < S) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 w;
-                        w.x = pack_bf16x2(v[e] * inv, v[e + 1] * inv);
-                        w.y = pack_bf16x2(v[e + 2] * inv, v[e + 3] * inv);
-                        w.z = pack_bf16x2(v[e + 4] * inv, v[e + 5] * inv);
-                        w.w = pack_bf16x2(v[e + 6] * inv, v[e + 7] * inv);
-                        *reinterpret_cast<uint4*>(orow + cc * 32 + e) = w;
-                    }
+            for (int cc = 0; cc < DH / 32; ++cc) {
+                reg_fence32(ov[cc]);
+#pragma unroll
+                for (int e = 0; e < 32; e += 8) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(ov[cc][e]) * inv, __uint_as_float(ov[cc][e + 1]) * inv);
+                    w.y = pack_bf16x2(__uint_as_float(ov[cc][e + 2]) * inv, __uint_as_float(ov[cc][e + 3]) * inv);
+                    w.z = pack_bf16x2(__uint_as_float(ov[cc][e + 4]) * inv, __uint_as_float(ov[cc][e + 5]) * inv);
+                    w.w = pack_bf16x2(__uint_as_float(ov[cc][e + 6]) * inv, __uint_as_float(ov[cc][e + 7]) * inv);
+                    *reinterpret_cast<uint4*>(orow + cc * 32 + e) = w;
                 }
             }
         }
