@@ -29,7 +29,9 @@
 // (which frees the P_x columns), so that wait overlaps them.  (Two threads per
 // row, 16 softmax warps exchanging partial row maxima through shared memory,
 // was measured slower: the bounded barrier round trip of the exchange costs
-// ~600 cycles per tile and the two tiles fall into lockstep.)  An MMA warp
+// ~600 cycles per tile and the two tiles fall into lockstep.  So was a separate
+// epilogue warpgroup writing O out, as the d_head 128 kernel does, at 16 warps
+// with a setmaxnreg split: long 139 -> 164 us, gpt2s 28 -> 33 us.)  An MMA warp
 // shares its scheduler with two softmax warps, which leaves it few issue slots;
 // one thread issuing all ~24 MMAs of a key tile was measured to be the bound,
 // hence two issuing threads.  All waits are bounded; tiles above the diagonal
