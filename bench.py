@@ -62,7 +62,10 @@ def load_peaks():
 DRAM_TRAFFIC = {
     ("small", "qkv_rope_gemm"): 10.04e6, ("small", "attention"): 25.18e6,
     ("small", "oproj_residual_gemm"): 25.74e6, ("small", "gateup_swiglu_gemm"): 11.19e6,
-    ("gqa", "qkv_rope_gemm"): 68.94e6, ("gqa", "attention"): 52.12e6,
+    ("long", "qkv_rope_gemm"): 28.57e6, ("long", "attention"): 51.54e6,
+    ("long", "oproj_residual_gemm"): 52.47e6, ("long", "gateup_swiglu_gemm"): 31.67e6,
+    ("long", "down_residual_gemm"): 87.43e6,
+    ("gqa", "qkv_rope_gemm"): 68.94e6, ("gqa", "attention"): 52.17e6,
     ("gqa", "oproj_residual_gemm"): 129.26e6, ("gqa", "gateup_swiglu_gemm"): 150.65e6,
 }
 
