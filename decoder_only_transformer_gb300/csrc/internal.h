@@ -30,6 +30,9 @@ struct EpiParams {
     void* q;
     void* k;
     void* v;
+    // Tensor-core GEMM: 1 = each staged 32 x 32 output block is written by one TMA
+    // store (or reduce-add for EPI_ACCUM_F32) through the output maps of TcMaps.
+    int tma_out;
 };
 
 // Launch with programmatic stream serialization allowed (see pdl_wait in
@@ -105,6 +108,13 @@ struct TcMaps {
     CUtensorMap a;
     CUtensorMap b;
     CUtensorMap b2;
+    // Output maps when EpiParams::tma_out is set, box 32 x 32: `out` ([M, N] fp32
+    // or bf16) for the plain, residual and SwiGLU kinds; `oq`, `ok`, `ov`
+    // ([B*heads, S, dh] bf16) for the QKV kind.
+    CUtensorMap out;
+    CUtensorMap oq;
+    CUtensorMap ok;
+    CUtensorMap ov;
 };
 struct GemmPlan {
     TcMaps maps;

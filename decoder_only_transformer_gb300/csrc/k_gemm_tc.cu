@@ -178,6 +178,33 @@ __device__ __forceinline__ void flush_block(const EpiParams& p, uint32_t buf, in
     }
 }
 
+// Writes the staged 32 x 32 block (rows row0.., columns col..) with one TMA
+// store (a reduce-add for the residual kind) issued by the calling thread; the
+// tensor map clips rows >= M and columns >= N.  The staging layouts are the
+// maps' swizzles: fp32 rows of 128 bytes (128-byte swizzle), bf16 rows of 64
+// bytes (64-byte swizzle).  QKV blocks lie inside one sequence (S % 32 == 0)
+// and one head (dh % 32 == 0): (d0, s0, b*heads + head) in its [B*heads, S, dh]
+// map.
+__device__ __forceinline__ void tma_out_block(const TcMaps& maps, const EpiParams& p, uint32_t buf,
+                                              int row0, int col) {
+    if (row0 >= p.M || col >= p.N) return;
+    switch (p.kind) {
+        case EPI_ACCUM_F32:
+            tma_reduce_add_2d(&maps.out, buf, col, row0);
+            break;
+        case EPI_QKV_ROPE: {
+            const QkvSlot q = qkv_slot(p, col);
+            const int b = row0 / p.S;
+            const CUtensorMap* m = q.region == 0 ? &maps.oq : (q.region == 1 ? &maps.ok : &maps.ov);
+            tma_store_3d(m, buf, q.d0, row0 - b * p.S, b * q.heads + q.head);
+            break;
+        }
+        default:
+            tma_store_2d(&maps.out, buf, col, row0);
+            break;
+    }
+}
+
 template <int BN, int STAGES, bool kDual, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ TcMaps maps, int M, int N, int K, EpiParams epi, int* err) {
@@ -345,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float rcs[32];
         int acc = 0;
         uint32_t acc_phase = 0;
+        uint32_t nblk = 0;                            // blocks written by TMA (buffer parity)
         // Rank 1 releases the accumulator on the leader's barrier.
         const uint32_t tempty0 = kPair ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
         for (int t = unit; t < num_tiles; t += units) {
@@ -388,10 +416,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     epi_compute<32>(epi, row, col, a, u, o);
                 }
-                stage_row(stg, lane, o, obf);
-                __syncwarp();
-                flush_block(epi, stg, lane, row0, col);
-                __syncwarp();                         // the buffer is reused by the next chunk
+                if (epi.tma_out && col + 32 <= N) {
+                    // One bulk copy per block, issued by lane 0; a bf16 block (2 KB)
+                    // alternates between the halves of the warp's 4 KB buffer, an fp32
+                    // block fills it.  A buffer is rewritten once the copy issued from
+                    // it has read it.  (Only blocks whole in N: a tensor store was seen
+                    // to write the rest of the last 16-byte segment past N, so a
+                    // ragged right edge takes the per-lane stores, which stop exactly.)
+                    const uint32_t buf = stg + (obf ? (nblk & 1u) * 2048u : 0u);
+                    if (lane == 0) {
+                        if (obf) bulk_wait_read<1>();
+                        else bulk_wait_read<0>();
+                    }
+                    __syncwarp();
+                    stage_row(buf, lane, o, obf);
+                    fence_proxy_async_smem();         // the block is read by the async proxy
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_out_block(maps, epi, buf, row0, col);
+                        bulk_commit();
+                    }
+                    ++nblk;
+                } else {
+                    if (epi.tma_out) {                // no bulk copy may still read the buffer
+                        if (lane == 0) bulk_wait_read<0>();
+                        __syncwarp();
+                    }
+                    stage_row(stg, lane, o, obf);
+                    __syncwarp();
+                    flush_block(epi, stg, lane, row0, col);
+                    __syncwarp();                     // the buffer is reused by the next chunk
+                }
             };
             // This warp takes every other chunk; a TMEM load costs only a few tens
             // of cycles, the global stores dominate, so more storing warps (not
@@ -415,6 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
+        // Every bulk copy this warp issued has completed before the CTA ends.
+        if (epi.tma_out && lane == 0) bulk_wait<0>();
     }
 
     tc_fence_before();
@@ -511,6 +568,70 @@ cudaError_t launch_inst(const GemmPlan& p, cudaStream_t st) {
 
 }  // namespace
 
+// Output map for the epilogue's TMA stores: [rows, cols] fp32 (128-byte swizzle)
+// or bf16 (64-byte swizzle), row stride ld elements, box 32 x 32.
+bool make_out_map(CUtensorMap* map, void* ptr, int64_t rows, int64_t cols, int64_t ld, bool bf16) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const int es = bf16 ? 2 : 4;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * es)};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr,
+              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Head-major bf16 output [n_seq_heads, S, dh], box 32 (of dh) x 32 (positions) x 1.
+bool make_heads_out_map(CUtensorMap* map, void* ptr, int64_t n_seq_heads, int64_t S, int64_t dh) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)dh, (cuuint64_t)S, (cuuint64_t)n_seq_heads};
+    cuuint64_t strides[2] = {(cuuint64_t)(dh * 2), (cuuint64_t)(S * dh * 2)};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16_ptr(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The epilogue writes through TMA when the destination allows it: 16-byte
+// aligned base and row stride; QKV only when no 32-row block crosses a sequence
+// (S % 32 == 0) and blocks tile the heads (dh % 32 == 0).  Otherwise it keeps
+// the per-lane stores.  Plain fp32 stores (the LM head's logits) keep them too:
+// a 4 KB fp32 block fills a warp's staging buffer, so each block waited for the
+// previous one's bulk read, and the LM head was measured slower (gpt2s 539 ->
+// 576 us) where the bf16 QKV blocks, two per buffer, were faster (gpt2s 32.5 ->
+// 28.8 us) and the fp32 reduce-add about even.
+bool plan_tma_out(TcMaps* maps, const EpiParams& e) {
+    switch (e.kind) {
+        case EPI_ACCUM_F32:
+            return e.out && aligned16_ptr(e.out) && (e.ldo * 4) % 16 == 0 &&
+                   make_out_map(&maps->out, e.out, e.M, e.N, e.ldo, false);
+        case EPI_STORE_BF16:
+            return e.out && aligned16_ptr(e.out) && (e.ldo * 2) % 16 == 0 &&
+                   make_out_map(&maps->out, e.out, e.M, e.N, e.ldo, true);
+        case EPI_SWIGLU:
+            return e.out_bf16 && e.out && aligned16_ptr(e.out) && (e.ldo * 2) % 16 == 0 &&
+                   make_out_map(&maps->out, e.out, e.M, e.N, e.ldo, true);
+        case EPI_QKV_ROPE: {
+            if (!e.out_bf16 || e.S <= 0 || e.S % 32 != 0 || e.dh % 32 != 0 || e.M % e.S != 0)
+                return false;
+            if (!aligned16_ptr(e.q) || !aligned16_ptr(e.k) || !aligned16_ptr(e.v)) return false;
+            const int64_t B = e.M / e.S;
+            return make_heads_out_map(&maps->oq, e.q, B * e.n_head, e.S, e.dh) &&
+                   make_heads_out_map(&maps->ok, e.k, B * e.n_kv_head, e.S, e.dh) &&
+                   make_heads_out_map(&maps->ov, e.v, B * e.n_kv_head, e.S, e.dh);
+        }
+        default:
+            return false;
+    }
+}
+
 tfm_status plan_gemm_tc(GemmPlan* plan, const void* A, int64_t lda, const void* B, const void* B2,
                         int64_t ldb, int M, int N, int K, const EpiParams& epi) {
     const bool dual = B2 != nullptr;
@@ -540,6 +661,7 @@ tfm_status plan_gemm_tc(GemmPlan* plan, const void* A, int64_t lda, const void* 
     } else {
         plan->maps.b2 = plan->maps.b;
     }
+    plan->epi.tma_out = plan_tma_out(&plan->maps, plan->epi) ? 1 : 0;
     return TFM_OK;
 }
 
