@@ -144,6 +144,8 @@ def test_attention_fp32(B, H, Hkv, S, dh):
     # several items: 384 query tiles (d_head 128, ragged S), 256 tile pairs
     # (d_head 64, an odd tile count: the last pair has no second tile)
     (3, 16, 4, 900, 128), (4, 16, 4, 830, 64),
+    # d_head 32 (mma.sync kernel): ragged S with GQA, and a longer sequence
+    (3, 8, 2, 333, 32), (1, 2, 2, 700, 32),
 ])
 def test_attention_bf16(B, H, Hkv, S, dh):
     q, k, v = _qkv(S * 3 + dh, B, H, Hkv, S, dh, True)
