@@ -93,8 +93,29 @@ def kernel_work(cfg, B, S):
     }
 
 
+def tensor_kernel_bytes(cfg, B, S):
+    """Algorithmic HBM bytes (operands read once, outputs written once) of ONE
+    launch of each tensor-core kernel, for its memory cap: the fp32 residual
+    stream is read and written by the o-proj and down GEMMs, the LM head writes
+    fp32 logits."""
+    M = B * S
+    D, F, V = cfg.d_model, cfg.d_ff, cfg.vocab
+    Dq, Dkv = cfg.n_head * cfg.d_head, cfg.n_kv_head * cfg.d_head
+    es = 2 if cfg.mode == "bf16" else 4
+    nqkv = Dq + 2 * Dkv
+    return {
+        "qkv_rope_gemm": M * D * es + nqkv * D * es + M * nqkv * es,
+        "attention": M * nqkv * es + M * Dq * es,
+        "oproj_residual_gemm": M * Dq * es + D * Dq * es + 2 * M * D * 4,
+        "gateup_swiglu_gemm": M * D * es + 2 * F * D * es + M * F * es,
+        "down_residual_gemm": M * F * es + D * F * es + 2 * M * D * 4,
+        "lmhead_gemm": M * D * es + V * D * es + M * V * 4,
+    }
+
+
 def kernel_table(cfg, B, S, prof, peaks):
     work = kernel_work(cfg, B, S)
+    tbytes = tensor_kernel_bytes(cfg, B, S)
     total_ms = sum(ms for ms, _ in prof.values()) or 1.0
     out = {}
     for name, (ms, n) in prof.items():
@@ -113,6 +134,12 @@ def kernel_table(cfg, B, S, prof, peaks):
         out[name] = {"bound": bound, "launches": n, "avg_us": round(avg_s * 1e6, 2),
                      "share": round(ms / total_ms, 4), "achieved": round(ach, 1), "unit": unit,
                      "frac": round(ach / peak, 4)}
+        if bound == "tensor":
+            # memory cap: min(1, arithmetic intensity x HBM bandwidth / tensor peak)
+            ai = units / tbytes[name]
+            cap = min(1.0, ai * peaks["hbm_gbs"] * 1e9 / (peak * 1e12))
+            out[name]["cap"] = round(cap, 4)
+            out[name]["frac_of_cap"] = round(ach / peak / cap, 4)
     return out
 
 
@@ -431,6 +458,9 @@ def main():
     roofline = {"kernel": dom_name, "bound": dom["bound"], "achieved": dom["achieved"],
                 "peak": peaks["bf16_tflops"] if dom["bound"] == "tensor" else peaks["hbm_gbs"],
                 "unit": dom["unit"], "frac": dom["frac"],
+                **({"cap": dom["cap"], "frac_of_cap": dom["frac_of_cap"],
+                    "cap_note": "min(1, algorithmic flop/byte x HBM copy bandwidth / tensor peak)"}
+                   if "cap" in dom else {}),
                 "traffic": DRAM_TRAFFIC.get((cfg.name, dom_name)),
                 "traffic_source": "ncu --set full of the layer-0 launch, cold caches, bytes per launch",
                 "peak_source": f"{peaks['source']} ({'bf16 burst' if dom['bound'] == 'tensor' else 'HBM copy'})",

@@ -80,3 +80,30 @@ def test_causal_flops_count_lower_triangle():
     d = accounting.forward_flops(100, 64, 1, 4, 128, 8, causal=False)
     assert f["attn"] * 64 == d["attn"] * 36
     assert accounting.attention_flops(1, 4, 8, 16) == f["attn"]
+
+
+def test_memory_caps_of_the_tensor_kernels():
+    """The caps the bench reports beside each tensor kernel's fraction of peak:
+    min(1, flop/byte x HBM bandwidth / tensor peak) with the fp32 residual
+    stream read and written by o-proj and down, and fp32 logits written by the
+    LM head.  With the ridge at 1932.1 / 6.7671 = 285.5 flop/B they are the
+    values of the hot-path table: small o-proj 35 %, down 69 %, LM head 85 %;
+    gpt2s o-proj 53 %; long o-proj 70 %; attention (q, k, v read and o written
+    once) 22.5 % at small and 90 % at gpt2s; everything else 100 %."""
+    import bench
+    peaks = {"hbm_gbs": 6767.1, "bf16_tflops": 1932.1}
+    want = {("small", "oproj_residual_gemm"): 0.354, ("small", "down_residual_gemm"): 0.693,
+            ("small", "lmhead_gemm"): 0.848, ("gpt2s", "oproj_residual_gemm"): 0.528,
+            ("long", "oproj_residual_gemm"): 0.700,
+            ("small", "attention"): 0.225, ("gpt2s", "attention"): 0.898}
+    for name in ("small", "gpt2s", "long", "gqa"):
+        cfg = workloads.get_config(name)
+        work = bench.kernel_work(cfg, cfg.batch, cfg.seq)
+        byts = bench.tensor_kernel_bytes(cfg, cfg.batch, cfg.seq)
+        for k, b in byts.items():
+            cap = min(1.0, work[k][1] / b * peaks["hbm_gbs"] * 1e9 / (peaks["bf16_tflops"] * 1e12))
+            assert abs(cap - want.get((name, k), 1.0)) < 2e-3, (name, k, cap)
+    # o-proj at small by hand: 2*M*D*D flop over o + Wo (bf16) and h read + written (fp32)
+    M, D = 8192, 512
+    assert bench.tensor_kernel_bytes(workloads.get_config("small"), 32, 256)["oproj_residual_gemm"] == \
+        M * D * 2 + D * D * 2 + 2 * M * D * 4
