@@ -128,7 +128,7 @@ Sizes sizes_of(const tfm_config* c) {
 
 // Workspace carve-up, every piece 256-byte aligned.
 struct Layout {
-    size_t h, xn, q, k, v, o, a, rope, tok, logits, total;
+    size_t h, xn, q, k, v, o, a, rope, tok, logits, logits2, total;
 };
 
 Layout layout_of(const tfm_config* c) {
@@ -151,6 +151,7 @@ Layout layout_of(const tfm_config* c) {
     L.rope = take((size_t)c->max_seq * (dh / 2) * 8);
     L.tok = take(s.M * 4);
     L.logits = take(s.M * s.ldV * 4);
+    L.logits2 = take(s.M * s.ldV * 4);    // second buffer of tfm_forward_host_async
     L.total = off;
     return L;
 }
@@ -192,13 +193,25 @@ struct Model {
     const float* plan_logits = nullptr;
     int64_t plan_ld = -1;
     int plan_S = -1;
-    // recorded forward (tfm_forward_graph) and the arguments it was recorded for
-    cudaGraphExec_t gexec = nullptr;
-    const void* g_tokens = nullptr;
-    const float* g_logits = nullptr;
-    int g_B = 0, g_S = 0;
-    int64_t g_ld = 0;
-    void* g_stream = nullptr;
+    // recorded forwards (tfm_forward_graph, tfm_forward_host_async) and the
+    // arguments each was recorded for; a few are kept, least recently used out
+    struct Graph {
+        cudaGraphExec_t exec = nullptr;
+        const void* tokens = nullptr;
+        const float* logits = nullptr;
+        int B = 0, S = 0;
+        int64_t ld = 0;
+        void* stream = nullptr;
+        uint64_t used = 0;
+    };
+    static constexpr int kGraphs = 4;
+    Graph graphs[kGraphs];
+    uint64_t graph_clock = 0;
+    // tfm_forward_host_async: copy stream, per-buffer events, calls so far
+    cudaStream_t copy_st = nullptr;
+    cudaEvent_t fwd_done[2] = {nullptr, nullptr}, copied[2] = {nullptr, nullptr};
+    bool copy_pending[2] = {false, false};
+    int64_t async_calls = 0;
     // per-kernel event timing (tfm_profile_*)
     bool prof = false;
     struct ProfRun {
@@ -228,6 +241,7 @@ struct Model {
     float* rope() { return reinterpret_cast<float*>(ws + lay.rope); }
     int32_t* tok() { return reinterpret_cast<int32_t*>(ws + lay.tok); }
     float* logits() { return reinterpret_cast<float*>(ws + lay.logits); }
+    float* logits_buf(int b) { return reinterpret_cast<float*>(ws + (b ? lay.logits2 : lay.logits)); }
 };
 
 }  // namespace tfm
@@ -288,12 +302,27 @@ tfm_status tfm_create(const tfm_config* cfg, void** handle) {
             hcs[((size_t)s * half + i) * 2 + 1] = (float)std::sin(ang);
         }
     e = cudaMemcpy(m->rope(), hcs.data(), hcs.size() * 4, cudaMemcpyHostToDevice);
+    // The internal logits buffers start zeroed: their columns [vocab, ldV) are
+    // never written, so a contiguous device->host copy gives zeros there.
+    if (e == cudaSuccess) e = cudaMemset(m->logits_buf(0), 0, (size_t)m->sz.M * m->sz.ldV * 4);
+    if (e == cudaSuccess) e = cudaMemset(m->logits_buf(1), 0, (size_t)m->sz.M * m->sz.ldV * 4);
     if (e == cudaSuccess && !tfm::device_error_word()) e = cudaErrorSymbolNotFound;
     if (e != cudaSuccess) {
         cudaFree(m->ws);
         cudaFree(m->wmem);
         delete m;
         return tfm::cuda_fail(e, "tfm_create");
+    }
+    // Copy stream and events of tfm_forward_host_async (non-blocking: no implicit
+    // ordering against the legacy stream).
+    e = cudaStreamCreateWithFlags(&m->copy_st, cudaStreamNonBlocking);
+    for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+        e = cudaEventCreateWithFlags(&m->fwd_done[b], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->copied[b], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) {
+        tfm_destroy(m);
+        return tfm::cuda_fail(e, "tfm_create: copy stream");
     }
     *handle = m;
     return TFM_OK;
@@ -302,7 +331,14 @@ tfm_status tfm_create(const tfm_config* cfg, void** handle) {
 void tfm_destroy(void* handle) {
     Model* m = static_cast<Model*>(handle);
     if (!m) return;
-    if (m->gexec) cudaGraphExecDestroy(m->gexec);
+    if (m->copy_st) cudaStreamSynchronize(m->copy_st);
+    for (auto& g : m->graphs)
+        if (g.exec) cudaGraphExecDestroy(g.exec);
+    for (int b = 0; b < 2; ++b) {
+        if (m->fwd_done[b]) cudaEventDestroy(m->fwd_done[b]);
+        if (m->copied[b]) cudaEventDestroy(m->copied[b]);
+    }
+    if (m->copy_st) cudaStreamDestroy(m->copy_st);
     for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
     cudaFree(m->ws);
     cudaFree(m->wmem);
@@ -579,6 +615,79 @@ tfm_status tfm_forward(void* handle, const int32_t* tokens, int32_t B, int32_t S
     return tfm::forward_impl(m, tokens, B, S, logits, ld_logits, static_cast<cudaStream_t>(stream));
 }
 
+}  // extern "C"
+
+namespace tfm {
+namespace {
+
+// Device -> host copy of the logits of M rows from an internal buffer (row
+// stride ldV): one contiguous copy when the host rows have the same stride (the
+// padding columns [vocab, ldV) are zeros), else a pitched copy of the vocab
+// columns only (a row of vocab fp32 values need not be a multiple of 16 bytes,
+// which slows the pitched copy).
+cudaError_t copy_logits_to_host(Model* m, float* host, int64_t ld, const float* dev, int64_t M,
+                                cudaStream_t st) {
+    if (ld == m->sz.ldV)
+        return cudaMemcpyAsync(host, dev, (size_t)M * ld * 4, cudaMemcpyDeviceToHost, st);
+    return cudaMemcpy2DAsync(host, ld * 4, dev, m->sz.ldV * 4, (size_t)m->cfg.vocab * 4, M,
+                             cudaMemcpyDeviceToHost, st);
+}
+
+// Launches the forward for these arguments from a recorded graph, recording it
+// first if no kept recording matches (the least recently used one is replaced).
+tfm_status graph_forward(Model* m, const int32_t* tokens, int B, int S, float* logits, int64_t ld,
+                         cudaStream_t cs) {
+    Model::Graph* g = nullptr;
+    for (auto& c : m->graphs)
+        if (c.exec && c.tokens == tokens && c.B == B && c.S == S && c.logits == logits &&
+            c.ld == ld && c.stream == (void*)cs)
+            g = &c;
+    if (!g) {
+        g = &m->graphs[0];
+        for (auto& c : m->graphs)
+            if (!c.exec || c.used < g->used) g = &c;
+        if (g->exec) {
+            cudaGraphExecDestroy(g->exec);
+            g->exec = nullptr;
+        }
+        const bool prof = m->prof;
+        m->prof = false;
+        cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+        if (e != cudaSuccess) {
+            m->prof = prof;
+            return cuda_fail(e, "begin capture");
+        }
+        tfm_status st = forward_impl(m, tokens, B, S, logits, ld, cs);
+        cudaGraph_t graph = nullptr;
+        e = cudaStreamEndCapture(cs, &graph);
+        m->prof = prof;
+        if (st != TFM_OK || e != cudaSuccess) {
+            if (graph) cudaGraphDestroy(graph);
+            return st != TFM_OK ? st : cuda_fail(e, "end capture");
+        }
+        e = cudaGraphInstantiate(&g->exec, graph, 0);
+        cudaGraphDestroy(graph);
+        if (e != cudaSuccess) {
+            g->exec = nullptr;
+            return cuda_fail(e, "graph instantiate");
+        }
+        g->tokens = tokens;
+        g->B = B;
+        g->S = S;
+        g->logits = logits;
+        g->ld = ld;
+        g->stream = cs;
+    }
+    g->used = ++m->graph_clock;
+    const cudaError_t e = cudaGraphLaunch(g->exec, cs);
+    return e == cudaSuccess ? TFM_OK : cuda_fail(e, "graph launch");
+}
+
+}  // namespace
+}  // namespace tfm
+
+extern "C" {
+
 tfm_status tfm_forward_graph(void* handle, const int32_t* tokens, int32_t B, int32_t S,
                              float* logits, int64_t ld_logits, void* stream) {
     Model* m = static_cast<Model*>(handle);
@@ -586,44 +695,46 @@ tfm_status tfm_forward_graph(void* handle, const int32_t* tokens, int32_t B, int
     if (st != TFM_OK) return st;
     if (!tfm::aligned16(logits)) return fail(TFM_EINVAL, "logits must be 16-byte aligned");
     if (!stream) return fail(TFM_EINVAL, "tfm_forward_graph needs a non-default stream");
+    return tfm::graph_forward(m, tokens, B, S, logits, ld_logits, static_cast<cudaStream_t>(stream));
+}
+
+tfm_status tfm_forward_host_async(void* handle, const int32_t* tokens_host, int32_t B, int32_t S,
+                                  float* logits_host, int64_t ld_logits, void* stream) {
+    Model* m = static_cast<Model*>(handle);
+    tfm_status st = tfm::check_forward_args(m, tokens_host, B, S, logits_host, ld_logits);
+    if (st != TFM_OK) return st;
+    if (!stream) return fail(TFM_EINVAL, "tfm_forward_host_async needs a non-default stream");
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const bool same = m->gexec && m->g_tokens == tokens && m->g_B == B && m->g_S == S &&
-                      m->g_logits == logits && m->g_ld == ld_logits && m->g_stream == stream;
-    if (!same) {
-        if (m->gexec) {
-            cudaGraphExecDestroy(m->gexec);
-            m->gexec = nullptr;
+    const int b = (int)(m->async_calls & 1);
+    const int64_t M = (int64_t)B * S;
+    // Buffer b is written again only once the copy that last read it is done.
+    cudaError_t e = m->copy_pending[b] ? cudaStreamWaitEvent(cs, m->copied[b], 0) : cudaSuccess;
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(m->tok(), tokens_host, M * 4, cudaMemcpyHostToDevice, cs);
+    if (e != cudaSuccess) return tfm::cuda_fail(e, "tokens host->device");
+    st = tfm::graph_forward(m, m->tok(), B, S, m->logits_buf(b), m->sz.ldV, cs);
+    if (st != TFM_OK) return st;
+    e = cudaEventRecord(m->fwd_done[b], cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(m->copy_st, m->fwd_done[b], 0);
+    if (e == cudaSuccess)
+        e = tfm::copy_logits_to_host(m, logits_host, ld_logits, m->logits_buf(b), M, m->copy_st);
+    if (e == cudaSuccess) e = cudaEventRecord(m->copied[b], m->copy_st);
+    if (e != cudaSuccess) return tfm::cuda_fail(e, "logits device->host");
+    m->copy_pending[b] = true;
+    ++m->async_calls;
+    return TFM_OK;
+}
+
+tfm_status tfm_forward_host_join(void* handle, void* stream) {
+    Model* m = static_cast<Model*>(handle);
+    if (!m) return fail(TFM_EINVAL, "NULL handle");
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    for (int b = 0; b < 2; ++b)
+        if (m->copy_pending[b]) {
+            const cudaError_t e = cudaStreamWaitEvent(cs, m->copied[b], 0);
+            if (e != cudaSuccess) return tfm::cuda_fail(e, "join copies");
         }
-        const bool prof = m->prof;
-        m->prof = false;
-        cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
-        if (e != cudaSuccess) {
-            m->prof = prof;
-            return tfm::cuda_fail(e, "begin capture");
-        }
-        st = tfm::forward_impl(m, tokens, B, S, logits, ld_logits, cs);
-        cudaGraph_t graph = nullptr;
-        e = cudaStreamEndCapture(cs, &graph);
-        m->prof = prof;
-        if (st != TFM_OK || e != cudaSuccess) {
-            if (graph) cudaGraphDestroy(graph);
-            return st != TFM_OK ? st : tfm::cuda_fail(e, "end capture");
-        }
-        e = cudaGraphInstantiate(&m->gexec, graph, 0);
-        cudaGraphDestroy(graph);
-        if (e != cudaSuccess) {
-            m->gexec = nullptr;
-            return tfm::cuda_fail(e, "graph instantiate");
-        }
-        m->g_tokens = tokens;
-        m->g_B = B;
-        m->g_S = S;
-        m->g_logits = logits;
-        m->g_ld = ld_logits;
-        m->g_stream = stream;
-    }
-    const cudaError_t e = cudaGraphLaunch(m->gexec, cs);
-    return e == cudaSuccess ? TFM_OK : tfm::cuda_fail(e, "graph launch");
+    return TFM_OK;
 }
 
 tfm_status tfm_forward_host(void* handle, const int32_t* tokens_host, int32_t B, int32_t S,
@@ -637,8 +748,7 @@ tfm_status tfm_forward_host(void* handle, const int32_t* tokens_host, int32_t B,
     if (e != cudaSuccess) return tfm::cuda_fail(e, "tokens host->device");
     st = tfm::forward_impl(m, m->tok(), B, S, m->logits(), m->sz.ldV, cs);
     if (st != TFM_OK) return st;
-    e = cudaMemcpy2DAsync(logits_host, ld_logits * 4, m->logits(), m->sz.ldV * 4,
-                          (size_t)m->cfg.vocab * 4, M, cudaMemcpyDeviceToHost, cs);
+    e = tfm::copy_logits_to_host(m, logits_host, ld_logits, m->logits(), M, cs);
     if (e != cudaSuccess) return tfm::cuda_fail(e, "logits device->host");
     return TFM_OK;
 }

@@ -57,6 +57,8 @@ _SIGS = {
     "tfm_load_weights": ([_V, ctypes.POINTER(Weights), _I32], _I32),
     "tfm_forward": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
     "tfm_forward_host": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
+    "tfm_forward_host_async": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
+    "tfm_forward_host_join": ([_V, _V], _I32),
     "tfm_forward_graph": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
     "tfm_device_status": ([_V], _I32),
     "tfm_selftest_wait_timeout": ([_I32, _V], _I32),
@@ -220,6 +222,18 @@ class Model:
         B, S = tokens.shape
         _check(self.lib.tfm_forward_host(self.handle, _ptr(tokens), B, S, _ptr(logits),
                                          logits.stride(0), _stream(stream)))
+
+    def forward_host_async(self, tokens, logits, stream=None):
+        """forward_host with the logits copy on the handle's copy stream,
+        overlapping the next call's forward; logits are final after
+        forward_host_join(stream) and a synchronise of that stream."""
+        B, S = tokens.shape
+        _check(self.lib.tfm_forward_host_async(self.handle, _ptr(tokens), B, S, _ptr(logits),
+                                               logits.stride(0), _stream(stream)))
+
+    def forward_host_join(self, stream=None):
+        """Makes the stream wait for every logits copy issued so far."""
+        _check(self.lib.tfm_forward_host_join(self.handle, _stream(stream)))
 
     def profile(self, enable: bool = True):
         _check(self.lib.tfm_profile_enable(self.handle, 1 if enable else 0))

@@ -148,7 +148,8 @@ tfm_status tfm_forward(void* handle, const int32_t* tokens, int32_t B, int32_t S
  * (tokens, B, S, logits, ld_logits, stream) records the launch sequence into a
  * graph (nothing executes while recording), instantiates it and launches it;
  * later calls with the same arguments only launch the graph, which removes the
- * per-kernel host launch cost.  Other arguments re-record.  Same results and
+ * per-kernel host launch cost.  Other arguments record another graph (the four
+ * most recently used recordings are kept).  Same results and
  * requirements as tfm_forward; `stream` must not be the legacy default stream
  * (NULL); per-kernel profiling does not apply to graph launches. */
 tfm_status tfm_forward_graph(void* handle, const int32_t* tokens, int32_t B, int32_t S,
@@ -156,9 +157,32 @@ tfm_status tfm_forward_graph(void* handle, const int32_t* tokens, int32_t B, int
 
 /* The same forward with HOST buffers: copies tokens host->device, runs the
  * forward, copies logits device->host, all enqueued on `stream` (the caller
- * synchronises).  tokens_host [B, S]; logits_host [B*S, ld_logits]. */
+ * synchronises).  tokens_host [B, S]; logits_host [B*S, ld_logits].  When
+ * ld_logits == round_up(vocab, 4) the rows are copied as one block and columns
+ * [vocab, ld_logits) receive zeros; otherwise only columns [0, vocab) are
+ * written. */
 tfm_status tfm_forward_host(void* handle, const int32_t* tokens_host, int32_t B, int32_t S,
                             float* logits_host, int64_t ld_logits, void* stream);
+
+/* Host round trip with the logits copy overlapped: copies tokens host->device
+ * and runs the forward (replayed from a recorded graph, as tfm_forward_graph) on
+ * `stream`, into one of two device logits buffers of the handle taken in turn;
+ * the device->host copy of the logits then runs on the handle's own copy
+ * stream, so it overlaps the next call's forward.  A buffer is written again only
+ * after its previous copy has completed.  Returns once everything is enqueued.
+ * The logits of a call are in logits_host [B*S, ld_logits] (columns [vocab,
+ * ld_logits) as for tfm_forward_host) once the caller has made a stream wait
+ * with tfm_forward_host_join and that
+ * stream has reached the wait.  logits_host should be pinned (page-locked) for
+ * the copy to be asynchronous; tokens_host may be reused as soon as `stream`
+ * has passed the call.  Same requirements as tfm_forward_graph otherwise
+ * (`stream` must not be NULL). */
+tfm_status tfm_forward_host_async(void* handle, const int32_t* tokens_host, int32_t B, int32_t S,
+                                  float* logits_host, int64_t ld_logits, void* stream);
+
+/* Makes `stream` wait (without blocking the host) for every logits copy that
+ * tfm_forward_host_async has issued on this handle so far. */
+tfm_status tfm_forward_host_join(void* handle, void* stream);
 
 /* Synchronises the device, then returns and clears the sticky device error word
  * (TFM_OK, TFM_EBADTOKEN or TFM_ETIMEOUT), or TFM_ECUDA if the context faulted.

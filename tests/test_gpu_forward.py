@@ -127,6 +127,65 @@ def test_forward_host_matches_device_forward():
     model.close()
 
 
+def test_forward_host_async_overlaps_and_matches():
+    """Four calls on two token batches alternate between the handle's two logits
+    buffers (the copy of one overlapping the next forward); after the join each
+    host buffer holds exactly its batch's logits."""
+    cfg = workloads.get_config("small").replace(n_layer=1)
+    w = workloads.make_weights(cfg)
+    model = tfm.Model(cfg, max_batch=4, max_seq=256)
+    model.load_weights(to_torch_weights(w, bf16=True))
+    ld = cfg.vocab
+    toks = [workloads.make_tokens(cfg, batch=2, seq=96, seed=s) for s in (11, 12, 13, 14)]
+    ref = []
+    for t in toks:
+        d = torch.empty(2 * 96, ld, device="cuda")
+        model.forward(torch.from_numpy(t).cuda(), d)
+        ref.append(d.cpu().numpy())
+    stream = torch.cuda.Stream()
+    host_tok = [torch.from_numpy(t).pin_memory() for t in toks]
+    host_logits = [torch.full((2 * 96, ld + 4), float("nan")).pin_memory() for _ in toks]
+    with torch.cuda.stream(stream):
+        for t, l in zip(host_tok, host_logits):
+            model.forward_host_async(t, l, stream)
+        model.forward_host_join(stream)
+    stream.synchronize()
+    tfm.device_status()
+    for r, l in zip(ref, host_logits):
+        assert np.array_equal(l.numpy()[:, :ld], r)
+        assert np.all(np.isnan(l.numpy()[:, ld:]))
+    model.close()
+
+
+def test_forward_host_contiguous_copy_zeroes_the_padding():
+    """With the host row stride equal to round_up(vocab, 4) the logits come back
+    as one contiguous block: the vocab columns as on the device, the padding
+    columns zero (both the synchronous and the overlapped call)."""
+    cfg = workloads.get_config("small").replace(n_layer=1, vocab=1001)
+    w = workloads.make_weights(cfg)
+    tok = workloads.make_tokens(cfg, batch=2, seq=64)
+    model = tfm.Model(cfg, max_batch=2, max_seq=64)
+    model.load_weights(to_torch_weights(w, bf16=True))
+    ld = 1004
+    d = torch.empty(2 * 64, ld, device="cuda")
+    model.forward(torch.from_numpy(tok).cuda(), d)
+    ref = d.cpu().numpy()[:, :cfg.vocab]
+    stream = torch.cuda.Stream()
+    host_tok = torch.from_numpy(tok).pin_memory()
+    a = torch.full((2 * 64, ld), float("nan")).pin_memory()
+    b = torch.full((2 * 64, ld), float("nan")).pin_memory()
+    with torch.cuda.stream(stream):
+        model.forward_host(host_tok, a, stream)
+        model.forward_host_async(host_tok, b, stream)
+        model.forward_host_join(stream)
+    stream.synchronize()
+    tfm.device_status()
+    for h in (a, b):
+        assert np.array_equal(h.numpy()[:, :cfg.vocab], ref)
+        assert np.all(h.numpy()[:, cfg.vocab:] == 0.0)
+    model.close()
+
+
 def test_forward_graph_matches_direct_forward_and_rerecords():
     cfg = workloads.get_config("small").replace(n_layer=2)
     w = workloads.make_weights(cfg, gains="random")
