@@ -122,6 +122,7 @@ struct GemmPlan {
     int block_n;          // tile width (128 or 256); SwiGLU: gate+up halves of block_n/2
     int dual;             // SwiGLU: B tile = [W1 rows; W3 rows]
     int pair;             // 1: CTA pairs (cta_group::2) on 256-row tiles
+    int n_fast;           // tile order: 1 = column blocks fastest, 0 = row blocks fastest
     EpiParams epi;
 };
 // Builds the tensor maps; returns TFM_OK or an error status with a message.

@@ -207,7 +207,8 @@ __device__ __forceinline__ void tma_out_block(const TcMaps& maps, const EpiParam
 
 template <int BN, int STAGES, bool kDual, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemm_tc(const __grid_constant__ TcMaps maps, int M, int N, int K, EpiParams epi, int* err) {
+    k_gemm_tc(const __grid_constant__ TcMaps maps, int M, int N, int K, int n_fast, EpiParams epi,
+              int* err) {
     using L = TcSmem<BN, STAGES, kPair>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -238,6 +239,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int unit = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;   // tile scheduler slot
     const int units = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
     const bool leader = rank == 0;
+    // Tile t -> (row block, column block): column blocks fastest when A is the
+    // larger operand (the tiles in flight then share a few A row blocks and read
+    // all of B, which stays in L2), row blocks fastest otherwise.
+    auto tile_m = [&](int t) { return n_fast ? t / num_n : t % num_m; };
+    auto tile_n = [&](int t) { return n_fast ? t % num_n : t / num_m; };
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -277,8 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int64_t issued = 0;
             bool ok = true;
             for (int t = unit; t < num_tiles && ok; t += units) {
-                const int m0 = (t % num_m) * tile_rows + (int)rank * kBM;
-                const int n0 = (t / num_m) * n_per_tile;
+                const int m0 = tile_m(t) * tile_rows + (int)rank * kBM;
+                const int n0 = tile_n(t) * n_per_tile;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, err, abort_flag)) { ok = false; break; }
                     const uint32_t sa = sA0 + stage * kTileABytes;
@@ -376,8 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Rank 1 releases the accumulator on the leader's barrier.
         const uint32_t tempty0 = kPair ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
         for (int t = unit; t < num_tiles; t += units) {
-            const int m0 = (t % num_m) * tile_rows + (int)rank * kBM;
-            const int n0 = (t / num_m) * n_per_tile;
+            const int m0 = tile_m(t) * tile_rows + (int)rank * kBM;
+            const int n0 = tile_n(t) * n_per_tile;
             if (rope_pre) {
                 const int r = m0 + q * 32 + lane;
                 const int pos = (r < M ? r : 0) % epi.S;
@@ -561,9 +567,10 @@ cudaError_t launch_inst(const GemmPlan& p, cudaStream_t st) {
     const int units = (int)(tiles < slots ? tiles : slots);
     if (kPair)
         return launch_pdl_pair(k_gemm_tc<BN, STAGES, kDual, kPair>, dim3(2 * units), dim3(kThreads),
-                               L::kBytes, st, p.maps, p.M, p.N, p.K, p.epi, device_error_word());
+                               L::kBytes, st, p.maps, p.M, p.N, p.K, p.n_fast, p.epi,
+                               device_error_word());
     return launch_pdl(k_gemm_tc<BN, STAGES, kDual, kPair>, dim3(units), dim3(kThreads), L::kBytes,
-                      st, p.maps, p.M, p.N, p.K, p.epi, device_error_word());
+                      st, p.maps, p.M, p.N, p.K, p.n_fast, p.epi, device_error_word());
 }
 
 }  // namespace
@@ -652,6 +659,14 @@ tfm_status plan_gemm_tc(GemmPlan* plan, const void* A, int64_t lda, const void* 
         plan->pair = (M > kBM && long_k) ? 1 : 0;
     }
     plan->block_n = plan->pair ? 256 : choose_block_n(M, N, dual);
+    // Column blocks fastest when A (M x K bf16) is larger than B and too large
+    // to stay in L2 (over 64 MB): with row blocks fastest every wave streams all
+    // of A once per column block, and at gqa the down projection (A 92 MB, B
+    // 23 MB) read 444 MB from DRAM against 182 MB algorithmic (194 MB in the
+    // other order, 124 -> 118 us).  Where A fits in L2 the order was measured
+    // neutral to slower (QKV gqa 75 -> 79 us), so it stays row blocks fastest.
+    const int64_t a_bytes = (int64_t)M * K * 2, b_bytes = (int64_t)N * (dual ? 2 : 1) * K * 2;
+    plan->n_fast = (a_bytes > b_bytes && a_bytes > (64ll << 20)) ? 1 : 0;
     plan->epi = epi;
     const int box_b = (dual || plan->pair) ? plan->block_n / 2 : plan->block_n;
     if (!make_operand_map(&plan->maps.a, A, M, K, lda, kBM)) return TFM_ECUDA;
