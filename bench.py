@@ -60,13 +60,15 @@ def load_peaks():
 # the layer-0 launches (cold caches) of the kernels as they are now; an op
 # without an entry reports traffic null.
 DRAM_TRAFFIC = {
-    ("small", "qkv_rope_gemm"): 10.04e6, ("small", "attention"): 25.18e6,
-    ("small", "oproj_residual_gemm"): 25.74e6, ("small", "gateup_swiglu_gemm"): 11.19e6,
-    ("long", "qkv_rope_gemm"): 28.57e6, ("long", "attention"): 51.54e6,
-    ("long", "oproj_residual_gemm"): 52.47e6, ("long", "gateup_swiglu_gemm"): 31.67e6,
-    ("long", "down_residual_gemm"): 87.43e6,
-    ("gqa", "qkv_rope_gemm"): 68.94e6, ("gqa", "attention"): 52.17e6,
-    ("gqa", "oproj_residual_gemm"): 129.26e6, ("gqa", "gateup_swiglu_gemm"): 150.65e6,
+    ("small", "qkv_rope_gemm"): 10.30e6, ("small", "attention"): 25.18e6,
+    ("small", "oproj_residual_gemm"): 25.74e6, ("small", "gateup_swiglu_gemm"): 14.78e6,
+    ("small", "down_residual_gemm"): 40.74e6,
+    ("long", "qkv_rope_gemm"): 30.14e6, ("long", "attention"): 51.54e6,
+    ("long", "oproj_residual_gemm"): 52.48e6, ("long", "gateup_swiglu_gemm"): 32.48e6,
+    ("long", "down_residual_gemm"): 87.36e6,
+    ("gqa", "qkv_rope_gemm"): 68.98e6, ("gqa", "attention"): 52.17e6,
+    ("gqa", "oproj_residual_gemm"): 130.13e6, ("gqa", "gateup_swiglu_gemm"): 151.39e6,
+    ("gqa", "down_residual_gemm"): 230.70e6,
 }
 
 
