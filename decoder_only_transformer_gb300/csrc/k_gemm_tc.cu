@@ -53,12 +53,6 @@ struct TcSmem {
     static constexpr int kBytes = kMiscOffset + 16 + 1024;   // + alignment slack
 };
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
-}
 
 // Thread `lane` writes row `lane` of a 32 x 32 block into the staging buffer:
 // fp32 rows of 128 bytes (16-byte chunk j of row r at position j ^ (r % 8)) or
