@@ -207,6 +207,18 @@ struct Model {
     static constexpr int kGraphs = 4;
     Graph graphs[kGraphs];
     uint64_t graph_clock = 0;
+    // KV cache (tfm_kv_cache_create): per layer K then V, each [max_batch, Hkv,
+    // max_seq, dh]; decode attention scratch; filled positions and batch
+    uint8_t* kv = nullptr;
+    size_t kv_layer_bytes = 0;      // one of K or V of one layer
+    float* dec_part = nullptr;
+    int kv_len = 0, kv_batch = 0;
+    // tensor-core plans of a decode step (M = batch rows), cached by batch and logits
+    std::vector<GemmPlan> d_qkv, d_o, d_gu, d_down;
+    GemmPlan d_lm;
+    int dplan_B = -1;
+    const float* dplan_logits = nullptr;
+    int64_t dplan_ld = -1;
     // tfm_forward_host_async: copy stream, per-buffer events, calls so far
     cudaStream_t copy_st = nullptr;
     cudaEvent_t fwd_done[2] = {nullptr, nullptr}, copied[2] = {nullptr, nullptr};
@@ -242,6 +254,8 @@ struct Model {
     int32_t* tok() { return reinterpret_cast<int32_t*>(ws + lay.tok); }
     float* logits() { return reinterpret_cast<float*>(ws + lay.logits); }
     float* logits_buf(int b) { return reinterpret_cast<float*>(ws + (b ? lay.logits2 : lay.logits)); }
+    void* kcache(int l) { return kv + (size_t)l * 2 * kv_layer_bytes; }
+    void* vcache(int l) { return kv + ((size_t)l * 2 + 1) * kv_layer_bytes; }
 };
 
 }  // namespace tfm
@@ -339,6 +353,7 @@ void tfm_destroy(void* handle) {
         if (m->copied[b]) cudaEventDestroy(m->copied[b]);
     }
     if (m->copy_st) cudaStreamDestroy(m->copy_st);
+    if (m->kv) cudaFree(m->kv);
     for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
     cudaFree(m->ws);
     cudaFree(m->wmem);
@@ -510,7 +525,7 @@ enum Kind { K_EMBED = 0, K_NORM, K_QKV, K_ATTN, K_OPROJ, K_GATEUP, K_DOWN, K_LMH
     } while (0)
 
 tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* logits, int64_t ld,
-                        cudaStream_t st) {
+                        cudaStream_t st, bool to_cache = false) {
     const tfm_config& c = m->cfg;
     const auto& s = m->sz;
     const int M = B * S;
@@ -541,6 +556,18 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
             if (l > 0)
                 TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 1, st));
             TFM_LAUNCH(K_QKV, launch_gemm_tc(m->p_qkv[l], st));
+            if (to_cache) {
+                // k, v of positions [0, S) into the layer's cache: rows (b, kv head)
+                // of S*dh elements, cache row pitch max_seq*dh.
+                const size_t row = (size_t)S * dh * 2, pitch = (size_t)c.max_seq * dh * 2;
+                const size_t rows = (size_t)B * c.n_kv_head;
+                cudaError_t e = cudaMemcpy2DAsync(m->kcache(l), pitch, m->k(), row, row, rows,
+                                                  cudaMemcpyDeviceToDevice, st);
+                if (e == cudaSuccess)
+                    e = cudaMemcpy2DAsync(m->vcache(l), pitch, m->v(), row, row, rows,
+                                          cudaMemcpyDeviceToDevice, st);
+                if (e != cudaSuccess) return cuda_fail(e, "k, v into the cache");
+            }
             if (m->attn_tc)
                 TFM_LAUNCH(K_ATTN, launch_attention_tc(m->p_attn, st));
             else
@@ -587,6 +614,95 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
                                               c.vocab, c.d_model,
                                               epi_basic(EPI_STORE_F32, M, c.vocab, logits, ld), st));
     }
+    return TFM_OK;
+}
+
+// Tensor-core plans of a decode step: M = B rows (one new token per sequence),
+// q, k, v of that token head-major with S = 1; the RoPE position is set per step.
+tfm_status build_decode_plans(Model* m, int B, float* logits, int64_t ld) {
+    if (m->dplan_B == B && m->dplan_logits == logits && m->dplan_ld == ld) return TFM_OK;
+    const tfm_config& c = m->cfg;
+    const auto& s = m->sz;
+    m->d_qkv.resize(c.n_layer);
+    m->d_o.resize(c.n_layer);
+    m->d_gu.resize(c.n_layer);
+    m->d_down.resize(c.n_layer);
+    m->dplan_B = -1;
+    tfm_status st = TFM_OK;
+    for (int l = 0; l < c.n_layer && st == TFM_OK; ++l) {
+        st = plan_gemm_tc(&m->d_qkv[l], m->xn(), s.D, m->wqkv[l], nullptr, s.D, B, (int)s.Nqkv,
+                          (int)s.D, epi_qkv(m, B, 1));
+        if (st == TFM_OK)
+            st = plan_gemm_tc(&m->d_o[l], m->o(), s.Dq, m->wo[l], nullptr, s.Dq, B, (int)s.D,
+                              (int)s.Dq, epi_basic(EPI_ACCUM_F32, B, (int)s.D, m->h(), s.D));
+        if (st == TFM_OK) {
+            EpiParams e = epi_basic(EPI_SWIGLU, B, (int)s.F, m->a(), s.F);
+            e.out_bf16 = 1;
+            st = plan_gemm_tc(&m->d_gu[l], m->xn(), s.D, m->w1[l], m->w3[l], s.D, B, (int)s.F,
+                              (int)s.D, e);
+        }
+        if (st == TFM_OK)
+            st = plan_gemm_tc(&m->d_down[l], m->a(), s.F, m->w2[l], nullptr, s.F, B, (int)s.D,
+                              (int)s.F, epi_basic(EPI_ACCUM_F32, B, (int)s.D, m->h(), s.D));
+    }
+    if (st == TFM_OK)
+        st = plan_gemm_tc(&m->d_lm, m->xn(), s.D, m->lm_head, nullptr, s.D, B, (int)s.V, (int)s.D,
+                          epi_basic(EPI_STORE_F32, B, (int)s.V, logits, ld));
+    if (st != TFM_OK) return fail(st, "could not encode TMA tensor maps (driver entry point missing?)");
+    m->dplan_B = B;
+    m->dplan_logits = logits;
+    m->dplan_ld = ld;
+    return TFM_OK;
+}
+
+// One decode step: token t_b of every sequence b at position pos, the cache
+// holding positions [0, pos).  The same blocks as the forward with M = B; each
+// layer appends the token's k, v to its cache and attends over [0, pos].
+tfm_status decode_impl(Model* m, const int32_t* tokens, int B, int pos, float* logits, int64_t ld,
+                       cudaStream_t st) {
+    const tfm_config& c = m->cfg;
+    const int dh = c.d_model / c.n_head;
+    const float scale = 1.0f / std::sqrt((float)dh);
+    if (!device_error_word()) return fail(TFM_ECUDA, "device error word unavailable");
+    tfm_status ps = build_decode_plans(m, B, logits, ld);
+    if (ps != TFM_OK) return ps;
+    Model::ProfRun* run = nullptr;
+    if (m->prof) {
+        m->runs.push_back(Model::ProfRun{m->ev_used, {}});
+        run = &m->runs.back();
+        cudaEvent_t ev = m->next_event();
+        if (!ev) return fail(TFM_ECUDA, "cudaEventCreate failed");
+        cudaEventRecord(ev, st);
+    }
+    TFM_LAUNCH(K_EMBED, launch_embed_rmsnorm(tokens, m->embed,
+                                             c.n_layer > 0 ? m->attn_norm[0] : m->final_norm,
+                                             m->h(), m->xn(), B, c.vocab, c.d_model, c.norm_eps,
+                                             1, st));
+    const size_t row = (size_t)dh * 2, pitch = (size_t)c.max_seq * dh * 2;
+    const size_t rows = (size_t)B * c.n_kv_head;
+    for (int l = 0; l < c.n_layer; ++l) {
+        if (l > 0)
+            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), B, c.d_model, c.norm_eps, 1, st));
+        m->d_qkv[l].epi.pos0 = pos;
+        TFM_LAUNCH(K_QKV, launch_gemm_tc(m->d_qkv[l], st));
+        // the token's k, v at position pos of every (sequence, kv head) row
+        cudaError_t e = cudaMemcpy2DAsync(static_cast<uint8_t*>(m->kcache(l)) + (size_t)pos * row,
+                                          pitch, m->k(), row, row, rows, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(static_cast<uint8_t*>(m->vcache(l)) + (size_t)pos * row, pitch,
+                                  m->v(), row, row, rows, cudaMemcpyDeviceToDevice, st);
+        if (e != cudaSuccess) return cuda_fail(e, "k, v into the cache");
+        TFM_LAUNCH(K_ATTN, launch_decode_attention(m->q(), m->kcache(l), m->vcache(l), m->dec_part,
+                                                   m->o(), B, c.n_head, c.n_kv_head, c.max_seq,
+                                                   pos + 1, dh, scale, st));
+        TFM_LAUNCH(K_OPROJ, launch_gemm_tc(m->d_o[l], st));
+        TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->ffn_norm[l], m->xn(), B, c.d_model, c.norm_eps, 1, st));
+        TFM_LAUNCH(K_GATEUP, launch_gemm_tc(m->d_gu[l], st));
+        TFM_LAUNCH(K_DOWN, launch_gemm_tc(m->d_down[l], st));
+    }
+    if (c.n_layer > 0)
+        TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->final_norm, m->xn(), B, c.d_model, c.norm_eps, 1, st));
+    TFM_LAUNCH(K_LMHEAD, launch_gemm_tc(m->d_lm, st));
     return TFM_OK;
 }
 
@@ -722,6 +838,63 @@ tfm_status tfm_forward_host_async(void* handle, const int32_t* tokens_host, int3
     if (e != cudaSuccess) return tfm::cuda_fail(e, "logits device->host");
     m->copy_pending[b] = true;
     ++m->async_calls;
+    return TFM_OK;
+}
+
+tfm_status tfm_kv_cache_create(void* handle) {
+    Model* m = static_cast<Model*>(handle);
+    if (!m) return fail(TFM_EINVAL, "NULL handle");
+    if (m->kv) return TFM_OK;
+    const tfm_config& c = m->cfg;
+    const int dh = c.d_model / c.n_head;
+    if (c.mode != TFM_BF16) return fail(TFM_EUNSUPPORTED, "the KV cache needs bf16 mode");
+    if (!tfm::decode_supported(dh, c.n_head / c.n_kv_head))
+        return fail(TFM_EUNSUPPORTED, "decode needs d_head in {32, 64, 128} and H/Hkv in {1, 2, 4, 8, 16}");
+    const size_t layer = (size_t)c.max_batch * c.n_kv_head * c.max_seq * dh * 2;
+    const size_t caches = (size_t)c.n_layer * 2 * layer;
+    const size_t part = tfm::decode_partial_floats(c.max_batch, c.n_head, c.max_seq, dh) * 4;
+    uint8_t* p = nullptr;
+    const cudaError_t e = cudaMalloc(&p, caches + part + 256);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(TFM_ENOMEM, "KV cache of %zu bytes: %s", caches + part, cudaGetErrorString(e));
+    }
+    m->kv = p;
+    m->kv_layer_bytes = layer;
+    m->dec_part = reinterpret_cast<float*>(p + (caches + 255) / 256 * 256);
+    m->kv_len = 0;
+    m->kv_batch = 0;
+    return TFM_OK;
+}
+
+tfm_status tfm_prefill(void* handle, const int32_t* tokens, int32_t B, int32_t S, float* logits,
+                       int64_t ld_logits, void* stream) {
+    Model* m = static_cast<Model*>(handle);
+    tfm_status st = tfm::check_forward_args(m, tokens, B, S, logits, ld_logits);
+    if (st != TFM_OK) return st;
+    if (!tfm::aligned16(logits)) return fail(TFM_EINVAL, "logits must be 16-byte aligned");
+    if (!m->kv) return fail(TFM_EINVAL, "no KV cache: call tfm_kv_cache_create first");
+    st = tfm::forward_impl(m, tokens, B, S, logits, ld_logits, static_cast<cudaStream_t>(stream),
+                           true);
+    if (st != TFM_OK) return st;
+    m->kv_len = S;
+    m->kv_batch = B;
+    return TFM_OK;
+}
+
+tfm_status tfm_decode_step(void* handle, const int32_t* tokens, int32_t B, int32_t pos,
+                           float* logits, int64_t ld_logits, void* stream) {
+    Model* m = static_cast<Model*>(handle);
+    tfm_status st = tfm::check_forward_args(m, tokens, B, 1, logits, ld_logits);
+    if (st != TFM_OK) return st;
+    if (!tfm::aligned16(logits)) return fail(TFM_EINVAL, "logits must be 16-byte aligned");
+    if (!m->kv) return fail(TFM_EINVAL, "no KV cache: call tfm_kv_cache_create first");
+    if (m->kv_batch != B) return fail(TFM_EINVAL, "B=%d differs from the cached batch %d", B, m->kv_batch);
+    if (pos != m->kv_len) return fail(TFM_EINVAL, "pos=%d must equal the cached length %d", pos, m->kv_len);
+    if (pos >= m->cfg.max_seq) return fail(TFM_EINVAL, "pos=%d reaches max_seq=%d", pos, m->cfg.max_seq);
+    st = tfm::decode_impl(m, tokens, B, pos, logits, ld_logits, static_cast<cudaStream_t>(stream));
+    if (st != TFM_OK) return st;
+    m->kv_len = pos + 1;
     return TFM_OK;
 }
 

@@ -145,7 +145,7 @@ __device__ __forceinline__ void epi_compute(const EpiParams& p, int row, int col
         const QkvSlot q = qkv_slot(p, col0);
         if (q.region < 2 && row < p.M) {
             const int dh = p.dh;
-            const int s = row % p.S;
+            const int s = p.pos0 + row % p.S;
             float cs[W];                       // (cos, sin) of the W/2 pairs
             load_vec<W>(p.rope_cs + ((int64_t)s * (dh / 2) + q.d0 / 2) * 2, cs);
 #pragma unroll

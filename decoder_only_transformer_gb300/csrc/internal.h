@@ -24,8 +24,11 @@ struct EpiParams {
     void* out;            // STORE/ACCUM/SWIGLU destination
     int64_t ldo;          // its row stride in elements
     int out_bf16;         // SWIGLU/QKV: 1 = bf16 outputs, 0 = fp32
-    // EPI_QKV_ROPE: row m = b*S + s; columns [0,Dq) -> q[b,h,s,:], then k, then v
+    // EPI_QKV_ROPE: row m = b*S + s; columns [0,Dq) -> q[b,h,s,:], then k, then v;
+    // q and k are rotated for position pos0 + s (pos0 = 0 for a whole sequence, the
+    // cache length for a decode step)
     int S, n_head, n_kv_head, dh;
+    int pos0;
     const float* rope_cs;    // [>= S, dh/2, 2]: cos, sin of s * theta^(-2i/dh)
     void* q;
     void* k;
@@ -133,6 +136,15 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t st);
 // ---- bf16 flash attention on mma.sync (k_attention.cu), any dh in {32, 64, 128}
 cudaError_t launch_attention_bf16(const void* q, const void* k, const void* v, void* o, int B,
                                   int H, int Hkv, int S, int dh, float scale, cudaStream_t st);
+
+// ---- attention of one new query per sequence over a KV cache (k_decode.cu):
+// q [B, H, dh], caches [B, Hkv, max_seq, dh] (positions [0, L) read), o [B, H*dh]
+// bf16; part holds decode_partial_floats(B, H, max_seq, dh) floats of scratch.
+size_t decode_partial_floats(int B, int H, int max_seq, int dh);
+bool decode_supported(int dh, int group);
+cudaError_t launch_decode_attention(const void* q, const void* kc, const void* vc, float* part,
+                                    void* o, int B, int H, int Hkv, int max_seq, int L, int dh,
+                                    float scale, cudaStream_t st);
 
 // ---- bf16 flash attention on tcgen05 (k_attention_tc.cu), dh in {64, 128}
 struct AttnPlan {

@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n0 = tile_n(t) * n_per_tile;
             if (rope_pre) {
                 const int r = m0 + q * 32 + lane;
-                const int pos = (r < M ? r : 0) % epi.S;
+                const int pos = epi.pos0 + (r < M ? r : 0) % epi.S;
                 load_vec<32>(epi.rope_cs + ((int64_t)pos * (epi.dh / 2) + rope_d0 / 2) * 2, rcs);
             }
             if (!warp_wait(tfull_bar(acc), acc_phase, err, abort_flag)) break;

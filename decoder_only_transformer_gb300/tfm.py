@@ -59,6 +59,9 @@ _SIGS = {
     "tfm_forward_host": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
     "tfm_forward_host_async": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
     "tfm_forward_host_join": ([_V, _V], _I32),
+    "tfm_kv_cache_create": ([_V], _I32),
+    "tfm_prefill": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
+    "tfm_decode_step": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
     "tfm_forward_graph": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
     "tfm_device_status": ([_V], _I32),
     "tfm_selftest_wait_timeout": ([_I32, _V], _I32),
@@ -234,6 +237,23 @@ class Model:
     def forward_host_join(self, stream=None):
         """Makes the stream wait for every logits copy issued so far."""
         _check(self.lib.tfm_forward_host_join(self.handle, _stream(stream)))
+
+    def kv_cache_create(self):
+        """Allocates the KV cache (bf16 mode) used by prefill / decode_step."""
+        _check(self.lib.tfm_kv_cache_create(self.handle))
+
+    def prefill(self, tokens, logits, stream=None):
+        """forward() that also fills the KV cache with positions [0, S)."""
+        B, S = tokens.shape
+        _check(self.lib.tfm_prefill(self.handle, _ptr(tokens), B, S, _ptr(logits),
+                                    logits.stride(0), _stream(stream)))
+
+    def decode_step(self, tokens, pos, logits, stream=None):
+        """tokens: int32 [B] (device), the new token of every sequence at position
+        pos (the cached length); logits: fp32 [B, ld] (device)."""
+        B = tokens.shape[0]
+        _check(self.lib.tfm_decode_step(self.handle, _ptr(tokens), B, int(pos), _ptr(logits),
+                                        logits.stride(0), _stream(stream)))
 
     def profile(self, enable: bool = True):
         _check(self.lib.tfm_profile_enable(self.handle, 1 if enable else 0))

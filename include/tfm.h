@@ -184,6 +184,33 @@ tfm_status tfm_forward_host_async(void* handle, const int32_t* tokens_host, int3
  * tfm_forward_host_async has issued on this handle so far. */
 tfm_status tfm_forward_host_join(void* handle, void* stream);
 
+/* ---- Incremental decoding with a KV cache ("LLM 2", sections KV cache and
+ * GQA / MQA: keys and values of the positions already seen are kept, a new token
+ * computes only its own q, k, v).  bf16 mode; d_head in {32, 64, 128}; H / Hkv in
+ * {1, 2, 4, 8, 16}. */
+
+/* Allocates the handle's cache once: per layer K and V, [max_batch, n_kv_head,
+ * max_seq, d_head] bf16 (2 * n_layer * max_batch * n_kv_head * max_seq * d_head
+ * * 2 bytes), plus the decode attention's scratch.  TFM_ENOMEM if it does not
+ * fit, TFM_EUNSUPPORTED outside the shapes above.  Freed by tfm_destroy. */
+tfm_status tfm_kv_cache_create(void* handle);
+
+/* tfm_forward (same arguments and results) that also stores every layer's k
+ * (after RoPE) and v of positions [0, S) of sequences [0, B) in the cache; the
+ * cache then holds S positions for B sequences. */
+tfm_status tfm_prefill(void* handle, const int32_t* tokens, int32_t B, int32_t S, float* logits,
+                       int64_t ld_logits, void* stream);
+
+/* One new token per sequence: tokens [B] (device) at position pos, which must be
+ * the cached length (pos < max_seq; B the prefill's batch).  Appends its k, v to
+ * every layer's cache and writes logits [B, ld_logits] (row b: the scores of the
+ * next token after position pos of sequence b, columns [0, vocab)), the same as
+ * row pos of tfm_forward over the sequence extended by this token.  The cached
+ * length becomes pos + 1.  Calls on a handle are ordered on the host in the order
+ * they are made (the length is advanced at enqueue time). */
+tfm_status tfm_decode_step(void* handle, const int32_t* tokens, int32_t B, int32_t pos,
+                           float* logits, int64_t ld_logits, void* stream);
+
 /* Synchronises the device, then returns and clears the sticky device error word
  * (TFM_OK, TFM_EBADTOKEN or TFM_ETIMEOUT), or TFM_ECUDA if the context faulted.
  * handle may be NULL (component calls share the same word). */

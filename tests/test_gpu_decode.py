@@ -1,0 +1,103 @@
+"""Incremental decoding with the KV cache (tfm_kv_cache_create, tfm_prefill,
+tfm_decode_step) on the GPU.
+
+A decode step at position p must give the logits of row p of the forward over
+the sequence extended by the new token: checked against the CPU oracle (float64
+forward over the whole extended sequence, the tolerances of the forward tests)
+and against the GPU's own forward (bf16 rounding differs only inside attention).
+The steps cross the decode kernel's 256-key chunks."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from helpers import argmax_agreement, rel_err, tie_aware_agreement, to_torch_weights
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from decoder_only_transformer_gb300 import tfm  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tfm.load()
+    yield
+
+
+def _model(cfg, w, B, S):
+    model = tfm.Model(cfg, max_batch=B, max_seq=S)
+    model.load_weights(to_torch_weights(w, bf16=True))
+    model.kv_cache_create()
+    return model
+
+
+@pytest.mark.parametrize("name,B,S0,T", [
+    ("small", 2, 250, 12),        # d_head 32, crosses the 256-key chunk
+    ("gpt2s", 3, 37, 5),          # d_head 64
+    ("gqa", 2, 300, 6),           # d_head 128, 4 query heads per kv head, 2 chunks
+])
+def test_decode_matches_oracle_and_forward(name, B, S0, T):
+    cfg = workloads.get_config(name).replace(n_layer=2, vocab=3001)
+    w = workloads.make_weights(cfg, gains="random")
+    tok = workloads.make_tokens(cfg, batch=B, seq=S0 + T, seed=77)
+    ld = (cfg.vocab + 3) // 4 * 4
+    model = _model(cfg, w, B, S0 + T)
+    dtok = torch.from_numpy(tok).cuda()
+    pre = torch.empty(B * S0, ld, device="cuda")
+    model.prefill(dtok[:, :S0].contiguous(), pre)
+    steps = []
+    for t in range(T):
+        lg = torch.empty(B, ld, device="cuda")
+        model.decode_step(dtok[:, S0 + t].contiguous(), S0 + t, lg)
+        steps.append(lg)
+    torch.cuda.synchronize()
+    tfm.device_status()
+    dec = torch.stack(steps, 1).cpu().numpy()[:, :, : cfg.vocab]       # [B, T, V]
+
+    # GPU forward over the whole sequence: rows S0.. match the decode steps
+    full = torch.empty(B * (S0 + T), ld, device="cuda")
+    model.forward(dtok, full)
+    full = full.cpu().numpy().reshape(B, S0 + T, ld)[:, :, : cfg.vocab]
+    assert np.array_equal(pre.cpu().numpy().reshape(B, S0, ld)[:, :, : cfg.vocab], full[:, :S0])
+    # (the forward's attention rounds P to bf16 before P.V, the decode kernel keeps
+    # p in fp32: the two differ by bf16 rounding, carried through later layers)
+    assert rel_err(dec, full[:, S0:]) < 1e-2
+
+    # the oracle over the extended sequences
+    ref = oracle.forward(tok, w, cfg)[:, S0:]
+    assert rel_err(dec, ref) < 2e-2, rel_err(dec, ref)
+    if argmax_agreement(dec, ref) < 0.999:
+        assert tie_aware_agreement(dec, ref) >= 0.999
+    model.close()
+
+
+def test_decode_argument_checks():
+    cfg = workloads.get_config("small").replace(n_layer=1, vocab=1000)
+    w = workloads.make_weights(cfg)
+    model = tfm.Model(cfg, max_batch=2, max_seq=64)
+    model.load_weights(to_torch_weights(w, bf16=True))
+    tok = torch.zeros(2, 8, dtype=torch.int32, device="cuda")
+    lg = torch.empty(16, 1000, device="cuda")
+    one = torch.zeros(2, dtype=torch.int32, device="cuda")
+    lg1 = torch.empty(2, 1000, device="cuda")
+    with pytest.raises(tfm.TfmError):             # no cache yet
+        model.prefill(tok, lg)
+    model.kv_cache_create()
+    model.prefill(tok, lg)
+    with pytest.raises(tfm.TfmError):             # position must be the cached length
+        model.decode_step(one, 9, lg1)
+    with pytest.raises(tfm.TfmError):             # batch must be the prefill's
+        model.decode_step(one[:1], 8, lg1[:1])
+    model.decode_step(one, 8, lg1)
+    model.decode_step(one, 9, lg1)
+    torch.cuda.synchronize()
+    tfm.device_status()
+    model.close()
+    f32 = workloads.get_config("tiny")
+    m2 = tfm.Model(f32, max_batch=1, max_seq=16)
+    with pytest.raises(tfm.TfmError):             # fp32 mode has no KV cache
+        m2.kv_cache_create()
+    m2.close()
