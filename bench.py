@@ -145,6 +145,58 @@ def kernel_table(cfg, B, S, prof, peaks):
     return out
 
 
+def decode_rate(tfm, torch, model, cfg, tok_np, stream, peaks, steps=32):
+    """Incremental decoding on the workload's batch: prefill the first S - steps
+    positions into the KV cache, then `steps` decode steps (one new token per
+    sequence each), timed with CUDA events around all steps (direct launches).
+    The decode attention's HBM fraction uses its algorithmic bytes: the cached
+    K and V of positions [0, pos] read once, q read, o written, the fp32 chunk
+    partials written and read back."""
+    B, S = tok_np.shape
+    S0 = S - steps
+    dh, H, Hkv = cfg.d_head, cfg.n_head, cfg.n_kv_head
+    ld = (cfg.vocab + 3) // 4 * 4
+    model.kv_cache_create()
+    dtok = torch.from_numpy(tok_np).cuda()
+    pre = torch.empty(B * S0, ld, device="cuda")
+    lg = torch.empty(B, ld, device="cuda")
+    cols = [dtok[:, S0 + t].contiguous() for t in range(steps)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    model.prefill(dtok[:, :S0].contiguous(), pre, stream)
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for t in range(steps):
+        model.decode_step(cols[t], S0 + t, lg, stream)
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    ms = ev[0].elapsed_time(ev[1])
+    # the same steps again, profiled per kernel kind (events after every kernel)
+    model.prefill(dtok[:, :S0].contiguous(), pre, stream)
+    model.profile(True)
+    for t in range(steps):
+        model.decode_step(cols[t], S0 + t, lg, stream)
+    torch.cuda.synchronize()
+    model.profile(False)
+    prof = model.profile_read()
+    tfm.device_status()
+    att_ms, att_n = prof["attention"]
+    nbytes = 0
+    for t in range(steps):
+        L = S0 + t + 1
+        nch = (L + 255) // 256
+        nbytes += (2 * B * Hkv * L * dh * 2 + 2 * B * H * dh * 2
+                   + 2 * B * H * nch * (dh + 2) * 4) * cfg.n_layer
+    gbs = nbytes / (att_ms / 1e3) / 1e9 if att_ms > 0 else None
+    return {"value": B * steps / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms / steps,
+            "batch": B, "prefill_len": S0, "steps": steps,
+            "attention": {"bound": "hbm", "achieved": round(gbs, 1) if gbs else None,
+                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                          "frac": round(gbs / peaks["hbm_gbs"], 4) if gbs else None,
+                          "avg_us_per_layer": round(att_ms * 1e3 / max(1, att_n // 2), 2)},
+            "how": "tfm_prefill of the first S - steps positions, then tfm_decode_step per "
+                   "position (direct launches); CUDA events around all steps"}
+
+
 def rmsnorm_hbm(tfm, torch, stream, peaks, rows=131072, d=2048, launches=20):
     """RMSNorm alone on a working set far above L2 (fp32 in 1 GiB, bf16 out),
     so that its bytes come from HBM: the bandwidth figure the in-forward
@@ -275,6 +327,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="time direct launches instead of the recorded (CUDA graph) forward")
     return ap.parse_args()
@@ -457,6 +510,8 @@ def main():
                       "joined after the last step; CUDA events around all K steps, inputs "
                       "from pinned host memory every step (no L2 flush in this region)"}
     rms = rmsnorm_hbm(tfm, torch, stream, load_peaks()) if rank == 0 else None
+    decode = (decode_rate(tfm, torch, model, cfg, tok_np, stream, load_peaks())
+              if rank == 0 and cfg.mode == "bf16" and not args.no_decode else None)
     rows = sampler.stop()
     clocks = ClockSampler.summary(rows)
     clocks["window_s"] = round(t_wall1 - t_wall0, 3)
@@ -509,6 +564,7 @@ def main():
                         "whole_forward_tflops": round(total_flops / (ms_per_step / 1e3) / 1e12, 1)},
         "kernels": kernels,
         "rmsnorm_hbm": rms,
+        "decode": decode,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": (2 + 7 * cfg.n_layer) * args.steps,

@@ -630,8 +630,15 @@ tfm_status build_decode_plans(Model* m, int B, float* logits, int64_t ld) {
     m->dplan_B = -1;
     tfm_status st = TFM_OK;
     for (int l = 0; l < c.n_layer && st == TFM_OK; ++l) {
-        st = plan_gemm_tc(&m->d_qkv[l], m->xn(), s.D, m->wqkv[l], nullptr, s.D, B, (int)s.Nqkv,
-                          (int)s.D, epi_qkv(m, B, 1));
+        {
+            // k and v of the new token go straight into the layer's cache
+            EpiParams e = epi_qkv(m, B, 1);
+            e.k = m->kcache(l);
+            e.v = m->vcache(l);
+            e.kv_stride = c.max_seq;
+            st = plan_gemm_tc(&m->d_qkv[l], m->xn(), s.D, m->wqkv[l], nullptr, s.D, B,
+                              (int)s.Nqkv, (int)s.D, e);
+        }
         if (st == TFM_OK)
             st = plan_gemm_tc(&m->d_o[l], m->o(), s.Dq, m->wo[l], nullptr, s.Dq, B, (int)s.D,
                               (int)s.Dq, epi_basic(EPI_ACCUM_F32, B, (int)s.D, m->h(), s.D));
@@ -678,20 +685,12 @@ tfm_status decode_impl(Model* m, const int32_t* tokens, int B, int pos, float* l
                                              c.n_layer > 0 ? m->attn_norm[0] : m->final_norm,
                                              m->h(), m->xn(), B, c.vocab, c.d_model, c.norm_eps,
                                              1, st));
-    const size_t row = (size_t)dh * 2, pitch = (size_t)c.max_seq * dh * 2;
-    const size_t rows = (size_t)B * c.n_kv_head;
     for (int l = 0; l < c.n_layer; ++l) {
         if (l > 0)
             TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), B, c.d_model, c.norm_eps, 1, st));
+        // RoPE at position pos; the token's k, v land at position pos of the cache
         m->d_qkv[l].epi.pos0 = pos;
         TFM_LAUNCH(K_QKV, launch_gemm_tc(m->d_qkv[l], st));
-        // the token's k, v at position pos of every (sequence, kv head) row
-        cudaError_t e = cudaMemcpy2DAsync(static_cast<uint8_t*>(m->kcache(l)) + (size_t)pos * row,
-                                          pitch, m->k(), row, row, rows, cudaMemcpyDeviceToDevice, st);
-        if (e == cudaSuccess)
-            e = cudaMemcpy2DAsync(static_cast<uint8_t*>(m->vcache(l)) + (size_t)pos * row, pitch,
-                                  m->v(), row, row, rows, cudaMemcpyDeviceToDevice, st);
-        if (e != cudaSuccess) return cuda_fail(e, "k, v into the cache");
         TFM_LAUNCH(K_ATTN, launch_decode_attention(m->q(), m->kcache(l), m->vcache(l), m->dec_part,
                                                    m->o(), B, c.n_head, c.n_kv_head, c.max_seq,
                                                    pos + 1, dh, scale, st));
@@ -849,7 +848,7 @@ tfm_status tfm_kv_cache_create(void* handle) {
     const int dh = c.d_model / c.n_head;
     if (c.mode != TFM_BF16) return fail(TFM_EUNSUPPORTED, "the KV cache needs bf16 mode");
     if (!tfm::decode_supported(dh, c.n_head / c.n_kv_head))
-        return fail(TFM_EUNSUPPORTED, "decode needs d_head in {32, 64, 128} and H/Hkv in {1, 2, 4, 8, 16}");
+        return fail(TFM_EUNSUPPORTED, "decode needs d_head in {32, 64, 128} and H/Hkv in {1, 2, 4, 8, 16} (<= 8 at d_head 128)");
     const size_t layer = (size_t)c.max_batch * c.n_kv_head * c.max_seq * dh * 2;
     const size_t caches = (size_t)c.n_layer * 2 * layer;
     const size_t part = tfm::decode_partial_floats(c.max_batch, c.n_head, c.max_seq, dh) * 4;

@@ -131,6 +131,16 @@ __device__ __forceinline__ QkvSlot qkv_slot(const EpiParams& p, int col0) {
     return r;
 }
 
+// Element offset of position s of sequence b in a chunk's head-major buffer: q
+// [B, H, S, dh]; k, v the same with n_kv_head heads, or, with kv_stride set, a
+// KV cache [B, n_kv_head, kv_stride, dh] at position pos0 + s.
+__device__ __forceinline__ int64_t qkv_offset(const EpiParams& p, const QkvSlot& q, int b, int s) {
+    const bool cache = q.region > 0 && p.kv_stride > 0;
+    const int64_t stride = cache ? p.kv_stride : p.S;
+    const int64_t pos = cache ? (int64_t)p.pos0 + s : s;
+    return (((int64_t)b * q.heads + q.head) * stride + pos) * p.dh + q.d0;
+}
+
 // Output values of one chunk: a = accumulator columns [col0, col0+W) of output
 // row `row`; u = the matching "up" columns for EPI_SWIGLU (ignored otherwise).
 // For EPI_QKV_ROPE the chunk lies inside one head (W divides dh), col0 % W == 0.
@@ -193,7 +203,7 @@ __device__ __forceinline__ void epi_store_direct(const EpiParams& p, int row, in
             const QkvSlot q = qkv_slot(p, col0);
             void* base = q.region == 0 ? p.q : (q.region == 1 ? p.k : p.v);
             const int b = row / p.S, s = row - b * p.S;
-            const int64_t off = (((int64_t)b * q.heads + q.head) * p.S + s) * p.dh + q.d0;
+            const int64_t off = qkv_offset(p, q, b, s);
             if (p.out_bf16)
                 store_row_bf16<W>(static_cast<__nv_bfloat16*>(base) + off, o, W);
             else

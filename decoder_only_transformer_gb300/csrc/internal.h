@@ -29,6 +29,9 @@ struct EpiParams {
     // cache length for a decode step)
     int S, n_head, n_kv_head, dh;
     int pos0;
+    // k and v into a KV cache instead: [B, n_kv_head, kv_stride, dh] at position
+    // pos0 + s (0: head-major like q, [B, n_kv_head, S, dh])
+    int kv_stride;
     const float* rope_cs;    // [>= S, dh/2, 2]: cos, sin of s * theta^(-2i/dh)
     void* q;
     void* k;

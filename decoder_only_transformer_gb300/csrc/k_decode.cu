@@ -29,9 +29,11 @@ __global__ void __launch_bounds__(kDecThreads) k_decode_partial(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
     const __nv_bfloat16* __restrict__ vc, float* __restrict__ part, int H, int Hkv, int max_seq,
     int L, int nch, float scale_log2) {
+    constexpr int NW = kDecThreads / 32;
     __shared__ float qs[G][DH];
     __shared__ float ps[G][kDecChunk];
-    __shared__ float red[G][kDecThreads / 32];
+    __shared__ float red[G][NW];
+    __shared__ float osum[NW][G][DH];
     pdl_wait();
     pdl_trigger();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -115,21 +117,64 @@ __global__ void __launch_bounds__(kDecThreads) k_decode_partial(
         if (lane == 0) red[hh][warp] = v;
     }
     __syncthreads();
-    // o_h[d] = sum_t p_h[t] v_t[d]: thread slots (head, column pair), v rows read
-    // along the columns (consecutive threads, consecutive pairs).
-    for (int i = tid; i < G * (DH / 2); i += kDecThreads) {
-        const int hh = i / (DH / 2), d2 = i - hh * (DH / 2);
-        float a0 = 0.f, a1 = 0.f;
-        const uint32_t* vr = reinterpret_cast<const uint32_t*>(vb) + d2;
-        for (int t = 0; t < n; ++t) {
-            const uint32_t w = __ldg(vr + (int64_t)t * (DH / 2));
-            const float p = ps[hh][t];
-            a0 = fmaf(p, bf16_lo(w), a0);
-            a1 = fmaf(p, bf16_hi(w), a1);
+    // o_h[d] = sum_t p_h[t] v_t[d]: warp w takes keys [64 w, 64 w + 64); lane l
+    // reads 16 bytes (8 columns, chunk l % CPR) of rows l / CPR + RPI i, so one
+    // warp load covers RPI whole rows and eight loads are in flight per step; a v
+    // row is applied to all G heads.  The lanes of a chunk are then summed with
+    // shuffles and the four warps through shared memory.
+    {
+        constexpr int CPR = DH / 8;                  // 16-byte chunks per row
+        constexpr int RPI = 32 / CPR;                // rows per warp load
+        constexpr int KPW = kDecChunk / NW;          // keys per warp
+        const int cl = lane % CPR, rl = lane / CPR;
+        float acc[G][8];
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[hh][e] = 0.f;
+        const int t0 = warp * KPW;
+        for (int i0 = 0; i0 < KPW; i0 += 8 * RPI) {
+            uint4 w[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = t0 + i0 + u * RPI + rl;
+                w[u] = t < n ? __ldg(reinterpret_cast<const uint4*>(vb + (int64_t)t * DH) + cl)
+                             : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = t0 + i0 + u * RPI + rl;
+                const float v8[8] = {bf16_lo(w[u].x), bf16_hi(w[u].x), bf16_lo(w[u].y), bf16_hi(w[u].y),
+                                     bf16_lo(w[u].z), bf16_hi(w[u].z), bf16_lo(w[u].w), bf16_hi(w[u].w)};
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    const float p = ps[hh][t];           // 0 past n
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[hh][e] = fmaf(p, v8[e], acc[hh][e]);
+                }
+            }
         }
-        float* dst = part + ((int64_t)(b * H + h0 + hh) * nch + c) * (DH + 2);
-        dst[2 * d2] = a0;
-        dst[2 * d2 + 1] = a1;
+        // lanes cl, cl + CPR, ... hold the same columns
+#pragma unroll
+        for (int off = CPR; off < 32; off <<= 1)
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[hh][e] += __shfl_xor_sync(0xffffffffu, acc[hh][e], off);
+        if (rl == 0) {
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) osum[warp][hh][cl * 8 + e] = acc[hh][e];
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < G * DH; i += kDecThreads) {
+        const int hh = i / DH, d = i - hh * DH;
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) v += osum[w][hh][d];
+        part[((int64_t)(b * H + h0 + hh) * nch + c) * (DH + 2) + d] = v;
     }
     if (tid < G) {
         float l = 0.f, m = mh[0];
@@ -199,7 +244,11 @@ cudaError_t decode_dh(const void* q, const void* kc, const void* vc, float* part
         case 2: return decode_launch<DH, 2>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, st);
         case 4: return decode_launch<DH, 4>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, st);
         case 8: return decode_launch<DH, 8>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, st);
-        case 16: return decode_launch<DH, 16>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, st);
+        case 16:
+            // 16 heads of 128 columns would need 57.6 KB of static shared memory
+            if constexpr (DH <= 64)
+                return decode_launch<DH, 16>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, st);
+            return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
 }
@@ -212,7 +261,7 @@ size_t decode_partial_floats(int B, int H, int max_seq, int dh) {
 
 bool decode_supported(int dh, int group) {
     return (dh == 32 || dh == 64 || dh == 128) &&
-           (group == 1 || group == 2 || group == 4 || group == 8 || group == 16);
+           (group == 1 || group == 2 || group == 4 || group == 8 || (group == 16 && dh <= 64));
 }
 
 cudaError_t launch_decode_attention(const void* q, const void* kc, const void* vc, float* part,

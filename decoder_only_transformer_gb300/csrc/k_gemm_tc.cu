@@ -156,7 +156,7 @@ __device__ __forceinline__ void flush_block(const EpiParams& p, uint32_t buf, in
         if (row >= p.M || ncol >= p.N) continue;
         __nv_bfloat16* d;
         if (p.kind == EPI_QKV_ROPE) {
-            d = qbase + (((int64_t)b * qs.heads + qs.head) * p.S + pos) * p.dh + qs.d0 + seg * 8;
+            d = qbase + qkv_offset(p, qs, b, pos) + seg * 8;
         } else {
             d = static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * p.ldo + ncol;
         }
@@ -620,7 +620,8 @@ bool plan_tma_out(TcMaps* maps, const EpiParams& e) {
             return e.out_bf16 && e.out && aligned16_ptr(e.out) && (e.ldo * 2) % 16 == 0 &&
                    make_out_map(&maps->out, e.out, e.M, e.N, e.ldo, true);
         case EPI_QKV_ROPE: {
-            if (!e.out_bf16 || e.S <= 0 || e.S % 32 != 0 || e.dh % 32 != 0 || e.M % e.S != 0)
+            if (!e.out_bf16 || e.S <= 0 || e.S % 32 != 0 || e.dh % 32 != 0 || e.M % e.S != 0 ||
+                e.kv_stride != 0)
                 return false;
             if (!aligned16_ptr(e.q) || !aligned16_ptr(e.k) || !aligned16_ptr(e.v)) return false;
             const int64_t B = e.M / e.S;

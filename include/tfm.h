@@ -187,7 +187,7 @@ tfm_status tfm_forward_host_join(void* handle, void* stream);
 /* ---- Incremental decoding with a KV cache ("LLM 2", sections KV cache and
  * GQA / MQA: keys and values of the positions already seen are kept, a new token
  * computes only its own q, k, v).  bf16 mode; d_head in {32, 64, 128}; H / Hkv in
- * {1, 2, 4, 8, 16}. */
+ * {1, 2, 4, 8, 16} (at most 8 for d_head 128). */
 
 /* Allocates the handle's cache once: per layer K and V, [max_batch, n_kv_head,
  * max_seq, d_head] bf16 (2 * n_layer * max_batch * n_kv_head * max_seq * d_head
