@@ -183,7 +183,7 @@ def decode_rate(tfm, torch, model, cfg, tok_np, stream, peaks, steps=32):
     nbytes = 0
     for t in range(steps):
         L = S0 + t + 1
-        nch = (L + 255) // 256
+        nch = (L + 16384 // dh - 1) // (16384 // dh)   # chunks of 16384 / dh keys
         nbytes += (2 * B * Hkv * L * dh * 2 + 2 * B * H * dh * 2
                    + 2 * B * H * nch * (dh + 2) * 4) * cfg.n_layer
     gbs = nbytes / (att_ms / 1e3) / 1e9 if att_ms > 0 else None
@@ -192,7 +192,7 @@ def decode_rate(tfm, torch, model, cfg, tok_np, stream, peaks, steps=32):
             "attention": {"bound": "hbm", "achieved": round(gbs, 1) if gbs else None,
                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
                           "frac": round(gbs / peaks["hbm_gbs"], 4) if gbs else None,
-                          "avg_us_per_layer": round(att_ms * 1e3 / max(1, att_n // 2), 2)},
+                          "avg_us_per_layer": round(att_ms * 1e3 / max(1, att_n), 2)},
             "how": "tfm_prefill of the first S - steps positions, then tfm_decode_step per "
                    "position (direct launches); CUDA events around all steps"}
 
@@ -328,6 +328,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="only the incremental-decoding measurement (prefill, then decode "
+                         "steps); prints its JSON object alone")
     ap.add_argument("--no-graph", action="store_true",
                     help="time direct launches instead of the recorded (CUDA graph) forward")
     return ap.parse_args()
@@ -429,6 +432,12 @@ def main():
     stream = torch.cuda.Stream()
     torch.cuda.set_stream(stream)
     run = model.forward if args.no_graph else model.forward_graph
+    if args.decode_only:
+        peaks = load_peaks()
+        print(json.dumps({"decode": decode_rate(tfm, torch, model, cfg, tok_np, stream, peaks),
+                          "config": {"workload": WORKLOAD_TEXT[cfg.name]}}))
+        model.close()
+        return
 
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     sampler = ClockSampler(int(vis.split(",")[local]) if vis and vis.split(",")[local].isdigit()

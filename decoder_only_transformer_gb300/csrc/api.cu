@@ -212,6 +212,10 @@ struct Model {
     uint8_t* kv = nullptr;
     size_t kv_layer_bytes = 0;      // one of K or V of one layer
     float* dec_part = nullptr;
+    int* pos_dev = nullptr;         // position of the decode step being run (device word)
+    int32_t* tok_dev = nullptr;     // its tokens [max_batch]
+    Graph dgraphs[2];               // recorded decode steps (position, tokens read on the device)
+    Graph dlast;                    // arguments of the previous decode step
     int kv_len = 0, kv_batch = 0;
     // tensor-core plans of a decode step (M = batch rows), cached by batch and logits
     std::vector<GemmPlan> d_qkv, d_o, d_gu, d_down;
@@ -347,6 +351,8 @@ void tfm_destroy(void* handle) {
     if (!m) return;
     if (m->copy_st) cudaStreamSynchronize(m->copy_st);
     for (auto& g : m->graphs)
+        if (g.exec) cudaGraphExecDestroy(g.exec);
+    for (auto& g : m->dgraphs)
         if (g.exec) cudaGraphExecDestroy(g.exec);
     for (int b = 0; b < 2; ++b) {
         if (m->fwd_done[b]) cudaEventDestroy(m->fwd_done[b]);
@@ -494,6 +500,10 @@ tfm_status build_plans(Model* m, int M, int S, float* logits, int64_t ld) {
         st = plan_gemm_tc(&m->p_lm, m->xn(), s.D, m->lm_head, nullptr, s.D, M, (int)s.V, (int)s.D,
                           epi_basic(EPI_STORE_F32, M, (int)s.V, logits, ld));
     if (st != TFM_OK) return fail(st, "could not encode TMA tensor maps (driver entry point missing?)");
+    // the model's weights: no launch writes them once loaded
+    for (int l = 0; l < c.n_layer; ++l)
+        m->p_qkv[l].b_static = m->p_o[l].b_static = m->p_gu[l].b_static = m->p_down[l].b_static = 1;
+    m->p_lm.b_static = 1;
     m->plan_m = M;
     m->plan_S = S;
     const int dh = c.d_model / c.n_head;
@@ -550,11 +560,11 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
     TFM_LAUNCH(K_EMBED, launch_embed_rmsnorm(tokens, m->embed,
                                              c.n_layer > 0 ? m->attn_norm[0] : m->final_norm,
                                              m->h(), m->xn(), M, c.vocab, c.d_model, c.norm_eps,
-                                             bf, st));
+                                             bf, st, 1));
     if (bf) {
         for (int l = 0; l < c.n_layer; ++l) {
             if (l > 0)
-                TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 1, st));
+                TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 1, st, 1));
             TFM_LAUNCH(K_QKV, launch_gemm_tc(m->p_qkv[l], st));
             if (to_cache) {
                 // k, v of positions [0, S) into the layer's cache: rows (b, kv head)
@@ -574,18 +584,18 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
                 TFM_LAUNCH(K_ATTN, launch_attention_bf16(m->q(), m->k(), m->v(), m->o(), B,
                                                          c.n_head, c.n_kv_head, S, dh, scale, st));
             TFM_LAUNCH(K_OPROJ, launch_gemm_tc(m->p_o[l], st));
-            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->ffn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 1, st));
+            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->ffn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 1, st, 1));
             TFM_LAUNCH(K_GATEUP, launch_gemm_tc(m->p_gu[l], st));
             TFM_LAUNCH(K_DOWN, launch_gemm_tc(m->p_down[l], st));
         }
         if (c.n_layer > 0)
-            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->final_norm, m->xn(), M, c.d_model, c.norm_eps, 1, st));
+            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->final_norm, m->xn(), M, c.d_model, c.norm_eps, 1, st, 1));
         TFM_LAUNCH(K_LMHEAD, launch_gemm_tc(m->p_lm, st));
     } else {
         const float* xn = static_cast<const float*>(m->xn());
         for (int l = 0; l < c.n_layer; ++l) {
             if (l > 0)
-                TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 0, st));
+                TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 0, st, 1));
             TFM_LAUNCH(K_QKV, launch_gemm_simt(xn, static_cast<const float*>(m->wqkv[l]), nullptr, M,
                                                (int)s.Nqkv, c.d_model, epi_qkv(m, M, S), st));
             TFM_LAUNCH(K_ATTN, launch_attention_simt(static_cast<const float*>(m->q()),
@@ -597,7 +607,7 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
                                                  static_cast<const float*>(m->wo[l]), nullptr, M,
                                                  c.d_model, (int)s.Dq,
                                                  epi_basic(EPI_ACCUM_F32, M, c.d_model, m->h(), s.D), st));
-            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->ffn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 0, st));
+            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->ffn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 0, st, 1));
             EpiParams e = epi_basic(EPI_SWIGLU, M, c.d_ff, m->a(), s.F);
             e.out_bf16 = 0;
             TFM_LAUNCH(K_GATEUP, launch_gemm_simt(xn, static_cast<const float*>(m->w1[l]),
@@ -609,7 +619,7 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
                                                 epi_basic(EPI_ACCUM_F32, M, c.d_model, m->h(), s.D), st));
         }
         if (c.n_layer > 0)
-            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->final_norm, m->xn(), M, c.d_model, c.norm_eps, 0, st));
+            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->final_norm, m->xn(), M, c.d_model, c.norm_eps, 0, st, 1));
         TFM_LAUNCH(K_LMHEAD, launch_gemm_simt(xn, static_cast<const float*>(m->lm_head), nullptr, M,
                                               c.vocab, c.d_model,
                                               epi_basic(EPI_STORE_F32, M, c.vocab, logits, ld), st));
@@ -636,6 +646,7 @@ tfm_status build_decode_plans(Model* m, int B, float* logits, int64_t ld) {
             e.k = m->kcache(l);
             e.v = m->vcache(l);
             e.kv_stride = c.max_seq;
+            e.pos0_dev = m->pos_dev;        // RoPE and cache position of the step
             st = plan_gemm_tc(&m->d_qkv[l], m->xn(), s.D, m->wqkv[l], nullptr, s.D, B,
                               (int)s.Nqkv, (int)s.D, e);
         }
@@ -656,16 +667,21 @@ tfm_status build_decode_plans(Model* m, int B, float* logits, int64_t ld) {
         st = plan_gemm_tc(&m->d_lm, m->xn(), s.D, m->lm_head, nullptr, s.D, B, (int)s.V, (int)s.D,
                           epi_basic(EPI_STORE_F32, B, (int)s.V, logits, ld));
     if (st != TFM_OK) return fail(st, "could not encode TMA tensor maps (driver entry point missing?)");
+    for (int l = 0; l < c.n_layer; ++l)
+        m->d_qkv[l].b_static = m->d_o[l].b_static = m->d_gu[l].b_static = m->d_down[l].b_static = 1;
+    m->d_lm.b_static = 1;
     m->dplan_B = B;
     m->dplan_logits = logits;
     m->dplan_ld = ld;
     return TFM_OK;
 }
 
-// One decode step: token t_b of every sequence b at position pos, the cache
-// holding positions [0, pos).  The same blocks as the forward with M = B; each
-// layer appends the token's k, v to its cache and attends over [0, pos].
-tfm_status decode_impl(Model* m, const int32_t* tokens, int B, int pos, float* logits, int64_t ld,
+// One decode step: token t_b of every sequence b at position *pos_dev, the cache
+// holding positions [0, *pos_dev).  The same blocks as the forward with M = B;
+// each layer writes the token's k, v into its cache (from the QKV epilogue) and
+// attends over [0, *pos_dev].  Nothing here depends on the position on the host,
+// so the launches can be recorded once and replayed at every position.
+tfm_status decode_body(Model* m, const int32_t* tokens, int B, float* logits, int64_t ld,
                        cudaStream_t st) {
     const tfm_config& c = m->cfg;
     const int dh = c.d_model / c.n_head;
@@ -684,25 +700,75 @@ tfm_status decode_impl(Model* m, const int32_t* tokens, int B, int pos, float* l
     TFM_LAUNCH(K_EMBED, launch_embed_rmsnorm(tokens, m->embed,
                                              c.n_layer > 0 ? m->attn_norm[0] : m->final_norm,
                                              m->h(), m->xn(), B, c.vocab, c.d_model, c.norm_eps,
-                                             1, st));
+                                             1, st, 1));
     for (int l = 0; l < c.n_layer; ++l) {
         if (l > 0)
-            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), B, c.d_model, c.norm_eps, 1, st));
-        // RoPE at position pos; the token's k, v land at position pos of the cache
-        m->d_qkv[l].epi.pos0 = pos;
+            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), B, c.d_model, c.norm_eps, 1, st, 1));
         TFM_LAUNCH(K_QKV, launch_gemm_tc(m->d_qkv[l], st));
         TFM_LAUNCH(K_ATTN, launch_decode_attention(m->q(), m->kcache(l), m->vcache(l), m->dec_part,
                                                    m->o(), B, c.n_head, c.n_kv_head, c.max_seq,
-                                                   pos + 1, dh, scale, st));
+                                                   m->pos_dev, dh, scale, st));
         TFM_LAUNCH(K_OPROJ, launch_gemm_tc(m->d_o[l], st));
-        TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->ffn_norm[l], m->xn(), B, c.d_model, c.norm_eps, 1, st));
+        TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->ffn_norm[l], m->xn(), B, c.d_model, c.norm_eps, 1, st, 1));
         TFM_LAUNCH(K_GATEUP, launch_gemm_tc(m->d_gu[l], st));
         TFM_LAUNCH(K_DOWN, launch_gemm_tc(m->d_down[l], st));
     }
     if (c.n_layer > 0)
-        TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->final_norm, m->xn(), B, c.d_model, c.norm_eps, 1, st));
+        TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->final_norm, m->xn(), B, c.d_model, c.norm_eps, 1, st, 1));
     TFM_LAUNCH(K_LMHEAD, launch_gemm_tc(m->d_lm, st));
     return TFM_OK;
+}
+
+// The step at position pos: the position and the tokens are stored on the
+// device, then the body runs.  A step with the same batch, logits and stream as
+// the previous one is recorded once and replayed from then on (not when
+// profiling, nor on the legacy stream, which cannot be captured).
+tfm_status decode_impl(Model* m, const int32_t* tokens, int B, int pos, float* logits, int64_t ld,
+                       cudaStream_t st) {
+    cudaError_t e = launch_decode_setup(m->pos_dev, pos, tokens, m->tok_dev, B, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode setup");
+    if (m->prof || !st) return decode_body(m, m->tok_dev, B, logits, ld, st);
+    Model::Graph* g = nullptr;
+    for (auto& c : m->dgraphs)
+        if (c.exec && c.B == B && c.logits == logits && c.ld == ld && c.stream == (void*)st) g = &c;
+    if (!g) {
+        Model::Graph& last = m->dlast;
+        const bool again = last.B == B && last.logits == logits && last.ld == ld && last.stream == (void*)st;
+        last.B = B;
+        last.logits = logits;
+        last.ld = ld;
+        last.stream = st;
+        if (!again) return decode_body(m, m->tok_dev, B, logits, ld, st);
+        g = &m->dgraphs[0];
+        for (auto& c : m->dgraphs)
+            if (!c.exec || c.used < g->used) g = &c;
+        if (g->exec) {
+            cudaGraphExecDestroy(g->exec);
+            g->exec = nullptr;
+        }
+        e = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal);
+        if (e != cudaSuccess) return cuda_fail(e, "begin capture");
+        tfm_status ts = decode_body(m, m->tok_dev, B, logits, ld, st);
+        cudaGraph_t graph = nullptr;
+        e = cudaStreamEndCapture(st, &graph);
+        if (ts != TFM_OK || e != cudaSuccess) {
+            if (graph) cudaGraphDestroy(graph);
+            return ts != TFM_OK ? ts : cuda_fail(e, "end capture");
+        }
+        e = cudaGraphInstantiate(&g->exec, graph, 0);
+        cudaGraphDestroy(graph);
+        if (e != cudaSuccess) {
+            g->exec = nullptr;
+            return cuda_fail(e, "graph instantiate");
+        }
+        g->B = B;
+        g->logits = logits;
+        g->ld = ld;
+        g->stream = st;
+    }
+    g->used = ++m->graph_clock;
+    e = cudaGraphLaunch(g->exec, st);
+    return e == cudaSuccess ? TFM_OK : cuda_fail(e, "graph launch");
 }
 
 tfm_status check_forward_args(Model* m, const void* tokens, int B, int S, const float* logits,
@@ -853,7 +919,7 @@ tfm_status tfm_kv_cache_create(void* handle) {
     const size_t caches = (size_t)c.n_layer * 2 * layer;
     const size_t part = tfm::decode_partial_floats(c.max_batch, c.n_head, c.max_seq, dh) * 4;
     uint8_t* p = nullptr;
-    const cudaError_t e = cudaMalloc(&p, caches + part + 256);
+    const cudaError_t e = cudaMalloc(&p, caches + part + 512 + (size_t)c.max_batch * 4);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(TFM_ENOMEM, "KV cache of %zu bytes: %s", caches + part, cudaGetErrorString(e));
@@ -861,6 +927,8 @@ tfm_status tfm_kv_cache_create(void* handle) {
     m->kv = p;
     m->kv_layer_bytes = layer;
     m->dec_part = reinterpret_cast<float*>(p + (caches + 255) / 256 * 256);
+    m->pos_dev = reinterpret_cast<int*>(p + (caches + 255) / 256 * 256 + (part + 255) / 256 * 256);
+    m->tok_dev = m->pos_dev + 4;
     m->kv_len = 0;
     m->kv_batch = 0;
     return TFM_OK;

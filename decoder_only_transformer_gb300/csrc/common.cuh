@@ -170,6 +170,16 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
         "r"(x), "r"(y), "r"(src)
         : "memory");
 }
+// Untiled bulk copy of `bytes` contiguous bytes global -> shared, completing on
+// an mbarrier (both addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

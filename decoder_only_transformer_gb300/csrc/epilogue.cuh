@@ -134,10 +134,13 @@ __device__ __forceinline__ QkvSlot qkv_slot(const EpiParams& p, int col0) {
 // Element offset of position s of sequence b in a chunk's head-major buffer: q
 // [B, H, S, dh]; k, v the same with n_kv_head heads, or, with kv_stride set, a
 // KV cache [B, n_kv_head, kv_stride, dh] at position pos0 + s.
+__device__ __forceinline__ int epi_pos0(const EpiParams& p) {
+    return p.pos0_dev ? __ldg(p.pos0_dev) : p.pos0;
+}
 __device__ __forceinline__ int64_t qkv_offset(const EpiParams& p, const QkvSlot& q, int b, int s) {
     const bool cache = q.region > 0 && p.kv_stride > 0;
     const int64_t stride = cache ? p.kv_stride : p.S;
-    const int64_t pos = cache ? (int64_t)p.pos0 + s : s;
+    const int64_t pos = cache ? (int64_t)epi_pos0(p) + s : s;
     return (((int64_t)b * q.heads + q.head) * stride + pos) * p.dh + q.d0;
 }
 
@@ -155,7 +158,7 @@ __device__ __forceinline__ void epi_compute(const EpiParams& p, int row, int col
         const QkvSlot q = qkv_slot(p, col0);
         if (q.region < 2 && row < p.M) {
             const int dh = p.dh;
-            const int s = p.pos0 + row % p.S;
+            const int s = epi_pos0(p) + row % p.S;
             float cs[W];                       // (cos, sin) of the W/2 pairs
             load_vec<W>(p.rope_cs + ((int64_t)s * (dh / 2) + q.d0 / 2) * 2, cs);
 #pragma unroll

@@ -32,6 +32,9 @@ struct EpiParams {
     // k and v into a KV cache instead: [B, n_kv_head, kv_stride, dh] at position
     // pos0 + s (0: head-major like q, [B, n_kv_head, S, dh])
     int kv_stride;
+    // when set, pos0 is read from this device word (a decode step replayed from a
+    // recorded graph, the position changing between replays)
+    const int* pos0_dev;
     const float* rope_cs;    // [>= S, dh/2, 2]: cos, sin of s * theta^(-2i/dh)
     void* q;
     void* k;
@@ -90,15 +93,17 @@ const char* cuda_error_text(cudaError_t e);
 // ---- elementwise kernels (k_rows.cu)
 cudaError_t launch_embedding(const int32_t* tok, const void* E, float* h, int64_t M, int V,
                              int D, int e_bf16, cudaStream_t st);
+// g_static = 1: no launch on the stream writes g (a model's gain), so a few-row
+// launch may load it before its grid dependency wait.
 cudaError_t launch_rmsnorm(const float* x, const float* g, void* y, int64_t M, int D, float eps,
-                           int out_bf16, cudaStream_t st);
+                           int out_bf16, cudaStream_t st, int g_static = 0);
 cudaError_t launch_rope(void* x, const int32_t* pos, int B, int H, int S, int dh, float theta,
                         int is_bf16, cudaStream_t st);
 cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t st);
 // h = E[tok] and y = RMSNorm(h) * g in one pass (bf16: E and y bf16; else fp32).
 cudaError_t launch_embed_rmsnorm(const int32_t* tok, const void* E, const float* g, float* h,
                                  void* y, int64_t M, int V, int D, float eps, int bf16,
-                                 cudaStream_t st);
+                                 cudaStream_t st, int g_static = 0);
 
 // ---- CUDA-core kernels (k_simt.cu), fp32 mode
 // C = A[M,K] . B[N,K]^T (and A . B2^T for EPI_SWIGLU), then the epilogue.
@@ -129,12 +134,21 @@ struct GemmPlan {
     int dual;             // SwiGLU: B tile = [W1 rows; W3 rows]
     int pair;             // 1: CTA pairs (cta_group::2) on 256-row tiles
     int n_fast;           // tile order: 1 = column blocks fastest, 0 = row blocks fastest
+    // M <= 128: the weight-streaming kernel (k_gemm_skinny.cu): A rows padded to
+    // sk_nm, sk_tiles tiles of 128 W rows (64 per weight for SwiGLU), K split
+    // over sk_splits CTAs of a cluster.  maps.a boxes sk_nm rows of A; maps.b
+    // (and maps.b2) box the W rows of a tile.
+    int skinny, sk_nm, sk_tiles, sk_splits;
+    // 1: no launch on the stream writes B (a model weight), so its loads may
+    // start before the grid dependency wait (set by the model's own plans)
+    int b_static;
     EpiParams epi;
 };
 // Builds the tensor maps; returns TFM_OK or an error status with a message.
 tfm_status plan_gemm_tc(GemmPlan* plan, const void* A, int64_t lda, const void* B,
                         const void* B2, int64_t ldb, int M, int N, int K, const EpiParams& epi);
 cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t st);
+cudaError_t launch_gemm_skinny(const GemmPlan& plan, cudaStream_t st);
 
 // ---- bf16 flash attention on mma.sync (k_attention.cu), any dh in {32, 64, 128}
 cudaError_t launch_attention_bf16(const void* q, const void* k, const void* v, void* o, int B,
@@ -143,11 +157,16 @@ cudaError_t launch_attention_bf16(const void* q, const void* k, const void* v, v
 // ---- attention of one new query per sequence over a KV cache (k_decode.cu):
 // q [B, H, dh], caches [B, Hkv, max_seq, dh] (positions [0, L) read), o [B, H*dh]
 // bf16; part holds decode_partial_floats(B, H, max_seq, dh) floats of scratch.
+// The attended length is *pos_dev + 1 (read on the device, so the launch can be
+// replayed from a recorded graph at every position); the grid covers max_seq.
 size_t decode_partial_floats(int B, int H, int max_seq, int dh);
 bool decode_supported(int dh, int group);
 cudaError_t launch_decode_attention(const void* q, const void* kc, const void* vc, float* part,
-                                    void* o, int B, int H, int Hkv, int max_seq, int L, int dh,
-                                    float scale, cudaStream_t st);
+                                    void* o, int B, int H, int Hkv, int max_seq,
+                                    const int* pos_dev, int dh, float scale, cudaStream_t st);
+// Stores the decode step's position and copies its B tokens into device words.
+cudaError_t launch_decode_setup(int* pos_dev, int pos, const int32_t* tok, int32_t* tok_dev, int B,
+                                cudaStream_t st);
 
 // ---- bf16 flash attention on tcgen05 (k_attention_tc.cu), dh in {64, 128}
 struct AttnPlan {

@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n0 = tile_n(t) * n_per_tile;
             if (rope_pre) {
                 const int r = m0 + q * 32 + lane;
-                const int pos = epi.pos0 + (r < M ? r : 0) % epi.S;
+                const int pos = epi_pos0(epi) + (r < M ? r : 0) % epi.S;
                 load_vec<32>(epi.rope_cs + ((int64_t)pos * (epi.dh / 2) + rope_d0 / 2) * 2, rcs);
             }
             if (!warp_wait(tfull_bar(acc), acc_phase, err, abort_flag)) break;
@@ -641,6 +641,36 @@ tfm_status plan_gemm_tc(GemmPlan* plan, const void* A, int64_t lda, const void* 
     plan->N = N;
     plan->K = K;
     plan->dual = dual ? 1 : 0;
+    plan->skinny = 0;
+    plan->b_static = 0;
+    if (M <= kBM) {
+        // A few rows: stream W over all SMs (k_gemm_skinny.cu).  Tiles of 128 W
+        // rows (64 output columns for SwiGLU); K split so that tiles x splits
+        // fills the SMs, two CTAs per SM where a CTA's ring fits twice.
+        plan->skinny = 1;
+        plan->pair = 0;
+        plan->n_fast = 0;
+        plan->block_n = 128;
+        plan->sk_nm = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+        const int out = dual ? 64 : 128;
+        plan->sk_tiles = (N + out - 1) / out;
+        const int num_kb = (K + kBK - 1) / kBK;
+        const int slots = sm_count() * (plan->sk_nm <= 32 ? 2 : 1);
+        int splits = slots / plan->sk_tiles;
+        if (splits > 8) splits = 8;              // portable cluster size
+        if (splits > num_kb) splits = num_kb;
+        plan->sk_splits = splits < 1 ? 1 : splits;
+        plan->epi = epi;
+        plan->epi.tma_out = 0;
+        if (!make_operand_map(&plan->maps.a, A, M, K, lda, plan->sk_nm)) return TFM_ECUDA;
+        if (!make_operand_map(&plan->maps.b, B, N, K, ldb, dual ? 64 : 128)) return TFM_ECUDA;
+        if (dual) {
+            if (!make_operand_map(&plan->maps.b2, B2, N, K, ldb, 64)) return TFM_ECUDA;
+        } else {
+            plan->maps.b2 = plan->maps.b;
+        }
+        return TFM_OK;
+    }
     // CTA pairs (256 x 256 tiles, half of B per SM): per k-block each SM holds
     // 32 KB instead of 48 KB, so six stages are in flight and a long main loop
     // keeps up with the tensor cores.  With a short K the tile time is set by the
@@ -677,6 +707,7 @@ tfm_status plan_gemm_tc(GemmPlan* plan, const void* A, int64_t lda, const void* 
 
 cudaError_t launch_gemm_tc(const GemmPlan& p, cudaStream_t st) {
     if (p.M <= 0 || p.N <= 0) return cudaSuccess;
+    if (p.skinny) return launch_gemm_skinny(p, st);
     if (p.pair) {
         if (p.dual) return launch_inst<256, 6, true, true>(p, st);
         return launch_inst<256, 6, false, true>(p, st);

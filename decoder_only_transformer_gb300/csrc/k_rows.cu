@@ -122,6 +122,112 @@ __global__ void __launch_bounds__(256) k_embed_rmsnorm(const int32_t* __restrict
     }
 }
 
+// ------------------------------------------------------------------ few rows
+// For a handful of rows (a decode step has one per sequence) the warp-per-row
+// kernels leave the latency of each dependent load exposed.  Here one CTA of 256
+// threads takes a row: thread t owns the 4-float groups t, t + 256, ... (kPer of
+// them); a model's gain is a weight that no launch writes, so it is loaded
+// before the dependency wait (g_static); the sum of squares is reduced over the
+// block.
+// kEmbed: the row is E[tok[m]] (fp32 or bf16), also written to h, as in
+// k_embed_rmsnorm.
+constexpr int kRowKernelMaxM = 64;
+
+template <int kPer, bool kEmbed, bool kBf16E, bool kBf16Y>
+__global__ void __launch_bounds__(256) k_norm_row(const int32_t* __restrict__ tok,
+                                                  const void* __restrict__ X,
+                                                  const float* __restrict__ g,
+                                                  float* __restrict__ h, void* __restrict__ y,
+                                                  int V, int D, float eps, int g_static,
+                                                  int* err) {
+    __shared__ float red[8];
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int64_t m = blockIdx.x;
+    const int n4 = D >> 2;
+    const float4* g4 = reinterpret_cast<const float4*>(g);
+    float4 gv[kPer];
+    if (!g_static) pdl_wait();                   // g may come from the launch before
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int c = tid + 256 * i;
+        gv[i] = c < n4 ? __ldg(g4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    pdl_wait();
+    pdl_trigger();
+    int64_t row = m;
+    bool ok = true;
+    if (kEmbed) {
+        const int t = __ldg(tok + m);
+        ok = (t >= 0 && t < V);
+        if (!ok && tid == 0) raise_error(err, TFM_EBADTOKEN);
+        row = ok ? t : 0;
+    }
+    float4 v[kPer];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int c = tid + 256 * i;
+        v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < n4 && ok) {
+            if (kBf16E) {
+                const uint2 w = __ldg(reinterpret_cast<const uint2*>(
+                                          static_cast<const __nv_bfloat16*>(X) + row * D) + c);
+                v[i] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+            } else {
+                v[i] = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(X) + row * D) + c);
+            }
+        }
+        if (kEmbed && c < n4) reinterpret_cast<float4*>(h + m * D)[c] = v[i];
+        ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) red[tid >> 5] = ss;
+    __syncthreads();
+    ss = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) ss += red[w];
+    const float r = 1.0f / sqrtf(ss / (float)D + eps);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int c = tid + 256 * i;
+        if (c >= n4) continue;
+        const float4 w = gv[i];
+        const float a0 = v[i].x * r * w.x, a1 = v[i].y * r * w.y;
+        const float a2 = v[i].z * r * w.z, a3 = v[i].w * r * w.w;
+        if (kBf16Y) {
+            uint2 o;
+            o.x = pack_bf16x2(a0, a1);
+            o.y = pack_bf16x2(a2, a3);
+            reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(y) + m * D)[c] = o;
+        } else {
+            reinterpret_cast<float4*>(static_cast<float*>(y) + m * D)[c] = make_float4(a0, a1, a2, a3);
+        }
+    }
+}
+
+// Few-row launch (M <= kRowKernelMaxM, D <= 8192); returns false when it does not apply.
+template <bool kEmbed>
+static bool norm_row_launch(cudaError_t* e, const int32_t* tok, const void* X, const float* g,
+                            float* h, void* y, int64_t M, int V, int D, float eps, int bf16,
+                            int g_static, cudaStream_t st) {
+    if (M > kRowKernelMaxM || D > 8192) return false;
+    const int per = (D / 4 + 255) / 256;
+    const dim3 grid((unsigned)M), block(256);
+    int* err = device_error_word();
+#define TFM_ROW_LAUNCH(P)                                                                        \
+    *e = bf16 ? launch_pdl(k_norm_row<P, kEmbed, kEmbed, true>, grid, block, 0, st, tok, X, g, h, \
+                           y, V, D, eps, g_static, err)                                           \
+              : launch_pdl(k_norm_row<P, kEmbed, false, false>, grid, block, 0, st, tok, X, g, h, \
+                           y, V, D, eps, g_static, err)
+    if (per <= 1) TFM_ROW_LAUNCH(1);
+    else if (per <= 2) TFM_ROW_LAUNCH(2);
+    else if (per <= 4) TFM_ROW_LAUNCH(4);
+    else TFM_ROW_LAUNCH(8);
+#undef TFM_ROW_LAUNCH
+    return true;
+}
+
 template <int kV>
 cudaError_t embed_norm_launch(const int32_t* tok, const void* E, const float* g, float* h, void* y,
                               int64_t M, int V, int D, float eps, int bf16, cudaStream_t st) {
@@ -135,8 +241,10 @@ cudaError_t embed_norm_launch(const int32_t* tok, const void* E, const float* g,
 
 cudaError_t launch_embed_rmsnorm(const int32_t* tok, const void* E, const float* g, float* h,
                                  void* y, int64_t M, int V, int D, float eps, int bf16,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, int g_static) {
     if (M <= 0) return cudaSuccess;
+    cudaError_t e;
+    if (norm_row_launch<true>(&e, tok, E, g, h, y, M, V, D, eps, bf16, g_static, st)) return e;
     const int groups = (D / 4 + 31) / 32;   // 4-float groups per lane
     if (groups <= 1) return embed_norm_launch<1>(tok, E, g, h, y, M, V, D, eps, bf16, st);
     if (groups <= 2) return embed_norm_launch<2>(tok, E, g, h, y, M, V, D, eps, bf16, st);
@@ -145,7 +253,7 @@ cudaError_t launch_embed_rmsnorm(const int32_t* tok, const void* E, const float*
     if (groups <= 16) return embed_norm_launch<16>(tok, E, g, h, y, M, V, D, eps, bf16, st);
     if (groups <= 32) return embed_norm_launch<32>(tok, E, g, h, y, M, V, D, eps, bf16, st);
     // Rows beyond 4096: the gather and the norm as two launches.
-    cudaError_t e = launch_embedding(tok, E, h, M, V, D, bf16, st);
+    e = launch_embedding(tok, E, h, M, V, D, bf16, st);
     if (e != cudaSuccess) return e;
     return launch_rmsnorm(h, g, y, M, D, eps, bf16, st);
 }
@@ -239,8 +347,11 @@ static cudaError_t rms_launch(const float* x, const float* g, void* y, int64_t M
 }
 
 cudaError_t launch_rmsnorm(const float* x, const float* g, void* y, int64_t M, int D, float eps,
-                           int out_bf16, cudaStream_t st) {
+                           int out_bf16, cudaStream_t st, int g_static) {
     if (M <= 0) return cudaSuccess;
+    cudaError_t e;
+    if (norm_row_launch<false>(&e, nullptr, x, g, nullptr, y, M, 0, D, eps, out_bf16, g_static, st))
+        return e;
     const int groups = (D / 4 + 31) / 32;   // float4 groups per lane
     if (groups <= 1) return rms_launch<1>(x, g, y, M, D, eps, out_bf16, st);
     if (groups <= 2) return rms_launch<2>(x, g, y, M, D, eps, out_bf16, st);

@@ -172,6 +172,10 @@ def test_attention_bf16_uniform_scores_prefix_mean():
     (1024, 2304, 768), (8192, 512, 512),
     # long K: CTA-pair kernel (256-row tiles over two SMs); ragged M, N and K
     (300, 1000, 2048), (257, 384, 2112), (2048, 768, 4096), (129, 256, 2048),
+    # M <= 128: the weight-streaming kernel, rows padded to 16 / 32 / 64 / 128, K
+    # split over clusters of up to 8 CTAs (ragged N and K, one K block, LM-head width)
+    (5, 50257, 768), (16, 3072, 2048), (17, 2048, 5632), (33, 1000, 136), (64, 384, 2048),
+    (65, 130, 520), (128, 2304, 768), (2, 32000, 2048), (3, 24, 8),
 ])
 def test_linear_bf16_fp32_out(M, N, K):
     r = rng(M + N + K)
@@ -214,7 +218,9 @@ def test_linear_fp32():
 # ---------------------------------------------------------------- SwiGLU
 @pytest.mark.parametrize("bf16", [False, True])
 @pytest.mark.parametrize("M,D,F", [(200, 64, 176), (1000, 512, 1344), (256, 768, 2048),
-                                   (600, 2048, 1000)])   # gate/up with K = 2048: CTA pairs
+                                   (600, 2048, 1000),    # gate/up with K = 2048: CTA pairs
+                                   # a few rows (weight-streaming kernel, split K)
+                                   (4, 2048, 5632), (32, 512, 1344), (8, 768, 2048), (100, 64, 176)])
 def test_swiglu(bf16, M, D, F):
     r = rng(M + F)
     cast = bf16_exact if bf16 else (lambda a: a)

@@ -5,7 +5,8 @@ A decode step at position p must give the logits of row p of the forward over
 the sequence extended by the new token: checked against the CPU oracle (float64
 forward over the whole extended sequence, the tolerances of the forward tests)
 and against the GPU's own forward (bf16 rounding differs only inside attention).
-The steps cross the decode kernel's 256-key chunks."""
+The steps cross the decode kernel's key chunks (16384 / d_head keys each), so a
+step's new key lands both inside a chunk and as the first key of a new one."""
 import numpy as np
 import pytest
 
@@ -35,9 +36,10 @@ def _model(cfg, w, B, S):
 
 
 @pytest.mark.parametrize("name,B,S0,T", [
-    ("small", 2, 250, 12),        # d_head 32, crosses the 256-key chunk
-    ("gpt2s", 3, 37, 5),          # d_head 64
-    ("gqa", 2, 300, 6),           # d_head 128, 4 query heads per kv head, 2 chunks
+    ("small", 2, 505, 12),        # d_head 32: 512-key chunks, crosses the first
+    ("gpt2s", 3, 250, 10),        # d_head 64: 256-key chunks, crosses the first
+    ("gpt2s", 1, 37, 3),          # one chunk, partly filled
+    ("gqa", 2, 380, 6),           # d_head 128, 4 query heads per kv head: crosses key 384
 ])
 def test_decode_matches_oracle_and_forward(name, B, S0, T):
     cfg = workloads.get_config(name).replace(n_layer=2, vocab=3001)
@@ -101,3 +103,42 @@ def test_decode_argument_checks():
     with pytest.raises(tfm.TfmError):             # fp32 mode has no KV cache
         m2.kv_cache_create()
     m2.close()
+
+
+@pytest.mark.parametrize("name", ["small", "gqa"])
+def test_decode_replay_matches_direct(name):
+    """Steps on a side stream with one logits buffer are recorded after the second
+    step and replayed at every later position (the position and the tokens are read
+    from device words): each step's logits equal those of the launches run one by
+    one on the legacy stream, bit for bit."""
+    cfg = workloads.get_config(name).replace(n_layer=2, vocab=3001)
+    w = workloads.make_weights(cfg, gains="random")
+    B, S0, T = 2, 250, 10
+    tok = workloads.make_tokens(cfg, batch=B, seq=S0 + T, seed=5)
+    ld = (cfg.vocab + 3) // 4 * 4
+    model = _model(cfg, w, B, S0 + T)
+    dtok = torch.from_numpy(tok).cuda()
+    pre = torch.empty(B * S0, ld, device="cuda")
+    cols = [dtok[:, S0 + t].contiguous() for t in range(T)]
+
+    model.prefill(dtok[:, :S0].contiguous(), pre)
+    direct = []
+    for t in range(T):
+        lg = torch.empty(B, ld, device="cuda")
+        model.decode_step(cols[t], S0 + t, lg)
+        direct.append(lg)
+    torch.cuda.synchronize()
+
+    side = torch.cuda.Stream()
+    lg = torch.empty(B, ld, device="cuda")
+    replay = []
+    with torch.cuda.stream(side):
+        model.prefill(dtok[:, :S0].contiguous(), pre, side)
+        for t in range(T):
+            model.decode_step(cols[t], S0 + t, lg, side)
+            replay.append(lg.clone())
+    torch.cuda.synchronize()
+    tfm.device_status()
+    for t in range(T):
+        assert torch.equal(replay[t][:, : cfg.vocab], direct[t][:, : cfg.vocab]), t
+    model.close()
