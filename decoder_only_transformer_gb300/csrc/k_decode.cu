@@ -52,8 +52,9 @@ struct DecSmem {
 template <int DH, int G>
 __global__ void __launch_bounds__(kDecThreads) k_decode_partial(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
-    const __nv_bfloat16* __restrict__ vc, float* __restrict__ part, int H, int Hkv, int max_seq,
-    const int* __restrict__ pos_dev, int nch, float scale_log2, int* err) {
+    const __nv_bfloat16* __restrict__ vc, float* __restrict__ part, __nv_bfloat16* __restrict__ o,
+    int H, int Hkv, int max_seq, const int* __restrict__ pos_dev, int nch, float scale_log2,
+    int* err) {
     using Sm = DecSmem<DH, G>;
     constexpr int NK = Sm::kKeys, NW = kDecNW;
     constexpr int CPR = DH / 8;                      // lanes per key row, 16 bytes each
@@ -218,6 +219,21 @@ __global__ void __launch_bounds__(kDecThreads) k_decode_partial(
         }
     }
     __syncthreads();
+    if (pos < NK) {
+        // All keys in this one chunk: the normalised output directly (the
+        // combining launch sees a single chunk and does nothing).
+        for (int i = tid; i < G * DH; i += kDecThreads) {
+            const int hh = i / DH, d = i - hh * DH;
+            float v = 0.f, l = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                v += osum[(w * G + hh) * DH + d];
+                l += red_l[hh * NW + w];
+            }
+            o[(int64_t)(b * H + h0 + hh) * DH + d] = __float2bfloat16_rn(v / l);
+        }
+        return;
+    }
     for (int i = tid; i < G * DH; i += kDecThreads) {
         const int hh = i / DH, d = i - hh * DH;
         float v = 0.f;
@@ -252,6 +268,7 @@ __global__ void __launch_bounds__(128) k_decode_combine(const float* __restrict_
     if (w >= BH) return;
     constexpr int NK = dec_keys(DH);
     const int nch = (__ldg(pos_dev) + NK) / NK;      // chunks holding keys [0, pos]
+    if (nch == 1) return;                            // written by the chunk kernel itself
     const float* p = part + (int64_t)w * nch_stride * (DH + 2);
     // chunk statistics with one chunk per lane, so their loads go out together
     float M = -INFINITY;
@@ -296,7 +313,8 @@ cudaError_t decode_launch(const void* q, const void* kc, const void* vc, float* 
     cudaError_t e = launch_pdl(k_decode_partial<DH, G>, dim3((unsigned)(B * Hkv * nch)),
                                dim3(kDecThreads), Sm::kBytes, st, static_cast<const __nv_bfloat16*>(q),
                                static_cast<const __nv_bfloat16*>(kc),
-                               static_cast<const __nv_bfloat16*>(vc), part, H, Hkv, max_seq,
+                               static_cast<const __nv_bfloat16*>(vc), part,
+                               static_cast<__nv_bfloat16*>(o), H, Hkv, max_seq,
                                pos_dev, nch, scale * 1.4426950408889634f, device_error_word());
     if (e != cudaSuccess) return e;
     const int BH = B * H;
