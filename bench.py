@@ -187,14 +187,25 @@ def decode_rate(tfm, torch, model, cfg, tok_np, stream, peaks, steps=32):
         nbytes += (2 * B * Hkv * L * dh * 2 + 2 * B * H * dh * 2
                    + 2 * B * H * nch * (dh + 2) * 4) * cfg.n_layer
     gbs = nbytes / (att_ms / 1e3) / 1e9 if att_ms > 0 else None
+    # Whole step against HBM: every weight matrix is read once per step (the
+    # rows of the embedding for the step's tokens only) and the cache as above.
+    D, F, V, L = cfg.d_model, cfg.d_ff, cfg.vocab, cfg.n_layer
+    w_layer = ((H + 2 * Hkv) * dh * D + D * H * dh + 3 * D * F) * 2 + 2 * D * 4
+    w_step = L * w_layer + V * D * 2 + B * D * 2 + D * 4
+    step_bytes = w_step + nbytes / steps
+    step_gbs = step_bytes / (ms / steps / 1e3) / 1e9
     return {"value": B * steps / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms / steps,
             "batch": B, "prefill_len": S0, "steps": steps,
+            "step_roofline": {"bound": "hbm", "bytes_per_step": int(step_bytes),
+                              "achieved": round(step_gbs, 1), "peak": peaks["hbm_gbs"],
+                              "unit": "GB/s", "frac": round(step_gbs / peaks["hbm_gbs"], 4)},
             "attention": {"bound": "hbm", "achieved": round(gbs, 1) if gbs else None,
                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
                           "frac": round(gbs / peaks["hbm_gbs"], 4) if gbs else None,
                           "avg_us_per_layer": round(att_ms * 1e3 / max(1, att_n), 2)},
             "how": "tfm_prefill of the first S - steps positions, then tfm_decode_step per "
-                   "position (direct launches); CUDA events around all steps"}
+                   "position (recorded as a graph on its second call, replayed after); CUDA "
+                   "events around all steps; attention from a second, profiled pass"}
 
 
 def rmsnorm_hbm(tfm, torch, stream, peaks, rows=131072, d=2048, launches=20):

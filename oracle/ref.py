@@ -16,7 +16,9 @@ Pages cited (all are tutorials; none prints code for a particular GPU):
   Position Embedding)", "GQA / MQA", the LayerNorm/RMSNorm comparison.
 * [CS336-B] "手把手带工程同学从零实现一个完整的LLM（CS336）——Transformer篇"
   (fengye404.top): sections 6 RMSNorm, 7 RoPE, 8 Attention, 9 SwiGLU,
-  10 组装完整模型, 11 算参数和开销.
+  10 组装完整模型, 11 算参数和开销, 12 训练 (next-token targets, cross-entropy).
+* [LLM2] also: section "Optimize", subsection "Loss" (cross-entropy in the
+  log-sum-exp form, perplexity).
 
 Every function computes its plain definition in float64 with NumPy; matmul is
 the only library primitive used as a step.  No blocking, fusion or reordering
@@ -28,6 +30,8 @@ beyond the definition.  Where the pages are silent the readings are:
 3. Grouped-query attention: query head h reads kv head h // (H / H_kv).
 4. SwiGLU: silu(x W1^T) * (x W3^T), then W2; silu(z) = z / (1 + exp(-z)).
 5. Positions are 0..S-1 in every sequence.
+6. Cross-entropy is per position (no reduction inside); the mean over all
+   positions and its exponential (perplexity) are separate steps.
 
 Pinning: every function here is checked by the non-GPU tests against values the
 pages print, closed forms, invariants and brute force (see the oracle pin tests).
@@ -41,7 +45,7 @@ __all__ = [
     "rope_angles", "rope", "softmax", "causal_mask", "causal_attention",
     "naive_causal_attention", "silu", "swiglu", "multihead_self_attention",
     "transformer_block",
-    "forward", "param_count",
+    "forward", "param_count", "cross_entropy", "perplexity",
 ]
 
 F64 = np.float64
@@ -244,3 +248,22 @@ def param_count(vocab, d_model, n_layer, d_ff, n_head=1, n_kv_head=1):
     dkv = n_kv_head * dh
     per_layer = 2 * d_model * d_model + 2 * dkv * d_model + 3 * d_model * d_ff + 2 * d_model
     return 2 * vocab * d_model + n_layer * per_layer + d_model
+
+
+def cross_entropy(logits, targets):
+    """Next-token cross-entropy of each position, -log softmax(z)[t], in the
+    log-sum-exp form: with mx = max_j z_j, lse = log(sum_j exp(z_j - mx)) + mx
+    and loss = lse - z[t].  Returns (loss, lse), each shaped like ``targets``.
+    [LLM2] Optimize / Loss; [CS336-B] 12 训练 (the targets are the inputs
+    shifted left by one position)."""
+    z = np.asarray(logits, dtype=F64)
+    t = np.asarray(targets)
+    mx = z.max(axis=-1)
+    lse = np.log(np.exp(z - mx[..., None]).sum(axis=-1)) + mx
+    zt = np.take_along_axis(z, t[..., None].astype(np.int64), axis=-1)[..., 0]
+    return lse - zt, lse
+
+
+def perplexity(mean_loss):
+    """exp of the mean cross-entropy.  [LLM2] Optimize / Loss."""
+    return float(np.exp(F64(mean_loss)))

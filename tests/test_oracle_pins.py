@@ -331,3 +331,53 @@ def test_param_count_formula():
             total = w["embed"].size + w["final_norm"].size + w["lm_head"].size
             total += sum(a.size for layer in w["layers"] for a in layer.values())
             assert total == oracle.param_count(c2.vocab, c2.d_model, c2.n_layer, c2.d_ff, c2.n_head, kv)
+
+
+# ---------------------------------------------------------------- cross-entropy
+def test_cross_entropy_uniform_logits_is_log_vocab():
+    # equal logits: softmax is 1/V everywhere, whatever the level and the target
+    V = 37
+    z = np.full((3, V), 5.25)
+    loss, lse = oracle.cross_entropy(z, np.array([0, 17, 36]))
+    assert np.allclose(loss, np.log(V), rtol=0, atol=1e-12)
+    assert np.allclose(lse, 5.25 + np.log(V), rtol=0, atol=1e-12)
+    assert abs(oracle.perplexity(loss.mean()) - V) < 1e-9
+
+
+def test_cross_entropy_two_classes_is_softplus():
+    # V = 2: -log(e^a / (e^a + e^b)) = log(1 + e^(b - a)) for target a
+    r = np.random.default_rng(3)
+    z = r.standard_normal((50, 2)) * 4
+    t = r.integers(0, 2, 50)
+    other = z[np.arange(50), 1 - t]
+    mine = z[np.arange(50), t]
+    loss, _ = oracle.cross_entropy(z, t)
+    assert np.allclose(loss, np.log1p(np.exp(other - mine)), rtol=1e-13, atol=1e-13)
+
+
+def test_cross_entropy_row_shift_invariance_and_axis():
+    r = np.random.default_rng(4)
+    z = r.standard_normal((4, 6, 11))
+    t = r.integers(0, 11, (4, 6))
+    c = r.standard_normal((4, 6, 1)) * 100        # a different shift per row
+    l0, s0 = oracle.cross_entropy(z, t)
+    l1, s1 = oracle.cross_entropy(z + c, t)
+    assert np.allclose(l0, l1, rtol=0, atol=1e-10)
+    assert np.allclose(s1 - s0, c[..., 0], rtol=0, atol=1e-10)
+    assert np.all(l0 > 0)                          # -log of a probability below 1
+
+
+def test_cross_entropy_brute_force_and_no_overflow():
+    r = np.random.default_rng(5)
+    z = r.standard_normal((7, 9))
+    t = r.integers(0, 9, 7)
+    loss, lse = oracle.cross_entropy(z, t)
+    for i in range(7):
+        s = math.fsum(math.exp(v) for v in z[i])
+        assert abs(lse[i] - math.log(s)) < 1e-12
+        assert abs(loss[i] - (-math.log(math.exp(z[i, t[i]]) / s))) < 1e-12
+    big = np.array([[1000.0, 0.0, 0.0]])
+    l_hit, _ = oracle.cross_entropy(big, np.array([0]))
+    l_miss, _ = oracle.cross_entropy(big, np.array([1]))
+    assert np.isfinite(l_hit).all() and abs(l_hit[0]) < 1e-300 + 1e-12
+    assert abs(l_miss[0] - 1000.0) < 1e-9
