@@ -208,6 +208,69 @@ def decode_rate(tfm, torch, model, cfg, tok_np, stream, peaks, steps=32):
                    "events around all steps; attention from a second, profiled pass"}
 
 
+def loss_rate(tfm, torch, model, cfg, tok_np, logits, stream, flush, peaks, steps=10):
+    """The fused next-token cross-entropy (tfm_forward_loss: the LM head's GEMM
+    keeps per-row log-sum-exp statistics instead of writing fp32 logits) against
+    the forward that writes the logits, both launched directly, L2 flushed
+    between steps; the LM head kind of a profiled pass of each for the kernel
+    figures.  Targets: the next token, the last position's a seeded draw."""
+    B, S = tok_np.shape
+    M = B * S
+    tgt = np.empty_like(tok_np)
+    tgt[:, :-1] = tok_np[:, 1:]
+    tgt[:, -1] = np.random.default_rng(1).integers(0, cfg.vocab, B)
+    dtok = torch.from_numpy(tok_np).cuda()
+    dtgt = torch.from_numpy(tgt).cuda()
+    loss = torch.empty(M, device="cuda")
+    mean = torch.empty(1, device="cuda")
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+            flush.zero_()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        torch.cuda.synchronize()
+        for a, b in ev:
+            a.record(stream)
+            fn()
+            b.record(stream)
+            flush.zero_()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / steps
+
+    def lm_us(fn):
+        model.profile(True)
+        for _ in range(steps):
+            fn()
+            flush.zero_()
+        torch.cuda.synchronize()
+        model.profile(False)
+        ms, n = model.profile_read()["lmhead_gemm"]
+        return ms * 1e3 / steps
+
+    fwd = lambda: model.forward(dtok, logits, stream)
+    fl = lambda: model.forward_loss(dtok, dtgt, loss, None, mean, stream)
+    ms_logits, ms_loss = timed(fwd), timed(fl)
+    us_lm_logits, us_lm_loss = lm_us(fwd), lm_us(fl)
+    tfm.device_status()
+    flops = 2.0 * M * cfg.vocab * cfg.d_model
+    peak = peaks["bf16_tflops"] if cfg.mode == "bf16" else None
+    ach = flops / (us_lm_loss * 1e-6) / 1e12
+    return {"value": M / (ms_loss / 1e3), "unit": "tokens/s", "ms_per_step": ms_loss,
+            "forward_logits_ms_per_step": ms_logits,
+            "mean_loss": mean.item(),
+            "logits_bytes_not_written": M * cfg.vocab * 4,
+            "lmhead_us": {"lse": round(us_lm_loss, 2), "logits": round(us_lm_logits, 2)},
+            "roofline": ({"bound": "tensor", "achieved": round(ach, 1), "peak": peak,
+                          "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+                          "note": "LM head GEMM with the log-sum-exp epilogue plus the merge "
+                                  "of the per-tile statistics, 2 M V D flops"}
+                         if peak else None),
+            "how": "tfm_forward_loss vs tfm_forward, direct launches, CUDA events per step, "
+                   "L2 flushed between steps"}
+
+
 def rmsnorm_hbm(tfm, torch, stream, peaks, rows=131072, d=2048, launches=20):
     """RMSNorm alone on a working set far above L2 (fp32 in 1 GiB, bf16 out),
     so that its bytes come from HBM: the bandwidth figure the in-forward
@@ -339,6 +402,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-loss", action="store_true")
     ap.add_argument("--decode-only", action="store_true",
                     help="only the incremental-decoding measurement (prefill, then decode "
                          "steps); prints its JSON object alone")
@@ -532,6 +596,8 @@ def main():
     rms = rmsnorm_hbm(tfm, torch, stream, load_peaks()) if rank == 0 else None
     decode = (decode_rate(tfm, torch, model, cfg, tok_np, stream, load_peaks())
               if rank == 0 and cfg.mode == "bf16" and not args.no_decode else None)
+    lossr = (loss_rate(tfm, torch, model, cfg, tok_np, logits, stream, flush, load_peaks())
+             if rank == 0 and not args.no_loss else None)
     rows = sampler.stop()
     clocks = ClockSampler.summary(rows)
     clocks["window_s"] = round(t_wall1 - t_wall0, 3)
@@ -585,6 +651,7 @@ def main():
         "kernels": kernels,
         "rmsnorm_hbm": rms,
         "decode": decode,
+        "loss": lossr,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": (2 + 7 * cfg.n_layer) * args.steps,

@@ -212,6 +212,17 @@ struct Model {
     uint8_t* kv = nullptr;
     size_t kv_layer_bytes = 0;      // one of K or V of one layer
     float* dec_part = nullptr;
+    // fused cross-entropy (tfm_forward_loss): per-row LSE slots [M][slots] float2,
+    // target logits [M], per-row losses [M]; fp32 mode also materialises logits
+    uint8_t* loss_mem = nullptr;
+    int64_t loss_rows = 0;          // rows the scratch holds
+    float2* lse_part = nullptr;
+    float* lse_tgt = nullptr;
+    float* loss_tmp = nullptr;
+    float* loss_logits = nullptr;   // fp32 mode [M, ldV]
+    GemmPlan p_lse;                 // LM head with the EPI_LSE epilogue
+    int lse_M = -1;
+    const int32_t* lse_targets = nullptr;
     int* pos_dev = nullptr;         // position of the decode step being run (device word)
     int32_t* tok_dev = nullptr;     // its tokens [max_batch]
     Graph dgraphs[2];               // recorded decode steps (position, tokens read on the device)
@@ -360,6 +371,7 @@ void tfm_destroy(void* handle) {
     }
     if (m->copy_st) cudaStreamDestroy(m->copy_st);
     if (m->kv) cudaFree(m->kv);
+    if (m->loss_mem) cudaFree(m->loss_mem);
     for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
     cudaFree(m->ws);
     cudaFree(m->wmem);
@@ -534,8 +546,64 @@ enum Kind { K_EMBED = 0, K_NORM, K_QKV, K_ATTN, K_OPROJ, K_GATEUP, K_DOWN, K_LMH
         }                                                                       \
     } while (0)
 
+// Targets and outputs of tfm_forward_loss.
+struct LossArgs {
+    const int32_t* targets;
+    float* loss;
+    float* lse;
+    float* mean;
+};
+
+int lse_slots_max(int V) { return 2 * ((V + 127) / 128); }
+
+// Scratch of the fused cross-entropy for M rows (grown on demand).
+tfm_status ensure_loss_scratch(Model* m, int64_t M) {
+    if (m->loss_mem && m->loss_rows >= M) return TFM_OK;
+    if (m->loss_mem) cudaFree(m->loss_mem);
+    m->loss_mem = nullptr;
+    m->loss_rows = 0;
+    m->lse_M = -1;
+    const int64_t V = m->cfg.vocab, ldV = (V + 3) / 4 * 4;
+    const size_t part = (size_t)M * lse_slots_max((int)V) * 8, vec = (size_t)M * 4;
+    const size_t lg = m->cfg.mode == TFM_BF16 ? 0 : (size_t)M * ldV * 4;
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    cudaError_t e = cudaMalloc(&m->loss_mem, up(part) + 2 * up(vec) + lg);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        m->loss_mem = nullptr;
+        return fail(TFM_ENOMEM, "cross-entropy scratch for %lld rows: %s", (long long)M,
+                    cudaGetErrorString(e));
+    }
+    m->lse_part = reinterpret_cast<float2*>(m->loss_mem);
+    m->lse_tgt = reinterpret_cast<float*>(m->loss_mem + up(part));
+    m->loss_tmp = reinterpret_cast<float*>(m->loss_mem + up(part) + up(vec));
+    m->loss_logits = lg ? reinterpret_cast<float*>(m->loss_mem + up(part) + 2 * up(vec)) : nullptr;
+    m->loss_rows = M;
+    return TFM_OK;
+}
+
+// The LM head as the fused cross-entropy's GEMM: statistics instead of logits.
+tfm_status build_lse_plan(Model* m, int M, const int32_t* targets) {
+    if (m->lse_M == M && m->lse_targets == targets) return TFM_OK;
+    const auto& s = m->sz;
+    EpiParams e = epi_basic(EPI_LSE, M, (int)s.V, nullptr, 0);
+    e.targets = targets;
+    e.lse_part = m->lse_part;
+    e.lse_tgt = m->lse_tgt;
+    m->lse_M = -1;
+    tfm_status st = plan_gemm_tc(&m->p_lse, m->xn(), s.D, m->lm_head, nullptr, s.D, M, (int)s.V,
+                                 (int)s.D, e);
+    if (st != TFM_OK) return fail(st, "could not encode TMA tensor maps (driver entry point missing?)");
+    // slot 2 * column tile + half; at most lse_slots_max(V) for tiles of >= 128 columns
+    m->p_lse.epi.lse_slots = 2 * (int)((s.V + m->p_lse.block_n - 1) / m->p_lse.block_n);
+    m->p_lse.b_static = 1;
+    m->lse_M = M;
+    m->lse_targets = targets;
+    return TFM_OK;
+}
+
 tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* logits, int64_t ld,
-                        cudaStream_t st, bool to_cache = false) {
+                        cudaStream_t st, bool to_cache = false, const LossArgs* la = nullptr) {
     const tfm_config& c = m->cfg;
     const auto& s = m->sz;
     const int M = B * S;
@@ -543,6 +611,22 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
     const float scale = 1.0f / std::sqrt((float)dh);
     const bool bf = c.mode == TFM_BF16;
     if (!device_error_word()) return fail(TFM_ECUDA, "device error word unavailable");
+    if (la) {
+        tfm_status ls = ensure_loss_scratch(m, M);
+        if (ls != TFM_OK) return ls;
+        if (bf) {
+            ls = build_lse_plan(m, M, la->targets);
+            if (ls != TFM_OK) return ls;
+        }
+        // the logits plan is not launched: keep the one already built for (M, S)
+        if (m->plan_m == M && m->plan_S == S) {
+            logits = const_cast<float*>(m->plan_logits);
+            ld = m->plan_ld;
+        } else {
+            logits = nullptr;
+            ld = 0;
+        }
+    }
     if (bf) {
         tfm_status ps = build_plans(m, M, S, logits, ld);
         if (ps != TFM_OK) return ps;
@@ -590,7 +674,14 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
         }
         if (c.n_layer > 0)
             TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->final_norm, m->xn(), M, c.d_model, c.norm_eps, 1, st, 1));
-        TFM_LAUNCH(K_LMHEAD, launch_gemm_tc(m->p_lm, st));
+        if (la) {
+            TFM_LAUNCH(K_LMHEAD, launch_gemm_tc(m->p_lse, st));
+            TFM_LAUNCH(K_LMHEAD, launch_lse_finish(m->lse_part, m->p_lse.epi.lse_slots, m->lse_tgt,
+                                                   la->targets, M, c.vocab, la->loss, la->lse,
+                                                   m->loss_tmp, la->mean, st));
+        } else {
+            TFM_LAUNCH(K_LMHEAD, launch_gemm_tc(m->p_lm, st));
+        }
     } else {
         const float* xn = static_cast<const float*>(m->xn());
         for (int l = 0; l < c.n_layer; ++l) {
@@ -620,9 +711,23 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
         }
         if (c.n_layer > 0)
             TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->final_norm, m->xn(), M, c.d_model, c.norm_eps, 0, st, 1));
-        TFM_LAUNCH(K_LMHEAD, launch_gemm_simt(xn, static_cast<const float*>(m->lm_head), nullptr, M,
-                                              c.vocab, c.d_model,
-                                              epi_basic(EPI_STORE_F32, M, c.vocab, logits, ld), st));
+        if (la) {
+            // fp32 mode: the logits in scratch, then one pass over each row
+            const int64_t ldV = (c.vocab + 3) / 4 * 4;
+            TFM_LAUNCH(K_LMHEAD, launch_gemm_simt(xn, static_cast<const float*>(m->lm_head), nullptr, M,
+                                                  c.vocab, c.d_model,
+                                                  epi_basic(EPI_STORE_F32, M, c.vocab, m->loss_logits, ldV),
+                                                  st));
+            TFM_LAUNCH(K_LMHEAD, launch_lse_rows(m->loss_logits, ldV, M, c.vocab, la->targets,
+                                                 m->lse_part, m->lse_tgt, st));
+            TFM_LAUNCH(K_LMHEAD, launch_lse_finish(m->lse_part, 1, m->lse_tgt, la->targets, M,
+                                                   c.vocab, la->loss, la->lse, m->loss_tmp, la->mean,
+                                                   st));
+        } else {
+            TFM_LAUNCH(K_LMHEAD, launch_gemm_simt(xn, static_cast<const float*>(m->lm_head), nullptr, M,
+                                                  c.vocab, c.d_model,
+                                                  epi_basic(EPI_STORE_F32, M, c.vocab, logits, ld), st));
+        }
     }
     return TFM_OK;
 }
@@ -794,6 +899,20 @@ tfm_status tfm_forward(void* handle, const int32_t* tokens, int32_t B, int32_t S
     if (st != TFM_OK) return st;
     if (!tfm::aligned16(logits)) return fail(TFM_EINVAL, "logits must be 16-byte aligned");
     return tfm::forward_impl(m, tokens, B, S, logits, ld_logits, static_cast<cudaStream_t>(stream));
+}
+
+tfm_status tfm_forward_loss(void* handle, const int32_t* tokens, const int32_t* targets, int32_t B,
+                            int32_t S, float* loss, float* lse, float* mean_loss, void* stream) {
+    Model* m = static_cast<Model*>(handle);
+    if (!m) return fail(TFM_EINVAL, "NULL handle");
+    if (!targets) return fail(TFM_EINVAL, "NULL targets");
+    // the logits-free forward takes the same token checks as tfm_forward
+    const float dummy = 0.f;
+    tfm_status st = tfm::check_forward_args(m, tokens, B, S, &dummy, (m->cfg.vocab + 3) / 4 * 4);
+    if (st != TFM_OK) return st;
+    const tfm::LossArgs la{targets, loss, lse, mean_loss};
+    return tfm::forward_impl(m, tokens, B, S, nullptr, 0, static_cast<cudaStream_t>(stream), false,
+                             &la);
 }
 
 }  // extern "C"

@@ -16,6 +16,8 @@ enum EpiKind {
     EPI_STORE_BF16 = 2,  // out[m, n] = bf16(acc)
     EPI_SWIGLU = 3,      // out[m, f] = silu(gate) * up          (bf16 or fp32 hidden activation)
     EPI_QKV_ROPE = 4,    // RoPE on q/k columns, scatter to head-major q, k, v
+    EPI_LSE = 5,         // no output: per row running (max, sum exp) of the tile's
+                         // columns and the target column's logit (fused cross-entropy)
 };
 
 struct EpiParams {
@@ -42,6 +44,13 @@ struct EpiParams {
     // Tensor-core GEMM: 1 = each staged 32 x 32 output block is written by one TMA
     // store (or reduce-add for EPI_ACCUM_F32) through the output maps of TcMaps.
     int tma_out;
+    // EPI_LSE: targets [M]; lse_part [M][lse_slots] (max, sum of exp(z - max))
+    // pairs, slot 2 * column tile + half (the two warps of a lane quarter take
+    // alternate 32-column chunks); lse_tgt [M] the logit of the target column.
+    const int32_t* targets;
+    float2* lse_part;
+    float* lse_tgt;
+    int lse_slots;
 };
 
 // Launch with programmatic stream serialization allowed (see pdl_wait in
@@ -104,6 +113,17 @@ cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t st);
 cudaError_t launch_embed_rmsnorm(const int32_t* tok, const void* E, const float* g, float* h,
                                  void* y, int64_t M, int V, int D, float eps, int bf16,
                                  cudaStream_t st, int g_static = 0);
+
+// ---- fused cross-entropy (k_loss.cu): per row of materialised logits [M, ld]
+// one (max, sum exp) slot and the target logit; then, from any number of slots
+// per row, lse = max + log(sum), loss = lse - target logit (NaN and
+// TFM_EBADTOKEN for a target outside [0, V)); mean over the M rows in a fixed
+// order (one CTA).  loss_out / lse_out may be null; mean_out may be null.
+cudaError_t launch_lse_rows(const float* logits, int64_t ld, int M, int V, const int32_t* targets,
+                            float2* part, float* tgt, cudaStream_t st);
+cudaError_t launch_lse_finish(const float2* part, int slots, const float* tgt,
+                              const int32_t* targets, int M, int V, float* loss_out,
+                              float* lse_out, float* loss_tmp, float* mean_out, cudaStream_t st);
 
 // ---- CUDA-core kernels (k_simt.cu), fp32 mode
 // C = A[M,K] . B[N,K]^T (and A . B2^T for EPI_SWIGLU), then the epilogue.

@@ -451,16 +451,57 @@ __global__ void __launch_bounds__(kThreads, 1)
             // This warp takes every other chunk; a TMEM load costs only a few tens
             // of cycles, the global stores dominate, so more storing warps (not
             // deeper load pipelining) is what raises the epilogue's throughput.
+            if (epi.kind == EPI_LSE) {
+                // Fused cross-entropy: nothing is stored but, per row, the running
+                // max and sum of exp(z - max) over this warp's chunks of the tile,
+                // and the logit of the target column where the tile holds it.
+                constexpr float kLog2e = 1.4426950408889634f;
+                const int trg = row < M ? __ldg(epi.targets + row) : -1;
+                float mx = -INFINITY, sm = 0.f, tv = 0.f;
+                bool has_t = false;
 #pragma unroll 1
-            for (int c = half; c < nck; c += 2) {
-                uint32_t ra[32], ru[32];
-                __syncwarp();
-                tmem_ld32_issue(trow + c * 32, ra);
-                if (kDual) tmem_ld32_issue(trow + BN / 2 + c * 32, ru);
-                tmem_ld_wait();
-                reg_fence32(ra);
-                if (kDual) reg_fence32(ru);
-                process(ra, kDual ? ru : ra, c);
+                for (int c = half; c < nck; c += 2) {
+                    uint32_t ra[32];
+                    __syncwarp();
+                    tmem_ld32_issue(trow + c * 32, ra);
+                    tmem_ld_wait();
+                    reg_fence32(ra);
+                    const int col = n0 + c * 32;
+                    float cm = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (col + e < N) cm = fmaxf(cm, __uint_as_float(ra[e]));
+                    const float nm = fmaxf(mx, cm);      // finite: the chunk has a column < N
+                    float acc = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (col + e < N) acc += exp2f((__uint_as_float(ra[e]) - nm) * kLog2e);
+                    sm = sm * exp2f((mx - nm) * kLog2e) + acc;   // 2^-inf = 0 on the first chunk
+                    mx = nm;
+                    if (trg >= col && trg < col + 32) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (col + e == trg) tv = __uint_as_float(ra[e]);
+                        has_t = true;
+                    }
+                }
+                if (row < M) {
+                    epi.lse_part[(int64_t)row * epi.lse_slots + tile_n(t) * 2 + half] =
+                        make_float2(mx, sm);
+                    if (has_t) epi.lse_tgt[row] = tv;
+                }
+            } else {
+#pragma unroll 1
+                for (int c = half; c < nck; c += 2) {
+                    uint32_t ra[32], ru[32];
+                    __syncwarp();
+                    tmem_ld32_issue(trow + c * 32, ra);
+                    if (kDual) tmem_ld32_issue(trow + BN / 2 + c * 32, ru);
+                    tmem_ld_wait();
+                    reg_fence32(ra);
+                    if (kDual) reg_fence32(ru);
+                    process(ra, kDual ? ru : ra, c);
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -643,7 +684,7 @@ tfm_status plan_gemm_tc(GemmPlan* plan, const void* A, int64_t lda, const void* 
     plan->dual = dual ? 1 : 0;
     plan->skinny = 0;
     plan->b_static = 0;
-    if (M <= kBM) {
+    if (M <= kBM && epi.kind != EPI_LSE) {
         // A few rows: stream W over all SMs (k_gemm_skinny.cu).  Tiles of 128 W
         // rows (64 output columns for SwiGLU); K split so that tiles x splits
         // fills the SMs, two CTAs per SM where a CTA's ring fits twice.

@@ -62,6 +62,7 @@ _SIGS = {
     "tfm_kv_cache_create": ([_V], _I32),
     "tfm_prefill": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
     "tfm_decode_step": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
+    "tfm_forward_loss": ([_V, _V, _V, _I32, _I32, _V, _V, _V, _V], _I32),
     "tfm_forward_graph": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
     "tfm_device_status": ([_V], _I32),
     "tfm_selftest_wait_timeout": ([_I32, _V], _I32),
@@ -247,6 +248,17 @@ class Model:
         B, S = tokens.shape
         _check(self.lib.tfm_prefill(self.handle, _ptr(tokens), B, S, _ptr(logits),
                                     logits.stride(0), _stream(stream)))
+
+    def forward_loss(self, tokens, targets, loss=None, lse=None, mean=None, stream=None):
+        """Next-token cross-entropy without the logits: tokens, targets int32
+        [B, S] (device); loss, lse fp32 [B*S] and mean fp32 [1] (device), each
+        optional."""
+        B, S = tokens.shape
+        _check(self.lib.tfm_forward_loss(self.handle, _ptr(tokens), _ptr(targets), B, S,
+                                         _ptr(loss) if loss is not None else None,
+                                         _ptr(lse) if lse is not None else None,
+                                         _ptr(mean) if mean is not None else None,
+                                         _stream(stream)))
 
     def decode_step(self, tokens, pos, logits, stream=None):
         """tokens: int32 [B] (device), the new token of every sequence at position

@@ -144,6 +144,26 @@ tfm_status tfm_load_weights(void* handle, const tfm_weights* w, int32_t weights_
 tfm_status tfm_forward(void* handle, const int32_t* tokens, int32_t B, int32_t S,
                        float* logits, int64_t ld_logits, void* stream);
 
+/* Next-token cross-entropy of the forward over tokens [B, S] against targets
+ * [B, S] (int32, device; position b*S + s is scored against targets[b*S + s],
+ * normally the token after it), without writing the [B*S, vocab] logits:
+ * for each position i with logits z_i, lse_i = log sum_j exp(z_i[j]) and
+ * loss_i = lse_i - z_i[targets_i] ("LLM 2", section Optimize / Loss; CS336
+ * walkthrough (fengye404.top), section 12 训练).  In bf16 mode the LM head's
+ * GEMM keeps per row a running maximum and sum of exponentials over each tile
+ * of vocab columns and the target column's logit, and a second pass merges the
+ * tiles; fp32 mode materialises the logits in scratch and reduces each row.
+ * Outputs (device, each may be NULL): loss [B*S] and lse [B*S] fp32,
+ * mean_loss one fp32 value, the mean of loss over the B*S positions (summed in
+ * a fixed order, so repeated calls agree bit for bit).  Same limits as
+ * tfm_forward.  A target outside [0, vocab) gives that position a NaN loss and
+ * raises TFM_EBADTOKEN in the device error word (tfm_device_status).  The
+ * first call for a larger B*S allocates the scratch (blocking); later calls
+ * launch 3 + 7 n_layer kernels (4 + 7 n_layer with mean_loss) on `stream`.
+ * Calls on the same handle must not overlap. */
+tfm_status tfm_forward_loss(void* handle, const int32_t* tokens, const int32_t* targets, int32_t B,
+                            int32_t S, float* loss, float* lse, float* mean_loss, void* stream);
+
 /* tfm_forward replayed from a CUDA graph.  The first call for a given
  * (tokens, B, S, logits, ld_logits, stream) records the launch sequence into a
  * graph (nothing executes while recording), instantiates it and launches it;
