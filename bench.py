@@ -403,6 +403,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-loss", action="store_true")
+    ap.add_argument("--loss-only", action="store_true",
+                    help="only the fused cross-entropy measurement (--steps timed steps); prints "
+                         "its JSON object alone")
     ap.add_argument("--decode-only", action="store_true",
                     help="only the incremental-decoding measurement (prefill, then decode "
                          "steps); prints its JSON object alone")
@@ -507,6 +510,12 @@ def main():
     stream = torch.cuda.Stream()
     torch.cuda.set_stream(stream)
     run = model.forward if args.no_graph else model.forward_graph
+    if args.loss_only:
+        print(json.dumps({"loss": loss_rate(tfm, torch, model, cfg, tok_np, logits, stream, flush,
+                                            load_peaks(), steps=args.steps),
+                          "config": {"workload": WORKLOAD_TEXT[cfg.name]}}))
+        model.close()
+        return
     if args.decode_only:
         peaks = load_peaks()
         print(json.dumps({"decode": decode_rate(tfm, torch, model, cfg, tok_np, stream, peaks),
