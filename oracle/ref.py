@@ -19,6 +19,13 @@ Pages cited (all are tutorials; none prints code for a particular GPU):
   10 组装完整模型, 11 算参数和开销, 12 训练 (next-token targets, cross-entropy).
 * [LLM2] also: section "Optimize", subsection "Loss" (cross-entropy in the
   log-sum-exp form, perplexity).
+* GPT-2-style family: [CS336-A] the TinyGPT listing of its opening section
+  (learned position table, LayerNorm, biased linears, 4 x d_model GELU MLP);
+  [Scratch] "从零构建大语言模型" section 3 (GPT class: learned positions, Pre-LN,
+  LN then LM head); [Ch4] "Chapter 4: Implement a Transformer from Scratch"
+  sections 2 PositionalEncoding (sinusoidal table), 4 Feed-Forward (GELU), 5
+  (LayerNorm with gain and shift), 6 (weight tying); [CS336-B] 9-10 (GELUFFN,
+  the pre_norm switch: post-norm is norm(x + f(x))).
 
 Every function computes its plain definition in float64 with NumPy; matmul is
 the only library primitive used as a step.  No blocking, fusion or reordering
@@ -32,6 +39,10 @@ beyond the definition.  Where the pages are silent the readings are:
 5. Positions are 0..S-1 in every sequence.
 6. Cross-entropy is per position (no reduction inside); the mean over all
    positions and its exponential (perplexity) are separate steps.
+7. GPT-2-style family: GELU is the exact form x * Phi(x) (nn.GELU's default);
+   the sinusoidal table puts sin at even and cos at odd coordinates with
+   angle pos / 10000^(2i/d_model); post-norm blocks are still followed by the
+   final LayerNorm; the fused qkv projection's output columns are [q | k | v].
 
 Pinning: every function here is checked by the non-GPU tests against values the
 pages print, closed forms, invariants and brute force (see the oracle pin tests).
@@ -46,6 +57,8 @@ __all__ = [
     "naive_causal_attention", "silu", "swiglu", "multihead_self_attention",
     "transformer_block",
     "forward", "param_count", "cross_entropy", "perplexity",
+    "gelu", "sinusoidal_positions", "linear_bias", "gpt2_attention", "gpt2_mlp",
+    "gpt2_block", "gpt2_forward",
 ]
 
 F64 = np.float64
@@ -75,8 +88,9 @@ def rmsnorm(x, g, eps=1e-5):
 
 def layernorm(x, g, b, eps=1e-5):
     """LayerNorm over the last axis: (x - mean) / sqrt(var + eps) * g + b, with the
-    population variance.  Used only to cross-check RMSNorm ([LLM2] compares the two:
-    LayerNorm subtracts the mean, RMSNorm does not)."""
+    population variance ([LLM2] compares it with RMSNorm: LayerNorm subtracts the
+    mean, RMSNorm does not; [Ch4] 5 层归一化 writes it with gain and shift).  The
+    norm of the GPT-2-style family below."""
     x = np.asarray(x, dtype=F64)
     mu = np.mean(x, axis=-1, keepdims=True)
     var = np.mean((x - mu) ** 2, axis=-1, keepdims=True)
@@ -267,3 +281,84 @@ def cross_entropy(logits, targets):
 def perplexity(mean_loss):
     """exp of the mean cross-entropy.  [LLM2] Optimize / Loss."""
     return float(np.exp(F64(mean_loss)))
+
+
+# ---------------------------------------------------------------- GPT-2-style family
+def gelu(x):
+    """GELU(x) = x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)), the exact form.
+    [Ch4] 4 Feed-Forward Network; [CS336-B] 9 (GELUFFN)."""
+    from scipy.special import erf
+    x = np.asarray(x, dtype=F64)
+    return 0.5 * x * (1.0 + erf(x / np.sqrt(2.0)))
+
+
+def sinusoidal_positions(S, D):
+    """pe[pos, 2i] = sin(pos / 10000^(2i/D)), pe[pos, 2i+1] = cos(same), [S, D].
+    [Ch4] 2 PositionalEncoding (the formula of the original paper's section 3.5)."""
+    pos = np.arange(S, dtype=F64)[:, None]
+    i2 = np.arange(0, D, 2, dtype=F64)[None, :]
+    ang = pos / np.power(10000.0, i2 / D)
+    pe = np.zeros((S, D), dtype=F64)
+    pe[:, 0::2] = np.sin(ang)
+    pe[:, 1::2] = np.cos(ang)
+    return pe
+
+
+def linear_bias(x, W, b):
+    """Linear with a bias: y = x W^T + b.  [CS336-A] TinyGPT (nn.Linear defaults)."""
+    return linear(x, W) + np.asarray(b, dtype=F64)
+
+
+def gpt2_attention(u, layer, cfg):
+    """Fused qkv projection with bias (columns [q | k | v]), heads, causal
+    attention scaled by 1/sqrt(d_head) (no rotation: positions are in the
+    embedding), merge, output projection with bias.  [CS336-A] TinyGPT
+    CausalSelfAttention; [Ch4] 3 Multi-Head Self-Attention."""
+    H, Hkv, dh = cfg.n_head, cfg.n_kv_head, cfg.d_head
+    qkv = linear_bias(u, layer["w_qkv"], layer["b_qkv"])
+    q = _split_heads(qkv[..., : H * dh], H, dh)
+    k = _split_heads(qkv[..., H * dh: (H + Hkv) * dh], Hkv, dh)
+    v = _split_heads(qkv[..., (H + Hkv) * dh:], Hkv, dh)
+    return linear_bias(_merge_heads(causal_attention(q, k, v)), layer["w_proj"], layer["b_proj"])
+
+
+def gpt2_mlp(u, layer):
+    """fc2(GELU(fc(u))), both with bias.  [CS336-A] TinyGPT Block.mlp; [Ch4] 4."""
+    return linear_bias(gelu(linear_bias(u, layer["w_fc"], layer["b_fc"])), layer["w_fc2"],
+                       layer["b_fc2"])
+
+
+def gpt2_block(x, layer, cfg, post_norm=False):
+    """Pre-norm: x + attn(LN1(x)), then + mlp(LN2(.)).  Post-norm: LN1(x + attn(x)),
+    then LN2(. + mlp(.)).  [Scratch] 3.1; [CS336-B] 10 (the pre_norm switch)."""
+    eps = cfg.norm_eps
+    if not post_norm:
+        x = x + gpt2_attention(layernorm(x, layer["ln1_g"], layer["ln1_b"], eps), layer, cfg)
+        return x + gpt2_mlp(layernorm(x, layer["ln2_g"], layer["ln2_b"], eps), layer)
+    x = layernorm(x + gpt2_attention(x, layer, cfg), layer["ln1_g"], layer["ln1_b"], eps)
+    return layernorm(x + gpt2_mlp(x, layer), layer["ln2_g"], layer["ln2_b"], eps)
+
+
+def gpt2_forward(tokens, weights, cfg, post_norm=False, rows=None):
+    """logits of the GPT-2-style model: token embedding + position rows (the
+    learned table ``weights["pos"]``, or the sinusoidal table when it is None),
+    the blocks, the final LayerNorm, the LM head (+ its bias when given).
+    Positions are 0..S-1 per sequence.  [CS336-A] TinyGPT.forward; [Scratch] 3.2
+    GPT.forward; [Ch4] 6 TransformerLM."""
+    tokens = np.asarray(tokens)
+    B, S = tokens.shape
+    D = cfg.d_model
+    P = (np.asarray(weights["pos"], dtype=F64)[:S] if weights["pos"] is not None
+         else sinusoidal_positions(S, D))
+    rows = range(B) if rows is None else rows
+    out = []
+    for b in rows:
+        x = embedding(weights["embed"], tokens[b:b + 1]) + P[None]
+        for layer in weights["layers"][: cfg.n_layer]:
+            x = gpt2_block(x, layer, cfg, post_norm)
+        x = layernorm(x, weights["lnf_g"], weights["lnf_b"], cfg.norm_eps)
+        y = linear(x, weights["lm_head"])
+        if weights.get("lm_bias") is not None:
+            y = y + np.asarray(weights["lm_bias"], dtype=F64)
+        out.append(y[0])
+    return np.stack(out)

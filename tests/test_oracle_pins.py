@@ -381,3 +381,103 @@ def test_cross_entropy_brute_force_and_no_overflow():
     l_miss, _ = oracle.cross_entropy(big, np.array([1]))
     assert np.isfinite(l_hit).all() and abs(l_hit[0]) < 1e-300 + 1e-12
     assert abs(l_miss[0] - 1000.0) < 1e-9
+
+
+# ---------------------------------------------------------------- GPT-2-style family
+def test_gelu_exact_values_and_odd_part():
+    # x Phi(x): Phi(1) and Phi(-1) of the standard normal; gelu(x) - gelu(-x) = x
+    assert abs(oracle.gelu(1.0) - 0.8413447460685429) < 1e-15
+    assert abs(oracle.gelu(-1.0) + 0.15865525393145707) < 1e-15
+    assert oracle.gelu(0.0) == 0.0
+    x = np.linspace(-6, 6, 101)
+    assert np.allclose(oracle.gelu(x) - oracle.gelu(-x), x, rtol=0, atol=1e-14)
+    assert abs(oracle.gelu(12.0) - 12.0) < 1e-25 + 1e-14 and abs(oracle.gelu(-12.0)) < 1e-30
+
+
+def test_sinusoidal_table_values_and_rotation():
+    D = 16
+    pe = oracle.sinusoidal_positions(50, D)
+    assert np.array_equal(pe[0], np.tile([0.0, 1.0], D // 2))           # sin 0, cos 0
+    assert abs(pe[7, 0] - math.sin(7.0)) < 1e-15 and abs(pe[7, 1] - math.cos(7.0)) < 1e-15
+    assert abs(pe[3, 6] - math.sin(3 / 10000 ** (6 / D))) < 1e-15
+    # each (sin, cos) pair turns by k * omega_i from position p to p + k
+    for i in range(D // 2):
+        w = 10000.0 ** (-2 * i / D)
+        for p, k in ((4, 9), (20, 1), (0, 33)):
+            c, s = math.cos(k * w), math.sin(k * w)
+            a, b = pe[p, 2 * i], pe[p, 2 * i + 1]
+            assert abs(pe[p + k, 2 * i] - (a * c + b * s)) < 1e-12
+            assert abs(pe[p + k, 2 * i + 1] - (b * c - a * s)) < 1e-12
+
+
+def test_layernorm_shift_scale_invariance_and_moments():
+    r = np.random.default_rng(21)
+    x = r.standard_normal((5, 32))
+    g, b = r.uniform(0.5, 1.5, 32), r.standard_normal(32)
+    y = oracle.layernorm(x, np.ones(32), np.zeros(32), eps=1e-12)
+    assert np.allclose(y.mean(axis=-1), 0, atol=1e-12) and np.allclose(y.var(axis=-1), 1, atol=1e-9)
+    assert np.allclose(oracle.layernorm(3.5 * x + 7.0, g, b, eps=0), oracle.layernorm(x, g, b, eps=0),
+                       rtol=0, atol=1e-12)
+
+
+def _gpt2_zero(cfg, layers=1):
+    c = cfg.replace(n_layer=layers)
+    return c, workloads.make_gpt2_weights(c, seed=5)
+
+
+def test_gpt2_prenorm_block_with_zero_matrices_adds_the_output_biases():
+    # every matrix zero: attention rows are all b_v, so attn(u) = b_proj; mlp(u) = b_fc2
+    cfg, w = _gpt2_zero(workloads.GPT2_CONFIGS["gpt2_tiny"])
+    L = w["layers"][0]
+    for k in ("w_qkv", "w_proj", "w_fc", "w_fc2"):
+        L[k] = np.zeros_like(L[k])
+    x = np.random.default_rng(2).standard_normal((1, 9, cfg.d_model))
+    y = oracle.gpt2_block(x, L, cfg)
+    assert np.allclose(y, x + L["b_proj"] + L["b_fc2"], rtol=0, atol=1e-12)
+    # post-norm: LN2(LN1(x + b_proj) + b_fc2)
+    y = oracle.gpt2_block(x, L, cfg, post_norm=True)
+    x1 = oracle.layernorm(x + L["b_proj"], L["ln1_g"], L["ln1_b"], cfg.norm_eps)
+    assert np.allclose(y, oracle.layernorm(x1 + L["b_fc2"], L["ln2_g"], L["ln2_b"], cfg.norm_eps),
+                       rtol=0, atol=1e-12)
+
+
+def test_gpt2_attention_matches_rope_free_brute_force():
+    cfg, w = _gpt2_zero(workloads.GPT2_CONFIGS["gpt2_tiny"])
+    L = w["layers"][0]
+    u = np.random.default_rng(3).standard_normal((1, 7, cfg.d_model))
+    got = oracle.gpt2_attention(u, L, cfg)
+    D, H, dh = cfg.d_model, cfg.n_head, cfg.d_head
+    qkv = u[0] @ L["w_qkv"].astype(np.float64).T + L["b_qkv"]
+    heads = []
+    for h in range(H):
+        q = qkv[:, h * dh:(h + 1) * dh]
+        k = qkv[:, D + h * dh: D + (h + 1) * dh]
+        v = qkv[:, 2 * D + h * dh: 2 * D + (h + 1) * dh]
+        o = np.zeros((7, dh))
+        for i in range(7):
+            s = [float(q[i] @ k[j]) / math.sqrt(dh) for j in range(i + 1)]
+            m = max(s)
+            e = [math.exp(t - m) for t in s]
+            o[i] = sum(e[j] * v[j] for j in range(i + 1)) / sum(e)
+        heads.append(o)
+    ref = np.concatenate(heads, axis=1) @ L["w_proj"].astype(np.float64).T + L["b_proj"]
+    assert np.allclose(got[0], ref, rtol=0, atol=1e-12)
+
+
+def test_gpt2_model_causal_tied_and_position_tables():
+    cfg = workloads.GPT2_CONFIGS["gpt2_tiny"]
+    t = workloads.make_tokens(cfg, batch=1, seq=12, seed=9)
+    for pos, post in (("learned", False), ("sinusoidal", True)):
+        w = workloads.make_gpt2_weights(cfg, pos=pos, lm_bias=True, tied=True, max_seq=12)
+        assert w["lm_head"] is w["embed"]
+        a = oracle.gpt2_forward(t, w, cfg, post_norm=post)
+        t2 = t.copy()
+        t2[0, 8] = (t2[0, 8] + 1) % cfg.vocab
+        b = oracle.gpt2_forward(t2, w, cfg, post_norm=post)
+        assert np.array_equal(a[0, :8], b[0, :8]) and not np.allclose(a[0, 8:], b[0, 8:])
+    # zero layers, learned table: LN_f(E[t] + P[s]) E^T + bias
+    c0 = cfg.replace(n_layer=0)
+    w = workloads.make_gpt2_weights(c0, pos="learned", lm_bias=True, tied=True, max_seq=12)
+    x = w["embed"][t[0]].astype(np.float64) + w["pos"][:12]
+    ref = oracle.layernorm(x, w["lnf_g"], w["lnf_b"], cfg.norm_eps) @ w["embed"].astype(np.float64).T
+    assert np.allclose(oracle.gpt2_forward(t, w, c0)[0], ref + w["lm_bias"], rtol=0, atol=1e-12)

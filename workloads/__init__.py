@@ -27,6 +27,7 @@ import numpy as np
 __all__ = [
     "ModelConfig", "CONFIGS", "get_config", "round_to_bf16", "bf16_bits",
     "make_weights", "make_tokens", "zipf_tokens", "LAYER_KEYS",
+    "GPT2_CONFIGS", "GPT2_LAYER_KEYS", "make_gpt2_weights",
 ]
 
 
@@ -166,3 +167,74 @@ def make_tokens(cfg: ModelConfig, batch: int | None = None, seq: int | None = No
     else:
         t = rng.integers(0, cfg.vocab, B * S, dtype=np.int64).astype(np.int32)
     return t.reshape(B, S)
+
+
+# ---------------------------------------------------------------- GPT-2-style family
+# The second model family of the pages: absolute positions added to the token
+# embedding, LayerNorm with a shift, biased linears, a 4 x d_model GELU MLP, an
+# optionally tied and biased LM head.  Shapes: the toy character model of
+# "Chapter 4: Implement a Transformer from Scratch" (d_model 64, 4 heads, 2
+# layers, hidden 256) and the GPT-2-small width (768, 12 heads, 12 layers, 3072).
+GPT2_CONFIGS = {
+    "gpt2_tiny": ModelConfig("gpt2_tiny", 23, 64, 4, 4, 2, 256, 4, 64, "fp32",
+                             weight_seed=1100, token_seed=2100),
+    "gpt2_small": ModelConfig("gpt2_small", 50257, 768, 12, 12, 12, 3072, 8, 1024, "bf16",
+                              weight_seed=1101, token_seed=2101, token_dist="zipf1.1"),
+}
+
+# Per-layer names in draw order: LayerNorm gain/shift, fused [Wq; Wk; Wv] and its
+# bias, output projection and bias, LayerNorm 2, MLP up (fc) and down (fc2).
+GPT2_LAYER_KEYS = ("ln1_g", "ln1_b", "w_qkv", "b_qkv", "w_proj", "b_proj",
+                   "ln2_g", "ln2_b", "w_fc", "b_fc", "w_fc2", "b_fc2")
+
+
+def make_gpt2_weights(cfg: ModelConfig, pos: str = "learned", lm_bias: bool = False,
+                      tied: bool = False, max_seq: int | None = None,
+                      seed: int | None = None) -> dict:
+    """Draw every weight of the GPT-2-style model ``cfg`` from its seed.
+
+    Returns ``{"embed": [V,D], "pos": [max_seq,D] or None, "layers": [...],
+    "lnf_g", "lnf_b": [D], "lm_head": [V,D] (the embed array itself when tied),
+    "lm_bias": [V] or None}``.  Matrices (and the learned position table) are
+    N(0, std) (bf16-exact in bf16 mode); LayerNorm gains U(0.5, 1.5), shifts and
+    biases N(0, 0.02) in float32 from a second generator (seed + 7919)."""
+    base = cfg.weight_seed if seed is None else seed
+    rng = np.random.Generator(np.random.PCG64(base))
+    grng = np.random.Generator(np.random.PCG64(base + 7919))
+    rnd = round_to_bf16 if cfg.mode == "bf16" else (lambda a: a)
+    D, V, F, dh = cfg.d_model, cfg.vocab, cfg.d_ff, cfg.d_head
+    Nqkv = (cfg.n_head + 2 * cfg.n_kv_head) * dh
+    T = cfg.seq if max_seq is None else max_seq
+
+    def normal(shape, std):
+        return rnd(rng.standard_normal(shape, dtype=np.float32) * np.float32(std))
+
+    def small(n):
+        return (grng.standard_normal(n, dtype=np.float32) * np.float32(0.02)).astype(np.float32)
+
+    def gain(n):
+        return grng.uniform(0.5, 1.5, n).astype(np.float32)
+
+    w = {"embed": normal((V, D), cfg.std)}
+    w["pos"] = normal((T, D), cfg.std) if pos == "learned" else None
+    shapes = {"w_qkv": (Nqkv, D), "w_proj": (D, cfg.n_head * dh), "w_fc": (F, D), "w_fc2": (D, F)}
+    vecs = {"b_qkv": Nqkv, "b_proj": D, "b_fc": F, "b_fc2": D}
+    w["layers"] = []
+    for _ in range(cfg.n_layer):
+        layer = {}
+        for key in GPT2_LAYER_KEYS:
+            if key.endswith("_g"):
+                layer[key] = gain(D)
+            elif key.startswith("ln"):
+                layer[key] = small(D)
+            elif key.startswith("b_"):
+                layer[key] = small(vecs[key])
+            else:
+                std = cfg.out_proj_std if key in ("w_proj", "w_fc2") else cfg.std
+                layer[key] = normal(shapes[key], std)
+        w["layers"].append(layer)
+    w["lnf_g"] = gain(D)
+    w["lnf_b"] = small(D)
+    w["lm_head"] = w["embed"] if tied else normal((V, D), cfg.std)
+    w["lm_bias"] = small(V) if lm_bias else None
+    return w
