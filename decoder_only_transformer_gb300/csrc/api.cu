@@ -79,7 +79,7 @@ void set_last_error(const char* msg) { t_last_error = msg ? msg : ""; }
 // ------------------------------------------------------------------ config
 namespace {
 
-tfm_status check_config(const tfm_config* c) {
+tfm_status check_config(const tfm_config* c, int arch = 0) {
     if (!c) return fail(TFM_EINVAL, "config is NULL");
     if (c->vocab < 1 || c->d_model < 1 || c->n_head < 1 || c->n_kv_head < 1 || c->n_layer < 0 ||
         c->d_ff < 1 || c->max_seq < 1 || c->max_batch < 1)
@@ -90,7 +90,8 @@ tfm_status check_config(const tfm_config* c) {
     const int dh = c->d_model / c->n_head;
     if (dh % 2) return fail(TFM_EINVAL, "d_head must be even for RoPE");
     if (!(c->norm_eps > 0.f) || !std::isfinite(c->norm_eps)) return fail(TFM_EINVAL, "norm_eps must be > 0");
-    if (!(c->rope_theta > 1.f) || !std::isfinite(c->rope_theta)) return fail(TFM_EINVAL, "rope_theta must be > 1");
+    if (arch == 0 && (!(c->rope_theta > 1.f) || !std::isfinite(c->rope_theta)))
+        return fail(TFM_EINVAL, "rope_theta must be > 1");
     if ((int64_t)c->max_seq * c->max_batch > (int64_t)1 << 30) return fail(TFM_EINVAL, "max_batch*max_seq too large");
     if (c->mode == TFM_BF16) {
         if (dh != 32 && dh != 64 && dh != 128)
@@ -106,6 +107,14 @@ tfm_status check_config(const tfm_config* c) {
 }
 
 inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// float -> bf16 bit pattern, round to nearest, ties to even (finite values).
+inline uint16_t bf16_bits_rne(float f) {
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
 
 struct Sizes {
     int64_t M, D, Dq, Dkv, Nqkv, F, V, ldV, es;   // es = element size of matrices/activations
@@ -166,6 +175,18 @@ size_t weight_bytes_of(const tfm_config* c) {
            3 * 256;
 }
 
+// GPT-2-style family: matrices (fused qkv, proj, fc, fc2), LayerNorm gains and
+// shifts, biases per layer; embed, position table, final LayerNorm, LM head and
+// its bias; each piece rounded up to 256 bytes.
+size_t gpt2_weight_bytes_of(const tfm_config* c) {
+    const Sizes s = sizes_of(c);
+    const size_t per_layer =
+        (size_t)(s.Nqkv * s.D + s.D * s.Dq + 2 * s.F * s.D) * s.es +
+        (size_t)(4 * s.D + s.Nqkv + s.D + s.F + s.D) * 4;
+    return (size_t)c->n_layer * (per_layer + 12 * 256) + 2 * (size_t)s.V * s.D * s.es +
+           (size_t)c->max_seq * s.D * s.es + 2 * s.D * 4 + s.V * 4 + 6 * 256;
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ handle
@@ -184,6 +205,15 @@ struct Model {
     float* final_norm = nullptr;
     std::vector<float*> attn_norm, ffn_norm;
     std::vector<void*> wqkv, wo, w1, w3, w2;
+    // GPT-2-style family (tfm_create_gpt2): attn_norm / ffn_norm / final_norm
+    // hold the LayerNorm gains, wqkv the fused qkv, wo the projection, w1 / w2
+    // the MLP's fc / fc2; these hold the rest
+    int arch = 0;                   // 0: RMSNorm / RoPE / SwiGLU; 1: GPT-2-style
+    tfm_gpt2_options g2{};
+    void* pos = nullptr;            // position rows [max_seq, D], matrix type
+    std::vector<float*> ln1_b, ln2_b, b_qkv, b_proj, b_fc, b_fc2;
+    float* lnf_b = nullptr;
+    float* lm_bias = nullptr;
     // cached tensor-core plans for the current token count
     int64_t plan_m = -1;
     std::vector<GemmPlan> p_qkv, p_o, p_gu, p_down;
@@ -296,12 +326,30 @@ size_t tfm_weight_bytes(const tfm_config* cfg) {
     return tfm::weight_bytes_of(cfg);
 }
 
+static tfm_status create_impl(const tfm_config* cfg, int arch, const tfm_gpt2_options* opt,
+                              void** handle);
+
 tfm_status tfm_create(const tfm_config* cfg, void** handle) {
+    return create_impl(cfg, 0, nullptr, handle);
+}
+
+tfm_status tfm_create_gpt2(const tfm_config* cfg, const tfm_gpt2_options* opt, void** handle) {
+    if (!opt) return fail(TFM_EINVAL, "NULL options");
+    if (opt->pos != TFM_POS_LEARNED && opt->pos != TFM_POS_SINUSOIDAL)
+        return fail(TFM_EINVAL, "unknown position kind %d", opt->pos);
+    if (cfg && cfg->d_model % 2) return fail(TFM_EINVAL, "d_model must be even");
+    return create_impl(cfg, 1, opt, handle);
+}
+
+static tfm_status create_impl(const tfm_config* cfg, int arch, const tfm_gpt2_options* opt,
+                              void** handle) {
     if (!handle) return fail(TFM_EINVAL, "handle pointer is NULL");
-    tfm_status st = tfm::check_config(cfg);
+    tfm_status st = tfm::check_config(cfg, arch);
     if (st != TFM_OK) return st;
     Model* m = new Model();
     m->cfg = *cfg;
+    m->arch = arch;
+    if (opt) m->g2 = *opt;
     m->sz = tfm::sizes_of(cfg);
     m->lay = tfm::layout_of(cfg);
     cudaGetDevice(&m->device);
@@ -312,7 +360,7 @@ tfm_status tfm_create(const tfm_config* cfg, void** handle) {
         cudaGetLastError();
         return fail(TFM_ENOMEM, "workspace of %zu bytes: %s", bytes, cudaGetErrorString(e));
     }
-    m->wbytes = tfm::weight_bytes_of(cfg);
+    m->wbytes = arch ? tfm::gpt2_weight_bytes_of(cfg) : tfm::weight_bytes_of(cfg);
     e = cudaMalloc(&m->wmem, m->wbytes);
     if (e != cudaSuccess) {
         cudaFree(m->ws);
@@ -324,9 +372,10 @@ tfm_status tfm_create(const tfm_config* cfg, void** handle) {
     // (cos, sin) pairs, [max_seq][dh/2][2].
     const int dh = cfg->d_model / cfg->n_head, half = dh / 2;
     std::vector<float> hcs((size_t)cfg->max_seq * half * 2);
+    const double theta = arch ? 10000.0 : (double)cfg->rope_theta;   // unused by the GPT-2 family
     for (int s = 0; s < cfg->max_seq; ++s)
         for (int i = 0; i < half; ++i) {
-            const double ang = (double)s * std::pow((double)cfg->rope_theta, -2.0 * i / dh);
+            const double ang = (double)s * std::pow(theta, -2.0 * i / dh);
             hcs[((size_t)s * half + i) * 2] = (float)std::cos(ang);
             hcs[((size_t)s * half + i) * 2 + 1] = (float)std::sin(ang);
         }
@@ -381,6 +430,7 @@ void tfm_destroy(void* handle) {
 tfm_status tfm_load_weights(void* handle, const tfm_weights* w, int32_t weights_on_host) {
     Model* m = static_cast<Model*>(handle);
     if (!m || !w) return fail(TFM_EINVAL, "NULL handle or weights");
+    if (m->arch != 0) return fail(TFM_EINVAL, "a GPT-2-style handle takes tfm_load_gpt2_weights");
     const tfm_config& c = m->cfg;
     const auto& s = m->sz;
     if (!w->embed || !w->final_norm || !w->lm_head) return fail(TFM_EINVAL, "NULL embed/final_norm/lm_head");
@@ -446,6 +496,117 @@ tfm_status tfm_load_weights(void* handle, const tfm_weights* w, int32_t weights_
     return TFM_OK;
 }
 
+tfm_status tfm_load_gpt2_weights(void* handle, const tfm_gpt2_weights* w, int32_t weights_on_host) {
+    Model* m = static_cast<Model*>(handle);
+    if (!m || !w) return fail(TFM_EINVAL, "NULL handle or weights");
+    if (m->arch != 1) return fail(TFM_EINVAL, "tfm_load_gpt2_weights needs a tfm_create_gpt2 handle");
+    const tfm_config& c = m->cfg;
+    const auto& s = m->sz;
+    if (!w->embed || !w->lnf_g || !w->lnf_b || !w->lm_head)
+        return fail(TFM_EINVAL, "NULL embed / lnf_g / lnf_b / lm_head");
+    if (m->g2.pos == TFM_POS_LEARNED && !w->pos) return fail(TFM_EINVAL, "NULL learned position table");
+    if (m->g2.lm_bias && !w->lm_bias) return fail(TFM_EINVAL, "NULL lm_bias");
+    if (c.n_layer > 0 && (!w->ln1_g || !w->ln1_b || !w->w_qkv || !w->b_qkv || !w->w_proj ||
+                          !w->b_proj || !w->ln2_g || !w->ln2_b || !w->w_fc || !w->b_fc ||
+                          !w->w_fc2 || !w->b_fc2))
+        return fail(TFM_EINVAL, "NULL per-layer weight array");
+    for (int l = 0; l < c.n_layer; ++l)
+        if (!w->ln1_g[l] || !w->ln1_b[l] || !w->w_qkv[l] || !w->b_qkv[l] || !w->w_proj[l] ||
+            !w->b_proj[l] || !w->ln2_g[l] || !w->ln2_b[l] || !w->w_fc[l] || !w->b_fc[l] ||
+            !w->w_fc2[l] || !w->b_fc2[l])
+            return fail(TFM_EINVAL, "NULL weight pointer in layer %d", l);
+    const cudaMemcpyKind kind = weights_on_host ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice;
+    size_t off = 0;
+    bool over = false;
+    auto take = [&](size_t bytes) {
+        uint8_t* p = m->wmem + off;
+        off += (bytes + 255) / 256 * 256;
+        if (off > m->wbytes) over = true;
+        return p;
+    };
+    cudaError_t e = cudaSuccess;
+    auto copy = [&](void* dst, const void* src, size_t bytes) {
+        if (e == cudaSuccess && !over) e = cudaMemcpy(dst, src, bytes, kind);
+    };
+    const size_t es = s.es;
+    m->embed = take(s.V * s.D * es);
+    copy(m->embed, w->embed, s.V * s.D * es);
+    m->pos = take((size_t)c.max_seq * s.D * es);
+    if (m->g2.pos == TFM_POS_LEARNED) {
+        copy(m->pos, w->pos, (size_t)c.max_seq * s.D * es);
+    } else if (!over && e == cudaSuccess) {
+        // pe[p, 2i] = sin(p / 10000^(2i/D)), pe[p, 2i+1] = cos(same), in float64,
+        // stored in the matrix type ("Chapter 4", section 2 PositionalEncoding)
+        std::vector<uint8_t> host((size_t)c.max_seq * s.D * es);
+        for (int p = 0; p < c.max_seq; ++p)
+            for (int i = 0; i < s.D; i += 2) {
+                const double ang = (double)p / std::pow(10000.0, (double)i / (double)s.D);
+                const double v2[2] = {std::sin(ang), std::cos(ang)};
+                for (int k = 0; k < 2 && i + k < s.D; ++k) {
+                    const size_t at = (size_t)p * s.D + i + k;
+                    if (es == 2) {
+                        const uint16_t b = tfm::bf16_bits_rne((float)v2[k]);
+                        std::memcpy(host.data() + at * 2, &b, 2);
+                    } else {
+                        const float f = (float)v2[k];
+                        std::memcpy(host.data() + at * 4, &f, 4);
+                    }
+                }
+            }
+        e = cudaMemcpy(m->pos, host.data(), host.size(), cudaMemcpyHostToDevice);
+    }
+    auto vec = [&](std::vector<float*>& dst, const void* const* src, int64_t n) {
+        dst.assign(c.n_layer, nullptr);
+        for (int l = 0; l < c.n_layer; ++l) {
+            dst[l] = reinterpret_cast<float*>(take(n * 4));
+            copy(dst[l], src[l], n * 4);
+        }
+    };
+    auto mat = [&](std::vector<void*>& dst, const void* const* src, int64_t rows, int64_t cols) {
+        dst.assign(c.n_layer, nullptr);
+        for (int l = 0; l < c.n_layer; ++l) {
+            dst[l] = take(rows * cols * es);
+            copy(dst[l], src[l], rows * cols * es);
+        }
+    };
+    if (c.n_layer > 0) {
+        vec(m->attn_norm, w->ln1_g, s.D);
+        vec(m->ln1_b, w->ln1_b, s.D);
+        mat(m->wqkv, w->w_qkv, s.Nqkv, s.D);
+        vec(m->b_qkv, w->b_qkv, s.Nqkv);
+        mat(m->wo, w->w_proj, s.D, s.Dq);
+        vec(m->b_proj, w->b_proj, s.D);
+        vec(m->ffn_norm, w->ln2_g, s.D);
+        vec(m->ln2_b, w->ln2_b, s.D);
+        mat(m->w1, w->w_fc, s.F, s.D);
+        vec(m->b_fc, w->b_fc, s.F);
+        mat(m->w2, w->w_fc2, s.D, s.F);
+        vec(m->b_fc2, w->b_fc2, s.D);
+    }
+    m->w3.assign(c.n_layer, nullptr);
+    m->final_norm = reinterpret_cast<float*>(take(s.D * 4));
+    copy(m->final_norm, w->lnf_g, s.D * 4);
+    m->lnf_b = reinterpret_cast<float*>(take(s.D * 4));
+    copy(m->lnf_b, w->lnf_b, s.D * 4);
+    if (w->lm_head == w->embed) {
+        m->lm_head = m->embed;
+    } else {
+        m->lm_head = take(s.V * s.D * es);
+        copy(m->lm_head, w->lm_head, s.V * s.D * es);
+    }
+    m->lm_bias = nullptr;
+    if (m->g2.lm_bias) {
+        m->lm_bias = reinterpret_cast<float*>(take(s.V * 4));
+        copy(m->lm_bias, w->lm_bias, s.V * 4);
+    }
+    if (over) return fail(TFM_EINVAL, "internal: weight storage overflow");
+    if (e != cudaSuccess) return tfm::cuda_fail(e, "tfm_load_gpt2_weights");
+    m->loaded = true;
+    m->plan_m = -1;
+    m->lse_M = -1;
+    return TFM_OK;
+}
+
 }  // extern "C"
 
 namespace tfm {
@@ -492,25 +653,37 @@ tfm_status build_plans(Model* m, int M, int S, float* logits, int64_t ld) {
     m->p_down.resize(c.n_layer);
     m->plan_m = -1;
     tfm_status st = TFM_OK;
+    const bool g2 = m->arch == 1;   // GPT-2-style: biases, no RoPE, a GELU MLP
     for (int l = 0; l < c.n_layer && st == TFM_OK; ++l) {
+        EpiParams eq = epi_qkv(m, M, S);
+        if (g2) {
+            eq.rope_cs = nullptr;
+            eq.bias = m->b_qkv[l];
+        }
         st = plan_gemm_tc(&m->p_qkv[l], m->xn(), s.D, m->wqkv[l], nullptr, s.D, M, (int)s.Nqkv,
-                          (int)s.D, epi_qkv(m, M, S));
+                          (int)s.D, eq);
+        EpiParams eo = epi_basic(EPI_ACCUM_F32, M, (int)s.D, m->h(), s.D);
+        if (g2) eo.bias = m->b_proj[l];
         if (st == TFM_OK)
             st = plan_gemm_tc(&m->p_o[l], m->o(), s.Dq, m->wo[l], nullptr, s.Dq, M, (int)s.D,
-                              (int)s.Dq, epi_basic(EPI_ACCUM_F32, M, (int)s.D, m->h(), s.D));
+                              (int)s.Dq, eo);
         if (st == TFM_OK) {
-            EpiParams e = epi_basic(EPI_SWIGLU, M, (int)s.F, m->a(), s.F);
+            EpiParams e = epi_basic(g2 ? EPI_GELU : EPI_SWIGLU, M, (int)s.F, m->a(), s.F);
             e.out_bf16 = 1;
-            st = plan_gemm_tc(&m->p_gu[l], m->xn(), s.D, m->w1[l], m->w3[l], s.D, M, (int)s.F,
-                              (int)s.D, e);
+            if (g2) e.bias = m->b_fc[l];
+            st = plan_gemm_tc(&m->p_gu[l], m->xn(), s.D, m->w1[l], g2 ? nullptr : m->w3[l], s.D, M,
+                              (int)s.F, (int)s.D, e);
         }
+        EpiParams ed = epi_basic(EPI_ACCUM_F32, M, (int)s.D, m->h(), s.D);
+        if (g2) ed.bias = m->b_fc2[l];
         if (st == TFM_OK)
             st = plan_gemm_tc(&m->p_down[l], m->a(), s.F, m->w2[l], nullptr, s.F, M, (int)s.D,
-                              (int)s.F, epi_basic(EPI_ACCUM_F32, M, (int)s.D, m->h(), s.D));
+                              (int)s.F, ed);
     }
+    EpiParams el = epi_basic(EPI_STORE_F32, M, (int)s.V, logits, ld);
+    el.bias = m->lm_bias;
     if (st == TFM_OK)
-        st = plan_gemm_tc(&m->p_lm, m->xn(), s.D, m->lm_head, nullptr, s.D, M, (int)s.V, (int)s.D,
-                          epi_basic(EPI_STORE_F32, M, (int)s.V, logits, ld));
+        st = plan_gemm_tc(&m->p_lm, m->xn(), s.D, m->lm_head, nullptr, s.D, M, (int)s.V, (int)s.D, el);
     if (st != TFM_OK) return fail(st, "could not encode TMA tensor maps (driver entry point missing?)");
     // the model's weights: no launch writes them once loaded
     for (int l = 0; l < c.n_layer; ++l)
@@ -587,6 +760,7 @@ tfm_status build_lse_plan(Model* m, int M, const int32_t* targets) {
     if (m->lse_M == M && m->lse_targets == targets) return TFM_OK;
     const auto& s = m->sz;
     EpiParams e = epi_basic(EPI_LSE, M, (int)s.V, nullptr, 0);
+    e.bias = m->lm_bias;
     e.targets = targets;
     e.lse_part = m->lse_part;
     e.lse_tgt = m->lse_tgt;
@@ -639,16 +813,57 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
         if (!ev) return fail(TFM_ECUDA, "cudaEventCreate failed");
         cudaEventRecord(ev, st);
     }
+    // The GPT-2-style family: LayerNorm (gain, shift), position rows in the
+    // embedding, post-norm blocks normalising the residual stream in place.
+    const bool g2 = m->arch == 1;
+    const bool post = g2 && m->g2.post_norm;
+    auto ln_args = [&](const float* b, float* h_out) {
+        NormArgs n{};
+        n.kind = kNormLayer;
+        n.b = b;
+        n.h_out = h_out;
+        return n;
+    };
     // Embedding and the first norm (layer 0's input norm, or the final norm of a
-    // model without layers) in one pass.
+    // model without layers; none before a post-norm block) in one pass.
+    NormArgs na0{};
+    if (g2) {
+        if (c.n_layer == 0) na0 = ln_args(m->lnf_b, nullptr);
+        else if (post) na0.kind = kNormNone;
+        else na0 = ln_args(m->ln1_b[0], nullptr);
+        na0.pos = m->pos;
+        na0.S = S;
+    }
     TFM_LAUNCH(K_EMBED, launch_embed_rmsnorm(tokens, m->embed,
                                              c.n_layer > 0 ? m->attn_norm[0] : m->final_norm,
                                              m->h(), m->xn(), M, c.vocab, c.d_model, c.norm_eps,
-                                             bf, st, 1));
+                                             bf, st, 1, g2 ? &na0 : nullptr));
+    // the norms of a layer: before the attention (pre-norm, l > 0), after the
+    // output projection (post-norm LN1 in place, or the pre-norm FFN input), after
+    // the MLP (post-norm LN2 in place)
+    auto norm_pre_attn = [&](int l) -> cudaError_t {
+        NormArgs n = g2 ? ln_args(m->ln1_b[l], nullptr) : NormArgs{};
+        return launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), M, c.d_model, c.norm_eps, bf, st, 1,
+                              g2 ? &n : nullptr);
+    };
+    auto norm_mid = [&](int l) -> cudaError_t {
+        NormArgs n = post ? ln_args(m->ln1_b[l], m->h())
+                          : (g2 ? ln_args(m->ln2_b[l], nullptr) : NormArgs{});
+        return launch_rmsnorm(m->h(), post ? m->attn_norm[l] : m->ffn_norm[l], m->xn(), M,
+                              c.d_model, c.norm_eps, bf, st, 1, g2 ? &n : nullptr);
+    };
+    auto norm_post_mlp = [&](int l) -> cudaError_t {
+        NormArgs n = ln_args(m->ln2_b[l], m->h());
+        return launch_rmsnorm(m->h(), m->ffn_norm[l], m->xn(), M, c.d_model, c.norm_eps, bf, st, 1, &n);
+    };
+    auto norm_final = [&]() -> cudaError_t {
+        NormArgs n = g2 ? ln_args(m->lnf_b, nullptr) : NormArgs{};
+        return launch_rmsnorm(m->h(), m->final_norm, m->xn(), M, c.d_model, c.norm_eps, bf, st, 1,
+                              g2 ? &n : nullptr);
+    };
     if (bf) {
         for (int l = 0; l < c.n_layer; ++l) {
-            if (l > 0)
-                TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 1, st, 1));
+            if (l > 0 && !post) TFM_LAUNCH(K_NORM, norm_pre_attn(l));
             TFM_LAUNCH(K_QKV, launch_gemm_tc(m->p_qkv[l], st));
             if (to_cache) {
                 // k, v of positions [0, S) into the layer's cache: rows (b, kv head)
@@ -668,12 +883,12 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
                 TFM_LAUNCH(K_ATTN, launch_attention_bf16(m->q(), m->k(), m->v(), m->o(), B,
                                                          c.n_head, c.n_kv_head, S, dh, scale, st));
             TFM_LAUNCH(K_OPROJ, launch_gemm_tc(m->p_o[l], st));
-            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->ffn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 1, st, 1));
+            TFM_LAUNCH(K_NORM, norm_mid(l));
             TFM_LAUNCH(K_GATEUP, launch_gemm_tc(m->p_gu[l], st));
             TFM_LAUNCH(K_DOWN, launch_gemm_tc(m->p_down[l], st));
+            if (post) TFM_LAUNCH(K_NORM, norm_post_mlp(l));
         }
-        if (c.n_layer > 0)
-            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->final_norm, m->xn(), M, c.d_model, c.norm_eps, 1, st, 1));
+        if (c.n_layer > 0) TFM_LAUNCH(K_NORM, norm_final());
         if (la) {
             TFM_LAUNCH(K_LMHEAD, launch_gemm_tc(m->p_lse, st));
             TFM_LAUNCH(K_LMHEAD, launch_lse_finish(m->lse_part, m->p_lse.epi.lse_slots, m->lse_tgt,
@@ -685,39 +900,48 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
     } else {
         const float* xn = static_cast<const float*>(m->xn());
         for (int l = 0; l < c.n_layer; ++l) {
-            if (l > 0)
-                TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 0, st, 1));
+            if (l > 0 && !post) TFM_LAUNCH(K_NORM, norm_pre_attn(l));
+            EpiParams eq = epi_qkv(m, M, S);
+            if (g2) {
+                eq.rope_cs = nullptr;
+                eq.bias = m->b_qkv[l];
+            }
             TFM_LAUNCH(K_QKV, launch_gemm_simt(xn, static_cast<const float*>(m->wqkv[l]), nullptr, M,
-                                               (int)s.Nqkv, c.d_model, epi_qkv(m, M, S), st));
+                                               (int)s.Nqkv, c.d_model, eq, st));
             TFM_LAUNCH(K_ATTN, launch_attention_simt(static_cast<const float*>(m->q()),
                                                      static_cast<const float*>(m->k()),
                                                      static_cast<const float*>(m->v()),
                                                      static_cast<float*>(m->o()), B, c.n_head,
                                                      c.n_kv_head, S, dh, scale, st));
+            EpiParams eo = epi_basic(EPI_ACCUM_F32, M, c.d_model, m->h(), s.D);
+            if (g2) eo.bias = m->b_proj[l];
             TFM_LAUNCH(K_OPROJ, launch_gemm_simt(static_cast<const float*>(m->o()),
                                                  static_cast<const float*>(m->wo[l]), nullptr, M,
-                                                 c.d_model, (int)s.Dq,
-                                                 epi_basic(EPI_ACCUM_F32, M, c.d_model, m->h(), s.D), st));
-            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->ffn_norm[l], m->xn(), M, c.d_model, c.norm_eps, 0, st, 1));
-            EpiParams e = epi_basic(EPI_SWIGLU, M, c.d_ff, m->a(), s.F);
+                                                 c.d_model, (int)s.Dq, eo, st));
+            TFM_LAUNCH(K_NORM, norm_mid(l));
+            EpiParams e = epi_basic(g2 ? EPI_GELU : EPI_SWIGLU, M, c.d_ff, m->a(), s.F);
             e.out_bf16 = 0;
+            if (g2) e.bias = m->b_fc[l];
             TFM_LAUNCH(K_GATEUP, launch_gemm_simt(xn, static_cast<const float*>(m->w1[l]),
-                                                  static_cast<const float*>(m->w3[l]), M, c.d_ff,
-                                                  c.d_model, e, st));
+                                                  g2 ? nullptr : static_cast<const float*>(m->w3[l]),
+                                                  M, c.d_ff, c.d_model, e, st));
+            EpiParams ed = epi_basic(EPI_ACCUM_F32, M, c.d_model, m->h(), s.D);
+            if (g2) ed.bias = m->b_fc2[l];
             TFM_LAUNCH(K_DOWN, launch_gemm_simt(static_cast<const float*>(m->a()),
                                                 static_cast<const float*>(m->w2[l]), nullptr, M,
-                                                c.d_model, c.d_ff,
-                                                epi_basic(EPI_ACCUM_F32, M, c.d_model, m->h(), s.D), st));
+                                                c.d_model, c.d_ff, ed, st));
+            if (post) TFM_LAUNCH(K_NORM, norm_post_mlp(l));
         }
-        if (c.n_layer > 0)
-            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->final_norm, m->xn(), M, c.d_model, c.norm_eps, 0, st, 1));
+        if (c.n_layer > 0) TFM_LAUNCH(K_NORM, norm_final());
+        EpiParams el = epi_basic(EPI_STORE_F32, M, c.vocab, logits, ld);
+        el.bias = m->lm_bias;
         if (la) {
             // fp32 mode: the logits in scratch, then one pass over each row
             const int64_t ldV = (c.vocab + 3) / 4 * 4;
+            el.out = m->loss_logits;
+            el.ldo = ldV;
             TFM_LAUNCH(K_LMHEAD, launch_gemm_simt(xn, static_cast<const float*>(m->lm_head), nullptr, M,
-                                                  c.vocab, c.d_model,
-                                                  epi_basic(EPI_STORE_F32, M, c.vocab, m->loss_logits, ldV),
-                                                  st));
+                                                  c.vocab, c.d_model, el, st));
             TFM_LAUNCH(K_LMHEAD, launch_lse_rows(m->loss_logits, ldV, M, c.vocab, la->targets,
                                                  m->lse_part, m->lse_tgt, st));
             TFM_LAUNCH(K_LMHEAD, launch_lse_finish(m->lse_part, 1, m->lse_tgt, la->targets, M,
@@ -725,8 +949,7 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
                                                    st));
         } else {
             TFM_LAUNCH(K_LMHEAD, launch_gemm_simt(xn, static_cast<const float*>(m->lm_head), nullptr, M,
-                                                  c.vocab, c.d_model,
-                                                  epi_basic(EPI_STORE_F32, M, c.vocab, logits, ld), st));
+                                                  c.vocab, c.d_model, el, st));
         }
     }
     return TFM_OK;
@@ -1032,6 +1255,7 @@ tfm_status tfm_kv_cache_create(void* handle) {
     const tfm_config& c = m->cfg;
     const int dh = c.d_model / c.n_head;
     if (c.mode != TFM_BF16) return fail(TFM_EUNSUPPORTED, "the KV cache needs bf16 mode");
+    if (m->arch != 0) return fail(TFM_EUNSUPPORTED, "the KV cache is for the RoPE family only");
     if (!tfm::decode_supported(dh, c.n_head / c.n_kv_head))
         return fail(TFM_EUNSUPPORTED, "decode needs d_head in {32, 64, 128} and H/Hkv in {1, 2, 4, 8, 16} (<= 8 at d_head 128)");
     const size_t layer = (size_t)c.max_batch * c.n_kv_head * c.max_seq * dh * 2;

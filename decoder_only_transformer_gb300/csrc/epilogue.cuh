@@ -147,16 +147,33 @@ __device__ __forceinline__ int64_t qkv_offset(const EpiParams& p, const QkvSlot&
 // Output values of one chunk: a = accumulator columns [col0, col0+W) of output
 // row `row`; u = the matching "up" columns for EPI_SWIGLU (ignored otherwise).
 // For EPI_QKV_ROPE the chunk lies inside one head (W divides dh), col0 % W == 0.
+// GELU(z) = z * Phi(z) = 0.5 z (1 + erf(z / sqrt 2)), the exact form ("Chapter 4",
+// section 4; CS336 walkthrough (fengye404.top), section 9 GELUFFN).
+__device__ __forceinline__ float gelu_exact(float z) {
+    return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
+}
+
 template <int W>
 __device__ __forceinline__ void epi_compute(const EpiParams& p, int row, int col0,
-                                            const float (&a)[W], const float (&u)[W],
+                                            const float (&a_in)[W], const float (&u)[W],
                                             float (&o)[W]) {
-    if (p.kind == EPI_SWIGLU) {
+    float a[W];
+#pragma unroll
+    for (int i = 0; i < W; ++i) a[i] = a_in[i];
+    if (p.bias) {
+#pragma unroll
+        for (int i = 0; i < W; ++i)
+            if (col0 + i < p.N) a[i] += __ldg(p.bias + col0 + i);
+    }
+    if (p.kind == EPI_GELU) {
+#pragma unroll
+        for (int i = 0; i < W; ++i) o[i] = gelu_exact(a[i]);
+    } else if (p.kind == EPI_SWIGLU) {
 #pragma unroll
         for (int i = 0; i < W; ++i) o[i] = silu(a[i]) * u[i];
     } else if (p.kind == EPI_QKV_ROPE) {
         const QkvSlot q = qkv_slot(p, col0);
-        if (q.region < 2 && row < p.M) {
+        if (q.region < 2 && row < p.M && p.rope_cs) {
             const int dh = p.dh;
             const int s = epi_pos0(p) + row % p.S;
             float cs[W];                       // (cos, sin) of the W/2 pairs
@@ -195,6 +212,7 @@ __device__ __forceinline__ void epi_store_direct(const EpiParams& p, int row, in
                               n_valid);
             break;
         case EPI_SWIGLU:
+        case EPI_GELU:
             if (p.out_bf16)
                 store_row_bf16<W>(static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * p.ldo + col0,
                                   o, n_valid);

@@ -18,6 +18,7 @@ enum EpiKind {
     EPI_QKV_ROPE = 4,    // RoPE on q/k columns, scatter to head-major q, k, v
     EPI_LSE = 5,         // no output: per row running (max, sum exp) of the tile's
                          // columns and the target column's logit (fused cross-entropy)
+    EPI_GELU = 6,        // out[m, n] = gelu(acc), exact form  (bf16 or fp32 hidden activation)
 };
 
 struct EpiParams {
@@ -37,7 +38,10 @@ struct EpiParams {
     // when set, pos0 is read from this device word (a decode step replayed from a
     // recorded graph, the position changing between replays)
     const int* pos0_dev;
-    const float* rope_cs;    // [>= S, dh/2, 2]: cos, sin of s * theta^(-2i/dh)
+    const float* rope_cs;    // [>= S, dh/2, 2]: cos, sin of s * theta^(-2i/dh); null: no rotation
+    // fp32 [N], added to the accumulator column before everything else (the
+    // biased linears of the GPT-2-style family); null: none
+    const float* bias;
     void* q;
     void* k;
     void* v;
@@ -100,19 +104,32 @@ int sm_count();
 const char* cuda_error_text(cudaError_t e);
 
 // ---- elementwise kernels (k_rows.cu)
+// How a row is normalised: RMSNorm (the default), LayerNorm with shift b, or no
+// norm (cast only).  h_out: also store the fp32 normalised row (may equal the
+// input).  pos (embedding kernels only): position rows [>= S, D] in the
+// embedding's type added to E[tok[m]], row m taking position m % S.
+enum NormKind { kNormRms = 0, kNormLayer = 1, kNormNone = 2 };
+struct NormArgs {
+    int kind;
+    const float* b;
+    float* h_out;
+    const void* pos;
+    int S;
+};
 cudaError_t launch_embedding(const int32_t* tok, const void* E, float* h, int64_t M, int V,
                              int D, int e_bf16, cudaStream_t st);
 // g_static = 1: no launch on the stream writes g (a model's gain), so a few-row
 // launch may load it before its grid dependency wait.
 cudaError_t launch_rmsnorm(const float* x, const float* g, void* y, int64_t M, int D, float eps,
-                           int out_bf16, cudaStream_t st, int g_static = 0);
+                           int out_bf16, cudaStream_t st, int g_static = 0,
+                           const NormArgs* na = nullptr);
 cudaError_t launch_rope(void* x, const int32_t* pos, int B, int H, int S, int dh, float theta,
                         int is_bf16, cudaStream_t st);
 cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t st);
 // h = E[tok] and y = RMSNorm(h) * g in one pass (bf16: E and y bf16; else fp32).
 cudaError_t launch_embed_rmsnorm(const int32_t* tok, const void* E, const float* g, float* h,
                                  void* y, int64_t M, int V, int D, float eps, int bf16,
-                                 cudaStream_t st, int g_static = 0);
+                                 cudaStream_t st, int g_static = 0, const NormArgs* na = nullptr);
 
 // ---- fused cross-entropy (k_loss.cu): per row of materialised logits [M, ld]
 // one (max, sum exp) slot and the target logit; then, from any number of slots

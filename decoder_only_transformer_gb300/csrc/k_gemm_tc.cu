@@ -366,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // offset inside its head (chunks step by 64 columns), so the thread's
         // (cos, sin) pairs are the same for all of them.  They are loaded once per
         // tile, before the accumulator wait, instead of once per chunk.
-        const bool rope_pre = epi.kind == EPI_QKV_ROPE && epi.dh <= 64;
+        const bool rope_pre = epi.kind == EPI_QKV_ROPE && epi.dh <= 64 && epi.rope_cs && !epi.bias;
         const int rope_d0 = (half * 32) % epi.dh;
         const int rot_cols = (epi.n_head + epi.n_kv_head) * epi.dh;   // q and k columns
         float rcs[32];
@@ -467,6 +467,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_wait();
                     reg_fence32(ra);
                     const int col = n0 + c * 32;
+                    if (epi.bias) {                      // a biased LM head
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (col + e < N)
+                                ra[e] = __float_as_uint(__uint_as_float(ra[e]) + __ldg(epi.bias + col + e));
+                    }
                     float cm = -INFINITY;
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
@@ -658,6 +664,7 @@ bool plan_tma_out(TcMaps* maps, const EpiParams& e) {
             return e.out && aligned16_ptr(e.out) && (e.ldo * 2) % 16 == 0 &&
                    make_out_map(&maps->out, e.out, e.M, e.N, e.ldo, true);
         case EPI_SWIGLU:
+        case EPI_GELU:
             return e.out_bf16 && e.out && aligned16_ptr(e.out) && (e.ldo * 2) % 16 == 0 &&
                    make_out_map(&maps->out, e.out, e.M, e.N, e.ldo, true);
         case EPI_QKV_ROPE: {

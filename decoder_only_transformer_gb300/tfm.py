@@ -44,6 +44,24 @@ class Weights(ctypes.Structure):
                 ("w2", _PP), ("final_norm", ctypes.c_void_p), ("lm_head", ctypes.c_void_p)]
 
 
+class Gpt2Options(ctypes.Structure):
+    _fields_ = [("pos", ctypes.c_int32), ("post_norm", ctypes.c_int32),
+                ("lm_bias", ctypes.c_int32)]
+
+
+GPT2_WEIGHT_FIELDS = ("embed", "pos", "ln1_g", "ln1_b", "w_qkv", "b_qkv", "w_proj", "b_proj",
+                      "ln2_g", "ln2_b", "w_fc", "b_fc", "w_fc2", "b_fc2", "lnf_g", "lnf_b",
+                      "lm_head", "lm_bias")
+_GPT2_LAYER = ("ln1_g", "ln1_b", "w_qkv", "b_qkv", "w_proj", "b_proj", "ln2_g", "ln2_b", "w_fc",
+               "b_fc", "w_fc2", "b_fc2")
+
+
+class Gpt2Weights(ctypes.Structure):
+    _fields_ = [(k, _PP if k in _GPT2_LAYER else ctypes.c_void_p) for k in GPT2_WEIGHT_FIELDS]
+
+
+TFM_POS_LEARNED, TFM_POS_SINUSOIDAL = 0, 1
+
 _lib = None
 
 _V, _I32, _I64, _F, _SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
@@ -54,6 +72,8 @@ _SIGS = {
     "tfm_workspace_bytes": ([ctypes.POINTER(Config)], _SZ),
     "tfm_weight_bytes": ([ctypes.POINTER(Config)], _SZ),
     "tfm_create": ([ctypes.POINTER(Config), ctypes.POINTER(_V)], _I32),
+    "tfm_create_gpt2": ([ctypes.POINTER(Config), ctypes.POINTER(Gpt2Options), ctypes.POINTER(_V)], _I32),
+    "tfm_load_gpt2_weights": ([_V, ctypes.POINTER(Gpt2Weights), _I32], _I32),
     "tfm_load_weights": ([_V, ctypes.POINTER(Weights), _I32], _I32),
     "tfm_forward": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
     "tfm_forward_host": ([_V, _V, _I32, _I32, _V, _I64, _V], _I32),
@@ -338,3 +358,39 @@ def swiglu(x, w1, w3, w2, y, workspace, accumulate=False, stream=None):
     _check(load().tfm_swiglu(_ptr(x), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(y), M, D, F,
                              1 if accumulate else 0, _ptr(workspace), nbytes, _mode_of(x),
                              _stream(stream)))
+
+
+class Gpt2Model(Model):
+    """A libtfm handle of the GPT-2-style family (tfm_create_gpt2).  ``weights``
+    is the dict layout of ``workloads.make_gpt2_weights`` with torch tensors
+    (device or pinned host); ``pos`` is "learned" or "sinusoidal"."""
+
+    def __init__(self, cfg, pos="learned", post_norm=False, lm_bias=False, max_batch=None,
+                 max_seq=None):
+        self.lib = load()
+        self.cfg = cfg
+        self.c = make_config(cfg, max_batch, max_seq)
+        self.opt = Gpt2Options(TFM_POS_LEARNED if pos == "learned" else TFM_POS_SINUSOIDAL,
+                               1 if post_norm else 0, 1 if lm_bias else 0)
+        h = ctypes.c_void_p()
+        _check(self.lib.tfm_create_gpt2(ctypes.byref(self.c), ctypes.byref(self.opt),
+                                        ctypes.byref(h)))
+        self.handle = h
+
+    def load_weights(self, w: dict):
+        L = self.cfg.n_layer
+        keep = []
+        vals = []
+        for key in GPT2_WEIGHT_FIELDS:
+            if key in _GPT2_LAYER:
+                a = (ctypes.c_void_p * max(L, 1))()
+                for i in range(L):
+                    a[i] = w["layers"][i][key].data_ptr()
+                keep.append(a)
+                vals.append(ctypes.cast(a, _PP))
+            else:
+                t = w.get(key)
+                vals.append(t.data_ptr() if t is not None else None)
+        ws = Gpt2Weights(*vals)
+        on_host = 0 if w["embed"].is_cuda else 1
+        _check(self.lib.tfm_load_gpt2_weights(self.handle, ctypes.byref(ws), on_host))

@@ -133,6 +133,71 @@ tfm_status tfm_create(const tfm_config* cfg, void** handle);
  * afterwards. */
 tfm_status tfm_load_weights(void* handle, const tfm_weights* w, int32_t weights_on_host);
 
+/* ---- GPT-2-style family (a second model the pages build): absolute
+ * positions added to the token embedding (a learned table, "从零构建大语言模型"
+ * section 3.2 and the CS336 walkthrough's TinyGPT; or the sinusoidal table,
+ * "Chapter 4: Implement a Transformer from Scratch" section 2), LayerNorm with
+ * gain and shift, biased linears, a fused qkv projection, an MLP
+ * fc2(GELU(fc(x))) with the exact GELU (Chapter 4 section 4; CS336 walkthrough
+ * (fengye404.top) section 9 GELUFFN), no RoPE, a final LayerNorm and an LM head
+ * that may be tied to the embedding and may carry a bias:
+ *   h = E[tokens] + P[position]
+ *   pre-norm:  h += proj(Attn(qkv(LN1(h)))),  h += fc2(GELU(fc(LN2(h))))
+ *   post-norm: h = LN1(h + proj(Attn(qkv(h)))), h = LN2(h + fc2(GELU(fc(h))))
+ *              (the CS336 walkthrough's pre_norm=False switch, section 10)
+ *   logits = lm_head . LNf(h) (+ lm_bias)
+ * tfm_config is read as for the first family except rope_theta (unused, not
+ * checked); d_ff is the MLP width (4 d_model in the pages).  The forward,
+ * graph, host-buffer and cross-entropy entry points take either kind of
+ * handle; the KV cache (tfm_kv_cache_create) is for the first family only. */
+typedef enum { TFM_POS_LEARNED = 0, TFM_POS_SINUSOIDAL = 1 } tfm_pos_kind;
+typedef struct {
+    int32_t pos;           /* tfm_pos_kind */
+    int32_t post_norm;     /* 0: pre-norm blocks; 1: post-norm blocks */
+    int32_t lm_bias;       /* 1: the LM head has a bias */
+} tfm_gpt2_options;
+
+/* Weights of the GPT-2-style family.  Matrices (out_features, in_features)
+ * row-major, bf16 in bf16 mode and fp32 in fp32 mode; LayerNorm gains/shifts and
+ * biases fp32.  Per-layer entries are arrays of n_layer pointers.  With
+ * Nqkv = (n_head + 2 n_kv_head) d_head:
+ *   embed [vocab, d_model]; pos [max_seq, d_model] (learned positions; ignored
+ *   for sinusoidal, which the library builds in float64 and stores in the
+ *   matrix type); ln1_g, ln1_b, ln2_g, ln2_b [d_model]; w_qkv [Nqkv, d_model]
+ *   (rows q | k | v), b_qkv [Nqkv]; w_proj [d_model, n_head d_head], b_proj
+ *   [d_model]; w_fc [d_ff, d_model], b_fc [d_ff]; w_fc2 [d_model, d_ff], b_fc2
+ *   [d_model]; lnf_g, lnf_b [d_model]; lm_head [vocab, d_model] (may be the
+ *   embed pointer: tied); lm_bias [vocab] (when options.lm_bias). */
+typedef struct {
+    const void* embed;
+    const void* pos;
+    const void* const* ln1_g;
+    const void* const* ln1_b;
+    const void* const* w_qkv;
+    const void* const* b_qkv;
+    const void* const* w_proj;
+    const void* const* b_proj;
+    const void* const* ln2_g;
+    const void* const* ln2_b;
+    const void* const* w_fc;
+    const void* const* b_fc;
+    const void* const* w_fc2;
+    const void* const* b_fc2;
+    const void* lnf_g;
+    const void* lnf_b;
+    const void* lm_head;
+    const void* lm_bias;
+} tfm_gpt2_weights;
+
+/* As tfm_create, for the GPT-2-style family with the given options.  Errors:
+ * TFM_EINVAL for a NULL opt, an unknown position kind, an odd d_model or the
+ * tfm_create checks (rope_theta excepted). */
+tfm_status tfm_create_gpt2(const tfm_config* cfg, const tfm_gpt2_options* opt, void** handle);
+
+/* As tfm_load_weights, for a tfm_create_gpt2 handle (TFM_EINVAL otherwise, and
+ * tfm_load_weights refuses a GPT-2-style handle). */
+tfm_status tfm_load_gpt2_weights(void* handle, const tfm_gpt2_weights* w, int32_t weights_on_host);
+
 /* Forward pass of the CS336 walkthrough's TransformerLM.forward (section 5.7):
  * tokens [B, S] int32 (device) -> logits [B*S, ld_logits] fp32 (device), row
  * b*S + s holding the vocab scores of token s of sequence b in columns

@@ -46,3 +46,25 @@ def tie_aware_agreement(got, ref) -> float:
     best = ref.max(axis=-1)
     at = np.take_along_axis(ref, ag[..., None], axis=-1)[..., 0]
     return float(np.mean(at >= best - tol))
+
+
+def to_torch_gpt2_weights(w: dict, device="cuda", bf16=False):
+    """workloads.make_gpt2_weights dict -> torch tensors: matrices and the learned
+    position table bf16 or fp32, LayerNorm gains/shifts and biases fp32.  A tied
+    LM head stays the same tensor as the embedding."""
+    import torch
+
+    mat_dtype = torch.bfloat16 if bf16 else torch.float32
+    vec_keys = {"ln1_g", "ln1_b", "b_qkv", "b_proj", "ln2_g", "ln2_b", "b_fc", "b_fc2", "lnf_g",
+                "lnf_b", "lm_bias"}
+
+    def conv(key, a):
+        if a is None:
+            return None
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return t.to(torch.float32 if key in vec_keys else mat_dtype).to(device)
+
+    out = {k: conv(k, w[k]) for k in ("embed", "pos", "lnf_g", "lnf_b", "lm_bias")}
+    out["lm_head"] = out["embed"] if w["lm_head"] is w["embed"] else conv("lm_head", w["lm_head"])
+    out["layers"] = [{k: conv(k, v) for k, v in layer.items()} for layer in w["layers"]]
+    return out
