@@ -95,6 +95,108 @@ def kernel_work(cfg, B, S):
     }
 
 
+def gpt2_kernel_work(cfg, B, S):
+    """kernel_work for the GPT-2-style family: a single F-wide fc GEMM (GELU)
+    instead of gate/up, LayerNorm reading a gain and a shift, the embedding
+    gather adding the position rows."""
+    M = B * S
+    D, F, V = cfg.d_model, cfg.d_ff, cfg.vocab
+    dh = cfg.d_head
+    Dq, Dkv = cfg.n_head * dh, cfg.n_kv_head * dh
+    es = 2 if cfg.mode == "bf16" else 4
+    return {
+        "embedding_rmsnorm": ("hbm", M * 4 + 2 * M * D * es + M * D * 4 + M * D * es + 8 * D),
+        "rmsnorm": ("hbm", M * D * (4 + es) + 8 * D),
+        "qkv_rope_gemm": ("tensor", accounting.gemm_flops(M, Dq + 2 * Dkv, D)),
+        "attention": ("tensor", accounting.attention_flops(B, cfg.n_head, S, dh)),
+        "oproj_residual_gemm": ("tensor", accounting.gemm_flops(M, D, Dq)),
+        "gateup_swiglu_gemm": ("tensor", accounting.gemm_flops(M, F, D)),
+        "down_residual_gemm": ("tensor", accounting.gemm_flops(M, D, F)),
+        "lmhead_gemm": ("tensor", accounting.gemm_flops(M, V, D)),
+    }
+
+
+GPT2_KIND_NAMES = {"embedding_rmsnorm": "embedding_positions_layernorm", "rmsnorm": "layernorm",
+                   "qkv_rope_gemm": "qkv_bias_gemm", "attention": "attention",
+                   "oproj_residual_gemm": "proj_bias_residual_gemm",
+                   "gateup_swiglu_gemm": "fc_bias_gelu_gemm",
+                   "down_residual_gemm": "fc2_bias_residual_gemm", "lmhead_gemm": "lmhead_gemm"}
+
+
+def gpt2_rate(tfm, torch, stream, flush, peaks, steps=10):
+    """The GPT-2-style family on the GPT-2-small widths (vocab 50257, d_model 768,
+    12 heads, 12 layers, MLP 3072, learned positions, pre-norm, tied LM head;
+    batch 8 x seq 1024, bf16, Zipf(1.1) tokens): the recorded forward timed with
+    CUDA events per step, L2 flushed between steps; per-kind times from a
+    profiled pass of direct launches."""
+    cfg = workloads.GPT2_CONFIGS["gpt2_small"]
+    w = workloads.make_gpt2_weights(cfg, pos="learned", tied=True)
+    vec = {"ln1_g", "ln1_b", "b_qkv", "b_proj", "ln2_g", "ln2_b", "b_fc", "b_fc2", "lnf_g", "lnf_b"}
+
+    def conv(k, a):
+        return torch.from_numpy(a).to(torch.float32 if k in vec else torch.bfloat16).cuda()
+
+    tw = {k: conv(k, w[k]) for k in ("embed", "pos", "lnf_g", "lnf_b")}
+    tw["lm_head"] = tw["embed"]
+    tw["lm_bias"] = None
+    tw["layers"] = [{k: conv(k, v) for k, v in layer.items()} for layer in w["layers"]]
+    model = tfm.Gpt2Model(cfg, pos="learned")
+    model.load_weights(tw)
+    del tw
+    B, S = cfg.batch, cfg.seq
+    M = B * S
+    tok = torch.from_numpy(workloads.make_tokens(cfg)).cuda()
+    logits = torch.empty(M, (cfg.vocab + 3) // 4 * 4, device="cuda")
+    for _ in range(3):
+        model.forward_graph(tok, logits, stream)
+        flush.zero_()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record(stream)
+        model.forward_graph(tok, logits, stream)
+        b.record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    model.profile(True)
+    for _ in range(steps):
+        model.forward(tok, logits, stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    model.profile(False)
+    prof = model.profile_read()
+    tfm.device_status()
+    model.close()
+    work = gpt2_kernel_work(cfg, B, S)
+    total = sum(v[0] for v in prof.values()) or 1.0
+    kernels = {}
+    for name, (kms, n) in prof.items():
+        if n == 0:
+            continue
+        bound, units = work[name]
+        avg_s = kms / n / 1e3
+        ach = units / avg_s / (1e12 if bound == "tensor" else 1e9)
+        peak = peaks["bf16_tflops"] if bound == "tensor" else peaks["hbm_gbs"]
+        kernels[GPT2_KIND_NAMES[name]] = {
+            "bound": bound, "launches": n, "avg_us": round(avg_s * 1e6, 2),
+            "share": round(kms / total, 4), "achieved": round(ach, 1),
+            "unit": "TFLOP/s" if bound == "tensor" else "GB/s", "frac": round(ach / peak, 4)}
+    flops = sum(work[k][1] * prof[k][1] / steps for k in work
+                if work[k][0] == "tensor" and k in prof and prof[k][1])
+    return {"value": M / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "config": {"workload": "GPT-2-style family at GPT-2-small widths: vocab 50257, d_model "
+                                   "768, 12 heads (d_head 64), 12 layers, GELU MLP 3072, learned "
+                                   "positions, pre-norm LayerNorm, biased linears, tied LM head; "
+                                   "batch 8 x seq 1024, bf16, Zipf(1.1) tokens"},
+            "whole_forward_tflops": round(flops / (ms / 1e3) / 1e12, 1),
+            "kernels": kernels,
+            "how": "tfm_create_gpt2 handle, tfm_forward_graph per step, CUDA events per step, L2 "
+                   "flushed between steps; kernels from a profiled pass (events after every "
+                   "kernel, launch gaps included)"}
+
+
 def tensor_kernel_bytes(cfg, B, S):
     """Algorithmic HBM bytes (operands read once, outputs written once) of ONE
     launch of each tensor-core kernel, for its memory cap: the fp32 residual
@@ -403,6 +505,10 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-loss", action="store_true")
+    ap.add_argument("--no-gpt2", action="store_true",
+                    help="skip the GPT-2-style family measurement")
+    ap.add_argument("--gpt2-only", action="store_true",
+                    help="only the GPT-2-style family measurement; prints its JSON object alone")
     ap.add_argument("--loss-only", action="store_true",
                     help="only the fused cross-entropy measurement (--steps timed steps); prints "
                          "its JSON object alone")
@@ -510,6 +616,11 @@ def main():
     stream = torch.cuda.Stream()
     torch.cuda.set_stream(stream)
     run = model.forward if args.no_graph else model.forward_graph
+    if args.gpt2_only:
+        print(json.dumps({"gpt2_family": gpt2_rate(tfm, torch, stream, flush, load_peaks(),
+                                                   steps=args.steps)}))
+        model.close()
+        return
     if args.loss_only:
         print(json.dumps({"loss": loss_rate(tfm, torch, model, cfg, tok_np, logits, stream, flush,
                                             load_peaks(), steps=args.steps),
@@ -607,6 +718,8 @@ def main():
               if rank == 0 and cfg.mode == "bf16" and not args.no_decode else None)
     lossr = (loss_rate(tfm, torch, model, cfg, tok_np, logits, stream, flush, load_peaks())
              if rank == 0 and not args.no_loss else None)
+    g2 = (gpt2_rate(tfm, torch, stream, flush, load_peaks())
+          if rank == 0 and not args.no_gpt2 else None)
     rows = sampler.stop()
     clocks = ClockSampler.summary(rows)
     clocks["window_s"] = round(t_wall1 - t_wall0, 3)
@@ -661,6 +774,7 @@ def main():
         "rmsnorm_hbm": rms,
         "decode": decode,
         "loss": lossr,
+        "gpt2_family": g2,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": (2 + 7 * cfg.n_layer) * args.steps,

@@ -148,7 +148,9 @@ __device__ __forceinline__ int64_t qkv_offset(const EpiParams& p, const QkvSlot&
 // row `row`; u = the matching "up" columns for EPI_SWIGLU (ignored otherwise).
 // For EPI_QKV_ROPE the chunk lies inside one head (W divides dh), col0 % W == 0.
 // GELU(z) = z * Phi(z) = 0.5 z (1 + erf(z / sqrt 2)), the exact form ("Chapter 4",
-// section 4; CS336 walkthrough (fengye404.top), section 9 GELUFFN).
+// section 4; CS336 walkthrough (fengye404.top), section 9 GELUFFN).  (A
+// five-term erf polynomial, Abramowitz & Stegun 7.1.26, measured no faster in
+// the MLP's GEMM epilogue at GPT-2-small widths: 63.9 against 60.8 us.)
 __device__ __forceinline__ float gelu_exact(float z) {
     return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
 }
@@ -161,9 +163,24 @@ __device__ __forceinline__ void epi_compute(const EpiParams& p, int row, int col
 #pragma unroll
     for (int i = 0; i < W; ++i) a[i] = a_in[i];
     if (p.bias) {
+        if constexpr (W % 4 == 0) {
+            if (col0 + W <= p.N) {               // whole chunk: 16-byte loads (bias 16-byte aligned)
+                const float4* b4 = reinterpret_cast<const float4*>(p.bias + col0);
 #pragma unroll
-        for (int i = 0; i < W; ++i)
-            if (col0 + i < p.N) a[i] += __ldg(p.bias + col0 + i);
+                for (int i = 0; i < W / 4; ++i) {
+                    const float4 t = __ldg(b4 + i);
+                    a[4 * i] += t.x; a[4 * i + 1] += t.y; a[4 * i + 2] += t.z; a[4 * i + 3] += t.w;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < W; ++i)
+                    if (col0 + i < p.N) a[i] += __ldg(p.bias + col0 + i);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < W; ++i)
+                if (col0 + i < p.N) a[i] += __ldg(p.bias + col0 + i);
+        }
     }
     if (p.kind == EPI_GELU) {
 #pragma unroll
