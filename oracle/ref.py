@@ -43,6 +43,9 @@ beyond the definition.  Where the pages are silent the readings are:
    the sinusoidal table puts sin at even and cos at odd coordinates with
    angle pos / 10000^(2i/d_model); post-norm blocks are still followed by the
    final LayerNorm; the fused qkv projection's output columns are [q | k | v].
+8. Sliding window w > 0: query i sees keys j with i - w < j <= i (itself and
+   the w - 1 positions before it); w = 0, or w >= S, is full causal attention;
+   each layer has its own w (hybrid models).
 
 Pinning: every function here is checked by the non-GPU tests against values the
 pages print, closed forms, invariants and brute force (see the oracle pin tests).
@@ -138,12 +141,18 @@ def softmax(x, axis=-1):
     return e / np.sum(e, axis=axis, keepdims=True)
 
 
-def causal_mask(S):
-    """Boolean [S, S], True where key j is visible from query i (j <= i)."""
-    return np.tril(np.ones((S, S), dtype=bool))
+def causal_mask(S, window=0):
+    """Boolean [S, S], True where key j is visible from query i: j <= i, and with
+    a sliding window of w > 0 positions also j > i - w (the query and the w - 1
+    positions before it).  [LLM2] 滑动窗口和混合注意力 (each token sees a local
+    window: a band of the causal graph)."""
+    m = np.tril(np.ones((S, S), dtype=bool))
+    if window:
+        m &= ~np.tril(np.ones((S, S), dtype=bool), -window)
+    return m
 
 
-def causal_attention(q, k, v, scale=None):
+def causal_attention(q, k, v, scale=None, window=0):
     """softmax(q k^T * scale + M) v with M = -inf above the diagonal.
 
     q: [B, H, S, dh]; k, v: [B, Hkv, S, dh].  Query head h reads kv head
@@ -156,7 +165,7 @@ def causal_attention(q, k, v, scale=None):
         raise ValueError("n_head must be a multiple of n_kv_head")
     group = H // Hkv
     scale = 1.0 / np.sqrt(dh) if scale is None else scale
-    mask = causal_mask(S)
+    mask = causal_mask(S, window)
     o = np.empty_like(q)
     for h in range(H):
         g = h // group
@@ -166,7 +175,7 @@ def causal_attention(q, k, v, scale=None):
     return o
 
 
-def naive_causal_attention(q, k, v, scale=None):
+def naive_causal_attention(q, k, v, scale=None, window=0):
     """The same map as causal_attention written with explicit Python loops over
     queries and keys (brute force, for tiny shapes only)."""
     q, k, v = (np.asarray(t, dtype=F64) for t in (q, k, v))
@@ -178,12 +187,13 @@ def naive_causal_attention(q, k, v, scale=None):
         for h in range(H):
             g = h // group
             for i in range(S):
-                sc = [float(np.dot(q[b, h, i], k[b, g, j])) * scale for j in range(i + 1)]
+                j0 = max(0, i - window + 1) if window else 0
+                sc = [float(np.dot(q[b, h, i], k[b, g, j])) * scale for j in range(j0, i + 1)]
                 mx = max(sc)
                 w = [np.exp(s - mx) for s in sc]
                 tot = sum(w)
-                for j in range(i + 1):
-                    o[b, h, i] += (w[j] / tot) * v[b, g, j]
+                for j in range(j0, i + 1):
+                    o[b, h, i] += (w[j - j0] / tot) * v[b, g, j]
     return o
 
 
@@ -209,7 +219,7 @@ def _merge_heads(t):
     return t.transpose(0, 2, 1, 3).reshape(B, S, n * dh)
 
 
-def multihead_self_attention(u, layer, cfg, positions):
+def multihead_self_attention(u, layer, cfg, positions, window=0):
     """Q, K, V projections, head split (head h owns columns [h*dh, (h+1)*dh)),
     RoPE on q and k (not v), causal attention, head merge, output projection.
     [CS336-A] 5.4 多头注意力 and 5.5 (RoPE inside attention)."""
@@ -219,24 +229,26 @@ def multihead_self_attention(u, layer, cfg, positions):
     v = _split_heads(linear(u, layer["wv"]), Hkv, dh)
     q = rope(q, positions[:, None, :], cfg.rope_theta)
     k = rope(k, positions[:, None, :], cfg.rope_theta)
-    o = causal_attention(q, k, v)
+    o = causal_attention(q, k, v, window=window)
     return linear(_merge_heads(o), layer["wo"])
 
 
-def transformer_block(x, layer, cfg, positions):
+def transformer_block(x, layer, cfg, positions, window=0):
     """Pre-norm block: x = x + Attn(RMSNorm(x)); x = x + SwiGLU(RMSNorm(x)).
     [CS336-A] 5.7 (TransformerBlock.forward); [CS336-B] 10."""
     x = x + multihead_self_attention(rmsnorm(x, layer["attn_norm"], cfg.norm_eps),
-                                     layer, cfg, positions)
+                                     layer, cfg, positions, window)
     u = rmsnorm(x, layer["ffn_norm"], cfg.norm_eps)
     return x + swiglu(u, layer["w1"], layer["w3"], layer["w2"])
 
 
-def forward(tokens, weights, cfg, rows=None):
+def forward(tokens, weights, cfg, rows=None, windows=None):
     """logits[b, s, :] of the TransformerLM: embedding -> n_layer blocks ->
     final RMSNorm -> LM head (untied unless the caller passes the same matrix).
     Positions are 0..S-1 per sequence.  ``rows`` selects batch rows to compute
     (sequences are independent); each is computed on its own to bound memory.
+    ``windows`` gives each layer's sliding window (0: full causal attention; a
+    hybrid model mixes both, [LLM2] 滑动窗口和混合注意力).
     [CS336-A] 5.7 (TransformerLM.forward); [CS336-B] 10."""
     tokens = np.asarray(tokens)
     B, S = tokens.shape
@@ -246,8 +258,8 @@ def forward(tokens, weights, cfg, rows=None):
         tok = tokens[b:b + 1]
         positions = np.arange(S, dtype=F64)[None, :]
         x = embedding(weights["embed"], tok)
-        for layer in weights["layers"][: cfg.n_layer]:
-            x = transformer_block(x, layer, cfg, positions)
+        for li, layer in enumerate(weights["layers"][: cfg.n_layer]):
+            x = transformer_block(x, layer, cfg, positions, windows[li] if windows else 0)
         x = rmsnorm(x, weights["final_norm"], cfg.norm_eps)
         out.append(linear(x, weights["lm_head"])[0])
     return np.stack(out)

@@ -481,3 +481,51 @@ def test_gpt2_model_causal_tied_and_position_tables():
     x = w["embed"][t[0]].astype(np.float64) + w["pos"][:12]
     ref = oracle.layernorm(x, w["lnf_g"], w["lnf_b"], cfg.norm_eps) @ w["embed"].astype(np.float64).T
     assert np.allclose(oracle.gpt2_forward(t, w, c0)[0], ref + w["lm_bias"], rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- sliding window
+def _qkv(seed, B=1, H=4, Hkv=2, S=13, dh=8):
+    r = np.random.default_rng(seed)
+    return (r.standard_normal((B, H, S, dh)), r.standard_normal((B, Hkv, S, dh)),
+            r.standard_normal((B, Hkv, S, dh)))
+
+
+def test_window_mask_band_and_limits():
+    m = oracle.causal_mask(6, 2)
+    assert [list(np.nonzero(row)[0]) for row in m] == [[0], [0, 1], [1, 2], [2, 3], [3, 4], [4, 5]]
+    assert np.array_equal(oracle.causal_mask(6, 6), oracle.causal_mask(6))
+    assert np.array_equal(oracle.causal_mask(6, 100), oracle.causal_mask(6))
+
+
+def test_window_one_returns_v_and_large_window_is_causal():
+    q, k, v = _qkv(31)
+    o1 = oracle.causal_attention(q, k, v, window=1)
+    assert np.allclose(o1, np.repeat(v, 2, axis=1), rtol=0, atol=1e-14)   # softmax over one key
+    assert np.allclose(oracle.causal_attention(q, k, v, window=13), oracle.causal_attention(q, k, v),
+                       rtol=0, atol=1e-14)
+
+
+def test_window_matches_brute_force_and_ignores_far_keys():
+    q, k, v = _qkv(32)
+    for w in (2, 3, 5):
+        a = oracle.causal_attention(q, k, v, window=w)
+        assert np.allclose(a, oracle.naive_causal_attention(q, k, v, window=w), rtol=0, atol=1e-12)
+        # keys at or before i - w cannot change row i
+        k2, v2 = k.copy(), v.copy()
+        k2[:, :, 0] += 5.0
+        v2[:, :, 0] -= 3.0
+        b = oracle.causal_attention(q, k2, v2, window=w)
+        assert np.array_equal(a[:, :, w:], b[:, :, w:]) and not np.allclose(a[:, :, 0], b[:, :, 0])
+
+
+def test_model_windows_per_layer():
+    cfg = workloads.get_config("tiny").replace(n_layer=2)
+    w = workloads.make_weights(cfg, gains="random")
+    t = workloads.make_tokens(cfg, batch=1, seq=20, seed=4)
+    full = oracle.forward(t, w, cfg)
+    assert np.array_equal(oracle.forward(t, w, cfg, windows=[0, 0]), full)
+    assert np.allclose(oracle.forward(t, w, cfg, windows=[20, 64]), full, rtol=0, atol=1e-12)
+    hyb = oracle.forward(t, w, cfg, windows=[4, 0])
+    # the first 4 positions see their whole prefix in both layers
+    assert np.allclose(hyb[0, :4], full[0, :4], rtol=0, atol=1e-12)
+    assert not np.allclose(hyb[0, 4:], full[0, 4:])
