@@ -214,6 +214,8 @@ struct Model {
     std::vector<float*> ln1_b, ln2_b, b_qkv, b_proj, b_fc, b_fc2;
     float* lnf_b = nullptr;
     float* lm_bias = nullptr;
+    // sliding window of each layer's attention (tfm_set_attention_windows; 0: full)
+    std::vector<int> windows;
     // cached tensor-core plans for the current token count
     int64_t plan_m = -1;
     std::vector<GemmPlan> p_qkv, p_o, p_gu, p_down;
@@ -719,6 +721,14 @@ enum Kind { K_EMBED = 0, K_NORM, K_QKV, K_ATTN, K_OPROJ, K_GATEUP, K_DOWN, K_LMH
         }                                                                       \
     } while (0)
 
+// Sliding window of layer l for sequences of length S: 0 when the layer attends
+// to the whole prefix (no window, or a window of at least S positions).
+int layer_window(const Model* m, int l, int S) {
+    if (m->windows.empty()) return 0;
+    const int w = m->windows[l];
+    return (w > 0 && w < S) ? w : 0;
+}
+
 // Targets and outputs of tfm_forward_loss.
 struct LossArgs {
     const int32_t* targets;
@@ -877,11 +887,15 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
                                           cudaMemcpyDeviceToDevice, st);
                 if (e != cudaSuccess) return cuda_fail(e, "k, v into the cache");
             }
-            if (m->attn_tc)
+            // a sliding-window layer (window < S) runs the flash kernel with the
+            // band's tile skip; full layers the persistent tensor-core kernels
+            const int win = layer_window(m, l, S);
+            if (m->attn_tc && win == 0)
                 TFM_LAUNCH(K_ATTN, launch_attention_tc(m->p_attn, st));
             else
                 TFM_LAUNCH(K_ATTN, launch_attention_bf16(m->q(), m->k(), m->v(), m->o(), B,
-                                                         c.n_head, c.n_kv_head, S, dh, scale, st));
+                                                         c.n_head, c.n_kv_head, S, dh, scale, st,
+                                                         win));
             TFM_LAUNCH(K_OPROJ, launch_gemm_tc(m->p_o[l], st));
             TFM_LAUNCH(K_NORM, norm_mid(l));
             TFM_LAUNCH(K_GATEUP, launch_gemm_tc(m->p_gu[l], st));
@@ -912,7 +926,8 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
                                                      static_cast<const float*>(m->k()),
                                                      static_cast<const float*>(m->v()),
                                                      static_cast<float*>(m->o()), B, c.n_head,
-                                                     c.n_kv_head, S, dh, scale, st));
+                                                     c.n_kv_head, S, dh, scale, st,
+                                                     layer_window(m, l, S)));
             EpiParams eo = epi_basic(EPI_ACCUM_F32, M, c.d_model, m->h(), s.D);
             if (g2) eo.bias = m->b_proj[l];
             TFM_LAUNCH(K_OPROJ, launch_gemm_simt(static_cast<const float*>(m->o()),
@@ -1035,7 +1050,8 @@ tfm_status decode_body(Model* m, const int32_t* tokens, int B, float* logits, in
         TFM_LAUNCH(K_QKV, launch_gemm_tc(m->d_qkv[l], st));
         TFM_LAUNCH(K_ATTN, launch_decode_attention(m->q(), m->kcache(l), m->vcache(l), m->dec_part,
                                                    m->o(), B, c.n_head, c.n_kv_head, c.max_seq,
-                                                   m->pos_dev, dh, scale, st));
+                                                   m->pos_dev, dh, scale, st,
+                                                   m->windows.empty() ? 0 : m->windows[l]));
         TFM_LAUNCH(K_OPROJ, launch_gemm_tc(m->d_o[l], st));
         TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->ffn_norm[l], m->xn(), B, c.d_model, c.norm_eps, 1, st, 1));
         TFM_LAUNCH(K_GATEUP, launch_gemm_tc(m->d_gu[l], st));
@@ -1136,6 +1152,29 @@ tfm_status tfm_forward_loss(void* handle, const int32_t* tokens, const int32_t* 
     const tfm::LossArgs la{targets, loss, lse, mean_loss};
     return tfm::forward_impl(m, tokens, B, S, nullptr, 0, static_cast<cudaStream_t>(stream), false,
                              &la);
+}
+
+tfm_status tfm_set_attention_windows(void* handle, const int32_t* windows, int32_t n) {
+    Model* m = static_cast<Model*>(handle);
+    if (!m) return fail(TFM_EINVAL, "NULL handle");
+    if (n != 0 && n != m->cfg.n_layer) return fail(TFM_EINVAL, "n must be 0 or n_layer (%d)", m->cfg.n_layer);
+    if (n > 0 && !windows) return fail(TFM_EINVAL, "NULL windows");
+    for (int l = 0; l < n; ++l)
+        if (windows[l] < 0) return fail(TFM_EINVAL, "window of layer %d is negative", l);
+    // recorded forwards and decode steps hold the previous windows
+    for (auto& g : m->graphs)
+        if (g.exec) {
+            cudaGraphExecDestroy(g.exec);
+            g = Model::Graph{};
+        }
+    for (auto& g : m->dgraphs)
+        if (g.exec) {
+            cudaGraphExecDestroy(g.exec);
+            g = Model::Graph{};
+        }
+    m->dlast = Model::Graph{};
+    m->windows.assign(windows, windows + n);
+    return TFM_OK;
 }
 
 }  // extern "C"
@@ -1437,7 +1476,15 @@ tfm_status tfm_rope(void* x, const int32_t* positions, int32_t B, int32_t H, int
 tfm_status tfm_causal_attention(const void* q, const void* k, const void* v, void* o, int32_t B,
                                 int32_t H, int32_t Hkv, int32_t S, int32_t dh, float scale,
                                 int32_t mode, void* stream) {
+    return tfm_causal_attention_window(q, k, v, o, B, H, Hkv, S, dh, scale, 0, mode, stream);
+}
+
+tfm_status tfm_causal_attention_window(const void* q, const void* k, const void* v, void* o,
+                                       int32_t B, int32_t H, int32_t Hkv, int32_t S, int32_t dh,
+                                       float scale, int32_t window, int32_t mode, void* stream) {
     if (!q || !k || !v || !o) return fail(TFM_EINVAL, "NULL pointer");
+    if (window < 0) return fail(TFM_EINVAL, "window must be >= 0");
+    if (window >= S) window = 0;
     if (B < 0 || S < 0 || H < 1 || Hkv < 1 || H % Hkv) return fail(TFM_EINVAL, "bad head counts");
     if (!tfm::aligned16(q) || !tfm::aligned16(k) || !tfm::aligned16(v) || !tfm::aligned16(o))
         return fail(TFM_EINVAL, "q, k, v, o must be 16-byte aligned");
@@ -1446,19 +1493,19 @@ tfm_status tfm_causal_attention(const void* q, const void* k, const void* v, voi
     cudaError_t e;
     if (mode == TFM_BF16) {
         if (dh != 32 && dh != 64 && dh != 128) return fail(TFM_EUNSUPPORTED, "bf16 attention: dh in {32,64,128}");
-        if (tfm::attention_tc_supported(dh)) {
+        if (window == 0 && tfm::attention_tc_supported(dh)) {
             tfm::AttnPlan plan;
             tfm_status ps = tfm::plan_attention_tc(&plan, q, k, v, o, B, H, Hkv, S, dh, scale);
             if (ps != TFM_OK) return fail(ps, "could not encode attention tensor maps");
             e = tfm::launch_attention_tc(plan, cs);
         } else {
-            e = tfm::launch_attention_bf16(q, k, v, o, B, H, Hkv, S, dh, scale, cs);
+            e = tfm::launch_attention_bf16(q, k, v, o, B, H, Hkv, S, dh, scale, cs, window);
         }
     } else if (mode == TFM_FP32) {
         if (dh < 1 || dh > 128) return fail(TFM_EUNSUPPORTED, "fp32 attention: dh <= 128");
         e = tfm::launch_attention_simt(static_cast<const float*>(q), static_cast<const float*>(k),
                                        static_cast<const float*>(v), static_cast<float*>(o), B, H,
-                                       Hkv, S, dh, scale, cs);
+                                       Hkv, S, dh, scale, cs, window);
     } else {
         return fail(TFM_EINVAL, "bad mode");
     }

@@ -148,7 +148,7 @@ cudaError_t launch_gemm_simt(const float* A, const float* B, const float* B2, in
                              int K, const EpiParams& epi, cudaStream_t st);
 cudaError_t launch_attention_simt(const float* q, const float* k, const float* v, float* o,
                                   int B, int H, int Hkv, int S, int dh, float scale,
-                                  cudaStream_t st);
+                                  cudaStream_t st, int window = 0);
 
 // ---- tensor-core GEMM (k_gemm_tc.cu), bf16 mode
 // Tensor maps of one GEMM: A [M,K] and B [N,K] bf16 row-major (B2 = W3 for SwiGLU).
@@ -188,8 +188,10 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t st);
 cudaError_t launch_gemm_skinny(const GemmPlan& plan, cudaStream_t st);
 
 // ---- bf16 flash attention on mma.sync (k_attention.cu), any dh in {32, 64, 128}
+// window > 0: sliding window, query i sees keys i-window < j <= i (>= S: causal).
 cudaError_t launch_attention_bf16(const void* q, const void* k, const void* v, void* o, int B,
-                                  int H, int Hkv, int S, int dh, float scale, cudaStream_t st);
+                                  int H, int Hkv, int S, int dh, float scale, cudaStream_t st,
+                                  int window = 0);
 
 // ---- attention of one new query per sequence over a KV cache (k_decode.cu):
 // q [B, H, dh], caches [B, Hkv, max_seq, dh] (positions [0, L) read), o [B, H*dh]
@@ -198,9 +200,11 @@ cudaError_t launch_attention_bf16(const void* q, const void* k, const void* v, v
 // replayed from a recorded graph at every position); the grid covers max_seq.
 size_t decode_partial_floats(int B, int H, int max_seq, int dh);
 bool decode_supported(int dh, int group);
+// window > 0: only keys [pos - window + 1, pos] (a sliding-window layer).
 cudaError_t launch_decode_attention(const void* q, const void* kc, const void* vc, float* part,
                                     void* o, int B, int H, int Hkv, int max_seq,
-                                    const int* pos_dev, int dh, float scale, cudaStream_t st);
+                                    const int* pos_dev, int dh, float scale, cudaStream_t st,
+                                    int window = 0);
 // Stores the decode step's position and copies its B tokens into device words.
 cudaError_t launch_decode_setup(int* pos_dev, int pos, const int32_t* tok, int32_t* tok_dev, int B,
                                 cudaStream_t st);

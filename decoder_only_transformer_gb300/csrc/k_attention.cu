@@ -5,7 +5,11 @@
 // reading kv head h / (H / Hkv) ("LLM 2", section GQA / MQA).  The softmax is
 // evaluated online over key tiles (running row max and sum, rescaling the
 // partial output when the max grows), so the S x S score matrix is never
-// stored and key tiles entirely above the diagonal are never loaded.
+// stored and key tiles entirely above the diagonal are never loaded.  With a
+// sliding window w > 0 ("LLM 2", section 滑动窗口和混合注意力: each token sees a
+// local band of the causal graph) query i sees keys i-w < j <= i: key tiles
+// entirely before the window of the tile's first query are skipped too, and
+// the tiles the window edge crosses are masked below it as well.
 //
 // One CTA = 64 query rows of one (sequence, head); 4 warps x 16 rows.  Key and
 // value tiles of 64 rows are double-buffered in shared memory with cp.async
@@ -13,6 +17,8 @@
 // with mma.sync m16n8k16 (bf16 in, fp32 accumulate); the score fragments are
 // reused in registers as the A operand of P.V.  Heavy (late) query tiles of
 // every head are scheduled before any light one.
+#include <climits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -67,7 +73,8 @@ __global__ void __launch_bounds__(128) k_attention_mma(const __nv_bfloat16* __re
                                                        const __nv_bfloat16* __restrict__ k,
                                                        const __nv_bfloat16* __restrict__ v,
                                                        __nv_bfloat16* __restrict__ o, int H,
-                                                       int Hkv, int S, float scale_log2) {
+                                                       int Hkv, int S, float scale_log2,
+                                                       int window) {
     using L = AttSmem<DH>;
     constexpr int LD = L::kLd;
     extern __shared__ __align__(16) __nv_bfloat16 att_smem[];
@@ -98,10 +105,15 @@ __global__ void __launch_bounds__(128) k_attention_mma(const __nv_bfloat16* __re
         }
     };
 
-    load_tile(Qs, qg, qt * kAttBM);
+    // First key tile: the one holding the window start of the tile's first query.
+    const int q0 = qt * kAttBM;
+    const int jbeg = (window > 0 && q0 - window + 1 > 0) ? (q0 - window + 1) / kAttBN : 0;
+    // Tiles below this key index can hold keys before some row's window start.
+    const int win_lo = window > 0 ? q0 + kAttBM - window : INT_MIN;
+    load_tile(Qs, qg, q0);
     cp_async_commit();
-    load_tile(Ks, kg, 0);
-    load_tile(Vs, vg, 0);
+    load_tile(Ks + (jbeg & 1) * L::kTile, kg, jbeg * kAttBN);
+    load_tile(Vs + (jbeg & 1) * L::kTile, vg, jbeg * kAttBN);
     cp_async_commit();
     cp_async_wait<1>();
     __syncthreads();
@@ -120,7 +132,7 @@ __global__ void __launch_bounds__(128) k_attention_mma(const __nv_bfloat16* __re
     const int row_lo = qt * kAttBM + warp * 16 + (lane >> 2);
     const int row_hi = row_lo + 8;
 
-    for (int j = 0; j <= qt; ++j) {
+    for (int j = jbeg; j <= qt; ++j) {
         const int buf = j & 1;
         if (j + 1 <= qt) {
             load_tile(Ks + (buf ^ 1) * L::kTile, kg, (j + 1) * kAttBN);
@@ -162,6 +174,19 @@ __global__ void __launch_bounds__(128) k_attention_mma(const __nv_bfloat16* __re
                     const int key = key0 + nb * 8 + e;
                     if (key > row_lo || key >= S) s[nb][e] = -INFINITY;
                     if (key > row_hi || key >= S) s[nb][2 + e] = -INFINITY;
+                }
+        }
+        // Keys before a row's window (a row left with none in this tile keeps
+        // the -inf max, handled below as for the causal mask).
+        if (j * kAttBN < win_lo) {
+            const int key0 = j * kAttBN + 2 * (lane & 3);
+#pragma unroll
+            for (int nb = 0; nb < 8; ++nb)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int key = key0 + nb * 8 + e;
+                    if (key <= row_lo - window) s[nb][e] = -INFINITY;
+                    if (key <= row_hi - window) s[nb][2 + e] = -INFINITY;
                 }
         }
         // Row max of the raw scores (the scale is positive, so it commutes with
@@ -244,7 +269,7 @@ __global__ void __launch_bounds__(128) k_attention_mma(const __nv_bfloat16* __re
 
 template <int DH>
 cudaError_t launch_dh(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv,
-                      int S, float scale, cudaStream_t st) {
+                      int S, float scale, int window, cudaStream_t st) {
     using L = AttSmem<DH>;
     static bool attr_set = false;
     if (!attr_set) {
@@ -257,18 +282,20 @@ cudaError_t launch_dh(const void* q, const void* k, const void* v, void* o, int 
     return launch_pdl(k_attention_mma<DH>, grid, dim3(128), L::kBytes, st,
                       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
                       static_cast<const __nv_bfloat16*>(v), static_cast<__nv_bfloat16*>(o), H, Hkv,
-                      S, scale * 1.4426950408889634f);
+                      S, scale * 1.4426950408889634f, window);
 }
 
 }  // namespace
 
 cudaError_t launch_attention_bf16(const void* q, const void* k, const void* v, void* o, int B,
-                                  int H, int Hkv, int S, int dh, float scale, cudaStream_t st) {
+                                  int H, int Hkv, int S, int dh, float scale, cudaStream_t st,
+                                  int window) {
     if (B <= 0 || S <= 0) return cudaSuccess;
+    if (window >= S) window = 0;                        // the whole prefix: plain causal
     switch (dh) {
-        case 32: return launch_dh<32>(q, k, v, o, B, H, Hkv, S, scale, st);
-        case 64: return launch_dh<64>(q, k, v, o, B, H, Hkv, S, scale, st);
-        case 128: return launch_dh<128>(q, k, v, o, B, H, Hkv, S, scale, st);
+        case 32: return launch_dh<32>(q, k, v, o, B, H, Hkv, S, scale, window, st);
+        case 64: return launch_dh<64>(q, k, v, o, B, H, Hkv, S, scale, window, st);
+        case 128: return launch_dh<128>(q, k, v, o, B, H, Hkv, S, scale, window, st);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kDecThreads) k_decode_partial(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
     const __nv_bfloat16* __restrict__ vc, float* __restrict__ part, __nv_bfloat16* __restrict__ o,
     int H, int Hkv, int max_seq, const int* __restrict__ pos_dev, int nch, float scale_log2,
-    int* err) {
+    int window, int* err) {
     using Sm = DecSmem<DH, G>;
     constexpr int NK = Sm::kKeys, NW = kDecNW;
     constexpr int CPR = DH / 8;                      // lanes per key row, 16 bytes each
@@ -77,7 +77,9 @@ __global__ void __launch_bounds__(kDecThreads) k_decode_partial(
     // prefill), all complete before the launch before this one could start.
     const int pos = __ldg(pos_dev);
     const int k0 = c * NK;
-    if (k0 > pos) return;                            // chunk past the attended keys [0, pos]
+    // attended keys [ws, pos]: ws = 0, or the sliding window's first key
+    const int ws = (window > 0 && pos - window + 1 > 0) ? pos - window + 1 : 0;
+    if (k0 > pos || k0 + NK <= ws) return;           // chunk outside the attended keys
     const int n = min(NK, pos + 1 - k0);             // keys of this chunk
     const int nprev = min(NK, pos - k0);             // of them, those cached before this step
     const int b = bg / Hkv, g = bg - b * Hkv;
@@ -143,7 +145,8 @@ __global__ void __launch_bounds__(kDecThreads) k_decode_partial(
         if (cl == 0) {
 #pragma unroll
             for (int hh = 0; hh < G; ++hh) {
-                const float sc = row < n ? d[hh] * scale_log2 : -INFINITY;   // rows >= n unused
+                // rows >= n unused; rows before the window start masked
+                const float sc = (row < n && k0 + row >= ws) ? d[hh] * scale_log2 : -INFINITY;
                 ps[hh * NK + row] = sc;
                 mloc[hh] = fmaxf(mloc[hh], sc);
             }
@@ -219,9 +222,9 @@ __global__ void __launch_bounds__(kDecThreads) k_decode_partial(
         }
     }
     __syncthreads();
-    if (pos < NK) {
-        // All keys in this one chunk: the normalised output directly (the
-        // combining launch sees a single chunk and does nothing).
+    if (ws / NK == pos / NK) {
+        // All attended keys in this one chunk: the normalised output directly
+        // (the combining launch sees a single chunk and does nothing).
         for (int i = tid; i < G * DH; i += kDecThreads) {
             const int hh = i / DH, d = i - hh * DH;
             float v = 0.f, l = 0.f;
@@ -260,30 +263,34 @@ template <int DH>
 __global__ void __launch_bounds__(128) k_decode_combine(const float* __restrict__ part,
                                                        __nv_bfloat16* __restrict__ o, int BH,
                                                        int H, int nch_stride,
-                                                       const int* __restrict__ pos_dev) {
+                                                       const int* __restrict__ pos_dev,
+                                                       int window) {
     pdl_wait();
     pdl_trigger();
     const int w = (int)(blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5));
     const int lane = threadIdx.x & 31;
     if (w >= BH) return;
     constexpr int NK = dec_keys(DH);
-    const int nch = (__ldg(pos_dev) + NK) / NK;      // chunks holding keys [0, pos]
-    if (nch == 1) return;                            // written by the chunk kernel itself
+    const int pos = __ldg(pos_dev);
+    const int nch = (pos + NK) / NK;                 // chunks holding keys [0, pos]
+    const int ws = (window > 0 && pos - window + 1 > 0) ? pos - window + 1 : 0;
+    const int c0 = ws / NK;                          // the first chunk in the window
+    if (nch - c0 == 1) return;                       // written by the chunk kernel itself
     const float* p = part + (int64_t)w * nch_stride * (DH + 2);
     // chunk statistics with one chunk per lane, so their loads go out together
     float M = -INFINITY;
-    for (int c = lane; c < nch; c += 32) M = fmaxf(M, p[c * (DH + 2) + DH]);
+    for (int c = c0 + lane; c < nch; c += 32) M = fmaxf(M, p[c * (DH + 2) + DH]);
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
     float l = 0.f;
-    for (int c = lane; c < nch; c += 32) l += exp2f(p[c * (DH + 2) + DH] - M) * p[c * (DH + 2) + DH + 1];
+    for (int c = c0 + lane; c < nch; c += 32) l += exp2f(p[c * (DH + 2) + DH] - M) * p[c * (DH + 2) + DH + 1];
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) l += __shfl_xor_sync(0xffffffffu, l, s);
     float acc[DH / 32];
 #pragma unroll
     for (int i = 0; i < DH / 32; ++i) acc[i] = 0.f;
 #pragma unroll 4
-    for (int c = 0; c < nch; ++c) {
+    for (int c = c0; c < nch; ++c) {
         const float* pc = p + c * (DH + 2);
         const float wgt = exp2f(pc[DH] - M);
 #pragma unroll
@@ -299,7 +306,7 @@ __global__ void __launch_bounds__(128) k_decode_combine(const float* __restrict_
 template <int DH, int G>
 cudaError_t decode_launch(const void* q, const void* kc, const void* vc, float* part, void* o,
                           int B, int H, int Hkv, int max_seq, const int* pos_dev, float scale,
-                          cudaStream_t st) {
+                          int window, cudaStream_t st) {
     // chunks for the longest possible cache; those past the length return at once
     using Sm = DecSmem<DH, G>;
     static bool attr_set = false;   // per instantiation; set once per process
@@ -315,12 +322,13 @@ cudaError_t decode_launch(const void* q, const void* kc, const void* vc, float* 
                                static_cast<const __nv_bfloat16*>(kc),
                                static_cast<const __nv_bfloat16*>(vc), part,
                                static_cast<__nv_bfloat16*>(o), H, Hkv, max_seq,
-                               pos_dev, nch, scale * 1.4426950408889634f, device_error_word());
+                               pos_dev, nch, scale * 1.4426950408889634f, window,
+                               device_error_word());
     if (e != cudaSuccess) return e;
     const int BH = B * H;
     return launch_pdl(k_decode_combine<DH>, dim3((unsigned)((BH + 3) / 4)), dim3(128), 0, st,
                       static_cast<const float*>(part), static_cast<__nv_bfloat16*>(o), BH, H, nch,
-                      pos_dev);
+                      pos_dev, window);
 }
 
 // Start of a decode step: the step's position and its B tokens go to device
@@ -334,16 +342,17 @@ __global__ void k_decode_setup(int* pos_dev, int pos, const int32_t* tok, int32_
 
 template <int DH>
 cudaError_t decode_dh(const void* q, const void* kc, const void* vc, float* part, void* o, int B,
-                      int H, int Hkv, int max_seq, const int* L, float scale, cudaStream_t st) {
+                      int H, int Hkv, int max_seq, const int* L, float scale, int window,
+                      cudaStream_t st) {
     switch (H / Hkv) {
-        case 1: return decode_launch<DH, 1>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, st);
-        case 2: return decode_launch<DH, 2>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, st);
-        case 4: return decode_launch<DH, 4>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, st);
-        case 8: return decode_launch<DH, 8>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, st);
+        case 1: return decode_launch<DH, 1>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, window, st);
+        case 2: return decode_launch<DH, 2>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, window, st);
+        case 4: return decode_launch<DH, 4>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, window, st);
+        case 8: return decode_launch<DH, 8>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, window, st);
         case 16:
             // 16 heads of 128 columns would need 57.6 KB of static shared memory
             if constexpr (DH <= 64)
-                return decode_launch<DH, 16>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, st);
+                return decode_launch<DH, 16>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, window, st);
             return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
@@ -363,12 +372,13 @@ bool decode_supported(int dh, int group) {
 
 cudaError_t launch_decode_attention(const void* q, const void* kc, const void* vc, float* part,
                                     void* o, int B, int H, int Hkv, int max_seq,
-                                    const int* L, int dh, float scale, cudaStream_t st) {
+                                    const int* L, int dh, float scale, cudaStream_t st,
+                                    int window) {
     if (B <= 0) return cudaSuccess;
     switch (dh) {
-        case 32: return decode_dh<32>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, st);
-        case 64: return decode_dh<64>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, st);
-        case 128: return decode_dh<128>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, st);
+        case 32: return decode_dh<32>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, window, st);
+        case 64: return decode_dh<64>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, window, st);
+        case 128: return decode_dh<128>(q, kc, vc, part, o, B, H, Hkv, max_seq, L, scale, window, st);
         default: return cudaErrorInvalidValue;
     }
 }

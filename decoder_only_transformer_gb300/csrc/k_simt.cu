@@ -74,12 +74,15 @@ cudaError_t launch_gemm_simt(const float* A, const float* B, const float* B2, in
 // Lane l holds coordinates l, l+32, ... of the query and of its output; keys
 // 0..i are visited in order with a running max and sum (the stable softmax of
 // the CS336 walkthrough section 5.4, evaluated online), so the masked keys
-// j > i are never read.  o is written with heads merged: o[b, i, h*dh + d].
+// j > i are never read; with a sliding window w > 0 only keys i-w < j <= i
+// ("LLM 2", section 滑动窗口和混合注意力).  o is written with heads merged:
+// o[b, i, h*dh + d].
 __global__ void __launch_bounds__(256) k_attention_simt(const float* __restrict__ q,
                                                         const float* __restrict__ k,
                                                         const float* __restrict__ v,
                                                         float* __restrict__ o, int B, int H,
-                                                        int Hkv, int S, int dh, float scale) {
+                                                        int Hkv, int S, int dh, float scale,
+                                                        int window) {
     const int lane = threadIdx.x & 31;
     const int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (w >= (int64_t)B * H * S) return;
@@ -99,7 +102,8 @@ __global__ void __launch_bounds__(256) k_attention_simt(const float* __restrict_
         acc[t] = 0.f;
     }
     float mx = -INFINITY, sum = 0.f;
-    for (int j = 0; j <= i; ++j) {
+    const int j0 = (window > 0 && i - window + 1 > 0) ? i - window + 1 : 0;
+    for (int j = j0; j <= i; ++j) {
         float part = 0.f;
 #pragma unroll
         for (int t = 0; t < kMaxT; ++t) {
@@ -130,11 +134,12 @@ __global__ void __launch_bounds__(256) k_attention_simt(const float* __restrict_
 }
 
 cudaError_t launch_attention_simt(const float* q, const float* k, const float* v, float* o, int B,
-                                  int H, int Hkv, int S, int dh, float scale, cudaStream_t st) {
+                                  int H, int Hkv, int S, int dh, float scale, cudaStream_t st,
+                                  int window) {
     const int64_t warps = (int64_t)B * H * S;
     if (warps <= 0) return cudaSuccess;
     const int64_t blocks = (warps + 7) / 8;
-    k_attention_simt<<<(unsigned)blocks, 256, 0, st>>>(q, k, v, o, B, H, Hkv, S, dh, scale);
+    k_attention_simt<<<(unsigned)blocks, 256, 0, st>>>(q, k, v, o, B, H, Hkv, S, dh, scale, window);
     return cudaGetLastError();
 }
 

@@ -92,6 +92,9 @@ _SIGS = {
     "tfm_rmsnorm": ([_V, _V, _V, _I64, _I32, _F, _I32, _V], _I32),
     "tfm_rope": ([_V, _V, _I32, _I32, _I32, _I32, _F, _I32, _V], _I32),
     "tfm_causal_attention": ([_V, _V, _V, _V, _I32, _I32, _I32, _I32, _I32, _F, _I32, _V], _I32),
+    "tfm_causal_attention_window": ([_V, _V, _V, _V, _I32, _I32, _I32, _I32, _I32, _F, _I32, _I32,
+                                     _V], _I32),
+    "tfm_set_attention_windows": ([_V, ctypes.POINTER(ctypes.c_int32), _I32], _I32),
     "tfm_linear": ([_V, _V, _V, _I64, _I32, _I32, _I64, _I32, _I32, _I32, _V], _I32),
     "tfm_swiglu": ([_V, _V, _V, _V, _V, _I64, _I32, _I32, _I32, _V, _SZ, _I32, _V], _I32),
     "tfm_swiglu_workspace_bytes": ([_I64, _I32, _I32], _SZ),
@@ -280,6 +283,12 @@ class Model:
                                          _ptr(mean) if mean is not None else None,
                                          _stream(stream)))
 
+    def set_attention_windows(self, windows=None):
+        """Per-layer sliding windows (0: full causal attention); None: all full."""
+        n = 0 if not windows else len(windows)
+        arr = (ctypes.c_int32 * max(n, 1))(*(windows or [0]))
+        _check(self.lib.tfm_set_attention_windows(self.handle, arr, n))
+
     def decode_step(self, tokens, pos, logits, stream=None):
         """tokens: int32 [B] (device), the new token of every sequence at position
         pos (the cached length); logits: fp32 [B, ld] (device)."""
@@ -322,6 +331,15 @@ def causal_attention(q, k, v, o, scale=0.0, stream=None):
     Hkv = k.shape[1]
     _check(load().tfm_causal_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Hkv, S, dh,
                                        scale, _mode_of(q), _stream(stream)))
+
+
+def causal_attention_window(q, k, v, o, window, scale=0.0, stream=None):
+    """causal_attention where query i sees keys i-window < j <= i (0: all)."""
+    B, H, S, dh = q.shape
+    Hkv = k.shape[1]
+    _check(load().tfm_causal_attention_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Hkv, S,
+                                              dh, scale, int(window), _mode_of(q),
+                                              _stream(stream)))
 
 
 def linear(x, W, y, accumulate=False, stream=None):

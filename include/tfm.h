@@ -229,6 +229,18 @@ tfm_status tfm_forward(void* handle, const int32_t* tokens, int32_t B, int32_t S
 tfm_status tfm_forward_loss(void* handle, const int32_t* tokens, const int32_t* targets, int32_t B,
                             int32_t S, float* loss, float* lse, float* mean_loss, void* stream);
 
+/* Sliding-window attention per layer (hybrid models: "LLM 2", section
+ * 滑动窗口和混合注意力 — most layers local, a few full): windows[l] >= 0 is layer
+ * l's window (query i sees keys i - w < j <= i; 0 = full causal attention), n
+ * = n_layer, or n = 0 to make every layer full again.  Applies to every later
+ * forward, loss and decode call of the handle (a decode step then reads only
+ * the window's positions of the cache); recorded forwards and decode steps are
+ * dropped and recorded again.  Windowed layers run the flash kernel with the
+ * band's tile skip (the persistent tensor-core kernels serve full layers).
+ * Host only, not stream-ordered: call it between forwards.  TFM_EINVAL for
+ * n not in {0, n_layer} or a negative window. */
+tfm_status tfm_set_attention_windows(void* handle, const int32_t* windows, int32_t n);
+
 /* tfm_forward replayed from a CUDA graph.  The first call for a given
  * (tokens, B, S, logits, ld_logits, stream) records the launch sequence into a
  * graph (nothing executes while recording), instantiates it and launches it;
@@ -364,6 +376,16 @@ tfm_status tfm_rope(void* x, const int32_t* positions, int32_t B, int32_t H, int
 tfm_status tfm_causal_attention(const void* q, const void* k, const void* v, void* o,
                                 int32_t B, int32_t H, int32_t Hkv, int32_t S, int32_t dh,
                                 float scale, int32_t mode, void* stream);
+
+/* tfm_causal_attention with a sliding window ("LLM 2", section
+ * 滑动窗口和混合注意力: each token sees a local band of the causal graph):
+ * query i attends to keys j with i - window < j <= i (itself and the
+ * window - 1 positions before it); window = 0, or window >= S, is plain causal
+ * attention.  Key tiles entirely before a query tile's window are never loaded.
+ * TFM_EINVAL for window < 0; otherwise as tfm_causal_attention. */
+tfm_status tfm_causal_attention_window(const void* q, const void* k, const void* v, void* o,
+                                       int32_t B, int32_t H, int32_t Hkv, int32_t S, int32_t dh,
+                                       float scale, int32_t window, int32_t mode, void* stream);
 
 /* Bias-free Linear (CS336 walkthrough, section 5.3): y = x W^T.
  * x [M, K], W [N, K] (bf16 or fp32 by mode); y [M, ldy] fp32 when
