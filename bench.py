@@ -95,6 +95,77 @@ def kernel_work(cfg, B, S):
     }
 
 
+def window_rate(tfm, torch, stream, flush, peaks, window=1024, launches=10):
+    """Sliding-window attention at the long-context shapes (batch 1 x 8192
+    positions, 16 heads, d_head 64, bf16): the windowed flash kernel
+    (tfm_causal_attention_window) against the full causal attention
+    (tfm_causal_attention, the persistent tcgen05 kernel), each launched
+    `launches` times with the L2 flushed between launches; then the whole forward
+    of the long-context model with every layer windowed against the full one
+    (recorded forward, 10 steps each).  Band flops: 4 d_head per (query, visible
+    key) pair, sum_i min(i + 1, w) pairs per head."""
+    cfg = workloads.get_config("long")
+    B, H, S, dh = cfg.batch, cfg.n_head, cfg.seq, cfg.d_head
+    g = torch.Generator(device="cuda").manual_seed(7)
+    q, k, v = (torch.randn(B, H, S, dh, device="cuda", generator=g).to(torch.bfloat16)
+               for _ in range(3))
+    o = torch.empty(B, S, H * dh, device="cuda", dtype=torch.bfloat16)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+            flush.zero_()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(launches)]
+        torch.cuda.synchronize()
+        for a, b in ev:
+            a.record(stream)
+            fn()
+            b.record(stream)
+            flush.zero_()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / launches
+
+    ms_win = timed(lambda: tfm.causal_attention_window(q, k, v, o, window, stream=stream))
+    ms_full = timed(lambda: tfm.causal_attention(q, k, v, o, stream=stream))
+    pairs_win = sum(min(i + 1, window) for i in range(S))
+    pairs_full = S * (S + 1) // 2
+    fl_win = 4.0 * B * H * dh * pairs_win
+    fl_full = 4.0 * B * H * dh * pairs_full
+    ach = fl_win / (ms_win / 1e3) / 1e12
+    # the whole long-context forward, all layers windowed vs all full
+    w = workloads.make_weights(cfg)
+    conv = lambda key, a: torch.from_numpy(a).to(torch.float32 if key.endswith("norm")
+                                                else torch.bfloat16).cuda()
+    tw = {kk: conv(kk, w[kk]) for kk in ("embed", "final_norm", "lm_head")}
+    tw["layers"] = [{kk: conv(kk, vv) for kk, vv in layer.items()} for layer in w["layers"]]
+    model = tfm.Model(cfg)
+    model.load_weights(tw)
+    del tw
+    tok = torch.from_numpy(workloads.make_tokens(cfg)).cuda()
+    logits = torch.empty(B * S, (cfg.vocab + 3) // 4 * 4, device="cuda")
+    fwd_full = timed(lambda: model.forward_graph(tok, logits, stream))
+    model.set_attention_windows([window] * cfg.n_layer)
+    fwd_win = timed(lambda: model.forward_graph(tok, logits, stream))
+    tfm.device_status()
+    model.close()
+    return {"window": window,
+            "config": {"workload": "long-context shapes: batch 1 x seq 8192, 16 heads, d_head 64, "
+                                   "bf16; model: the long-context configuration, 4 layers"},
+            "attention_window_us": round(ms_win * 1e3, 2),
+            "attention_full_causal_us": round(ms_full * 1e3, 2),
+            "band_fraction_of_causal_pairs": round(pairs_win / pairs_full, 4),
+            "roofline": {"bound": "tensor", "achieved": round(ach, 1),
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(ach / peaks["bf16_tflops"], 4),
+                         "note": "windowed flash kernel (mma.sync m16n8k16), band flops"},
+            "full_causal_tflops": round(fl_full / (ms_full / 1e3) / 1e12, 1),
+            "forward_tokens_per_s": {"all_layers_window": round(B * S / (fwd_win / 1e3)),
+                                     "full": round(B * S / (fwd_full / 1e3))},
+            "how": "CUDA events around each launch, L2 flushed between launches; forwards "
+                   "recorded as graphs"}
+
+
 def gpt2_kernel_work(cfg, B, S):
     """kernel_work for the GPT-2-style family: a single F-wide fc GEMM (GELU)
     instead of gate/up, LayerNorm reading a gain and a shift, the embedding
@@ -505,6 +576,10 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-loss", action="store_true")
+    ap.add_argument("--no-window", action="store_true",
+                    help="skip the sliding-window attention measurement")
+    ap.add_argument("--window-only", action="store_true",
+                    help="only the sliding-window measurement; prints its JSON object alone")
     ap.add_argument("--no-gpt2", action="store_true",
                     help="skip the GPT-2-style family measurement")
     ap.add_argument("--gpt2-only", action="store_true",
@@ -616,6 +691,10 @@ def main():
     stream = torch.cuda.Stream()
     torch.cuda.set_stream(stream)
     run = model.forward if args.no_graph else model.forward_graph
+    if args.window_only:
+        print(json.dumps({"window": window_rate(tfm, torch, stream, flush, load_peaks())}))
+        model.close()
+        return
     if args.gpt2_only:
         print(json.dumps({"gpt2_family": gpt2_rate(tfm, torch, stream, flush, load_peaks(),
                                                    steps=args.steps)}))
@@ -720,6 +799,8 @@ def main():
              if rank == 0 and not args.no_loss else None)
     g2 = (gpt2_rate(tfm, torch, stream, flush, load_peaks())
           if rank == 0 and not args.no_gpt2 else None)
+    winr = (window_rate(tfm, torch, stream, flush, load_peaks())
+            if rank == 0 and not args.no_window and cfg.mode == "bf16" else None)
     rows = sampler.stop()
     clocks = ClockSampler.summary(rows)
     clocks["window_s"] = round(t_wall1 - t_wall0, 3)
@@ -775,6 +856,7 @@ def main():
         "decode": decode,
         "loss": lossr,
         "gpt2_family": g2,
+        "window": winr,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": (2 + 7 * cfg.n_layer) * args.steps,
