@@ -97,9 +97,9 @@ def kernel_work(cfg, B, S):
 
 def window_rate(tfm, torch, stream, flush, peaks, window=1024, launches=10):
     """Sliding-window attention at the long-context shapes (batch 1 x 8192
-    positions, 16 heads, d_head 64, bf16): the windowed flash kernel
-    (tfm_causal_attention_window) against the full causal attention
-    (tfm_causal_attention, the persistent tcgen05 kernel), each launched
+    positions, 16 heads, d_head 64, bf16): the persistent tcgen05 kernel with the
+    window (tfm_causal_attention_window) against the same kernel's full causal
+    attention (tfm_causal_attention), each launched
     `launches` times with the L2 flushed between launches; then the whole forward
     of the long-context model with every layer windowed against the full one
     (recorded forward, 10 steps each).  Band flops: 4 d_head per (query, visible
@@ -158,7 +158,8 @@ def window_rate(tfm, torch, stream, flush, peaks, window=1024, launches=10):
             "roofline": {"bound": "tensor", "achieved": round(ach, 1),
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": round(ach / peaks["bf16_tflops"], 4),
-                         "note": "windowed flash kernel (mma.sync m16n8k16), band flops"},
+                         "note": "persistent tcgen05 attention with the window's tile skip "
+                                 "(d_head 64: two query tiles per item), band flops"},
             "full_causal_tflops": round(fl_full / (ms_full / 1e3) / 1e12, 1),
             "forward_tokens_per_s": {"all_layers_window": round(B * S / (fwd_win / 1e3)),
                                      "full": round(B * S / (fwd_full / 1e3))},

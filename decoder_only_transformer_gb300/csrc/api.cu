@@ -887,12 +887,14 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
                                           cudaMemcpyDeviceToDevice, st);
                 if (e != cudaSuccess) return cuda_fail(e, "k, v into the cache");
             }
-            // a sliding-window layer (window < S) runs the flash kernel with the
-            // band's tile skip; full layers the persistent tensor-core kernels
+            // a sliding-window layer (window < S) skips the key tiles before each
+            // query tile's window and masks the band's edge
             const int win = layer_window(m, l, S);
-            if (m->attn_tc && win == 0)
-                TFM_LAUNCH(K_ATTN, launch_attention_tc(m->p_attn, st));
-            else
+            if (m->attn_tc) {
+                AttnPlan pw = m->p_attn;
+                pw.window = win;
+                TFM_LAUNCH(K_ATTN, launch_attention_tc(pw, st));
+            } else
                 TFM_LAUNCH(K_ATTN, launch_attention_bf16(m->q(), m->k(), m->v(), m->o(), B,
                                                          c.n_head, c.n_kv_head, S, dh, scale, st,
                                                          win));
@@ -1493,10 +1495,11 @@ tfm_status tfm_causal_attention_window(const void* q, const void* k, const void*
     cudaError_t e;
     if (mode == TFM_BF16) {
         if (dh != 32 && dh != 64 && dh != 128) return fail(TFM_EUNSUPPORTED, "bf16 attention: dh in {32,64,128}");
-        if (window == 0 && tfm::attention_tc_supported(dh)) {
+        if (tfm::attention_tc_supported(dh)) {
             tfm::AttnPlan plan;
             tfm_status ps = tfm::plan_attention_tc(&plan, q, k, v, o, B, H, Hkv, S, dh, scale);
             if (ps != TFM_OK) return fail(ps, "could not encode attention tensor maps");
+            plan.window = window;
             e = tfm::launch_attention_tc(plan, cs);
         } else {
             e = tfm::launch_attention_bf16(q, k, v, o, B, H, Hkv, S, dh, scale, cs, window);

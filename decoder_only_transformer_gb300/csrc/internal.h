@@ -215,6 +215,7 @@ struct AttnPlan {
     int B, H, Hkv, S, dh;
     float scale;
     void* o;                        // [B, S, H*dh] bf16
+    int window;                     // > 0: sliding window (query i sees keys i-window < j <= i)
 };
 bool attention_tc_supported(int dh);
 tfm_status plan_attention_tc(AttnPlan* p, const void* q, const void* k, const void* v, void* o,

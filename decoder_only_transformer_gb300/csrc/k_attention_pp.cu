@@ -36,6 +36,8 @@
 // one thread issuing all ~24 MMAs of a key tile was measured to be the bound,
 // hence two issuing threads.  All waits are bounded; tiles above the diagonal
 // are never loaded.
+#include <climits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -86,11 +88,11 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t swz, uint32_t
     return d;
 }
 
-template <int DH>
+template <int DH, bool kWin>
 __global__ void __launch_bounds__(kThreadsPP, 1)
     k_attention_pp(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, __nv_bfloat16* __restrict__ o, int BH,
-                   int H, int Hkv, int S, float scale_log2, int* err) {
+                   int H, int Hkv, int S, float scale_log2, int window, int* err) {
     using L = AttPP<DH>;
     constexpr int ST = L::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -124,8 +126,11 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
     // G-1-c), which keeps the sum of item lengths per CTA even.  Every role walks
     // the same sequence; barrier phases follow running counters across items.
     const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    // Key tiles j0 + j for j in [0, nmax): j0 = 0, or with a sliding window the
+    // tile holding tile A's first window start (earlier tiles are never loaded);
+    // query tile x uses j in [lo[x], n[x]).
     struct Item {
-        int qA, qB, n[2], nmax, b, h, g;
+        int qA, qB, j0, lo[2], n[2], nmax, b, h, g;
     };
     auto item_of = [&](int rnd, Item& it) -> bool {
         const int idx = rnd * G + ((rnd & 1) ? G - 1 - c : c);
@@ -137,8 +142,14 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
         it.g = it.h / (H / Hkv);
         it.qA = 2 * pair;
         it.qB = 2 * pair + 1;
-        it.n[0] = it.qA + 1;                                     // key tiles of tile A
-        it.n[1] = it.qB < num_qt ? it.qB + 1 : 0;                // 0: tile B does not exist
+        const int wsA = it.qA * kQ - window + 1, wsB = it.qB * kQ - window + 1;
+        const int jA = (kWin && wsA > 0) ? wsA / kKV : 0;
+        const int jB = (kWin && wsB > 0) ? wsB / kKV : 0;
+        it.j0 = jA;
+        it.lo[0] = 0;
+        it.n[0] = it.qA + 1 - jA;                                // key tiles of tile A
+        it.lo[1] = it.qB < num_qt ? jB - jA : 0;
+        it.n[1] = it.qB < num_qt ? it.qB + 1 - jA : 0;           // 0: tile B does not exist
         it.nmax = it.n[1] > it.n[0] ? it.n[1] : it.n[0];
         return true;
     };
@@ -205,14 +216,16 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                     const uint32_t ph = ((uint32_t)(kv / ST) & 1u) ^ 1u;
                     if (!mbar_wait(k_empty(st), ph, err, abort_flag)) { ok = false; break; }
                     mbar_arrive_expect_tx(k_full(st), L::kKBytes);
-                    tma_load_3d(sK + st * L::kKBytes, &kmap, 0, j * kKV, it.b * Hkv + it.g, k_full(st));
+                    tma_load_3d(sK + st * L::kKBytes, &kmap, 0, (it.j0 + j) * kKV, it.b * Hkv + it.g,
+                                k_full(st));
                     if (!mbar_wait(v_empty(st), ph, err, abort_flag)) {
                         mbar_wait(k_full(st), (uint32_t)((kv / ST) & 1), err, abort_flag);
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(v_full(st), L::kVBytes);
-                    tma_load_3d(sV + st * L::kVBytes, &vmap, 0, j * kKV, it.b * Hkv + it.g, v_full(st));
+                    tma_load_3d(sV + st * L::kVBytes, &vmap, 0, (it.j0 + j) * kKV, it.b * Hkv + it.g,
+                                v_full(st));
                     ++kv;
                 }
             }
@@ -258,7 +271,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                         const int st = kv % ST;
                         ok = mbar_wait(k_full(st), (uint32_t)(kv / ST) & 1u, err, abort_flag);
                         for (int x = 0; x < 2 && ok; ++x) {
-                            if (j >= it.n[x]) continue;
+                            if (j < it.lo[x] || j >= it.n[x]) continue;
                             // S_x is free once the softmax has read the previous
                             // scores into registers (possibly of the previous item).
                             if (cnt[x] > 0)
@@ -294,14 +307,14 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                         const int st = kv % ST;
                         ok = mbar_wait(v_full(st), (uint32_t)(kv / ST) & 1u, err, abort_flag);
                         for (int x = 0; x < 2 && ok; ++x) {
-                            if (j >= it.n[x]) continue;
+                            if (j < it.lo[x] || j >= it.n[x]) continue;
                             // The first P of an item is written only after the
                             // softmax has read the previous item's O_x, so the
                             // overwrite (first = true) cannot race that read.
                             ok = mbar_wait(p_full(x), (uint32_t)cnt[x] & 1u, err, abort_flag);
                             if (ok) {
                                 tc_fence_after();
-                                issue_pv(x, st, j == 0);
+                                issue_pv(x, st, j == it.lo[x]);
                                 ++cnt[x];
                             }
                         }
@@ -333,8 +346,12 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
             if (n == 0) continue;
             const int qt = x == 0 ? it.qA : it.qB;
             const int qi = qt * kQ + r;
+            // first visible key: 0, or the window start of the row (rows past S
+            // take the window of row S - 1)
+            const int kmin = kWin ? (qi < S ? qi : S - 1) - window + 1 : 0;
+            const int win_lo = kWin ? qt * kQ + kQ - window : INT_MIN;
             float m = -INFINITY, l = 0.f;
-            for (int j = 0; j < n && ok; ++j, ++cnt) {
+            for (int j = it.lo[x]; j < n && ok; ++j, ++cnt) {
                 if (!warp_wait(s_full(x), (uint32_t)cnt & 1u, err, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t sr[kKV / 32][32];
@@ -352,11 +369,19 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) s[cc * 32 + e] = __uint_as_float(sr[cc][e]);
                 }
-                const int k0 = j * kKV;
-                if (j == qt || k0 + kKV > S) {
+                const int jt = it.j0 + j;              // key tile index
+                const int k0 = jt * kKV;
+                if (jt == qt || k0 + kKV > S) {
 #pragma unroll
                     for (int cc = 0; cc < kKV; ++cc)
                         if (k0 + cc > qi || k0 + cc >= S) s[cc] = -INFINITY;
+                }
+                // Keys before the row's window start (CTA-uniform test); a row with
+                // none left in this tile keeps m = -inf and gets p = 0 below.
+                if (kWin && k0 < win_lo) {
+#pragma unroll
+                    for (int cc = 0; cc < kKV; ++cc)
+                        if (k0 + cc < kmin) s[cc] = -INFINITY;
                 }
                 // Row max: four independent chains of three-input maxima.
                 float mx4[4] = {s[0], s[1], s[2], s[3]};
@@ -370,13 +395,15 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                     corr = fast_exp2(m - mx);
                     m = mx;
                 }
-                const bool need_rescale = __any_sync(0xffffffffu, corr != 1.f && j > 0);
+                const bool need_rescale = __any_sync(0xffffffffu, corr != 1.f && j > it.lo[x]);
                 // p = 2^(s*scale - m): scale and offset as packed pairs, one exponential
                 // per element, row sum in four packed accumulators, P kept in registers
                 // as bf16 pairs.  The exponentials do not depend on the previous P.V,
                 // so they run before the wait for it.
                 const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
-                const uint64_t negm2 = f2_pack(-m, -m);
+                // (m = -inf: no visible key yet, every p is 0)
+                const float negm = (kWin && m == -INFINITY) ? 0.f : -m;
+                const uint64_t negm2 = f2_pack(negm, negm);
                 uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
                 uint32_t pw[kKV / 64][32];
 #pragma unroll
@@ -457,13 +484,13 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
     if (warp == 1) tmem_dealloc(tmem_base, 512);
 }
 
-template <int DH>
-cudaError_t launch_pp(const AttnPlan& p, cudaStream_t st) {
+template <int DH, bool kWin>
+cudaError_t launch_pp_w(const AttnPlan& p, cudaStream_t st) {
     using L = AttPP<DH>;
     static_assert(L::kBytes <= 232448, "shared memory budget");
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_attention_pp<DH>,
+        cudaError_t e = cudaFuncSetAttribute(k_attention_pp<DH, kWin>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -472,9 +499,16 @@ cudaError_t launch_pp(const AttnPlan& p, cudaStream_t st) {
     const int num_qt = (p.S + kQ - 1) / kQ;
     const int items = ((num_qt + 1) / 2) * p.B * p.H;
     const int grid = items < sm_count() ? items : sm_count();
-    return launch_pdl(k_attention_pp<DH>, dim3(grid), dim3(kThreadsPP), L::kBytes, st, p.qmap,
+    return launch_pdl(k_attention_pp<DH, kWin>, dim3(grid), dim3(kThreadsPP), L::kBytes, st, p.qmap,
                       p.kmap, p.vmap, static_cast<__nv_bfloat16*>(p.o), p.B * p.H, p.H, p.Hkv,
-                      p.S, p.scale * 1.4426950408889634f, device_error_word());
+                      p.S, p.scale * 1.4426950408889634f, p.window, device_error_word());
+}
+
+// The window is a template parameter: the full-causal instantiation keeps the
+// code (and the registers) it had without the window.
+template <int DH>
+cudaError_t launch_pp(const AttnPlan& p, cudaStream_t st) {
+    return p.window > 0 ? launch_pp_w<DH, true>(p, st) : launch_pp_w<DH, false>(p, st);
 }
 
 }  // namespace

@@ -39,6 +39,8 @@
 //               O / l as bf16 to global memory (heads merged).
 // S_{j+1} runs on the tensor cores while the softmax warps work on S_j.
 // Tiles entirely above the diagonal are never loaded.  All waits are bounded.
+#include <climits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -73,11 +75,11 @@ struct AttTc {
     static constexpr int kBytes = kMiscOff + 16 + 1024;
 };
 
-template <int DH>
+template <int DH, bool kWin>
 __global__ void __launch_bounds__(kThreadsAtt, 1)
     k_attention_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, __nv_bfloat16* __restrict__ o, int BH,
-                   int H, int Hkv, int S, float scale_log2, int* err) {
+                   int H, int Hkv, int S, float scale_log2, int window, int* err) {
     using L = AttTc<DH>;
     constexpr int ST = L::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -113,13 +115,17 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
     // counter g across items.
     const int G = (int)gridDim.x, c = (int)blockIdx.x;
     struct Item {
-        int qt, n, b, h, g;
+        int qt, j0, n, b, h, g;
     };
+    // Key tiles j0..qt: j0 = 0, or with a sliding window the tile holding the
+    // window start of the query tile's first row (earlier tiles are never loaded).
     auto item_of = [&](int rnd, Item& it) -> bool {
         const int idx = rnd * G + ((rnd & 1) ? G - 1 - c : c);
         if (idx >= total) return false;
         it.qt = num_qt - 1 - idx / BH;
-        it.n = it.qt + 1;                              // key tiles 0..qt
+        const int ws0 = it.qt * kQ - window + 1;
+        it.j0 = (kWin && ws0 > 0) ? ws0 / kKV : 0;
+        it.n = it.qt + 1 - it.j0;
         const int bh = idx % BH;
         it.b = bh / H;
         it.h = bh - it.b * H;
@@ -207,9 +213,9 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
                 for (int sub = 0; sub < L::kSub; ++sub)
                     tma_load_3d(sQ + sub * 16384, &qmap, 64 * sub, it.qt * kQ, it.b * H + it.h, q_full);
                 ++items;
-                ok = load_k(0);
-                for (int j = 1; j < it.n && ok; ++j) ok = load_k(j) && load_v(j - 1);
-                if (ok) ok = load_v(it.n - 1);
+                ok = load_k(it.j0);
+                for (int j = 1; j < it.n && ok; ++j) ok = load_k(it.j0 + j) && load_v(it.j0 + j - 1);
+                if (ok) ok = load_v(it.j0 + it.n - 1);
             }
             // Drain: the copies of every armed slot (and the last Q) must land.
             if (items > 0) mbar_wait(q_full, (uint32_t)(items - 1) & 1u, err, abort_flag);
@@ -309,8 +315,12 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
             if (!item_of(rnd, it)) continue;
             const int qt = it.qt;
             const int qi = qt * kQ + r;               // query position
-            // Last visible key of this row: the diagonal, or S - 1 past the end.
+            // Last visible key of this row: the diagonal, or S - 1 past the end;
+            // first visible key: 0, or the window start.
             const int kmax = qi < S ? qi : S - 1;
+            const int kmin = kWin ? kmax - window + 1 : 0;
+            // tiles starting below this key hold keys before some row's window
+            const int win_lo = kWin ? qt * kQ + kQ - window : INT_MIN;
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < it.n; ++j, ++g) {
                 const int sb = g & 1;
@@ -328,13 +338,21 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) s[cc * 32 + e] = __uint_as_float(sr[cc][e]);
                 }
-                const int k0 = j * kKV;
+                const int jt = it.j0 + j;             // key tile index
+                const int k0 = jt * kKV;
                 // Only the diagonal tile and a tile reaching past S need the mask
                 // (warp-uniform test).
-                if (j == qt || k0 + kKV > S) {
+                if (jt == qt || k0 + kKV > S) {
                     const int lim = kmax - k0;         // keys cc > lim are masked
 #pragma unroll
                     for (int cc = 0; cc < kKV; ++cc) s[cc] = cc > lim ? -INFINITY : s[cc];
+                }
+                // Keys before the row's window start (CTA-uniform test); a row with
+                // none left in this tile keeps m = -inf and gets p = 0 below.
+                if (kWin && k0 < win_lo) {
+                    const int lo = kmin - k0;          // keys cc < lo are masked
+#pragma unroll
+                    for (int cc = 0; cc < kKV; ++cc) s[cc] = cc < lo ? -INFINITY : s[cc];
                 }
                 // Row max over raw scores: four independent chains of three-input
                 // maxima (the scale is positive, so it commutes with the max).
@@ -354,7 +372,9 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
                 // exponential per element, row sum in four packed accumulators, P
                 // kept in registers as bf16 pairs until its buffer is free.
                 const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
-                const uint64_t negm2 = f2_pack(-m, -m);
+                // (m = -inf: no visible key yet, every p is 0)
+                const float negm = (kWin && m == -INFINITY) ? 0.f : -m;
+                const uint64_t negm2 = f2_pack(negm, negm);
                 uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
                 uint32_t pw[kKV / 64][32];
 #pragma unroll
@@ -513,13 +533,13 @@ bool heads_map(CUtensorMap* map, const void* ptr, int64_t n_seq_heads, int64_t S
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int DH>
-cudaError_t launch_tc(const AttnPlan& p, cudaStream_t st) {
+template <int DH, bool kWin>
+cudaError_t launch_tc_w(const AttnPlan& p, cudaStream_t st) {
     using L = AttTc<DH>;
     static_assert(L::kBytes <= 232448, "shared memory budget");
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_attention_tc<DH>,
+        cudaError_t e = cudaFuncSetAttribute(k_attention_tc<DH, kWin>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -527,9 +547,16 @@ cudaError_t launch_tc(const AttnPlan& p, cudaStream_t st) {
     // One CTA per SM (shared memory allows no more), each looping over items.
     const int items = ((p.S + kQ - 1) / kQ) * p.B * p.H;
     const int grid = items < sm_count() ? items : sm_count();
-    return launch_pdl(k_attention_tc<DH>, dim3(grid), dim3(kThreadsAtt), L::kBytes, st, p.qmap,
+    return launch_pdl(k_attention_tc<DH, kWin>, dim3(grid), dim3(kThreadsAtt), L::kBytes, st, p.qmap,
                       p.kmap, p.vmap, static_cast<__nv_bfloat16*>(p.o), p.B * p.H, p.H, p.Hkv,
-                      p.S, p.scale * 1.4426950408889634f, device_error_word());
+                      p.S, p.scale * 1.4426950408889634f, p.window, device_error_word());
+}
+
+// The window is a template parameter: the full-causal instantiation keeps the
+// code (and the registers) it had without the window.
+template <int DH>
+cudaError_t launch_tc(const AttnPlan& p, cudaStream_t st) {
+    return p.window > 0 ? launch_tc_w<DH, true>(p, st) : launch_tc_w<DH, false>(p, st);
 }
 
 }  // namespace
@@ -547,6 +574,7 @@ tfm_status plan_attention_tc(AttnPlan* p, const void* q, const void* k, const vo
     p->dh = dh;
     p->scale = scale;
     p->o = o;
+    p->window = 0;
     if (!heads_map(&p->qmap, q, (int64_t)B * H, S, dh) ||
         !heads_map(&p->kmap, k, (int64_t)B * Hkv, S, dh) ||
         !heads_map(&p->vmap, v, (int64_t)B * Hkv, S, dh))
