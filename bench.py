@@ -60,15 +60,15 @@ def load_peaks():
 # the layer-0 launches (cold caches) of the kernels as they are now; an op
 # without an entry reports traffic null.
 DRAM_TRAFFIC = {
-    ("small", "qkv_rope_gemm"): 10.30e6, ("small", "attention"): 25.18e6,
-    ("small", "oproj_residual_gemm"): 25.74e6, ("small", "gateup_swiglu_gemm"): 14.78e6,
-    ("small", "down_residual_gemm"): 40.74e6,
-    ("long", "qkv_rope_gemm"): 30.14e6, ("long", "attention"): 51.54e6,
-    ("long", "oproj_residual_gemm"): 52.48e6, ("long", "gateup_swiglu_gemm"): 32.48e6,
-    ("long", "down_residual_gemm"): 87.36e6,
-    ("gqa", "qkv_rope_gemm"): 68.98e6, ("gqa", "attention"): 52.17e6,
-    ("gqa", "oproj_residual_gemm"): 130.13e6, ("gqa", "gateup_swiglu_gemm"): 151.39e6,
-    ("gqa", "down_residual_gemm"): 230.70e6,
+    ("small", "qkv_rope_gemm"): 10.07e6, ("small", "attention"): 25.18e6,
+    ("small", "oproj_residual_gemm"): 25.77e6, ("small", "gateup_swiglu_gemm"): 11.22e6,
+    ("small", "down_residual_gemm"): 40.25e6,
+    ("long", "qkv_rope_gemm"): 29.66e6, ("long", "attention"): 50.41e6,
+    ("long", "oproj_residual_gemm"): 52.50e6, ("long", "gateup_swiglu_gemm"): 30.18e6,
+    ("long", "down_residual_gemm"): 84.69e6,
+    ("gqa", "qkv_rope_gemm"): 68.69e6, ("gqa", "attention"): 50.67e6,
+    ("gqa", "oproj_residual_gemm"): 126.73e6, ("gqa", "gateup_swiglu_gemm"): 147.84e6,
+    ("gqa", "down_residual_gemm"): 230.82e6,
 }
 
 
@@ -822,7 +822,8 @@ def main():
                     "cap_note": "min(1, algorithmic flop/byte x HBM copy bandwidth / tensor peak)"}
                    if "cap" in dom else {}),
                 "traffic": DRAM_TRAFFIC.get((cfg.name, dom_name)),
-                "traffic_source": "ncu --set full of the layer-0 launch, cold caches, bytes per launch",
+                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the layer-0 "
+                                  "launch, cold caches, bytes per launch (profiles/layer0_dram_bytes.md)",
                 "peak_source": f"{peaks['source']} ({'bf16 burst' if dom['bound'] == 'tensor' else 'HBM copy'})",
                 "timing": "average launch duration from CUDA events recorded on the launch stream "
                           "after every kernel, over K directly launched steps run after the value region"}
