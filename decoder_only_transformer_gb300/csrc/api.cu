@@ -984,6 +984,7 @@ tfm_status build_decode_plans(Model* m, int B, float* logits, int64_t ld) {
     m->d_down.resize(c.n_layer);
     m->dplan_B = -1;
     tfm_status st = TFM_OK;
+    const bool g2 = m->arch == 1;   // GPT-2-style: biases, no RoPE, a GELU MLP
     for (int l = 0; l < c.n_layer && st == TFM_OK; ++l) {
         {
             // k and v of the new token go straight into the layer's cache
@@ -992,25 +993,35 @@ tfm_status build_decode_plans(Model* m, int B, float* logits, int64_t ld) {
             e.v = m->vcache(l);
             e.kv_stride = c.max_seq;
             e.pos0_dev = m->pos_dev;        // RoPE and cache position of the step
+            if (g2) {
+                e.rope_cs = nullptr;
+                e.bias = m->b_qkv[l];
+            }
             st = plan_gemm_tc(&m->d_qkv[l], m->xn(), s.D, m->wqkv[l], nullptr, s.D, B,
                               (int)s.Nqkv, (int)s.D, e);
         }
+        EpiParams eo = epi_basic(EPI_ACCUM_F32, B, (int)s.D, m->h(), s.D);
+        if (g2) eo.bias = m->b_proj[l];
         if (st == TFM_OK)
             st = plan_gemm_tc(&m->d_o[l], m->o(), s.Dq, m->wo[l], nullptr, s.Dq, B, (int)s.D,
-                              (int)s.Dq, epi_basic(EPI_ACCUM_F32, B, (int)s.D, m->h(), s.D));
+                              (int)s.Dq, eo);
         if (st == TFM_OK) {
-            EpiParams e = epi_basic(EPI_SWIGLU, B, (int)s.F, m->a(), s.F);
+            EpiParams e = epi_basic(g2 ? EPI_GELU : EPI_SWIGLU, B, (int)s.F, m->a(), s.F);
             e.out_bf16 = 1;
-            st = plan_gemm_tc(&m->d_gu[l], m->xn(), s.D, m->w1[l], m->w3[l], s.D, B, (int)s.F,
-                              (int)s.D, e);
+            if (g2) e.bias = m->b_fc[l];
+            st = plan_gemm_tc(&m->d_gu[l], m->xn(), s.D, m->w1[l], g2 ? nullptr : m->w3[l], s.D, B,
+                              (int)s.F, (int)s.D, e);
         }
+        EpiParams ed = epi_basic(EPI_ACCUM_F32, B, (int)s.D, m->h(), s.D);
+        if (g2) ed.bias = m->b_fc2[l];
         if (st == TFM_OK)
             st = plan_gemm_tc(&m->d_down[l], m->a(), s.F, m->w2[l], nullptr, s.F, B, (int)s.D,
-                              (int)s.F, epi_basic(EPI_ACCUM_F32, B, (int)s.D, m->h(), s.D));
+                              (int)s.F, ed);
     }
+    EpiParams el = epi_basic(EPI_STORE_F32, B, (int)s.V, logits, ld);
+    el.bias = m->lm_bias;
     if (st == TFM_OK)
-        st = plan_gemm_tc(&m->d_lm, m->xn(), s.D, m->lm_head, nullptr, s.D, B, (int)s.V, (int)s.D,
-                          epi_basic(EPI_STORE_F32, B, (int)s.V, logits, ld));
+        st = plan_gemm_tc(&m->d_lm, m->xn(), s.D, m->lm_head, nullptr, s.D, B, (int)s.V, (int)s.D, el);
     if (st != TFM_OK) return fail(st, "could not encode TMA tensor maps (driver entry point missing?)");
     for (int l = 0; l < c.n_layer; ++l)
         m->d_qkv[l].b_static = m->d_o[l].b_static = m->d_gu[l].b_static = m->d_down[l].b_static = 1;
@@ -1042,25 +1053,60 @@ tfm_status decode_body(Model* m, const int32_t* tokens, int B, float* logits, in
         if (!ev) return fail(TFM_ECUDA, "cudaEventCreate failed");
         cudaEventRecord(ev, st);
     }
+    // The GPT-2-style family: LayerNorm, the position row of the step added in
+    // the embedding, post-norm blocks normalising the residual stream in place.
+    const bool g2 = m->arch == 1;
+    const bool post = g2 && m->g2.post_norm;
+    auto ln_args = [&](const float* bb, float* h_out) {
+        NormArgs n{};
+        n.kind = kNormLayer;
+        n.b = bb;
+        n.h_out = h_out;
+        return n;
+    };
+    NormArgs na0{};
+    if (g2) {
+        if (c.n_layer == 0) na0 = ln_args(m->lnf_b, nullptr);
+        else if (post) na0.kind = kNormNone;
+        else na0 = ln_args(m->ln1_b[0], nullptr);
+        na0.pos = m->pos;
+        na0.S = 1;
+        na0.pos_dev = m->pos_dev;
+    }
     TFM_LAUNCH(K_EMBED, launch_embed_rmsnorm(tokens, m->embed,
                                              c.n_layer > 0 ? m->attn_norm[0] : m->final_norm,
                                              m->h(), m->xn(), B, c.vocab, c.d_model, c.norm_eps,
-                                             1, st, 1));
+                                             1, st, 1, g2 ? &na0 : nullptr));
+    auto norm = [&](const float* gain, const NormArgs* n) {
+        return launch_rmsnorm(m->h(), gain, m->xn(), B, c.d_model, c.norm_eps, 1, st, 1, n);
+    };
     for (int l = 0; l < c.n_layer; ++l) {
-        if (l > 0)
-            TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->attn_norm[l], m->xn(), B, c.d_model, c.norm_eps, 1, st, 1));
+        if (l > 0 && !post) {
+            NormArgs n = ln_args(g2 ? m->ln1_b[l] : nullptr, nullptr);
+            TFM_LAUNCH(K_NORM, norm(m->attn_norm[l], g2 ? &n : nullptr));
+        }
         TFM_LAUNCH(K_QKV, launch_gemm_tc(m->d_qkv[l], st));
         TFM_LAUNCH(K_ATTN, launch_decode_attention(m->q(), m->kcache(l), m->vcache(l), m->dec_part,
                                                    m->o(), B, c.n_head, c.n_kv_head, c.max_seq,
                                                    m->pos_dev, dh, scale, st,
                                                    m->windows.empty() ? 0 : m->windows[l]));
         TFM_LAUNCH(K_OPROJ, launch_gemm_tc(m->d_o[l], st));
-        TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->ffn_norm[l], m->xn(), B, c.d_model, c.norm_eps, 1, st, 1));
+        {
+            NormArgs n = post ? ln_args(m->ln1_b[l], m->h())
+                              : ln_args(g2 ? m->ln2_b[l] : nullptr, nullptr);
+            TFM_LAUNCH(K_NORM, norm(post ? m->attn_norm[l] : m->ffn_norm[l], g2 ? &n : nullptr));
+        }
         TFM_LAUNCH(K_GATEUP, launch_gemm_tc(m->d_gu[l], st));
         TFM_LAUNCH(K_DOWN, launch_gemm_tc(m->d_down[l], st));
+        if (post) {
+            NormArgs n = ln_args(m->ln2_b[l], m->h());
+            TFM_LAUNCH(K_NORM, norm(m->ffn_norm[l], &n));
+        }
     }
-    if (c.n_layer > 0)
-        TFM_LAUNCH(K_NORM, launch_rmsnorm(m->h(), m->final_norm, m->xn(), B, c.d_model, c.norm_eps, 1, st, 1));
+    if (c.n_layer > 0) {
+        NormArgs n = ln_args(g2 ? m->lnf_b : nullptr, nullptr);
+        TFM_LAUNCH(K_NORM, norm(m->final_norm, g2 ? &n : nullptr));
+    }
     TFM_LAUNCH(K_LMHEAD, launch_gemm_tc(m->d_lm, st));
     return TFM_OK;
 }
@@ -1296,7 +1342,6 @@ tfm_status tfm_kv_cache_create(void* handle) {
     const tfm_config& c = m->cfg;
     const int dh = c.d_model / c.n_head;
     if (c.mode != TFM_BF16) return fail(TFM_EUNSUPPORTED, "the KV cache needs bf16 mode");
-    if (m->arch != 0) return fail(TFM_EUNSUPPORTED, "the KV cache is for the RoPE family only");
     if (!tfm::decode_supported(dh, c.n_head / c.n_kv_head))
         return fail(TFM_EUNSUPPORTED, "decode needs d_head in {32, 64, 128} and H/Hkv in {1, 2, 4, 8, 16} (<= 8 at d_head 128)");
     const size_t layer = (size_t)c.max_batch * c.n_kv_head * c.max_seq * dh * 2;

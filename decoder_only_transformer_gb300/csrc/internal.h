@@ -107,7 +107,8 @@ const char* cuda_error_text(cudaError_t e);
 // How a row is normalised: RMSNorm (the default), LayerNorm with shift b, or no
 // norm (cast only).  h_out: also store the fp32 normalised row (may equal the
 // input).  pos (embedding kernels only): position rows [>= S, D] in the
-// embedding's type added to E[tok[m]], row m taking position m % S.
+// embedding's type added to E[tok[m]], row m taking position m % S, plus
+// *pos_dev when set (a decode step's position, read on the device).
 enum NormKind { kNormRms = 0, kNormLayer = 1, kNormNone = 2 };
 struct NormArgs {
     int kind;
@@ -115,6 +116,7 @@ struct NormArgs {
     float* h_out;
     const void* pos;
     int S;
+    const int* pos_dev;
 };
 cudaError_t launch_embedding(const int32_t* tok, const void* E, float* h, int64_t M, int V,
                              int D, int e_bf16, cudaStream_t st);

@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(256) k_embed_rmsnorm(const int32_t* __restrict
     const bool ok = (t >= 0 && t < V);
     if (!ok && lane == 0) raise_error(err, TFM_EBADTOKEN);
     const int64_t row = ok ? t : 0;
-    const int64_t prow = na.pos ? m % na.S : 0;
+    const int64_t prow = na.pos ? (na.pos_dev ? __ldg(na.pos_dev) : 0) + m % na.S : 0;
     float4 v[kV];
 #pragma unroll
     for (int i = 0; i < kV; ++i) {
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(256) k_norm_row(const int32_t* __restrict__ to
         if (!ok && tid == 0) raise_error(err, TFM_EBADTOKEN);
         row = ok ? t : 0;
     }
-    const int64_t prow = na.pos ? m % na.S : 0;
+    const int64_t prow = na.pos ? (na.pos_dev ? __ldg(na.pos_dev) : 0) + m % na.S : 0;
     float4 v[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {

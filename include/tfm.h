@@ -149,7 +149,8 @@ tfm_status tfm_load_weights(void* handle, const tfm_weights* w, int32_t weights_
  * tfm_config is read as for the first family except rope_theta (unused, not
  * checked); d_ff is the MLP width (4 d_model in the pages).  The forward,
  * graph, host-buffer and cross-entropy entry points take either kind of
- * handle; the KV cache (tfm_kv_cache_create) is for the first family only. */
+ * handle, and so do the KV cache and decoding (a step adds the position row of
+ * its position, read on the device). */
 typedef enum { TFM_POS_LEARNED = 0, TFM_POS_SINUSOIDAL = 1 } tfm_pos_kind;
 typedef struct {
     int32_t pos;           /* tfm_pos_kind */

@@ -97,14 +97,45 @@ def test_gpt2_handles_and_weights_do_not_mix():
         tfm._check(g.lib.tfm_load_weights(g.handle, tfm.Weights(), 0))
     g.load_weights(to_torch_gpt2_weights(w))
     g.close()
-    cfg_b = workloads.GPT2_CONFIGS["gpt2_small"].replace(n_layer=1, vocab=1000)
-    gb = tfm.Gpt2Model(cfg_b, max_batch=1, max_seq=16)
-    gb.load_weights(to_torch_gpt2_weights(workloads.make_gpt2_weights(cfg_b, max_seq=16), bf16=True))
-    with pytest.raises(tfm.TfmError) as ei:       # the KV cache is for the RoPE family only
-        gb.kv_cache_create()
-    assert ei.value.status == tfm.TFM_EUNSUPPORTED
-    gb.close()
     r = tfm.Model(workloads.get_config("tiny"), max_batch=1, max_seq=8)
     with pytest.raises(tfm.TfmError):             # GPT-2 loader on a RoPE-family handle
         tfm._check(r.lib.tfm_load_gpt2_weights(r.handle, tfm.Gpt2Weights(), 0))
     r.close()
+
+
+@pytest.mark.parametrize("pos,post,lm_bias,tied", [
+    ("learned", False, True, False),
+    ("sinusoidal", True, False, True),
+])
+def test_gpt2_decode_matches_oracle(pos, post, lm_bias, tied):
+    """Prefill then decode steps (the position row of each step's position added
+    in the embedding, k and v into the cache, biases, GELU, pre/post-norm),
+    against the oracle's forward over the extended sequences."""
+    cfg = workloads.GPT2_CONFIGS["gpt2_small"].replace(n_layer=2, vocab=3001)
+    B, S0, T = 2, 250, 10                         # crosses the 256-key decode chunk
+    w = workloads.make_gpt2_weights(cfg, pos=pos, lm_bias=lm_bias, tied=tied, max_seq=S0 + T)
+    tok = workloads.make_tokens(cfg, batch=B, seq=S0 + T, seed=51)
+    ld = (cfg.vocab + 3) // 4 * 4
+    model = tfm.Gpt2Model(cfg, pos=pos, post_norm=post, lm_bias=lm_bias, max_batch=B,
+                          max_seq=S0 + T)
+    model.load_weights(to_torch_gpt2_weights(w, bf16=True))
+    model.kv_cache_create()
+    dtok = torch.from_numpy(tok).cuda()
+    pre = torch.empty(B * S0, ld, device="cuda")
+    model.prefill(dtok[:, :S0].contiguous(), pre)
+    # the side stream is non-blocking: the steps must not start before the prefill ends
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    lg = torch.empty(B, ld, device="cuda")
+    steps = []
+    with torch.cuda.stream(side):                 # recorded after the second step, replayed after
+        for t in range(T):
+            model.decode_step(dtok[:, S0 + t].contiguous(), S0 + t, lg, side)
+            steps.append(lg.clone())
+    torch.cuda.synchronize()
+    tfm.device_status()
+    dec = torch.stack(steps, 1).cpu().numpy()[:, :, : cfg.vocab]
+    ref = oracle.gpt2_forward(tok, w, cfg, post_norm=post)
+    _check(cfg, pre.cpu().numpy().reshape(B, S0, ld)[:, :, : cfg.vocab], ref[:, :S0])
+    _check(cfg, dec, ref[:, S0:])
+    model.close()

@@ -142,6 +142,8 @@ def test_decode_with_windows(name, windows, B, S0, T):
     dtok = torch.from_numpy(tok).cuda()
     pre = torch.empty(B * S0, ld, device="cuda")
     model.prefill(dtok[:, :S0].contiguous(), pre)
+    # the side stream is non-blocking: the steps must not start before the prefill ends
+    torch.cuda.synchronize()
     side = torch.cuda.Stream()
     lg = torch.empty(B, ld, device="cuda")
     steps = []
