@@ -368,8 +368,42 @@ def decode_rate(tfm, torch, model, cfg, tok_np, stream, peaks, steps=32):
     w_step = L * w_layer + V * D * 2 + B * D * 2 + D * 4
     step_bytes = w_step + nbytes / steps
     step_gbs = step_bytes / (ms / steps / 1e3) / 1e9
+    # The decode attention alone (tfm_decode_attention, the chunk kernel and the
+    # merge), at this workload's cache shape with every position filled (pos =
+    # S - 1), the L2 flushed before each launch: cold-cache HBM bytes over time.
+    g = torch.Generator(device="cuda").manual_seed(3)
+    qa = torch.randn(B, H, dh, device="cuda", generator=g).to(torch.bfloat16)
+    kca, vca = (torch.randn(B, Hkv, S, dh, device="cuda", generator=g).to(torch.bfloat16)
+                for _ in range(2))
+    oa = torch.empty(B, H * dh, device="cuda", dtype=torch.bfloat16)
+    wsa = torch.empty(tfm.decode_attention_workspace_bytes(B, H, S, dh), dtype=torch.uint8,
+                      device="cuda")
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        tfm.decode_attention(qa, kca, vca, oa, S - 1, wsa, stream=stream)
+    ev_a = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(20)]
+    for a, b_ in ev_a:
+        flush.zero_()
+        a.record(stream)
+        tfm.decode_attention(qa, kca, vca, oa, S - 1, wsa, stream=stream)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    us_a = sum(a.elapsed_time(b_) for a, b_ in ev_a) / len(ev_a) * 1e3
+    nk = 16384 // dh
+    bytes_a = (2 * B * Hkv * S * dh * 2 + 2 * B * H * dh * 2
+               + 2 * B * H * ((S + nk - 1) // nk) * (dh + 2) * 4)
+    gbs_a = bytes_a / (us_a * 1e-6) / 1e9
+    del flush
     return {"value": B * steps / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms / steps,
             "batch": B, "prefill_len": S0, "steps": steps,
+            "attention_alone": {"bound": "hbm", "positions": S, "avg_us": round(us_a, 2),
+                                "bytes": bytes_a, "achieved": round(gbs_a, 1),
+                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": round(gbs_a / peaks["hbm_gbs"], 4),
+                                "how": "tfm_decode_attention at the workload's cache shape, pos "
+                                       "= S - 1, L2 flushed before each of 20 launches, events "
+                                       "around each launch"},
             "step_roofline": {"bound": "hbm", "bytes_per_step": int(step_bytes),
                               "achieved": round(step_gbs, 1), "peak": peaks["hbm_gbs"],
                               "unit": "GB/s", "frac": round(step_gbs / peaks["hbm_gbs"], 4)},

@@ -1560,6 +1560,42 @@ tfm_status tfm_causal_attention_window(const void* q, const void* k, const void*
     return e == cudaSuccess ? TFM_OK : tfm::cuda_fail(e, "attention launch");
 }
 
+size_t tfm_decode_attention_workspace_bytes(int32_t B, int32_t H, int32_t max_seq, int32_t dh) {
+    if (B < 1 || H < 1 || max_seq < 1 || (dh != 32 && dh != 64 && dh != 128)) return 0;
+    // the position word (256 bytes reserved), then the chunk partials
+    return 256 + tfm::decode_partial_floats(B, H, max_seq, dh) * 4;
+}
+
+tfm_status tfm_decode_attention(const void* q, const void* k_cache, const void* v_cache, void* o,
+                                int32_t B, int32_t H, int32_t Hkv, int32_t max_seq, int32_t pos,
+                                int32_t dh, float scale, int32_t window, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    if (!q || !k_cache || !v_cache || !o || !workspace) return fail(TFM_EINVAL, "NULL pointer");
+    if (B < 0 || H < 1 || Hkv < 1 || H % Hkv || max_seq < 1) return fail(TFM_EINVAL, "bad sizes");
+    if (pos < 0 || pos >= max_seq) return fail(TFM_EINVAL, "pos=%d outside [0, max_seq=%d)", pos, max_seq);
+    if (window < 0) return fail(TFM_EINVAL, "window must be >= 0");
+    if (!tfm::aligned16(q) || !tfm::aligned16(k_cache) || !tfm::aligned16(v_cache) ||
+        !tfm::aligned16(o) || !tfm::aligned16(workspace))
+        return fail(TFM_EINVAL, "pointers must be 16-byte aligned");
+    if (!tfm::decode_supported(dh, H / Hkv))
+        return fail(TFM_EUNSUPPORTED, "dh in {32, 64, 128}, H/Hkv in {1, 2, 4, 8, 16} (<= 8 at dh 128)");
+    if (B == 0) return TFM_OK;
+    if (workspace_bytes < tfm_decode_attention_workspace_bytes(B, H, max_seq, dh))
+        return fail(TFM_EINVAL, "workspace too small");
+    if (scale <= 0.f) scale = 1.0f / std::sqrt((float)dh);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    int* pos_dev = static_cast<int*>(workspace);
+    float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256);
+    // The kernel reads the position (and prefetches cache rows) before its grid
+    // dependency wait, so the position must not come from the kernel launched just
+    // before it: a stream-ordered copy has no programmatic early start.
+    cudaError_t e = cudaMemcpyAsync(pos_dev, &pos, sizeof(int), cudaMemcpyHostToDevice, cs);
+    if (e == cudaSuccess)
+        e = tfm::launch_decode_attention(q, k_cache, v_cache, part, o, B, H, Hkv, max_seq, pos_dev,
+                                         dh, scale, cs, window);
+    return e == cudaSuccess ? TFM_OK : tfm::cuda_fail(e, "decode attention launch");
+}
+
 tfm_status tfm_linear(const void* x, const void* W, void* y, int64_t M, int32_t N, int32_t K,
                       int64_t ldy, int32_t out_fp32, int32_t accumulate, int32_t mode, void* stream) {
     if (!x || !W || !y) return fail(TFM_EINVAL, "NULL pointer");

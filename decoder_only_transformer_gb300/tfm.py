@@ -95,6 +95,9 @@ _SIGS = {
     "tfm_causal_attention_window": ([_V, _V, _V, _V, _I32, _I32, _I32, _I32, _I32, _F, _I32, _I32,
                                      _V], _I32),
     "tfm_set_attention_windows": ([_V, ctypes.POINTER(ctypes.c_int32), _I32], _I32),
+    "tfm_decode_attention_workspace_bytes": ([_I32, _I32, _I32, _I32], _SZ),
+    "tfm_decode_attention": ([_V, _V, _V, _V, _I32, _I32, _I32, _I32, _I32, _I32, _F, _I32, _V,
+                              _SZ, _V], _I32),
     "tfm_linear": ([_V, _V, _V, _I64, _I32, _I32, _I64, _I32, _I32, _I32, _V], _I32),
     "tfm_swiglu": ([_V, _V, _V, _V, _V, _I64, _I32, _I32, _I32, _V, _SZ, _I32, _V], _I32),
     "tfm_swiglu_workspace_bytes": ([_I64, _I32, _I32], _SZ),
@@ -340,6 +343,20 @@ def causal_attention_window(q, k, v, o, window, scale=0.0, stream=None):
     _check(load().tfm_causal_attention_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Hkv, S,
                                               dh, scale, int(window), _mode_of(q),
                                               _stream(stream)))
+
+
+def decode_attention_workspace_bytes(B, H, max_seq, dh):
+    return load().tfm_decode_attention_workspace_bytes(B, H, max_seq, dh)
+
+
+def decode_attention(q, k_cache, v_cache, o, pos, workspace, window=0, scale=0.0, stream=None):
+    """q [B, H, dh]; caches [B, Hkv, max_seq, dh]; o [B, H*dh]; all bf16 (device)."""
+    B, H, dh = q.shape
+    Hkv, max_seq = k_cache.shape[1], k_cache.shape[2]
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().tfm_decode_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), B, H, Hkv,
+                                       max_seq, int(pos), dh, scale, int(window), _ptr(workspace),
+                                       nbytes, _stream(stream)))
 
 
 def linear(x, W, y, accumulate=False, stream=None):

@@ -388,6 +388,28 @@ tfm_status tfm_causal_attention_window(const void* q, const void* k, const void*
                                        int32_t B, int32_t H, int32_t Hkv, int32_t S, int32_t dh,
                                        float scale, int32_t window, int32_t mode, void* stream);
 
+/* Attention of one new query per sequence over a KV cache, the attention of a
+ * decode step ("LLM 2", sections KV cache and GQA / MQA; the last row of the
+ * causal mask of the CS336 walkthrough, section 5.4): q [B, H, dh] (the query of
+ * position pos), k_cache and v_cache [B, Hkv, max_seq, dh] holding positions
+ * [0, pos], o [B, H*dh]; o = softmax(q k^T * scale) v over positions
+ * [max(0, pos - window + 1), pos] (window 0: all of [0, pos]), query head h
+ * reading kv head h / (H / Hkv); scale <= 0 means 1/sqrt(dh).  bf16 only;
+ * dh in {32, 64, 128}; H / Hkv in {1, 2, 4, 8, 16} (<= 8 at dh 128).  The keys
+ * are split over CTAs in chunks of 16384/dh positions, each fetched by bulk
+ * asynchronous copies, and the chunks are merged exactly by a second kernel.
+ * workspace: device, 16-byte aligned, at least
+ * tfm_decode_attention_workspace_bytes(B, H, max_seq, dh) bytes, not used by
+ * another call in flight.  The position goes to the workspace by a small
+ * host-to-device copy on `stream` (so the call is not capturable in a graph;
+ * tfm_decode_step is).  TFM_EINVAL for bad sizes (0 <= pos < max_seq,
+ * window >= 0) or a small workspace; TFM_EUNSUPPORTED for other dh / groups. */
+size_t tfm_decode_attention_workspace_bytes(int32_t B, int32_t H, int32_t max_seq, int32_t dh);
+tfm_status tfm_decode_attention(const void* q, const void* k_cache, const void* v_cache, void* o,
+                                int32_t B, int32_t H, int32_t Hkv, int32_t max_seq, int32_t pos,
+                                int32_t dh, float scale, int32_t window, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
 /* Bias-free Linear (CS336 walkthrough, section 5.3): y = x W^T.
  * x [M, K], W [N, K] (bf16 or fp32 by mode); y [M, ldy] fp32 when
  * out_fp32 != 0 (accumulate != 0 adds into y instead of overwriting), else

@@ -142,3 +142,41 @@ def test_decode_replay_matches_direct(name):
     for t in range(T):
         assert torch.equal(replay[t][:, : cfg.vocab], direct[t][:, : cfg.vocab]), t
     model.close()
+
+
+@pytest.mark.parametrize("dh,H,Hkv,pos,window", [
+    (32, 8, 8, 700, 0),          # 512-key chunks: two
+    (64, 12, 3, 255, 0),         # the last key of the first 256-key chunk
+    (64, 12, 3, 256, 100),       # the first key of the second chunk, windowed
+    (128, 16, 4, 1000, 0),       # 128-key chunks, GQA
+    (128, 16, 2, 127, 0),        # one chunk
+    (128, 8, 8, 383, 200),       # window over three chunks
+])
+def test_decode_attention_component(dh, H, Hkv, pos, window):
+    """tfm_decode_attention against the last row of the oracle's causal
+    (windowed) attention; cache positions past pos hold large values that must
+    not be read."""
+    B, max_seq = 3, pos + 18
+    r = np.random.default_rng(pos + dh)
+    bf = workloads.round_to_bf16
+    q = bf(r.standard_normal((B, H, dh), dtype=np.float32))
+    kc = bf(r.standard_normal((B, Hkv, max_seq, dh), dtype=np.float32))
+    vc = bf(r.standard_normal((B, Hkv, max_seq, dh), dtype=np.float32))
+    kc[:, :, pos + 1:] = 1e4
+    vc[:, :, pos + 1:] = -1e4
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).cuda()
+    o = torch.empty(B, H * dh, device="cuda", dtype=torch.bfloat16)
+    ws = torch.empty(tfm.decode_attention_workspace_bytes(B, H, max_seq, dh), dtype=torch.uint8,
+                     device="cuda")
+    tfm.decode_attention(t(q), t(kc), t(vc), o, pos, ws, window=window)
+    torch.cuda.synchronize()
+    tfm.device_status()
+    qf = np.zeros((B, H, pos + 1, dh), dtype=np.float32)
+    qf[:, :, pos] = q
+    ref = oracle.causal_attention(qf, kc[:, :, : pos + 1], vc[:, :, : pos + 1], window=window)
+    ref = ref[:, :, pos].reshape(B, H * dh)
+    assert rel_err(o.float().cpu().numpy(), ref) < 8e-3
+    if dh == 64:                                 # a group of 3 query heads is not supported
+        with pytest.raises(tfm.TfmError) as ei:
+            tfm.decode_attention(t(q[:, :9]), t(kc), t(vc), o, pos, ws)
+        assert ei.value.status == tfm.TFM_EUNSUPPORTED
