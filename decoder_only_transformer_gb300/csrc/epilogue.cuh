@@ -155,14 +155,15 @@ __device__ __forceinline__ float gelu_exact(float z) {
     return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
 }
 
-template <int W>
+// kBias = false compiles the bias out (plans without one).
+template <int W, bool kBias = true>
 __device__ __forceinline__ void epi_compute(const EpiParams& p, int row, int col0,
                                             const float (&a_in)[W], const float (&u)[W],
                                             float (&o)[W]) {
     float a[W];
 #pragma unroll
     for (int i = 0; i < W; ++i) a[i] = a_in[i];
-    if (p.bias) {
+    if (kBias && p.bias) {
         if constexpr (W % 4 == 0) {
             if (col0 + W <= p.N) {               // whole chunk: 16-byte loads (bias 16-byte aligned)
                 const float4* b4 = reinterpret_cast<const float4*>(p.bias + col0);

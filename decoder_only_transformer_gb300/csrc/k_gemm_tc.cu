@@ -199,7 +199,10 @@ __device__ __forceinline__ void tma_out_block(const TcMaps& maps, const EpiParam
     }
 }
 
-template <int BN, int STAGES, bool kDual, bool kPair>
+// kExt: the epilogues of the second model family and the fused loss (a bias
+// vector, EPI_LSE); without it those paths are compiled out, so the plans that
+// need neither keep the code they had without them.
+template <int BN, int STAGES, bool kDual, bool kPair, bool kExt>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ TcMaps maps, int M, int N, int K, int n_fast, EpiParams epi,
               int* err) {
@@ -414,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < 32; ++j) o[j] = a[j];
                     }
                 } else {
-                    epi_compute<32>(epi, row, col, a, u, o);
+                    epi_compute<32, kExt>(epi, row, col, a, u, o);
                 }
                 if (epi.tma_out && col + 32 <= N) {
                     // One bulk copy per block, issued by lane 0; a bf16 block (2 KB)
@@ -451,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // This warp takes every other chunk; a TMEM load costs only a few tens
             // of cycles, the global stores dominate, so more storing warps (not
             // deeper load pipelining) is what raises the epilogue's throughput.
-            if (epi.kind == EPI_LSE) {
+            if (kExt && epi.kind == EPI_LSE) {
                 // Fused cross-entropy: nothing is stored but, per row, the running
                 // max and sum of exp(z - max) over this warp's chunks of the tile,
                 // and the logit of the target column where the tile holds it.
@@ -590,13 +593,13 @@ int choose_block_n(int M, int N, bool dual) {
     return best;
 }
 
-template <int BN, int STAGES, bool kDual, bool kPair = false>
+template <int BN, int STAGES, bool kDual, bool kPair = false, bool kExt = false>
 cudaError_t launch_inst(const GemmPlan& p, cudaStream_t st) {
     using L = TcSmem<BN, STAGES, kPair>;
     static_assert(L::kBytes <= 232448, "shared memory budget");
     static bool attr_set = false;   // per instantiation; set once per process
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, STAGES, kDual, kPair>,
+        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, STAGES, kDual, kPair, kExt>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -607,10 +610,10 @@ cudaError_t launch_inst(const GemmPlan& p, cudaStream_t st) {
     const int slots = kPair ? sm_count() / 2 : sm_count();
     const int units = (int)(tiles < slots ? tiles : slots);
     if (kPair)
-        return launch_pdl_pair(k_gemm_tc<BN, STAGES, kDual, kPair>, dim3(2 * units), dim3(kThreads),
+        return launch_pdl_pair(k_gemm_tc<BN, STAGES, kDual, kPair, kExt>, dim3(2 * units), dim3(kThreads),
                                L::kBytes, st, p.maps, p.M, p.N, p.K, p.n_fast, p.epi,
                                device_error_word());
-    return launch_pdl(k_gemm_tc<BN, STAGES, kDual, kPair>, dim3(units), dim3(kThreads), L::kBytes,
+    return launch_pdl(k_gemm_tc<BN, STAGES, kDual, kPair, kExt>, dim3(units), dim3(kThreads), L::kBytes,
                       st, p.maps, p.M, p.N, p.K, p.n_fast, p.epi, device_error_word());
 }
 
@@ -753,19 +756,25 @@ tfm_status plan_gemm_tc(GemmPlan* plan, const void* A, int64_t lda, const void* 
     return TFM_OK;
 }
 
+template <bool kExt>
+cudaError_t launch_gemm_tc_ext(const GemmPlan& p, cudaStream_t st) {
+    if (p.pair) {
+        if (p.dual) return launch_inst<256, 6, true, true, kExt>(p, st);
+        return launch_inst<256, 6, false, true, kExt>(p, st);
+    }
+    if (p.dual) {
+        if (p.block_n == 256) return launch_inst<256, 4, true, false, kExt>(p, st);
+        return launch_inst<128, 6, true, false, kExt>(p, st);
+    }
+    if (p.block_n == 256) return launch_inst<256, 4, false, false, kExt>(p, st);
+    return launch_inst<128, 6, false, false, kExt>(p, st);
+}
+
 cudaError_t launch_gemm_tc(const GemmPlan& p, cudaStream_t st) {
     if (p.M <= 0 || p.N <= 0) return cudaSuccess;
     if (p.skinny) return launch_gemm_skinny(p, st);
-    if (p.pair) {
-        if (p.dual) return launch_inst<256, 6, true, true>(p, st);
-        return launch_inst<256, 6, false, true>(p, st);
-    }
-    if (p.dual) {
-        if (p.block_n == 256) return launch_inst<256, 4, true>(p, st);
-        return launch_inst<128, 6, true>(p, st);
-    }
-    if (p.block_n == 256) return launch_inst<256, 4, false>(p, st);
-    return launch_inst<128, 6, false>(p, st);
+    if (p.epi.bias || p.epi.kind == EPI_LSE) return launch_gemm_tc_ext<true>(p, st);
+    return launch_gemm_tc_ext<false>(p, st);
 }
 
 }  // namespace tfm
