@@ -56,19 +56,16 @@ def load_peaks():
             "source": "fallback"}
 
 
-# DRAM bytes (read + written) of one launch, from one ncu --set full capture of
-# the layer-0 launches (cold caches) of the kernels as they are now; an op
-# without an entry reports traffic null.
+# DRAM bytes (read + written) of one launch, from one ncu capture of
+# dram__bytes_read.sum + dram__bytes_write.sum (cold caches) of the first
+# forward's launches of the kernels as they are now: layer 0 for the per-layer
+# kernels, and the LM head.  An op without an entry reports traffic null.
 DRAM_TRAFFIC = {
-    ("small", "qkv_rope_gemm"): 10.07e6, ("small", "attention"): 25.18e6,
-    ("small", "oproj_residual_gemm"): 25.77e6, ("small", "gateup_swiglu_gemm"): 11.22e6,
-    ("small", "down_residual_gemm"): 40.25e6,
-    ("long", "qkv_rope_gemm"): 29.66e6, ("long", "attention"): 50.41e6,
-    ("long", "oproj_residual_gemm"): 52.50e6, ("long", "gateup_swiglu_gemm"): 30.18e6,
-    ("long", "down_residual_gemm"): 84.69e6,
-    ("gqa", "qkv_rope_gemm"): 68.69e6, ("gqa", "attention"): 50.67e6,
-    ("gqa", "oproj_residual_gemm"): 126.73e6, ("gqa", "gateup_swiglu_gemm"): 147.84e6,
-    ("gqa", "down_residual_gemm"): 230.82e6,
+    ("small", "qkv_rope_gemm"): 10.06e6, ("small", "attention"): 25.20e6,
+    ("small", "oproj_residual_gemm"): 25.76e6, ("small", "gateup_swiglu_gemm"): 11.21e6,
+    ("small", "down_residual_gemm"): 40.25e6, ("small", "lmhead_gemm"): 285.30e6,
+    ("long", "attention"): 50.41e6,
+    ("gqa", "attention"): 50.67e6,
 }
 
 
@@ -856,8 +853,9 @@ def main():
                     "cap_note": "min(1, algorithmic flop/byte x HBM copy bandwidth / tensor peak)"}
                    if "cap" in dom else {}),
                 "traffic": DRAM_TRAFFIC.get((cfg.name, dom_name)),
-                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the layer-0 "
-                                  "launch, cold caches, bytes per launch (profiles/layer0_dram_bytes.md)",
+                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the first "
+                                  "forward's launch (layer 0 for per-layer kernels), cold caches, "
+                                  "bytes per launch (profiles/layer0_dram_bytes.md)",
                 "peak_source": f"{peaks['source']} ({'bf16 burst' if dom['bound'] == 'tensor' else 'HBM copy'})",
                 "timing": "average launch duration from CUDA events recorded on the launch stream "
                           "after every kernel, over K directly launched steps run after the value region"}
