@@ -716,7 +716,8 @@ enum Kind { K_EMBED = 0, K_NORM, K_QKV, K_ATTN, K_OPROJ, K_GATEUP, K_DOWN, K_LMH
         if (run) {                                                              \
             cudaEvent_t _ev = m->next_event();                                  \
             if (!_ev) return fail(TFM_ECUDA, "cudaEventCreate failed");         \
-            cudaEventRecord(_ev, st);                                           \
+            _e = cudaEventRecord(_ev, st);                                      \
+            if (_e != cudaSuccess) return cuda_fail(_e, "cudaEventRecord");    \
             run->kinds.push_back(kind);                                         \
         }                                                                       \
     } while (0)
@@ -821,7 +822,8 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
         run = &m->runs.back();
         cudaEvent_t ev = m->next_event();
         if (!ev) return fail(TFM_ECUDA, "cudaEventCreate failed");
-        cudaEventRecord(ev, st);
+        cudaError_t re = cudaEventRecord(ev, st);
+        if (re != cudaSuccess) return cuda_fail(re, "cudaEventRecord");
     }
     // The GPT-2-style family: LayerNorm (gain, shift), position rows in the
     // embedding, post-norm blocks normalising the residual stream in place.
@@ -1051,7 +1053,8 @@ tfm_status decode_body(Model* m, const int32_t* tokens, int B, float* logits, in
         run = &m->runs.back();
         cudaEvent_t ev = m->next_event();
         if (!ev) return fail(TFM_ECUDA, "cudaEventCreate failed");
-        cudaEventRecord(ev, st);
+        cudaError_t re = cudaEventRecord(ev, st);
+        if (re != cudaSuccess) return cuda_fail(re, "cudaEventRecord");
     }
     // The GPT-2-style family: LayerNorm, the position row of the step added in
     // the embedding, post-norm blocks normalising the residual stream in place.
