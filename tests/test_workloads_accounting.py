@@ -107,3 +107,27 @@ def test_memory_caps_of_the_tensor_kernels():
     M, D = 8192, 512
     assert bench.tensor_kernel_bytes(workloads.get_config("small"), 32, 256)["oproj_residual_gemm"] == \
         M * D * 2 + D * D * 2 + 2 * M * D * 4
+
+
+def test_dram_traffic_entries_name_real_kernels_and_exceed_the_algorithmic_reads():
+    """Every ncu DRAM figure the bench may report as `traffic` names a workload
+    and a kernel kind the bench accounts for, and is at least the kernel's
+    unavoidable reads (a figure below them would belong to another launch).
+    Lower bounds: a GEMM reads A and W once; attention reads q, k and v."""
+    import bench
+    for (name, kind), traffic in bench.DRAM_TRAFFIC.items():
+        cfg = workloads.get_config(name)
+        work = bench.kernel_work(cfg, cfg.batch, cfg.seq)
+        assert kind in work, (name, kind)
+        M, D, dh = cfg.batch * cfg.seq, cfg.d_model, cfg.d_head
+        Dq, Dkv = cfg.n_head * dh, cfg.n_kv_head * dh
+        es = 2 if cfg.mode == "bf16" else 4
+        reads = {
+            "qkv_rope_gemm": M * D * es + (Dq + 2 * Dkv) * D * es,
+            "attention": M * (Dq + 2 * Dkv) * es,
+            "oproj_residual_gemm": M * Dq * es + D * Dq * es,
+            "gateup_swiglu_gemm": M * D * es + 2 * cfg.d_ff * D * es,
+            "down_residual_gemm": M * cfg.d_ff * es + D * cfg.d_ff * es,
+            "lmhead_gemm": M * D * es + cfg.vocab * D * es,
+        }
+        assert traffic >= 0.98 * reads[kind], (name, kind, traffic, reads[kind])
