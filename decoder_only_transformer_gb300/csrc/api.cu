@@ -1587,6 +1587,13 @@ tfm_status tfm_decode_attention(const void* q, const void* k_cache, const void* 
         return fail(TFM_EINVAL, "workspace too small");
     if (scale <= 0.f) scale = 1.0f / std::sqrt((float)dh);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // The position is copied from the host at call time, which a recorded graph
+    // could not replay with a new value: refuse a capturing stream up front
+    // instead of letting the capture fail.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(cs, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusActive)
+        return fail(TFM_EINVAL, "tfm_decode_attention cannot be recorded into a graph (the position "
+                                "is copied from the host at call time); use tfm_decode_step");
     int* pos_dev = static_cast<int*>(workspace);
     float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256);
     // The kernel reads the position (and prefetches cache rows) before its grid

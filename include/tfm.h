@@ -401,8 +401,9 @@ tfm_status tfm_causal_attention_window(const void* q, const void* k, const void*
  * workspace: device, 16-byte aligned, at least
  * tfm_decode_attention_workspace_bytes(B, H, max_seq, dh) bytes, not used by
  * another call in flight.  The position goes to the workspace by a small
- * host-to-device copy on `stream` (so the call is not capturable in a graph;
- * tfm_decode_step is).  TFM_EINVAL for bad sizes (0 <= pos < max_seq,
+ * host-to-device copy on `stream`, so the call cannot be recorded into a graph:
+ * on a capturing stream it returns TFM_EINVAL before enqueueing anything
+ * (tfm_decode_step can be recorded).  TFM_EINVAL for bad sizes (0 <= pos < max_seq,
  * window >= 0) or a small workspace; TFM_EUNSUPPORTED for other dh / groups. */
 size_t tfm_decode_attention_workspace_bytes(int32_t B, int32_t H, int32_t max_seq, int32_t dh);
 tfm_status tfm_decode_attention(const void* q, const void* k_cache, const void* v_cache, void* o,
