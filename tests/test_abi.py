@@ -84,3 +84,27 @@ def test_workspace_grows_with_batch(lib):
     a = tfm.workspace_bytes(_cfg(max_batch=1))
     b = tfm.workspace_bytes(_cfg(max_batch=4))
     assert b > a > 0
+
+
+def test_every_declared_function_is_documented():
+    """Each function include/tfm.h declares follows a comment (its own, or the
+    one heading a group of declarations): the header states each entry point's
+    arguments, layout, ownership and errors."""
+    import os
+    import re
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "tfm.h")
+    lines = open(path).read().split("\n")
+    undocumented = []
+    for i, line in enumerate(lines):
+        s = line.strip()
+        m = re.match(r"^(?:const\s+)?[A-Za-z_][A-Za-z0-9_ *]*\b(tfm_[a-z0-9_]+)\s*\(", s)
+        if not m or s.startswith("*") or s.startswith("//"):
+            continue
+        j = i - 1
+        while j >= 0 and lines[j].strip() and not lines[j].strip().endswith("*/") \
+                and not lines[j].strip().startswith("//"):
+            j -= 1
+        if j < 0 or not (lines[j].strip().endswith("*/") or lines[j].strip().startswith("//")):
+            undocumented.append(m.group(1))
+    assert not undocumented, undocumented
+    assert len(set(re.findall(r"\b(tfm_[a-z0-9_]+)\s*\(", "\n".join(lines)))) >= len(tfm.header_functions())
