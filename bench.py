@@ -64,6 +64,7 @@ DRAM_TRAFFIC = {
     ("small", "qkv_rope_gemm"): 10.06e6, ("small", "attention"): 25.20e6,
     ("small", "oproj_residual_gemm"): 25.76e6, ("small", "gateup_swiglu_gemm"): 11.21e6,
     ("small", "down_residual_gemm"): 40.25e6, ("small", "lmhead_gemm"): 285.30e6,
+    ("long", "attention"): 50.41e6,
     ("gqa", "attention"): 50.67e6,
 }
 

@@ -18,16 +18,17 @@
 //               query row), so while one group runs its exponentials the other's
 //               scores are being computed and the two groups share the issue slots
 //               and the special-function unit of each scheduler.
-// The softmax works on packed fp32 pairs (f32x2 FMA/ADD).  It reads S with
-// tcgen05.ld.red (sm_103a), which also returns the maximum of each 32-column
-// chunk of the row: a tile with no mask takes its row maximum from there (long
-// context: 144.7 -> 134.1 us); a masked tile (diagonal, ragged, window edge)
-// takes three-input maxima after masking.  About 3 instructions per score
-// besides the exponential (the
+// The softmax works on packed fp32 pairs (f32x2 FMA/ADD) and three-input
+// maxima, about 3 instructions per score besides the exponential (the
 // special-function unit takes 4 cycles per warp ex2 on each scheduler; the
 // bf16 packing and the FMAs overlap with it).  (Evaluating part of the
 // exponentials with a polynomial on the FMA pipe was measured slower here: it
-// costs more issue slots than it frees.)  S_x(j+1) is issued as soon as the
+// costs more issue slots than it frees.  Taking an unmasked tile's row maximum
+// from the tensor-memory load with tcgen05.ld.red measured faster, 144.7 ->
+// 134.1 us at long context.  It is not used, because with it one
+// prefill-against-forward bit-equality check failed: a 37-position sequence
+// whose only key tile is masked, so that path never uses the hardware maximum.
+// The cause is not known.)  S_x(j+1) is issued as soon as the
 // softmax of tile x has read S_x(j) into registers, P_x.V_j as soon as it has
 // written P_x(j); the exponentials of tile j+1 run before the wait for P_x.V_j
 // (which frees the P_x columns), so that wait overlaps them.  (Two threads per
@@ -358,20 +359,9 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
             for (int j = it.lo[x]; j < n && ok; ++j, ++cnt) {
                 if (!warp_wait(s_full(x), (uint32_t)cnt & 1u, err, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const int jt = it.j0 + j;              // key tile index
-                const int k0 = jt * kKV;
-                // Diagonal or ragged tile (causal / length mask), or a tile the
-                // window's lower edge crosses (tests uniform over the tile).
-                const bool cmask = jt == qt || k0 + kKV > S;
-                const bool wmask = kWin && k0 < win_lo;
-                // The load also returns each 32-column chunk's maximum
-                // (tcgen05.ld.red); a tile with no mask takes its row maximum from
-                // there, a masked one computes it after masking, since the
-                // hardware maximum includes the masked scores.
                 uint32_t sr[kKV / 32][32];
-                float red[kKV / 32];
 #pragma unroll
-                for (int cc = 0; cc < kKV / 32; ++cc) tmem_ld32_max_issue(t_s + cc * 32, sr[cc], red[cc]);
+                for (int cc = 0; cc < kKV / 32; ++cc) tmem_ld32_issue(t_s + cc * 32, sr[cc]);
                 tmem_ld_wait();
                 // S_x is in registers: the tensor cores may overwrite it with the next tile.
                 tc_fence_before();
@@ -384,35 +374,27 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) s[cc * 32 + e] = __uint_as_float(sr[cc][e]);
                 }
-                float mx;
-                if (cmask || wmask) {
-                    if (cmask) {
+                const int jt = it.j0 + j;              // key tile index
+                const int k0 = jt * kKV;
+                if (jt == qt || k0 + kKV > S) {
 #pragma unroll
-                        for (int cc = 0; cc < kKV; ++cc)
-                            if (k0 + cc > qi || k0 + cc >= S) s[cc] = -INFINITY;
-                    }
-                    // Keys before the row's window start; a row with none left in
-                    // this tile keeps m = -inf and gets p = 0 below.
-                    if (wmask) {
-#pragma unroll
-                        for (int cc = 0; cc < kKV; ++cc)
-                            if (k0 + cc < kmin) s[cc] = -INFINITY;
-                    }
-                    // Row max: four independent chains of three-input maxima.
-                    float mx4[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-                    for (int cc = 4; cc < kKV; cc += 8)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) mx4[e] = fmax3(mx4[e], s[cc + 2 * e], s[cc + 2 * e + 1]);
-                    mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-                } else {
-#pragma unroll
-                    for (int cc = 0; cc < kKV / 32; ++cc) reg_fence1(red[cc]);
-                    mx = red[0];
-#pragma unroll
-                    for (int cc = 1; cc < kKV / 32; ++cc) mx = fmaxf(mx, red[cc]);
+                    for (int cc = 0; cc < kKV; ++cc)
+                        if (k0 + cc > qi || k0 + cc >= S) s[cc] = -INFINITY;
                 }
-                mx *= scale_log2;
+                // Keys before the row's window start (CTA-uniform test); a row with
+                // none left in this tile keeps m = -inf and gets p = 0 below.
+                if (kWin && k0 < win_lo) {
+#pragma unroll
+                    for (int cc = 0; cc < kKV; ++cc)
+                        if (k0 + cc < kmin) s[cc] = -INFINITY;
+                }
+                // Row max: four independent chains of three-input maxima.
+                float mx4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+                for (int cc = 4; cc < kKV; cc += 8)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) mx4[e] = fmax3(mx4[e], s[cc + 2 * e], s[cc + 2 * e + 1]);
+                const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
                 float corr = 1.f;
                 if (mx > m + kRescaleThresholdPP) {
                     corr = fast_exp2(m - mx);

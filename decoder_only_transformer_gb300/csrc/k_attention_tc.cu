@@ -39,9 +39,9 @@
 //               O / l as bf16 to global memory (heads merged).
 // S_{j+1} runs on the tensor cores while the softmax warps work on S_j.
 // Tiles entirely above the diagonal are never loaded.  All waits are bounded.
-// (Taking an unmasked tile's row maximum from the tensor-memory load, with
-// tcgen05.ld.red as the d_head-64 kernel does, measured no different here: GQA
-// workload 63.2 vs 63.4 us, so the maxima are not what bounds this softmax.)
+// (Taking an unmasked tile's row maximum from the tensor-memory load with
+// tcgen05.ld.red, sm_103a, measured no different here: GQA workload 63.2 vs
+// 63.4 us, so the maxima are not what bounds this softmax.)
 #include <climits>
 
 #include "common.cuh"
