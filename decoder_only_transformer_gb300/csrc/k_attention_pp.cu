@@ -28,7 +28,10 @@
 // 134.1 us at long context.  It is not used, because with it one
 // prefill-against-forward bit-equality check failed: a 37-position sequence
 // whose only key tile is masked, so that path never uses the hardware maximum.
-// The cause is not known.)  S_x(j+1) is issued as soon as the
+// The likely cause: on that path the load's maximum outputs were dead while the
+// asynchronous load could still write them, so their registers may have been
+// reused meanwhile.  Every destination of an asynchronous load has to stay live
+// until its wait.)  S_x(j+1) is issued as soon as the
 // softmax of tile x has read S_x(j) into registers, P_x.V_j as soon as it has
 // written P_x(j); the exponentials of tile j+1 run before the wait for P_x.V_j
 // (which frees the P_x columns), so that wait overlaps them.  (Two threads per

@@ -173,6 +173,10 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 uint32_t v[32];
                 tmem_ld32_issue(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), v);
                 tmem_ld_wait();
+                // All 32 destinations stay live until the wait: the load writes
+                // them asynchronously, so a register the compiler saw as dead
+                // (columns past NM) must not be handed to another value meanwhile.
+                reg_fence32(v);
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                     if (c * 32 + j < NM && c * 32 + j < M) part[(c * 32 + j) * 128 + r] = __uint_as_float(v[j]);
