@@ -314,6 +314,143 @@ def test_gqa_model_equals_mha_model_with_replicated_kv_weights():
     assert np.allclose(oracle.forward(tok, w, cfg), oracle.forward(tok, w_mha, mha_cfg), atol=1e-13)
 
 
+# ---------------------------------------------------------------- attention block assembly
+# The functions below the block (rope, causal_attention, rmsnorm, swiglu) have their
+# own pins; these check how multihead_self_attention and transformer_block put them
+# together: which tensors RoPE turns, which gain feeds which branch, how heads split.
+
+def _block_case(seed=11, H=4, Hkv=2, D=32, S=7, F=24):
+    cfg = workloads.get_config("tiny").replace(d_model=D, n_head=H, n_kv_head=Hkv, d_ff=F, n_layer=1)
+    rng = np.random.default_rng(seed)
+    dh = D // H
+    layer = {
+        "attn_norm": rng.uniform(0.5, 1.5, D), "ffn_norm": rng.uniform(0.5, 1.5, D),
+        "wq": rng.standard_normal((H * dh, D)) * 0.3, "wk": rng.standard_normal((Hkv * dh, D)) * 0.3,
+        "wv": rng.standard_normal((Hkv * dh, D)) * 0.3, "wo": rng.standard_normal((D, H * dh)) * 0.3,
+        "w1": rng.standard_normal((F, D)) * 0.3, "w3": rng.standard_normal((F, D)) * 0.3,
+        "w2": rng.standard_normal((D, F)) * 0.3,
+    }
+    u = rng.standard_normal((1, S, D))
+    return cfg, layer, u
+
+
+def test_block_attention_depends_only_on_relative_positions():
+    """RoPE turns q and k by their absolute positions, so q.k depends only on the
+    offset n - m ([CS336-B] 7; [LLM2] RoPE): shifting every position by c leaves
+    the attention output unchanged.  Rotating v as well, or leaving k (or q)
+    unrotated, makes the output depend on c."""
+    cfg, layer, u = _block_case()
+    S = u.shape[1]
+    pos = np.arange(S, dtype=float)[None, :]
+    base = oracle.multihead_self_attention(u, layer, cfg, pos)
+    for c in (1.0, 5.0, 37.0, 1000.0):
+        shifted = oracle.multihead_self_attention(u, layer, cfg, pos + c)
+        assert np.allclose(shifted, base, atol=1e-11, rtol=0), c
+
+
+def test_block_attention_sees_the_order_of_earlier_positions():
+    """Without any rotation attention is a function of the set of earlier rows; with
+    RoPE on q and k, swapping two earlier rows changes a later output.  Fails if the
+    rotation is dropped from both q and k (or given position 0 everywhere)."""
+    cfg, layer, u = _block_case(seed=12)
+    S = u.shape[1]
+    pos = np.arange(S, dtype=float)[None, :]
+    base = oracle.multihead_self_attention(u, layer, cfg, pos)
+    swapped = u.copy()
+    swapped[:, [0, 1]] = u[:, [1, 0]]
+    other = oracle.multihead_self_attention(swapped, layer, cfg, pos)
+    assert np.abs(other[:, S - 1] - base[:, S - 1]).max() > 1e-4
+    # and a layer whose q and k projections are zero is order-blind (scores all 0)
+    flat = dict(layer, wq=np.zeros_like(layer["wq"]))
+    a = oracle.multihead_self_attention(u, flat, cfg, pos)
+    b = oracle.multihead_self_attention(swapped, flat, cfg, pos)
+    assert np.allclose(a[:, 2:], b[:, 2:], atol=1e-13)
+
+
+def test_block_attention_with_zero_queries_is_prefix_mean_of_values():
+    """Wq = 0 makes every score 0, so each head returns the running mean of its
+    kv head's value rows, unrotated (the target's "uniform scores return the
+    prefix mean of V"); the block output is that mean through Wo."""
+    cfg, layer, u = _block_case(seed=13)
+    S, H, Hkv, dh = u.shape[1], cfg.n_head, cfg.n_kv_head, cfg.d_head
+    layer = dict(layer, wq=np.zeros_like(layer["wq"]))
+    pos = np.arange(S, dtype=float)[None, :]
+    got = oracle.multihead_self_attention(u, layer, cfg, pos)
+    v = u[0] @ layer["wv"].T                                   # [S, Hkv*dh]
+    mean = np.cumsum(v, axis=0) / np.arange(1, S + 1)[:, None]
+    # query head h takes kv head h // (H / Hkv)
+    o = np.concatenate([mean[:, (h // (H // Hkv)) * dh:(h // (H // Hkv) + 1) * dh] for h in range(H)], axis=1)
+    assert np.allclose(got[0], o @ layer["wo"].T, atol=1e-12)
+
+
+def test_block_attention_matches_per_head_scalar_loops():
+    """The assembled attention (head split, RoPE on q and k, GQA map, merge, output
+    projection) against scalar loops over positions, heads and coordinates on a
+    tiny shape, written from the definitions: head h owns columns [h*dh, (h+1)*dh)
+    of q ([CS336-A] 5.4 多头注意力), pair (2i, 2i+1) turns by s*theta^(-2i/dh)."""
+    cfg, layer, u = _block_case(seed=14, H=4, Hkv=2, D=16, S=5, F=8)
+    S, D, H, Hkv, dh = u.shape[1], cfg.d_model, cfg.n_head, cfg.n_kv_head, cfg.d_head
+    theta = cfg.rope_theta
+
+    def proj(W, s, row):
+        return sum(W[row, d] * u[0, s, d] for d in range(D))
+
+    def rotated(W, head, s):
+        x = [proj(W, s, head * dh + e) for e in range(dh)]
+        out = list(x)
+        for i in range(dh // 2):
+            a = s * theta ** (-2.0 * i / dh)
+            out[2 * i] = x[2 * i] * math.cos(a) - x[2 * i + 1] * math.sin(a)
+            out[2 * i + 1] = x[2 * i] * math.sin(a) + x[2 * i + 1] * math.cos(a)
+        return out
+
+    merged = np.zeros((S, H * dh))
+    for h in range(H):
+        g = h * Hkv // H
+        for i in range(S):
+            qi = rotated(layer["wq"], h, i)
+            sc = []
+            for j in range(i + 1):
+                kj = rotated(layer["wk"], g, j)
+                sc.append(sum(qi[e] * kj[e] for e in range(dh)) / math.sqrt(dh))
+            mx = max(sc)
+            p = [math.exp(x - mx) for x in sc]
+            z = sum(p)
+            for e in range(dh):
+                merged[i, h * dh + e] = sum(p[j] / z * proj(layer["wv"], j, g * dh + e) for j in range(i + 1))
+    want = np.array([[sum(layer["wo"][n, c] * merged[i, c] for c in range(H * dh)) for n in range(D)]
+                     for i in range(S)])
+    got = oracle.multihead_self_attention(u, layer, cfg, np.arange(S, dtype=float)[None, :])
+    assert np.allclose(got[0], want, atol=1e-12)
+
+
+def test_block_norm_gains_feed_their_own_branch():
+    """Pre-norm block ([CS336-A] 5.7): attn_norm scales the attention input and
+    ffn_norm the SwiGLU input.  With Wo = 0 the block cannot depend on attn_norm,
+    with W2 = 0 it cannot depend on ffn_norm; each gain does move the block when
+    its branch is live."""
+    cfg, layer, u = _block_case(seed=15)
+    S = u.shape[1]
+    pos = np.arange(S, dtype=float)[None, :]
+    rng = np.random.default_rng(16)
+
+    def run(**kw):
+        return oracle.transformer_block(u, dict(layer, **kw), cfg, pos)
+
+    g_a, g_f = rng.uniform(0.5, 1.5, cfg.d_model), rng.uniform(0.5, 1.5, cfg.d_model)
+    zo, z2 = np.zeros_like(layer["wo"]), np.zeros_like(layer["w2"])
+    assert np.allclose(run(wo=zo), run(wo=zo, attn_norm=g_a), atol=1e-13)
+    assert np.allclose(run(w2=z2), run(w2=z2, ffn_norm=g_f), atol=1e-13)
+    assert np.abs(run(w2=z2) - run(w2=z2, attn_norm=g_a)).max() > 1e-4
+    assert np.abs(run(wo=zo) - run(wo=zo, ffn_norm=g_f)).max() > 1e-4
+    # the SwiGLU branch reads the residual after the attention add (x + Attn), not x
+    u2 = oracle.rmsnorm(u, layer["attn_norm"], cfg.norm_eps)
+    x1 = u + oracle.multihead_self_attention(u2, layer, cfg, pos)
+    want = x1 + oracle.swiglu(oracle.rmsnorm(x1, layer["ffn_norm"], cfg.norm_eps),
+                              layer["w1"], layer["w3"], layer["w2"])
+    assert np.allclose(run(), want, atol=1e-13)
+
+
 def test_param_count_formula():
     g = GOLD["param_counts"]
     c = g["cs336b"]
