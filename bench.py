@@ -5,7 +5,8 @@ kernel of the path: embedding fused with the first RMSNorm, 2L more RMSNorms, L 
 attention, output projection + residual, gate/up + SwiGLU, down + residual],
 LM head).  Prints one JSON line.
 
-  python bench.py [--config small] [--steps K] [--warmup W] [--gpus N] [--impl ours|reference]
+  python bench.py [--config gqa] [--also long,small] [--steps K] [--warmup W] [--gpus N]
+                  [--impl ours|reference]
 
 Inputs are seeded synthetic weights and tokens of the workload's shapes,
 resident in HBM before timing.  Each timed step is bracketed by CUDA events on
@@ -602,7 +603,11 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="small", choices=list(workloads.CONFIGS))
+    ap.add_argument("--config", default="gqa", choices=list(workloads.CONFIGS),
+                    help="the workload of the headline line (default: gqa, the largest)")
+    ap.add_argument("--also", default="long,small",
+                    help="comma-separated further workloads measured the same way on rank 0 and "
+                         "reported under other_workloads (empty: none)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -683,6 +688,162 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def roofline_of(cfg, kernels, peaks):
+    """The roofline object of a workload's dominant kernel (largest share of the
+    profiled step)."""
+    dom_name = max(kernels, key=lambda k: kernels[k]["share"])
+    dom = kernels[dom_name]
+    return {"kernel": dom_name, "bound": dom["bound"], "achieved": dom["achieved"],
+            "peak": peaks["bf16_tflops"] if dom["bound"] == "tensor" else peaks["hbm_gbs"],
+            "unit": dom["unit"], "frac": dom["frac"],
+            **({"cap": dom["cap"], "frac_of_cap": dom["frac_of_cap"],
+                "cap_note": "min(1, algorithmic flop/byte x HBM copy bandwidth / tensor peak)"}
+               if "cap" in dom else {}),
+            "traffic": DRAM_TRAFFIC.get((cfg.name, dom_name)),
+            "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch of "
+                              "this kernel in the first forward (layer 0 for per-layer kernels), "
+                              "cold caches, bytes per launch; null where the kernel changed since "
+                              "the capture",
+            "peak_source": f"{peaks['source']} "
+                           f"({'bf16 burst' if dom['bound'] == 'tensor' else 'HBM copy'})",
+            "timing": "average launch duration from CUDA events recorded on the launch stream "
+                      "after every kernel, over K directly launched steps run after the value "
+                      "region"}
+
+
+def measure_workload(tfm, torch, cfg, tok_np, stream, flush, steps, warmup, graph, dist, world,
+                     do_e2e):
+    """Time `steps` forwards of one workload (device time, CUDA events on the
+    launch stream around each forward, L2 flushed between steps), then the same
+    number of directly launched forwards with an event after every kernel (the
+    per-kernel table), then the end-to-end rate through the host-buffer entry
+    point.  Returns (result, model, tokens, logits); the caller closes the model."""
+    B, S = tok_np.shape
+    M = B * S
+    w = workloads.make_weights(cfg)
+    mat = torch.bfloat16 if cfg.mode == "bf16" else torch.float32
+
+    def conv(key, a):
+        return torch.from_numpy(a).to(torch.float32 if key.endswith("norm") else mat).cuda()
+
+    tw = {k: conv(k, w[k]) for k in ("embed", "final_norm", "lm_head")}
+    tw["layers"] = [{k: conv(k, v) for k, v in layer.items()} for layer in w["layers"]]
+    model = tfm.Model(cfg)
+    model.load_weights(tw)
+    del tw
+    ld = (cfg.vocab + 3) // 4 * 4
+    tokens = torch.from_numpy(tok_np).cuda()
+    logits = torch.empty(M, ld, device="cuda")
+    run = model.forward_graph if graph else model.forward
+    for _ in range(max(warmup, 3)):
+        run(tokens, logits)
+        flush.zero_()
+    torch.cuda.synchronize()
+    tfm.device_status()
+
+    # ---- timed region: exactly K steps, device time of each forward
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(steps):
+        starts[i].record(stream)
+        run(tokens, logits)
+        ends[i].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t_wall1 = time.time()
+    tfm.device_status()
+    total_ms = sum(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends))
+
+    # ---- per-kernel durations: K more steps launched directly with an event
+    # after every kernel (events between kernels prevent graph replay and launch
+    # overlap, so this region is kept apart from the one that gives `value`)
+    model.profile(True)
+    for _ in range(steps):
+        model.forward(tokens, logits)
+        flush.zero_()
+    torch.cuda.synchronize()
+    model.profile(False)
+    prof = model.profile_read()
+    tfm.device_status()
+    total_ms = max_over_ranks(total_ms, dist, "cuda")
+    ms_per_step = total_ms / steps
+    value = job_rate(world, M, steps, total_ms)
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if do_e2e:
+        # Every step copies its tokens host->device, runs the forward and copies
+        # all fp32 logits device->host; tfm_forward_host_async puts the logits
+        # copy on the handle's copy stream, where it overlaps the next step's
+        # forward (two device logits buffers taken in turn), and the join makes
+        # the launch stream wait for the last copies before the closing event.
+        h_tok = torch.from_numpy(tok_np).pin_memory()
+        h_logits = [torch.empty(M, ld, dtype=torch.float32).pin_memory() for _ in range(2)]
+        for i in range(2):
+            model.forward_host_async(h_tok, h_logits[i], stream)
+        model.forward_host_join(stream)
+        torch.cuda.synchronize()
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        if dist:
+            dist.barrier()
+        es[0].record(stream)
+        for i in range(steps):
+            model.forward_host_async(h_tok, h_logits[i % 2], stream)
+        model.forward_host_join(stream)
+        es[1].record(stream)
+        torch.cuda.synchronize()
+        tfm.device_status()
+        e2e_ms = es[0].elapsed_time(es[1])
+        e2e_ms = max_over_ranks(e2e_ms, dist, "cuda")
+        e2e = {"value": job_rate(world, M, steps, e2e_ms), "unit": UNIT,
+               "h2d_bytes_per_step": M * 4,
+               # rows copied as one block when the host stride is round_up(vocab, 4)
+               "d2h_bytes_per_step": M * (ld if ld == (cfg.vocab + 3) // 4 * 4 else cfg.vocab) * 4,
+               "how": "tfm_forward_host_async every step (tokens host->device and the "
+                      "recorded forward on the launch stream, all fp32 logits device->host "
+                      "on the handle's copy stream, overlapping the next step's forward), "
+                      "joined after the last step; CUDA events around all K steps, inputs "
+                      "from pinned host memory every step (no L2 flush in this region)"}
+        del h_tok, h_logits
+    peaks = load_peaks()
+    kernels = kernel_table(cfg, B, S, prof, peaks)
+    gemm_attn = {k: v for k, v in kernels.items() if v["bound"] == "tensor"}
+    ms_t = sum(prof[k][0] for k in gemm_attn)
+    fl_t = sum(kernel_work(cfg, B, S)[k][1] * prof[k][1] for k in gemm_attn)
+    total_flops = accounting.forward_flops(cfg.vocab, cfg.d_model, cfg.n_layer, cfg.n_head,
+                                           cfg.d_ff, S, B, cfg.n_kv_head, causal=True)["total"]
+    res = {"value": value, "unit": UNIT, "ms_per_step": ms_per_step, "steps": steps,
+           "window_s": t_wall1 - t_wall0,
+           "roofline": roofline_of(cfg, kernels, peaks),
+           "tensor_path": {"achieved_tflops": round(fl_t / (ms_t / 1e3) / 1e12, 1) if ms_t else None,
+                           "frac": round(fl_t / (ms_t / 1e3) / 1e12 / peaks["bf16_tflops"], 4)
+                           if ms_t else None,
+                           "whole_forward_tflops": round(total_flops / (ms_per_step / 1e3) / 1e12, 1)},
+           "kernels": kernels, "e2e": e2e, "weights": w}
+    return res, model, tokens, logits
+
+
+def cpu_baseline_of(cfg, w, tok_np, budget_s):
+    rate, sample, secs = oracle_rate(cfg, w, tok_np, budget_s=budget_s)
+    return {"value": rate, "unit": UNIT, "cores": int(os.environ["OPENBLAS_NUM_THREADS"]),
+            "kind": "oracle", "sample": sample + f", {secs:.1f} s"}
+
+
+def workload_config(cfg, world, graph):
+    return {"workload": WORKLOAD_TEXT[cfg.name], "global_batch": cfg.batch * world,
+            "seq_len": cfg.seq,
+            "parallelism": f"replicas x{world} (independent batches, no collective)",
+            "l2": "flushed between timed steps (512 MiB write)",
+            "launch": "CUDA graph replay of the recorded forward (tfm_forward_graph)" if graph
+                      else "direct launches"}
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup()
@@ -701,47 +862,38 @@ def main():
 
     cfg = workloads.get_config(args.config)
     B, S = cfg.batch, cfg.seq
-    M = B * S
-    w = workloads.make_weights(cfg)
     tok_np = rank_tokens(cfg, rank)
     bf = cfg.mode == "bf16"
-    mat = torch.bfloat16 if bf else torch.float32
-
-    def conv(key, a):
-        return torch.from_numpy(a).to(torch.float32 if key.endswith("norm") else mat).cuda()
-
-    tw = {k: conv(k, w[k]) for k in ("embed", "final_norm", "lm_head")}
-    tw["layers"] = [{k: conv(k, v) for k, v in layer.items()} for layer in w["layers"]]
-    model = tfm.Model(cfg)
-    model.load_weights(tw)
-    del tw
-    ld = (cfg.vocab + 3) // 4 * 4
-    tokens = torch.from_numpy(tok_np).cuda()
-    logits = torch.empty(M, ld, device="cuda")
     flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
     # A stream of our own: the recorded (graph) forward cannot use the legacy default stream.
     stream = torch.cuda.Stream()
     torch.cuda.set_stream(stream)
-    run = model.forward if args.no_graph else model.forward_graph
+    graph = not args.no_graph
     if args.window_only:
         print(json.dumps({"window": window_rate(tfm, torch, stream, flush, load_peaks())}))
-        model.close()
         return
     if args.gpt2_only:
         print(json.dumps({"gpt2_family": gpt2_rate(tfm, torch, stream, flush, load_peaks(),
                                                    steps=args.steps)}))
-        model.close()
         return
-    if args.loss_only:
-        print(json.dumps({"loss": loss_rate(tfm, torch, model, cfg, tok_np, logits, stream, flush,
-                                            load_peaks(), steps=args.steps),
-                          "config": {"workload": WORKLOAD_TEXT[cfg.name]}}))
-        model.close()
-        return
-    if args.decode_only:
-        peaks = load_peaks()
-        print(json.dumps({"decode": decode_rate(tfm, torch, model, cfg, tok_np, stream, peaks),
-                          "config": {"workload": WORKLOAD_TEXT[cfg.name]}}))
+    if args.loss_only or args.decode_only:
+        w = workloads.make_weights(cfg)
+        mat = torch.bfloat16 if bf else torch.float32
+        conv = lambda key, a: torch.from_numpy(a).to(torch.float32 if key.endswith("norm")
+                                                     else mat).cuda()
+        tw = {k: conv(k, w[k]) for k in ("embed", "final_norm", "lm_head")}
+        tw["layers"] = [{k: conv(k, v) for k, v in layer.items()} for layer in w["layers"]]
+        model = tfm.Model(cfg)
+        model.load_weights(tw)
+        del tw
+        logits = torch.empty(B * S, (cfg.vocab + 3) // 4 * 4, device="cuda")
+        if args.loss_only:
+            out = {"loss": loss_rate(tfm, torch, model, cfg, tok_np, logits, stream, flush,
+                                     load_peaks(), steps=args.steps)}
+        else:
+            out = {"decode": decode_rate(tfm, torch, model, cfg, tok_np, stream, load_peaks())}
+        out["config"] = {"workload": WORKLOAD_TEXT[cfg.name]}
+        print(json.dumps(out))
         model.close()
         return
 
@@ -749,150 +901,70 @@ def main():
     sampler = ClockSampler(int(vis.split(",")[local]) if vis and vis.split(",")[local].isdigit()
                            else local)
     sampler.start()
-    for _ in range(max(args.warmup, 3)):
-        run(tokens, logits)
-        flush.zero_()
-    torch.cuda.synchronize()
-    tfm.device_status()
-
-    # ---- timed region: exactly K steps, device time of each forward
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_wall0 = time.time()
-    for i in range(args.steps):
-        starts[i].record(stream)
-        run(tokens, logits)
-        ends[i].record(stream)
-        flush.zero_()
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    t_wall1 = time.time()
-    tfm.device_status()
-    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
-
-    # ---- per-kernel durations: K more steps launched directly with an event
-    # after every kernel (events between kernels prevent graph replay and launch
-    # overlap, so this region is kept apart from the one that gives `value`)
-    model.profile(True)
-    for i in range(args.steps):
-        model.forward(tokens, logits)
-        flush.zero_()
-    torch.cuda.synchronize()
-    model.profile(False)
-    prof = model.profile_read()
-    tfm.device_status()
-    total_ms = max_over_ranks(total_ms, dist, "cuda")
-    ms_per_step = total_ms / args.steps
-    value = job_rate(world, M, args.steps, total_ms)
-
-    # ---- end to end through the C ABI with host buffers
-    e2e = None
-    if not args.no_e2e:
-        # Every step copies its tokens host->device, runs the forward and copies
-        # all fp32 logits device->host; tfm_forward_host_async puts the logits
-        # copy on the handle's copy stream, where it overlaps the next step's
-        # forward (two device logits buffers taken in turn), and the join makes
-        # the launch stream wait for the last copies before the closing event.
-        h_tok = torch.from_numpy(tok_np).pin_memory()
-        h_logits = [torch.empty(M, ld, dtype=torch.float32).pin_memory() for _ in range(2)]
-        for i in range(2):
-            model.forward_host_async(h_tok, h_logits[i], stream)
-        model.forward_host_join(stream)
-        torch.cuda.synchronize()
-        es = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        if dist:
-            dist.barrier()
-        es[0].record(stream)
-        for i in range(args.steps):
-            model.forward_host_async(h_tok, h_logits[i % 2], stream)
-        model.forward_host_join(stream)
-        es[1].record(stream)
-        torch.cuda.synchronize()
-        tfm.device_status()
-        e2e_ms = es[0].elapsed_time(es[1])
-        e2e_ms = max_over_ranks(e2e_ms, dist, "cuda")
-        e2e = {"value": job_rate(world, M, args.steps, e2e_ms), "unit": UNIT,
-               "h2d_bytes_per_step": M * 4,
-               # rows copied as one block when the host stride is round_up(vocab, 4)
-               "d2h_bytes_per_step": M * (ld if ld == (cfg.vocab + 3) // 4 * 4 else cfg.vocab) * 4,
-               "how": "tfm_forward_host_async every step (tokens host->device and the "
-                      "recorded forward on the launch stream, all fp32 logits device->host "
-                      "on the handle's copy stream, overlapping the next step's forward), "
-                      "joined after the last step; CUDA events around all K steps, inputs "
-                      "from pinned host memory every step (no L2 flush in this region)"}
+    head, model, _, logits = measure_workload(tfm, torch, cfg, tok_np, stream, flush, args.steps,
+                                              args.warmup, graph, dist, world, not args.no_e2e)
+    w = head.pop("weights")
     rms = rmsnorm_hbm(tfm, torch, stream, load_peaks()) if rank == 0 else None
     decode = (decode_rate(tfm, torch, model, cfg, tok_np, stream, load_peaks())
-              if rank == 0 and cfg.mode == "bf16" and not args.no_decode else None)
+              if rank == 0 and bf and not args.no_decode else None)
     lossr = (loss_rate(tfm, torch, model, cfg, tok_np, logits, stream, flush, load_peaks())
              if rank == 0 and not args.no_loss else None)
+    model.close()
+    del logits
     g2 = (gpt2_rate(tfm, torch, stream, flush, load_peaks())
           if rank == 0 and not args.no_gpt2 else None)
     winr = (window_rate(tfm, torch, stream, flush, load_peaks())
-            if rank == 0 and not args.no_window and cfg.mode == "bf16" else None)
+            if rank == 0 and not args.no_window and bf else None)
+    # The other full-size workloads, each timed the same way (its own K steps,
+    # per-kernel table, end to end, an oracle sample) on rank 0.
+    extra = {}
+    if rank == 0 and args.also:
+        for name in [n for n in args.also.split(",") if n and n != cfg.name]:
+            xcfg = workloads.get_config(name)
+            xtok = workloads.make_tokens(xcfg)
+            res, xmodel, _, _ = measure_workload(tfm, torch, xcfg, xtok, stream, flush,
+                                                 args.steps, args.warmup, graph, None, 1,
+                                                 not args.no_e2e)
+            xmodel.close()
+            xw = res.pop("weights")
+            res.pop("window_s")
+            res["config"] = workload_config(xcfg, 1, graph)
+            res["dtype"] = "bf16" if xcfg.mode == "bf16" else "f32"
+            res["gpu_launches"] = (2 + 7 * xcfg.n_layer) * args.steps
+            if world == 1 and not args.no_cpu_baseline:
+                res["cpu_baseline"] = cpu_baseline_of(xcfg, xw, xtok, 8.0)
+            extra[name] = res
     rows = sampler.stop()
     clocks = ClockSampler.summary(rows)
-    clocks["window_s"] = round(t_wall1 - t_wall0, 3)
+    clocks["window_s"] = round(head.pop("window_s"), 3)
 
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return
 
-    peaks = load_peaks()
-    kernels = kernel_table(cfg, B, S, prof, peaks)
-    dom_name = max(kernels, key=lambda k: kernels[k]["share"])
-    dom = kernels[dom_name]
-    roofline = {"kernel": dom_name, "bound": dom["bound"], "achieved": dom["achieved"],
-                "peak": peaks["bf16_tflops"] if dom["bound"] == "tensor" else peaks["hbm_gbs"],
-                "unit": dom["unit"], "frac": dom["frac"],
-                **({"cap": dom["cap"], "frac_of_cap": dom["frac_of_cap"],
-                    "cap_note": "min(1, algorithmic flop/byte x HBM copy bandwidth / tensor peak)"}
-                   if "cap" in dom else {}),
-                "traffic": DRAM_TRAFFIC.get((cfg.name, dom_name)),
-                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the first "
-                                  "forward's launch (layer 0 for per-layer kernels), cold caches, "
-                                  "bytes per launch (profiles/layer0_dram_bytes.md)",
-                "peak_source": f"{peaks['source']} ({'bf16 burst' if dom['bound'] == 'tensor' else 'HBM copy'})",
-                "timing": "average launch duration from CUDA events recorded on the launch stream "
-                          "after every kernel, over K directly launched steps run after the value region"}
-    gemm_attn = {k: v for k, v in kernels.items() if v["bound"] == "tensor"}
-    ms_t = sum(prof[k][0] for k in gemm_attn)
-    fl_t = sum(kernel_work(cfg, B, S)[k][1] * prof[k][1] for k in gemm_attn)
-    total_flops = accounting.forward_flops(cfg.vocab, cfg.d_model, cfg.n_layer, cfg.n_head,
-                                           cfg.d_ff, S, B, cfg.n_kv_head, causal=True)["total"]
-
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        rate, sample, secs = oracle_rate(cfg, w, tok_np, budget_s=12.0)
-        cpu = {"value": rate, "unit": UNIT, "cores": int(os.environ["OPENBLAS_NUM_THREADS"]),
-               "kind": "oracle", "sample": sample + f", {secs:.1f} s"}
+        cpu = cpu_baseline_of(cfg, w, tok_np, 12.0)
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf else "f32",
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if bf else "f32",
         "data": "synthetic (seeded N(0,0.02) weights, token ids of the workload's distribution)",
-        "config": {"workload": WORKLOAD_TEXT[cfg.name], "global_batch": B * world, "seq_len": S,
-                   "parallelism": f"replicas x{world} (independent batches, no collective)",
-                   "l2": "flushed between timed steps (512 MiB write)",
-                   "launch": "direct launches" if args.no_graph else
-                             "CUDA graph replay of the recorded forward (tfm_forward_graph)"},
-        "roofline": roofline,
-        "tensor_path": {"achieved_tflops": round(fl_t / (ms_t / 1e3) / 1e12, 1) if ms_t else None,
-                        "frac": round(fl_t / (ms_t / 1e3) / 1e12 / peaks["bf16_tflops"], 4) if ms_t else None,
-                        "whole_forward_tflops": round(total_flops / (ms_per_step / 1e3) / 1e12, 1)},
-        "kernels": kernels,
+        "config": workload_config(cfg, world, graph),
+        "roofline": head["roofline"],
+        "tensor_path": head["tensor_path"],
+        "kernels": head["kernels"],
         "rmsnorm_hbm": rms,
         "decode": decode,
         "loss": lossr,
         "gpt2_family": g2,
         "window": winr,
+        "other_workloads": extra or None,
         "cpu_baseline": cpu,
-        "e2e": e2e,
+        "e2e": head["e2e"],
         "gpu_launches": (2 + 7 * cfg.n_layer) * args.steps,
         "clocks": clocks,
     }

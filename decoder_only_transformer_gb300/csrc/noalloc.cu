@@ -3,13 +3,13 @@
 //
 // tfm_swiglu keeps the hidden activation silu(x W1^T) * (x W3^T), an [M, F]
 // matrix, in a workspace the caller allocates.  Some callers cannot allocate
-// device memory at the point where they want to run the block: code being
-// recorded into a CUDA graph (cudaMalloc is not a stream operation and is not
-// allowed during capture), plugins running under a host framework that owns
-// the device allocator, and deployments with a fixed memory budget decided at
-// start-up.  tfm_swiglu_noalloc gives them the same computation with the
-// hidden activation in a fixed array that the library declares in device
-// memory; it calls no allocator at all.
+// device memory at the point where they want to run the block: plugins running
+// under a host framework that owns the device allocator (and may have handed
+// all of the memory to its own pool), and deployments whose device memory is
+// budgeted once at start-up, where a later cudaMalloc would fail or break the
+// budget.  tfm_swiglu_noalloc gives them the same computation with the hidden
+// activation in a fixed array that the library declares in device memory; it
+// calls no allocator at all.
 //
 // The array is kSwigluScratchBytes (16 MiB) per device, reserved on every GPU
 // that loads the library until the process exits.  Every call shares it and
@@ -66,8 +66,13 @@ size_t tfm_swiglu_noalloc_max_bytes(void) { return kSwigluScratchBytes; }
 tfm_status tfm_swiglu_noalloc(const void* x, const void* w1, const void* w3, const void* w2,
                               float* y, int64_t M, int32_t D, int32_t F, int32_t accumulate,
                               int32_t mode, void* stream) {
+    if (M < 0 || F < 1) {
+        snprintf(t_msg, sizeof t_msg, "tfm_swiglu_noalloc: bad sizes M=%lld F=%d", (long long)M, (int)F);
+        tfm::set_last_error(t_msg);
+        return TFM_EINVAL;
+    }
     const size_t need = tfm_swiglu_workspace_bytes(M, F, mode);
-    if (M < 0 || F < 1 || need > kSwigluScratchBytes) {
+    if (need > kSwigluScratchBytes) {
         snprintf(t_msg, sizeof t_msg,
                  "tfm_swiglu_noalloc: M*F activation of %zu bytes exceeds the %zu-byte scratch array",
                  need, kSwigluScratchBytes);

@@ -434,19 +434,20 @@ size_t tfm_swiglu_workspace_bytes(int64_t M, int32_t F, int32_t mode);
 /* tfm_swiglu for callers that cannot allocate device memory.  The tutorial
  * pages have no counterpart: this is a deployment convenience of the library.
  *
- * Who needs it: code being recorded into a CUDA graph (cudaMalloc is not a
- * stream operation and cannot be captured), plugins running inside a host
- * framework that owns the device allocator, and deployments whose device
- * memory is budgeted once at start-up.  Arguments and results are those of
+ * Who needs it: plugins running inside a host framework that owns the device
+ * allocator (and may have given all free memory to its own pool), and
+ * deployments whose device memory is budgeted once at start-up, where a later
+ * cudaMalloc would fail or break the budget.  Arguments and results are those of
  * tfm_swiglu without the workspace: the [M, F] hidden activation lives in a
  * fixed array the library declares in device memory, of
  * tfm_swiglu_noalloc_max_bytes() bytes (16 MiB) per device, held on every GPU
  * that loads the library until the process exits.  A call whose activation
- * (tfm_swiglu_workspace_bytes(M, F, mode)) does not fit returns TFM_EINVAL.
+ * (tfm_swiglu_workspace_bytes(M, F, mode)) does not fit, or M < 0 or F < 1,
+ * returns TFM_EINVAL.
  * No allocator is called, not even on the first call; that first call on each
  * device looks up the array's device address (cudaGetSymbolAddress) with that
- * device current, so make it before any stream capture that should contain
- * the call.  All calls share the array and it keeps the last call's contents
+ * device current; make that first call before any stream capture begins.
+ * All calls share the array and it keeps the last call's contents
  * (nothing needs clearing: each call overwrites every entry it reads); calls
  * whose kernels overlap on the GPU race on it, so order them on one stream. */
 tfm_status tfm_swiglu_noalloc(const void* x, const void* w1, const void* w3, const void* w2,

@@ -38,14 +38,67 @@ def argmax_agreement(got, ref) -> float:
 
 def tie_aware_agreement(got, ref) -> float:
     """A position agrees if the oracle's logit at the GPU's argmax is within
-    2*max|got-ref| of the oracle's maximum (a near-tie flipped by rounding)."""
+    2*e of the oracle's maximum, e = max |got - ref| over that position's row.
+    Whenever every logit of the row is within e of the oracle's, this holds by
+    construction, so the rate is a consistency check (it fails on NaN rows), not
+    a second measure of agreement; the exact rate is the measure."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
-    tol = 2.0 * np.abs(got - ref).max()
+    tol = 2.0 * np.abs(got - ref).max(axis=-1)
     ag = np.argmax(got, axis=-1)
     best = ref.max(axis=-1)
     at = np.take_along_axis(ref, ag[..., None], axis=-1)[..., 0]
     return float(np.mean(at >= best - tol))
+
+
+# Rows of the argmax report, printed at the end of the pytest session (conftest).
+ARGMAX_LOG: list = []
+
+
+def argmax_check(label, mode, got, ref, model=None):
+    """Measure and record argmax agreement of ``got`` against the oracle ``ref``
+    (both [..., V]) and assert the criterion.
+
+    The target asks for argmax agreement on >= 99.9 % of positions.  fp32 mode
+    must meet it exactly.  bf16 mode cannot in general: rounding the LM head's
+    input to bf16 alone flips 0.3-0.4 % of the positions of the random-weight
+    workloads (test_argmax_reading).  There the exact rate is reported beside
+    the rate of the CPU bf16 rounding model (``model``: its logits on the same
+    positions, tests/bf16_model.py), and the GPU may flip at most
+    2 x the model's flips + 3 positions; without a model, at most 2 % + 3.
+    Returns the report row."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    n = int(np.prod(got.shape[:-1]))
+    flips = int(np.sum(np.argmax(got, -1) != np.argmax(ref, -1)))
+    row = {"label": label, "mode": mode, "positions": n, "exact": 1.0 - flips / n,
+           "tie_aware": tie_aware_agreement(got, ref), "model": None}
+    if model is not None:
+        m_flips = int(np.sum(np.argmax(model, -1) != np.argmax(ref, -1)))
+        row["model"] = 1.0 - m_flips / n
+    ARGMAX_LOG.append(row)
+    assert row["tie_aware"] == 1.0, row
+    if mode == "fp32":
+        assert row["exact"] >= 0.999, row
+    elif model is not None:
+        assert flips <= 2 * m_flips + 3, row
+    else:
+        assert flips <= 0.02 * n + 3, row
+    return row
+
+
+def format_argmax_log(rows) -> list:
+    """Lines of the argmax table: exact rate, tie-aware rate, bf16 model rate."""
+    out = ["argmax agreement with the oracle (exact = the target's plain reading; "
+           "bf16 model = the same positions through the CPU bf16 rounding model)"]
+    # whole-configuration rows last, so that the end of a log shows them
+    rows = sorted(rows, key=lambda r: r["label"].startswith("full "))
+    for r in rows:
+        model = "-" if r["model"] is None else f"{r['model']:.4f}"
+        note = "" if r["exact"] >= 0.999 else "  (exact below 99.9 %)"
+        out.append(f"  {r['label']:<44} {r['mode']:<4} n={r['positions']:<6} exact {r['exact']:.4f}"
+                   f"  tie-aware {r['tie_aware']:.4f}  bf16 model {model}{note}")
+    return out
 
 
 def to_torch_gpt2_weights(w: dict, device="cuda", bf16=False):

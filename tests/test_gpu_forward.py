@@ -2,16 +2,20 @@
 
 Tolerances (max |got - ref| / max |ref| over the logits, as the oracle's
 float64 forward sees the same bf16-exact weights): 1e-4 in fp32 mode and
-2e-2 in bf16 mode; argmax over the vocabulary must agree on >= 99.9 % of the
-positions checked.  Large configurations are checked on sampled sequences
-(sequences are independent, a property the oracle tests pin).
+2e-2 in bf16 mode.  Argmax agreement over the vocabulary is measured exactly
+and reported at the end of the session (helpers.argmax_check): fp32 mode must
+agree on >= 99.9 % of the positions; bf16 mode is held to the rate of the CPU
+bf16 rounding model on the same positions.  Large configurations are checked
+on sampled sequences (sequences are independent, a property the oracle tests
+pin).
 """
 import numpy as np
 import pytest
 
 import oracle
 import workloads
-from helpers import argmax_agreement, rel_err, tie_aware_agreement, to_torch_weights
+import bf16_model
+from helpers import argmax_check, rel_err, to_torch_weights
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -43,15 +47,11 @@ def run_model(cfg, w, tokens, max_batch=None, max_seq=None):
     return out[:, : cfg.vocab].reshape(B, S, cfg.vocab)
 
 
-def check(cfg, got, ref, positions_note=""):
+def check(cfg, got, ref, label, model=None):
     err = rel_err(got, ref)
-    agree = argmax_agreement(got, ref)
-    assert err < TOL[cfg.mode], f"{cfg.name}: rel err {err:.3e}"
-    if agree < 0.999:
-        # reading for near-ties flipped by bf16 rounding; reported separately
-        tie = tie_aware_agreement(got, ref)
-        assert tie >= 0.999, f"{cfg.name}: argmax {agree:.4f}, tie-aware {tie:.4f} {positions_note}"
-    return err, agree
+    assert err < TOL[cfg.mode], f"{label}: rel err {err:.3e}"
+    row = argmax_check(label, cfg.mode, got, ref, model)
+    return err, row["exact"]
 
 
 @pytest.mark.parametrize("gains", ["ones", "random"])
@@ -61,7 +61,7 @@ def test_tiny_fp32_full_config(gains):
     tok = workloads.make_tokens(cfg)
     got = run_model(cfg, w, tok)
     ref = oracle.forward(tok, w, cfg)
-    err, agree = check(cfg, got, ref)
+    err, agree = check(cfg, got, ref, f"full tiny, gains {gains}")
     assert agree == 1.0
 
 
@@ -69,7 +69,7 @@ def test_tiny_gqa_ragged_fp32():
     cfg = workloads.get_config("tiny").replace(n_kv_head=2, n_layer=3)
     w = workloads.make_weights(cfg, gains="random")
     tok = workloads.make_tokens(cfg, batch=3, seq=37)
-    check(cfg, run_model(cfg, w, tok), oracle.forward(tok, w, cfg))
+    check(cfg, run_model(cfg, w, tok), oracle.forward(tok, w, cfg), "tiny GQA 3x37, 3 layers")
 
 
 @pytest.mark.parametrize("name,B,S", [
@@ -82,7 +82,8 @@ def test_bf16_reduced_shapes(name, B, S):
     cfg = workloads.get_config(name).replace(n_layer=2)
     w = workloads.make_weights(cfg, gains="random")
     tok = workloads.make_tokens(cfg, batch=B, seq=S)
-    check(cfg, run_model(cfg, w, tok), oracle.forward(tok, w, cfg))
+    check(cfg, run_model(cfg, w, tok), oracle.forward(tok, w, cfg), f"{name} {B}x{S}, 2 layers",
+          bf16_model.forward(tok, w, cfg))
 
 
 @pytest.mark.parametrize("name,rows", [("small", [0, 31]), ("gpt2s", [5]), ("long", [0]), ("gqa", [2])])
@@ -94,7 +95,7 @@ def test_bf16_full_configs_sampled_sequences(name, rows):
     tok = workloads.make_tokens(cfg)
     got = run_model(cfg, w, tok)
     ref = oracle.forward(tok, w, cfg, rows=rows)
-    check(cfg, got[rows], ref, f"rows {rows}")
+    check(cfg, got[rows], ref, f"full {name}, sequences {rows}", bf16_model.forward(tok, w, cfg, rows=rows))
 
 
 def test_bf16_causality_end_to_end():

@@ -1,11 +1,15 @@
 """GPU check of tfm_swiglu_noalloc, the SwiGLU entry point for callers that
-cannot allocate device memory (graph capture, a host framework that owns the
-allocator, a fixed memory budget).
+cannot allocate device memory: plugins under a host framework that owns the
+device allocator, and deployments whose device memory is budgeted once at
+start-up.
 
-It must give what tfm_swiglu gives with a caller-allocated workspace, on two
-calls in a row (the second reuses the library's scratch array, which still
-holds the first call's activation), and refuse sizes beyond the array.  This
-file is collected last so a failure here stops a run only after every other test.
+It runs the same kernels as tfm_swiglu, only with the hidden activation in the
+library's fixed scratch array instead of a caller workspace, so its output must
+equal tfm_swiglu's bit for bit, on two calls in a row (the second reuses the
+array, which still holds the first call's activation), overwriting and
+accumulating.  It must refuse sizes beyond the array and bad sizes with their
+own messages.  This file is collected last so a failure here stops a run only
+after every other test.
 """
 import numpy as np
 import pytest
@@ -16,13 +20,6 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 from decoder_only_transformer_gb300 import tfm  # noqa: E402
-
-TOL = {True: 8e-3, False: 1e-5}   # the swiglu component tolerances (bf16 / fp32)
-
-
-def _rel(got, ref):
-    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
-    return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30))
 
 
 def _operands(seed, M, D, F, bf16):
@@ -49,20 +46,23 @@ def test_noalloc_matches_workspace_entry_point_twice(bf16):
         assert tfm.swiglu_workspace_bytes(M, F, mode) <= tfm.swiglu_noalloc_max_bytes()
         x, w1, w3, w2 = _operands(seed, M, D, F, bf16)
         ws = torch.empty(tfm.swiglu_workspace_bytes(M, F, mode), dtype=torch.uint8, device="cuda")
-        want = torch.empty(M, D, device="cuda")
-        tfm.swiglu(x, w1, w3, w2, want, ws, accumulate=False)
-        got = torch.full((M, D), float("nan"), device="cuda")
-        tfm.swiglu_noalloc(x, w1, w3, w2, got, accumulate=False)
         h0 = torch.randn(M, D, device="cuda")
-        acc = h0.clone()
-        tfm.swiglu_noalloc(x, w1, w3, w2, acc, accumulate=True)
+        want = torch.empty(M, D, device="cuda")
+        want_acc = h0.clone()
+        tfm.swiglu(x, w1, w3, w2, want, ws, accumulate=False)
+        tfm.swiglu(x, w1, w3, w2, want_acc, ws, accumulate=True)
+        got = torch.full((M, D), float("nan"), device="cuda")
+        got_acc = h0.clone()
+        tfm.swiglu_noalloc(x, w1, w3, w2, got, accumulate=False)
+        tfm.swiglu_noalloc(x, w1, w3, w2, got_acc, accumulate=True)
         torch.cuda.synchronize()
         tfm.device_status()
-        assert _rel(got.cpu().numpy(), want.cpu().numpy()) <= TOL[bf16]
-        assert _rel((acc - h0).cpu().numpy(), want.cpu().numpy()) <= 2 * TOL[bf16]
+        assert torch.equal(got, want)
+        assert torch.equal(got_acc, want_acc)
+        assert not torch.equal(got_acc, h0)
 
 
-def test_noalloc_rejects_sizes_beyond_the_array():
+def test_noalloc_rejects_sizes_beyond_the_array_and_bad_sizes():
     cap = tfm.swiglu_noalloc_max_bytes()
     F = 4096
     M = cap // (F * 2) + 1                      # one row more than fits in bf16
@@ -70,7 +70,10 @@ def test_noalloc_rejects_sizes_beyond_the_array():
     w = torch.empty(F, 512, dtype=torch.bfloat16, device="cuda")
     y = torch.empty(8, 512, device="cuda")
     lib = tfm.load()
-    st = lib.tfm_swiglu_noalloc(x.data_ptr(), w.data_ptr(), w.data_ptr(), w.data_ptr(),
-                                y.data_ptr(), M, 512, F, 0, tfm.TFM_BF16, None)
-    assert st == tfm.TFM_EINVAL
+    args = (x.data_ptr(), w.data_ptr(), w.data_ptr(), w.data_ptr(), y.data_ptr())
+    assert lib.tfm_swiglu_noalloc(*args, M, 512, F, 0, tfm.TFM_BF16, None) == tfm.TFM_EINVAL
     assert b"scratch" in lib.tfm_last_error()
+    assert lib.tfm_swiglu_noalloc(*args, -1, 512, F, 0, tfm.TFM_BF16, None) == tfm.TFM_EINVAL
+    assert b"bad sizes" in lib.tfm_last_error()
+    assert lib.tfm_swiglu_noalloc(*args, 8, 512, 0, 0, tfm.TFM_BF16, None) == tfm.TFM_EINVAL
+    assert b"bad sizes" in lib.tfm_last_error()
