@@ -17,8 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libtfm.so")
-SOURCES = ["api.cu", "k_rows.cu", "k_simt.cu", "k_gemm_tc.cu", "k_gemm_skinny.cu", "k_attention.cu", "k_decode.cu", "k_loss.cu",
-           "k_attention_tc.cu", "k_attention_pp.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "k_rows.cu", "k_simt.cu", "k_gemm_tc.cu", "k_gemm_skinny.cu", "k_decode.cu", "k_loss.cu",
+           "k_attention_tc.cu", "k_attention_pp.cu", "k_attention_short.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I", INCLUDE, "-I", CSRC]

@@ -220,8 +220,7 @@ struct Model {
     int64_t plan_m = -1;
     std::vector<GemmPlan> p_qkv, p_o, p_gu, p_down;
     GemmPlan p_lm;
-    AttnPlan p_attn;               // tcgen05 attention (d_head 64 / 128)
-    bool attn_tc = false;
+    AttnPlan p_attn;               // tcgen05 attention
     const float* plan_logits = nullptr;
     int64_t plan_ld = -1;
     int plan_S = -1;
@@ -694,9 +693,8 @@ tfm_status build_plans(Model* m, int M, int S, float* logits, int64_t ld) {
     m->plan_m = M;
     m->plan_S = S;
     const int dh = c.d_model / c.n_head;
-    m->attn_tc = attention_tc_supported(dh);
-    if (m->attn_tc &&
-        plan_attention_tc(&m->p_attn, m->q(), m->k(), m->v(), m->o(), M / S, c.n_head,
+    // (bf16 mode: every supported d_head, 32, 64 and 128, runs on tcgen05)
+    if (plan_attention_tc(&m->p_attn, m->q(), m->k(), m->v(), m->o(), M / S, c.n_head,
                           c.n_kv_head, S, dh, 1.0f / std::sqrt((float)dh)) != TFM_OK) {
         m->plan_m = -1;
         return fail(TFM_ECUDA, "could not encode attention tensor maps");
@@ -892,14 +890,11 @@ tfm_status forward_impl(Model* m, const int32_t* tokens, int B, int S, float* lo
             // a sliding-window layer (window < S) skips the key tiles before each
             // query tile's window and masks the band's edge
             const int win = layer_window(m, l, S);
-            if (m->attn_tc) {
+            {
                 AttnPlan pw = m->p_attn;
                 pw.window = win;
                 TFM_LAUNCH(K_ATTN, launch_attention_tc(pw, st));
-            } else
-                TFM_LAUNCH(K_ATTN, launch_attention_bf16(m->q(), m->k(), m->v(), m->o(), B,
-                                                         c.n_head, c.n_kv_head, S, dh, scale, st,
-                                                         win));
+            }
             TFM_LAUNCH(K_OPROJ, launch_gemm_tc(m->p_o[l], st));
             TFM_LAUNCH(K_NORM, norm_mid(l));
             TFM_LAUNCH(K_GATEUP, launch_gemm_tc(m->p_gu[l], st));
@@ -1542,16 +1537,12 @@ tfm_status tfm_causal_attention_window(const void* q, const void* k, const void*
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (mode == TFM_BF16) {
-        if (dh != 32 && dh != 64 && dh != 128) return fail(TFM_EUNSUPPORTED, "bf16 attention: dh in {32,64,128}");
-        if (tfm::attention_tc_supported(dh)) {
-            tfm::AttnPlan plan;
-            tfm_status ps = tfm::plan_attention_tc(&plan, q, k, v, o, B, H, Hkv, S, dh, scale);
-            if (ps != TFM_OK) return fail(ps, "could not encode attention tensor maps");
-            plan.window = window;
-            e = tfm::launch_attention_tc(plan, cs);
-        } else {
-            e = tfm::launch_attention_bf16(q, k, v, o, B, H, Hkv, S, dh, scale, cs, window);
-        }
+        if (!tfm::attention_tc_supported(dh)) return fail(TFM_EUNSUPPORTED, "bf16 attention: dh in {32,64,128}");
+        tfm::AttnPlan plan;
+        tfm_status ps = tfm::plan_attention_tc(&plan, q, k, v, o, B, H, Hkv, S, dh, scale);
+        if (ps != TFM_OK) return fail(ps, "could not encode attention tensor maps");
+        plan.window = window;
+        e = tfm::launch_attention_tc(plan, cs);
     } else if (mode == TFM_FP32) {
         if (dh < 1 || dh > 128) return fail(TFM_EUNSUPPORTED, "fp32 attention: dh <= 128");
         e = tfm::launch_attention_simt(static_cast<const float*>(q), static_cast<const float*>(k),

@@ -189,12 +189,6 @@ tfm_status plan_gemm_tc(GemmPlan* plan, const void* A, int64_t lda, const void* 
 cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t st);
 cudaError_t launch_gemm_skinny(const GemmPlan& plan, cudaStream_t st);
 
-// ---- bf16 flash attention on mma.sync (k_attention.cu), any dh in {32, 64, 128}
-// window > 0: sliding window, query i sees keys i-window < j <= i (>= S: causal).
-cudaError_t launch_attention_bf16(const void* q, const void* k, const void* v, void* o, int B,
-                                  int H, int Hkv, int S, int dh, float scale, cudaStream_t st,
-                                  int window = 0);
-
 // ---- attention of one new query per sequence over a KV cache (k_decode.cu):
 // q [B, H, dh], caches [B, Hkv, max_seq, dh] (positions [0, L) read), o [B, H*dh]
 // bf16; part holds decode_partial_floats(B, H, max_seq, dh) floats of scratch.
@@ -211,7 +205,8 @@ cudaError_t launch_decode_attention(const void* q, const void* kc, const void* v
 cudaError_t launch_decode_setup(int* pos_dev, int pos, const int32_t* tok, int32_t* tok_dev, int B,
                                 cudaStream_t st);
 
-// ---- bf16 flash attention on tcgen05 (k_attention_tc.cu), dh in {64, 128}
+// ---- bf16 flash attention on tcgen05 (k_attention_tc.cu, k_attention_pp.cu,
+// k_attention_short.cu), dh in {32, 64, 128}
 struct AttnPlan {
     CUtensorMap qmap, kmap, vmap;   // [B*heads, S, dh] views of q, k, v
     int B, H, Hkv, S, dh;
@@ -225,5 +220,9 @@ tfm_status plan_attention_tc(AttnPlan* p, const void* q, const void* k, const vo
 cudaError_t launch_attention_tc(const AttnPlan& p, cudaStream_t st);
 // two query tiles per CTA, dh in {32, 64} (k_attention_pp.cu)
 cudaError_t launch_attention_pp(const AttnPlan& p, cudaStream_t st);
+// dh 32, S <= 256, no window: the three causal 128 x 128 blocks of a (sequence,
+// head) side by side (k_attention_short.cu)
+bool attention_short_supported(int dh, int S, int window);
+cudaError_t launch_attention_short(const AttnPlan& p, cudaStream_t st);
 
 }  // namespace tfm

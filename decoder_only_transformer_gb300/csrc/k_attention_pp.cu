@@ -84,18 +84,6 @@ struct AttPP {
     static constexpr uint32_t kGroup = 8 * kRowBytes;        // 8-row swizzle atom
 };
 
-// Shared-memory matrix descriptor with a given swizzle code, leading and stride
-// byte offsets (tcgen05 descriptor version 1).
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t swz, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)swz << 61;
-    return d;
-}
-
 template <int DH, bool kWin>
 __global__ void __launch_bounds__(kThreadsPP, 1)
     k_attention_pp(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,

@@ -564,9 +564,7 @@ cudaError_t launch_tc(const AttnPlan& p, cudaStream_t st) {
 
 }  // namespace
 
-// d_head 32 stays on the mma.sync kernel (k_attention.cu): measured faster at the
-// short sequences it is used with.
-bool attention_tc_supported(int dh) { return dh == 64 || dh == 128; }
+bool attention_tc_supported(int dh) { return dh == 32 || dh == 64 || dh == 128; }
 
 tfm_status plan_attention_tc(AttnPlan* p, const void* q, const void* k, const void* v, void* o,
                              int B, int H, int Hkv, int S, int dh, float scale) {
@@ -587,8 +585,13 @@ tfm_status plan_attention_tc(AttnPlan* p, const void* q, const void* k, const vo
 
 cudaError_t launch_attention_tc(const AttnPlan& p, cudaStream_t st) {
     if (p.B <= 0 || p.S <= 0) return cudaSuccess;
+    // d_head 32: up to 256 positions, the three causal blocks of a sequence side
+    // by side (k_attention_short.cu), else two query tiles per CTA as for 64;
     // d_head 64: two query tiles per CTA (k_attention_pp.cu); d_head 128: one tile
     // per CTA (two Q tiles, two P tiles and a K/V ring exceed shared memory).
+    if (p.dh == 32)
+        return attention_short_supported(p.dh, p.S, p.window) ? launch_attention_short(p, st)
+                                                               : launch_attention_pp(p, st);
     if (p.dh == 64) return launch_attention_pp(p, st);
     if (p.dh == 128) return launch_tc<128>(p, st);
     return cudaErrorInvalidValue;

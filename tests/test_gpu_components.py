@@ -144,8 +144,14 @@ def test_attention_fp32(B, H, Hkv, S, dh):
     # several items: 384 query tiles (d_head 128, ragged S), 256 tile pairs
     # (d_head 64, an odd tile count: the last pair has no second tile)
     (3, 16, 4, 900, 128), (4, 16, 4, 830, 64),
-    # d_head 32 (mma.sync kernel): ragged S with GQA, and a longer sequence
+    # d_head 32 beyond 256 positions (two query tiles per CTA): ragged S with
+    # GQA, and a longer sequence
     (3, 8, 2, 333, 32), (1, 2, 2, 700, 32),
+    # d_head 32 up to 256 positions (the three causal blocks side by side): one
+    # position, one tile exactly, one row into the second tile, ragged with GQA,
+    # MQA, and the short-sequence workload's shape (512 items over the SMs)
+    (1, 2, 2, 1, 32), (2, 4, 2, 128, 32), (1, 4, 4, 129, 32), (3, 8, 2, 200, 32),
+    (5, 8, 1, 250, 32), (32, 16, 16, 256, 32),
 ])
 def test_attention_bf16(B, H, Hkv, S, dh):
     q, k, v = _qkv(S * 3 + dh, B, H, Hkv, S, dh, True)
@@ -155,9 +161,10 @@ def test_attention_bf16(B, H, Hkv, S, dh):
     assert rel_err(o.float().cpu().numpy(), ref) < TOL_BF16
 
 
-def test_attention_bf16_uniform_scores_prefix_mean():
+@pytest.mark.parametrize("S,dh", [(300, 64), (256, 32), (300, 32)])
+def test_attention_bf16_uniform_scores_prefix_mean(S, dh):
     # q = 0: every visible key weighs the same, o_t is the mean of v_0..v_t
-    B, H, S, dh = 1, 2, 300, 64
+    B, H = 1, 2
     _, k, v = _qkv(5, B, H, H, S, dh, True)
     q = np.zeros_like(k)
     o = torch.empty(B, S, H * dh, device="cuda", dtype=torch.bfloat16)
