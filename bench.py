@@ -62,11 +62,14 @@ def load_peaks():
 # forward's launches of the kernels as they are now: layer 0 for the per-layer
 # kernels, and the LM head.  An op without an entry reports traffic null.
 DRAM_TRAFFIC = {
-    ("small", "qkv_rope_gemm"): 10.06e6, ("small", "attention"): 25.20e6,
+    ("small", "qkv_rope_gemm"): 10.06e6,
     ("small", "oproj_residual_gemm"): 25.76e6, ("small", "gateup_swiglu_gemm"): 11.21e6,
     ("small", "down_residual_gemm"): 40.25e6, ("small", "lmhead_gemm"): 285.30e6,
-    ("long", "attention"): 50.41e6,
-    ("gqa", "attention"): 50.67e6,
+    ("long", "attention"): 50.41e6, ("long", "oproj_residual_gemm"): 52.49e6,
+    ("long", "gateup_swiglu_gemm"): 29.89e6, ("long", "down_residual_gemm"): 84.44e6,
+    ("gqa", "qkv_rope_gemm"): 69.77e6, ("gqa", "attention"): 50.67e6,
+    ("gqa", "oproj_residual_gemm"): 123.10e6, ("gqa", "gateup_swiglu_gemm"): 148.89e6,
+    ("gqa", "down_residual_gemm"): 229.41e6,
 }
 
 

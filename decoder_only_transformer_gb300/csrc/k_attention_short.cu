@@ -19,22 +19,30 @@
 // One CTA of 16 warps per SM, persistent over (sequence, head) items:
 //   warp 0      TMA: Q, K and V of an item (six 128 x 32 boxes, 48 KB) into one
 //               of three buffers, so the next items' loads run ahead
-//   warps 4-7, 8-11, 12-15  blocks 0, 1, 2, one thread per query row.  Each
-//               warpgroup drives its own block: its first thread issues the S
-//               product (M = N = 128, K = 32) and, once all four warps have
-//               written P (a bounded mbarrier), the P.V product (P from tensor memory, V MN-major,
-//               M = 128, N = 32, K = 128); the next item's S is issued as soon
-//               as this item's P.V is done, so it runs under the output readout.
-//               The softmax takes the row max over the block's S columns, then
-//               computes p = 2^(s scale log2e - m), sums it and writes it back as
-//               bf16 pairs over the S columns already read.  Warps 4-7 write
-//               query tile A's output rows, warps 8-11 hand block 1's rows to
-//               warps 12-15 through shared memory, which merge and write tile B's.
-// (A separate MMA-issuing warp was measured to be the bound: sharing its
-// scheduler with busy softmax warps it took ~1000 cycles to issue a block's
-// eight P.V products, against a ~2500-cycle softmax.)
+//   warp 1      S MMAs: S_x = Q K^T into 128 TMEM columns per block (M = N = 128,
+//               K = 32)
+//   warp 2      P.V MMAs: O_x = P_x V, P read from tensor memory, V MN-major
+//               (M = 128, N = 32, K = 128)
+//   warps 4-7, 8-11, 12-15  softmax of blocks 0, 1, 2, one thread per query row:
+//               a first pass over the block's S columns takes the row max, a
+//               second computes p = 2^(s scale log2e - m), sums it and writes it
+//               back as bf16 pairs over the S columns already read; warps 4-7
+//               then write query tile A's output rows, warps 12-15 merge blocks 1
+//               and 2 (block 1's output read from tensor memory, its max and sum
+//               from shared memory) and write tile B's.
 // Chunks of 32 keys that lie wholly above a block's diagonal, or past the
 // sequence, are skipped (their p are written as 0).  Every wait is bounded.
+//
+// Measured at the short-sequence workload (32 x 256 positions, 16 heads): 19.1
+// us against 21.0 us for an mma.sync flash kernel.  A per-CTA clock-stamp
+// timeline gives ~5500 cycles per item: ~450 from issuing S to the softmax
+// seeing it, ~700 for the max pass, ~2500 for the exponential pass, ~1000 from
+// P to the end of P.V (the three blocks' 24 P.V products, N = 32, share the
+// tensor pipe at about a third of its rate).  Tensor memory (480 of 512
+// columns) allows no second item in flight.  Two reorganisations measured
+// slower (21.7 us): issuer warps that poll every block's barriers and issue
+// whichever is ready, with block 1's output handed over through shared memory;
+// and warpgroups that issue their own products.
 #include <climits>
 
 #include "common.cuh"
@@ -50,15 +58,11 @@ constexpr int kThreadsShort = 512;
 constexpr int kBufs = 3;                          // item buffers in shared memory
 constexpr int kBoxBytes = kT * kDH * 2;           // one 128 x 32 bf16 box, 64-byte rows
 constexpr int kBufBytes = 6 * kBoxBytes;          // Q_A, Q_B, K_A, K_B, V_A, V_B
-// Block 1's output handed to block 2's merge: per slot (item parity) the 32
-// unnormalised values of each row stored column-major ([e][row], conflict-free
-// for a warp), then the rows' (max, sum).
-constexpr int kHandFloats = kDH * kT + 2 * kT;
-constexpr int kHandOff = kBufs * kBufBytes;
-constexpr int kBarOff = kHandOff + 2 * kHandFloats * 4;
-// full[3], empty[3], s_full[3], o_done[3], p_ready[3], hand_full[2], hand_free[2]
-constexpr int kNumBars = 2 * kBufs + 3 * 3 + 4;
-constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+constexpr int kBarOff = kBufs * kBufBytes;
+// full[3], empty[3], s_full[3], p_full[3], o_done[3], o_free[3], stats, done
+constexpr int kNumBars = 2 * kBufs + 5 * 3 + 2;
+constexpr int kStatsOff = kBarOff + 8 * kNumBars; // (m, l) of block 1 rows, two items
+constexpr int kMiscOff = kStatsOff + 2 * kT * 8;
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
 constexpr int kOCol = 3 * kT;                     // O_x at tensor-memory column 384 + 32 x
 constexpr uint32_t kSwz64 = 4u;                   // 64-byte swizzle (descriptor code)
@@ -77,11 +81,12 @@ __global__ void __launch_bounds__(kThreadsShort, 1)
     auto full_bar = [&](int b) { return bars + 8u * b; };
     auto empty_bar = [&](int b) { return bars + 8u * (kBufs + b); };
     auto s_full = [&](int x) { return bars + 8u * (2 * kBufs + x); };
-    auto o_done = [&](int x) { return bars + 8u * (2 * kBufs + 3 + x); };
-    auto p_ready = [&](int x) { return bars + 8u * (2 * kBufs + 6 + x); };
-    auto hand_full = [&](int sl) { return bars + 8u * (2 * kBufs + 9 + sl); };
-    auto hand_free = [&](int sl) { return bars + 8u * (2 * kBufs + 11 + sl); };
-    float* hand = reinterpret_cast<float*>(gbase + kHandOff);
+    auto p_full = [&](int x) { return bars + 8u * (2 * kBufs + 3 + x); };
+    auto o_done = [&](int x) { return bars + 8u * (2 * kBufs + 6 + x); };
+    auto o_free = [&](int x) { return bars + 8u * (2 * kBufs + 9 + x); };
+    const uint32_t stats_bar = bars + 8u * (2 * kBufs + 12);
+    const uint32_t done_bar = bars + 8u * (2 * kBufs + 13);
+    float2* stats = reinterpret_cast<float2*>(gbase + kStatsOff);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + kMiscOff + 4);
 
@@ -95,17 +100,16 @@ __global__ void __launch_bounds__(kThreadsShort, 1)
     if (warp == 0 && lane == 0) {
         for (int b = 0; b < kBufs; ++b) {
             mbar_init(full_bar(b), 1);
-            mbar_init(empty_bar(b), nblk);             // each block's last product releases it
+            mbar_init(empty_bar(b), 2);                // both MMA issuers release a buffer
         }
         for (int x = 0; x < 3; ++x) {
             mbar_init(s_full(x), 1);
+            mbar_init(p_full(x), 4);
             mbar_init(o_done(x), 1);
-            mbar_init(p_ready(x), 4);
+            mbar_init(o_free(x), 4);
         }
-        for (int sl = 0; sl < 2; ++sl) {
-            mbar_init(hand_full(sl), 4);
-            mbar_init(hand_free(sl), 4);
-        }
+        mbar_init(stats_bar, 4);
+        mbar_init(done_bar, 2);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&qmap);
@@ -148,12 +152,68 @@ __global__ void __launch_bounds__(kThreadsShort, 1)
             for (int i = issued - kBufs < 0 ? 0 : issued - kBufs; i < issued; ++i)
                 mbar_wait(full_bar(i % kBufs), (uint32_t)(i / kBufs) & 1u, err, abort_flag);
         }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- S issuer
+        // Releases an item's buffer (with the P.V issuer) by a commit after its
+        // last product reading it; both commit to done_bar at the end, so no
+        // product is in flight when tensor memory is freed.
+        if (lane == 0) {
+            bool ok = true;
+            constexpr uint32_t idesc_s = umma_idesc_bf16(kT, kT);
+            const uint64_t d0 = sdesc(base, kSwz64, 16, kGroup);
+            for (int i = 0; i < items && ok; ++i) {
+                const int buf = i % kBufs;
+                ok = mbar_wait(full_bar(buf), (uint32_t)(i / kBufs) & 1u, err, abort_flag);
+                for (int x = 0; x < nblk && ok; ++x) {
+                    // P_x is written over S_x: the next S_x waits for the last P_x.V
+                    if (i > 0) ok = mbar_wait(o_done(x), (uint32_t)(i - 1) & 1u, err, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const int qbox = x == 0 ? 0 : 1, kbox = x == 2 ? 3 : 2;
+                    const uint64_t a0 = d0 + (uint64_t)((buf * kBufBytes + qbox * kBoxBytes) >> 4);
+                    const uint64_t b0 = d0 + (uint64_t)((buf * kBufBytes + kbox * kBoxBytes) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < kDH / 16; ++kk)
+                        umma_bf16(tmem_base + x * kT, a0 + 2 * kk, b0 + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
+                    umma_commit(s_full(x));
+                }
+                if (ok) umma_commit(empty_bar(buf));
+            }
+            umma_commit(done_bar);
+            mbar_wait(done_bar, 0, err, abort_flag);
+        }
+    } else if (warp == 2) {
+        // ---------------------------------------------------------- P.V issuer
+        if (lane == 0) {
+            bool ok = true;
+            constexpr uint32_t idesc_o = umma_idesc_bf16(kT, kDH, true);
+            const uint64_t dv = sdesc(base, kSwz64, 0, kGroup);
+            for (int i = 0; i < items && ok; ++i) {
+                const int buf = i % kBufs;
+                for (int x = 0; x < nblk && ok; ++x) {
+                    ok = mbar_wait(p_full(x), (uint32_t)i & 1u, err, abort_flag);
+                    // O_x is overwritten once the previous item's O_x has been read
+                    if (ok && i > 0) ok = mbar_wait(o_free(x), (uint32_t)(i - 1) & 1u, err, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const int vbox = x == 2 ? 5 : 4;
+                    const uint64_t b0 = dv + (uint64_t)((buf * kBufBytes + vbox * kBoxBytes) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < kT / 16; ++kk)
+                        umma_bf16_ts(tmem_base + kOCol + x * kDH, tmem_base + x * kT + kk * 8,
+                                     b0 + kk * ((16 * kDH * 2) >> 4), idesc_o, kk > 0 ? 1u : 0u);
+                    umma_commit(o_done(x));
+                }
+                if (ok) umma_commit(empty_bar(buf));
+            }
+            umma_commit(done_bar);
+            mbar_wait(done_bar, 0, err, abort_flag);
+        }
     } else if (warp >= 4 && (warp - 4) / 4 < nblk) {
-        // ---------------------------------------------------------- blocks
+        // ---------------------------------------------------------- softmax
         const int x = (warp - 4) >> 2;                 // block of this warpgroup
         const int q4 = warp & 3;                       // TMEM lane quarter
         const int r = q4 * 32 + lane;                  // row inside the query tile
-        const bool issuer = q4 == 0 && lane == 0;      // issues this block's products
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const uint32_t t_s = tmem_base + x * kT + lane_off;
         const uint32_t t_o = tmem_base + kOCol + x * kDH + lane_off;
@@ -171,32 +231,10 @@ __global__ void __launch_bounds__(kThreadsShort, 1)
         if (diag && q4 * 32 + 32 < wend) wend = q4 * 32 + 32;
         const int nck = wend > 0 ? (wend + 31) / 32 : 0;
         const int kfull = __reduce_min_sync(0xffffffffu, kend < 0 ? 0 : kend);
-        constexpr uint32_t idesc_s = umma_idesc_bf16(kT, kT);
-        constexpr uint32_t idesc_o = umma_idesc_bf16(kT, kDH, true);
-        const uint64_t dq = sdesc(base, kSwz64, 16, kGroup);
-        const uint64_t dv = sdesc(base, kSwz64, 0, kGroup);
-        const int qbox = x == 0 ? 0 : 1, kbox = x == 2 ? 3 : 2, vbox = x == 2 ? 5 : 4;
-        // S_x of item i (the issuer; P_x of item i - 1, written over S_x, has been
-        // consumed: its P.V is complete).
-        auto issue_s = [&](int i) -> bool {
-            const int buf = i % kBufs;
-            if (!mbar_wait(full_bar(buf), (uint32_t)(i / kBufs) & 1u, err, abort_flag)) return false;
-            tc_fence_after();
-            const uint64_t a0 = dq + (uint64_t)((buf * kBufBytes + qbox * kBoxBytes) >> 4);
-            const uint64_t b0 = dq + (uint64_t)((buf * kBufBytes + kbox * kBoxBytes) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < kDH / 16; ++kk)
-                umma_bf16(tmem_base + x * kT, a0 + 2 * kk, b0 + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
-            umma_commit(s_full(x));
-            return true;
-        };
         bool ok = true;
-        if (issuer && items > 0) ok = issue_s(0);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
         for (int i = 0; i < items && ok; ++i) {
             const int bh = c + i * G;
             const int b = bh / H, h = bh - b * H;
-            const int buf = i % kBufs;
             if (!warp_wait(s_full(x), (uint32_t)i & 1u, err, abort_flag)) { ok = false; break; }
             tc_fence_after();
             // Pass 1: the row max over the visible keys.
@@ -225,32 +263,21 @@ __global__ void __launch_bounds__(kThreadsShort, 1)
             // (a row with no visible key, past the sequence: p = 0, never written out)
             const float negm = m == -INFINITY ? 0.f : -m;
             // Pass 2: p = 2^(s scale - m), row sum, P over the consumed S columns
-            // (keys 32 cc .. 32 cc + 31 -> columns 16 cc .. 16 cc + 15).  Chunk
-            // cc + 1's load is in flight while chunk cc is computed; every
-            // destination of a load stays live until its wait.
+            // (keys 32 cc .. 32 cc + 31 -> columns 16 cc .. 16 cc + 15).
             const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
             const uint64_t negm2 = f2_pack(negm, negm);
             uint64_t sum2[2] = {0ull, 0ull};
-            uint32_t cur[32];
-            if (nck > 0) {
-                tmem_ld32_issue(t_s, cur);
-                tmem_ld_wait();
-                reg_fence32(cur);
-            }
 #pragma unroll
             for (int cc = 0; cc < kT / 32; ++cc) {
                 uint32_t pw[16];
                 if (cc < nck) {
-                    uint32_t nxt[32];
-                    const bool more = cc + 1 < nck;
-                    if (more) tmem_ld32_issue(t_s + (cc + 1) * 32, nxt);
+                    float v[32];
+                    tmem_ld32(t_s + cc * 32, v);
                     const bool masked = (cc + 1) * 32 > kfull;
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         float t0, t1;
-                        f2_unpack(f2_fma(f2_pack(__uint_as_float(cur[e]), __uint_as_float(cur[e + 1])),
-                                         scale2, negm2),
-                                  t0, t1);
+                        f2_unpack(f2_fma(f2_pack(v[e], v[e + 1]), scale2, negm2), t0, t1);
                         float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
                         if (masked) {
                             if (cc * 32 + e >= kend) p0 = 0.f;
@@ -258,12 +285,6 @@ __global__ void __launch_bounds__(kThreadsShort, 1)
                         }
                         sum2[(e >> 1) & 1] = f2_add(sum2[(e >> 1) & 1], f2_pack(p0, p1));
                         pw[e >> 1] = pack_bf16x2(p0, p1);
-                    }
-                    if (more) {
-                        tmem_ld_wait();
-                        reg_fence32(nxt);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) cur[e] = nxt[e];
                     }
                 } else {
 #pragma unroll
@@ -276,70 +297,44 @@ __global__ void __launch_bounds__(kThreadsShort, 1)
             f2_unpack(sum2[0], sa[0], sb[0]);
             f2_unpack(sum2[1], sa[1], sb[1]);
             const float l = (sa[0] + sb[0]) + (sa[1] + sb[1]);
-            // Once P_x is complete in all four lane quarters (p_ready), the issuer
-            // starts P_x.V; a second commit releases the item's buffer when this
-            // block's products of the item are done.
-            bool nok_p = true;
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_ready(x));
-            if (issuer) {
-                if (!mbar_wait(p_ready(x), (uint32_t)i & 1u, err, abort_flag)) nok_p = false;
-            }
-            if (!__shfl_sync(0xffffffffu, nok_p ? 1 : 0, 0)) { ok = false; break; }
-            if (issuer) {
-                tc_fence_after();
-                const uint64_t b0 = dv + (uint64_t)((buf * kBufBytes + vbox * kBoxBytes) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < kT / 16; ++kk)
-                    umma_bf16_ts(tmem_base + kOCol + x * kDH, tmem_base + x * kT + kk * 8,
-                                 b0 + kk * ((16 * kDH * 2) >> 4), idesc_o, kk > 0 ? 1u : 0u);
-                umma_commit(o_done(x));
-                umma_commit(empty_bar(buf));
-            }
-            if (!warp_wait(o_done(x), (uint32_t)i & 1u, err, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            // P_x is consumed: the next item's S_x runs under this item's readout.
-            bool nok = true;
-            if (issuer && i + 1 < items) nok = issue_s(i + 1);
-            if (!__shfl_sync(0xffffffffu, nok ? 1 : 0, 0)) { ok = false; break; }
-            const int sl = i & 1;
-            float* hs = hand + sl * kHandFloats;
-            float ov[32];
-            tmem_ld32(t_o, ov);
+            if (lane == 0) mbar_arrive(p_full(x));
             if (x == 1) {
-                // Block 1: the unnormalised rows and their (max, sum) go to the
-                // merge of warps 12-15 through shared memory (slot i % 2, rewritten
-                // after the merge of item i - 2).
-                if (i >= 2 && !warp_wait(hand_free(sl), (uint32_t)((i >> 1) - 1) & 1u, err, abort_flag)) {
+                // Block 1 hands its (max, sum) to the merge of warps 12-15; the
+                // slot of item i is rewritten only after item i - 2's merge.
+                if (i > 0 && !warp_wait(o_free(1), (uint32_t)(i - 1) & 1u, err, abort_flag)) {
                     ok = false;
                     break;
                 }
-#pragma unroll
-                for (int e = 0; e < 32; ++e) hs[e * kT + r] = ov[e];
-                hs[kDH * kT + 2 * r] = m;
-                hs[kDH * kT + 2 * r + 1] = l;
+                stats[(i & 1) * kT + r] = make_float2(m, l);
                 __syncwarp();
-                if (lane == 0) mbar_arrive(hand_full(sl));
+                if (lane == 0) mbar_arrive(stats_bar);
                 continue;
             }
+            // Blocks 0 and 2: wait for this block's P.V (block 2 also for block
+            // 1's and its statistics), then write the output rows.
+            bool got = warp_wait(o_done(x), (uint32_t)i & 1u, err, abort_flag);
+            if (got && x == 2)
+                got = warp_wait(o_done(1), (uint32_t)i & 1u, err, abort_flag) &&
+                      warp_wait(stats_bar, (uint32_t)i & 1u, err, abort_flag);
+            if (!got) { ok = false; break; }
+            tc_fence_after();
+            float ov[32];
+            tmem_ld32(t_o, ov);
             float inv;
             if (x == 0) {
                 inv = 1.0f / l;
             } else {
                 // exact merge with block 1 (same rows, its own max and sum)
-                if (!warp_wait(hand_full(sl), (uint32_t)(i >> 1) & 1u, err, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const float m1 = hs[kDH * kT + 2 * r], l1 = hs[kDH * kT + 2 * r + 1];
-                const float mm = fmaxf(m1, m);
-                const float a1 = fast_exp2(m1 - mm), a2 = fast_exp2(m - mm);
-                inv = 1.0f / (l1 * a1 + l * a2);
+                float o1[32];
+                tmem_ld32(tmem_base + kOCol + kDH + lane_off, o1);
+                const float2 st = stats[(i & 1) * kT + r];
+                const float mm = fmaxf(st.x, m);
+                const float a1 = fast_exp2(st.x - mm), a2 = fast_exp2(m - mm);
+                inv = 1.0f / (st.y * a1 + l * a2);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) ov[e] = hs[e * kT + r] * a1 + ov[e] * a2;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(hand_free(sl));
+                for (int e = 0; e < 32; ++e) ov[e] = o1[e] * a1 + ov[e] * a2;
             }
             if (qi < S) {
                 __nv_bfloat16* orow = o + ((int64_t)(b * S + qi) * H + h) * kDH;
@@ -352,6 +347,12 @@ __global__ void __launch_bounds__(kThreadsShort, 1)
                     w.w = pack_bf16x2(ov[e + 6] * inv, ov[e + 7] * inv);
                     *reinterpret_cast<uint4*>(orow + e) = w;
                 }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(o_free(x));
+                if (x == 2) mbar_arrive(o_free(1));
             }
         }
     }

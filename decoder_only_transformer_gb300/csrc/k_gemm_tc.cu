@@ -727,11 +727,15 @@ tfm_status plan_gemm_tc(GemmPlan* plan, const void* A, int64_t lda, const void* 
     // keeps up with the tensor cores.  With a short K the tile time is set by the
     // epilogue's stores, and the pair (whose accumulator is released only when
     // both CTAs' epilogues are done) was measured slower; so pairs are used for
-    // K >= 2048, or K >= 1024 with many waves of tiles.
+    // K >= 2048, or K >= 1024 with N >= 2048 or many waves of tiles.  (At
+    // K = 1024: long-context QKV, N = 3072, 46.1 -> 43.1 us with pairs; the
+    // output projection, N = 1024, unchanged; pairs for every K >= 1024 made the
+    // short workload's down projection, N = 512, K = 1344, slower: 18.9 -> 20.3 us.)
     {
         const int64_t pair_tiles = (int64_t)((M + 2 * kBM - 1) / (2 * kBM)) *
                                    ((N + (dual ? 127 : 255)) / (dual ? 128 : 256));
-        const bool long_k = K >= 2048 || (K >= 1024 && pair_tiles >= 8LL * (sm_count() / 2));
+        const bool long_k = K >= 2048 ||
+                            (K >= 1024 && (N >= 2048 || pair_tiles >= 8LL * (sm_count() / 2)));
         plan->pair = (M > kBM && long_k) ? 1 : 0;
     }
     plan->block_n = plan->pair ? 256 : choose_block_n(M, N, dual);
