@@ -15,10 +15,15 @@
 // item left the SMs idle ~30 % of the kernel between CTAs, and writing O out
 // from the softmax warps stalled them ~4000 cycles per item (wait for the last
 // P.V, read O, normalise, store 32 KB) against ~1400 cycles per key tile.
-//   warp 0      TMA: each item's Q tile (once the previous item's S MMAs are done
-//               with the buffer), then K and V tiles (3-D maps [seq*heads, S,
-//               dh], 128-byte swizzle, zero fill past S) into separate K and V
-//               rings, in the order the MMA threads consume them
+//   warp 0      TMA: each item's Q tile into one of two Q buffers (item parity;
+//               refilled once the S MMAs of the item two back are done, so the
+//               next item's Q arrives while this one runs), then K and V tiles
+//               (3-D maps [seq*heads, S, dh], 128-byte swizzle, zero fill past S)
+//               into a 2-deep K ring and a 3-deep V ring, in the order the MMA
+//               threads consume them.  (With one Q buffer the next item's S had
+//               to wait for this item's last S and then a TMA round trip: GQA
+//               workload 61.2 -> 59.6 us with two; the second buffer took a K
+//               ring slot, shared memory being full.)
 //   warp 1      TMEM (512 columns: S double buffer 2 x 128, O dh, P double buffer
 //               2 x 64) and the S MMAs: S_j = Q K_j^T (M=128, N=128, K=dh)
 //   warp 2      the P.V MMAs: O += P_j V_j (M=128, N=dh, K=128; P read from tensor
@@ -58,20 +63,21 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 template <int DH>
 struct AttTc {
-    static constexpr int kStages = DH == 64 ? 4 : 3;
+    static constexpr int kStages = DH == 64 ? 4 : 3;  // V ring
+    static constexpr int kKStages = DH == 64 ? 4 : 2; // K ring (the second Q buffer took a slot)
     static constexpr int kSub = DH / 64;              // 64-column (128-byte) sub-tiles
     static constexpr int kQBytes = kQ * DH * 2;
     static constexpr int kKBytes = kKV * DH * 2;
     static constexpr int kVBytes = kKV * DH * 2;
-    static constexpr int kQOff = 0;
-    static constexpr int kKOff = kQOff + kQBytes;
-    static constexpr int kVOff = kKOff + kStages * kKBytes;
+    static constexpr int kQOff = 0;                   // two Q buffers (item parity)
+    static constexpr int kKOff = kQOff + 2 * kQBytes;
+    static constexpr int kVOff = kKOff + kKStages * kKBytes;
     static constexpr int kBarOff = kVOff + kStages * kVBytes;
     static constexpr int kOCol = 2 * kKV;             // TMEM columns: S[2], O, P[2]
     static constexpr int kPCol = kOCol + DH;
-    // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2],
-    // o_done[2], done, q_empty, l_ready, o_free
-    static constexpr int kNumBars = 1 + 4 * kStages + 10;
+    // k_full[SK], k_empty[SK], v_full[S], v_empty[S], s_full[2], p_full[2],
+    // o_done[2], done, l_ready, o_free, q_full[2], q_empty[2]
+    static constexpr int kNumBars = 2 * kKStages + 2 * kStages + 13;
     // Row sums handed from the softmax to the epilogue warps, [item parity][row].
     static constexpr int kRedOff = kBarOff + 8 * kNumBars;
     static constexpr int kMiscOff = kRedOff + 2 * kQ * 4;
@@ -84,25 +90,26 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
                    const __grid_constant__ CUtensorMap vmap, __nv_bfloat16* __restrict__ o, int BH,
                    int H, int Hkv, int S, float scale_log2, int window, int* err) {
     using L = AttTc<DH>;
-    constexpr int ST = L::kStages;
+    constexpr int ST = L::kStages, SK = L::kKStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
     const uint32_t sQ = base + L::kQOff, sK = base + L::kKOff, sV = base + L::kVOff;
     const uint32_t bars = base + L::kBarOff;
-    const uint32_t q_full = bars;
-    auto k_full = [&](int s) { return bars + 8u * (1 + s); };
-    auto k_empty = [&](int s) { return bars + 8u * (1 + ST + s); };
-    auto v_full = [&](int s) { return bars + 8u * (1 + 2 * ST + s); };
-    auto v_empty = [&](int s) { return bars + 8u * (1 + 3 * ST + s); };
-    auto s_full = [&](int i) { return bars + 8u * (1 + 4 * ST + i); };
-    auto p_full = [&](int i) { return bars + 8u * (3 + 4 * ST + i); };
-    auto o_done = [&](int i) { return bars + 8u * (5 + 4 * ST + i); };
-    const uint32_t done_bar = bars + 8u * (7 + 4 * ST);
-    const uint32_t q_empty = bars + 8u * (8 + 4 * ST);
-    const uint32_t l_ready = bars + 8u * (9 + 4 * ST);
-    const uint32_t o_free = bars + 8u * (10 + 4 * ST);
+    constexpr int B0 = 2 * SK + 2 * ST;               // first barrier after the rings
+    auto k_full = [&](int s) { return bars + 8u * s; };
+    auto k_empty = [&](int s) { return bars + 8u * (SK + s); };
+    auto v_full = [&](int s) { return bars + 8u * (2 * SK + s); };
+    auto v_empty = [&](int s) { return bars + 8u * (2 * SK + ST + s); };
+    auto s_full = [&](int i) { return bars + 8u * (B0 + i); };
+    auto p_full = [&](int i) { return bars + 8u * (B0 + 2 + i); };
+    auto o_done = [&](int i) { return bars + 8u * (B0 + 4 + i); };
+    const uint32_t done_bar = bars + 8u * (B0 + 6);
+    const uint32_t l_ready = bars + 8u * (B0 + 7);
+    const uint32_t o_free = bars + 8u * (B0 + 8);
+    auto q_full = [&](int qb) { return bars + 8u * (B0 + 9 + qb); };
+    auto q_empty = [&](int qb) { return bars + 8u * (B0 + 11 + qb); };
     float* red_l = reinterpret_cast<float*>(gbase + L::kRedOff);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + L::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMiscOff + 4);
@@ -138,11 +145,15 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
     const int rounds = (total + G - 1) / G;
 
     if (warp == 0 && lane == 0) {
-        mbar_init(q_full, 1);
-        mbar_init(q_empty, 1);
-        for (int s = 0; s < ST; ++s) {
+        for (int qb = 0; qb < 2; ++qb) {
+            mbar_init(q_full(qb), 1);
+            mbar_init(q_empty(qb), 1);
+        }
+        for (int s = 0; s < SK; ++s) {
             mbar_init(k_full(s), 1);
             mbar_init(k_empty(s), 1);
+        }
+        for (int s = 0; s < ST; ++s) {
             mbar_init(v_full(s), 1);
             mbar_init(v_empty(s), 1);
         }
@@ -187,8 +198,8 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
             bool ok = true;
             Item it;
             auto load_k = [&](int j) -> bool {
-                const int st = kn % ST;
-                if (!mbar_wait(k_empty(st), ((uint32_t)(kn / ST) & 1u) ^ 1u, err, abort_flag)) return false;
+                const int st = kn % SK;
+                if (!mbar_wait(k_empty(st), ((uint32_t)(kn / SK) & 1u) ^ 1u, err, abort_flag)) return false;
                 mbar_arrive_expect_tx(k_full(st), L::kKBytes);
 #pragma unroll
                 for (int sub = 0; sub < L::kSub; ++sub)
@@ -210,21 +221,25 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
             };
             for (int rnd = 0; rnd < rounds && ok; ++rnd) {
                 if (!item_of(rnd, it)) continue;
-                if (items > 0 && !mbar_wait(q_empty, (uint32_t)(items - 1) & 1u, err, abort_flag)) break;
-                mbar_arrive_expect_tx(q_full, L::kQBytes);
+                // Q buffer items % 2, free once item items - 2's S MMAs are done
+                const int qb = items & 1;
+                if (items >= 2 && !mbar_wait(q_empty(qb), (uint32_t)((items >> 1) - 1) & 1u, err, abort_flag)) break;
+                mbar_arrive_expect_tx(q_full(qb), L::kQBytes);
 #pragma unroll
                 for (int sub = 0; sub < L::kSub; ++sub)
-                    tma_load_3d(sQ + sub * 16384, &qmap, 64 * sub, it.qt * kQ, it.b * H + it.h, q_full);
+                    tma_load_3d(sQ + qb * L::kQBytes + sub * 16384, &qmap, 64 * sub, it.qt * kQ,
+                                it.b * H + it.h, q_full(qb));
                 ++items;
                 ok = load_k(it.j0);
                 for (int j = 1; j < it.n && ok; ++j) ok = load_k(it.j0 + j) && load_v(it.j0 + j - 1);
                 if (ok) ok = load_v(it.j0 + it.n - 1);
             }
             // Drain: the copies of every armed slot (and the last Q) must land.
-            if (items > 0) mbar_wait(q_full, (uint32_t)(items - 1) & 1u, err, abort_flag);
-            for (int s = 0; s < ST && s < kn; ++s) {
-                const int last = kn - 1 - ((kn - 1 - s) % ST);
-                mbar_wait(k_full(s), (uint32_t)((last / ST) & 1), err, abort_flag);
+            for (int k = items - 2 < 0 ? 0 : items - 2; k < items; ++k)
+                mbar_wait(q_full(k & 1), (uint32_t)(k >> 1) & 1u, err, abort_flag);
+            for (int s = 0; s < SK && s < kn; ++s) {
+                const int last = kn - 1 - ((kn - 1 - s) % SK);
+                mbar_wait(k_full(s), (uint32_t)((last / SK) & 1), err, abort_flag);
             }
             for (int s = 0; s < ST && s < vn; ++s) {
                 const int last = vn - 1 - ((vn - 1 - s) % ST);
@@ -247,27 +262,29 @@ __global__ void __launch_bounds__(kThreadsAtt, 1)
                 const uint64_t dq = umma_desc_sw128(sQ), dk = umma_desc_sw128(sK);
                 for (int rnd = 0; rnd < rounds && ok; ++rnd) {
                     if (!item_of(rnd, it)) continue;
-                    ok = mbar_wait(q_full, (uint32_t)items & 1u, err, abort_flag);
+                    const int qb = items & 1;
+                    ok = mbar_wait(q_full(qb), (uint32_t)(items >> 1) & 1u, err, abort_flag);
+                    const uint64_t dqi = dq + (uint64_t)((qb * L::kQBytes) >> 4);
                     for (int j = 0; j < it.n && ok; ++j, ++g) {
-                        const int sb = g & 1, st = g % ST;
+                        const int sb = g & 1, st = g % SK;
                         if (g >= 2 && !mbar_wait(p_full(sb), (uint32_t)((g - 2) >> 1) & 1u, err, abort_flag)) {
                             ok = false;
                             break;
                         }
-                        if (!mbar_wait(k_full(st), (uint32_t)(g / ST) & 1u, err, abort_flag)) { ok = false; break; }
+                        if (!mbar_wait(k_full(st), (uint32_t)(g / SK) & 1u, err, abort_flag)) { ok = false; break; }
                         tc_fence_after();
                         const uint32_t d = tmem_base + (uint32_t)(sb * kKV);
                         const uint64_t kb = dk + (uint64_t)((st * L::kKBytes) >> 4);
 #pragma unroll
                         for (int kk = 0; kk < DH / 16; ++kk) {
                             const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                            umma_bf16(d, dq + off, kb + off, idesc_s, kk > 0 ? 1u : 0u);
+                            umma_bf16(d, dqi + off, kb + off, idesc_s, kk > 0 ? 1u : 0u);
                         }
                         umma_commit(k_empty(st));
                         umma_commit(s_full(sb));
                     }
                     // The Q buffer may be refilled once this item's S MMAs are complete.
-                    if (ok) umma_commit(q_empty);
+                    if (ok) umma_commit(q_empty(qb));
                     ++items;
                 }
             } else {
