@@ -236,8 +236,9 @@ tfm_status tfm_forward_loss(void* handle, const int32_t* tokens, const int32_t* 
  * = n_layer, or n = 0 to make every layer full again.  Applies to every later
  * forward, loss and decode call of the handle (a decode step then reads only
  * the window's positions of the cache); recorded forwards and decode steps are
- * dropped and recorded again.  Windowed layers run the flash kernel with the
- * band's tile skip (the persistent tensor-core kernels serve full layers).
+ * dropped and recorded again.  Windowed layers run the same persistent
+ * tensor-core attention kernels with the band's tile skip (key tiles wholly
+ * before a query tile's window are never loaded).
  * Host only, not stream-ordered: call it between forwards.  TFM_EINVAL for
  * n not in {0, n_layer} or a negative window. */
 tfm_status tfm_set_attention_windows(void* handle, const int32_t* windows, int32_t n);

@@ -104,7 +104,7 @@ def _check(cfg, got, ref, label="windowed model"):
 @pytest.mark.parametrize("name,windows,B,S", [
     ("tiny", [5, 0], 2, 64),                 # fp32 mode
     ("small", [64, 0], 2, 300),              # d_head 32
-    ("gpt2s", [0, 100], 2, 256),             # d_head 64: the windowed layer leaves the tcgen05 kernel
+    ("gpt2s", [0, 100], 2, 256),             # d_head 64: the two-tile kernel with and without a window
     ("gqa", [129, 1000], 1, 384),            # d_head 128, GQA; the second window covers S
 ])
 def test_model_with_per_layer_windows(name, windows, B, S):
