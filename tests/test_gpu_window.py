@@ -104,6 +104,8 @@ def _check(cfg, got, ref, label="windowed model"):
 @pytest.mark.parametrize("name,windows,B,S", [
     ("tiny", [5, 0], 2, 64),                 # fp32 mode
     ("small", [64, 0], 2, 300),              # d_head 32
+    ("small", [100, 0], 3, 256),             # d_head 32 at 256 positions: the windowed layer on
+                                             # the two-tile kernel, the full one on the three-block one
     ("gpt2s", [0, 100], 2, 256),             # d_head 64: the two-tile kernel with and without a window
     ("gqa", [129, 1000], 1, 384),            # d_head 128, GQA; the second window covers S
 ])
