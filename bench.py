@@ -168,6 +168,42 @@ def window_rate(tfm, torch, stream, flush, peaks, window=1024, launches=10):
                    "recorded as graphs"}
 
 
+def attention_rate(tfm, torch, cfg, stream, flush, peaks, launches=20):
+    """The causal attention alone at the workload's shape (batch, heads, positions,
+    d_head; seeded random q, k, v), through tfm_causal_attention: CUDA events
+    around each launch, L2 flushed between launches.  Algorithmic flops: QK^T
+    and PV over the causal lower triangle including the diagonal."""
+    B, H, Hkv, S, dh = cfg.batch, cfg.n_head, cfg.n_kv_head, cfg.seq, cfg.d_head
+    g = torch.Generator(device="cuda").manual_seed(11)
+    dt = torch.bfloat16 if cfg.mode == "bf16" else torch.float32
+    q = torch.randn(B, H, S, dh, device="cuda", generator=g).to(dt)
+    k, v = (torch.randn(B, Hkv, S, dh, device="cuda", generator=g).to(dt) for _ in range(2))
+    o = torch.empty(B, S, H * dh, device="cuda", dtype=dt)
+    for _ in range(3):
+        tfm.causal_attention(q, k, v, o, stream=stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(launches)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        tfm.causal_attention(q, k, v, o, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    tfm.device_status()
+    us = sorted(a.elapsed_time(b) * 1e3 for a, b in ev)
+    med = us[len(us) // 2]
+    flops = accounting.attention_flops(B, H, S, dh)
+    ach = flops / (med * 1e-6) / 1e12
+    return {"shape": {"batch": B, "heads": H, "kv_heads": Hkv, "seq": S, "d_head": dh},
+            "median_us": round(med, 2), "min_us": round(us[0], 2), "achieved": round(ach, 1),
+            "unit": "TFLOP/s", "peak": peaks["bf16_tflops"],
+            "frac": round(ach / peaks["bf16_tflops"], 4),
+            "how": "tfm_causal_attention, CUDA events around each of 20 launches after 3 "
+                   "warm-up calls, L2 flushed before each launch; the events include the "
+                   "launch and the host-side tensor-map encoding of the component call"}
+
+
 def gpt2_kernel_work(cfg, B, S):
     """kernel_work for the GPT-2-style family: a single F-wide fc GEMM (GELU)
     instead of gate/up, LayerNorm reading a gain and a shift, the embedding
@@ -627,6 +663,9 @@ def parse():
     ap.add_argument("--loss-only", action="store_true",
                     help="only the fused cross-entropy measurement (--steps timed steps); prints "
                          "its JSON object alone")
+    ap.add_argument("--attention-only", action="store_true",
+                    help="only the causal attention at the workload's shape, through "
+                         "tfm_causal_attention; prints its JSON object alone")
     ap.add_argument("--decode-only", action="store_true",
                     help="only the incremental-decoding measurement (prefill, then decode "
                          "steps); prints its JSON object alone")
@@ -874,6 +913,10 @@ def main():
     graph = not args.no_graph
     if args.window_only:
         print(json.dumps({"window": window_rate(tfm, torch, stream, flush, load_peaks())}))
+        return
+    if args.attention_only:
+        print(json.dumps({"attention": attention_rate(tfm, torch, cfg, stream, flush, load_peaks()),
+                          "config": {"workload": WORKLOAD_TEXT[cfg.name]}}))
         return
     if args.gpt2_only:
         print(json.dumps({"gpt2_family": gpt2_rate(tfm, torch, stream, flush, load_peaks(),
