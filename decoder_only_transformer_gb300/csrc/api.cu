@@ -1483,10 +1483,11 @@ tfm_status tfm_device_status(void* handle) {
 
 tfm_status tfm_embedding(const int32_t* tokens, const void* E, float* h, int64_t M, int32_t V,
                          int32_t D, int32_t mode, void* stream) {
-    if (!tokens || !E || !h) return fail(TFM_EINVAL, "NULL pointer");
     if (M < 0 || V < 1 || D < 1) return fail(TFM_EINVAL, "bad sizes");
     if (mode != TFM_FP32 && mode != TFM_BF16) return fail(TFM_EINVAL, "bad mode");
     if (D % (mode == TFM_BF16 ? 8 : 4)) return fail(TFM_EINVAL, "D must be a multiple of %d", mode == TFM_BF16 ? 8 : 4);
+    if (M == 0) return TFM_OK;
+    if (!tokens || !E || !h) return fail(TFM_EINVAL, "NULL pointer");
     if (!tfm::aligned16(E) || !tfm::aligned16(h)) return fail(TFM_EINVAL, "E and h must be 16-byte aligned");
     if (!tfm::device_error_word()) return fail(TFM_ECUDA, "device error word unavailable");
     cudaError_t e = tfm::launch_embedding(tokens, E, h, M, V, D, mode == TFM_BF16,
@@ -1496,10 +1497,11 @@ tfm_status tfm_embedding(const int32_t* tokens, const void* E, float* h, int64_t
 
 tfm_status tfm_rmsnorm(const float* x, const float* g, void* y, int64_t M, int32_t D, float eps,
                        int32_t out_mode, void* stream) {
-    if (!x || !g || !y) return fail(TFM_EINVAL, "NULL pointer");
     if (M < 0 || D < 8 || D % 8) return fail(TFM_EINVAL, "D must be a positive multiple of 8");
     if (!(eps > 0.f)) return fail(TFM_EINVAL, "eps must be > 0");
     if (out_mode != TFM_FP32 && out_mode != TFM_BF16) return fail(TFM_EINVAL, "bad out_mode");
+    if (M == 0) return TFM_OK;
+    if (!x || !g || !y) return fail(TFM_EINVAL, "NULL pointer");
     if (!tfm::aligned16(x) || !tfm::aligned16(g) || !tfm::aligned16(y))
         return fail(TFM_EINVAL, "x, g, y must be 16-byte aligned");
     cudaError_t e = tfm::launch_rmsnorm(x, g, y, M, D, eps, out_mode == TFM_BF16,
@@ -1509,10 +1511,11 @@ tfm_status tfm_rmsnorm(const float* x, const float* g, void* y, int64_t M, int32
 
 tfm_status tfm_rope(void* x, const int32_t* positions, int32_t B, int32_t H, int32_t S, int32_t dh,
                     float theta, int32_t mode, void* stream) {
-    if (!x) return fail(TFM_EINVAL, "NULL x");
     if (B < 0 || H < 0 || S < 0 || dh < 2 || dh % 2 || dh > 256) return fail(TFM_EINVAL, "bad sizes");
     if (!(theta > 1.f)) return fail(TFM_EINVAL, "theta must be > 1");
     if (mode != TFM_FP32 && mode != TFM_BF16) return fail(TFM_EINVAL, "bad mode");
+    if ((int64_t)B * H * S == 0) return TFM_OK;
+    if (!x) return fail(TFM_EINVAL, "NULL x");
     cudaError_t e = tfm::launch_rope(x, positions, B, H, S, dh, theta, mode == TFM_BF16,
                                      static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TFM_OK : tfm::cuda_fail(e, "rope launch");
@@ -1527,29 +1530,30 @@ tfm_status tfm_causal_attention(const void* q, const void* k, const void* v, voi
 tfm_status tfm_causal_attention_window(const void* q, const void* k, const void* v, void* o,
                                        int32_t B, int32_t H, int32_t Hkv, int32_t S, int32_t dh,
                                        float scale, int32_t window, int32_t mode, void* stream) {
-    if (!q || !k || !v || !o) return fail(TFM_EINVAL, "NULL pointer");
     if (window < 0) return fail(TFM_EINVAL, "window must be >= 0");
     if (window >= S) window = 0;
     if (B < 0 || S < 0 || H < 1 || Hkv < 1 || H % Hkv) return fail(TFM_EINVAL, "bad head counts");
+    if (mode != TFM_FP32 && mode != TFM_BF16) return fail(TFM_EINVAL, "bad mode");
+    if (mode == TFM_BF16 && !tfm::attention_tc_supported(dh))
+        return fail(TFM_EUNSUPPORTED, "bf16 attention: dh in {32,64,128}");
+    if (mode == TFM_FP32 && (dh < 1 || dh > 128)) return fail(TFM_EUNSUPPORTED, "fp32 attention: dh <= 128");
+    if (B == 0 || S == 0) return TFM_OK;
+    if (!q || !k || !v || !o) return fail(TFM_EINVAL, "NULL pointer");
     if (!tfm::aligned16(q) || !tfm::aligned16(k) || !tfm::aligned16(v) || !tfm::aligned16(o))
         return fail(TFM_EINVAL, "q, k, v, o must be 16-byte aligned");
     if (scale <= 0.f) scale = 1.0f / std::sqrt((float)dh);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (mode == TFM_BF16) {
-        if (!tfm::attention_tc_supported(dh)) return fail(TFM_EUNSUPPORTED, "bf16 attention: dh in {32,64,128}");
         tfm::AttnPlan plan;
         tfm_status ps = tfm::plan_attention_tc(&plan, q, k, v, o, B, H, Hkv, S, dh, scale);
         if (ps != TFM_OK) return fail(ps, "could not encode attention tensor maps");
         plan.window = window;
         e = tfm::launch_attention_tc(plan, cs);
-    } else if (mode == TFM_FP32) {
-        if (dh < 1 || dh > 128) return fail(TFM_EUNSUPPORTED, "fp32 attention: dh <= 128");
+    } else {
         e = tfm::launch_attention_simt(static_cast<const float*>(q), static_cast<const float*>(k),
                                        static_cast<const float*>(v), static_cast<float*>(o), B, H,
                                        Hkv, S, dh, scale, cs, window);
-    } else {
-        return fail(TFM_EINVAL, "bad mode");
     }
     return e == cudaSuccess ? TFM_OK : tfm::cuda_fail(e, "attention launch");
 }
@@ -1564,16 +1568,16 @@ tfm_status tfm_decode_attention(const void* q, const void* k_cache, const void* 
                                 int32_t B, int32_t H, int32_t Hkv, int32_t max_seq, int32_t pos,
                                 int32_t dh, float scale, int32_t window, void* workspace,
                                 size_t workspace_bytes, void* stream) {
-    if (!q || !k_cache || !v_cache || !o || !workspace) return fail(TFM_EINVAL, "NULL pointer");
     if (B < 0 || H < 1 || Hkv < 1 || H % Hkv || max_seq < 1) return fail(TFM_EINVAL, "bad sizes");
     if (pos < 0 || pos >= max_seq) return fail(TFM_EINVAL, "pos=%d outside [0, max_seq=%d)", pos, max_seq);
     if (window < 0) return fail(TFM_EINVAL, "window must be >= 0");
-    if (!tfm::aligned16(q) || !tfm::aligned16(k_cache) || !tfm::aligned16(v_cache) ||
-        !tfm::aligned16(o) || !tfm::aligned16(workspace))
-        return fail(TFM_EINVAL, "pointers must be 16-byte aligned");
     if (!tfm::decode_supported(dh, H / Hkv))
         return fail(TFM_EUNSUPPORTED, "dh in {32, 64, 128}, H/Hkv in {1, 2, 4, 8, 16} (<= 8 at dh 128)");
     if (B == 0) return TFM_OK;
+    if (!q || !k_cache || !v_cache || !o || !workspace) return fail(TFM_EINVAL, "NULL pointer");
+    if (!tfm::aligned16(q) || !tfm::aligned16(k_cache) || !tfm::aligned16(v_cache) ||
+        !tfm::aligned16(o) || !tfm::aligned16(workspace))
+        return fail(TFM_EINVAL, "pointers must be 16-byte aligned");
     if (workspace_bytes < tfm_decode_attention_workspace_bytes(B, H, max_seq, dh))
         return fail(TFM_EINVAL, "workspace too small");
     if (scale <= 0.f) scale = 1.0f / std::sqrt((float)dh);
@@ -1599,25 +1603,25 @@ tfm_status tfm_decode_attention(const void* q, const void* k_cache, const void* 
 
 tfm_status tfm_linear(const void* x, const void* W, void* y, int64_t M, int32_t N, int32_t K,
                       int64_t ldy, int32_t out_fp32, int32_t accumulate, int32_t mode, void* stream) {
-    if (!x || !W || !y) return fail(TFM_EINVAL, "NULL pointer");
     if (M < 0 || M > INT32_MAX || N < 1 || K < 1 || ldy < N || ldy % 8) return fail(TFM_EINVAL, "bad sizes");
-    if (!tfm::aligned16(x) || !tfm::aligned16(W) || !tfm::aligned16(y)) return fail(TFM_EINVAL, "pointers must be 16-byte aligned");
+    if (mode != TFM_FP32 && mode != TFM_BF16) return fail(TFM_EINVAL, "bad mode");
     if (!out_fp32 && (accumulate || mode != TFM_BF16)) return fail(TFM_EINVAL, "bf16 output: bf16 mode, no accumulate");
+    if (mode == TFM_BF16 && K % 8) return fail(TFM_EINVAL, "bf16 mode: K %% 8 == 0");
+    if (M == 0) return TFM_OK;
+    if (!x || !W || !y) return fail(TFM_EINVAL, "NULL pointer");
+    if (!tfm::aligned16(x) || !tfm::aligned16(W) || !tfm::aligned16(y)) return fail(TFM_EINVAL, "pointers must be 16-byte aligned");
     const int kind = out_fp32 ? (accumulate ? tfm::EPI_ACCUM_F32 : tfm::EPI_STORE_F32) : tfm::EPI_STORE_BF16;
     tfm::EpiParams epi = tfm::epi_basic(kind, (int)M, N, y, ldy);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (mode == TFM_BF16) {
-        if (K % 8) return fail(TFM_EINVAL, "bf16 mode: K %% 8 == 0");
         tfm::GemmPlan plan;
         tfm_status st = tfm::plan_gemm_tc(&plan, x, K, W, nullptr, K, (int)M, N, K, epi);
         if (st != TFM_OK) return fail(st, "tensor map encoding failed");
         e = tfm::launch_gemm_tc(plan, cs);
-    } else if (mode == TFM_FP32) {
+    } else {
         e = tfm::launch_gemm_simt(static_cast<const float*>(x), static_cast<const float*>(W), nullptr,
                                   (int)M, N, K, epi, cs);
-    } else {
-        return fail(TFM_EINVAL, "bad mode");
     }
     return e == cudaSuccess ? TFM_OK : tfm::cuda_fail(e, "linear launch");
 }
@@ -1630,14 +1634,15 @@ size_t tfm_swiglu_workspace_bytes(int64_t M, int32_t F, int32_t mode) {
 tfm_status tfm_swiglu(const void* x, const void* w1, const void* w3, const void* w2, float* y,
                       int64_t M, int32_t D, int32_t F, int32_t accumulate, void* workspace,
                       size_t workspace_bytes, int32_t mode, void* stream) {
-    if (!x || !w1 || !w3 || !w2 || !y || !workspace) return fail(TFM_EINVAL, "NULL pointer");
     if (M < 0 || M > INT32_MAX || D < 1 || F < 1) return fail(TFM_EINVAL, "bad sizes");
     if (mode != TFM_FP32 && mode != TFM_BF16) return fail(TFM_EINVAL, "bad mode");
+    if (D % 8 || F % 8) return fail(TFM_EINVAL, "D and F must be multiples of 8");
+    if (M == 0) return TFM_OK;
+    if (!x || !w1 || !w3 || !w2 || !y || !workspace) return fail(TFM_EINVAL, "NULL pointer");
     if (workspace_bytes < tfm_swiglu_workspace_bytes(M, F, mode)) return fail(TFM_EINVAL, "workspace too small");
     if (!tfm::aligned16(x) || !tfm::aligned16(w1) || !tfm::aligned16(w3) || !tfm::aligned16(w2) ||
         !tfm::aligned16(y) || !tfm::aligned16(workspace))
         return fail(TFM_EINVAL, "pointers must be 16-byte aligned");
-    if (D % 8 || F % 8) return fail(TFM_EINVAL, "D and F must be multiples of 8");
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     tfm::EpiParams eg = tfm::epi_basic(tfm::EPI_SWIGLU, (int)M, F, workspace, F);
     tfm::EpiParams ed = tfm::epi_basic(accumulate ? tfm::EPI_ACCUM_F32 : tfm::EPI_STORE_F32, (int)M,

@@ -347,7 +347,10 @@ const char* tfm_profile_kind_name(int32_t kind);
 
 /* ---------------------------------------------------------------- components
  * Single operations on caller buffers (device pointers), for testing each step
- * against the oracle and for callers that assemble their own model. */
+ * against the oracle and for callers that assemble their own model.
+ * Empty calls (M = 0; B, H or S = 0 for RoPE; B or S = 0 for attention; B = 0
+ * for decode attention) check their other arguments, then return TFM_OK
+ * without launching anything or reading any pointer, which may then be NULL. */
 
 /* Embedding lookup (CS336 walkthrough, section 5.2): h[m, :] = E[tokens[m], :]
  * as fp32.  tokens [M] int32; E [V, D] bf16 or fp32 (mode); h [M, D] fp32.

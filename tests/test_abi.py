@@ -80,6 +80,41 @@ def test_null_arguments_are_rejected_on_the_host(lib):
     lib.tfm_destroy(None)
 
 
+def test_empty_calls_return_ok_on_the_host(lib):
+    """Empty component calls check their sizes and modes, then return before
+    touching a pointer or the device (so this runs without a GPU)."""
+    B16, F32 = tfm.TFM_BF16, tfm.TFM_FP32
+    assert lib.tfm_embedding(None, None, None, 0, 10, 64, B16, None) == tfm.TFM_OK
+    assert lib.tfm_rmsnorm(None, None, None, 0, 64, 1e-5, B16, None) == tfm.TFM_OK
+    assert lib.tfm_rope(None, None, 0, 4, 16, 32, 1e4, B16, None) == tfm.TFM_OK
+    assert lib.tfm_rope(None, None, 2, 4, 0, 32, 1e4, F32, None) == tfm.TFM_OK
+    for mode in (B16, F32):
+        for B, S in ((0, 16), (2, 0)):
+            assert lib.tfm_causal_attention(None, None, None, None, B, 4, 2, S, 64, 0.0, mode,
+                                            None) == tfm.TFM_OK
+            assert lib.tfm_causal_attention_window(None, None, None, None, B, 4, 2, S, 64, 0.0,
+                                                   4, mode, None) == tfm.TFM_OK
+        assert lib.tfm_linear(None, None, None, 0, 16, 64, 16, 1, 1, mode, None) == tfm.TFM_OK
+        assert lib.tfm_swiglu(None, None, None, None, None, 0, 64, 176, 0, None, 0, mode,
+                              None) == tfm.TFM_OK
+    assert lib.tfm_decode_attention(None, None, None, None, 0, 4, 4, 16, 3, 64, 0.0, 0, None, 0,
+                                    None) == tfm.TFM_OK
+    # the other arguments are still checked
+    assert lib.tfm_rmsnorm(None, None, None, 0, 60, 1e-5, B16, None) == tfm.TFM_EINVAL
+    assert lib.tfm_linear(None, None, None, 0, 16, 60, 16, 1, 0, B16, None) == tfm.TFM_EINVAL
+    assert lib.tfm_linear(None, None, None, 0, 16, 64, 16, 0, 1, B16, None) == tfm.TFM_EINVAL
+    assert lib.tfm_causal_attention(None, None, None, None, 0, 4, 2, 16, 48, 0.0, B16,
+                                    None) == tfm.TFM_EUNSUPPORTED
+    assert lib.tfm_causal_attention(None, None, None, None, 0, 4, 3, 16, 64, 0.0, B16,
+                                    None) == tfm.TFM_EINVAL
+    assert lib.tfm_swiglu(None, None, None, None, None, 0, 64, 170, 0, None, 0, B16,
+                          None) == tfm.TFM_EINVAL
+    assert lib.tfm_decode_attention(None, None, None, None, 0, 4, 4, 16, 16, 64, 0.0, 0, None, 0,
+                                    None) == tfm.TFM_EINVAL
+    assert lib.tfm_rope(None, None, 0, 4, 16, 33, 1e4, B16, None) == tfm.TFM_EINVAL
+    assert lib.tfm_forward(None, None, 0, 1, None, 8, None) == tfm.TFM_EINVAL
+
+
 def test_workspace_grows_with_batch(lib):
     a = tfm.workspace_bytes(_cfg(max_batch=1))
     b = tfm.workspace_bytes(_cfg(max_batch=4))

@@ -248,3 +248,43 @@ def test_swiglu(bf16, M, D, F):
     y = dev(h0, torch.float32)
     tfm.swiglu(*args, y, ws, accumulate=True)
     assert rel_err(y.cpu().numpy() - h0, ref) < 2 * tol
+
+
+# ---------------------------------------------------------------- empty calls
+def test_empty_calls_are_no_ops():
+    """Zero rows (or zero sequences / positions) return OK and write nothing:
+    once with empty torch tensors (NULL pointers), once with zero-row views of
+    a live buffer whose contents must survive."""
+    D, F, V, H, dh = 64, 176, 50, 4, 32
+    bf = torch.bfloat16
+    sentinel = torch.full((4096,), 7.0, device="cuda")
+    e_bf = torch.empty((V, D), dtype=bf, device="cuda")
+    g = torch.ones(D, device="cuda")
+    w = torch.zeros((F, D), dtype=bf, device="cuda")
+    w2 = torch.zeros((D, F), dtype=bf, device="cuda")
+    for live in (False, True):
+        def rows(n_cols, dtype=torch.float32):
+            if live:
+                return sentinel.view(dtype)[:0].view(0, n_cols)
+            return torch.empty((0, n_cols), dtype=dtype, device="cuda")
+        none = rows(1, torch.uint8).view(-1)
+        tfm.embedding(rows(1, torch.int32).view(-1), e_bf, rows(D))
+        tfm.rmsnorm(rows(D), g, rows(D, bf))
+        tfm.linear(rows(D, bf), w, rows(F))
+        tfm.linear(rows(D, bf), w, rows(F, bf))
+        tfm.linear(rows(D), w.float(), rows(F))
+        tfm.swiglu(rows(D, bf), w, w, w2, rows(D), none)
+        tfm.swiglu(rows(D), w.float(), w.float(), w2.float(), rows(D), none)
+        for shape in ((0, H, 40, dh), (2, H, 0, dh)):
+            q = rows(dh, bf).reshape(shape)
+            for dt in (bf, torch.float32):
+                qq = q.to(dt)
+                tfm.causal_attention(qq, qq, qq, rows(H * dh, dt))
+                tfm.causal_attention_window(qq, qq, qq, rows(H * dh, dt), 8)
+                tfm.rope(qq, 10000.0)
+        cache = torch.zeros((1, H, 16, dh), dtype=bf, device="cuda")
+        tfm.decode_attention(rows(H * dh, bf).view(0, H, dh), cache, cache, rows(H * dh, bf), 3,
+                             none)
+    torch.cuda.synchronize()
+    assert torch.equal(sentinel, torch.full_like(sentinel, 7.0))
+    tfm.device_status()
