@@ -42,7 +42,22 @@
 // columns) allows no second item in flight.  Two reorganisations measured
 // slower (21.7 us): issuer warps that poll every block's barriers and issue
 // whichever is ready, with block 1's output handed over through shared memory;
-// and warpgroups that issue their own products.
+// and warpgroups that issue their own products.  Also measured against this
+// kernel on one box (per-CTA clock stamps, 13.3 us for the whole launch with q,
+// k, v in L2), none kept:
+//   - tile A's 32-row groups loaded in reverse order, so that the heavy rows of
+//     the two diagonal blocks fall on different schedulers: 14.3 us.  Block 2
+//     runs about one step of the pipeline behind blocks 0 and 1, so the two
+//     triangles never overlap and the reversal only moves the heavy scheduler.
+//   - P handed to the P.V issuer 32 keys at a time, so that the products run
+//     under the exponentials: 15-20 us.  The issuing thread gets about a quarter
+//     of its scheduler's issue slots, and per-chunk waits and fences on it delay
+//     every block's output; a second issuer for block 1 (15-16.5 us) and polling
+//     with a short sleep (no change) did not recover it.
+//   - the masking test written per score as (diagonal chunk and column past the
+//     row) or (column past the sequence): the exponential pass took twice as
+//     long as with one precomputed threshold per chunk.  Every instruction per
+//     score counts in that loop.
 #include <climits>
 
 #include "common.cuh"
