@@ -42,8 +42,13 @@
 // with a setmaxnreg split: long 139 -> 164 us, gpt2s 28 -> 33 us.)  An MMA warp
 // shares its scheduler with two softmax warps, which leaves it few issue slots;
 // one thread issuing all ~24 MMAs of a key tile was measured to be the bound,
-// hence two issuing threads.  All waits are bounded; tiles above the diagonal
-// are never loaded.
+// hence two issuing threads.  Making the two warps of a lane quarter (one per
+// tile, same scheduler) take turns at the exponentials, as a strict A, B, A, ...
+// alternation through a pair of barriers per quarter, was measured slower
+// (long attention 154 -> 170 us, whole launch): one warp alone runs the
+// exponentials at ~6 cycles per ex2, two in step at ~4.3, the special-function
+// unit's rate.  All waits are bounded; tiles above the diagonal are never
+// loaded.
 #include <climits>
 
 #include "common.cuh"
