@@ -58,6 +58,12 @@
 //     row) or (column past the sequence): the exponential pass took twice as
 //     long as with one precomputed threshold per chunk.  Every instruction per
 //     score counts in that loop.
+//   - P in shared memory (128-byte swizzled, the A operand of P.V) instead of
+//     over S, so that the next item's S_x is issued as soon as the softmax has
+//     read S_x: 13.7-14.7 us with two item buffers (the shared-memory budget),
+//     also with Q/K and V released separately and with the reversed groups.
+//     The three blocks then run side by side and each exponential pass slows
+//     down as much as the chain got shorter.
 #include <climits>
 
 #include "common.cuh"
