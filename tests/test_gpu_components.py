@@ -140,6 +140,8 @@ def test_attention_fp32(B, H, Hkv, S, dh):
 @pytest.mark.parametrize("B,H,Hkv,S,dh", [
     (1, 2, 2, 1, 64), (2, 2, 2, 63, 64), (1, 3, 3, 64, 64), (1, 2, 2, 65, 32),
     (2, 4, 2, 200, 128), (1, 4, 1, 257, 64), (1, 2, 2, 1024, 64), (2, 4, 4, 256, 32),
+    # d_head 128: one position (MQA), one row into the second query tile
+    (1, 4, 1, 1, 128), (1, 2, 2, 129, 128),
     # more work items than SMs, so every CTA of the persistent kernels walks
     # several items: 384 query tiles (d_head 128, ragged S), 256 tile pairs
     # (d_head 64, an odd tile count: the last pair has no second tile)
