@@ -258,17 +258,22 @@ __global__ void __launch_bounds__(kDecThreads) k_decode_partial(
     }
 }
 
-// One warp per (sequence, head): combine the chunks, write o[b, h*DH + d] bf16.
+// One CTA per (sequence, head) combines the chunks and writes o[b, h*DH + d]
+// bf16: warp w owns columns [32 w, 32 w + 32), lane c takes chunk c0 + c (and
+// c0 + c + 32, ...), so each chunk's max, sum and 32 columns are requested
+// together and the combine costs one L2 round trip; the lanes' weighted column
+// vectors are then summed through shared memory.
 template <int DH>
-__global__ void __launch_bounds__(128) k_decode_combine(const float* __restrict__ part,
-                                                       __nv_bfloat16* __restrict__ o, int BH,
-                                                       int H, int nch_stride,
-                                                       const int* __restrict__ pos_dev,
-                                                       int window) {
+__global__ void __launch_bounds__(DH) k_decode_combine(const float* __restrict__ part,
+                                                      __nv_bfloat16* __restrict__ o, int BH,
+                                                      int H, int nch_stride,
+                                                      const int* __restrict__ pos_dev,
+                                                      int window) {
+    __shared__ float red[DH / 32][32][33];           // [warp][lane][column], padded
     pdl_wait();
     pdl_trigger();
-    const int w = (int)(blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5));
-    const int lane = threadIdx.x & 31;
+    const int w = (int)blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (w >= BH) return;
     constexpr int NK = dec_keys(DH);
     const int pos = __ldg(pos_dev);
@@ -277,30 +282,48 @@ __global__ void __launch_bounds__(128) k_decode_combine(const float* __restrict_
     const int c0 = ws / NK;                          // the first chunk in the window
     if (nch - c0 == 1) return;                       // written by the chunk kernel itself
     const float* p = part + (int64_t)w * nch_stride * (DH + 2);
-    // chunk statistics with one chunk per lane, so their loads go out together
-    float M = -INFINITY;
-    for (int c = c0 + lane; c < nch; c += 32) M = fmaxf(M, p[c * (DH + 2) + DH]);
+    float M = -INFINITY, L = 0.f;
+    float acc[32];
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
-    float l = 0.f;
-    for (int c = c0 + lane; c < nch; c += 32) l += exp2f(p[c * (DH + 2) + DH] - M) * p[c * (DH + 2) + DH + 1];
+    for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+    for (int cb = c0; cb < nch; cb += 32) {
+        const int c = cb + lane;
+        const bool has = c < nch;
+        const float* pc = p + (int64_t)(has ? c : c0) * (DH + 2);
+        const float mc = has ? pc[DH] : -INFINITY;
+        const float lc = has ? pc[DH + 1] : 0.f;
+        // a chunk's record is DH + 2 floats (even, so 8-byte aligned, not 16)
+        float2 v[16];
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) l += __shfl_xor_sync(0xffffffffu, l, s);
-    float acc[DH / 32];
+        for (int j = 0; j < 16; ++j)
+            v[j] = has ? *reinterpret_cast<const float2*>(pc + 32 * warp + 2 * j)
+                       : make_float2(0.f, 0.f);
+        // running max over the chunks seen so far (all lanes), rescaling what
+        // earlier groups of 32 chunks accumulated
+        float mb = mc;
 #pragma unroll
-    for (int i = 0; i < DH / 32; ++i) acc[i] = 0.f;
-#pragma unroll 4
-    for (int c = c0; c < nch; ++c) {
-        const float* pc = p + c * (DH + 2);
-        const float wgt = exp2f(pc[DH] - M);
+        for (int s2 = 16; s2 > 0; s2 >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, s2));
+        const float Mn = fmaxf(M, mb);
+        const float keep = M == -INFINITY ? 0.f : exp2f(M - Mn);
+        const float wgt = has ? exp2f(mc - Mn) : 0.f;
+        L = L * keep + wgt * lc;
 #pragma unroll
-        for (int i = 0; i < DH / 32; ++i) acc[i] = fmaf(wgt, pc[lane + 32 * i], acc[i]);
+        for (int j = 0; j < 16; ++j) {
+            acc[2 * j] = acc[2 * j] * keep + wgt * v[j].x;
+            acc[2 * j + 1] = acc[2 * j + 1] * keep + wgt * v[j].y;
+        }
+        M = Mn;
     }
-    const float inv = 1.0f / l;
-    const int b = w / H, h = w - b * H;
-    __nv_bfloat16* dst = o + (int64_t)b * H * DH + (int64_t)h * DH;
 #pragma unroll
-    for (int i = 0; i < DH / 32; ++i) dst[lane + 32 * i] = __float2bfloat16_rn(acc[i] * inv);
+    for (int s2 = 16; s2 > 0; s2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, s2);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) red[warp][lane][j] = acc[j];
+    __syncwarp();
+    float t = 0.f;
+#pragma unroll 8
+    for (int r = 0; r < 32; ++r) t += red[warp][r][lane];
+    const int b = w / H, h = w - b * H;
+    o[(int64_t)b * H * DH + (int64_t)h * DH + 32 * warp + lane] = __float2bfloat16_rn(t / L);
 }
 
 template <int DH, int G>
@@ -326,7 +349,7 @@ cudaError_t decode_launch(const void* q, const void* kc, const void* vc, float* 
                                device_error_word());
     if (e != cudaSuccess) return e;
     const int BH = B * H;
-    return launch_pdl(k_decode_combine<DH>, dim3((unsigned)((BH + 3) / 4)), dim3(128), 0, st,
+    return launch_pdl(k_decode_combine<DH>, dim3((unsigned)BH), dim3(DH), 0, st,
                       static_cast<const float*>(part), static_cast<__nv_bfloat16*>(o), BH, H, nch,
                       pos_dev, window);
 }
