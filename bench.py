@@ -47,6 +47,11 @@ WORKLOAD_TEXT = {
 }
 
 
+# Keys per decode-attention chunk times d_head (the library's chunking: 16 KB of K
+# per chunk), for the bytes of the partial results each chunk writes and the merge reads.
+DECODE_CHUNK = 8192
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -394,7 +399,7 @@ def decode_rate(tfm, torch, model, cfg, tok_np, stream, peaks, steps=32):
     nbytes = 0
     for t in range(steps):
         L = S0 + t + 1
-        nch = (L + 16384 // dh - 1) // (16384 // dh)   # chunks of 16384 / dh keys
+        nch = (L + DECODE_CHUNK // dh - 1) // (DECODE_CHUNK // dh)   # chunks of DECODE_CHUNK / dh keys
         nbytes += (2 * B * Hkv * L * dh * 2 + 2 * B * H * dh * 2
                    + 2 * B * H * nch * (dh + 2) * 4) * cfg.n_layer
     gbs = nbytes / (att_ms / 1e3) / 1e9 if att_ms > 0 else None
@@ -427,7 +432,7 @@ def decode_rate(tfm, torch, model, cfg, tok_np, stream, peaks, steps=32):
         b_.record(stream)
     torch.cuda.synchronize()
     us_a = sum(a.elapsed_time(b_) for a, b_ in ev_a) / len(ev_a) * 1e3
-    nk = 16384 // dh
+    nk = DECODE_CHUNK // dh
     bytes_a = (2 * B * Hkv * S * dh * 2 + 2 * B * H * dh * 2
                + 2 * B * H * ((S + nk - 1) // nk) * (dh + 2) * 4)
     gbs_a = bytes_a / (us_a * 1e-6) / 1e9

@@ -10,15 +10,18 @@
 // tensor cores to tile, and the work is reading the cache: the kernel is bound by
 // HBM bandwidth, so it runs on the CUDA cores and splits the keys over many CTAs
 // (flash-decoding): CTA (b, g, c) takes the G = H / Hkv query heads that read kv
-// head g of sequence b against the c-th chunk of NK = 16384 / dh keys, writes the
+// head g of sequence b against the c-th chunk of NK = 8192 / dh keys, writes the
 // partial row max m (log2 domain), row sum l and unnormalised output o per head,
 // and a second kernel combines the chunks exactly: with M = max_c m_c,
 // o = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c.
 //
 // Bandwidth comes from bytes in flight: a CTA fetches its whole K and V chunk
-// (32 KB each, contiguous in the cache layout) with two bulk asynchronous copies
+// (16 KB each, contiguous in the cache layout) with two bulk asynchronous copies
 // at its start, so the chunk costs one DRAM round trip instead of one per load
-// wave, and several CTAs per SM keep ~200 KB per SM in flight.  Positions before
+// wave, and several CTAs per SM keep ~150 KB per SM in flight.  (Chunks of 32 KB
+// measured slower at long caches: long 176.9 vs 182.0 us per step, gpt2s 426.4 vs
+// 433.6 us; 8 KB slower again at gqa, whose 17 MB per layer are over 256 CTAs
+// either way.)  Positions before
 // the new one were written by earlier launches and are copied before the grid
 // dependency wait, overlapping the QKV projection's tail; the new token's row
 // (written by the launch just before) and q are read after it.  The math then
@@ -33,7 +36,7 @@ namespace {
 
 constexpr int kDecThreads = 128;
 constexpr int kDecNW = kDecThreads / 32;
-__host__ __device__ constexpr int dec_keys(int dh) { return 16384 / dh; }   // keys per CTA: 32 KB of K
+__host__ __device__ constexpr int dec_keys(int dh) { return 8192 / dh; }   // keys per CTA: 16 KB of K
 
 // Dynamic shared memory of one CTA.
 template <int DH, int G>

@@ -400,7 +400,7 @@ tfm_status tfm_causal_attention_window(const void* q, const void* k, const void*
  * [max(0, pos - window + 1), pos] (window 0: all of [0, pos]), query head h
  * reading kv head h / (H / Hkv); scale <= 0 means 1/sqrt(dh).  bf16 only;
  * dh in {32, 64, 128}; H / Hkv in {1, 2, 4, 8, 16} (<= 8 at dh 128).  The keys
- * are split over CTAs in chunks of 16384/dh positions, each fetched by bulk
+ * are split over CTAs in chunks of 8192/dh positions, each fetched by bulk
  * asynchronous copies, and the chunks are merged exactly by a second kernel.
  * workspace: device, 16-byte aligned, at least
  * tfm_decode_attention_workspace_bytes(B, H, max_seq, dh) bytes, not used by

@@ -5,7 +5,7 @@ A decode step at position p must give the logits of row p of the forward over
 the sequence extended by the new token: checked against the CPU oracle (float64
 forward over the whole extended sequence, the tolerances of the forward tests)
 and against the GPU's own forward (bf16 rounding differs only inside attention).
-The steps cross the decode kernel's key chunks (16384 / d_head keys each), so a
+The steps cross the decode kernel's key chunks (8192 / d_head keys each), so a
 step's new key lands both inside a chunk and as the first key of a new one."""
 import numpy as np
 import pytest
@@ -36,10 +36,10 @@ def _model(cfg, w, B, S):
 
 
 @pytest.mark.parametrize("name,B,S0,T", [
-    ("small", 2, 505, 12),        # d_head 32: 512-key chunks, crosses the first
-    ("gpt2s", 3, 250, 10),        # d_head 64: 256-key chunks, crosses the first
+    ("small", 2, 505, 12),        # d_head 32: 256-key chunks, crosses key 512
+    ("gpt2s", 3, 250, 10),        # d_head 64: 128-key chunks, crosses key 256
     ("gpt2s", 1, 37, 3),          # one chunk, partly filled
-    ("gqa", 2, 380, 6),           # d_head 128, 4 query heads per kv head: crosses key 384
+    ("gqa", 2, 380, 6),           # d_head 128 (64-key chunks), 4 query heads per kv head: crosses key 384
 ])
 def test_decode_matches_oracle_and_forward(name, B, S0, T):
     cfg = workloads.get_config(name).replace(n_layer=2, vocab=3001)
@@ -144,12 +144,13 @@ def test_decode_replay_matches_direct(name):
 
 
 @pytest.mark.parametrize("dh,H,Hkv,pos,window", [
-    (32, 8, 8, 700, 0),          # 512-key chunks: two
-    (64, 12, 3, 255, 0),         # the last key of the first 256-key chunk
-    (64, 12, 3, 256, 100),       # the first key of the second chunk, windowed
-    (128, 16, 4, 1000, 0),       # 128-key chunks, GQA
-    (128, 16, 2, 127, 0),        # one chunk
-    (128, 8, 8, 383, 200),       # window over three chunks
+    (32, 8, 8, 700, 0),          # 256-key chunks: three
+    (64, 12, 3, 255, 0),         # the last key of the second 128-key chunk
+    (64, 12, 3, 256, 100),       # the first key of the third chunk, windowed
+    (128, 16, 4, 1000, 0),       # 64-key chunks, GQA
+    (128, 16, 2, 63, 0),         # one chunk, filled
+    (128, 16, 2, 127, 0),        # the last key of the second chunk
+    (128, 8, 8, 383, 200),       # window over four chunks
 ])
 def test_decode_attention_component(dh, H, Hkv, pos, window):
     """tfm_decode_attention against the last row of the oracle's causal

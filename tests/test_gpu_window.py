@@ -127,9 +127,9 @@ def test_model_with_per_layer_windows(name, windows, B, S):
 
 
 @pytest.mark.parametrize("name,windows,B,S0,T", [
-    ("small", [40, 0], 2, 500, 20),          # 512-key chunks; the window inside one chunk
-    ("gpt2s", [300, 10], 2, 250, 12),        # 256-key chunks: the window spans two, crosses one
-    ("gqa", [200, 0], 1, 380, 8),            # 128-key chunks, GQA
+    ("small", [40, 0], 2, 500, 20),          # 256-key chunks; the window crosses key 512
+    ("gpt2s", [300, 10], 2, 250, 12),        # 128-key chunks: the window spans three, crosses key 256
+    ("gqa", [200, 0], 1, 380, 8),            # 64-key chunks, GQA
 ])
 def test_decode_with_windows(name, windows, B, S0, T):
     cfg = workloads.get_config(name).replace(n_layer=2, vocab=3001)
