@@ -72,3 +72,21 @@ def test_single_rank_needs_no_process_group():
     assert bench.job_rate(1, 1000, 4, 2000.0) == pytest.approx(2000.0)
     t0 = bench.rank_tokens(workloads.get_config("tiny"), 0)
     assert np.array_equal(t0, workloads.make_tokens(workloads.get_config("tiny")))
+
+
+def test_reference_arm_runs_on_rank_zero_only(capsys):
+    """bench.py --impl reference: rank 0 times the oracle and prints one JSON line
+    with the reference fields; any other rank returns without work or output."""
+    import argparse
+    import json
+    args = argparse.Namespace(config="tiny", steps=1, warmup=0, gpus=2)
+    bench.run_reference(args, world=2, rank=1)
+    assert capsys.readouterr().out == ""
+    bench.run_reference(args, world=2, rank=0)
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["n_gpus"] == 2
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
