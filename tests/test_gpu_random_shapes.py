@@ -187,3 +187,51 @@ def test_decode_attention(B, H, Hkv, max_seq, pos, dh, window):
     qf[:, :, pos] = q
     ref = oracle.causal_attention(qf, kc[:, :, :pos + 1], vc[:, :, :pos + 1], window=window)
     assert rel_err(o.float().cpu().numpy(), ref[:, :, pos].reshape(B, H * dh)) < TOL_BF16
+
+
+def _model_cases(n, mode):
+    out = []
+    while len(out) < n:
+        if mode == "bf16":
+            dh = int(_G.choice([32, 64, 128]))
+            h = _ri(1, 8)
+            if (h * dh) % 64:
+                continue
+            d_ff, vocab, s_max = 8 * _ri(8, 200), _ri(50, 6000), 300
+        else:
+            dh = int(_G.choice([8, 16, 24, 40, 64]))
+            h = _ri(1, 6)
+            d_ff, vocab, s_max = 4 * _ri(4, 100), _ri(10, 500), 100
+        hkv = int(_G.choice([d for d in range(1, h + 1) if h % d == 0]))
+        out.append((mode, vocab, h * dh, h, hkv, _ri(1, 2), d_ff, _ri(1, 3), _ri(1, s_max)))
+    return out
+
+
+MODELS = _model_cases(6, "bf16") + _model_cases(3, "fp32")
+
+
+@pytest.mark.parametrize("mode,vocab,d_model,n_head,n_kv_head,n_layer,d_ff,B,S", MODELS)
+def test_forward(mode, vocab, d_model, n_head, n_kv_head, n_layer, d_ff, B, S):
+    """The whole forward of a random model (its plan: tile shapes, kernels per
+    d_head, GQA packing, ragged vocabulary) against the oracle's forward."""
+    from helpers import argmax_check, to_torch_weights
+    base = workloads.get_config("small" if mode == "bf16" else "tiny")
+    cfg = base.replace(vocab=vocab, d_model=d_model, n_head=n_head, n_kv_head=n_kv_head,
+                       n_layer=n_layer, d_ff=d_ff)
+    key = zlib.crc32(repr((mode, vocab, d_model, n_head, n_layer, d_ff, B, S)).encode())
+    w = workloads.make_weights(cfg, gains="random", seed=key % 100000)
+    tok = workloads.make_tokens(cfg, batch=B, seq=S, seed=key % 99991)
+    model = tfm.Model(cfg, max_batch=B, max_seq=S)
+    model.load_weights(to_torch_weights(w, bf16=mode == "bf16"))
+    ld = (vocab + 3) // 4 * 4
+    logits = torch.full((B * S, ld), float("nan"), device="cuda")
+    model.forward(torch.from_numpy(tok).cuda(), logits)
+    tfm.device_status()
+    got = logits.cpu().numpy()
+    model.close()
+    assert np.all(np.isnan(got[:, vocab:]))
+    got = got[:, :vocab].reshape(B, S, vocab)
+    ref = oracle.forward(tok, w, cfg)
+    assert rel_err(got, ref) < (2e-2 if mode == "bf16" else 1e-4)
+    argmax_check(f"random {mode} V{vocab} D{d_model} H{n_head}/{n_kv_head} L{n_layer} {B}x{S}",
+                 mode, got, ref)
