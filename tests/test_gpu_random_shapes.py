@@ -235,3 +235,51 @@ def test_forward(mode, vocab, d_model, n_head, n_kv_head, n_layer, d_ff, B, S):
     assert rel_err(got, ref) < (2e-2 if mode == "bf16" else 1e-4)
     argmax_check(f"random {mode} V{vocab} D{d_model} H{n_head}/{n_kv_head} L{n_layer} {B}x{S}",
                  mode, got, ref)
+
+
+def _decode_model_cases(n):
+    out = []
+    while len(out) < n:
+        m = _model_cases(1, "bf16")[0]
+        if m[3] // m[4] in (1, 2, 4, 8):          # the decode kernel's query-to-kv groups
+            out.append((m[1], m[2], m[3], m[4], m[5], m[6], _ri(1, 4), _ri(1, 400), _ri(1, 8)))
+    return out
+
+
+DECODE_MODELS = _decode_model_cases(4)
+
+
+@pytest.mark.parametrize("vocab,d_model,n_head,n_kv_head,n_layer,d_ff,B,S0,T", DECODE_MODELS)
+def test_decode_steps(vocab, d_model, n_head, n_kv_head, n_layer, d_ff, B, S0, T):
+    """Prefill S0 positions of a random model, then T decode steps, against the
+    GPU forward (1e-2) and the oracle (2e-2) over the extended sequences."""
+    from helpers import argmax_check, to_torch_weights
+    cfg = workloads.get_config("small").replace(vocab=vocab, d_model=d_model, n_head=n_head,
+                                                n_kv_head=n_kv_head, n_layer=n_layer, d_ff=d_ff)
+    key = zlib.crc32(repr(("decode", vocab, d_model, n_head, n_layer, d_ff, B, S0, T)).encode())
+    w = workloads.make_weights(cfg, gains="random", seed=key % 100000)
+    tok = workloads.make_tokens(cfg, batch=B, seq=S0 + T, seed=key % 99991)
+    model = tfm.Model(cfg, max_batch=B, max_seq=S0 + T)
+    model.load_weights(to_torch_weights(w, bf16=True))
+    model.kv_cache_create()
+    ld = (vocab + 3) // 4 * 4
+    dtok = torch.from_numpy(tok).cuda()
+    pre = torch.empty(B * S0, ld, device="cuda")
+    model.prefill(dtok[:, :S0].contiguous(), pre)
+    steps = []
+    for t in range(T):
+        lg = torch.empty(B, ld, device="cuda")
+        model.decode_step(dtok[:, S0 + t].contiguous(), S0 + t, lg)
+        steps.append(lg)
+    full = torch.empty(B * (S0 + T), ld, device="cuda")
+    model.forward(dtok, full)
+    torch.cuda.synchronize()
+    tfm.device_status()
+    dec = torch.stack(steps, 1).cpu().numpy()[:, :, :vocab]
+    full = full.cpu().numpy().reshape(B, S0 + T, ld)[:, :, :vocab]
+    model.close()
+    assert rel_err(dec, full[:, S0:]) < 1e-2
+    ref = oracle.forward(tok, w, cfg)[:, S0:]
+    assert rel_err(dec, ref) < 2e-2
+    argmax_check(f"random decode V{vocab} D{d_model} H{n_head}/{n_kv_head} {B}x{T} after {S0}",
+                 "bf16", dec, ref)
