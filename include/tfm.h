@@ -450,7 +450,7 @@ size_t tfm_swiglu_workspace_bytes(int64_t M, int32_t F, int32_t mode);
  * returns TFM_EINVAL.
  * No allocator is called, not even on the first call; that first call on each
  * device looks up the array's device address (cudaGetSymbolAddress) with that
- * device current; make that first call before any stream capture begins.
+ * device current.
  * All calls share the array and it keeps the last call's contents
  * (nothing needs clearing: each call overwrites every entry it reads); calls
  * whose kernels overlap on the GPU race on it, so order them on one stream. */
