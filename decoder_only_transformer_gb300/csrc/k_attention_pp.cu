@@ -47,8 +47,16 @@
 // alternation through a pair of barriers per quarter, was measured slower
 // (long attention 154 -> 170 us, whole launch): one warp alone runs the
 // exponentials at ~6 cycles per ex2, two in step at ~4.3, the special-function
-// unit's rate.  All waits are bounded; tiles above the diagonal are never
-// loaded.
+// unit's rate.  The packed forms ex2.approx.ftz.bf16x2 and ex2.approx.f16x2 take
+// 8 cycles per warp instruction, the same 32 results per cycle per SM as the f32
+// form, so packing P's exponentials gains nothing.  Splitting the tile into four
+// 32-column chunks, each loaded from tensor memory while the previous one runs
+// its exponentials against the running maximum (raised, with the earlier chunks'
+// P rescaled, when a chunk passes it by the threshold), was correct but much
+// slower (long 140.5 -> 191 us, gpt2s 28.8 -> 38.5 us): S_x can be released only
+// after its last chunk is loaded, which holds back the next S MMA that each
+// tile's softmax then waits for.  All waits are bounded; tiles above the
+// diagonal are never loaded.
 #include <climits>
 
 #include "common.cuh"
