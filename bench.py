@@ -70,6 +70,7 @@ DRAM_TRAFFIC = {
     ("small", "qkv_rope_gemm"): 10.06e6,
     ("small", "oproj_residual_gemm"): 25.76e6, ("small", "gateup_swiglu_gemm"): 11.21e6,
     ("small", "down_residual_gemm"): 40.25e6, ("small", "lmhead_gemm"): 285.30e6,
+    ("long", "qkv_rope_gemm"): 29.98e6,
     ("long", "attention"): 50.41e6, ("long", "oproj_residual_gemm"): 52.49e6,
     ("long", "gateup_swiglu_gemm"): 29.89e6, ("long", "down_residual_gemm"): 84.44e6,
     ("gqa", "qkv_rope_gemm"): 69.77e6, ("gqa", "attention"): 50.67e6,
