@@ -54,7 +54,7 @@ typedef enum {
     TFM_ECUDA = 3,         /* a CUDA runtime call failed; see tfm_last_error() */
     TFM_EBADTOKEN = 4,     /* device: a token id was outside [0, vocab); its row was zeroed */
     TFM_ETIMEOUT = 5,      /* device: a bounded pipeline wait gave up; outputs are invalid */
-    TFM_EUNSUPPORTED = 6   /* valid request this build does not implement (e.g. d_head 48 in bf16) */
+    TFM_EUNSUPPORTED = 6   /* valid request the library does not implement (e.g. d_head 48 in bf16) */
 } tfm_status;
 
 typedef enum { TFM_FP32 = 0, TFM_BF16 = 1 } tfm_mode;
