@@ -263,6 +263,9 @@ struct Model {
     std::vector<GemmPlan> d_qkv, d_o, d_gu, d_down;
     GemmPlan d_lm;
     int dplan_B = -1;
+    // the decode GEMMs behind RMSNorms (QKV of layers after the first, gate/up,
+    // LM head) compute those norms themselves (GemmPlan::norm_x)
+    bool dnorm_fused = false;
     const float* dplan_logits = nullptr;
     int64_t dplan_ld = -1;
     // tfm_forward_host_async: copy stream, per-buffer events, calls so far
@@ -1023,6 +1026,28 @@ tfm_status build_decode_plans(Model* m, int B, float* logits, int64_t ld) {
     for (int l = 0; l < c.n_layer; ++l)
         m->d_qkv[l].b_static = m->d_o[l].b_static = m->d_gu[l].b_static = m->d_down[l].b_static = 1;
     m->d_lm.b_static = 1;
+    // RMSNorm models with up to 16 sequences: the weight-streaming GEMMs after
+    // each norm take the residual rows and normalise them on the way in, so the
+    // step has no norm launches after the first (fused with the embedding).
+    m->dnorm_fused = !g2 && c.n_layer > 0 && m->d_lm.skinny && m->d_lm.sk_nm == 16;
+    for (int l = 0; l < c.n_layer && m->dnorm_fused; ++l)
+        m->dnorm_fused = m->d_qkv[l].skinny && m->d_qkv[l].sk_nm == 16 && m->d_gu[l].skinny &&
+                         m->d_gu[l].sk_nm == 16;
+    if (m->dnorm_fused) {
+        for (int l = 0; l < c.n_layer; ++l) {
+            if (l > 0) {
+                m->d_qkv[l].norm_x = m->h();
+                m->d_qkv[l].norm_g = m->attn_norm[l];
+                m->d_qkv[l].norm_eps = c.norm_eps;
+            }
+            m->d_gu[l].norm_x = m->h();
+            m->d_gu[l].norm_g = m->ffn_norm[l];
+            m->d_gu[l].norm_eps = c.norm_eps;
+        }
+        m->d_lm.norm_x = m->h();
+        m->d_lm.norm_g = m->final_norm;
+        m->d_lm.norm_eps = c.norm_eps;
+    }
     m->dplan_B = B;
     m->dplan_logits = logits;
     m->dplan_ld = ld;
@@ -1079,7 +1104,7 @@ tfm_status decode_body(Model* m, const int32_t* tokens, int B, float* logits, in
         return launch_rmsnorm(m->h(), gain, m->xn(), B, c.d_model, c.norm_eps, 1, st, 1, n);
     };
     for (int l = 0; l < c.n_layer; ++l) {
-        if (l > 0 && !post) {
+        if (l > 0 && !post && !m->dnorm_fused) {
             NormArgs n = ln_args(g2 ? m->ln1_b[l] : nullptr, nullptr);
             TFM_LAUNCH(K_NORM, norm(m->attn_norm[l], g2 ? &n : nullptr));
         }
@@ -1089,7 +1114,7 @@ tfm_status decode_body(Model* m, const int32_t* tokens, int B, float* logits, in
                                                    m->pos_dev, dh, scale, st,
                                                    m->windows.empty() ? 0 : m->windows[l]));
         TFM_LAUNCH(K_OPROJ, launch_gemm_tc(m->d_o[l], st));
-        {
+        if (!m->dnorm_fused) {
             NormArgs n = post ? ln_args(m->ln1_b[l], m->h())
                               : ln_args(g2 ? m->ln2_b[l] : nullptr, nullptr);
             TFM_LAUNCH(K_NORM, norm(post ? m->attn_norm[l] : m->ffn_norm[l], g2 ? &n : nullptr));
@@ -1101,7 +1126,7 @@ tfm_status decode_body(Model* m, const int32_t* tokens, int B, float* logits, in
             TFM_LAUNCH(K_NORM, norm(m->ffn_norm[l], &n));
         }
     }
-    if (c.n_layer > 0) {
+    if (c.n_layer > 0 && !m->dnorm_fused) {
         NormArgs n = ln_args(g2 ? m->lnf_b : nullptr, nullptr);
         TFM_LAUNCH(K_NORM, norm(m->final_norm, g2 ? &n : nullptr));
     }

@@ -182,6 +182,13 @@ struct GemmPlan {
     // start before the grid dependency wait (set by the model's own plans)
     int b_static;
     EpiParams epi;
+    // Weight-streaming plans with sk_nm == 16: when norm_x is set, A is the
+    // RMSNorm of the fp32 rows norm_x [M, K] with gain norm_g [K] (bf16 of
+    // x / sqrt(mean(x^2) + eps) * g), computed by the kernel in place of loading
+    // A; null: A as given.
+    const float* norm_x;
+    const float* norm_g;
+    float norm_eps;
 };
 // Builds the tensor maps; returns TFM_OK or an error status with a message.
 tfm_status plan_gemm_tc(GemmPlan* plan, const void* A, int64_t lda, const void* B,

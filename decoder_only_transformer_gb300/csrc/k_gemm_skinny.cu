@@ -18,6 +18,19 @@
 //               tcgen05.mma.cta_group::1.kind::f16 (M=128, N=NM, K=16).
 //   warps 2..5  read their TMEM lane quarter (one W row per thread, NM columns)
 //               and store the partial C^T tile to shared memory as [NM][128] fp32.
+//               With a norm input (16-row plans, GemmPlan::norm_x), they first
+//               build A themselves: the RMSNorm of the residual rows (a warp per
+//               row for the sums of squares, all of a row's loads in flight), then
+//               each k-block's 16 x 64 bf16 tile written into its stage where the
+//               TMA would have put it, their 128 arrivals joining the W copy's on
+//               the stage barrier.  A decode step then needs no norm launches after
+//               the first (the step measured 393.7 -> 371.0 us at the GQA workload,
+//               425.7 -> 403.8 us at GPT-2-small widths, 176.9 -> 165.9 us at long
+//               context: each launch removed took a kernel boundary and an L2 round
+//               trip off the chain; a first form whose row sums went through
+//               dependent loads, one round trip after another, was slower).
+//               Their numerics are the norm kernels': r = 1 / sqrt(sum(x^2)/K + eps)
+//               in fp32, then bf16(x * r * g).
 // After a cluster barrier every CTA sums a share of the tile's 8-column output
 // chunks over the cluster's partial tiles (distributed shared memory, split 0
 // first: the result does not depend on timing) and applies the epilogue to it;
@@ -44,6 +57,13 @@ struct SkSmem {
     static constexpr int kBytes = kMisc + 16 + 1024;        // + alignment slack
 };
 
+// A as the RMSNorm of fp32 rows (GemmPlan::norm_x): x [M, K], gain g [K].
+struct NormIn {
+    const float* x;
+    const float* g;
+    float eps;
+};
+
 __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
     float4 v;
     asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -56,7 +76,7 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
 template <int NM, int STAGES, bool kDual>
 __global__ void __launch_bounds__(kSkThreads, 1)
     k_gemm_skinny(const __grid_constant__ TcMaps maps, int M, int N, int K, int splits,
-                  int w_static, EpiParams epi, int* err) {
+                  int w_static, EpiParams epi, NormIn nin, int* err) {
     using L = SkSmem<NM, STAGES>;
     constexpr int kTmemCols = NM < 32 ? 32 : NM;
     constexpr int kOut = kDual ? 64 : 128;       // output columns of a tile
@@ -80,10 +100,13 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     const int kb0 = (int)((int64_t)split * num_kb / splits);
     const int kb1 = (int)((int64_t)(split + 1) * num_kb / splits);
     const int nkb = kb1 - kb0;                   // >= 1: splits <= num_kb
+    // A computed here from norm rows (16-row plans only): each stage's A tile is
+    // written by warps 2..5, whose 128 arrivals join the producer's on its barrier.
+    const bool fused = NM == 16 && nin.x != nullptr;
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
+            mbar_init(full_bar(s), fused ? 1 + 128 : 1);
             mbar_init(empty_bar(s), 1);
         }
         mbar_init(tfull_bar, 1);
@@ -119,21 +142,23 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                             full_bar(s));
             };
             const int pre = nkb < STAGES ? nkb : STAGES;
+            const uint32_t tx = fused ? (uint32_t)kSkWBytes : (uint32_t)L::kStage;
             if (!w_static) pdl_wait();           // W may come from the launch before
             for (int i = 0; i < pre; ++i) {
-                mbar_arrive_expect_tx(full_bar(i), L::kStage);
+                mbar_arrive_expect_tx(full_bar(i), tx);
                 load_w(i);
             }
             pdl_wait();
             pdl_trigger();
-            for (int i = 0; i < pre; ++i) load_x(i);
+            if (!fused)
+                for (int i = 0; i < pre; ++i) load_x(i);
             for (int i = pre; i < nkb; ++i) {
                 const int s = i % STAGES;
                 if (!mbar_wait(empty_bar(s), (uint32_t)(((i / STAGES) - 1) & 1), err, abort_flag))
                     break;
-                mbar_arrive_expect_tx(full_bar(s), L::kStage);
+                mbar_arrive_expect_tx(full_bar(s), tx);
                 load_w(i);
-                load_x(i);
+                if (!fused) load_x(i);
             }
         } else {
             pdl_wait();
@@ -164,7 +189,82 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         pdl_wait();
         pdl_trigger();
         const int q = warp & 3;                  // TMEM lane quarter of this warp
-        if (warp_wait(tfull_bar, 0, err, abort_flag)) {
+        bool conv_ok = true;
+        if (fused) {
+            // ------------------------------------------------ A from the norm rows
+            // The RMSNorm of the CS336 walkthrough (section 5.6) with the same
+            // arithmetic as the norm kernels: r = 1 / sqrt(sum(x^2) / K + eps) in
+            // fp32, then bf16(x * r * g).  For the tiles thread ct owns row ct / 8,
+            // 16-byte chunk ct % 8 (8 columns) of each k-block's 16 x 64 tile, stored
+            // where a 128-byte-swizzled TMA box would put it (chunk j of row r at
+            // j ^ r % 8).
+            const int ct = (int)threadIdx.x - 64;
+            const int row = ct >> 3, ch = ct & 7;
+            const float* xrow = nin.x + (int64_t)(row < M ? row : 0) * K;
+            // Prefetch ring over the k-blocks, one slot per stage; the first
+            // stages' loads are issued before the sums, so the two overlap.
+            float4 xa[STAGES][2], ga[STAGES][2];
+            auto fetch = [&](int i, int u) {
+                const int kx = (kb0 + i) * kSkBK + ch * 8;
+                const bool in = i < nkb && row < M && kx < K;
+                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                xa[u][0] = in ? __ldg(reinterpret_cast<const float4*>(xrow + kx)) : z;
+                xa[u][1] = in ? __ldg(reinterpret_cast<const float4*>(xrow + kx + 4)) : z;
+                ga[u][0] = in ? __ldg(reinterpret_cast<const float4*>(nin.g + kx)) : z;
+                ga[u][1] = in ? __ldg(reinterpret_cast<const float4*>(nin.g + kx + 4)) : z;
+            };
+#pragma unroll
+            for (int u = 0; u < STAGES; ++u) fetch(u, u);
+            // Sums of squares: warp w takes rows w, w + 4, ...; lane l the float4
+            // groups l, l + 32, ... of the row, sixteen loads in flight at a time,
+            // then a shuffle reduction (the summation order of the norm kernels).
+            float* red = reinterpret_cast<float*>(gbase + L::kRed);   // [16], free until the MMAs end
+            const int k4 = K >> 2;
+            for (int m = warp - 2; m < M; m += 4) {
+                const float4* xr = reinterpret_cast<const float4*>(nin.x + (int64_t)m * K);
+                float ssum = 0.f;
+                for (int c0 = 0; c0 < k4; c0 += 32 * 16) {
+                    float4 v[16];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const int c = c0 + lane + 32 * u;
+                        v[u] = c < k4 ? __ldg(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 16; ++u)
+                        ssum += v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+                if (lane == 0) red[m] = ssum;
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");   // warps 2..5 only
+            float rinv = 0.f;                                // rows >= M are zero
+            if (row < M) rinv = 1.0f / sqrtf(red[row] / (float)K + nin.eps);
+            for (int i0 = 0; i0 < nkb && conv_ok; i0 += STAGES) {
+#pragma unroll
+                for (int u = 0; u < STAGES; ++u) {
+                    const int i = i0 + u;                    // stage u
+                    if (i >= nkb) break;
+                    if (i >= STAGES &&
+                        !warp_wait(empty_bar(u), (uint32_t)(((i / STAGES) - 1) & 1), err, abort_flag)) {
+                        conv_ok = false;
+                        break;
+                    }
+                    const float4 a0 = xa[u][0], a1 = xa[u][1], g0 = ga[u][0], g1 = ga[u][1];
+                    const uint32_t sx = base + (uint32_t)(u * L::kStage + kSkWBytes);
+                    st_shared_v4(sx + row * 128 + ((ch ^ (row & 7)) << 4),
+                                 pack_bf16x2(a0.x * rinv * g0.x, a0.y * rinv * g0.y),
+                                 pack_bf16x2(a0.z * rinv * g0.z, a0.w * rinv * g0.w),
+                                 pack_bf16x2(a1.x * rinv * g1.x, a1.y * rinv * g1.y),
+                                 pack_bf16x2(a1.z * rinv * g1.z, a1.w * rinv * g1.w));
+                    fence_proxy_async_smem();           // read by the tensor cores
+                    mbar_arrive(full_bar(u));
+                    fetch(i + STAGES, u);
+                }
+            }
+        }
+        if (conv_ok && warp_wait(tfull_bar, 0, err, abort_flag)) {
             tc_fence_after();
             const int r = q * 32 + lane;         // W row of the tile held by this thread
             float* part = reinterpret_cast<float*>(gbase + L::kRed);
@@ -238,8 +338,9 @@ cudaError_t skinny_inst(const GemmPlan& p, cudaStream_t st) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
+    const NormIn nin{p.norm_x, p.norm_g, p.norm_eps};
     return cudaLaunchKernelEx(&cfg, k_gemm_skinny<NM, STAGES, kDual>, p.maps, p.M, p.N, p.K,
-                              p.sk_splits, p.b_static, p.epi, device_error_word());
+                              p.sk_splits, p.b_static, p.epi, nin, device_error_word());
 }
 
 // Ring depth per NM: the W stages of two CTAs per SM (NM <= 32) or of one.

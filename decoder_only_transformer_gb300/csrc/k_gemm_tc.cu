@@ -694,6 +694,9 @@ tfm_status plan_gemm_tc(GemmPlan* plan, const void* A, int64_t lda, const void* 
     plan->dual = dual ? 1 : 0;
     plan->skinny = 0;
     plan->b_static = 0;
+    plan->norm_x = nullptr;
+    plan->norm_g = nullptr;
+    plan->norm_eps = 0.f;
     if (M <= kBM && epi.kind != EPI_LSE) {
         // A few rows: stream W over all SMs (k_gemm_skinny.cu).  Tiles of 128 W
         // rows (64 output columns for SwiGLU); K split so that tiles x splits
