@@ -362,35 +362,38 @@ def kernel_table(cfg, B, S, prof, peaks):
     return out
 
 
-def decode_rate(tfm, torch, model, cfg, tok_np, stream, peaks, steps=32):
-    """Incremental decoding on the workload's batch: prefill the first S - steps
-    positions into the KV cache, then `steps` decode steps (one new token per
-    sequence each), timed with CUDA events around all steps (direct launches).
-    The decode attention's HBM fraction uses its algorithmic bytes: the cached
-    K and V of positions [0, pos] read once, q read, o written, the fp32 chunk
-    partials written and read back."""
+def decode_rate(tfm, torch, model, cfg, tok_np, stream, peaks, steps=32, warmup=3):
+    """Incremental decoding on the workload's batch: prefill the first
+    S - warmup - steps positions into the KV cache, run `warmup` untimed decode
+    steps (the step is recorded as a graph on its second call), then time `steps`
+    decode steps (one new token per sequence each, graph replays) with CUDA events
+    around all of them.  The decode attention's HBM fraction uses its algorithmic
+    bytes: the cached K and V of positions [0, pos] read once, q read, o written,
+    the fp32 chunk partials written and read back."""
     B, S = tok_np.shape
-    S0 = S - steps
+    S0 = S - steps - warmup
     dh, H, Hkv = cfg.d_head, cfg.n_head, cfg.n_kv_head
     ld = (cfg.vocab + 3) // 4 * 4
     model.kv_cache_create()
     dtok = torch.from_numpy(tok_np).cuda()
-    pre = torch.empty(B * S0, ld, device="cuda")
+    pre = torch.empty(B * (S0 + warmup), ld, device="cuda")
     lg = torch.empty(B, ld, device="cuda")
-    cols = [dtok[:, S0 + t].contiguous() for t in range(steps)]
+    cols = [dtok[:, S0 + t].contiguous() for t in range(warmup + steps)]
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     model.prefill(dtok[:, :S0].contiguous(), pre, stream)
+    for t in range(warmup):
+        model.decode_step(cols[t], S0 + t, lg, stream)
     torch.cuda.synchronize()
     ev[0].record(stream)
-    for t in range(steps):
+    for t in range(warmup, warmup + steps):
         model.decode_step(cols[t], S0 + t, lg, stream)
     ev[1].record(stream)
     torch.cuda.synchronize()
     ms = ev[0].elapsed_time(ev[1])
     # the same steps again, profiled per kernel kind (events after every kernel)
-    model.prefill(dtok[:, :S0].contiguous(), pre, stream)
+    model.prefill(dtok[:, :S0 + warmup].contiguous(), pre, stream)
     model.profile(True)
-    for t in range(steps):
+    for t in range(warmup, warmup + steps):
         model.decode_step(cols[t], S0 + t, lg, stream)
     torch.cuda.synchronize()
     model.profile(False)
@@ -398,7 +401,7 @@ def decode_rate(tfm, torch, model, cfg, tok_np, stream, peaks, steps=32):
     tfm.device_status()
     att_ms, att_n = prof["attention"]
     nbytes = 0
-    for t in range(steps):
+    for t in range(warmup, warmup + steps):
         L = S0 + t + 1
         nch = (L + DECODE_CHUNK // dh - 1) // (DECODE_CHUNK // dh)   # chunks of DECODE_CHUNK / dh keys
         nbytes += (2 * B * Hkv * L * dh * 2 + 2 * B * H * dh * 2
@@ -439,7 +442,7 @@ def decode_rate(tfm, torch, model, cfg, tok_np, stream, peaks, steps=32):
     gbs_a = bytes_a / (us_a * 1e-6) / 1e9
     del flush
     return {"value": B * steps / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms / steps,
-            "batch": B, "prefill_len": S0, "steps": steps,
+            "batch": B, "prefill_len": S0, "warmup_steps": warmup, "steps": steps,
             "attention_alone": {"bound": "hbm", "positions": S, "avg_us": round(us_a, 2),
                                 "bytes": bytes_a, "achieved": round(gbs_a, 1),
                                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -454,9 +457,10 @@ def decode_rate(tfm, torch, model, cfg, tok_np, stream, peaks, steps=32):
                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
                           "frac": round(gbs / peaks["hbm_gbs"], 4) if gbs else None,
                           "avg_us_per_layer": round(att_ms * 1e3 / max(1, att_n), 2)},
-            "how": "tfm_prefill of the first S - steps positions, then tfm_decode_step per "
-                   "position (recorded as a graph on its second call, replayed after); CUDA "
-                   "events around all steps; attention from a second, profiled pass"}
+            "how": "tfm_prefill of the first S - warmup - steps positions, tfm_decode_step "
+                   "per position: `warmup` untimed steps (the graph is recorded on the "
+                   "second), then CUDA events around the `steps` replayed steps; attention "
+                   "from a second, profiled pass of the same steps"}
 
 
 def loss_rate(tfm, torch, model, cfg, tok_np, logits, stream, flush, peaks, steps=10):
