@@ -40,6 +40,10 @@ def _model(cfg, w, B, S):
     ("gpt2s", 3, 250, 10),        # d_head 64: 128-key chunks, crosses key 256
     ("gpt2s", 1, 37, 3),          # one chunk, partly filled
     ("gqa", 2, 380, 6),           # d_head 128 (64-key chunks), 4 query heads per kv head: crosses key 384
+    # Up to 16 sequences the weight-streaming GEMMs after each RMSNorm normalise the
+    # residual rows themselves; from 17 on the norms are their own launches.
+    ("gpt2s", 16, 60, 3),         # the largest batch with the norms inside the GEMMs
+    ("small", 17, 60, 3),         # the smallest batch with separate norm launches
 ])
 def test_decode_matches_oracle_and_forward(name, B, S0, T):
     cfg = workloads.get_config(name).replace(n_layer=2, vocab=3001)
