@@ -557,6 +557,18 @@ def test_layernorm_shift_scale_invariance_and_moments():
                        rtol=0, atol=1e-12)
 
 
+def test_layernorm_gain_and_shift_by_hand():
+    # The definition's closed forms ([Ch4] 5, gain and shift): a constant row has
+    # no deviation from its mean, so the output is the shift alone; and for
+    # x = (1, 2, 3) (mean 2, population variance 2/3, eps 0) the normalised row is
+    # (-1, 0, 1) * sqrt(3/2), then scaled by g and moved by b element by element.
+    b = np.array([0.5, -1.0, 2.0, 0.25])
+    assert np.array_equal(oracle.layernorm(np.full(4, 3.0), np.array([2.0, 3.0, 4.0, 5.0]), b, 1e-5), b)
+    g, b3 = np.array([2.0, -1.0, 0.5]), np.array([1.0, 10.0, -3.0])
+    want = np.array([-1.0, 0.0, 1.0]) * np.sqrt(1.5) * g + b3
+    assert np.allclose(oracle.layernorm(np.array([1.0, 2.0, 3.0]), g, b3, 0.0), want, rtol=0, atol=1e-12)
+
+
 def _gpt2_zero(cfg, layers=1):
     c = cfg.replace(n_layer=layers)
     return c, workloads.make_gpt2_weights(c, seed=5)
