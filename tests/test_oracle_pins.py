@@ -569,6 +569,65 @@ def test_layernorm_gain_and_shift_by_hand():
     assert np.allclose(oracle.layernorm(np.array([1.0, 2.0, 3.0]), g, b3, 0.0), want, rtol=0, atol=1e-12)
 
 
+def test_gpt2_blocks_match_scalar_loops():
+    """The GPT-2-style block in both orders against scalar loops written from the
+    definitions on a tiny shape: LayerNorm with the population variance, gain and
+    shift ([Ch4] 5); the fused qkv projection with its bias, columns [q | k | v],
+    head h owning columns [h*dh, (h+1)*dh), causal softmax attention scaled by
+    1/sqrt(dh), merge, output projection with its bias ([CS336-A] TinyGPT
+    CausalSelfAttention; [Ch4] 3); the MLP fc -> exact GELU -> fc2 with biases
+    ([Ch4] 4).  Pre-norm: x + attn(LN1 x), then + mlp(LN2 of that).  Post-norm:
+    LN1(x + attn x), then LN2(. + mlp .) ([Scratch] 3.1)."""
+    cfg = workloads.GPT2_CONFIGS["gpt2_tiny"].replace(d_model=8, n_head=2, n_kv_head=2, d_ff=16,
+                                                      n_layer=1)
+    L = workloads.make_gpt2_weights(cfg, seed=41)["layers"][0]
+    r = np.random.default_rng(42)
+    L = dict(L, **{k: r.standard_normal(L[k].shape) * 0.5 for k in
+                   ("b_qkv", "b_proj", "b_fc", "b_fc2", "ln1_b", "ln2_b")})
+    L = dict(L, **{k: r.standard_normal(L[k].shape) * 0.4 for k in ("w_qkv", "w_proj", "w_fc", "w_fc2")})
+    S, D, H, dh, F = 4, 8, 2, 4, 16
+    u = r.standard_normal((1, S, D))
+    eps = cfg.norm_eps
+
+    def ln(v, g, b):
+        mu = sum(v) / D
+        var = sum((x - mu) ** 2 for x in v) / D
+        return [(v[i] - mu) / math.sqrt(var + eps) * g[i] + b[i] for i in range(D)]
+
+    def lin(v, W, bias):
+        return [sum(W[o, c] * v[c] for c in range(len(v))) + bias[o] for o in range(W.shape[0])]
+
+    def attn(rows):
+        qkv = [lin(x, L["w_qkv"], L["b_qkv"]) for x in rows]
+        merged = [[0.0] * (H * dh) for _ in range(S)]
+        for h in range(H):
+            for i in range(S):
+                q = qkv[i][h * dh:(h + 1) * dh]
+                sc = [sum(q[e] * qkv[j][H * dh + h * dh + e] for e in range(dh)) / math.sqrt(dh)
+                      for j in range(i + 1)]
+                mx = max(sc)
+                p = [math.exp(x - mx) for x in sc]
+                z = sum(p)
+                for e in range(dh):
+                    merged[i][h * dh + e] = sum(p[j] / z * qkv[j][2 * H * dh + h * dh + e]
+                                                for j in range(i + 1))
+        return [lin(m, L["w_proj"], L["b_proj"]) for m in merged]
+
+    def mlp(v):
+        hid = [0.5 * x * (1.0 + math.erf(x / math.sqrt(2.0))) for x in lin(v, L["w_fc"], L["b_fc"])]
+        return lin(hid, L["w_fc2"], L["b_fc2"])
+
+    x = [list(u[0, i]) for i in range(S)]
+    a = attn([ln(xi, L["ln1_g"], L["ln1_b"]) for xi in x])
+    x1 = [[x[i][d] + a[i][d] for d in range(D)] for i in range(S)]
+    pre = [[x1[i][d] + y for d, y in enumerate(mlp(ln(x1[i], L["ln2_g"], L["ln2_b"])))] for i in range(S)]
+    a = attn(x)
+    x1 = [ln([x[i][d] + a[i][d] for d in range(D)], L["ln1_g"], L["ln1_b"]) for i in range(S)]
+    post = [ln([x1[i][d] + y for d, y in enumerate(mlp(x1[i]))], L["ln2_g"], L["ln2_b"]) for i in range(S)]
+    assert np.allclose(oracle.gpt2_block(u, L, cfg, post_norm=False)[0], pre, rtol=0, atol=1e-12)
+    assert np.allclose(oracle.gpt2_block(u, L, cfg, post_norm=True)[0], post, rtol=0, atol=1e-12)
+
+
 def _gpt2_zero(cfg, layers=1):
     c = cfg.replace(n_layer=layers)
     return c, workloads.make_gpt2_weights(c, seed=5)
@@ -678,3 +737,8 @@ def test_model_windows_per_layer():
     # the first 4 positions see their whole prefix in both layers
     assert np.allclose(hyb[0, :4], full[0, :4], rtol=0, atol=1e-12)
     assert not np.allclose(hyb[0, 4:], full[0, 4:])
+    # each layer takes its own window: one in the second layer alone changes the
+    # logits, and differently from the same window in the first layer alone
+    late = oracle.forward(t, w, cfg, windows=[0, 4])
+    assert not np.allclose(late[0, 4:], full[0, 4:])
+    assert not np.allclose(late[0, 4:], hyb[0, 4:])
