@@ -82,6 +82,15 @@ def test_causal_flops_count_lower_triangle():
     assert accounting.attention_flops(1, 4, 8, 16) == f["attn"]
 
 
+def test_rmsnorm_bytes_are_one_read_one_write_and_the_gain():
+    # The least a norm launch moves: x read once (fp32), y written once (bf16, or
+    # fp32 in fp32 mode), the gain read once.  131072 x 2048 rows (the bench's
+    # standalone RMSNorm): 268,435,456 elements x (4 + 2) bytes + 2048 x 4.
+    assert accounting.rmsnorm_bytes(131072, 2048) == 1_610_620_928
+    assert accounting.rmsnorm_bytes(3, 5, out_bytes=4) == 3 * 5 * 8 + 5 * 4
+    assert accounting.rmsnorm_bytes(1, 1) == 4 + 2 + 4
+
+
 def test_memory_caps_of_the_tensor_kernels():
     """The caps the bench reports beside each tensor kernel's fraction of peak:
     min(1, flop/byte x HBM bandwidth / tensor peak) with the fp32 residual
