@@ -155,6 +155,53 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
 
+def _dev(t, name, dtypes=None, rows=False):
+    """Pointer of a CUDA tensor in the layout the C header documents: densely
+    packed, or (rows=True) a matrix whose rows are dense at any row pitch.  Any
+    other tensor is refused here, before the library could read or write memory
+    it does not own."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name}: a CUDA tensor is required, got one on {t.device}")
+    return _checked(t, name, dtypes, rows)
+
+
+def _host(t, name, dtypes=None, rows=False):
+    """As _dev for the host-buffer entry points: a CPU tensor (pinned for the
+    copies to overlap)."""
+    if t.is_cuda:
+        raise ValueError(f"{name}: a host (CPU) tensor is required, got one on {t.device}")
+    return _checked(t, name, dtypes, rows)
+
+
+def _checked(t, name, dtypes, rows):
+    if dtypes is not None and t.dtype not in dtypes:
+        want = " or ".join(str(d) for d in dtypes)
+        raise TypeError(f"{name}: dtype {t.dtype}, {want} is required")
+    if rows:
+        if t.dim() != 2 or (t.numel() and t.stride(1) != 1):
+            raise ValueError(f"{name}: a matrix with dense rows is required")
+    elif not t.is_contiguous():
+        raise ValueError(f"{name}: a contiguous tensor is required")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _rows_at_least(t, n, name):
+    if t.shape[0] < n:
+        raise ValueError(f"{name}: {n} rows are written, the tensor has {t.shape[0]}")
+
+
+def _shape(t, shape, name):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, {tuple(shape)} is required")
+
+
+def _torch():
+    import torch
+    return torch
+
+
 def _mode_of(t):
     import torch
     if t.dtype == torch.bfloat16:
@@ -217,6 +264,8 @@ class Model:
 
     def load_weights(self, w: dict):
         L = self.cfg.n_layer
+        on_host = 0 if w["embed"].is_cuda else 1
+        self._check_weights(w, on_host)
 
         def arr(key):
             a = (ctypes.c_void_p * max(L, 1))()
@@ -231,35 +280,66 @@ class Model:
         ws = Weights(w["embed"].data_ptr(), fields["attn_norm"], fields["wq"], fields["wk"],
                      fields["wv"], fields["wo"], fields["ffn_norm"], fields["w1"], fields["w3"],
                      fields["w2"], w["final_norm"].data_ptr(), w["lm_head"].data_ptr())
-        on_host = 0 if w["embed"].is_cuda else 1
         _check(self.lib.tfm_load_weights(self.handle, ctypes.byref(ws), on_host))
+
+    def _check_weights(self, w, on_host):
+        """Every array on the embedding's side (host or device), dense, of the
+        configuration's shape: matrices in the mode's type, gains fp32."""
+        torch = _torch()
+        c = self.c
+        D, F, V = c.d_model, c.d_ff, c.vocab
+        dh = D // c.n_head
+        mat = torch.bfloat16 if c.mode == TFM_BF16 else torch.float32
+        place = _host if on_host else _dev
+
+        def one(t, name, shape, dtype):
+            place(t, name, (dtype,))
+            _shape(t, shape, name)
+
+        one(w["embed"], "embed", (V, D), mat)
+        one(w["lm_head"], "lm_head", (V, D), mat)
+        one(w["final_norm"], "final_norm", (D,), torch.float32)
+        if len(w["layers"]) < self.cfg.n_layer:
+            raise ValueError(f"layers: {self.cfg.n_layer} are required, got {len(w['layers'])}")
+        for i, layer in enumerate(w["layers"][: self.cfg.n_layer]):
+            for key, shape, dtype in (("attn_norm", (D,), torch.float32),
+                                      ("wq", (c.n_head * dh, D), mat),
+                                      ("wk", (c.n_kv_head * dh, D), mat),
+                                      ("wv", (c.n_kv_head * dh, D), mat),
+                                      ("wo", (D, c.n_head * dh), mat),
+                                      ("ffn_norm", (D,), torch.float32),
+                                      ("w1", (F, D), mat), ("w3", (F, D), mat), ("w2", (D, F), mat)):
+                one(layer[key], f"layers[{i}].{key}", shape, dtype)
 
     def forward(self, tokens, logits, stream=None):
         """tokens: int32 [B, S] (device); logits: fp32 [B*S, ld] (device)."""
         B, S = tokens.shape
-        _check(self.lib.tfm_forward(self.handle, _ptr(tokens), B, S, _ptr(logits),
-                                    logits.stride(0), _stream(stream)))
+        t, lg = self._io(tokens, logits, B * S, _dev)
+        _check(self.lib.tfm_forward(self.handle, t, B, S, lg, logits.stride(0), _stream(stream)))
 
     def forward_graph(self, tokens, logits, stream=None):
         """forward() replayed from a CUDA graph recorded on first use; the
         current torch stream must not be the legacy default stream."""
         B, S = tokens.shape
-        _check(self.lib.tfm_forward_graph(self.handle, _ptr(tokens), B, S, _ptr(logits),
-                                          logits.stride(0), _stream(stream)))
+        t, lg = self._io(tokens, logits, B * S, _dev)
+        _check(self.lib.tfm_forward_graph(self.handle, t, B, S, lg, logits.stride(0),
+                                          _stream(stream)))
 
     def forward_host(self, tokens, logits, stream=None):
         """tokens: int32 [B, S] (host, pinned); logits: fp32 [B*S, ld] (host, pinned)."""
         B, S = tokens.shape
-        _check(self.lib.tfm_forward_host(self.handle, _ptr(tokens), B, S, _ptr(logits),
-                                         logits.stride(0), _stream(stream)))
+        t, lg = self._io(tokens, logits, B * S, _host)
+        _check(self.lib.tfm_forward_host(self.handle, t, B, S, lg, logits.stride(0),
+                                         _stream(stream)))
 
     def forward_host_async(self, tokens, logits, stream=None):
         """forward_host with the logits copy on the handle's copy stream,
         overlapping the next call's forward; logits are final after
         forward_host_join(stream) and a synchronise of that stream."""
         B, S = tokens.shape
-        _check(self.lib.tfm_forward_host_async(self.handle, _ptr(tokens), B, S, _ptr(logits),
-                                               logits.stride(0), _stream(stream)))
+        t, lg = self._io(tokens, logits, B * S, _host)
+        _check(self.lib.tfm_forward_host_async(self.handle, t, B, S, lg, logits.stride(0),
+                                               _stream(stream)))
 
     def forward_host_join(self, stream=None):
         """Makes the stream wait for every logits copy issued so far."""
@@ -272,18 +352,25 @@ class Model:
     def prefill(self, tokens, logits, stream=None):
         """forward() that also fills the KV cache with positions [0, S)."""
         B, S = tokens.shape
-        _check(self.lib.tfm_prefill(self.handle, _ptr(tokens), B, S, _ptr(logits),
-                                    logits.stride(0), _stream(stream)))
+        t, lg = self._io(tokens, logits, B * S, _dev)
+        _check(self.lib.tfm_prefill(self.handle, t, B, S, lg, logits.stride(0), _stream(stream)))
 
     def forward_loss(self, tokens, targets, loss=None, lse=None, mean=None, stream=None):
         """Next-token cross-entropy without the logits: tokens, targets int32
         [B, S] (device); loss, lse fp32 [B*S] and mean fp32 [1] (device), each
         optional."""
+        torch = _torch()
         B, S = tokens.shape
-        _check(self.lib.tfm_forward_loss(self.handle, _ptr(tokens), _ptr(targets), B, S,
-                                         _ptr(loss) if loss is not None else None,
-                                         _ptr(lse) if lse is not None else None,
-                                         _ptr(mean) if mean is not None else None,
+        t = _dev(tokens, "tokens", (torch.int32,))
+        _shape(targets, (B, S), "targets")
+        tg = _dev(targets, "targets", (torch.int32,))
+        for v, n, name in ((loss, B * S, "loss"), (lse, B * S, "lse"), (mean, 1, "mean")):
+            if v is not None and v.numel() < n:
+                raise ValueError(f"{name}: {n} values are written, the tensor has {v.numel()}")
+        _check(self.lib.tfm_forward_loss(self.handle, t, tg, B, S,
+                                         _dev(loss, "loss", (torch.float32,)),
+                                         _dev(lse, "lse", (torch.float32,)),
+                                         _dev(mean, "mean", (torch.float32,)),
                                          _stream(stream)))
 
     def set_attention_windows(self, windows=None):
@@ -296,8 +383,19 @@ class Model:
         """tokens: int32 [B] (device), the new token of every sequence at position
         pos (the cached length); logits: fp32 [B, ld] (device)."""
         B = tokens.shape[0]
-        _check(self.lib.tfm_decode_step(self.handle, _ptr(tokens), B, int(pos), _ptr(logits),
-                                        logits.stride(0), _stream(stream)))
+        t, lg = self._io(tokens, logits, B, _dev)
+        _check(self.lib.tfm_decode_step(self.handle, t, B, int(pos), lg, logits.stride(0),
+                                        _stream(stream)))
+
+    @staticmethod
+    def _io(tokens, logits, rows, place):
+        """Token ids (int32, dense) and the fp32 logits matrix (dense rows at its
+        pitch, `rows` of them written) on the side `place` requires."""
+        torch = _torch()
+        t = place(tokens, "tokens", (torch.int32,))
+        lg = place(logits, "logits", (torch.float32,), rows=True)
+        _rows_at_least(logits, rows, "logits")
+        return t, lg
 
     def profile(self, enable: bool = True):
         _check(self.lib.tfm_profile_enable(self.handle, 1 if enable else 0))
@@ -312,37 +410,76 @@ class Model:
 
 
 # ---------------------------------------------------------------- components
+# Every component checks its tensors against the layouts of the C header (CUDA,
+# dense, the mode's types, sizes that cover what the call reads and writes)
+# before the library sees them.
+def _t(*names):
+    torch = _torch()
+    return tuple(getattr(torch, n) for n in names)
+
+
+def _numel(t, n, name):
+    if t.numel() != n:
+        raise ValueError(f"{name}: {n} elements are required, the tensor has {t.numel()}")
+
+
+def _room(t, n, name):
+    if t.numel() < n:
+        raise ValueError(f"{name}: {n} elements are written, the tensor has {t.numel()}")
+
+
 def embedding(tokens, E, h, stream=None):
     M = tokens.numel()
-    _check(load().tfm_embedding(_ptr(tokens), _ptr(E), _ptr(h), M, E.shape[0], E.shape[1],
-                                _mode_of(E), _stream(stream)))
+    tk = _dev(tokens, "tokens", _t("int32"))
+    e = _dev(E, "E", _t("bfloat16", "float32"))
+    _shape(h, (M, E.shape[1]), "h")
+    hh = _dev(h, "h", _t("float32"))
+    _check(load().tfm_embedding(tk, e, hh, M, E.shape[0], E.shape[1], _mode_of(E), _stream(stream)))
 
 
 def rmsnorm(x, g, y, eps=1e-5, stream=None):
     M, D = x.shape
-    _check(load().tfm_rmsnorm(_ptr(x), _ptr(g), _ptr(y), M, D, eps, _mode_of(y), _stream(stream)))
+    xp = _dev(x, "x", _t("float32"))
+    _shape(g, (D,), "g")
+    gp = _dev(g, "g", _t("float32"))
+    _shape(y, (M, D), "y")
+    yp = _dev(y, "y", _t("float32", "bfloat16"))
+    _check(load().tfm_rmsnorm(xp, gp, yp, M, D, eps, _mode_of(y), _stream(stream)))
 
 
 def rope(x, theta, positions=None, stream=None):
     B, H, S, dh = x.shape
-    _check(load().tfm_rope(_ptr(x), _ptr(positions), B, H, S, dh, theta, _mode_of(x),
-                           _stream(stream)))
+    xp = _dev(x, "x", _t("bfloat16", "float32"))
+    if positions is not None:
+        _numel(positions, B * S, "positions")
+    pp = _dev(positions, "positions", _t("int32"))
+    _check(load().tfm_rope(xp, pp, B, H, S, dh, theta, _mode_of(x), _stream(stream)))
+
+
+def _attention_args(q, k, v, o):
+    B, H, S, dh = q.shape
+    Hkv = k.shape[1]
+    dt = (q.dtype,)
+    qp = _dev(q, "q", _t("bfloat16", "float32"))
+    for t, name in ((k, "k"), (v, "v")):
+        _shape(t, (B, Hkv, S, dh), name)
+    kp, vp = _dev(k, "k", dt), _dev(v, "v", dt)
+    _room(o, B * S * H * dh, "o")
+    op = _dev(o, "o", dt)
+    return (qp, kp, vp, op), (B, H, Hkv, S, dh)
 
 
 def causal_attention(q, k, v, o, scale=0.0, stream=None):
-    B, H, S, dh = q.shape
-    Hkv = k.shape[1]
-    _check(load().tfm_causal_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Hkv, S, dh,
-                                       scale, _mode_of(q), _stream(stream)))
+    ptrs, (B, H, Hkv, S, dh) = _attention_args(q, k, v, o)
+    _check(load().tfm_causal_attention(*ptrs, B, H, Hkv, S, dh, scale, _mode_of(q),
+                                       _stream(stream)))
 
 
 def causal_attention_window(q, k, v, o, window, scale=0.0, stream=None):
     """causal_attention where query i sees keys i-window < j <= i (0: all)."""
-    B, H, S, dh = q.shape
-    Hkv = k.shape[1]
-    _check(load().tfm_causal_attention_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Hkv, S,
-                                              dh, scale, int(window), _mode_of(q),
-                                              _stream(stream)))
+    ptrs, (B, H, Hkv, S, dh) = _attention_args(q, k, v, o)
+    _check(load().tfm_causal_attention_window(*ptrs, B, H, Hkv, S, dh, scale, int(window),
+                                              _mode_of(q), _stream(stream)))
 
 
 def decode_attention_workspace_bytes(B, H, max_seq, dh):
@@ -353,18 +490,34 @@ def decode_attention(q, k_cache, v_cache, o, pos, workspace, window=0, scale=0.0
     """q [B, H, dh]; caches [B, Hkv, max_seq, dh]; o [B, H*dh]; all bf16 (device)."""
     B, H, dh = q.shape
     Hkv, max_seq = k_cache.shape[1], k_cache.shape[2]
+    bf = _t("bfloat16")
+    qp = _dev(q, "q", bf)
+    if B:
+        for t, name in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+            if t.dim() != 4 or t.shape[0] < B or t.shape[3] != dh or tuple(t.shape) != tuple(k_cache.shape):
+                raise ValueError(f"{name}: shape {tuple(t.shape)} does not hold {B} sequences of "
+                                 f"d_head {dh}")
+    kp, vp = _dev(k_cache, "k_cache", bf), _dev(v_cache, "v_cache", bf)
+    _room(o, B * H * dh, "o")
+    op = _dev(o, "o", bf)
+    wp = _dev(workspace, "workspace")
     nbytes = workspace.numel() * workspace.element_size()
-    _check(load().tfm_decode_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), B, H, Hkv,
-                                       max_seq, int(pos), dh, scale, int(window), _ptr(workspace),
-                                       nbytes, _stream(stream)))
+    _check(load().tfm_decode_attention(qp, kp, vp, op, B, H, Hkv, max_seq, int(pos), dh, scale,
+                                       int(window), wp, nbytes, _stream(stream)))
 
 
 def linear(x, W, y, accumulate=False, stream=None):
     M, K = x.shape
     N = W.shape[0]
-    import torch
+    torch = _torch()
+    xp = _dev(x, "x", _t("bfloat16", "float32"))
+    _shape(W, (N, K), "W")
+    wp = _dev(W, "W", (x.dtype,))
+    yp = _dev(y, "y", _t("float32", "bfloat16"), rows=True)
+    if y.shape[0] != M or y.shape[1] < N:
+        raise ValueError(f"y: {M} rows of at least {N} columns are required, got {tuple(y.shape)}")
     out_fp32 = 1 if y.dtype == torch.float32 else 0
-    _check(load().tfm_linear(_ptr(x), _ptr(W), _ptr(y), M, N, K, y.stride(0), out_fp32,
+    _check(load().tfm_linear(xp, wp, yp, M, N, K, y.stride(0), out_fp32,
                              1 if accumulate else 0, _mode_of(x), _stream(stream)))
 
 
@@ -372,14 +525,27 @@ def swiglu_workspace_bytes(M, F, mode):
     return load().tfm_swiglu_workspace_bytes(M, F, mode)
 
 
+def _swiglu_args(x, w1, w3, w2, y):
+    M, D = x.shape
+    F = w1.shape[0]
+    xp = _dev(x, "x", _t("bfloat16", "float32"))
+    dt = (x.dtype,)
+    _shape(w1, (F, D), "w1")
+    _shape(w3, (F, D), "w3")
+    _shape(w2, (D, F), "w2")
+    _shape(y, (M, D), "y")
+    ptrs = (xp, _dev(w1, "w1", dt), _dev(w3, "w3", dt), _dev(w2, "w2", dt),
+            _dev(y, "y", _t("float32")))
+    return ptrs, (M, D, F)
+
+
 def swiglu_noalloc(x, w1, w3, w2, y, accumulate=False, stream=None):
     """tfm_swiglu without a workspace argument, for callers that cannot
     allocate device memory: the hidden activation goes to a fixed device array
     of swiglu_noalloc_max_bytes() bytes owned by the library."""
-    M, D = x.shape
-    F = w1.shape[0]
-    _check(load().tfm_swiglu_noalloc(_ptr(x), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(y), M, D, F,
-                                     1 if accumulate else 0, _mode_of(x), _stream(stream)))
+    ptrs, (M, D, F) = _swiglu_args(x, w1, w3, w2, y)
+    _check(load().tfm_swiglu_noalloc(*ptrs, M, D, F, 1 if accumulate else 0, _mode_of(x),
+                                     _stream(stream)))
 
 
 def swiglu_noalloc_max_bytes() -> int:
@@ -387,11 +553,10 @@ def swiglu_noalloc_max_bytes() -> int:
 
 
 def swiglu(x, w1, w3, w2, y, workspace, accumulate=False, stream=None):
-    M, D = x.shape
-    F = w1.shape[0]
+    ptrs, (M, D, F) = _swiglu_args(x, w1, w3, w2, y)
+    wp = _dev(workspace, "workspace")
     nbytes = workspace.numel() * workspace.element_size()
-    _check(load().tfm_swiglu(_ptr(x), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(y), M, D, F,
-                             1 if accumulate else 0, _ptr(workspace), nbytes, _mode_of(x),
+    _check(load().tfm_swiglu(*ptrs, M, D, F, 1 if accumulate else 0, wp, nbytes, _mode_of(x),
                              _stream(stream)))
 
 
@@ -414,6 +579,16 @@ class Gpt2Model(Model):
 
     def load_weights(self, w: dict):
         L = self.cfg.n_layer
+        on_host = 0 if w["embed"].is_cuda else 1
+        place = _host if on_host else _dev
+        if len(w["layers"]) < L:
+            raise ValueError(f"layers: {L} are required, got {len(w['layers'])}")
+        for key in GPT2_WEIGHT_FIELDS:             # all on one side, each dense
+            if key in _GPT2_LAYER:
+                for i in range(L):
+                    place(w["layers"][i][key], f"layers[{i}].{key}")
+            elif w.get(key) is not None:
+                place(w[key], key)
         keep = []
         vals = []
         for key in GPT2_WEIGHT_FIELDS:
@@ -427,5 +602,4 @@ class Gpt2Model(Model):
                 t = w.get(key)
                 vals.append(t.data_ptr() if t is not None else None)
         ws = Gpt2Weights(*vals)
-        on_host = 0 if w["embed"].is_cuda else 1
         _check(self.lib.tfm_load_gpt2_weights(self.handle, ctypes.byref(ws), on_host))
