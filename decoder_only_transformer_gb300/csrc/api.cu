@@ -46,6 +46,9 @@ int current_device() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// Element alignment of a typed array (n a power of two); kernels read int32 ids
+// and fp32 scalars with naturally aligned loads.
+bool aligned_to(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
 
 }  // namespace
 
@@ -1191,6 +1194,7 @@ tfm_status check_forward_args(Model* m, const void* tokens, int B, int S, const 
     if (!m) return fail(TFM_EINVAL, "NULL handle");
     if (!m->loaded) return fail(TFM_EINVAL, "weights not loaded");
     if (!tokens || !logits) return fail(TFM_EINVAL, "NULL tokens or logits");
+    if (!aligned_to(tokens, 4)) return fail(TFM_EINVAL, "tokens must be 4-byte aligned");
     if (B < 1 || B > m->cfg.max_batch) return fail(TFM_EINVAL, "B=%d outside [1, max_batch=%d]", B, m->cfg.max_batch);
     if (S < 1 || S > m->cfg.max_seq) return fail(TFM_EINVAL, "S=%d outside [1, max_seq=%d]", S, m->cfg.max_seq);
     if (ld < m->cfg.vocab || ld % 4) return fail(TFM_EINVAL, "ld_logits=%lld must be >= vocab and a multiple of 4", (long long)ld);
@@ -1216,6 +1220,9 @@ tfm_status tfm_forward_loss(void* handle, const int32_t* tokens, const int32_t* 
     Model* m = static_cast<Model*>(handle);
     if (!m) return fail(TFM_EINVAL, "NULL handle");
     if (!targets) return fail(TFM_EINVAL, "NULL targets");
+    if (!tfm::aligned_to(targets, 4) || !tfm::aligned_to(loss, 4) || !tfm::aligned_to(lse, 4) ||
+        !tfm::aligned_to(mean_loss, 4))
+        return fail(TFM_EINVAL, "targets, loss, lse and mean_loss must be 4-byte aligned");
     // the logits-free forward takes the same token checks as tfm_forward
     const float dummy = 0.f;
     tfm_status st = tfm::check_forward_args(m, tokens, B, S, &dummy, (m->cfg.vocab + 3) / 4 * 4);
@@ -1514,6 +1521,7 @@ tfm_status tfm_embedding(const int32_t* tokens, const void* E, float* h, int64_t
     if (M == 0) return TFM_OK;
     if (!tokens || !E || !h) return fail(TFM_EINVAL, "NULL pointer");
     if (!tfm::aligned16(E) || !tfm::aligned16(h)) return fail(TFM_EINVAL, "E and h must be 16-byte aligned");
+    if (!tfm::aligned_to(tokens, 4)) return fail(TFM_EINVAL, "tokens must be 4-byte aligned");
     if (!tfm::device_error_word()) return fail(TFM_ECUDA, "device error word unavailable");
     cudaError_t e = tfm::launch_embedding(tokens, E, h, M, V, D, mode == TFM_BF16,
                                           static_cast<cudaStream_t>(stream));
@@ -1541,6 +1549,8 @@ tfm_status tfm_rope(void* x, const int32_t* positions, int32_t B, int32_t H, int
     if (mode != TFM_FP32 && mode != TFM_BF16) return fail(TFM_EINVAL, "bad mode");
     if ((int64_t)B * H * S == 0) return TFM_OK;
     if (!x) return fail(TFM_EINVAL, "NULL x");
+    if (!tfm::aligned_to(x, mode == TFM_BF16 ? 2 : 4) || !tfm::aligned_to(positions, 4))
+        return fail(TFM_EINVAL, "x must be aligned to its element size, positions to 4 bytes");
     cudaError_t e = tfm::launch_rope(x, positions, B, H, S, dh, theta, mode == TFM_BF16,
                                      static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TFM_OK : tfm::cuda_fail(e, "rope launch");

@@ -204,7 +204,8 @@ tfm_status tfm_load_gpt2_weights(void* handle, const tfm_gpt2_weights* w, int32_
  * b*S + s holding the vocab scores of token s of sequence b in columns
  * [0, vocab); columns [vocab, ld_logits) are not written.  Positions are
  * 0..S-1 in every sequence.  Requires 1 <= B <= max_batch, 1 <= S <= max_seq,
- * ld_logits >= vocab, ld_logits % 4 == 0, logits 16-byte aligned.  Launches
+ * ld_logits >= vocab, ld_logits % 4 == 0, logits 16-byte aligned, tokens
+ * 4-byte aligned.  Launches
  * 2 + 7 n_layer kernels on `stream`; capturable in a CUDA graph.  Calls on the
  * same handle must not overlap (they share the workspace). */
 tfm_status tfm_forward(void* handle, const int32_t* tokens, int32_t B, int32_t S,
@@ -221,8 +222,8 @@ tfm_status tfm_forward(void* handle, const int32_t* tokens, int32_t B, int32_t S
  * tiles; fp32 mode materialises the logits in scratch and reduces each row.
  * Outputs (device, each may be NULL): loss [B*S] and lse [B*S] fp32,
  * mean_loss one fp32 value, the mean of loss over the B*S positions (summed in
- * a fixed order, so repeated calls agree bit for bit).  Same limits as
- * tfm_forward.  A target outside [0, vocab) gives that position a NaN loss and
+ * a fixed order, so repeated calls agree bit for bit); targets and the
+ * outputs 4-byte aligned.  Same limits as tfm_forward.  A target outside [0, vocab) gives that position a NaN loss and
  * raises TFM_EBADTOKEN in the device error word (tfm_device_status).  The
  * first call for a larger B*S allocates the scratch (blocking); later calls
  * launch 3 + 7 n_layer kernels (4 + 7 n_layer with mean_loss) on `stream`.
@@ -354,7 +355,8 @@ const char* tfm_profile_kind_name(int32_t kind);
 
 /* Embedding lookup (CS336 walkthrough, section 5.2): h[m, :] = E[tokens[m], :]
  * as fp32.  tokens [M] int32; E [V, D] bf16 or fp32 (mode); h [M, D] fp32.
- * An id outside [0, V) writes a zero row and sets TFM_EBADTOKEN. */
+ * An id outside [0, V) writes a zero row and sets TFM_EBADTOKEN.  E and h
+ * 16-byte aligned, tokens 4-byte aligned, else TFM_EINVAL. */
 tfm_status tfm_embedding(const int32_t* tokens, const void* E, float* h, int64_t M,
                          int32_t V, int32_t D, int32_t mode, void* stream);
 
@@ -368,7 +370,8 @@ tfm_status tfm_rmsnorm(const float* x, const float* g, void* y, int64_t M, int32
 /* RoPE in place (CS336 walkthrough, section 5.5; "LLM 2", section RoPE):
  * x [B, H, S, dh] (bf16 or fp32), each adjacent pair (x[2i], x[2i+1]) of token
  * s turned by pos * theta^(-2i/dh), pos = positions[b*S + s] (int32 [B, S],
- * device) or s when positions is NULL.  dh even, dh <= 256. */
+ * device) or s when positions is NULL.  dh even, dh <= 256.  x aligned to its
+ * element size and positions to 4 bytes, else TFM_EINVAL. */
 tfm_status tfm_rope(void* x, const int32_t* positions, int32_t B, int32_t H, int32_t S,
                     int32_t dh, float theta, int32_t mode, void* stream);
 

@@ -80,6 +80,37 @@ def test_null_arguments_are_rejected_on_the_host(lib):
     lib.tfm_destroy(None)
 
 
+def test_misaligned_pointers_are_rejected_on_the_host(lib):
+    """A pointer that breaks the header's alignment rule is refused before any
+    launch: kernels load int32 ids, fp32 scalars and bf16 elements with
+    naturally aligned accesses, and a misaligned one would fault on the device."""
+    B16, F32 = tfm.TFM_BF16, tfm.TFM_FP32
+    a = ctypes.c_void_p(256)
+    for off in (1, 2, 3):                            # tokens not on a 4-byte boundary
+        t = ctypes.c_void_p(256 + off)
+        assert lib.tfm_embedding(t, a, a, 4, 10, 64, B16, None) == tfm.TFM_EINVAL
+        assert b"tokens" in lib.tfm_last_error()
+        assert lib.tfm_rope(a, t, 1, 4, 16, 32, 1e4, F32, None) == tfm.TFM_EINVAL
+        assert b"positions" in lib.tfm_last_error()
+    for mode, bad in ((B16, (257,)), (F32, (257, 258, 259))):   # x off its element size
+        for p in bad:
+            assert lib.tfm_rope(ctypes.c_void_p(p), None, 1, 4, 16, 32, 1e4, mode,
+                                None) == tfm.TFM_EINVAL
+    for p in (258, 264):                             # 16-byte rule of the vector paths
+        m = ctypes.c_void_p(p)
+        calls = [
+            lambda: lib.tfm_embedding(a, m, a, 4, 10, 64, B16, None),
+            lambda: lib.tfm_linear(m, a, a, 4, 16, 64, 16, 1, 0, B16, None),
+            lambda: lib.tfm_causal_attention(a, a, m, a, 1, 4, 2, 16, 64, 0.0, B16, None),
+            lambda: lib.tfm_swiglu(a, a, a, a, a, 4, 64, 176, 0, m, 1 << 20, B16, None),
+            lambda: lib.tfm_decode_attention(a, a, a, m, 1, 4, 4, 16, 3, 64, 0.0, 0, a, 1 << 20,
+                                             None),
+        ]
+        for call in calls:
+            assert call() == tfm.TFM_EINVAL
+            assert b"16-byte aligned" in lib.tfm_last_error()
+
+
 def test_empty_calls_return_ok_on_the_host(lib):
     """Empty component calls check their sizes and modes, then return before
     touching a pointer or the device (so this runs without a GPU)."""

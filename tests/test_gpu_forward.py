@@ -9,6 +9,8 @@ bf16 rounding model on the same positions.  Large configurations are checked
 on sampled sequences (sequences are independent, a property the oracle tests
 pin).
 """
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -237,6 +239,10 @@ def test_forward_rejects_bad_arguments():
         model.forward(torch.zeros(1, 17, dtype=torch.int32, device="cuda"), logits)
     with pytest.raises(tfm.TfmError):          # ld not a multiple of 4
         model.forward(tok, torch.empty(32, 23, device="cuda"))
+    # int32 ids off a 4-byte boundary are refused on the host, before any launch
+    st = model.lib.tfm_forward(model.handle, ctypes.c_void_p(tok.data_ptr() + 2), 1, 8,
+                               tfm._ptr(logits), 24, None)
+    assert st == tfm.TFM_EINVAL and b"4-byte" in model.lib.tfm_last_error()
     model.close()
 
 
