@@ -580,15 +580,7 @@ class Gpt2Model(Model):
     def load_weights(self, w: dict):
         L = self.cfg.n_layer
         on_host = 0 if w["embed"].is_cuda else 1
-        place = _host if on_host else _dev
-        if len(w["layers"]) < L:
-            raise ValueError(f"layers: {L} are required, got {len(w['layers'])}")
-        for key in GPT2_WEIGHT_FIELDS:             # all on one side, each dense
-            if key in _GPT2_LAYER:
-                for i in range(L):
-                    place(w["layers"][i][key], f"layers[{i}].{key}")
-            elif w.get(key) is not None:
-                place(w[key], key)
+        self._check_weights(w, on_host)
         keep = []
         vals = []
         for key in GPT2_WEIGHT_FIELDS:
@@ -603,3 +595,52 @@ class Gpt2Model(Model):
                 vals.append(t.data_ptr() if t is not None else None)
         ws = Gpt2Weights(*vals)
         _check(self.lib.tfm_load_gpt2_weights(self.handle, ctypes.byref(ws), on_host))
+
+    def _check_weights(self, w, on_host):
+        """Every array the options use on the embedding's side (host or device),
+        dense, of the configuration's shape: matrices and the learned position
+        table (at least max_seq rows) in the mode's type; LayerNorm gains, shifts
+        and biases fp32.  Arrays the options leave unused are only checked for
+        their side."""
+        torch = _torch()
+        c = self.c
+        D, F, V = c.d_model, c.d_ff, c.vocab
+        dh = D // c.n_head
+        nqkv = (c.n_head + 2 * c.n_kv_head) * dh
+        mat = torch.bfloat16 if c.mode == TFM_BF16 else torch.float32
+        f32 = torch.float32
+        place = _host if on_host else _dev
+
+        def one(t, name, shape, dtype):
+            if t is None:
+                raise ValueError(f"{name}: required by the configuration")
+            place(t, name, (dtype,))
+            _shape(t, shape, name)
+
+        one(w["embed"], "embed", (V, D), mat)
+        one(w["lm_head"], "lm_head", (V, D), mat)
+        one(w.get("lnf_g"), "lnf_g", (D,), f32)
+        one(w.get("lnf_b"), "lnf_b", (D,), f32)
+        pos = w.get("pos")
+        if self.opt.pos == TFM_POS_LEARNED:
+            if pos is None:
+                raise ValueError("pos: the learned position table is required")
+            place(pos, "pos", (mat,))
+            if pos.dim() != 2 or pos.shape[1] != D or pos.shape[0] < c.max_seq:
+                raise ValueError(f"pos: {c.max_seq} rows of {D} are required, got {tuple(pos.shape)}")
+        elif pos is not None:
+            place(pos, "pos")
+        if self.opt.lm_bias:
+            one(w.get("lm_bias"), "lm_bias", (V,), f32)
+        elif w.get("lm_bias") is not None:
+            place(w["lm_bias"], "lm_bias")
+        if len(w["layers"]) < self.cfg.n_layer:
+            raise ValueError(f"layers: {self.cfg.n_layer} are required, got {len(w['layers'])}")
+        per_layer = (("ln1_g", (D,), f32), ("ln1_b", (D,), f32), ("w_qkv", (nqkv, D), mat),
+                     ("b_qkv", (nqkv,), f32), ("w_proj", (D, c.n_head * dh), mat),
+                     ("b_proj", (D,), f32), ("ln2_g", (D,), f32), ("ln2_b", (D,), f32),
+                     ("w_fc", (F, D), mat), ("b_fc", (F,), f32), ("w_fc2", (D, F), mat),
+                     ("b_fc2", (D,), f32))
+        for i, layer in enumerate(w["layers"][: self.cfg.n_layer]):
+            for key, shape, dtype in per_layer:
+                one(layer.get(key), f"layers[{i}].{key}", shape, dtype)

@@ -93,3 +93,69 @@ def test_weights_checked_against_the_configuration():
         m._check_weights(w, on_host=1)
     with pytest.raises(ValueError, match="CUDA tensor"):              # host arrays, device flag
         m._check_weights(_host_weights(cfg), on_host=0)
+
+
+def _gpt2_model_without_handle(cfg, pos, lm_bias, max_seq):
+    m = tfm.Gpt2Model.__new__(tfm.Gpt2Model)   # the checks below run before any library call
+    m.cfg, m.handle, m.lib = cfg, None, None
+    m.c = tfm.make_config(cfg, 1, max_seq)
+    m.opt = tfm.Gpt2Options(tfm.TFM_POS_LEARNED if pos == "learned" else tfm.TFM_POS_SINUSOIDAL,
+                            0, 1 if lm_bias else 0)
+    return m
+
+
+def _gpt2_host_weights(cfg, **kw):
+    from helpers import to_torch_gpt2_weights
+    return to_torch_gpt2_weights(workloads.make_gpt2_weights(cfg, **kw), device="cpu",
+                                 bf16=cfg.mode == "bf16")
+
+
+@pytest.mark.parametrize("name,pos,lm_bias,tied,max_seq", [
+    ("tiny", "learned", False, False, None),
+    ("tiny", "sinusoidal", True, False, None),
+    ("tiny", "learned", True, True, None),
+    ("tiny", "sinusoidal", False, True, None),
+    ("small2", "learned", True, False, 128),
+    ("small2", "sinusoidal", False, True, 160),
+    ("small2", "learned", False, True, 260),
+])
+def test_gpt2_weights_the_gpu_tests_load_pass(name, pos, lm_bias, tied, max_seq):
+    cfg = (workloads.GPT2_CONFIGS["gpt2_tiny"] if name == "tiny" else
+           workloads.GPT2_CONFIGS["gpt2_small"].replace(n_layer=2, vocab=3001))
+    m = _gpt2_model_without_handle(cfg, pos, lm_bias, max_seq or cfg.seq)
+    w = _gpt2_host_weights(cfg, pos=pos, lm_bias=lm_bias, tied=tied, max_seq=max_seq)
+    m._check_weights(w, on_host=1)
+
+
+def test_gpt2_weights_checked_against_the_configuration():
+    cfg = workloads.GPT2_CONFIGS["gpt2_tiny"]        # fp32 mode
+    m = _gpt2_model_without_handle(cfg, "learned", True, cfg.seq)
+    ok = dict(pos="learned", lm_bias=True)
+    w = _gpt2_host_weights(cfg, **ok)
+    w["layers"][1]["b_qkv"] = w["layers"][1]["b_qkv"][:-1]
+    with pytest.raises(ValueError, match=r"layers\[1\]\.b_qkv"):
+        m._check_weights(w, on_host=1)
+    w = _gpt2_host_weights(cfg, **ok)
+    w["layers"][0]["w_fc2"] = w["layers"][0]["w_fc2"].t().contiguous()   # [d_ff, d_model]
+    with pytest.raises(ValueError, match=r"layers\[0\]\.w_fc2"):
+        m._check_weights(w, on_host=1)
+    w = _gpt2_host_weights(cfg, **ok)
+    w["pos"] = w["pos"][:-1]                          # one position short of max_seq
+    with pytest.raises(ValueError, match="pos"):
+        m._check_weights(w, on_host=1)
+    w = _gpt2_host_weights(cfg, pos="sinusoidal", lm_bias=True)   # no table to read
+    with pytest.raises(ValueError, match="pos"):
+        m._check_weights(w, on_host=1)
+    w = _gpt2_host_weights(cfg, pos="learned", lm_bias=False)     # options want a bias
+    with pytest.raises(ValueError, match="lm_bias"):
+        m._check_weights(w, on_host=1)
+    w = _gpt2_host_weights(cfg, **ok)
+    w["lnf_b"] = w["lnf_b"].double()
+    with pytest.raises(TypeError, match="lnf_b"):
+        m._check_weights(w, on_host=1)
+    w = _gpt2_host_weights(cfg, **ok)
+    w["layers"][0]["w_qkv"] = w["layers"][0]["w_qkv"].to(torch.bfloat16)   # the other mode's type
+    with pytest.raises(TypeError, match=r"layers\[0\]\.w_qkv"):
+        m._check_weights(w, on_host=1)
+    with pytest.raises(ValueError, match="CUDA tensor"):          # host arrays, device flag
+        m._check_weights(_gpt2_host_weights(cfg, **ok), on_host=0)
