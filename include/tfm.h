@@ -22,11 +22,14 @@
  *    managed) memory of the current device; "host" pointers are host memory
  *    (page-locked for asynchronous copies).  The caller owns every buffer it
  *    passes; the library keeps no pointer to a caller buffer after a call
- *    returns, except the weights of tfm_load_weights when weights_on_host == 0
- *    and TFM_LOAD_BORROW is set (not the default; see there).
+ *    returns (tfm_load_weights copies the weights into the handle's own
+ *    storage).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
- *    Compute calls only enqueue work on that stream and return; they never
- *    synchronise, allocate or free memory.
+ *    Compute calls enqueue work on that stream and return without
+ *    synchronising, allocating or freeing memory, except where a function's
+ *    comment names a first call that does: tfm_forward_loss sizing its scratch,
+ *    tfm_forward_graph, tfm_forward_host_async and tfm_decode_step recording a
+ *    CUDA graph.
  *  - Every function returns a tfm_status.  Argument errors are found on the
  *    host before anything is launched (TFM_EINVAL / TFM_EUNSUPPORTED) and
  *    leave outputs untouched.  Errors found on the device (a token id outside
@@ -307,7 +310,12 @@ tfm_status tfm_prefill(void* handle, const int32_t* tokens, int32_t B, int32_t S
  * next token after position pos of sequence b, columns [0, vocab)), the same as
  * row pos of tfm_forward over the sequence extended by this token.  The cached
  * length becomes pos + 1.  Calls on a handle are ordered on the host in the order
- * they are made (the length is advanced at enqueue time). */
+ * they are made (the length is advanced at enqueue time).  A step whose B,
+ * logits, ld_logits and stream equal the previous step's is recorded into a
+ * CUDA graph (the position and tokens are read on the device, so the recording
+ * serves every later position) and replayed from then on; the two most recent
+ * recordings are kept.  Steps on the legacy default stream (NULL) or with
+ * profiling on launch their kernels directly. */
 tfm_status tfm_decode_step(void* handle, const int32_t* tokens, int32_t B, int32_t pos,
                            float* logits, int64_t ld_logits, void* stream);
 
