@@ -148,7 +148,7 @@ __device__ __forceinline__ float4 load_group(const void* base, int64_t row, int 
 // the 4-float groups l, l+32, ...; an id outside [0, V) writes zeros and raises
 // TFM_EBADTOKEN.
 template <int kKind, int kV, bool kBf16E, bool kBf16Y>
-__global__ void __launch_bounds__(256, kV >= 16 ? 3 : 1) k_embed_rmsnorm(const int32_t* __restrict__ tok,
+__global__ void __launch_bounds__(256, kV == 16 ? 3 : 1) k_embed_rmsnorm(const int32_t* __restrict__ tok,
                                                        const void* __restrict__ E,
                                                        const float* __restrict__ g,
                                                        float* __restrict__ h, void* __restrict__ y,
@@ -156,10 +156,12 @@ __global__ void __launch_bounds__(256, kV >= 16 ? 3 : 1) k_embed_rmsnorm(const i
                                                        NormArgs na, int* err) {
     const int lane = threadIdx.x & 31;
     // The gain, staged once per CTA: each warp's stores then wait on no global
-    // load after its row's reduction.  With that and three CTAs per SM (rows of up
-    // to 4096 floats in 80 registers), 24 rows are in flight per SM instead of 16:
-    // the GQA workload's gather + norm 52.1 -> 38.4 us, the long-context one's
-    // 21.0 -> 18.6 us (each warp's row is a chain of dependent memory waits).
+    // load after its row's reduction.  With that and three CTAs per SM (rows of
+    // 1025 to 2048 floats, 64 per lane, in 80 registers), 24 rows are in flight
+    // per SM instead of 16: the GQA workload's gather + norm 52.1 -> 38.4 us, the
+    // long-context one's 21.0 -> 18.6 us (each warp's row is a chain of dependent
+    // memory waits).  Longer rows (128 floats per lane) do not fit that register
+    // budget and take no occupancy bound.
     __shared__ float4 gs[kKind == kNormRms ? kV * 32 : 1];
     pdl_wait();
     pdl_trigger();
