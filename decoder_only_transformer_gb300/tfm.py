@@ -361,8 +361,8 @@ class Model:
         optional."""
         torch = _torch()
         B, S = tokens.shape
-        t = _dev(tokens, "tokens", (torch.int32,))
         _shape(targets, (B, S), "targets")
+        t = _dev(tokens, "tokens", (torch.int32,))
         tg = _dev(targets, "targets", (torch.int32,))
         for v, n, name in ((loss, B * S, "loss"), (lse, B * S, "lse"), (mean, 1, "mean")):
             if v is not None and v.numel() < n:

@@ -2,6 +2,8 @@
 library sees them: a host tensor where a device pointer is documented, the wrong
 element type, a non-dense layout, or too little room for what a call writes.
 Host-side only: every check fires before any library call or device access."""
+import types
+
 import numpy as np
 import pytest
 import torch
@@ -59,6 +61,13 @@ def test_host_forward_arguments():
         m.decode_step(torch.zeros(2, dtype=torch.int32), 3, _cpu(2, 24))
     with pytest.raises(ValueError, match="CUDA tensor"):
         m.forward_loss(tok, tok)
+    with pytest.raises(ValueError, match="targets"):                # one target per position
+        m.forward_loss(tok, tok[:, :-1])
+    with pytest.raises(ValueError, match="contiguous"):             # ids densely packed
+        m.forward_host(torch.zeros(8, 2, dtype=torch.int32).t(), _cpu(16, 24))
+    fake_cuda = types.SimpleNamespace(is_cuda=True, device="cuda:0", shape=(2, 8))
+    with pytest.raises(ValueError, match="host"):                    # host entry point, device ids
+        m.forward_host(fake_cuda, _cpu(16, 24))
 
 
 def _host_weights(cfg, mat=torch.float32):
@@ -93,6 +102,24 @@ def test_weights_checked_against_the_configuration():
         m._check_weights(w, on_host=1)
     with pytest.raises(ValueError, match="CUDA tensor"):              # host arrays, device flag
         m._check_weights(_host_weights(cfg), on_host=0)
+
+
+def test_weights_checked_in_bf16_mode_with_grouped_heads():
+    """bf16 matrices and fp32 gains, and k / v projections of n_kv_head heads."""
+    cfg = workloads.get_config("small").replace(vocab=50, d_model=64, n_head=2, n_kv_head=1,
+                                                n_layer=1, d_ff=176)
+    m = _model_without_handle(cfg)
+    m._check_weights(_host_weights(cfg, mat=torch.bfloat16), on_host=1)
+    with pytest.raises(TypeError, match="embed"):                     # fp32 matrices
+        m._check_weights(_host_weights(cfg), on_host=1)
+    w = _host_weights(cfg, mat=torch.bfloat16)
+    w["final_norm"] = w["final_norm"].to(torch.bfloat16)              # gains stay fp32
+    with pytest.raises(TypeError, match="final_norm"):
+        m._check_weights(w, on_host=1)
+    w = _host_weights(cfg, mat=torch.bfloat16)
+    w["layers"][0]["wk"] = w["layers"][0]["wq"]                       # full-width k projection
+    with pytest.raises(ValueError, match=r"layers\[0\]\.wk"):
+        m._check_weights(w, on_host=1)
 
 
 def _gpt2_model_without_handle(cfg, pos, lm_bias, max_seq):
@@ -144,7 +171,7 @@ def test_gpt2_weights_checked_against_the_configuration():
     with pytest.raises(ValueError, match="pos"):
         m._check_weights(w, on_host=1)
     w = _gpt2_host_weights(cfg, pos="sinusoidal", lm_bias=True)   # no table to read
-    with pytest.raises(ValueError, match="pos"):
+    with pytest.raises(ValueError, match="learned position table is required"):
         m._check_weights(w, on_host=1)
     w = _gpt2_host_weights(cfg, pos="learned", lm_bias=False)     # options want a bias
     with pytest.raises(ValueError, match="lm_bias"):
