@@ -140,3 +140,40 @@ def test_dram_traffic_entries_name_real_kernels_and_exceed_the_algorithmic_reads
             "lmhead_gemm": M * D * es + cfg.vocab * D * es,
         }
         assert traffic >= 0.98 * reads[kind], (name, kind, traffic, reads[kind])
+
+
+def test_kernel_work_adds_up_to_the_forward_flops():
+    """The per-kernel FLOPs behind each roofline fraction add up, kind by kind,
+    to the forward's matmul FLOPs of the accounting that reproduces the pages'
+    GPT-2 XL table (causal pairs, grouped k / v heads): the projections to QKV +
+    o-proj, the SwiGLU matrices to gate/up + down, the attention matmuls, the
+    LM head.  The GPT-2-style MLP has two of the three SwiGLU matrices."""
+    import bench
+    for name in workloads.CONFIGS:
+        cfg = workloads.get_config(name)
+        B, S = cfg.batch, cfg.seq
+        work = bench.kernel_work(cfg, B, S)
+        f = accounting.forward_flops(cfg.vocab, cfg.d_model, cfg.n_layer, cfg.n_head, cfg.d_ff, S,
+                                     batch=B, n_kv_head=cfg.n_kv_head, causal=True)
+        L = cfg.n_layer
+        assert L * (work["qkv_rope_gemm"][1] + work["oproj_residual_gemm"][1]) == f["proj"], name
+        assert L * (work["gateup_swiglu_gemm"][1] + work["down_residual_gemm"][1]) == f["swiglu"], name
+        assert L * work["attention"][1] == f["attn"], name
+        assert work["lmhead_gemm"][1] == f["lm_head"], name
+        g2 = bench.gpt2_kernel_work(cfg, B, S)
+        assert 3 * L * (g2["gateup_swiglu_gemm"][1] + g2["down_residual_gemm"][1]) == 2 * f["swiglu"]
+        for k in ("qkv_rope_gemm", "attention", "oproj_residual_gemm", "lmhead_gemm"):
+            assert g2[k] == work[k], (name, k)
+
+
+def test_fused_embedding_norm_bytes_are_the_norm_plus_the_gather():
+    """The gather + first norm moves a norm's bytes (its fp32 write of h in place of
+    the norm's fp32 read of x) plus the token ids and the gathered table rows."""
+    import bench
+    for name in workloads.CONFIGS:
+        cfg = workloads.get_config(name)
+        M, D = cfg.batch * cfg.seq, cfg.d_model
+        es = 2 if cfg.mode == "bf16" else 4
+        work = bench.kernel_work(cfg, cfg.batch, cfg.seq)
+        assert work["rmsnorm"][1] == accounting.rmsnorm_bytes(M, D, out_bytes=es)
+        assert work["embedding_rmsnorm"][1] == M * 4 + M * D * es + work["rmsnorm"][1], name
