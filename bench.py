@@ -362,6 +362,27 @@ def kernel_table(cfg, B, S, prof, peaks):
     return out
 
 
+def decode_attention_bytes(B, H, Hkv, L, dh):
+    """Algorithmic HBM bytes of one decode attention over L cached positions: the
+    cached K and V of the L positions (bf16) read once, q read and o written
+    (bf16), and the fp32 partials of every (sequence, head, chunk of
+    DECODE_CHUNK / dh keys) -- a partial output of dh floats, its maximum and its
+    sum -- written by the chunk kernel and read back by the merge."""
+    nk = DECODE_CHUNK // dh
+    nch = (L + nk - 1) // nk
+    return 2 * B * Hkv * L * dh * 2 + 2 * B * H * dh * 2 + 2 * B * H * nch * (dh + 2) * 4
+
+
+def decode_step_weight_bytes(cfg, B):
+    """Weight bytes a decode step reads once: every layer's matrices (bf16) and
+    gains (fp32), the LM head, the embedding rows of the step's B tokens and the
+    final gain."""
+    dh, H, Hkv = cfg.d_head, cfg.n_head, cfg.n_kv_head
+    D, F, V, L = cfg.d_model, cfg.d_ff, cfg.vocab, cfg.n_layer
+    w_layer = ((H + 2 * Hkv) * dh * D + D * H * dh + 3 * D * F) * 2 + 2 * D * 4
+    return L * w_layer + V * D * 2 + B * D * 2 + D * 4
+
+
 def decode_rate(tfm, torch, model, cfg, tok_np, stream, peaks, steps=32, warmup=3):
     """Incremental decoding on the workload's batch: prefill the first
     S - warmup - steps positions into the KV cache, run `warmup` untimed decode
@@ -402,17 +423,11 @@ def decode_rate(tfm, torch, model, cfg, tok_np, stream, peaks, steps=32, warmup=
     att_ms, att_n = prof["attention"]
     nbytes = 0
     for t in range(warmup, warmup + steps):
-        L = S0 + t + 1
-        nch = (L + DECODE_CHUNK // dh - 1) // (DECODE_CHUNK // dh)   # chunks of DECODE_CHUNK / dh keys
-        nbytes += (2 * B * Hkv * L * dh * 2 + 2 * B * H * dh * 2
-                   + 2 * B * H * nch * (dh + 2) * 4) * cfg.n_layer
+        nbytes += decode_attention_bytes(B, H, Hkv, S0 + t + 1, dh) * cfg.n_layer
     gbs = nbytes / (att_ms / 1e3) / 1e9 if att_ms > 0 else None
     # Whole step against HBM: every weight matrix is read once per step (the
     # rows of the embedding for the step's tokens only) and the cache as above.
-    D, F, V, L = cfg.d_model, cfg.d_ff, cfg.vocab, cfg.n_layer
-    w_layer = ((H + 2 * Hkv) * dh * D + D * H * dh + 3 * D * F) * 2 + 2 * D * 4
-    w_step = L * w_layer + V * D * 2 + B * D * 2 + D * 4
-    step_bytes = w_step + nbytes / steps
+    step_bytes = decode_step_weight_bytes(cfg, B) + nbytes / steps
     step_gbs = step_bytes / (ms / steps / 1e3) / 1e9
     # The decode attention alone (tfm_decode_attention, the chunk kernel and the
     # merge), at this workload's cache shape with every position filled (pos =
@@ -436,9 +451,7 @@ def decode_rate(tfm, torch, model, cfg, tok_np, stream, peaks, steps=32, warmup=
         b_.record(stream)
     torch.cuda.synchronize()
     us_a = sum(a.elapsed_time(b_) for a, b_ in ev_a) / len(ev_a) * 1e3
-    nk = DECODE_CHUNK // dh
-    bytes_a = (2 * B * Hkv * S * dh * 2 + 2 * B * H * dh * 2
-               + 2 * B * H * ((S + nk - 1) // nk) * (dh + 2) * 4)
+    bytes_a = decode_attention_bytes(B, H, Hkv, S, dh)
     gbs_a = bytes_a / (us_a * 1e-6) / 1e9
     del flush
     return {"value": B * steps / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms / steps,

@@ -6,7 +6,7 @@ import numpy as np
 import torch
 
 import workloads
-from decoder_only_transformer_gb300 import accounting
+from decoder_only_transformer_gb300 import accounting, tfm
 
 GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_examples.json")))
 
@@ -177,3 +177,23 @@ def test_fused_embedding_norm_bytes_are_the_norm_plus_the_gather():
         work = bench.kernel_work(cfg, cfg.batch, cfg.seq)
         assert work["rmsnorm"][1] == accounting.rmsnorm_bytes(M, D, out_bytes=es)
         assert work["embedding_rmsnorm"][1] == M * 4 + M * D * es + work["rmsnorm"][1], name
+
+
+def test_decode_bytes_agree_with_the_library_sizes():
+    """The decode roofline's bytes against what the library itself allocates:
+    a step reads every weight the handle stores once, except that of the
+    embedding only the step's B rows (tfm_weight_bytes less its 256-byte padding
+    of each piece: nine per layer, three more); the decode attention writes and
+    reads back every chunk partial its workspace holds (less the position word's
+    256 bytes)."""
+    import bench
+    for name in ("small", "gpt2s", "long", "gqa"):                  # the bf16 workloads
+        cfg = workloads.get_config(name)
+        B, S, D, V = cfg.batch, cfg.seq, cfg.d_model, cfg.vocab
+        stored = tfm.weight_bytes(tfm.make_config(cfg)) - (9 * cfg.n_layer + 3) * 256
+        assert bench.decode_step_weight_bytes(cfg, B) == stored - V * D * 2 + B * D * 2, name
+        for L in (1, S // 2 + 1, S):
+            partials = tfm.decode_attention_workspace_bytes(B, cfg.n_head, L, cfg.d_head) - 256
+            cache_q_o = 2 * B * cfg.n_kv_head * L * cfg.d_head * 2 + 2 * B * cfg.n_head * cfg.d_head * 2
+            got = bench.decode_attention_bytes(B, cfg.n_head, cfg.n_kv_head, L, cfg.d_head)
+            assert got == cache_q_o + 2 * partials, (name, L)
